@@ -1,0 +1,216 @@
+"""ctypes binding of libkvq (include/kvq.h).
+
+Argument marshalling only: every step of the path runs in the CUDA kernels of
+libkvq.so.  Tensors are torch tensors on a CUDA device; their ``data_ptr()`` and
+the current torch stream are passed straight to the C entry points.  If the
+library has not been built, loading raises: there is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "_build", "libkvq.so")
+
+OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_WORKSPACE_TOO_SMALL = 0, -1, -2, -3, -4
+DEV_BAD_SLOT, DEV_BAD_PAGE, DEV_BAD_LENGTH, DEV_BAD_INDEX, DEV_TIMEOUT = 1, 2, 4, 8, 16
+DT_F32, DT_BF16 = 0, 1
+FMT_Q4_HAD32, FMT_BF16, FMT_FP8_ROW = 0, 1, 2
+
+_P = ctypes.c_void_p
+_I32 = ctypes.c_int32
+_I64 = ctypes.c_int64
+_SZ = ctypes.c_size_t
+_F = ctypes.c_float
+
+
+class CacheDesc(ctypes.Structure):
+    _fields_ = [("format", _I32), ("num_kv_heads", _I32), ("head_dim", _I32), ("rope_dim", _I32),
+                ("page_size", _I32), ("num_pages", _I32), ("k", _P), ("k_scale", _P), ("v", _P), ("v_scale", _P)]
+
+
+# name -> (restype, argtypes); mirrors include/kvq.h
+SIGNATURES = {
+    "kvq_version": (_I32, []),
+    "kvq_status_string": (ctypes.c_char_p, [_I32]),
+    "kvq_last_cuda_error": (_I32, []),
+    "kvq_plane_bytes": (_SZ, [ctypes.POINTER(CacheDesc), _I32]),
+    "kvq_store": (_I32, [ctypes.POINTER(CacheDesc), _P, _P, _I32, _I64, _P, _P, _P]),
+    "kvq_rotate_query": (_I32, [_P, _I32, _P, _I64, _I32, _P]),
+    "kvq_decode_workspace_size": (_SZ, [ctypes.POINTER(CacheDesc), _I32, _I32, _I32, _I32]),
+    "kvq_decode_attn": (_I32, [ctypes.POINTER(CacheDesc), _P, _I32, _I32, _P, _P, _I32, _I32, _P, _I32, _F, _P,
+                               _SZ, _P]),
+    "kvq_merge": (_I32, [ctypes.POINTER(CacheDesc), _P, _SZ, _I32, _I32, _P, _I32, _I32, _I32, _P, _P]),
+    "kvq_prefill_attn": (_I32, [ctypes.POINTER(CacheDesc), _P, _I32, _I32, _I32, _I32, _P, _I32, _F, _P, _P, _P]),
+    "kvq_read_status": (_I32, [_P, _P, _P]),
+}
+
+_lib = None
+
+
+def lib():
+    """Load libkvq.so (raises if it is missing: the CUDA path has no substitute)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"libkvq.so is not built ({LIB_PATH}); run bit_quantized_kv_store_gb300.build.build()")
+        L = ctypes.CDLL(LIB_PATH)
+        for name, (res, args) in SIGNATURES.items():
+            f = getattr(L, name)
+            f.restype = res
+            f.argtypes = args
+        _lib = L
+    return _lib
+
+
+class KvqError(RuntimeError):
+    def __init__(self, status, where):
+        msg = lib().kvq_status_string(status).decode()
+        if status == ERR_CUDA:
+            msg += f" (cudaError {lib().kvq_last_cuda_error()})"
+        super().__init__(f"{where}: {msg} [{status}]")
+        self.status = status
+
+
+def _check(status, where):
+    if status != OK:
+        raise KvqError(status, where)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream=None):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _dtype_code(t):
+    if t.dtype == torch.float32:
+        return DT_F32
+    if t.dtype == torch.bfloat16:
+        return DT_BF16
+    raise TypeError(f"unsupported activation dtype {t.dtype}")
+
+
+class Cache:
+    """A paged KV cache: the planes are caller-owned torch tensors on one device.
+
+    Q4:   k, v codes [num_pages, Hk, page_size, D/2] uint8; k_scale, v_scale
+          [num_pages, Hk, page_size, D/32] float16.
+    BF16: k, v [num_pages, Hk, page_size, D] bfloat16.
+    FP8:  k (latent codes) [num_pages, page_size, D] uint8, v (rope codes)
+          [num_pages, page_size, R] uint8, k_scale / v_scale [num_pages, page_size] f32.
+    """
+
+    def __init__(self, fmt, num_kv_heads, head_dim, page_size, num_pages, device="cuda", rope_dim=0):
+        self.fmt, self.Hk, self.D, self.page_size, self.num_pages = fmt, num_kv_heads, head_dim, page_size, num_pages
+        self.rope = rope_dim
+        rows = (num_pages, num_kv_heads, page_size)
+        if fmt == FMT_Q4_HAD32:
+            self.k = torch.zeros(rows + (head_dim // 2,), dtype=torch.uint8, device=device)
+            self.v = torch.zeros_like(self.k)
+            self.k_scale = torch.zeros(rows + (head_dim // 32,), dtype=torch.float16, device=device)
+            self.v_scale = torch.zeros_like(self.k_scale)
+        elif fmt == FMT_BF16:
+            self.k = torch.zeros(rows + (head_dim,), dtype=torch.bfloat16, device=device)
+            self.v = torch.zeros_like(self.k)
+            self.k_scale = self.v_scale = None
+        elif fmt == FMT_FP8_ROW:
+            assert num_kv_heads == 1
+            self.k = torch.zeros(rows + (head_dim,), dtype=torch.uint8, device=device)
+            self.v = torch.zeros(rows + (rope_dim,), dtype=torch.uint8, device=device)
+            self.k_scale = torch.zeros(rows, dtype=torch.float32, device=device)
+            self.v_scale = torch.zeros(rows, dtype=torch.float32, device=device)
+        else:
+            raise ValueError(fmt)
+        self.refresh()
+
+    def refresh(self):
+        self.desc = CacheDesc(self.fmt, self.Hk, self.D, self.rope, self.page_size, self.num_pages,
+                              self.k.data_ptr(), 0 if self.k_scale is None else self.k_scale.data_ptr(),
+                              self.v.data_ptr(), 0 if self.v_scale is None else self.v_scale.data_ptr())
+
+    @property
+    def ref(self):
+        return ctypes.byref(self.desc)
+
+    def nbytes(self):
+        return sum(t.numel() * t.element_size() for t in (self.k, self.v, self.k_scale, self.v_scale) if t is not None)
+
+
+def store(cache: Cache, k, v, slot_mapping, status=None, stream=None):
+    n_tok = k.shape[0]
+    _check(lib().kvq_store(cache.ref, _ptr(k), _ptr(v), _dtype_code(k), n_tok, _ptr(slot_mapping), _ptr(status),
+                           _stream(stream)), "kvq_store")
+
+
+def rotate_query(x, out=None, stream=None):
+    D = x.shape[-1]
+    rows = x.numel() // D
+    if out is None:
+        out = torch.empty(x.shape, dtype=torch.float32, device=x.device)
+    _check(lib().kvq_rotate_query(_ptr(x), _dtype_code(x), _ptr(out), rows, D, _stream(stream)), "kvq_rotate_query")
+    return out
+
+
+def workspace_size(cache: Cache, num_seqs, num_q_heads, max_seq_len, n_sel=0):
+    return lib().kvq_decode_workspace_size(cache.ref, num_seqs, num_q_heads, max_seq_len, n_sel)
+
+
+def alloc_workspace(cache: Cache, num_seqs, num_q_heads, max_seq_len, n_sel=0, device="cuda"):
+    n = workspace_size(cache, num_seqs, num_q_heads, max_seq_len, n_sel)
+    return torch.zeros(n, dtype=torch.uint8, device=device)
+
+
+def decode_attn(cache: Cache, q, seq_lens, block_tables, max_seq_len, sm_scale, workspace, sel=None, stream=None):
+    B, Hq = q.shape[0], q.shape[1]
+    n_sel = 0 if sel is None else sel.shape[1]
+    _check(lib().kvq_decode_attn(cache.ref, _ptr(q), B, Hq, _ptr(seq_lens), _ptr(block_tables),
+                                 block_tables.shape[1], max_seq_len, _ptr(sel), n_sel, float(sm_scale),
+                                 _ptr(workspace), workspace.numel(), _stream(stream)), "kvq_decode_attn")
+
+
+def merge(cache: Cache, workspace, num_seqs, num_q_heads, seq_lens, max_seq_len, out, n_sel=0, rotate_back=None,
+          stream=None):
+    if rotate_back is None:
+        rotate_back = cache.fmt == FMT_Q4_HAD32
+    _check(lib().kvq_merge(cache.ref, _ptr(workspace), workspace.numel(), num_seqs, num_q_heads, _ptr(seq_lens),
+                           max_seq_len, n_sel, int(rotate_back), _ptr(out), _stream(stream)), "kvq_merge")
+    return out
+
+
+def decode(cache: Cache, q, seq_lens, block_tables, max_seq_len, sm_scale, workspace, out=None, sel=None,
+           stream=None):
+    """Rotate the query (4-bit format), decode partials, merge: one decode step."""
+    B, Hq = q.shape[0], q.shape[1]
+    qq = q
+    if cache.fmt == FMT_Q4_HAD32:
+        qq = rotate_query(q, stream=stream)
+    elif q.dtype != torch.float32:
+        qq = q.float()
+    decode_attn(cache, qq, seq_lens, block_tables, max_seq_len, sm_scale, workspace, sel=sel, stream=stream)
+    if out is None:
+        out = torch.empty((B, Hq, cache.D), dtype=torch.float32, device=q.device)
+    return merge(cache, workspace, B, Hq, seq_lens, max_seq_len, out, n_sel=0 if sel is None else sel.shape[1],
+                 stream=stream)
+
+
+def prefill_attn(cache: Cache, q, q_start, block_table, sm_scale, out=None, status=None, stream=None):
+    n_q, Hq = q.shape[0], q.shape[1]
+    if out is None:
+        out = torch.empty((n_q, Hq, cache.D), dtype=torch.float32, device=q.device)
+    bt = block_table.reshape(-1)
+    _check(lib().kvq_prefill_attn(cache.ref, _ptr(q), _dtype_code(q), n_q, Hq, int(q_start), _ptr(bt), bt.numel(),
+                                  float(sm_scale), _ptr(out), _ptr(status), _stream(stream)), "kvq_prefill_attn")
+    return out
+
+
+def read_status(d_status, stream=None):
+    v = ctypes.c_int32(0)
+    _check(lib().kvq_read_status(_ptr(d_status), ctypes.byref(v), _stream(stream)), "kvq_read_status")
+    return v.value

@@ -1,0 +1,236 @@
+// api.cu -- the C ABI of libkvq (declared in include/kvq.h): host-side argument
+// validation, workspace geometry and kernel launches.  Nothing here allocates.
+#include <cstdio>
+
+#include "kernels.cuh"
+
+namespace kvq {
+
+static thread_local int32_t g_last_cuda_error = 0;
+
+static int32_t cuda_fail(cudaError_t e) {
+  g_last_cuda_error = static_cast<int32_t>(e);
+  return KVQ_ERR_CUDA;
+}
+
+static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+static size_t round256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+// Validate a cache description; returns KVQ_OK or a negative status.
+static int32_t check_cache(const kvq_cache* c) {
+  if (!c) return KVQ_ERR_INVALID_ARG;
+  if (c->format < KVQ_FMT_Q4_HAD32 || c->format > KVQ_FMT_FP8_ROW) return KVQ_ERR_INVALID_ARG;
+  if (c->num_kv_heads < 1 || c->head_dim <= 0 || c->page_size <= 0 || c->num_pages < 0)
+    return KVQ_ERR_INVALID_ARG;
+  if (c->head_dim % 32 != 0) return KVQ_ERR_UNSUPPORTED;  // rows are built from 32-value groups
+  if (c->page_size % 16 != 0) return KVQ_ERR_UNSUPPORTED;
+  if (!c->k || !c->v || !aligned16(c->k) || !aligned16(c->v)) return KVQ_ERR_INVALID_ARG;
+  if (c->format == KVQ_FMT_Q4_HAD32) {
+    if (!c->k_scale || !c->v_scale || !aligned16(c->k_scale) || !aligned16(c->v_scale)) return KVQ_ERR_INVALID_ARG;
+    const int ng = c->head_dim / 32;
+    if (ng != 1 && ng != 2 && ng != 4 && ng != 8) return KVQ_ERR_UNSUPPORTED;
+    if (c->rope_dim != 0) return KVQ_ERR_INVALID_ARG;
+  } else if (c->format == KVQ_FMT_BF16) {
+    if (c->rope_dim != 0) return KVQ_ERR_INVALID_ARG;
+  } else {
+    if (c->num_kv_heads != 1 || c->rope_dim <= 0 || c->rope_dim % 16 != 0) return KVQ_ERR_INVALID_ARG;
+    if (!c->k_scale || !c->v_scale) return KVQ_ERR_INVALID_ARG;
+  }
+  return KVQ_OK;
+}
+
+static int value_width(const kvq_cache* c) { return c->head_dim; }
+
+struct WsLayout {
+  size_t m_off, z_off, acc_off, total;
+  int P;
+};
+
+static WsLayout ws_layout(const kvq_cache* c, int B, int Hq, int max_seq_len, int n_sel) {
+  WsLayout w;
+  const int64_t T = n_sel > 0 ? n_sel : max_seq_len;
+  w.P = static_cast<int>((T + kPart - 1) / kPart);
+  if (w.P < 1) w.P = 1;
+  const size_t n = static_cast<size_t>(B) * Hq * w.P;
+  w.m_off = 256;
+  w.z_off = w.m_off + round256(n * sizeof(float));
+  w.acc_off = w.z_off + round256(n * sizeof(float));
+  w.total = w.acc_off + round256(n * value_width(c) * sizeof(float));
+  return w;
+}
+
+// Shared checks of the decode and merge arguments.
+static int32_t check_decode_shape(const kvq_cache* c, int B, int Hq, const int32_t* seq_lens, int max_seq_len,
+                                  bool gather, int n_sel) {
+  if (B < 0 || Hq < 1 || max_seq_len < 0) return KVQ_ERR_INVALID_ARG;
+  if (Hq % c->num_kv_heads != 0) return KVQ_ERR_INVALID_ARG;
+  if (B > 0 && !seq_lens) return KVQ_ERR_INVALID_ARG;
+  if (gather && (n_sel < 1 || n_sel > 4096)) return KVQ_ERR_INVALID_ARG;
+  if (!gather && n_sel != 0) return KVQ_ERR_INVALID_ARG;
+  const int group = Hq / c->num_kv_heads;
+  if (c->format == KVQ_FMT_Q4_HAD32 || c->format == KVQ_FMT_BF16) {
+    if (c->head_dim != 256 || group > 8) return KVQ_ERR_UNSUPPORTED;
+  } else {
+    if (c->head_dim != 512 || c->rope_dim != 64 || Hq % 16 != 0) return KVQ_ERR_UNSUPPORTED;
+  }
+  return KVQ_OK;
+}
+
+}  // namespace kvq
+
+using namespace kvq;
+
+extern "C" {
+
+int32_t kvq_version(void) { return 100; }
+
+const char* kvq_status_string(int32_t s) {
+  switch (s) {
+    case KVQ_OK: return "ok";
+    case KVQ_ERR_INVALID_ARG: return "invalid argument";
+    case KVQ_ERR_UNSUPPORTED: return "unsupported shape or format";
+    case KVQ_ERR_CUDA: return "CUDA error";
+    case KVQ_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
+    default: return "unknown status";
+  }
+}
+
+int32_t kvq_last_cuda_error(void) { return g_last_cuda_error; }
+
+size_t kvq_plane_bytes(const kvq_cache* c, int32_t plane) {
+  if (!c || c->head_dim <= 0 || c->head_dim % 32 || c->num_kv_heads < 1 || c->page_size <= 0 || c->num_pages < 0)
+    return 0;
+  const size_t rows = static_cast<size_t>(c->num_pages) * c->num_kv_heads * c->page_size;
+  switch (c->format) {
+    case KVQ_FMT_Q4_HAD32:
+      return (plane == 0 || plane == 2) ? rows * (c->head_dim / 2) : rows * (c->head_dim / 32) * 2;
+    case KVQ_FMT_BF16:
+      return (plane == 0 || plane == 2) ? rows * c->head_dim * 2 : 0;
+    case KVQ_FMT_FP8_ROW:
+      if (plane == 0) return rows * c->head_dim;
+      if (plane == 2) return rows * c->rope_dim;
+      return rows * 4;
+    default:
+      return 0;
+  }
+}
+
+int32_t kvq_store(const kvq_cache* cache, const void* k, const void* v, int32_t dtype, int64_t n_tok,
+                  const int32_t* d_slot_mapping, int32_t* d_status, void* stream) {
+  int32_t st = check_cache(cache);
+  if (st != KVQ_OK) return st;
+  if (n_tok < 0 || (dtype != KVQ_DT_F32 && dtype != KVQ_DT_BF16)) return KVQ_ERR_INVALID_ARG;
+  if (n_tok == 0) return KVQ_OK;
+  if (!k || !d_slot_mapping) return KVQ_ERR_INVALID_ARG;
+  if (cache->format == KVQ_FMT_FP8_ROW) {
+    if (v) return KVQ_ERR_INVALID_ARG;
+  } else if (!v) {
+    return KVQ_ERR_INVALID_ARG;
+  }
+  cudaError_t e = launch_store(*cache, k, v, dtype, n_tok, d_slot_mapping, d_status,
+                               static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? KVQ_OK : cuda_fail(e);
+}
+
+int32_t kvq_rotate_query(const void* x, int32_t dtype, float* y, int64_t rows, int32_t head_dim, void* stream) {
+  if (rows < 0 || head_dim <= 0) return KVQ_ERR_INVALID_ARG;
+  if (head_dim % 32 != 0) return KVQ_ERR_UNSUPPORTED;
+  if (dtype != KVQ_DT_F32 && dtype != KVQ_DT_BF16) return KVQ_ERR_INVALID_ARG;
+  if (rows == 0) return KVQ_OK;
+  if (!x || !y) return KVQ_ERR_INVALID_ARG;
+  if (x == static_cast<const void*>(y) && dtype != KVQ_DT_F32) return KVQ_ERR_INVALID_ARG;
+  cudaError_t e = launch_rotate(x, dtype, y, rows, head_dim, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? KVQ_OK : cuda_fail(e);
+}
+
+size_t kvq_decode_workspace_size(const kvq_cache* cache, int32_t num_seqs, int32_t num_q_heads,
+                                 int32_t max_seq_len, int32_t n_sel) {
+  if (!cache || num_seqs < 0 || num_q_heads < 0 || max_seq_len < 0 || n_sel < 0 || cache->head_dim <= 0) return 0;
+  return ws_layout(cache, num_seqs, num_q_heads, max_seq_len, n_sel).total;
+}
+
+int32_t kvq_decode_attn(const kvq_cache* cache, const float* q, int32_t num_seqs, int32_t num_q_heads,
+                        const int32_t* d_seq_lens, const int32_t* d_block_tables, int32_t max_pages_per_seq,
+                        int32_t max_seq_len, const int32_t* d_sel, int32_t n_sel, float sm_scale, void* workspace,
+                        size_t ws_bytes, void* stream) {
+  int32_t st = check_cache(cache);
+  if (st != KVQ_OK) return st;
+  st = check_decode_shape(cache, num_seqs, num_q_heads, d_seq_lens, max_seq_len, d_sel != nullptr, n_sel);
+  if (st != KVQ_OK) return st;
+  if (num_seqs == 0) return KVQ_OK;
+  if (!q || !d_block_tables || max_pages_per_seq < 1 || !workspace || !aligned16(q) || !aligned16(workspace))
+    return KVQ_ERR_INVALID_ARG;
+  if (!d_sel && static_cast<int64_t>(max_seq_len) > static_cast<int64_t>(max_pages_per_seq) * cache->page_size)
+    return KVQ_ERR_INVALID_ARG;
+  const WsLayout w = ws_layout(cache, num_seqs, num_q_heads, max_seq_len, d_sel ? n_sel : 0);
+  if (ws_bytes < w.total) return KVQ_ERR_WORKSPACE_TOO_SMALL;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int group = num_q_heads / cache->num_kv_heads;
+  cudaError_t e;
+  if (cache->format == KVQ_FMT_Q4_HAD32) {
+    DecodeArgs a{*cache, q, num_q_heads, group, d_seq_lens, d_block_tables, max_pages_per_seq, max_seq_len,
+                 d_sel, d_sel ? n_sel : 0, sm_scale * kLog2e,
+                 reinterpret_cast<float*>(ws + w.m_off), reinterpret_cast<float*>(ws + w.z_off),
+                 reinterpret_cast<float*>(ws + w.acc_off), w.P, reinterpret_cast<int32_t*>(ws)};
+    e = launch_decode_q4(a, num_seqs, s);
+  } else {
+    RowsArgs a{*cache, q, num_q_heads, group, cache->format == KVQ_FMT_BF16 ? group : 16, d_seq_lens,
+               d_block_tables, max_pages_per_seq, max_seq_len, d_sel, d_sel ? n_sel : 0, sm_scale * kLog2e,
+               reinterpret_cast<float*>(ws + w.m_off), reinterpret_cast<float*>(ws + w.z_off),
+               reinterpret_cast<float*>(ws + w.acc_off), w.P, reinterpret_cast<int32_t*>(ws)};
+    e = launch_decode_rows(a, num_seqs, s);
+  }
+  return e == cudaSuccess ? KVQ_OK : cuda_fail(e);
+}
+
+int32_t kvq_merge(const kvq_cache* cache, const void* workspace, size_t ws_bytes, int32_t num_seqs,
+                  int32_t num_q_heads, const int32_t* d_seq_lens, int32_t max_seq_len, int32_t n_sel,
+                  int32_t rotate_back, float* out, void* stream) {
+  int32_t st = check_cache(cache);
+  if (st != KVQ_OK) return st;
+  if (n_sel < 0 || n_sel > 4096) return KVQ_ERR_INVALID_ARG;
+  st = check_decode_shape(cache, num_seqs, num_q_heads, d_seq_lens, max_seq_len, n_sel > 0, n_sel);
+  if (st != KVQ_OK) return st;
+  if (rotate_back && cache->format != KVQ_FMT_Q4_HAD32) return KVQ_ERR_INVALID_ARG;
+  if (num_seqs == 0) return KVQ_OK;
+  if (!workspace || !out || !aligned16(workspace)) return KVQ_ERR_INVALID_ARG;
+  const WsLayout w = ws_layout(cache, num_seqs, num_q_heads, max_seq_len, n_sel);
+  if (ws_bytes < w.total) return KVQ_ERR_WORKSPACE_TOO_SMALL;
+  const uint8_t* ws = static_cast<const uint8_t*>(workspace);
+  MergeArgs a{reinterpret_cast<const float*>(ws + w.m_off), reinterpret_cast<const float*>(ws + w.z_off),
+              reinterpret_cast<const float*>(ws + w.acc_off), w.P, num_q_heads, value_width(cache), d_seq_lens,
+              max_seq_len, n_sel, rotate_back ? 1 : 0, out};
+  cudaError_t e = launch_merge(a, num_seqs, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? KVQ_OK : cuda_fail(e);
+}
+
+int32_t kvq_prefill_attn(const kvq_cache* cache, const void* q, int32_t dtype, int32_t n_q, int32_t num_q_heads,
+                         int32_t q_start, const int32_t* d_block_table, int32_t max_pages, float sm_scale, float* out,
+                         int32_t* d_status, void* stream) {
+  int32_t st = check_cache(cache);
+  if (st != KVQ_OK) return st;
+  if (cache->format != KVQ_FMT_Q4_HAD32 || cache->head_dim != 256) return KVQ_ERR_UNSUPPORTED;
+  if (n_q < 0 || q_start < 0 || num_q_heads < 1 || num_q_heads % cache->num_kv_heads != 0) return KVQ_ERR_INVALID_ARG;
+  if (dtype != KVQ_DT_F32 && dtype != KVQ_DT_BF16) return KVQ_ERR_INVALID_ARG;
+  if (num_q_heads / cache->num_kv_heads > 8) return KVQ_ERR_UNSUPPORTED;
+  if (n_q == 0) return KVQ_OK;
+  if (!q || !out || !d_block_table || max_pages < 1) return KVQ_ERR_INVALID_ARG;
+  if (static_cast<int64_t>(q_start) + n_q > static_cast<int64_t>(max_pages) * cache->page_size)
+    return KVQ_ERR_INVALID_ARG;
+  PrefillArgs a{*cache, q, dtype, n_q, num_q_heads, num_q_heads / cache->num_kv_heads, q_start, d_block_table,
+                max_pages, sm_scale * kLog2e, out, d_status};
+  cudaError_t e = launch_prefill_q4(a, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? KVQ_OK : cuda_fail(e);
+}
+
+int32_t kvq_read_status(const void* d_status, int32_t* host_code, void* stream) {
+  if (!d_status || !host_code) return KVQ_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaMemcpyAsync(host_code, d_status, sizeof(int32_t), cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  return e == cudaSuccess ? KVQ_OK : cuda_fail(e);
+}
+
+}  // extern "C"

@@ -1,0 +1,88 @@
+// kernels.cuh -- argument blocks and launchers shared between the C-ABI layer
+// (api.cu) and the kernel translation units.
+#pragma once
+#include "common.cuh"
+
+namespace kvq {
+
+// Split-T decode over the 4-bit rotated cache (decode_q4.cu).
+struct DecodeArgs {
+  kvq_cache c;
+  const float* q;  // [B, Hq, D], rotated
+  int Hq;
+  int group;  // Hq / Hk
+  const int32_t* seq_lens;
+  const int32_t* block_tables;
+  int max_pages;
+  int max_seq_len;
+  const int32_t* sel;  // NULL: dense
+  int n_sel;
+  float qscale;  // sm_scale * log2(e)
+  float* ws_m;
+  float* ws_z;
+  float* ws_acc;
+  int P;  // partitions per (seq, head) in the workspace
+  int32_t* status;
+};
+
+// Split-T decode over bf16 rows or fp8 latent rows (decode_rows.cu).
+struct RowsArgs {
+  kvq_cache c;
+  const float* q;  // [B, Hq, W]
+  int Hq;
+  int group;
+  int hb;  // query heads per CTA
+  const int32_t* seq_lens;
+  const int32_t* block_tables;
+  int max_pages;
+  int max_seq_len;
+  const int32_t* sel;
+  int n_sel;
+  float qscale;
+  float* ws_m;
+  float* ws_z;
+  float* ws_acc;
+  int P;
+  int32_t* status;
+};
+
+// Log-sum-exp merge of the partials (merge.cu).
+struct MergeArgs {
+  const float* ws_m;
+  const float* ws_z;
+  const float* ws_acc;
+  int P;
+  int Hq;
+  int Dv;
+  const int32_t* seq_lens;
+  int max_seq_len;
+  int n_sel;
+  int rotate_back;
+  float* out;
+};
+
+// Causal prefill over decoded 4-bit slots (prefill_q4.cu).
+struct PrefillArgs {
+  kvq_cache c;
+  const void* q;
+  int dtype;
+  int n_q;
+  int Hq;
+  int group;
+  int q_start;
+  const int32_t* block_table;
+  int max_pages;
+  float qscale;
+  float* out;
+  int32_t* status;
+};
+
+cudaError_t launch_store(const kvq_cache& c, const void* k, const void* v, int dtype, int64_t n_tok,
+                         const int32_t* slots, int32_t* status, cudaStream_t s);
+cudaError_t launch_rotate(const void* x, int dtype, float* y, int64_t rows, int head_dim, cudaStream_t s);
+cudaError_t launch_decode_q4(const DecodeArgs& a, int B, cudaStream_t s);
+cudaError_t launch_decode_rows(const RowsArgs& a, int B, cudaStream_t s);
+cudaError_t launch_merge(const MergeArgs& a, int B, cudaStream_t s);
+cudaError_t launch_prefill_q4(const PrefillArgs& a, cudaStream_t s);
+
+}  // namespace kvq

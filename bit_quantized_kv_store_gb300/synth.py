@@ -48,16 +48,19 @@ def outlier_normal(shape, n_out, scale, device, *keys):
     return x
 
 
-def heavy_tailed(shape, device, *keys, frac=0.05, nu=3, scale=10.0, dtype=torch.bfloat16):
+def heavy_tailed(shape, device, *keys, frac=0.05, nu=3, scale=10.0, dtype=torch.bfloat16, subset=None):
     """Values with 95 % N(0,1) channels and 5 % Student-t(nu) x scale channels.
-    shape = (..., heads, D); the heavy channel subset is seeded per head."""
+    shape = (..., heads, D).  The heavy channel subset of each head is drawn from
+    `subset` (a tuple of keys; default: the value keys), so a cache filled in
+    chunks keeps one subset per (layer, tensor, head)."""
     g = generator(device, "heavy_tailed", *keys)
+    gs = generator("cpu", "heavy_subset", *(subset if subset is not None else keys))
     heads, D = shape[-2], shape[-1]
     n_heavy = int(round(frac * D))
     x = torch.randn(shape, generator=g, device=device, dtype=torch.float32)
     lead = shape[:-2]
     for h in range(heads):
-        ch = torch.randperm(D, generator=g, device=device)[:n_heavy]
+        ch = torch.randperm(D, generator=gs)[:n_heavy].to(device)
         z = torch.randn(lead + (n_heavy,), generator=g, device=device, dtype=torch.float32)
         chi = torch.zeros_like(z)
         for _ in range(nu):

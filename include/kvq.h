@@ -1,0 +1,199 @@
+/*
+ * kvq.h -- C ABI of libkvq: attention over a sub-byte quantized KV cache on GB300.
+ *
+ * The library implements the hot path described on three public pages:
+ *   [P1] "qwen27 CUDA: an opt-in 4-bit attention cache (262K on a 24 GB card)",
+ *        section "What it is" -- rows of Hadamard-rotated 32-value groups kept as
+ *        4-bit codes plus an fp16 scale (144 bytes for a 256-wide head); queries
+ *        rotated once; attention in the rotated space over shared 512-key chunks
+ *        plus the tail, merged in order; output rotated back once; prompt chunks
+ *        packed into the cache and attended over decoded slots.
+ *   [P2] "feat(kvcache): add reliable quantized KV cache", PR body -- 32 values
+ *        -> 16 bytes + one fp16 scale; paged pools with a packed last dimension and
+ *        a separate scale buffer; the engine rejects head_dim not divisible by 32.
+ *   [P3] "KV cache quantization: fp8 (KV8) + 4-bit TurboQuant", KV8 base and
+ *        split-T commits -- MLA latent rows as e4m3 with a per-row f32 scale
+ *        amax/448; absorbed attention with (H,P) partials merged by log-sum-exp;
+ *        a gather over selected absolute rows (at most 4096).
+ *
+ * Conventions for every entry point:
+ *  - Pointers named d_* or documented as "device" are device pointers owned by the
+ *    caller.  The library never allocates, frees or keeps device memory between
+ *    calls and holds no global mutable state; calls are reentrant.
+ *  - `stream` is a cudaStream_t (NULL = the legacy default stream).  All work is
+ *    enqueued asynchronously on it.
+ *  - Host-side arguments are validated before anything is launched; on failure a
+ *    negative kvq_status is returned and nothing is enqueued.  A failed launch
+ *    returns KVQ_ERR_CUDA.
+ *  - Device-resident metadata (slot mappings, block tables, sequence lengths,
+ *    selected indices) cannot be checked on the host.  Kernels check it and, on a
+ *    bad value, skip the access, write NaN to the affected output and OR a
+ *    KVQ_DEV_* bit into the caller's status word; nothing traps.
+ *  - Every kernel that waits (on a TMA copy) does so with an iteration limit and
+ *    reports KVQ_DEV_TIMEOUT instead of hanging.
+ */
+#ifndef KVQ_H
+#define KVQ_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  KVQ_OK = 0,
+  KVQ_ERR_INVALID_ARG = -1,        /* null pointer, negative size, inconsistent shapes */
+  KVQ_ERR_UNSUPPORTED = -2,        /* valid but not implemented (e.g. head_dim % 32 != 0) */
+  KVQ_ERR_CUDA = -3,               /* a CUDA call failed; see kvq_last_cuda_error() */
+  KVQ_ERR_WORKSPACE_TOO_SMALL = -4 /* ws_bytes < kvq_decode_workspace_size(...) */
+} kvq_status;
+
+/* Bits of the device status word (int32, caller-owned, zero it before use). */
+enum {
+  KVQ_DEV_BAD_SLOT = 1,      /* store: slot outside the pool */
+  KVQ_DEV_BAD_PAGE = 2,      /* a block-table entry outside [0, num_pages) */
+  KVQ_DEV_BAD_LENGTH = 4,    /* a sequence length < 0 or > the stated maximum */
+  KVQ_DEV_BAD_INDEX = 8,     /* a selected index outside [0, seq_len) */
+  KVQ_DEV_TIMEOUT = 16       /* a bounded wait on an asynchronous copy gave up */
+};
+
+/* Element type of caller-provided activations (new K/V rows, queries). */
+typedef enum { KVQ_DT_F32 = 0, KVQ_DT_BF16 = 1 } kvq_dtype;
+
+/* Cache formats.
+ *
+ * KVQ_FMT_Q4_HAD32 ([P1] "What it is"; [P2] PR body): every (position, KV head) row
+ *   of head_dim D values is split into D/32 groups; each group is rotated by the
+ *   orthonormal 32-point Walsh-Hadamard matrix H (natural Sylvester order,
+ *   H[i][j] = (-1)^popcount(i&j) / sqrt(32)) and kept as 32 4-bit codes plus one
+ *   fp16 scale:  scale = fp16_rne(amax/8) (saturated to 65504),
+ *   code = clamp(rint_even(y / scale), -8, 7) + 8  (all codes 8 when scale == 0),
+ *   value = (code - 8) * scale, in the rotated space.
+ *   Codes plane: row r occupies D/2 bytes at r * D/2.  Inside a row, canonical
+ *   group G (16 bytes; byte b = element 2b in the low nibble, 2b+1 in the high
+ *   nibble) is cut into 8 half-words; half-word h of group G (elements
+ *   32G+4h .. 32G+4h+3) is stored at byte offset 2 * (h * D/32 + G).
+ *   Scale plane: row r occupies D/32 fp16 values at r * D/32, in group order.
+ *   For D = 256 a row is 128 + 16 = 144 bytes.
+ * KVQ_FMT_BF16: unrotated bf16 rows of D values (the uncompressed comparison).
+ * KVQ_FMT_FP8_ROW ([P3] KV8 base commit): one latent row per position (num_kv_heads
+ *   must be 1): head_dim latent values ("Lc") and rope_dim rope values ("Rc"), each
+ *   part kept as e4m3 bytes with its own f32 scale amax/448: inv = 448/amax (fp32),
+ *   code = e4m3_rne_satfinite(x * inv); amax == 0 or a non-finite inv stores zero
+ *   codes; NaN inputs store 0x00.  In attention the key is Lc ++ Rc and the value
+ *   is Lc (absorbed attention: the latent is both key and value).
+ *
+ * Row index of (page, kv_head, slot) in every plane:
+ *   r = (page * num_kv_heads + kv_head) * page_size + slot.
+ * A token's slot number is page * page_size + slot; block tables list page ids. */
+typedef enum { KVQ_FMT_Q4_HAD32 = 0, KVQ_FMT_BF16 = 1, KVQ_FMT_FP8_ROW = 2 } kvq_format;
+
+typedef struct kvq_cache {
+  int32_t format;       /* kvq_format */
+  int32_t num_kv_heads; /* Hk (FP8_ROW: 1) */
+  int32_t head_dim;     /* D: key/value width (FP8_ROW: latent width) */
+  int32_t rope_dim;     /* FP8_ROW: rope width; otherwise 0 */
+  int32_t page_size;    /* slots per page; a positive multiple of 16 */
+  int32_t num_pages;    /* pages in the pool */
+  void* k;              /* Q4: K codes plane (u8); BF16: K plane; FP8_ROW: Lc codes [rows][D] */
+  void* k_scale;        /* Q4: K scale plane (fp16); BF16: unused; FP8_ROW: Lc scales [rows] f32 */
+  void* v;              /* Q4: V codes plane; BF16: V plane; FP8_ROW: Rc codes [rows][rope_dim] */
+  void* v_scale;        /* Q4: V scale plane; BF16: unused; FP8_ROW: Rc scales [rows] f32 */
+} kvq_cache;
+
+/* Version of the ABI (major * 10000 + minor * 100 + patch). */
+int32_t kvq_version(void);
+/* Short text of a kvq_status value (static storage). */
+const char* kvq_status_string(int32_t status);
+/* The cudaError_t of the last KVQ_ERR_CUDA returned on this thread (0 if none). */
+int32_t kvq_last_cuda_error(void);
+
+/* Bytes of each plane for a cache description (0 for unused planes). */
+size_t kvq_plane_bytes(const kvq_cache* cache, int32_t plane /* 0 k, 1 k_scale, 2 v, 3 v_scale */);
+
+/* kvq_store -- pack new tokens into the cache ([P1] "What it is": "pack the
+ * window's new keys and values the same way"; [P3] KV8 base: the producer
+ * quantises the fresh row).
+ *   k, v:   device, [n_tok, num_kv_heads, head_dim] of dtype (Q4 / BF16).
+ *           FP8_ROW: k is [n_tok, head_dim + rope_dim] and v must be NULL.
+ *   d_slot_mapping: device int32 [n_tok]; slot = page * page_size + offset;
+ *           a negative slot skips the token; a slot >= num_pages * page_size is
+ *           skipped and flagged KVQ_DEV_BAD_SLOT.
+ *   d_status: optional device int32 status word (may be NULL).
+ * Bit-exact with the definition above (fp32 rotation by the butterfly with
+ * stages 1, 2, 4, 8, 16, then one multiply by fp32(1/sqrt(32)); IEEE division;
+ * round half to even).  Rows are independent: storing tokens one by one or all
+ * at once writes the same bytes. */
+int32_t kvq_store(const kvq_cache* cache, const void* k, const void* v, int32_t dtype, int64_t n_tok,
+                  const int32_t* d_slot_mapping, int32_t* d_status, void* stream);
+
+/* kvq_rotate_query -- y = blockdiag(H) x for `rows` rows of head_dim values
+ * ([P1] "What it is": rotate the queries once; H is its own inverse, so the same
+ * call rotates an output back).  x: device [rows, head_dim] of dtype; y: device
+ * fp32 [rows, head_dim]; y may equal x when dtype is F32.  head_dim % 32 == 0. */
+int32_t kvq_rotate_query(const void* x, int32_t dtype, float* y, int64_t rows, int32_t head_dim,
+                         void* stream);
+
+/* Size in bytes of the workspace kvq_decode_attn needs for this problem:
+ * a 256-byte header (status word at offset 0), then partial maxima m and sums z
+ * [num_seqs][num_q_heads][P] f32 and partial contexts acc [num_seqs][num_q_heads]
+ * [P][value width] f32, where P = ceil(max(max_seq_len, n_sel) / 512). */
+size_t kvq_decode_workspace_size(const kvq_cache* cache, int32_t num_seqs, int32_t num_q_heads,
+                                 int32_t max_seq_len, int32_t n_sel);
+
+/* kvq_decode_attn -- split-T decode attention partials ([P1] "What it is": attend
+ * over the 4-bit cache in rotated space over shared 512-key chunks plus the tail;
+ * [P3] split-T commit: dim3(H,P) partial online-softmax blocks (cl, m, z)).
+ * For sequence b, query head h (reading KV head h / (num_q_heads / num_kv_heads))
+ * and partition p (keys [512p, min(512p + 512, T_b)), T_b = seq_lens[b], or the
+ * p-th run of 512 entries of sel[b] when gathering), writes
+ *   m = max_j s_j * log2(e),  z = sum_j 2^(s_j log2(e) - m),
+ *   acc = sum_j 2^(s_j log2(e) - m) * value_j,   s_j = sm_scale * (q . key_j)
+ * into the workspace.  Empty partitions get m = -inf, z = 0, acc = 0.
+ *   q:  device fp32 [num_seqs, num_q_heads, key width]; Q4: already rotated
+ *       (kvq_rotate_query); BF16 / FP8_ROW: as is.  Key width = head_dim
+ *       (+ rope_dim for FP8_ROW).
+ *   d_seq_lens: device int32 [num_seqs], each in [0, max_seq_len].
+ *   d_block_tables: device int32 [num_seqs, max_pages_per_seq].
+ *   d_sel: NULL for dense attention, else device int32 [num_seqs, n_sel] absolute
+ *       positions, each < seq_lens[b] (gather; n_sel <= 4096, [P3] split-T commit).
+ *   Q4 / BF16 need num_q_heads / num_kv_heads <= 8 and head_dim == 256.
+ *   FP8_ROW needs head_dim == 512, rope_dim == 64 and num_q_heads % 64 == 0. */
+int32_t kvq_decode_attn(const kvq_cache* cache, const float* q, int32_t num_seqs, int32_t num_q_heads,
+                        const int32_t* d_seq_lens, const int32_t* d_block_tables, int32_t max_pages_per_seq,
+                        int32_t max_seq_len, const int32_t* d_sel, int32_t n_sel, float sm_scale,
+                        void* workspace, size_t ws_bytes, void* stream);
+
+/* kvq_merge -- log-sum-exp merge of the partials ([P1] "in-order merge ... and
+ * rotate the output back once"; [P3] split-T commit: merge kernel):
+ *   M = max_p m_p,  Z = sum_p z_p 2^(m_p - M),  o = sum_p acc_p 2^(m_p - M) / Z,
+ * taking partitions in ascending order in a fixed grouping (runs are
+ * bit-reproducible), then out = blockdiag(H) o when rotate_back != 0 (Q4 only).
+ * A sequence with no keys gives zeros.  Arguments as for kvq_decode_attn.
+ * out: device fp32 [num_seqs, num_q_heads, value width]. */
+int32_t kvq_merge(const kvq_cache* cache, const void* workspace, size_t ws_bytes, int32_t num_seqs,
+                  int32_t num_q_heads, const int32_t* d_seq_lens, int32_t max_seq_len, int32_t n_sel,
+                  int32_t rotate_back, float* out, void* stream);
+
+/* kvq_prefill_attn -- causal attention of a prompt chunk over decoded slots
+ * ([P1] "What it is": prompt chunks are packed into the cache, then attended with
+ * the prefill-attention kernel over decoded slots).  Query i (absolute position
+ * q_start + i) attends keys 0 .. q_start + i of the sequence whose block table is
+ * d_block_table; the chunk's own keys must already be stored (kvq_store).
+ *   q:   device [n_q, num_q_heads, head_dim] of dtype, unrotated.
+ *   out: device fp32 [n_q, num_q_heads, head_dim], rotated back.
+ *   Q4 only; head_dim == 256; num_q_heads / num_kv_heads <= 8. */
+int32_t kvq_prefill_attn(const kvq_cache* cache, const void* q, int32_t dtype, int32_t n_q,
+                         int32_t num_q_heads, int32_t q_start, const int32_t* d_block_table,
+                         int32_t max_pages, float sm_scale, float* out, int32_t* d_status, void* stream);
+
+/* Copy the device status word at the start of a decode workspace (or any
+ * device int32) to *host_code; synchronises `stream`. */
+int32_t kvq_read_status(const void* d_status, int32_t* host_code, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* KVQ_H */

@@ -1,0 +1,120 @@
+"""The C-ABI library loads, exports every entry point include/kvq.h declares,
+and rejects bad host-side arguments before touching the GPU (no GPU needed)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from tests.conftest import ROOT, golden
+
+HEADER = os.path.join(ROOT, "include", "kvq.h")
+
+
+@pytest.fixture(scope="module")
+def K():
+    from bit_quantized_kv_store_gb300 import build
+    build.build()
+    from bit_quantized_kv_store_gb300 import _lib
+    _lib.lib()
+    return _lib
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(kvq_[a-z_0-9]+)\s*\(", text)))
+
+
+def test_exports_every_declared_symbol(K):
+    names = declared_functions()
+    assert len(names) >= 10
+    L = K.lib()
+    for n in names:
+        assert hasattr(L, n), n
+    assert set(names) == set(K.SIGNATURES), "binding and header disagree"
+
+
+def test_version_and_status_strings(K):
+    L = K.lib()
+    assert L.kvq_version() >= 100
+    for s in (0, -1, -2, -3, -4):
+        assert L.kvq_status_string(s)
+
+
+def _desc(K, fmt=0, Hk=4, D=256, ps=16, pages=4, rope=0, ptr=4096):
+    return K.CacheDesc(fmt, Hk, D, rope, ps, pages, ptr, ptr, ptr, ptr)
+
+
+def test_host_validation_without_gpu(K):
+    L = K.lib()
+    d = _desc(K)
+    dummy = ctypes.c_void_p(4096)
+    # null cache / bad format / head_dim not a multiple of 32 / page size
+    assert L.kvq_store(None, dummy, dummy, 0, 1, dummy, None, None) == K.ERR_INVALID_ARG
+    assert L.kvq_store(ctypes.byref(_desc(K, fmt=7)), dummy, dummy, 0, 1, dummy, None, None) == K.ERR_INVALID_ARG
+    assert L.kvq_store(ctypes.byref(_desc(K, D=48)), dummy, dummy, 0, 1, dummy, None, None) == K.ERR_UNSUPPORTED
+    assert L.kvq_store(ctypes.byref(_desc(K, ps=8)), dummy, dummy, 0, 1, dummy, None, None) == K.ERR_UNSUPPORTED
+    assert L.kvq_store(ctypes.byref(d), dummy, dummy, 5, 1, dummy, None, None) == K.ERR_INVALID_ARG   # dtype
+    assert L.kvq_store(ctypes.byref(d), dummy, None, 0, 1, dummy, None, None) == K.ERR_INVALID_ARG    # v missing
+    assert L.kvq_store(ctypes.byref(d), dummy, dummy, 0, -1, dummy, None, None) == K.ERR_INVALID_ARG  # n_tok
+    assert L.kvq_store(ctypes.byref(d), dummy, dummy, 0, 0, dummy, None, None) == K.OK                # nothing to do
+    fp8 = _desc(K, fmt=2, Hk=1, D=512, rope=64)
+    assert L.kvq_store(ctypes.byref(fp8), dummy, dummy, 0, 1, dummy, None, None) == K.ERR_INVALID_ARG  # v must be NULL
+    # unaligned planes
+    assert L.kvq_store(ctypes.byref(_desc(K, ptr=4097)), dummy, dummy, 0, 1, dummy, None, None) == K.ERR_INVALID_ARG
+    # rotation
+    assert L.kvq_rotate_query(dummy, 0, dummy, 4, 40, None) == K.ERR_UNSUPPORTED
+    assert L.kvq_rotate_query(dummy, 1, ctypes.c_void_p(4096), 4, 64, None) == K.ERR_INVALID_ARG  # in place needs f32
+    # decode: group > 8, workspace too small, gather list too long, bad max_seq_len
+    ws = L.kvq_decode_workspace_size(ctypes.byref(d), 2, 24, 1000, 0)
+    assert ws > 0
+    args = lambda Hq=24, msl=1000, sel=None, nsel=0, wsb=ws, mp=100: (
+        ctypes.byref(d), dummy, 2, Hq, dummy, dummy, mp, msl, sel, nsel, ctypes.c_float(0.1), dummy, wsb, None)
+    assert L.kvq_decode_attn(*args(Hq=40)) == K.ERR_UNSUPPORTED
+    assert L.kvq_decode_attn(*args(wsb=ws - 1)) == K.ERR_WORKSPACE_TOO_SMALL
+    assert L.kvq_decode_attn(*args(sel=dummy, nsel=5000)) == K.ERR_INVALID_ARG
+    assert L.kvq_decode_attn(*args(msl=100 * 16 + 1)) == K.ERR_INVALID_ARG
+    assert L.kvq_decode_attn(*args(Hq=25)) == K.ERR_INVALID_ARG   # not a multiple of Hk
+    # merge: rotate_back only for the 4-bit format
+    bf = _desc(K, fmt=1)
+    assert L.kvq_merge(ctypes.byref(bf), dummy, 1 << 30, 1, 8, dummy, 100, 0, 1, dummy, None) == K.ERR_INVALID_ARG
+    # prefill: only the 4-bit format
+    assert L.kvq_prefill_attn(ctypes.byref(bf), dummy, 0, 4, 8, 0, dummy, 4, ctypes.c_float(0.1), dummy, None,
+                              None) == K.ERR_UNSUPPORTED
+    assert L.kvq_prefill_attn(ctypes.byref(d), dummy, 0, 100, 24, 0, dummy, 4, ctypes.c_float(0.1), dummy, None,
+                              None) == K.ERR_INVALID_ARG   # chunk beyond the block table
+
+
+def test_workspace_geometry(K):
+    L = K.lib()
+    d = _desc(K)
+    for B, Hq, T in ((1, 24, 32769), (32, 24, 65537), (1, 24, 262145)):
+        P = -(-T // 512)
+        n = B * Hq * P
+        r = lambda x: (x + 255) // 256 * 256
+        assert L.kvq_decode_workspace_size(ctypes.byref(d), B, Hq, T, 0) == 256 + 2 * r(4 * n) + r(4 * n * 256)
+
+
+def test_plane_bytes_match_page_figures(K):
+    L = K.lib()
+    fig = golden("page_figures.txt")
+    d = _desc(K, Hk=4, D=256, ps=16, pages=1)
+    per_pos = sum(L.kvq_plane_bytes(ctypes.byref(d), p) for p in range(4)) // 16
+    assert per_pos * 16 == fig["q4_bytes_per_position_16_layers_4_heads"]
+    assert per_pos // (2 * 4) == fig["q4_row_bytes_d256"]
+    b = _desc(K, fmt=1, Hk=4, D=256, ps=16, pages=1)
+    assert sum(L.kvq_plane_bytes(ctypes.byref(b), p) for p in range(4)) // 16 * 16 == \
+        fig["bf16_bytes_per_position_16_layers_4_heads"]
+    f = _desc(K, fmt=2, Hk=1, D=512, ps=16, pages=1, rope=64)
+    assert sum(L.kvq_plane_bytes(ctypes.byref(f), p) for p in range(4)) // 16 == fig["fp8_latent_bytes_per_token"]
+
+
+def test_product_path_has_no_oracle_or_cpu_fallback():
+    pkg = os.path.join(ROOT, "bit_quantized_kv_store_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h")):
+                text = open(os.path.join(dirpath, f)).read()
+                assert "import oracle" not in text and "from oracle" not in text, f
+                assert "kvq_oracle" not in text, f

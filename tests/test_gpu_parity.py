@@ -1,0 +1,361 @@
+"""GPU parity: the CUDA library through its C ABI against the CPU oracle.
+
+Codes, scales and fp8 bytes must be bit-exact; attention outputs must satisfy
+max|gpu - oracle| <= 2e-3 * max|oracle| per (sequence) output tensor [Hq, D]
+(per query row for prefill), the oracle computing in fp64 over the same
+quantised cache.  Sizes span several 16-key tiles, several 512-key
+partitions and ragged tails.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+from bit_quantized_kv_store_gb300 import synth
+
+pytestmark = pytest.mark.gpu
+
+TOL = 2e-3
+
+
+@pytest.fixture(scope="module")
+def K():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from bit_quantized_kv_store_gb300 import build
+    build.build()
+    from bit_quantized_kv_store_gb300 import _lib
+    _lib.lib()
+    return _lib
+
+
+DEV = "cuda"
+
+
+def bits_u16(t):
+    return t.cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+
+
+def assert_close(got, ref, tol=TOL, what=""):
+    got = np.asarray(got, np.float64)
+    scale = np.abs(ref).max()
+    err = np.abs(got - ref).max()
+    assert np.isfinite(got).all(), f"{what}: non-finite output"
+    assert err <= tol * scale, f"{what}: max-abs error {err:.3g} > {tol} * {scale:.3g}"
+    return err / scale
+
+
+def make_cache_pair(K, fmt, Hk, D, ps, n_pages, rope=0):
+    g = K.Cache(fmt, Hk, D, ps, n_pages, device=DEV, rope_dim=rope)
+    ofmt = {K.FMT_Q4_HAD32: O.Q4, K.FMT_BF16: O.BF16, K.FMT_FP8_ROW: O.FP8}[fmt]
+    o = O.Cache(ofmt, Hk, D, ps, n_pages, rope_dim=rope)
+    return g, o
+
+
+def to_np_in(t):
+    """Host copy of an input tensor for the oracle (bf16 as uint16 bits)."""
+    if t.dtype == torch.bfloat16:
+        return bits_u16(t)
+    return t.cpu().numpy()
+
+
+def check_planes_equal(g, o):
+    assert np.array_equal(g.k.cpu().numpy().view(np.uint8) if g.k.dtype == torch.uint8 else bits_u16(g.k), o.k)
+    assert np.array_equal(g.v.cpu().numpy().view(np.uint8) if g.v.dtype == torch.uint8 else bits_u16(g.v), o.v)
+    if o.k_scale is not None:
+        if g.k_scale.dtype == torch.float16:
+            assert np.array_equal(bits_u16(g.k_scale), o.k_scale)
+            assert np.array_equal(bits_u16(g.v_scale), o.v_scale)
+        else:
+            assert np.array_equal(g.k_scale.cpu().numpy().view(np.uint32), o.k_scale.view(np.uint32))
+            assert np.array_equal(g.v_scale.cpu().numpy().view(np.uint32), o.v_scale.view(np.uint32))
+
+
+def fill_sequence(K, g, o, k, v, bt_row, T, status=None):
+    ps = g.page_size
+    slots = np.array([bt_row[j // ps] * ps + j % ps for j in range(T)], np.int32)
+    K.store(g, k.to(DEV), None if v is None else v.to(DEV), torch.from_numpy(slots).to(DEV), status=status)
+    O.store(o, to_np_in(k), None if v is None else to_np_in(v), slots)
+
+
+# --------------------------------------------------------------------------- store
+
+@pytest.mark.parametrize("D", [64, 128, 256])
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+def test_store_q4_bit_exact(K, D, dtype):
+    Hk, ps, n_pages, T = 3, 32, 9, 250
+    k = synth.outlier_normal((T, Hk, D), 4, 20.0, "cpu", D, "k").to(dtype)
+    v = synth.heavy_tailed((T, Hk, D), "cpu", D, "v").to(dtype)
+    g, o = make_cache_pair(K, K.FMT_Q4_HAD32, Hk, D, ps, n_pages)
+    bt = synth.page_permutation(n_pages, D, "pages").numpy().astype(np.int32)
+    fill_sequence(K, g, o, k, v, bt, T)
+    torch.cuda.synchronize()
+    check_planes_equal(g, o)
+
+
+def test_store_q4_exact_scale_and_edge_rows(K):
+    """Exact-scale rows (codes equal the inputs), zero rows, tiny rows, huge rows."""
+    D, Hk = 256, 1
+    rows = []
+    rng = np.random.default_rng(5)
+    for _ in range(8):
+        c = rng.integers(-8, 8, D)
+        c.reshape(8, 32)[:, 3] = -8
+        rows.append(O.hadamard32_f64(c.astype(np.float64)).astype(np.float32))
+    rows.append(np.zeros(D, np.float32))
+    rows.append(np.full(D, 1e-9, np.float32))
+    rows.append((rng.standard_normal(D) * 1e6).astype(np.float32))
+    rows.append((rng.standard_normal(D) * 1e-5).astype(np.float32))
+    x = torch.from_numpy(np.stack(rows)[:, None, :])
+    T = x.shape[0]
+    g, o = make_cache_pair(K, K.FMT_Q4_HAD32, Hk, D, 16, 1)
+    fill_sequence(K, g, o, x, x, np.array([0], np.int32), T)
+    torch.cuda.synchronize()
+    check_planes_equal(g, o)
+    assert np.all(bits_u16(g.k_scale)[0, 0, :8] == 0x3C00)   # scale 1.0
+
+
+def test_store_skips_negative_and_flags_bad_slots(K):
+    D, Hk, ps = 64, 2, 16
+    g, o = make_cache_pair(K, K.FMT_Q4_HAD32, Hk, D, ps, 2)
+    k = synth.normal((4, Hk, D), "cpu", "k")
+    slots = torch.tensor([3, -1, 40, 17], dtype=torch.int32)
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    K.store(g, k.to(DEV), k.to(DEV), slots.to(DEV), status=st)
+    torch.cuda.synchronize()
+    assert K.read_status(st) & K.DEV_BAD_SLOT
+    assert O.store(o, k.numpy(), k.numpy(), slots.numpy()) == 1
+    check_planes_equal(g, o)
+
+
+def test_store_one_at_a_time_equals_batch(K):
+    D, Hk, ps, T = 256, 4, 16, 70
+    k = synth.heavy_tailed((T, Hk, D), "cpu", 7, "k")
+    v = synth.heavy_tailed((T, Hk, D), "cpu", 7, "v")
+    g1 = K.Cache(K.FMT_Q4_HAD32, Hk, D, ps, 5, device=DEV)
+    g2 = K.Cache(K.FMT_Q4_HAD32, Hk, D, ps, 5, device=DEV)
+    slots = torch.arange(T, dtype=torch.int32, device=DEV)
+    K.store(g1, k.to(DEV), v.to(DEV), slots)
+    for j in range(T):
+        K.store(g2, k[j:j + 1].to(DEV), v[j:j + 1].to(DEV), slots[j:j + 1])
+    torch.cuda.synchronize()
+    assert torch.equal(g1.k, g2.k) and torch.equal(g1.v, g2.v)
+    assert torch.equal(g1.k_scale.view(torch.int16), g2.k_scale.view(torch.int16))
+
+
+def test_store_fp8_bit_exact(K):
+    T, D, R, ps = 300, 512, 64, 16
+    rows = synth.latent_rows(T, D + R, "cpu", "fp8")
+    rows[5] = 0.0                       # zero row
+    rows[6] = 1e-40                     # subnormal amax (448/amax overflows)
+    rows[7, :D] = torch.linspace(-500, 500, D)
+    g, o = make_cache_pair(K, K.FMT_FP8_ROW, 1, D, ps, 20, rope=R)
+    bt = synth.page_permutation(20, "fp8pages").numpy().astype(np.int32)
+    fill_sequence(K, g, o, rows, None, bt, T)
+    torch.cuda.synchronize()
+    check_planes_equal(g, o)
+
+
+def test_store_bf16_bit_exact(K):
+    T, Hk, D = 100, 4, 256
+    k = synth.outlier_normal((T, Hk, D), 4, 20.0, "cpu", "bk")
+    v = synth.outlier_normal((T, Hk, D), 4, 20.0, "cpu", "bv")
+    g, o = make_cache_pair(K, K.FMT_BF16, Hk, D, 16, 7)
+    fill_sequence(K, g, o, k, v, np.arange(7, dtype=np.int32), T)
+    torch.cuda.synchronize()
+    check_planes_equal(g, o)
+
+
+def test_rotate_query(K):
+    x = synth.heavy_tailed((5, 24, 256), "cpu", "rq")
+    y = K.rotate_query(x.to(DEV)).cpu().numpy().astype(np.float64)
+    ref = O.hadamard32_f64(x.float().numpy().astype(np.float64).reshape(-1)).reshape(y.shape)
+    assert np.abs(y - ref).max() <= 1e-5 * np.abs(ref).max()
+    xf = synth.normal((3, 64), "cpu", "rq2").to(DEV)
+    K.rotate_query(xf, out=xf)   # in place
+    assert np.allclose(xf.cpu().numpy(), O.hadamard32_f64(synth.normal((3, 64), "cpu", "rq2").numpy().astype(
+        np.float64).reshape(-1)).reshape(3, 64), atol=1e-5)
+
+
+# --------------------------------------------------------------------------- decode
+
+def decode_case(K, lens, Hk=4, Hq=24, D=256, ps=16, fmt=None, seed=0, dtype=torch.bfloat16, shuffle=True, gen="heavy"):
+    fmt = K.FMT_Q4_HAD32 if fmt is None else fmt
+    B = len(lens)
+    pages_per = [(L + ps - 1) // ps for L in lens]
+    n_pages = sum(pages_per) + 2
+    max_pages = max(max(pages_per), 1)
+    perm = synth.page_permutation(n_pages, seed, "perm").numpy().astype(np.int32) if shuffle else \
+        np.arange(n_pages, dtype=np.int32)
+    bt = np.zeros((B, max_pages), np.int32)
+    off = 0
+    for b, npg in enumerate(pages_per):
+        bt[b, :npg] = perm[off:off + npg]
+        off += npg
+    g, o = make_cache_pair(K, fmt, Hk, D, ps, n_pages)
+    for b, L in enumerate(lens):
+        if L == 0:
+            continue
+        if gen == "heavy":
+            k = synth.heavy_tailed((L, Hk, D), "cpu", seed, b, "k", dtype=dtype)
+            v = synth.heavy_tailed((L, Hk, D), "cpu", seed, b, "v", dtype=dtype)
+        else:
+            k = synth.outlier_normal((L, Hk, D), 4, 20.0, "cpu", seed, b, "k").to(dtype)
+            v = synth.outlier_normal((L, Hk, D), 4, 20.0, "cpu", seed, b, "v").to(dtype)
+        fill_sequence(K, g, o, k, v, bt[b], L)
+    if gen == "heavy":
+        q = synth.heavy_tailed((B, Hq, D), "cpu", seed, "q", dtype=dtype)
+    else:
+        q = synth.outlier_normal((B, Hq, D), 4, 20.0, "cpu", seed, "q").to(dtype)
+    return g, o, bt, q, max(max(lens), 1)
+
+
+def run_decode(K, g, bt, q, lens, max_len, sm_scale, sel=None):
+    B, Hq = q.shape[0], q.shape[1]
+    ws = K.alloc_workspace(g, B, Hq, max_len, 0 if sel is None else sel.shape[1], device=DEV)
+    seq = torch.tensor(lens, dtype=torch.int32, device=DEV)
+    out = K.decode(g, q.to(DEV), seq, torch.from_numpy(bt).to(DEV), max_len, sm_scale, ws,
+                   sel=None if sel is None else torch.from_numpy(sel).to(DEV))
+    torch.cuda.synchronize()
+    return out.cpu().numpy(), ws
+
+
+def test_decode_tiny_config(K):
+    """1 sequence, 1024 keys, 4 KV / 24 query heads, head_dim 256, fp32 inputs with x20 outliers."""
+    lens = [1024]
+    g, o, bt, q, ml = decode_case(K, lens, dtype=torch.float32, gen="outlier", shuffle=False)
+    torch.cuda.synchronize()
+    check_planes_equal(g, o)
+    out, _ = run_decode(K, g, bt, q, lens, ml, 1 / 16)
+    ref = O.decode(o, to_np_in(q), lens, bt, 1 / 16)
+    assert_close(out[0], ref[0], what="tiny decode")
+
+
+@pytest.mark.parametrize("T", [1, 2, 15, 16, 17, 127, 128, 129, 511, 512, 513, 1025, 4097])
+def test_decode_lengths(K, T):
+    g, o, bt, q, ml = decode_case(K, [T], seed=T)
+    out, _ = run_decode(K, g, bt, q, [T], ml, 1 / 16)
+    ref = O.decode(o, to_np_in(q), [T], bt, 1 / 16)
+    assert_close(out[0], ref[0], what=f"T={T}")
+
+
+def test_decode_ragged_paged_batch(K):
+    lens = [1, 700, 33, 2048, 1500, 0, 513, 3000]
+    g, o, bt, q, ml = decode_case(K, lens, seed=11)
+    out, _ = run_decode(K, g, bt, q, lens, ml, 1 / 16)
+    ref = O.decode(o, to_np_in(q), lens, bt, 1 / 16)
+    for b in range(len(lens)):
+        if lens[b] == 0:
+            assert np.all(out[b] == 0)
+        else:
+            assert_close(out[b], ref[b], what=f"seq {b}")
+
+
+@pytest.mark.parametrize("Hk,Hq", [(1, 1), (2, 4), (1, 8), (8, 8), (3, 21)])
+def test_decode_gqa_groups(K, Hk, Hq):
+    lens = [900, 77]
+    g, o, bt, q, ml = decode_case(K, lens, Hk=Hk, Hq=Hq, seed=Hk * 100 + Hq)
+    out, _ = run_decode(K, g, bt, q, lens, ml, 0.07)
+    ref = O.decode(o, to_np_in(q), lens, bt, 0.07)
+    for b in range(2):
+        assert_close(out[b], ref[b], what=f"Hk={Hk} Hq={Hq} seq {b}")
+
+
+def test_decode_concurrent_equals_solo_and_deterministic(K):
+    lens = [1200, 530, 4100]
+    g, o, bt, q, ml = decode_case(K, lens, seed=3)
+    out, _ = run_decode(K, g, bt, q, lens, ml, 1 / 16)
+    out2, _ = run_decode(K, g, bt, q, lens, ml, 1 / 16)
+    assert np.array_equal(out, out2)
+    for b in range(3):
+        solo, _ = run_decode(K, g, bt[b:b + 1], q[b:b + 1], [lens[b]], lens[b], 1 / 16)
+        assert np.array_equal(solo[0], out[b])
+
+
+def test_decode_gather(K):
+    lens = [3000, 1800]
+    g, o, bt, q, ml = decode_case(K, lens, seed=21)
+    for n_sel in (1, 100, 512, 1300):
+        sel = np.stack([synth.distinct_sorted(n_sel, L, 21, b).numpy() for b, L in enumerate(lens)]).astype(np.int32)
+        out, _ = run_decode(K, g, bt, q, lens, ml, 1 / 16, sel=sel)
+        ref = O.decode(o, to_np_in(q), lens, bt, 1 / 16, sel=sel)
+        for b in range(2):
+            assert_close(out[b], ref[b], what=f"gather n_sel={n_sel} seq {b}")
+
+
+def test_decode_bad_page_and_length_are_flagged(K):
+    lens = [600, 300]
+    g, o, bt, q, ml = decode_case(K, lens, seed=4)
+    bad = bt.copy()
+    bad[0, 3] = 10_000
+    out, ws = run_decode(K, g, bad, q, lens, ml, 1 / 16)
+    assert K.read_status(ws) & K.DEV_BAD_PAGE
+    assert np.isnan(out[0]).all()
+    ref = O.decode(o, to_np_in(q), [lens[1]], bt[1:2], 1 / 16)
+    assert_close(out[1], ref[0], what="healthy sequence next to a bad one")
+    out, ws = run_decode(K, g, bt, q, [600, 5000], ml, 1 / 16)   # length above max_seq_len
+    assert K.read_status(ws) & K.DEV_BAD_LENGTH
+    assert np.isnan(out[1]).all()
+
+
+def test_decode_bf16_cache(K):
+    lens = [1500, 513, 20]
+    g, o, bt, q, ml = decode_case(K, lens, fmt=K.FMT_BF16, seed=8)
+    torch.cuda.synchronize()
+    check_planes_equal(g, o)
+    out, _ = run_decode(K, g, bt, q, lens, ml, 1 / 16)
+    ref = O.decode(o, to_np_in(q), lens, bt, 1 / 16)
+    for b in range(3):
+        assert_close(out[b], ref[b], what=f"bf16 seq {b}")
+
+
+def test_decode_fp8_latent(K):
+    D, R, ps, Hq = 512, 64, 16, 32
+    lens = [1100, 40]
+    n_pages = sum((L + ps - 1) // ps for L in lens) + 1
+    g, o = make_cache_pair(K, K.FMT_FP8_ROW, 1, D, ps, n_pages, rope=R)
+    perm = synth.page_permutation(n_pages, "fp8dec").numpy().astype(np.int32)
+    mp = max((L + ps - 1) // ps for L in lens)
+    bt = np.zeros((2, mp), np.int32)
+    off = 0
+    for b, L in enumerate(lens):
+        npg = (L + ps - 1) // ps
+        bt[b, :npg] = perm[off:off + npg]
+        off += npg
+        fill_sequence(K, g, o, synth.latent_rows(L, D + R, "cpu", "fp8dec", b), None, bt[b], L)
+    torch.cuda.synchronize()
+    check_planes_equal(g, o)
+    q = synth.normal((2, Hq, D + R), "cpu", "fp8q")
+    sm = 1 / math.sqrt(D + R)
+    out, _ = run_decode(K, g, bt, q, lens, max(lens), sm)
+    ref = O.decode(o, q.numpy(), lens, bt, sm)
+    for b in range(2):
+        assert_close(out[b], ref[b], what=f"fp8 seq {b}")
+    sel = np.stack([synth.distinct_sorted(37, L, "fp8sel", b).numpy() for b, L in enumerate(lens)]).astype(np.int32)
+    out, _ = run_decode(K, g, bt, q, lens, max(lens), sm, sel=sel)
+    ref = O.decode(o, q.numpy(), lens, bt, sm, sel=sel)
+    for b in range(2):
+        assert_close(out[b], ref[b], what=f"fp8 gather seq {b}")
+
+
+# --------------------------------------------------------------------------- prefill
+
+@pytest.mark.parametrize("depth,n_q", [(0, 20), (100, 37), (600, 150)])
+def test_prefill(K, depth, n_q):
+    Hk, Hq, D, ps = 4, 24, 256, 16
+    T = depth + n_q
+    n_pages = (T + ps - 1) // ps + 1
+    g, o = make_cache_pair(K, K.FMT_Q4_HAD32, Hk, D, ps, n_pages)
+    bt = synth.page_permutation(n_pages, "pf", depth).numpy().astype(np.int32)
+    k = synth.heavy_tailed((T, Hk, D), "cpu", "pfk", depth)
+    v = synth.heavy_tailed((T, Hk, D), "cpu", "pfv", depth)
+    fill_sequence(K, g, o, k, v, bt, T)
+    q = synth.heavy_tailed((n_q, Hq, D), "cpu", "pfq", depth)
+    out = K.prefill_attn(g, q.to(DEV), depth, torch.from_numpy(bt).to(DEV), 1 / 16)
+    torch.cuda.synchronize()
+    ref = O.prefill(o, to_np_in(q), depth, bt, 1 / 16)
+    got = out.cpu().numpy()
+    for i in range(n_q):
+        assert_close(got[i], ref[i], what=f"prefill row {i}")
