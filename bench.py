@@ -47,7 +47,14 @@ def parse():
     ap.add_argument("--long-context", type=int, default=262144)
     ap.add_argument("--no-long", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    return ap.parse_args()
+    ap.add_argument("--no-rows", action="store_true", help="skip the other hot-path rows (batched decode, prefill, "
+                    "fp8, bf16 cache, store)")
+    ap.add_argument("--layers", type=int, default=16, help="layers per step (16 for the benchmark; fewer "
+                    "only to profile a small case)")
+    args = ap.parse_args()
+    global LAYERS
+    LAYERS = args.layers
+    return args
 
 
 def load_peaks():
@@ -140,6 +147,11 @@ class Workload:
         self.sm_scale = 1.0 / math.sqrt(D)
         torch.cuda.synchronize()
 
+    def decode_only(self):
+        """The 16 layers' decode launches alone (for the per-launch timing)."""
+        for layer in range(LAYERS):
+            self.K.decode_attn(self.caches[layer], self.qrot, self.seq, self.bt, self.T, self.sm_scale, self.ws)
+
     def step(self, i, ev=None, new_k=None, new_v=None, q=None, out=None):
         """One token through the 16 layers; ev = list of (start, end) events per decode."""
         K = self.K
@@ -160,40 +172,66 @@ class Workload:
         return 4 * LAYERS   # kernels launched
 
 
+def capture(torch, fn):
+    """Capture fn() (launches on the current stream) into a CUDA graph."""
+    g = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        fn()  # warm-up outside the capture
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    with torch.cuda.graph(g, capture_error_mode="thread_local"):
+        fn()
+    torch.cuda.synchronize()
+    return g
+
+
 def time_device(W, steps, warmup, torch):
+    """Device time of `steps` steps (one graph replay each) and the average
+    duration of one decode launch (a graph of the 16 layers' decode launches,
+    timed with CUDA events on the replay stream)."""
+    n_in = W.new_k.shape[0]
+    graphs = [capture(torch, lambda i=i: W.step(i)) for i in range(n_in)]
+    dec_graph = capture(torch, W.decode_only)
     for i in range(warmup):
-        W.step(i % W.new_k.shape[0])
+        graphs[i % n_in].replay()
     torch.cuda.synchronize()
-    evs = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(LAYERS)]
-           for _ in range(steps)]
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    launches = 0
-    torch.cuda.synchronize()
     t0.record()
     for s in range(steps):
-        ev = [[e[0], e[1]] for e in evs[s]]
-        launches += W.step(s % W.new_k.shape[0], ev=ev)
+        graphs[s % n_in].replay()
     t1.record()
     torch.cuda.synchronize()
     total_ms = t0.elapsed_time(t1)
-    dec_ms = [a.elapsed_time(b) for st in evs for (a, b) in st]
-    return total_ms, dec_ms, launches
+    for _ in range(2):
+        dec_graph.replay()
+    d0, d1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    d0.record()
+    for s in range(steps):
+        dec_graph.replay()
+    d1.record()
+    torch.cuda.synchronize()
+    dec_avg_ms = d0.elapsed_time(d1) / (steps * LAYERS)
+    return total_ms, dec_avg_ms, 4 * LAYERS * steps, graphs
 
 
-def time_e2e(W, steps, warmup, torch):
-    """Host buffers in, host buffers out, copies inside the timed region."""
+def time_e2e(W, steps, warmup, torch, graphs):
+    """Host buffers in, host buffers out, copies inside the timed region: the
+    step's new K/V rows and queries are copied from pinned host memory into the
+    device buffers the captured step reads, the step graph runs, and the 16
+    layers' outputs are copied back."""
     n_in = W.new_k.shape[0]
     hk = [W.new_k[i].cpu().pin_memory() for i in range(n_in)]
     hv = [W.new_v[i].cpu().pin_memory() for i in range(n_in)]
     hq = [W.q[i].cpu().pin_memory() for i in range(n_in)]
     hout = torch.empty(W.out.shape, dtype=torch.float32).pin_memory()
-    dk, dv, dq = torch.empty_like(W.new_k[0]), torch.empty_like(W.new_v[0]), torch.empty_like(W.q[0])
 
     def one(i):
-        dk.copy_(hk[i], non_blocking=True)
-        dv.copy_(hv[i], non_blocking=True)
-        dq.copy_(hq[i], non_blocking=True)
-        W.step(i, new_k=dk, new_v=dv, q=dq)
+        W.new_k[i].copy_(hk[i], non_blocking=True)
+        W.new_v[i].copy_(hv[i], non_blocking=True)
+        W.q[i].copy_(hq[i], non_blocking=True)
+        graphs[i].replay()
         hout.copy_(W.out, non_blocking=True)
         torch.cuda.current_stream().synchronize()
 
@@ -204,7 +242,7 @@ def time_e2e(W, steps, warmup, torch):
     for s in range(steps):
         one(s % n_in)
     el = time.perf_counter() - t
-    h2d = dk.numel() * dk.element_size() + dv.numel() * dv.element_size() + dq.numel() * dq.element_size()
+    h2d = sum(x.numel() * x.element_size() for x in (hk[0], hv[0], hq[0]))
     d2h = hout.numel() * hout.element_size()
     return el * 1e3, h2d, d2h
 
@@ -256,6 +294,165 @@ def run_reference(args):
     print(json.dumps(line))
 
 
+# --------------------------------------------------------------------------- the other hot-path rows
+
+def _events_time(torch, fn, iters, warmup=3):
+    """Average device time (ms) of fn() over iters runs, CUDA events on the current stream."""
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(iters):
+        fn()
+    b.record()
+    torch.cuda.synchronize()
+    return a.elapsed_time(b) / iters
+
+
+def measure_rows(K, synth, torch, dev, peak, tflops_peak):
+    """Batched ragged paged decode, prefill chunk, fp8 latent decode (dense and
+    gathered), the bf16-cache comparison and the store, each timed with CUDA
+    events (inputs resident in HBM)."""
+    out = {}
+    seed = 1234 + 3
+    # ---- batched ragged paged decode: 32 sequences, lengths ~ U{1024..65536}, 16-token pages, shuffled tables
+    lens = synth.ragged_lengths(32, 1024, 65536, seed, "lens").tolist()
+    T = [L + 1 for L in lens]
+    pages = [(t + PS - 1) // PS for t in T]
+    n_pages = sum(pages)
+    perm = synth.page_permutation(n_pages, seed, "perm")
+    bt = torch.zeros((32, max(pages)), dtype=torch.int32)
+    off = 0
+    for i, npg in enumerate(pages):
+        bt[i, :npg] = perm[off:off + npg]
+        off += npg
+    bt = bt.to(dev)
+    c = K.Cache(K.FMT_Q4_HAD32, HK, D, PS, n_pages, device=dev)
+    for i, L in enumerate(lens):
+        k = synth.heavy_tailed((L, HK, D), dev, seed, i, "k", subset=(seed, "k"))
+        v = synth.heavy_tailed((L, HK, D), dev, seed, i, "v", subset=(seed, "v"))
+        pos = torch.arange(L, device=dev)
+        slots = (bt[i][pos // PS] * PS + pos % PS).to(torch.int32)
+        K.store(c, k, v, slots)
+    new_k = synth.heavy_tailed((32, HK, D), dev, seed, "nk", subset=(seed, "k"))
+    new_v = synth.heavy_tailed((32, HK, D), dev, seed, "nv", subset=(seed, "v"))
+    q = synth.heavy_tailed((32, HQ, D), dev, seed, "q")
+    new_slots = torch.tensor([int(bt[i][lens[i] // PS]) * PS + lens[i] % PS for i in range(32)], dtype=torch.int32,
+                             device=dev)
+    seq = torch.tensor(T, dtype=torch.int32, device=dev)
+    qrot = torch.empty((32, HQ, D), dtype=torch.float32, device=dev)
+    o = torch.empty((32, HQ, D), dtype=torch.float32, device=dev)
+    ws = K.alloc_workspace(c, 32, HQ, max(T), device=dev)
+
+    def batched_step():
+        K.store(c, new_k, new_v, new_slots)
+        K.rotate_query(q, out=qrot)
+        K.decode_attn(c, qrot, seq, bt, max(T), 1 / 16, ws)
+        K.merge(c, ws, 32, HQ, seq, max(T), o)
+
+    ms = _events_time(torch, batched_step, 10)
+    dec_ms = _events_time(torch, lambda: K.decode_attn(c, qrot, seq, bt, max(T), 1 / 16, ws), 10)
+    byts = sum(T) * BYTES_PER_POS_LAYER
+    out["batched_paged_decode"] = {
+        "workload": "32 sequences, lengths U{1024..65536} (+1 new token each), 16-token pages, shuffled block "
+                    "tables, 1 layer, 4 KV / 24 q heads", "us_per_step": ms * 1e3, "decode_kernel_us": dec_ms * 1e3,
+        "cache_bytes": byts, "achieved_GBs": byts / (dec_ms * 1e-3) / 1e9, "frac_of_hbm_peak": byts / (dec_ms * 1e-3) / 1e9 / peak}
+    del c, ws
+    torch.cuda.empty_cache()
+
+    # ---- prefill chunk: 4096 queries at depth 16384, causal over decoded 4-bit slots
+    depth, nq = 16384, 4096
+    Tp = depth + nq
+    npg = (Tp + PS - 1) // PS
+    bt1 = synth.page_permutation(npg, seed, "pf").to(torch.int32).to(dev)
+    c = K.Cache(K.FMT_Q4_HAD32, HK, D, PS, npg, device=dev)
+    k = synth.heavy_tailed((Tp, HK, D), dev, seed, "pfk", subset=(seed, "k"))
+    v = synth.heavy_tailed((Tp, HK, D), dev, seed, "pfv", subset=(seed, "v"))
+    pos = torch.arange(Tp, device=dev)
+    slots = (bt1[pos // PS] * PS + pos % PS).to(torch.int32)
+    K.store(c, k[:depth], v[:depth], slots[:depth])
+    qp = synth.heavy_tailed((nq, HQ, D), dev, seed, "pfq")
+    op = torch.empty((nq, HQ, D), dtype=torch.float32, device=dev)
+    kc, vc, sc = k[depth:].contiguous(), v[depth:].contiguous(), slots[depth:].contiguous()
+
+    def prefill():
+        K.store(c, kc, vc, sc)
+        K.prefill_attn(c, qp, depth, bt1, 1 / 16, out=op)
+
+    ms = _events_time(torch, prefill, 2, warmup=1)
+    st_ms = _events_time(torch, lambda: K.store(c, kc, vc, sc), 10)
+    flops = sum(depth + i + 1 for i in range(nq)) * HQ * 4 * D
+    out["prefill_chunk"] = {"workload": "4096-token chunk at depth 16384 (store + causal attention over decoded "
+                                        "4-bit slots), 4 KV / 24 q heads", "ms": ms, "flop": flops,
+                            "TFLOPs": flops / (ms * 1e-3) / 1e12, "frac_of_bf16_peak": flops / (ms * 1e-3) / 1e12 /
+                            tflops_peak, "kernel": "prefill_q4_simple_kernel (CUDA cores)"}
+    rows = nq * HK * 2
+    out["store"] = {"workload": "4096 tokens x 4 KV heads x (K, V) bf16 rows of 256 -> 4-bit rotated rows",
+                    "us": st_ms * 1e3, "rows_per_s": rows / (st_ms * 1e-3),
+                    "GBs": rows * (512 + 144) / (st_ms * 1e-3) / 1e9}
+    del c, k, v
+    torch.cuda.empty_cache()
+
+    # ---- fp8 latent rows: dense absorbed decode over 262144 rows, 128 heads, and a 2048-row gather
+    Tf, Hf, DL, R = 262144, 128, 512, 64
+    npg = Tf // PS
+    c = K.Cache(K.FMT_FP8_ROW, 1, DL, PS, npg, device=dev, rope_dim=R)
+    for s0 in range(0, Tf, 65536):
+        rows_ = synth.latent_rows(65536, DL + R, dev, seed, "fp8", s0)
+        K.store(c, rows_, None, torch.arange(s0, s0 + 65536, dtype=torch.int32, device=dev))
+    qf = synth.normal((1, Hf, DL + R), dev, seed, "fp8q")
+    btf = torch.arange(npg, dtype=torch.int32, device=dev).reshape(1, -1)
+    seqf = torch.tensor([Tf], dtype=torch.int32, device=dev)
+    of = torch.empty((1, Hf, DL), dtype=torch.float32, device=dev)
+    wsf = K.alloc_workspace(c, 1, Hf, Tf, device=dev)
+    smf = 1 / math.sqrt(DL + R)
+
+    def fp8_dense():
+        K.decode_attn(c, qf, seqf, btf, Tf, smf, wsf)
+        K.merge(c, wsf, 1, Hf, seqf, Tf, of)
+
+    ms = _events_time(torch, fp8_dense, 3, warmup=1)
+    flops = Hf * Tf * 2 * (DL + R + DL)
+    byts = Tf * (DL + R + 8)
+    sel = synth.distinct_sorted(2048, Tf, seed, "sel").to(torch.int32).to(dev).reshape(1, -1)
+    wsg = K.alloc_workspace(c, 1, Hf, Tf, n_sel=2048, device=dev)
+
+    def fp8_gather():
+        K.decode_attn(c, qf, seqf, btf, Tf, smf, wsg, sel=sel)
+        K.merge(c, wsg, 1, Hf, seqf, Tf, of, n_sel=2048)
+
+    gms = _events_time(torch, fp8_gather, 5)
+    out["fp8_latent"] = {"workload": "absorbed decode, 128 heads x (512 latent + 64 rope) e4m3 rows, context 262144, "
+                                     "split-T + merge", "us": ms * 1e3, "flop": flops, "TFLOPs": flops / (ms * 1e-3) / 1e12,
+                         "GBs": byts / (ms * 1e-3) / 1e9, "gather_2048_us": gms * 1e3,
+                         "kernel": "decode_rows_kernel (CUDA cores)"}
+    del c, wsf, wsg
+    torch.cuda.empty_cache()
+
+    # ---- bf16-cache comparison at 32K (same kernel structure, unrotated bf16 rows)
+    Tb = 32769
+    npg = (Tb + PS - 1) // PS
+    c = K.Cache(K.FMT_BF16, HK, D, PS, npg, device=dev)
+    k = synth.heavy_tailed((Tb, HK, D), dev, seed, "bk", subset=(seed, "k"))
+    v = synth.heavy_tailed((Tb, HK, D), dev, seed, "bv", subset=(seed, "v"))
+    K.store(c, k, v, torch.arange(Tb, dtype=torch.int32, device=dev))
+    qb = synth.heavy_tailed((1, HQ, D), dev, seed, "bq").float()
+    btb = torch.arange(npg, dtype=torch.int32, device=dev).reshape(1, -1)
+    seqb = torch.tensor([Tb], dtype=torch.int32, device=dev)
+    ob = torch.empty((1, HQ, D), dtype=torch.float32, device=dev)
+    wsb = K.alloc_workspace(c, 1, HQ, Tb, device=dev)
+    dms = _events_time(torch, lambda: K.decode_attn(c, qb, seqb, btb, Tb, 1 / 16, wsb), 10)
+    byts = Tb * HK * 2 * D * 2
+    out["bf16_cache_32k"] = {"workload": "bf16 (unrotated) cache, context 32768, 1 layer, same split-T + merge",
+                             "decode_kernel_us": dms * 1e3, "cache_bytes": byts, "achieved_GBs": byts / (dms * 1e-3) / 1e9,
+                             "bytes_vs_4bit": byts / (Tb * BYTES_PER_POS_LAYER),
+                             "kernel": "decode_rows_kernel (CUDA cores)"}
+    del c, wsb
+    torch.cuda.empty_cache()
+    return out
+
+
 def main():
     args = parse()
     if args.impl == "reference":
@@ -297,15 +494,15 @@ def main():
     W = Workload(K, synth, torch, args.context, n_inputs, 1234 + 1 + rank, dev)
     barrier()
     with Clocks(local) as clk:
-        total_ms, dec_ms, launches = time_device(W, args.steps, args.warmup, torch)
+        total_ms, dec_avg_ms, launches, graphs = time_device(W, args.steps, args.warmup, torch)
     barrier()
     total_ms = max_over_ranks(total_ms)
     layer_tokens = LAYERS * args.steps * world
     us_per_lt = total_ms * 1e3 / layer_tokens
-    dec_avg_ms = statistics.mean(dec_ms)
     bytes_per_launch = W.T * BYTES_PER_POS_LAYER
     achieved = bytes_per_launch / (dec_avg_ms * 1e-3) / 1e9
-    e2e_ms, h2d, d2h = time_e2e(W, max(3, args.steps // 2), 2, torch)
+    e2e_ms, h2d, d2h = time_e2e(W, max(3, args.steps // 2), 2, torch, graphs)
+    del graphs
     e2e_ms = max_over_ranks(e2e_ms)
     e2e_us = e2e_ms * 1e3 / (LAYERS * max(3, args.steps // 2) * world)
 
@@ -317,9 +514,9 @@ def main():
         lsteps = max(3, args.steps // 4)
         barrier()
         with Clocks(local) as clk2:
-            ltot, ldec, _ = time_device(WL, lsteps, max(3, args.warmup // 2), torch)
+            ltot, lavg, _, lgraphs = time_device(WL, lsteps, max(3, args.warmup // 2), torch)
+        del lgraphs
         ltot = max_over_ranks(ltot)
-        lavg = statistics.mean(ldec)
         lbytes = WL.T * BYTES_PER_POS_LAYER
         lach = lbytes / (lavg * 1e-3) / 1e9
         long = {"context": args.long_context, "value": ltot * 1e3 / (LAYERS * lsteps * world),
@@ -328,6 +525,16 @@ def main():
                              "traffic": None, "bytes_per_launch": lbytes},
                 "clocks": clk2.summary()}
         del WL
+
+    rows = None
+    if not args.no_rows and rank == 0:
+        tf_peak = 1922.8
+        try:
+            with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+                tf_peak = json.load(f).get("bf16_tflops", tf_peak)
+        except OSError:
+            pass
+        rows = measure_rows(K, synth, torch, dev, peak, tf_peak)
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
@@ -352,6 +559,7 @@ def main():
             "gpu_launches": launches,
             "clocks": clk.summary(),
             "long_context": long,
+            "rows": rows,
             "cpu_baseline": cpu,
         }
         print(json.dumps(line))

@@ -1,5 +1,7 @@
 // api.cu -- the C ABI of libkvq (declared in include/kvq.h): host-side argument
 // validation, workspace geometry and kernel launches.  Nothing here allocates.
+#include <cudaTypedefs.h>
+
 #include <cstdio>
 
 #include "kernels.cuh"
@@ -12,6 +14,8 @@ static int32_t cuda_fail(cudaError_t e) {
   g_last_cuda_error = static_cast<int32_t>(e);
   return KVQ_ERR_CUDA;
 }
+
+int32_t record_cuda_failure(cudaError_t e) { return cuda_fail(e); }
 
 static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -41,6 +45,35 @@ static int32_t check_cache(const kvq_cache* c) {
 }
 
 static int value_width(const kvq_cache* c) { return c->head_dim; }
+
+// cuTensorMapEncodeTiled through the runtime's driver entry point (no link-time
+// dependency on libcuda); the pointer is looked up once.
+static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      p = nullptr;
+    return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }();
+  return fn;
+}
+
+// A plane of `rows` rows of `row_bytes` bytes, read in boxes of box_rows rows
+// with the 128-byte shared-memory swizzle.
+static bool encode_rows_map(CUtensorMap* m, const void* base, uint64_t rows, uint32_t row_bytes, uint32_t box_rows) {
+  PFN_cuTensorMapEncodeTiled_v12000 fn = tensor_map_encoder();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {row_bytes, rows > 0 ? rows : 1};
+  cuuint64_t strides[1] = {row_bytes};
+  cuuint32_t box[2] = {row_bytes, box_rows};
+  cuuint32_t es[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
 
 struct WsLayout {
   size_t m_off, z_off, acc_off, total;
@@ -170,10 +203,29 @@ int32_t kvq_decode_attn(const kvq_cache* cache, const float* q, int32_t num_seqs
   const int group = num_q_heads / cache->num_kv_heads;
   cudaError_t e;
   if (cache->format == KVQ_FMT_Q4_HAD32) {
-    DecodeArgs a{*cache, q, num_q_heads, group, d_seq_lens, d_block_tables, max_pages_per_seq, max_seq_len,
-                 d_sel, d_sel ? n_sel : 0, sm_scale * kLog2e,
-                 reinterpret_cast<float*>(ws + w.m_off), reinterpret_cast<float*>(ws + w.z_off),
-                 reinterpret_cast<float*>(ws + w.acc_off), w.P, reinterpret_cast<int32_t*>(ws)};
+    DecodeArgs a{};
+    a.c = *cache;
+    a.q = q;
+    a.Hq = num_q_heads;
+    a.group = group;
+    a.seq_lens = d_seq_lens;
+    a.block_tables = d_block_tables;
+    a.max_pages = max_pages_per_seq;
+    a.max_seq_len = max_seq_len;
+    a.sel = d_sel;
+    a.n_sel = d_sel ? n_sel : 0;
+    a.qscale = sm_scale * kLog2e;
+    a.ws_m = reinterpret_cast<float*>(ws + w.m_off);
+    a.ws_z = reinterpret_cast<float*>(ws + w.z_off);
+    a.ws_acc = reinterpret_cast<float*>(ws + w.acc_off);
+    a.P = w.P;
+    a.status = reinterpret_cast<int32_t*>(ws);
+    if (!d_sel) {
+      const uint64_t rows = static_cast<uint64_t>(cache->num_pages) * cache->num_kv_heads * cache->page_size;
+      if (rows >= (1ull << 31)) return KVQ_ERR_UNSUPPORTED;
+      if (!encode_rows_map(&a.tm_k, cache->k, rows, 128, 16) || !encode_rows_map(&a.tm_v, cache->v, rows, 128, 16))
+        return cuda_fail(cudaErrorInvalidValue);
+    }
     e = launch_decode_q4(a, num_seqs, s);
   } else {
     RowsArgs a{*cache, q, num_q_heads, group, cache->format == KVQ_FMT_BF16 ? group : 16, d_seq_lens,

@@ -6,128 +6,145 @@
 // order; and "KV cache quantization: fp8 (KV8) + 4-bit TurboQuant", split-T
 // commit: (H, P) partial online-softmax blocks (cl, m, z) + a log-sum-exp merge.
 //
-// GB300 design (one CTA per (partition of 512 keys, KV head, sequence)):
-//  * 4 warps, each owning 128 keys = 8 tiles of 16 keys.  Each warp streams its
-//    tiles through a private 4-stage ring in shared memory, filled by 1-D bulk
-//    (TMA) copies of whole 16-slot page rows: 2 KB of K codes, 256 B of K scales,
-//    2 KB of V codes, 256 B of V scales per tile.
-//  * Scores on the tensor cores with mma.m16n8k16 (keys on M, the <= 8 query
-//    heads of the GQA group on N).  The 4-bit codes minus 8 are exact in f16; the
-//    query is split into an f16 high and low part so the product keeps ~22 bits.
-//    Each 32-value group gets its own partial product, multiplied by the group's
-//    fp32 scale, so the dequantised keys are used exactly.
-//  * P.V on the tensor cores with the value dimension on M: the probabilities
-//    are transposed in registers (movmatrix) and multiplied by the V group scale
-//    in f16 before the MMA; V codes minus 8 are exact in f16.
-//  * Online softmax in base 2 (the query is pre-multiplied by sm_scale*log2 e).
-//  * The four warps' (m, z, acc) are combined in shared memory and written as the
-//    partition's partial.
+// GB300 design.  One CTA (4 warps) per (partition of 512 keys, KV head,
+// sequence); up to 3 CTAs per SM.  Warp w owns keys [128w, 128w + 128) of the
+// partition: 8 tiles of 16 keys streamed through a private 3-stage shared-memory
+// ring.  A tile is 2 KB of K codes and 2 KB of V codes, brought by 2-D TMA
+// tensor copies with the hardware 128-byte swizzle (16-byte chunk c of row r
+// lands at chunk c ^ (r & 7), so the fragment loads below are free of bank
+// conflicts), plus 256 B of K scales and 256 B of V scales by 1-D bulk copies.
+//  * Scores on the tensor cores: mma.m16n8k16, the 16 keys on M, the <= 8 query
+//    heads of the GQA group on N.  Codes minus 8 are exact in f16; the query is
+//    split into f16 high and low parts (~22 bits; its fragments sit in shared
+//    memory); each 32-value group gets its own partial product multiplied by
+//    the group's fp32 scale, so the dequantised keys enter exactly.
+//  * Online softmax in base 2 (the query carries sm_scale * log2 e).
+//  * P.V on the tensor cores with the value dims on M: the probabilities are
+//    transposed in registers (movmatrix) and multiplied by the V group scale in
+//    f16; V codes minus 8 are exact in f16.
+// The four warps' (m, z, acc) are combined in shared memory into the
+// partition's partial.  The gather variant (selected rows) copies row by row
+// with 1-D bulk copies into an unswizzled ring.
 #include "kernels.cuh"
 
 namespace kvq {
 
 constexpr int kQ4Warps = 4;
-constexpr int kQ4Ring = 4;
+constexpr int kQ4Ring = 3;
 constexpr int kQ4TilesPerWarp = kPart / 16 / kQ4Warps;  // 8
 constexpr int kQ4D = 256;
 constexpr int kQ4NG = 8;
 
-struct __align__(128) Q4Stage {
-  uint8_t kc[16 * 128];
-  uint16_t ks[16 * 8];
-  uint8_t vc[16 * 128];
-  uint16_t vs[16 * 8];
+// Stage layout (1024-byte aligned for the 128-byte swizzle of the code tiles).
+struct __align__(1024) Q4Stage {
+  uint8_t kc[16 * 128];  // K codes, swizzled (dense) or plain (gather)
+  uint8_t vc[16 * 128];  // V codes
+  uint16_t ks[16 * 8];   // K scales
+  uint16_t vs[16 * 8];   // V scales
+  uint8_t pad[512];
 };
-static_assert(sizeof(Q4Stage) == 4608, "stage size");
+static_assert(sizeof(Q4Stage) == 5120, "stage size");
 
 struct Q4Smem {
   Q4Stage stage[kQ4Warps][kQ4Ring];
+  uint4 qf[kQ4NG][2][32];  // query fragments [group][hi, lo][lane]
   uint64_t bar[kQ4Warps][kQ4Ring];
+  int poison;
 };
 
-struct Q4Combine {  // reuses the ring after all warps are done
+struct Q4Combine {  // reuses the ring once every warp is done
   float acc[kQ4Warps][8][kQ4D];
   float m[kQ4Warps][8];
   float z[kQ4Warps][8];
 };
-static_assert(sizeof(Q4Combine) <= sizeof(Q4Stage) * kQ4Warps * kQ4Ring, "combine fits");
+static_assert(sizeof(Q4Combine) <= sizeof(Q4Stage) * kQ4Warps * kQ4Ring, "combine fits in the ring");
 
-__device__ __forceinline__ uint32_t word_of(const uint4& v, int i) {
-  return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w;
-}
-
-__device__ __forceinline__ float half_of(const uint4& v, int G) {
-  const uint32_t w = word_of(v, G >> 1);
-  const uint16_t h = (G & 1) ? static_cast<uint16_t>(w >> 16) : static_cast<uint16_t>(w & 0xFFFFu);
-  return __half2float(__ushort_as_half(h));
+__device__ __forceinline__ void tma_rows_2d(void* dst, const CUtensorMap* map, int row, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+          smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(0), "r"(row), "r"(smem_u32(bar))
+      : "memory");
 }
 
 // Issue the copies of one 16-key tile into `st`.  Returns false if a page or a
-// selected index is invalid (the tile is then treated as poisoned).
+// selected index is invalid (the tile then counts as poisoned; its barrier is
+// still completed so the consumer does not wait on it).
+template <bool GATHER>
 __device__ __forceinline__ bool q4_issue_tile(const DecodeArgs& a, int b, int kvh, int key0, int nvalid,
                                               Q4Stage* st, uint64_t* bar) {
   const kvq_cache& c = a.c;
   const int32_t* bt = a.block_tables + (int64_t)b * a.max_pages;
-  if (a.sel == nullptr) {
-    const int pidx = key0 / c.page_size;
-    const int32_t page = bt[pidx];
+  if constexpr (!GATHER) {
+    const int32_t page = bt[key0 / c.page_size];
     if (page < 0 || page >= c.num_pages) {
       set_status(a.status, KVQ_DEV_BAD_PAGE);
       mbar_arrive(bar);
       return false;
     }
     const int64_t row0 = ((int64_t)page * c.num_kv_heads + kvh) * c.page_size + key0 % c.page_size;
-    mbar_arrive_expect_tx(bar, sizeof(Q4Stage));
-    bulk_g2s(st->kc, static_cast<const uint8_t*>(c.k) + row0 * 128, 16 * 128, bar);
+    mbar_arrive_expect_tx(bar, 2 * 16 * 128 + 2 * 16 * 16);
+    tma_rows_2d(st->kc, &a.tm_k, static_cast<int>(row0), bar);
+    tma_rows_2d(st->vc, &a.tm_v, static_cast<int>(row0), bar);
     bulk_g2s(st->ks, static_cast<const uint16_t*>(c.k_scale) + row0 * 8, 16 * 16, bar);
-    bulk_g2s(st->vc, static_cast<const uint8_t*>(c.v) + row0 * 128, 16 * 128, bar);
     bulk_g2s(st->vs, static_cast<const uint16_t*>(c.v_scale) + row0 * 8, 16 * 16, bar);
     return true;
-  }
-  // gather: one row per selected position
-  const int32_t T = a.seq_lens[b];
-  bool ok = true;
-  int nrows = 0;
-  int64_t rows[16];
-  for (int j = 0; j < nvalid; ++j) {
-    const int32_t pos = a.sel[(int64_t)b * a.n_sel + key0 + j];
-    if (pos < 0 || pos >= T) {
-      set_status(a.status, KVQ_DEV_BAD_INDEX);
-      ok = false;
-      break;
+  } else {
+    const int32_t T = a.seq_lens[b];
+    int64_t rows[16];
+    for (int j = 0; j < nvalid; ++j) {
+      const int32_t pos = a.sel[(int64_t)b * a.n_sel + key0 + j];
+      int32_t page = -1;
+      if (pos < 0 || pos >= T) {
+        set_status(a.status, KVQ_DEV_BAD_INDEX);
+      } else {
+        page = bt[pos / c.page_size];
+        if (page < 0 || page >= c.num_pages) set_status(a.status, KVQ_DEV_BAD_PAGE);
+      }
+      if (page < 0 || page >= c.num_pages) {
+        mbar_arrive(bar);
+        return false;
+      }
+      rows[j] = ((int64_t)page * c.num_kv_heads + kvh) * c.page_size + pos % c.page_size;
     }
-    const int32_t page = bt[pos / c.page_size];
-    if (page < 0 || page >= c.num_pages) {
-      set_status(a.status, KVQ_DEV_BAD_PAGE);
-      ok = false;
-      break;
+    mbar_arrive_expect_tx(bar, nvalid * 288);
+    for (int j = 0; j < nvalid; ++j) {
+      bulk_g2s(st->kc + j * 128, static_cast<const uint8_t*>(c.k) + rows[j] * 128, 128, bar);
+      bulk_g2s(st->vc + j * 128, static_cast<const uint8_t*>(c.v) + rows[j] * 128, 128, bar);
+      bulk_g2s(st->ks + j * 8, static_cast<const uint16_t*>(c.k_scale) + rows[j] * 8, 16, bar);
+      bulk_g2s(st->vs + j * 8, static_cast<const uint16_t*>(c.v_scale) + rows[j] * 8, 16, bar);
     }
-    rows[j] = ((int64_t)page * c.num_kv_heads + kvh) * c.page_size + pos % c.page_size;
-    ++nrows;
+    return true;
   }
-  if (!ok) {
-    mbar_arrive(bar);
-    return false;
-  }
-  mbar_arrive_expect_tx(bar, nrows * 288);
-  for (int j = 0; j < nrows; ++j) {
-    bulk_g2s(st->kc + j * 128, static_cast<const uint8_t*>(c.k) + rows[j] * 128, 128, bar);
-    bulk_g2s(st->ks + j * 8, static_cast<const uint16_t*>(c.k_scale) + rows[j] * 8, 16, bar);
-    bulk_g2s(st->vc + j * 128, static_cast<const uint8_t*>(c.v) + rows[j] * 128, 128, bar);
-    bulk_g2s(st->vs + j * 8, static_cast<const uint16_t*>(c.v_scale) + rows[j] * 8, 16, bar);
-  }
-  return true;
 }
 
-__global__ void __launch_bounds__(kQ4Warps * 32, 2) decode_q4_kernel(const DecodeArgs a) {
-  extern __shared__ __align__(128) uint8_t smem_raw[];
-  Q4Smem& sm = *reinterpret_cast<Q4Smem*>(smem_raw);
+// shared-memory loads at a 32-bit shared address
+__device__ __forceinline__ uint4 lds128a(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
+  return v;
+}
+
+__device__ __forceinline__ uint32_t word_of(const uint4& v, int i) {
+  return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w;
+}
+
+__device__ __forceinline__ float scale_of(const uint4& v, int G) {
+  const uint32_t w = word_of(v, G >> 1);
+  return __half2float(__ushort_as_half(static_cast<uint16_t>((G & 1) ? (w >> 16) : (w & 0xFFFFu))));
+}
+
+template <bool GATHER>
+__global__ void __launch_bounds__(kQ4Warps * 32, 3) decode_q4_kernel(const __grid_constant__ DecodeArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  // 1024-byte alignment for the swizzled tiles (the launch adds 1 KB of slack)
+  Q4Smem& sm = *reinterpret_cast<Q4Smem*>(smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u));
   const int p = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, t = lane & 3;
 
   int32_t T;
-  if (a.sel) {
+  if (GATHER) {
     T = a.n_sel;
   } else {
     T = a.seq_lens[b];
@@ -144,45 +161,39 @@ __global__ void __launch_bounds__(kQ4Warps * 32, 2) decode_q4_kernel(const Decod
   const int my_first = warp * kQ4TilesPerWarp;
   const int my_tiles = max(0, min(kQ4TilesPerWarp, ntiles - my_first));
 
+  bool poisoned = false;
   if (lane == 0) {
     for (int s = 0; s < kQ4Ring; ++s) mbar_init(&sm.bar[warp][s], 1);
     fence_barrier_init();
-  }
-  __syncwarp();
-
-  bool poisoned = false;
-  if (lane == 0) {
     for (int i = 0; i < min(kQ4Ring, my_tiles); ++i) {
       const int key0 = k0 + 16 * (my_first + i);
-      if (!q4_issue_tile(a, b, kvh, key0, min(16, k1 - key0), &sm.stage[warp][i], &sm.bar[warp][i]))
+      if (!q4_issue_tile<GATHER>(a, b, kvh, key0, min(16, k1 - key0), &sm.stage[warp][i], &sm.bar[warp][i]))
         poisoned = true;
     }
   }
+  if (threadIdx.x == 0) sm.poison = 0;
 
-  // ---- query fragments (B operand of the score MMA), high and low f16 parts
-  uint32_t qh[kQ4NG][2][2], ql[kQ4NG][2][2];
-  {
-    const int head = kvh * a.group + g;
+  // ---- query fragments (B operand of the score MMA), written once by warp 0
+  if (warp == 0) {
     const bool live = g < a.group;
-    const float* qrow = a.q + ((int64_t)b * a.Hq + (live ? head : 0)) * kQ4D;
+    const float* qrow = a.q + ((int64_t)b * a.Hq + kvh * a.group + (live ? g : 0)) * kQ4D;
+    const float s = live ? a.qscale : 0.f;
 #pragma unroll
     for (int G = 0; G < kQ4NG; ++G) {
-      float v[8];
       const float4 u0 = *reinterpret_cast<const float4*>(qrow + 32 * G + 8 * t);
       const float4 u1 = *reinterpret_cast<const float4*>(qrow + 32 * G + 8 * t + 4);
-      v[0] = u0.x; v[1] = u0.y; v[2] = u0.z; v[3] = u0.w;
-      v[4] = u1.x; v[5] = u1.y; v[6] = u1.z; v[7] = u1.w;
-#pragma unroll
-      for (int i = 0; i < 8; ++i) v[i] = live ? v[i] * a.qscale : 0.f;
-      // tile (G,0): slots (2t,2t+1) <- d (8t, 8t+2); slots (2t+8, 2t+9) <- d (8t+1, 8t+3)
-      // tile (G,1): the same with d + 4
-#pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        split_f16(v[4 * e + 0], v[4 * e + 2], qh[G][e][0], ql[G][e][0]);
-        split_f16(v[4 * e + 1], v[4 * e + 3], qh[G][e][1], ql[G][e][1]);
-      }
+      uint4 hi, lo;
+      // tile (G,0): slots (2t,2t+1) <- d (8t, 8t+2); slots (2t+8, 2t+9) <- d (8t+1, 8t+3); tile (G,1): d + 4
+      split_f16(u0.x * s, u0.z * s, hi.x, lo.x);
+      split_f16(u0.y * s, u0.w * s, hi.y, lo.y);
+      split_f16(u1.x * s, u1.z * s, hi.z, lo.z);
+      split_f16(u1.y * s, u1.w * s, hi.w, lo.w);
+      sm.qf[G][0][lane] = hi;
+      sm.qf[G][1][lane] = lo;
     }
   }
+  __syncthreads();
+  const uint32_t qf_addr = smem_u32(&sm.qf[0][0][lane]);
 
   float acc[kQ4NG][2][4];
 #pragma unroll
@@ -193,9 +204,20 @@ __global__ void __launch_bounds__(kQ4Warps * 32, 2) decode_q4_kernel(const Decod
       for (int i = 0; i < 4; ++i) acc[G][e][i] = 0.f;
   float m0 = -INFINITY, m1 = -INFINITY;  // running max of heads 2t, 2t+1 (base 2)
   float z0 = 0.f, z1 = 0.f;              // this thread's partial sums
-
   const bool head0_live = 2 * t < a.group, head1_live = 2 * t + 1 < a.group;
   bool timed_out = false;
+
+  // Byte offsets of this thread's fragments inside a stage (swizzle: chunk ^ (row & 7)).
+  const int sw = GATHER ? 0 : g;       // rows g and g+8 share (row & 7) = g
+  const int swv = GATHER ? 0 : 2 * t;  // rows 2t, 2t+8 -> 2t ; rows 2t+1, 2t+9 -> 2t+1
+  const uint32_t off_ka0 = g * 128 + (((2 * t) ^ sw) << 4);
+  const uint32_t off_ka1 = g * 128 + (((2 * t + 1) ^ sw) << 4);
+  const uint32_t off_kb0 = off_ka0 + 8 * 128;
+  const uint32_t off_kb1 = off_ka1 + 8 * 128;
+  const uint32_t off_v0 = 2048 + (2 * t) * 128 + ((g ^ swv) << 4);
+  const uint32_t off_v1 = 2048 + (2 * t + 1) * 128 + ((g ^ (GATHER ? 0 : swv + 1)) << 4);
+  const uint32_t off_v2 = off_v0 + 8 * 128;
+  const uint32_t off_v3 = off_v1 + 8 * 128;
 
   for (int i = 0; i < my_tiles; ++i) {
     const int s = i % kQ4Ring;
@@ -204,19 +226,22 @@ __global__ void __launch_bounds__(kQ4Warps * 32, 2) decode_q4_kernel(const Decod
       timed_out = true;
       break;
     }
+    const uint32_t sbase = smem_u32(&st);
     const int key0 = k0 + 16 * (my_first + i);
     const int nvalid = min(16, k1 - key0);
 
     // ---------------- scores S[key][head] for keys g, g+8 and heads 2t, 2t+1
-    const uint4 ka0 = lds128(st.kc + g * 128 + 32 * t);
-    const uint4 ka1 = lds128(st.kc + g * 128 + 32 * t + 16);
-    const uint4 kb0 = lds128(st.kc + (g + 8) * 128 + 32 * t);
-    const uint4 kb1 = lds128(st.kc + (g + 8) * 128 + 32 * t + 16);
-    const uint4 ska = lds128(st.ks + g * 8);
-    const uint4 skb = lds128(st.ks + (g + 8) * 8);
+    const uint4 ka0 = lds128a(sbase + off_ka0);  // half-words (2t, G = 0..7) of row g
+    const uint4 ka1 = lds128a(sbase + off_ka1);  // half-words (2t+1, G)
+    const uint4 kb0 = lds128a(sbase + off_kb0);  // row g+8
+    const uint4 kb1 = lds128a(sbase + off_kb1);
+    const uint4 ska = lds128a(sbase + 4096 + g * 16);
+    const uint4 skb = lds128a(sbase + 4096 + (g + 8) * 16);
     float S[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
     for (int G = 0; G < kQ4NG; ++G) {
+      const uint4 qh = lds128a(qf_addr + G * 1024);
+      const uint4 ql = lds128a(qf_addr + G * 1024 + 512);
       const uint32_t sel = (G & 1) ? 0x4342u : 0x4140u;
       const uint32_t xa1 = prmt(word_of(ka0, G >> 1), 0u, sel);
       const uint32_t xa2 = prmt(word_of(ka1, G >> 1), 0u, sel);
@@ -225,11 +250,11 @@ __global__ void __launch_bounds__(kQ4Warps * 32, 2) decode_q4_kernel(const Decod
       const uint32_t a10 = nib_lo_pair(xa1), a11 = nib_lo_pair(xb1), a12 = nib_hi_pair(xa1), a13 = nib_hi_pair(xb1);
       const uint32_t a20 = nib_lo_pair(xa2), a21 = nib_lo_pair(xb2), a22 = nib_hi_pair(xa2), a23 = nib_hi_pair(xb2);
       float part[4] = {0.f, 0.f, 0.f, 0.f};
-      mma_f16(part, a10, a11, a12, a13, qh[G][0][0], qh[G][0][1]);
-      mma_f16(part, a20, a21, a22, a23, qh[G][1][0], qh[G][1][1]);
-      mma_f16(part, a10, a11, a12, a13, ql[G][0][0], ql[G][0][1]);
-      mma_f16(part, a20, a21, a22, a23, ql[G][1][0], ql[G][1][1]);
-      const float sa = half_of(ska, G), sb = half_of(skb, G);
+      mma_f16(part, a10, a11, a12, a13, qh.x, qh.y);
+      mma_f16(part, a20, a21, a22, a23, qh.z, qh.w);
+      mma_f16(part, a10, a11, a12, a13, ql.x, ql.y);
+      mma_f16(part, a20, a21, a22, a23, ql.z, ql.w);
+      const float sa = scale_of(ska, G), sb = scale_of(skb, G);
       S[0] = fmaf(sa, part[0], S[0]);
       S[1] = fmaf(sa, part[1], S[1]);
       S[2] = fmaf(sb, part[2], S[2]);
@@ -273,21 +298,21 @@ __global__ void __launch_bounds__(kQ4Warps * 32, 2) decode_q4_kernel(const Decod
     const uint32_t pb0 = movmatrix_trans(pack_half2(p0, p1));  // keys 2t, 2t+1 of head g
     const uint32_t pb1 = movmatrix_trans(pack_half2(p2, p3));  // keys 2t+8, 2t+9
 
-    // V scales of keys 2t, 2t+1, 2t+8, 2t+9 (zero for keys past the end)
-    uint4 sva = lds128(st.vs + (2 * t) * 8);
-    uint4 svb = lds128(st.vs + (2 * t + 1) * 8);
-    uint4 svc = lds128(st.vs + (2 * t + 8) * 8);
-    uint4 svd = lds128(st.vs + (2 * t + 9) * 8);
+    // V scales of keys 2t, 2t+1, 2t+8, 2t+9 (zero past the end)
+    uint4 sva = lds128a(sbase + 4352 + (2 * t) * 16);
+    uint4 svb = lds128a(sbase + 4352 + (2 * t + 1) * 16);
+    uint4 svc = lds128a(sbase + 4352 + (2 * t + 8) * 16);
+    uint4 svd = lds128a(sbase + 4352 + (2 * t + 9) * 16);
     if (2 * t >= nvalid) sva = make_uint4(0, 0, 0, 0);
     if (2 * t + 1 >= nvalid) svb = make_uint4(0, 0, 0, 0);
     if (2 * t + 8 >= nvalid) svc = make_uint4(0, 0, 0, 0);
     if (2 * t + 9 >= nvalid) svd = make_uint4(0, 0, 0, 0);
 
-    // V codes: rows 2t, 2t+1, 2t+8, 2t+9, half-words h = g of every group
-    const uint4 v0 = lds128(st.vc + (2 * t) * 128 + 16 * g);
-    const uint4 v1 = lds128(st.vc + (2 * t + 1) * 128 + 16 * g);
-    const uint4 v2 = lds128(st.vc + (2 * t + 8) * 128 + 16 * g);
-    const uint4 v3 = lds128(st.vc + (2 * t + 9) * 128 + 16 * g);
+    // V codes: rows 2t, 2t+1, 2t+8, 2t+9, half-word h = g of every group
+    const uint4 v0 = lds128a(sbase + off_v0);
+    const uint4 v1 = lds128a(sbase + off_v1);
+    const uint4 v2 = lds128a(sbase + off_v2);
+    const uint4 v3 = lds128a(sbase + off_v3);
 #pragma unroll
     for (int G = 0; G < kQ4NG; ++G) {
       const int w = G >> 1;
@@ -296,7 +321,7 @@ __global__ void __launch_bounds__(kQ4Warps * 32, 2) decode_q4_kernel(const Decod
       const uint32_t shi = prmt(word_of(svc, w), word_of(svd, w), ssel);
       const uint32_t b0 = h2_as_u32(__hmul2(u32_as_h2(pb0), u32_as_h2(slo)));
       const uint32_t b1 = h2_as_u32(__hmul2(u32_as_h2(pb1), u32_as_h2(shi)));
-      const uint32_t s0 = (G & 1) ? 0x6622u : 0x4400u;  // byte X of row a -> byte 0, of row b -> byte 2
+      const uint32_t s0 = (G & 1) ? 0x6622u : 0x4400u;  // byte X of rows a, b -> bytes 0, 2
       const uint32_t s1 = (G & 1) ? 0x7733u : 0x5511u;  // byte X+1
       const uint32_t x01 = prmt(word_of(v0, w), word_of(v1, w), s0);
       const uint32_t x01b = prmt(word_of(v0, w), word_of(v1, w), s1);
@@ -311,24 +336,21 @@ __global__ void __launch_bounds__(kQ4Warps * 32, 2) decode_q4_kernel(const Decod
     if (lane == 0 && i + kQ4Ring < my_tiles) {
       fence_proxy_async();
       const int nk0 = k0 + 16 * (my_first + i + kQ4Ring);
-      if (!q4_issue_tile(a, b, kvh, nk0, min(16, k1 - nk0), &st, &sm.bar[warp][s])) poisoned = true;
+      if (!q4_issue_tile<GATHER>(a, b, kvh, nk0, min(16, k1 - nk0), &st, &sm.bar[warp][s])) poisoned = true;
     }
   }
   if (timed_out && lane == 0) set_status(a.status, KVQ_DEV_TIMEOUT);
   poisoned = __any_sync(0xffffffffu, poisoned || timed_out);
 
-  // ---------------- finish this warp: reduce z across the 8 key-row lanes
+  // ---------------- reduce z across the 8 key-row lanes
 #pragma unroll
   for (int o = 4; o < 32; o <<= 1) {
     z0 += __shfl_xor_sync(0xffffffffu, z0, o);
     z1 += __shfl_xor_sync(0xffffffffu, z1, o);
   }
-  __syncthreads();  // every warp is done with its ring
-  Q4Combine& cb = *reinterpret_cast<Q4Combine*>(smem_raw);
-  __shared__ int poison_any;
-  if (threadIdx.x == 0) poison_any = 0;
-  __syncthreads();
-  if (poisoned && lane == 0) poison_any = 1;
+  if (poisoned && lane == 0) atomicOr(&sm.poison, 1);
+  __syncthreads();  // every warp is done with the ring
+  Q4Combine& cb = *reinterpret_cast<Q4Combine*>(&sm.stage[0][0]);
 #pragma unroll
   for (int G = 0; G < kQ4NG; ++G) {
     const int d = 32 * G + 4 * g;
@@ -344,36 +366,48 @@ __global__ void __launch_bounds__(kQ4Warps * 32, 2) decode_q4_kernel(const Decod
     cb.z[warp][2 * t + 1] = z1;
   }
   __syncthreads();
-  const bool bad = poison_any != 0;
-  for (int idx = threadIdx.x; idx < a.group * kQ4D; idx += blockDim.x) {
-    const int h = idx / kQ4D, d = idx % kQ4D;
+  const bool bad = sm.poison != 0;
+  for (int idx = threadIdx.x; idx < a.group * (kQ4D / 4); idx += blockDim.x) {
+    const int h = idx / (kQ4D / 4), d4 = idx % (kQ4D / 4);
     float M = -INFINITY;
 #pragma unroll
     for (int w = 0; w < kQ4Warps; ++w) M = fmaxf(M, cb.m[w][h]);
-    float o = 0.f, Z = 0.f;
+    float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+    float Z = 0.f;
 #pragma unroll
     for (int w = 0; w < kQ4Warps; ++w) {
       const float wt = (M == -INFINITY) ? 0.f : exp2f(cb.m[w][h] - M);
-      o = fmaf(cb.acc[w][h][d], wt, o);
+      const float4 v = *reinterpret_cast<const float4*>(&cb.acc[w][h][4 * d4]);
+      o.x = fmaf(v.x, wt, o.x);
+      o.y = fmaf(v.y, wt, o.y);
+      o.z = fmaf(v.z, wt, o.z);
+      o.w = fmaf(v.w, wt, o.w);
       Z = fmaf(cb.z[w][h], wt, Z);
     }
     const int64_t pi = ((int64_t)b * a.Hq + kvh * a.group + h) * a.P + p;
-    a.ws_acc[pi * kQ4D + d] = bad ? NAN : o;
-    if (d == 0) {
+    if (bad) o = make_float4(NAN, NAN, NAN, NAN);
+    *reinterpret_cast<float4*>(a.ws_acc + pi * kQ4D + 4 * d4) = o;
+    if (d4 == 0) {
       a.ws_m[pi] = bad ? NAN : M;
       a.ws_z[pi] = bad ? NAN : Z;
     }
   }
 }
 
-size_t q4_decode_smem_bytes() { return sizeof(Q4Smem); }
-
 cudaError_t launch_decode_q4(const DecodeArgs& a, int B, cudaStream_t s) {
-  const size_t smem = sizeof(Q4Smem);
-  cudaError_t e = cudaFuncSetAttribute(decode_q4_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  if (e != cudaSuccess) return e;
+  const size_t smem = sizeof(Q4Smem) + 1024;
   dim3 grid(a.P, a.c.num_kv_heads, B);
-  decode_q4_kernel<<<grid, kQ4Warps * 32, smem, s>>>(a);
+  if (a.sel) {
+    cudaError_t e =
+        cudaFuncSetAttribute(decode_q4_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    decode_q4_kernel<true><<<grid, kQ4Warps * 32, smem, s>>>(a);
+  } else {
+    cudaError_t e =
+        cudaFuncSetAttribute(decode_q4_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    decode_q4_kernel<false><<<grid, kQ4Warps * 32, smem, s>>>(a);
+  }
   return cudaGetLastError();
 }
 

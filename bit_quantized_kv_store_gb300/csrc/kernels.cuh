@@ -1,12 +1,16 @@
 // kernels.cuh -- argument blocks and launchers shared between the C-ABI layer
 // (api.cu) and the kernel translation units.
 #pragma once
+#include <cuda.h>
+
 #include "common.cuh"
 
 namespace kvq {
 
 // Split-T decode over the 4-bit rotated cache (decode_q4.cu).
 struct DecodeArgs {
+  CUtensorMap tm_k;  // K codes plane as [rows][128 B], 16-row boxes, 128-byte swizzle
+  CUtensorMap tm_v;  // V codes plane, same shape
   kvq_cache c;
   const float* q;  // [B, Hq, D], rotated
   int Hq;
@@ -76,6 +80,9 @@ struct PrefillArgs {
   float* out;
   int32_t* status;
 };
+
+// Remember a failed CUDA call for kvq_last_cuda_error(); returns KVQ_ERR_CUDA.
+int32_t record_cuda_failure(cudaError_t e);
 
 cudaError_t launch_store(const kvq_cache& c, const void* k, const void* v, int dtype, int64_t n_tok,
                          const int32_t* slots, int32_t* status, cudaStream_t s);

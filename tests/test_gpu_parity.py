@@ -293,7 +293,7 @@ def test_decode_bad_page_and_length_are_flagged(K):
     out, ws = run_decode(K, g, bad, q, lens, ml, 1 / 16)
     assert K.read_status(ws) & K.DEV_BAD_PAGE
     assert np.isnan(out[0]).all()
-    ref = O.decode(o, to_np_in(q), [lens[1]], bt[1:2], 1 / 16)
+    ref = O.decode(o, to_np_in(q[1:2]), [lens[1]], bt[1:2], 1 / 16)
     assert_close(out[1], ref[0], what="healthy sequence next to a bad one")
     out, ws = run_decode(K, g, bt, q, [600, 5000], ml, 1 / 16)   # length above max_seq_len
     assert K.read_status(ws) & K.DEV_BAD_LENGTH
