@@ -46,6 +46,9 @@ SIGNATURES = {
     "kvq_merge": (_I32, [ctypes.POINTER(CacheDesc), _P, _SZ, _I32, _I32, _P, _I32, _I32, _I32, _P, _P]),
     "kvq_prefill_attn": (_I32, [ctypes.POINTER(CacheDesc), _P, _I32, _I32, _I32, _I32, _P, _I32, _F, _P, _P, _P]),
     "kvq_read_status": (_I32, [_P, _P, _P]),
+    "kvq_noalloc_scratch_bytes": (_SZ, []),
+    "kvq_decode_noalloc": (_I32, [ctypes.POINTER(CacheDesc), _P, _I32, _I32, _P, _P, _I32, _I32, _P, _I32, _F, _I32,
+                                  _P, _P, _P]),
 }
 
 _lib = None
@@ -207,6 +210,20 @@ def prefill_attn(cache: Cache, q, q_start, block_table, sm_scale, out=None, stat
     bt = block_table.reshape(-1)
     _check(lib().kvq_prefill_attn(cache.ref, _ptr(q), _dtype_code(q), n_q, Hq, int(q_start), _ptr(bt), bt.numel(),
                                   float(sm_scale), _ptr(out), _ptr(status), _stream(stream)), "kvq_prefill_attn")
+    return out
+
+
+def decode_noalloc(cache: Cache, q_rot, seq_lens, block_tables, max_seq_len, sm_scale, out, sel=None,
+                   rotate_back=None, status=None, stream=None):
+    """Decode partials + merge without a caller workspace (the library's fixed
+    device scratch array is used instead; see kvq_decode_noalloc in kvq.h)."""
+    B, Hq = q_rot.shape[0], q_rot.shape[1]
+    n_sel = 0 if sel is None else sel.shape[1]
+    if rotate_back is None:
+        rotate_back = cache.fmt == FMT_Q4_HAD32
+    _check(lib().kvq_decode_noalloc(cache.ref, _ptr(q_rot), B, Hq, _ptr(seq_lens), _ptr(block_tables),
+                                    block_tables.shape[1], max_seq_len, _ptr(sel), n_sel, float(sm_scale),
+                                    int(rotate_back), _ptr(out), _ptr(status), _stream(stream)), "kvq_decode_noalloc")
     return out
 
 

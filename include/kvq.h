@@ -193,6 +193,31 @@ int32_t kvq_prefill_attn(const kvq_cache* cache, const void* q, int32_t dtype, i
  * device int32) to *host_code; synchronises `stream`. */
 int32_t kvq_read_status(const void* d_status, int32_t* host_code, void* stream);
 
+/* kvq_decode_noalloc -- kvq_decode_attn followed by kvq_merge, for callers that
+ * cannot allocate device memory when they decode (a host that owns every device
+ * allocation, a memory pool that forbids new ones, a latency-critical path that
+ * cannot afford cudaMalloc).  The pages have no counterpart: this is an
+ * interface convenience of this library, with the same arithmetic as the two
+ * calls it replaces.
+ * Instead of a caller workspace it uses one file-scope device array of
+ * kvq_noalloc_scratch_bytes() bytes (16 MiB), which every GPU that loads the
+ * library holds until the process exits.  Problems whose workspace
+ * (kvq_decode_workspace_size) exceeds it are rejected with
+ * KVQ_ERR_WORKSPACE_TOO_SMALL before anything is enqueued.
+ * The first call on a device looks the array's address up
+ * (cudaGetSymbolAddress, with that device current): make that first call before
+ * any stream capture.  The call allocates and frees nothing.  All calls share the
+ * array and it keeps the last call's contents; the status word is cleared on
+ * `stream` at the start of every call.  Calls whose GPU work overlaps (on
+ * different streams without ordering) race on the array.
+ * Arguments as for kvq_decode_attn and kvq_merge; d_status_out (optional device
+ * int32) receives a copy of the call's status word. */
+size_t kvq_noalloc_scratch_bytes(void);
+int32_t kvq_decode_noalloc(const kvq_cache* cache, const float* q, int32_t num_seqs, int32_t num_q_heads,
+                           const int32_t* d_seq_lens, const int32_t* d_block_tables, int32_t max_pages_per_seq,
+                           int32_t max_seq_len, const int32_t* d_sel, int32_t n_sel, float sm_scale,
+                           int32_t rotate_back, float* out, int32_t* d_status_out, void* stream);
+
 #ifdef __cplusplus
 }
 #endif
