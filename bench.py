@@ -109,6 +109,24 @@ class Clocks:
                 "reasons": reasons, "samples": len(self.samples)}
 
 
+def reduce_max_over_ranks(x, world, device):
+    """Max of a host float over all ranks (replicas time independently; the job
+    time is the slowest replica's)."""
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.item()
+
+
+def aggregate_us_per_unit(max_elapsed_ms, units_per_rank, world):
+    """Whole-job time per unit: the slowest replica's elapsed time divided by the
+    units all replicas processed."""
+    return max_elapsed_ms * 1e3 / (units_per_rank * world)
+
+
 # --------------------------------------------------------------------------- workload
 
 class Workload:
@@ -484,11 +502,7 @@ def main():
         torch.cuda.synchronize()
 
     def max_over_ranks(x):
-        if world == 1:
-            return x
-        t = torch.tensor([x], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        return t.item()
+        return reduce_max_over_ranks(x, world, dev)
 
     n_inputs = 4
     W = Workload(K, synth, torch, args.context, n_inputs, 1234 + 1 + rank, dev)
@@ -497,8 +511,7 @@ def main():
         total_ms, dec_avg_ms, launches, graphs = time_device(W, args.steps, args.warmup, torch)
     barrier()
     total_ms = max_over_ranks(total_ms)
-    layer_tokens = LAYERS * args.steps * world
-    us_per_lt = total_ms * 1e3 / layer_tokens
+    us_per_lt = aggregate_us_per_unit(total_ms, LAYERS * args.steps, world)
     bytes_per_launch = W.T * BYTES_PER_POS_LAYER
     achieved = bytes_per_launch / (dec_avg_ms * 1e-3) / 1e9
     e2e_ms, h2d, d2h = time_e2e(W, max(3, args.steps // 2), 2, torch, graphs)

@@ -271,9 +271,26 @@ int32_t kvq_prefill_attn(const kvq_cache* cache, const void* q, int32_t dtype, i
   if (!q || !out || !d_block_table || max_pages < 1) return KVQ_ERR_INVALID_ARG;
   if (static_cast<int64_t>(q_start) + n_q > static_cast<int64_t>(max_pages) * cache->page_size)
     return KVQ_ERR_INVALID_ARG;
-  PrefillArgs a{*cache, q, dtype, n_q, num_q_heads, num_q_heads / cache->num_kv_heads, q_start, d_block_table,
-                max_pages, sm_scale * kLog2e, out, d_status};
-  cudaError_t e = launch_prefill_q4(a, static_cast<cudaStream_t>(stream));
+  PrefillArgs a{};
+  a.c = *cache;
+  a.q = q;
+  a.dtype = dtype;
+  a.n_q = n_q;
+  a.Hq = num_q_heads;
+  a.group = num_q_heads / cache->num_kv_heads;
+  a.q_start = q_start;
+  a.block_table = d_block_table;
+  a.max_pages = max_pages;
+  a.qscale = sm_scale * kLog2e;
+  a.out = out;
+  a.status = d_status;
+  {
+    const uint64_t rows = static_cast<uint64_t>(cache->num_pages) * cache->num_kv_heads * cache->page_size;
+    if (rows >= (1ull << 31)) return KVQ_ERR_UNSUPPORTED;
+    if (!encode_rows_map(&a.tm_k, cache->k, rows, 128, 16) || !encode_rows_map(&a.tm_v, cache->v, rows, 128, 16))
+      return cuda_fail(cudaErrorInvalidValue);
+  }
+  cudaError_t e = launch_prefill_tc(a, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? KVQ_OK : cuda_fail(e);
 }
 

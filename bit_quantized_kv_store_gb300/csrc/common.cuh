@@ -109,9 +109,7 @@ __device__ __forceinline__ uint4 lds128(const void* p) {
 // ---------------------------------------------------------------- register ops
 
 __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
-  uint32_t r;
-  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(sel));
-  return r;
+  return __byte_perm(a, b, sel);
 }
 
 // (a & b) | c  (lop3 with immLut 0xEA)
@@ -151,10 +149,11 @@ __device__ __forceinline__ void split_f16(float x0, float x1, uint32_t& hi, uint
 
 // ---------------------------------------------------------------- MMA
 
-// D += A(16x16, row) * B(16x8, col); f16 inputs, f32 accumulate.
+// D += A(16x16, row) * B(16x8, col); f16 inputs, f32 accumulate.  (Pure register
+// operations are not `volatile`, so the compiler may interleave independent chains.)
 __device__ __forceinline__ void mma_f16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
                                         uint32_t b0, uint32_t b1) {
-  asm volatile(
+  asm(
       "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
       "{%0,%1,%2,%3};"
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
@@ -163,7 +162,7 @@ __device__ __forceinline__ void mma_f16(float (&d)[4], uint32_t a0, uint32_t a1,
 
 __device__ __forceinline__ void mma_bf16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
                                          uint32_t b0, uint32_t b1) {
-  asm volatile(
+  asm(
       "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
       "{%0,%1,%2,%3};"
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
@@ -173,9 +172,23 @@ __device__ __forceinline__ void mma_bf16(float (&d)[4], uint32_t a0, uint32_t a1
 // Transpose an 8x8 matrix of 16-bit values held one row-pair per thread.
 __device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x) {
   uint32_t r;
-  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(r) : "r"(x));
+  asm("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(r) : "r"(x));
   return r;
 }
+
+// 2^x with the hardware approximation (relative error ~2^-22; results below the
+// smallest normal flush to zero, which only drops probabilities < 2^-126).
+__device__ __forceinline__ float fast_exp2(float x) {
+  float r;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+  return r;
+}
+
+// Two codes in bits [0,4) and [16,20) -> the f16 pair (1024 + c0, 1024 + c1), the
+// 8 left in (the caller removes the bias elsewhere).
+__device__ __forceinline__ uint32_t nib_lo_pair_biased(uint32_t x) { return and_or(x, 0x000F000Fu, 0x64006400u); }
+// Codes in bits [4,8) and [20,24) -> (1024 + 16 c0, 1024 + 16 c1).
+__device__ __forceinline__ uint32_t nib_hi_pair_biased(uint32_t x) { return and_or(x, 0x00F000F0u, 0x64006400u); }
 
 // ---------------------------------------------------------------- warp FWHT
 

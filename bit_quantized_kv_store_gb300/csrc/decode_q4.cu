@@ -14,10 +14,12 @@
 // lands at chunk c ^ (r & 7), so the fragment loads below are free of bank
 // conflicts), plus 256 B of K scales and 256 B of V scales by 1-D bulk copies.
 //  * Scores on the tensor cores: mma.m16n8k16, the 16 keys on M, the <= 8 query
-//    heads of the GQA group on N.  Codes minus 8 are exact in f16; the query is
-//    split into f16 high and low parts (~22 bits; its fragments sit in shared
-//    memory); each 32-value group gets its own partial product multiplied by
-//    the group's fp32 scale, so the dequantised keys enter exactly.
+//    heads of the GQA group on N.  The key codes enter as the exact f16 values
+//    1024 + c / 1024 + 16c (one lop3 per pair); the constant part is removed by
+//    starting each group's accumulator at a per-(head, group) query bias.  The
+//    query is split into f16 high and low parts (~22 bits; its fragments sit in
+//    shared memory); each 32-value group gets its own partial product multiplied
+//    by the group's fp32 scale, so the dequantised keys enter exactly.
 //  * Online softmax in base 2 (the query carries sm_scale * log2 e).
 //  * P.V on the tensor cores with the value dims on M: the probabilities are
 //    transposed in registers (movmatrix) and multiplied by the V group scale in
@@ -48,6 +50,7 @@ static_assert(sizeof(Q4Stage) == 5120, "stage size");
 struct Q4Smem {
   Q4Stage stage[kQ4Warps][kQ4Ring];
   uint4 qf[kQ4NG][2][32];  // query fragments [group][hi, lo][lane]
+  float2 qbias[kQ4NG][4];  // [group][head pair]: the code offset folded into the score MMA
   uint64_t bar[kQ4Warps][kQ4Ring];
   int poison;
 };
@@ -72,11 +75,11 @@ __device__ __forceinline__ void tma_rows_2d(void* dst, const CUtensorMap* map, i
 // still completed so the consumer does not wait on it).
 template <bool GATHER>
 __device__ __forceinline__ bool q4_issue_tile(const DecodeArgs& a, int b, int kvh, int key0, int nvalid,
-                                              Q4Stage* st, uint64_t* bar) {
+                                              int32_t page, Q4Stage* st, uint64_t* bar) {
   const kvq_cache& c = a.c;
   const int32_t* bt = a.block_tables + (int64_t)b * a.max_pages;
   if constexpr (!GATHER) {
-    const int32_t page = bt[key0 / c.page_size];
+    // `page` is the block-table entry of key0, fetched ahead by the caller
     if (page < 0 || page >= c.num_pages) {
       set_status(a.status, KVQ_DEV_BAD_PAGE);
       mbar_arrive(bar);
@@ -125,6 +128,12 @@ __device__ __forceinline__ uint4 lds128a(uint32_t addr) {
   return v;
 }
 
+__device__ __forceinline__ uint2 lds64a(uint32_t addr) {
+  uint2 v;
+  asm volatile("ld.shared.v2.u32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr));
+  return v;
+}
+
 __device__ __forceinline__ uint32_t word_of(const uint4& v, int i) {
   return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w;
 }
@@ -161,39 +170,76 @@ __global__ void __launch_bounds__(kQ4Warps * 32, 3) decode_q4_kernel(const __gri
   const int my_first = warp * kQ4TilesPerWarp;
   const int my_tiles = max(0, min(kQ4TilesPerWarp, ntiles - my_first));
 
+  // Page id of each of this warp's tiles, one per lane, fetched once (the
+  // producer lane then never waits on a global load inside the tile loop).
+  int32_t my_page = -1;
+  if (!GATHER && lane < my_tiles)
+    my_page = a.block_tables[(int64_t)b * a.max_pages + (k0 + 16 * (my_first + lane)) / a.c.page_size];
+  int32_t first_pages[kQ4Ring];
+#pragma unroll
+  for (int i = 0; i < kQ4Ring; ++i) first_pages[i] = __shfl_sync(0xffffffffu, my_page, i);
+
   bool poisoned = false;
   if (lane == 0) {
     for (int s = 0; s < kQ4Ring; ++s) mbar_init(&sm.bar[warp][s], 1);
     fence_barrier_init();
     for (int i = 0; i < min(kQ4Ring, my_tiles); ++i) {
       const int key0 = k0 + 16 * (my_first + i);
-      if (!q4_issue_tile<GATHER>(a, b, kvh, key0, min(16, k1 - key0), &sm.stage[warp][i], &sm.bar[warp][i]))
+      if (!q4_issue_tile<GATHER>(a, b, kvh, key0, min(16, k1 - key0), first_pages[i], &sm.stage[warp][i],
+                                 &sm.bar[warp][i]))
         poisoned = true;
     }
   }
   if (threadIdx.x == 0) sm.poison = 0;
 
-  // ---- query fragments (B operand of the score MMA), written once by warp 0
-  if (warp == 0) {
+  // ---- query fragments (B operand of the score MMA), written once by warp 0.
+  // The K codes enter the MMA as 1024 + c (even elements, low nibbles) and
+  // 1024 + 16c (odd elements, high nibbles), one lop3 each; the query values
+  // facing high nibbles are pre-divided by 16 (exact), and the accumulator of
+  // group G starts at -bias_G, bias_G = 1024 * sum(B) + 8 * sum(q~) over the
+  // group (B the f16 values in the fragments, q~ = B or 16 B), so the MMA
+  // returns sum_d q_d (c_d - 8) with the keys' codes used exactly.
+  {
     const bool live = g < a.group;
     const float* qrow = a.q + ((int64_t)b * a.Hq + kvh * a.group + (live ? g : 0)) * kQ4D;
     const float s = live ? a.qscale : 0.f;
+    const float s16 = s * 0.0625f;
 #pragma unroll
-    for (int G = 0; G < kQ4NG; ++G) {
+    for (int Gi = 0; Gi < kQ4NG / kQ4Warps; ++Gi) {  // warp w prepares groups 2w, 2w+1
+      const int G = warp * (kQ4NG / kQ4Warps) + Gi;
       const float4 u0 = *reinterpret_cast<const float4*>(qrow + 32 * G + 8 * t);
       const float4 u1 = *reinterpret_cast<const float4*>(qrow + 32 * G + 8 * t + 4);
       uint4 hi, lo;
       // tile (G,0): slots (2t,2t+1) <- d (8t, 8t+2); slots (2t+8, 2t+9) <- d (8t+1, 8t+3); tile (G,1): d + 4
       split_f16(u0.x * s, u0.z * s, hi.x, lo.x);
-      split_f16(u0.y * s, u0.w * s, hi.y, lo.y);
+      split_f16(u0.y * s16, u0.w * s16, hi.y, lo.y);
       split_f16(u1.x * s, u1.z * s, hi.z, lo.z);
-      split_f16(u1.y * s, u1.w * s, hi.w, lo.w);
+      split_f16(u1.y * s16, u1.w * s16, hi.w, lo.w);
       sm.qf[G][0][lane] = hi;
       sm.qf[G][1][lane] = lo;
+      float ev = 0.f, od = 0.f;  // sums of the even-slot and odd-slot B values (hi parts, then lo parts)
+      const uint32_t hv[4] = {hi.x, hi.y, hi.z, hi.w}, lv[4] = {lo.x, lo.y, lo.z, lo.w};
+#pragma unroll
+      for (int r = 0; r < 4; ++r) {
+        const float2 h2 = __half22float2(u32_as_h2(hv[r]));
+        if (r & 1) od += h2.x + h2.y; else ev += h2.x + h2.y;
+      }
+#pragma unroll
+      for (int r = 0; r < 4; ++r) {
+        const float2 l2 = __half22float2(u32_as_h2(lv[r]));
+        if (r & 1) od += l2.x + l2.y; else ev += l2.x + l2.y;
+      }
+      // bias = 1024 (ev + od) + 8 (ev + 16 od), summed over the 4 lanes of the head
+      float bias = 1032.f * ev + 1152.f * od;
+      bias += __shfl_xor_sync(0xffffffffu, bias, 1);
+      bias += __shfl_xor_sync(0xffffffffu, bias, 2);
+      // head g's bias -> qbias[G][g/2].x or .y
+      if (t == 0) reinterpret_cast<float*>(&sm.qbias[G][0])[g] = -bias;
     }
   }
   __syncthreads();
   const uint32_t qf_addr = smem_u32(&sm.qf[0][0][lane]);
+  const uint32_t qb_addr = smem_u32(&sm.qbias[0][t]);
 
   float acc[kQ4NG][2][4];
 #pragma unroll
@@ -222,7 +268,9 @@ __global__ void __launch_bounds__(kQ4Warps * 32, 3) decode_q4_kernel(const __gri
   for (int i = 0; i < my_tiles; ++i) {
     const int s = i % kQ4Ring;
     Q4Stage& st = sm.stage[warp][s];
-    if (!mbar_wait_bounded(&sm.bar[warp][s], (i / kQ4Ring) & 1)) {
+    // mma.sync / movmatrix below are warp-collective: the wait's outcome is made
+    // warp-uniform so that the warp stays converged (also when a wait gives up).
+    if (!__all_sync(0xffffffffu, mbar_wait_bounded(&sm.bar[warp][s], (i / kQ4Ring) & 1))) {
       timed_out = true;
       break;
     }
@@ -242,14 +290,17 @@ __global__ void __launch_bounds__(kQ4Warps * 32, 3) decode_q4_kernel(const __gri
     for (int G = 0; G < kQ4NG; ++G) {
       const uint4 qh = lds128a(qf_addr + G * 1024);
       const uint4 ql = lds128a(qf_addr + G * 1024 + 512);
+      const uint2 nb = lds64a(qb_addr + G * 32);  // -bias of heads 2t, 2t+1
       const uint32_t sel = (G & 1) ? 0x4342u : 0x4140u;
       const uint32_t xa1 = prmt(word_of(ka0, G >> 1), 0u, sel);
       const uint32_t xa2 = prmt(word_of(ka1, G >> 1), 0u, sel);
       const uint32_t xb1 = prmt(word_of(kb0, G >> 1), 0u, sel);
       const uint32_t xb2 = prmt(word_of(kb1, G >> 1), 0u, sel);
-      const uint32_t a10 = nib_lo_pair(xa1), a11 = nib_lo_pair(xb1), a12 = nib_hi_pair(xa1), a13 = nib_hi_pair(xb1);
-      const uint32_t a20 = nib_lo_pair(xa2), a21 = nib_lo_pair(xb2), a22 = nib_hi_pair(xa2), a23 = nib_hi_pair(xb2);
-      float part[4] = {0.f, 0.f, 0.f, 0.f};
+      const uint32_t a10 = nib_lo_pair_biased(xa1), a11 = nib_lo_pair_biased(xb1);
+      const uint32_t a12 = nib_hi_pair_biased(xa1), a13 = nib_hi_pair_biased(xb1);
+      const uint32_t a20 = nib_lo_pair_biased(xa2), a21 = nib_lo_pair_biased(xb2);
+      const uint32_t a22 = nib_hi_pair_biased(xa2), a23 = nib_hi_pair_biased(xb2);
+      float part[4] = {__uint_as_float(nb.x), __uint_as_float(nb.y), __uint_as_float(nb.x), __uint_as_float(nb.y)};
       mma_f16(part, a10, a11, a12, a13, qh.x, qh.y);
       mma_f16(part, a20, a21, a22, a23, qh.z, qh.w);
       mma_f16(part, a10, a11, a12, a13, ql.x, ql.y);
@@ -260,11 +311,12 @@ __global__ void __launch_bounds__(kQ4Warps * 32, 3) decode_q4_kernel(const __gri
       S[2] = fmaf(sb, part[2], S[2]);
       S[3] = fmaf(sb, part[3], S[3]);
     }
-    const bool va = g < nvalid, vb = g + 8 < nvalid;
-    if (!va || !head0_live) S[0] = -INFINITY;
-    if (!va || !head1_live) S[1] = -INFINITY;
-    if (!vb || !head0_live) S[2] = -INFINITY;
-    if (!vb || !head1_live) S[3] = -INFINITY;
+    if (!head0_live) S[0] = S[2] = -INFINITY;
+    if (!head1_live) S[1] = S[3] = -INFINITY;
+    if (nvalid < 16) {  // tail tile: mask keys past the end
+      if (g >= nvalid) S[0] = S[1] = -INFINITY;
+      if (g + 8 >= nvalid) S[2] = S[3] = -INFINITY;
+    }
 
     // ---------------- online softmax (base 2)
     float t0 = fmaxf(S[0], S[2]), t1 = fmaxf(S[1], S[3]);
@@ -275,14 +327,14 @@ __global__ void __launch_bounds__(kQ4Warps * 32, 3) decode_q4_kernel(const __gri
     }
     const float n0 = fmaxf(m0, t0), n1 = fmaxf(m1, t1);
     const float u0 = (n0 == -INFINITY) ? 0.f : n0, u1 = (n1 == -INFINITY) ? 0.f : n1;
-    const float c0 = exp2f(m0 - u0), c1 = exp2f(m1 - u1);
-    const float p0 = exp2f(S[0] - u0), p1 = exp2f(S[1] - u1);
-    const float p2 = exp2f(S[2] - u0), p3 = exp2f(S[3] - u1);
+    const float c0 = fast_exp2(m0 - u0), c1 = fast_exp2(m1 - u1);
+    const float p0 = fast_exp2(S[0] - u0), p1 = fast_exp2(S[1] - u1);
+    const float p2 = fast_exp2(S[2] - u0), p3 = fast_exp2(S[3] - u1);
     z0 = fmaf(z0, c0, p0 + p2);
     z1 = fmaf(z1, c1, p1 + p3);
     m0 = n0;
     m1 = n1;
-    if (__any_sync(0xffffffffu, c0 != 1.f || c1 != 1.f)) {
+    if (i > 0 && __any_sync(0xffffffffu, c0 != 1.f || c1 != 1.f)) {  // acc is still zero on the first tile
 #pragma unroll
       for (int G = 0; G < kQ4NG; ++G)
 #pragma unroll
@@ -303,10 +355,12 @@ __global__ void __launch_bounds__(kQ4Warps * 32, 3) decode_q4_kernel(const __gri
     uint4 svb = lds128a(sbase + 4352 + (2 * t + 1) * 16);
     uint4 svc = lds128a(sbase + 4352 + (2 * t + 8) * 16);
     uint4 svd = lds128a(sbase + 4352 + (2 * t + 9) * 16);
-    if (2 * t >= nvalid) sva = make_uint4(0, 0, 0, 0);
-    if (2 * t + 1 >= nvalid) svb = make_uint4(0, 0, 0, 0);
-    if (2 * t + 8 >= nvalid) svc = make_uint4(0, 0, 0, 0);
-    if (2 * t + 9 >= nvalid) svd = make_uint4(0, 0, 0, 0);
+    if (nvalid < 16) {  // tail tile: stale rows past the end must not reach P.V
+      if (2 * t >= nvalid) sva = make_uint4(0, 0, 0, 0);
+      if (2 * t + 1 >= nvalid) svb = make_uint4(0, 0, 0, 0);
+      if (2 * t + 8 >= nvalid) svc = make_uint4(0, 0, 0, 0);
+      if (2 * t + 9 >= nvalid) svd = make_uint4(0, 0, 0, 0);
+    }
 
     // V codes: rows 2t, 2t+1, 2t+8, 2t+9, half-word h = g of every group
     const uint4 v0 = lds128a(sbase + off_v0);
@@ -332,11 +386,13 @@ __global__ void __launch_bounds__(kQ4Warps * 32, 3) decode_q4_kernel(const __gri
       mma_f16(acc[G][1], nib_hi_pair(x01), nib_hi_pair(x01b), nib_hi_pair(x23), nib_hi_pair(x23b), b0, b1);
     }
 
+    const int32_t next_page = __shfl_sync(0xffffffffu, my_page, min(i + kQ4Ring, 31));
     __syncwarp();
     if (lane == 0 && i + kQ4Ring < my_tiles) {
       fence_proxy_async();
       const int nk0 = k0 + 16 * (my_first + i + kQ4Ring);
-      if (!q4_issue_tile<GATHER>(a, b, kvh, nk0, min(16, k1 - nk0), &st, &sm.bar[warp][s])) poisoned = true;
+      if (!q4_issue_tile<GATHER>(a, b, kvh, nk0, min(16, k1 - nk0), next_page, &st, &sm.bar[warp][s]))
+        poisoned = true;
     }
   }
   if (timed_out && lane == 0) set_status(a.status, KVQ_DEV_TIMEOUT);

@@ -65,8 +65,10 @@ struct MergeArgs {
   float* out;
 };
 
-// Causal prefill over decoded 4-bit slots (prefill_q4.cu).
+// Causal prefill over decoded 4-bit slots (prefill_tc.cu).
 struct PrefillArgs {
+  CUtensorMap tm_k;  // K codes plane as [rows][128 B], 16-row boxes, 128-byte swizzle
+  CUtensorMap tm_v;  // V codes plane, same shape
   kvq_cache c;
   const void* q;
   int dtype;
@@ -90,6 +92,6 @@ cudaError_t launch_rotate(const void* x, int dtype, float* y, int64_t rows, int 
 cudaError_t launch_decode_q4(const DecodeArgs& a, int B, cudaStream_t s);
 cudaError_t launch_decode_rows(const RowsArgs& a, int B, cudaStream_t s);
 cudaError_t launch_merge(const MergeArgs& a, int B, cudaStream_t s);
-cudaError_t launch_prefill_q4(const PrefillArgs& a, cudaStream_t s);
+cudaError_t launch_prefill_tc(const PrefillArgs& a, cudaStream_t s);
 
 }  // namespace kvq

@@ -359,3 +359,39 @@ def test_prefill(K, depth, n_q):
     got = out.cpu().numpy()
     for i in range(n_q):
         assert_close(got[i], ref[i], what=f"prefill row {i}")
+
+
+@pytest.mark.parametrize("Hk,Hq,depth,n_q", [(2, 16, 70, 33), (3, 3, 200, 129), (1, 5, 0, 64)])
+def test_prefill_gqa_groups(K, Hk, Hq, depth, n_q):
+    D, ps = 256, 16
+    T = depth + n_q
+    n_pages = (T + ps - 1) // ps + 2
+    g, o = make_cache_pair(K, K.FMT_Q4_HAD32, Hk, D, ps, n_pages)
+    bt = synth.page_permutation(n_pages, "pfg", Hk, Hq).numpy().astype(np.int32)
+    k = synth.heavy_tailed((T, Hk, D), "cpu", "pfgk", Hk, Hq)
+    v = synth.heavy_tailed((T, Hk, D), "cpu", "pfgv", Hk, Hq)
+    fill_sequence(K, g, o, k, v, bt, T)
+    q = synth.outlier_normal((n_q, Hq, D), 4, 20.0, "cpu", "pfgq", Hk, Hq)   # fp32 queries
+    out = K.prefill_attn(g, q.to(DEV), depth, torch.from_numpy(bt).to(DEV), 0.05)
+    torch.cuda.synchronize()
+    ref = O.prefill(o, q.numpy(), depth, bt, 0.05)
+    got = out.cpu().numpy()
+    for i in range(n_q):
+        assert_close(got[i], ref[i], what=f"prefill Hk={Hk} Hq={Hq} row {i}")
+
+
+def test_prefill_bad_page_is_flagged(K):
+    Hk, Hq, D, ps, depth, n_q = 1, 6, 256, 16, 40, 10
+    T = depth + n_q
+    g, o = make_cache_pair(K, K.FMT_Q4_HAD32, Hk, D, ps, 4)
+    bt = np.array([0, 1, 2, 3], np.int32)
+    k = synth.normal((T, Hk, D), "cpu", "pbk")
+    fill_sequence(K, g, o, k, k, bt, T)
+    bad = bt.copy()
+    bad[1] = 99
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    q = synth.normal((n_q, Hq, D), "cpu", "pbq")
+    out = K.prefill_attn(g, q.to(DEV), depth, torch.from_numpy(bad).to(DEV), 0.1, status=st)
+    torch.cuda.synchronize()
+    assert K.read_status(st) & K.DEV_BAD_PAGE
+    assert np.isnan(out.cpu().numpy()).all()
