@@ -49,6 +49,8 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-rows", action="store_true", help="skip the other hot-path rows (batched decode, prefill, "
                     "fp8, bf16 cache, store)")
+    ap.add_argument("--only", choices=["batched", "prefill", "fp8", "bf16"], default=None,
+                    help="run only one of the other hot-path rows and print its measurement (for profiling)")
     ap.add_argument("--layers", type=int, default=16, help="layers per step (16 for the benchmark; fewer "
                     "only to profile a small case)")
     args = ap.parse_args()
@@ -328,13 +330,27 @@ def _events_time(torch, fn, iters, warmup=3):
     return a.elapsed_time(b) / iters
 
 
-def measure_rows(K, synth, torch, dev, peak, tflops_peak):
+def measure_rows(K, synth, torch, dev, peak, tflops_peak, only=None):
     """Batched ragged paged decode, prefill chunk, fp8 latent decode (dense and
     gathered), the bf16-cache comparison and the store, each timed with CUDA
-    events (inputs resident in HBM)."""
+    events (inputs resident in HBM).  `only` restricts to one row."""
     out = {}
     seed = 1234 + 3
+    want = lambda name: only is None or only == name
     # ---- batched ragged paged decode: 32 sequences, lengths ~ U{1024..65536}, 16-token pages, shuffled tables
+    if want("batched"):
+        out.update(_row_batched(K, synth, torch, dev, peak, seed))
+    if want("prefill"):
+        out.update(_row_prefill(K, synth, torch, dev, tflops_peak, seed))
+    if want("fp8"):
+        out.update(_row_fp8(K, synth, torch, dev, seed))
+    if want("bf16"):
+        out.update(_row_bf16(K, synth, torch, dev, seed))
+    return out
+
+
+def _row_batched(K, synth, torch, dev, peak, seed):
+    out = {}
     lens = synth.ragged_lengths(32, 1024, 65536, seed, "lens").tolist()
     T = [L + 1 for L in lens]
     pages = [(t + PS - 1) // PS for t in T]
@@ -378,8 +394,13 @@ def measure_rows(K, synth, torch, dev, peak, tflops_peak):
         "cache_bytes": byts, "achieved_GBs": byts / (dec_ms * 1e-3) / 1e9, "frac_of_hbm_peak": byts / (dec_ms * 1e-3) / 1e9 / peak}
     del c, ws
     torch.cuda.empty_cache()
+    return out
 
-    # ---- prefill chunk: 4096 queries at depth 16384, causal over decoded 4-bit slots
+
+def _row_prefill(K, synth, torch, dev, tflops_peak, seed):
+    """Prefill chunk: 4096 queries at depth 16384, causal over decoded 4-bit slots;
+    also the store of the chunk's rows."""
+    out = {}
     depth, nq = 16384, 4096
     Tp = depth + nq
     npg = (Tp + PS - 1) // PS
@@ -404,15 +425,19 @@ def measure_rows(K, synth, torch, dev, peak, tflops_peak):
     out["prefill_chunk"] = {"workload": "4096-token chunk at depth 16384 (store + causal attention over decoded "
                                         "4-bit slots), 4 KV / 24 q heads", "ms": ms, "flop": flops,
                             "TFLOPs": flops / (ms * 1e-3) / 1e12, "frac_of_bf16_peak": flops / (ms * 1e-3) / 1e12 /
-                            tflops_peak, "kernel": "prefill_q4_simple_kernel (CUDA cores)"}
+                            tflops_peak, "kernel": "prefill_tc_kernel (tcgen05, TMEM accumulators)"}
     rows = nq * HK * 2
     out["store"] = {"workload": "4096 tokens x 4 KV heads x (K, V) bf16 rows of 256 -> 4-bit rotated rows",
                     "us": st_ms * 1e3, "rows_per_s": rows / (st_ms * 1e-3),
                     "GBs": rows * (512 + 144) / (st_ms * 1e-3) / 1e9}
     del c, k, v
     torch.cuda.empty_cache()
+    return out
 
-    # ---- fp8 latent rows: dense absorbed decode over 262144 rows, 128 heads, and a 2048-row gather
+
+def _row_fp8(K, synth, torch, dev, seed):
+    """fp8 latent rows: dense absorbed decode over 262144 rows, 128 heads, and a 2048-row gather."""
+    out = {}
     Tf, Hf, DL, R = 262144, 128, 512, 64
     npg = Tf // PS
     c = K.Cache(K.FMT_FP8_ROW, 1, DL, PS, npg, device=dev, rope_dim=R)
@@ -447,8 +472,12 @@ def measure_rows(K, synth, torch, dev, peak, tflops_peak):
                          "kernel": "decode_rows_kernel (CUDA cores)"}
     del c, wsf, wsg
     torch.cuda.empty_cache()
+    return out
 
-    # ---- bf16-cache comparison at 32K (same kernel structure, unrotated bf16 rows)
+
+def _row_bf16(K, synth, torch, dev, seed):
+    """bf16-cache comparison at 32K (same kernel structure, unrotated bf16 rows)."""
+    out = {}
     Tb = 32769
     npg = (Tb + PS - 1) // PS
     c = K.Cache(K.FMT_BF16, HK, D, PS, npg, device=dev)
@@ -503,6 +532,17 @@ def main():
 
     def max_over_ranks(x):
         return reduce_max_over_ranks(x, world, dev)
+
+    if args.only:
+        tf_peak = 1922.8
+        try:
+            with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+                tf_peak = json.load(f).get("bf16_tflops", tf_peak)
+        except OSError:
+            pass
+        if rank == 0:
+            print(json.dumps(measure_rows(K, synth, torch, dev, peak, tf_peak, only=args.only)))
+        return
 
     n_inputs = 4
     W = Workload(K, synth, torch, args.context, n_inputs, 1234 + 1 + rank, dev)
