@@ -10,23 +10,39 @@
 // One CTA per (block of 128/g query positions x the g query heads of a GQA group,
 // KV head): M = 128 rows (row = iq * g + h), so every decoded key/value tile
 // serves the whole group.  Keys are processed in tiles of 64.  Warp roles:
-//  * warp 0       producer: the raw 4-bit pages into a 2-stage ring -- codes by
-//                 2-D TMA boxes of 16 rows with the 128-byte swizzle (so the
-//                 decoders' shared-memory reads spread over the banks), scales
-//                 by 1-D bulk copies;
+//  * warps 0, 2   producers of the raw 4-bit K pages (warp 0) and V pages (warp
+//                 2), each into its own 2-stage ring so that neither side waits
+//                 for the other -- codes by 2-D TMA boxes of 16 rows with the
+//                 128-byte swizzle, scales by 1-D bulk copies;
 //  * warp 1       MMA issuer (one thread) and tensor-memory owner;
 //  * warps 4..7   softmax: one tensor-memory lane (= one row) per thread; they
 //                 also rotate and split the queries at the start and normalise,
 //                 rotate back and store the output at the end;
-//  * warps 8..11  decode the tile: K exactly as the sum of two f16 terms
-//                 K_a = f16((c-8)s), K_b = (c-8)s - K_a (exact), V as
-//                 f16((c-8)s) stored transposed (keys contiguous per value dim).
+//  * warps 8, 9, 12, 13   decode K exactly as the sum of two f16 terms
+//                 K_a = f16((c-8)s), K_b = (c-8)s - K_a (exact), written by
+//                 stmatrix, in two halves of 128 dims so that the next tile's
+//                 first half is decoded while the tensor cores still read the
+//                 second half;
+//  * warps 10, 11, 14, 15 decode V: f16((c-8)s), written transposed (keys
+//                 contiguous per value dim) by stmatrix.trans.
+// Warp w runs on SM sub-partition w % 4, so each sub-partition holds a softmax
+// warp and decoders of one kind only; the decoders' and the softmax's loops are
+// kept rolled (16-column / 8-key steps) so that the four roles' code sharing a
+// sub-partition stays small -- with every loop unrolled, instruction fetch
+// starved all roles.
+// Each decoder lane reads one 16- or 8-byte chunk of a key row and produces the
+// (row = key, two adjacent dims) fragment of 8x8 matrices; the stores fill whole
+// 128-byte core matrices, so neither side has shared-memory bank conflicts.
 // Scores S = q_hi.K_a + q_hi.K_b + q_lo.K_a (q split into f16 high and low
 // parts, ~22 bits; q_hi is the A operand from tensor memory, q_lo from shared
-// memory) accumulate in tensor memory; P (f16) is written back to tensor memory
-// and P.V accumulates into O (128 x 256 f32, tensor memory).  The softmax
-// rescales O lazily, only when the running maximum grows by more than 8 (base 2),
-// so P stays <= 256.
+// memory) accumulate in one of two tensor-memory S buffers, so the scores of
+// tile j+1 are computed while the softmax works on tile j (the softmax reads S
+// twice from tensor memory, for the maximum and for the exponentials, 16
+// columns at a time).  P (f16) goes to
+// shared memory and P.V accumulates into O (128 x 256 f32, tensor memory); the
+// MMA issuer runs P.V of tile j after the scores of tile j+1.  The softmax
+// rescales O lazily, only when the running maximum grows by more than 8 (base
+// 2), so P stays <= 256.
 #include "kernels.cuh"
 #include "tc05.cuh"
 
@@ -34,39 +50,42 @@ namespace kvq {
 
 constexpr int kPfKeys = 64;
 constexpr int kPfStages = 2;
-constexpr int kPfThreads = 384;
+constexpr int kPfThreads = 512;
 constexpr int kPfDim = 256;
 
 // tensor-memory columns (512 allocated)
-constexpr uint32_t kTmQhi = 0;    // 128 columns: q high part, f16 pairs (row = lane)
-constexpr uint32_t kTmS = 128;    // 64 columns: scores, f32
-constexpr uint32_t kTmP = 192;    // 32 columns: probabilities, f16 pairs
-constexpr uint32_t kTmO = 256;    // 256 columns: output accumulator, f32
+constexpr uint32_t kTmQhi = 0;  // 128 columns: q high part, f16 pairs (row = lane)
+constexpr uint32_t kTmS = 128;  // 2 x 64 columns: scores of even / odd tiles, f32
+constexpr uint32_t kTmO = 256;  // 256 columns: output accumulator, f32
 
-struct __align__(1024) PfRaw {  // one 64-key tile of raw cache rows (4 pages of 16 slots)
-  uint8_t kc[64 * 128];          // K codes, 128-byte swizzled per 16-row page (chunk c of row r at c ^ (r & 7))
-  uint8_t vc[64 * 128];          // V codes, same
-  uint16_t ks[64 * 8];
-  uint16_t vs[64 * 8];
+struct __align__(1024) PfRaw {  // one 64-key tile of raw K or V cache rows (4 pages of 16 slots)
+  uint8_t codes[64 * 128];       // 128-byte swizzled per 16-row page (chunk c of row r at c ^ (r & 7))
+  uint16_t scales[64 * 8];
 };
-static_assert(sizeof(PfRaw) == 18432, "raw stage size");
+static_assert(sizeof(PfRaw) == 9216, "raw stage size");
 
 struct PfSmem {
-  PfRaw raw[kPfStages];
+  PfRaw rawk[kPfStages];
+  PfRaw rawv[kPfStages];
   // UMMA K-major layouts, 8-row x 16-byte core matrices:
   //   qlo, ka, kb: element (row, d) at (row/8)*4096 + (d/8)*128 + (row%8)*16 + (d%8)*2
   //   vt:          element (d, key) at (d/8)*1024 + (key/8)*128 + (d%8)*16 + (key%8)*2
+  //   p:           element (row, key) at (row/8)*1024 + (key/8)*128 + (row%8)*16 + (key%8)*2
   uint8_t qlo[128 * kPfDim * 2];
   uint8_t ka[kPfKeys * kPfDim * 2];
   uint8_t kb[kPfKeys * kPfDim * 2];
   uint8_t vt[kPfDim * kPfKeys * 2];
-  uint64_t raw_full[kPfStages];
-  uint64_t raw_empty[kPfStages];
-  uint64_t k_ready, v_ready, s_full, p_full, pv_done;
+  uint8_t p[128 * kPfKeys * 2];
+  uint64_t rawk_full[kPfStages], rawk_empty[kPfStages];
+  uint64_t rawv_full[kPfStages], rawv_empty[kPfStages];
+  uint64_t k_ready[2], k_free[2];  // per half of the head dims
+  uint64_t s_full[2], s_free[2];   // per S buffer
+  uint64_t v_ready, p_full, pv_done, drained;
   uint32_t tmem_base;
   int abort;
   int poison;
 };
+static_assert(sizeof(PfSmem) + 1024 <= 232448, "prefill shared memory exceeds the 227 KB per-CTA limit");
 
 // Bounded wait shared by the roles: gives up on the CTA-wide abort flag or after
 // ~2 s (then raises the flag and KVQ_DEV_TIMEOUT) so that no role can hang.
@@ -86,16 +105,25 @@ __device__ __forceinline__ bool pf_wait(PfSmem& sm, uint64_t* bar, uint32_t pari
   }
 }
 
+// One arrival per warp: every lane has ordered its own accesses (generic ->
+// async-proxy fence, or tcgen05 fence) before calling; the warp converges and
+// lane 0 arrives, so a barrier counts warps, not threads.
+__device__ __forceinline__ void warp_arrive(uint64_t* bar, int lane) {
+  __syncwarp();
+  if (lane == 0) mbar_arrive(bar);
+}
+
+// Warp-uniform form of pf_wait for roles that issue warp-collective instructions.
+__device__ __forceinline__ bool pf_wait_warp(PfSmem& sm, uint64_t* bar, uint32_t parity, int32_t* status) {
+  return __all_sync(0xffffffffu, pf_wait(sm, bar, parity, status));
+}
+
 __device__ __forceinline__ void tma_rows_2d(void* dst, const CUtensorMap* map, int row, uint64_t* bar) {
   asm volatile(
       "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
           smem_u32(dst)),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(0), "r"(row), "r"(smem_u32(bar))
       : "memory");
-}
-
-__device__ __forceinline__ uint32_t bias_pair(uint32_t x) {  // (1024 + c) pair -> (c - 8) pair, exact
-  return h2_as_u32(__hsub2(u32_as_h2(x), u32_as_h2(0x64086408u)));
 }
 
 // In-register 32-point Walsh-Hadamard butterfly (stages 1, 2, 4, 8, 16), no scaling.
@@ -109,6 +137,41 @@ __device__ __forceinline__ void fwht32_regs(float (&x)[32]) {
         x[i] = u + v;
         x[i + h] = u - v;
       }
+}
+
+// shared-memory loads at a 32-bit shared address
+__device__ __forceinline__ uint4 pf_lds128(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
+  return v;
+}
+
+__device__ __forceinline__ uint2 pf_lds64(uint32_t addr) {
+  uint2 v;
+  asm volatile("ld.shared.v2.u32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr));
+  return v;
+}
+
+__device__ __forceinline__ uint32_t word_at(const uint4& v, int i) {
+  return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w;
+}
+
+// One stored code byte of w (element d in the low nibble, d+1 in the high
+// nibble; `prmt_sel` picks the byte) -> the exact f16 pair (c_d - 8, c_{d+1} - 8).
+// prmt copies the byte to bytes 0 and 2; the lop3 keeps the low nibble in the low
+// half and the high nibble (times 16) in the high half under the f16 exponent of
+// 1024; the hfma2 maps 1024 + c -> c - 8 and 1024 + 16c -> c - 8, exactly.
+__device__ __forceinline__ __half2 code_pair(uint32_t w, uint32_t prmt_sel) {
+  const uint32_t x = and_or(prmt(w, 0u, prmt_sel), 0x00F0000Fu, 0x64006400u);
+  return __hfma2(u32_as_h2(x), u32_as_h2(0x2C003C00u) /* (1, 1/16) */, u32_as_h2(0xD480E408u) /* (-1032, -72) */);
+}
+
+// prmt selector copying byte `b` of the first operand to bytes 0 and 2 (zeros elsewhere).
+__host__ __device__ constexpr uint32_t spread_sel(uint32_t b) { return 0x4040u | b | (b << 8); }
+
+// (s, s) from the f16 scale in half `hi` of word w.
+__device__ __forceinline__ __half2 scale_pair(uint32_t w, int hi) {
+  return u32_as_h2(prmt(w, w, hi ? 0x3232u : 0x1010u));
 }
 
 __global__ void __launch_bounds__(kPfThreads, 1) prefill_tc_kernel(const __grid_constant__ PrefillArgs a) {
@@ -126,14 +189,21 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_tc_kernel(const __grid_
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kPfStages; ++s) {
-      mbar_init(&sm.raw_full[s], 1);
-      mbar_init(&sm.raw_empty[s], 128);
+      mbar_init(&sm.rawk_full[s], 1);
+      mbar_init(&sm.rawk_empty[s], 4);  // one arrival per K-decoder warp
+      mbar_init(&sm.rawv_full[s], 1);
+      mbar_init(&sm.rawv_empty[s], 4);  // one arrival per V-decoder warp
     }
-    mbar_init(&sm.k_ready, 128);
-    mbar_init(&sm.v_ready, 128);
-    mbar_init(&sm.s_full, 1);
-    mbar_init(&sm.p_full, 128);
+    for (int h = 0; h < 2; ++h) {
+      mbar_init(&sm.k_ready[h], 4);
+      mbar_init(&sm.k_free[h], 1);
+      mbar_init(&sm.s_full[h], 1);
+      mbar_init(&sm.s_free[h], 4);
+    }
+    mbar_init(&sm.v_ready, 4);
+    mbar_init(&sm.p_full, 4);
     mbar_init(&sm.pv_done, 1);
+    mbar_init(&sm.drained, 1);
     sm.abort = 0;
     sm.poison = 0;
     fence_barrier_init();
@@ -183,14 +253,20 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_tc_kernel(const __grid_
   __syncthreads();  // queries ready (TMEM and shared memory)
   tc_fence_after();
 
-  if (warp == 0) {
-    // ---------------- producer
+  if (warp == 0 || warp == 2) {
+    // ---------------- producers: K pages (warp 0), V pages (warp 2)
     if (lane == 0) {
+      const bool is_k = warp == 0;
+      const CUtensorMap* map = is_k ? &a.tm_k : &a.tm_v;
+      const uint16_t* scales = static_cast<const uint16_t*>(is_k ? c.k_scale : c.v_scale);
+      PfRaw* ring = is_k ? sm.rawk : sm.rawv;
+      uint64_t* full = is_k ? sm.rawk_full : sm.rawv_full;
+      uint64_t* empty = is_k ? sm.rawk_empty : sm.rawv_empty;
       const int32_t* bt = a.block_table;
       for (int j = 0; j < ntiles; ++j) {
         const int s = j % kPfStages;
-        if (!pf_wait(sm, &sm.raw_empty[s], ((j / kPfStages) & 1) ^ 1, a.status)) break;
-        PfRaw& st = sm.raw[s];
+        if (!pf_wait(sm, &empty[s], ((j / kPfStages) & 1) ^ 1, a.status)) break;
+        PfRaw& st = ring[s];
         int64_t rows[4];
         uint32_t bytes = 0;
         for (int pg = 0; pg < 4; ++pg) {
@@ -204,47 +280,79 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_tc_kernel(const __grid_
             continue;
           }
           rows[pg] = ((int64_t)page * c.num_kv_heads + kvh) * c.page_size + key0 % c.page_size;
-          bytes += 2 * 16 * 128 + 2 * 16 * 16;
+          bytes += 16 * 128 + 16 * 16;
         }
         if (bytes == 0) {
-          mbar_arrive(&sm.raw_full[s]);
+          mbar_arrive(&full[s]);
           continue;
         }
-        mbar_arrive_expect_tx(&sm.raw_full[s], bytes);
+        mbar_arrive_expect_tx(&full[s], bytes);
         for (int pg = 0; pg < 4; ++pg) {
           if (rows[pg] < 0) continue;
-          tma_rows_2d(st.kc + pg * 2048, &a.tm_k, static_cast<int>(rows[pg]), &sm.raw_full[s]);
-          tma_rows_2d(st.vc + pg * 2048, &a.tm_v, static_cast<int>(rows[pg]), &sm.raw_full[s]);
-          bulk_g2s(st.ks + pg * 128, static_cast<const uint16_t*>(c.k_scale) + rows[pg] * 8, 256, &sm.raw_full[s]);
-          bulk_g2s(st.vs + pg * 128, static_cast<const uint16_t*>(c.v_scale) + rows[pg] * 8, 256, &sm.raw_full[s]);
+          tma_rows_2d(st.codes + pg * 2048, map, static_cast<int>(rows[pg]), &full[s]);
+          bulk_g2s(st.scales + pg * 128, scales + rows[pg] * 8, 256, &full[s]);
         }
       }
     }
   } else if (warp == 1) {
-    // ---------------- MMA issuer
+    // ---------------- MMA issuer: QK(j) into S[j % 2], then PV(j - 1)
+    // Descriptors are built once; a k-step of 16 advances every operand by 256
+    // bytes (16 in descriptor units) and the q_hi columns by 8, so the unrolled
+    // runs below issue one instruction per MMA.
     if (lane == 0) {
       constexpr uint32_t id_qk = idesc_f16_f32(128, kPfKeys);
       constexpr uint32_t id_pv = idesc_f16_f32(128, kPfDim);
-      const uint32_t qlo = smem_u32(sm.qlo), ka = smem_u32(sm.ka), kb = smem_u32(sm.kb), vt = smem_u32(sm.vt);
-      for (int j = 0; j < ntiles; ++j) {
-        if (!pf_wait(sm, &sm.k_ready, j & 1, a.status)) break;
-        tc_fence_after();
-        for (int s = 0; s < kPfDim / 16; ++s) {
-          const uint64_t da = umma_desc(ka + s * 256, 128, 4096);
-          const uint64_t db = umma_desc(kb + s * 256, 128, 4096);
-          umma_ts(tbase + kTmS, tbase + kTmQhi + 8 * s, da, id_qk, s > 0 ? 1u : 0u);
-          umma_ts(tbase + kTmS, tbase + kTmQhi + 8 * s, db, id_qk, 1u);
-          umma_ss(tbase + kTmS, umma_desc(qlo + s * 256, 128, 4096), da, id_qk, 1u);
+      const uint64_t dka = umma_desc(smem_u32(sm.ka), 128, 4096), dkb = umma_desc(smem_u32(sm.kb), 128, 4096);
+      const uint64_t dql = umma_desc(smem_u32(sm.qlo), 128, 4096);
+      const uint64_t dp = umma_desc(smem_u32(sm.p), 128, 1024), dvt = umma_desc(smem_u32(sm.vt), 128, 1024);
+      const uint32_t tq = tbase + kTmQhi;
+      bool ok = true;
+      for (int j = 0; j <= ntiles && ok; ++j) {
+        if (j < ntiles) {
+          const int b = j & 1;
+          const uint32_t sacc = tbase + kTmS + 64 * b;
+          // softmax(j - 2) has read S[b]
+          if (j >= 2 && !pf_wait(sm, &sm.s_free[b], ((j >> 1) - 1) & 1, a.status)) break;
+          // first half of the head dims: k-steps 0..7
+          if (!pf_wait(sm, &sm.k_ready[0], j & 1, a.status)) break;
+          tc_fence_after();
+          umma_ts(sacc, tq, dka, id_qk, 0u);
+          umma_ts_acc(sacc, tq, dkb, id_qk);
+          umma_ss_acc(sacc, dql, dka, id_qk);
+#pragma unroll
+          for (int s = 1; s < 8; ++s) {
+            umma_ts_acc(sacc, tq + 8 * s, dka + 16 * s, id_qk);
+            umma_ts_acc(sacc, tq + 8 * s, dkb + 16 * s, id_qk);
+            umma_ss_acc(sacc, dql + 16 * s, dka + 16 * s, id_qk);
+          }
+          umma_commit(&sm.k_free[0]);
+          // second half: k-steps 8..15
+          if (!pf_wait(sm, &sm.k_ready[1], j & 1, a.status)) break;
+          tc_fence_after();
+#pragma unroll
+          for (int s = 8; s < 16; ++s) {
+            umma_ts_acc(sacc, tq + 8 * s, dka + 16 * s, id_qk);
+            umma_ts_acc(sacc, tq + 8 * s, dkb + 16 * s, id_qk);
+            umma_ss_acc(sacc, dql + 16 * s, dka + 16 * s, id_qk);
+          }
+          umma_commit(&sm.k_free[1]);
+          umma_commit(&sm.s_full[b]);
         }
-        umma_commit(&sm.s_full);
-        if (!pf_wait(sm, &sm.p_full, j & 1, a.status)) break;
-        if (!pf_wait(sm, &sm.v_ready, j & 1, a.status)) break;
-        tc_fence_after();
-        for (int s = 0; s < kPfKeys / 16; ++s)
-          umma_ts(tbase + kTmO, tbase + kTmP + 8 * s, umma_desc(vt + s * 256, 128, 1024), id_pv,
-                  (j > 0 || s > 0) ? 1u : 0u);
-        umma_commit(&sm.pv_done);
+        if (j >= 1) {  // P.V of tile j - 1
+          const int jp = j - 1;
+          if (!pf_wait(sm, &sm.p_full, jp & 1, a.status)) break;
+          if (!pf_wait(sm, &sm.v_ready, jp & 1, a.status)) break;
+          tc_fence_after();
+          umma_ss(tbase + kTmO, dp, dvt, id_pv, jp > 0 ? 1u : 0u);
+#pragma unroll
+          for (int s = 1; s < kPfKeys / 16; ++s) umma_ss_acc(tbase + kTmO, dp + 16 * s, dvt + 16 * s, id_pv);
+          umma_commit(&sm.pv_done);
+        }
       }
+      // every MMA issued so far has finished before tensor memory is released
+      // (bounded, and independent of the abort flag)
+      umma_commit(&sm.drained);
+      mbar_wait_bounded(&sm.drained, 0);
     }
   } else if (warp >= 4 && warp < 8) {
     // ---------------- softmax, one row per thread
@@ -252,27 +360,27 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_tc_kernel(const __grid_
     const int iq = r / grp, h = r % grp;
     const bool valid = (r < qpb * grp) && (iq < nq_blk);
     const int qpos = a.q_start + q0 + iq;  // keys 0 .. qpos
+    uint8_t* prow = sm.p + (r >> 3) * 1024 + (r & 7) * 16;
     // tcgen05.ld/st are warp-collective (.sync.aligned): every branch around
     // them is made warp-uniform, including the failure paths.
     float m_run = -INFINITY, z = 0.f;
     bool ok = true;
     for (int j = 0; j < ntiles; ++j) {
-      ok = __all_sync(0xffffffffu, pf_wait(sm, &sm.s_full, j & 1, a.status));
+      const int b = j & 1;
+      ok = pf_wait_warp(sm, &sm.s_full[b], (j >> 1) & 1, a.status);
       if (!ok) break;
       tc_fence_after();
-      uint32_t s0[32], s1[32];
-      tmem_ld32(tbase + lane_off + kTmS, s0);
-      tmem_ld32(tbase + lane_off + kTmS + 32, s1);
-      tmem_wait_ld();
-      float sv[64];
-      const int key0 = j * kPfKeys;
+      const uint32_t sadr = tbase + lane_off + kTmS + 64 * b;
+      const int lim = valid ? qpos - j * kPfKeys : -1;  // keys i <= lim of this tile are visible
+      // pass 1: the row maximum over the visible keys, 16 columns at a time
       float tmax = -INFINITY;
+#pragma unroll 1
+      for (int cc = 0; cc < kPfKeys / 16; ++cc) {
+        uint32_t v[16];
+        tmem_ld16(sadr + 16 * cc, v);
+        tmem_wait_ld();
 #pragma unroll
-      for (int i = 0; i < 64; ++i) {
-        float v = __uint_as_float(i < 32 ? s0[i] : s1[i - 32]);
-        if (!valid || key0 + i > qpos) v = -INFINITY;
-        sv[i] = v;
-        tmax = fmaxf(tmax, v);
+        for (int i = 0; i < 16; ++i) tmax = fmaxf(tmax, (16 * cc + i > lim) ? -INFINITY : __uint_as_float(v[i]));
       }
       // Raise a row's reference maximum only when its scores grew by more than 8
       // (base 2); rows that rescale multiply their accumulated O and z by corr.
@@ -283,36 +391,49 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_tc_kernel(const __grid_
         z *= corr;
         m_run = tmax;
       }
-      if (j > 0 && __any_sync(0xffffffffu, raise && corr != 1.f)) {  // warp-uniform O rescale
-        ok = __all_sync(0xffffffffu, pf_wait(sm, &sm.pv_done, (j - 1) & 1, a.status));
+      const float mu = (m_run == -INFINITY) ? 0.f : m_run;
+      if (j > 0) {  // PV(j-1) must be done: it reads P and accumulates into O
+        ok = pf_wait_warp(sm, &sm.pv_done, (j - 1) & 1, a.status);
         if (!ok) break;
         tc_fence_after();
-        for (int cc = 0; cc < kPfDim / 32; ++cc) {
-          uint32_t o[32];
-          tmem_ld32(tbase + lane_off + kTmO + 32 * cc, o);
-          tmem_wait_ld();
+        if (__any_sync(0xffffffffu, raise && corr != 1.f)) {  // warp-uniform O rescale
+#pragma unroll 1
+          for (int cc = 0; cc < kPfDim / 16; ++cc) {
+            uint32_t o[16];
+            tmem_ld16(tbase + lane_off + kTmO + 16 * cc, o);
+            tmem_wait_ld();
 #pragma unroll
-          for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * corr);
-          tmem_st32(tbase + lane_off + kTmO + 32 * cc, o);
+            for (int i = 0; i < 16; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * corr);
+            tmem_st16(tbase + lane_off + kTmO + 16 * cc, o);
+          }
+          tmem_wait_st();
         }
       }
-      uint32_t pk[32];
+      // pass 2: p = 2^(s - mu) (0 for masked keys), f16 pairs into P, 16 keys at a time
       float zs = 0.f;
+#pragma unroll 1
+      for (int cc = 0; cc < kPfKeys / 16; ++cc) {
+        uint32_t v[16], pk[8];
+        tmem_ld16(sadr + 16 * cc, v);
+        tmem_wait_ld();
 #pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        const float p0 = (sv[2 * i] == -INFINITY) ? 0.f : fast_exp2(sv[2 * i] - m_run);
-        const float p1 = (sv[2 * i + 1] == -INFINITY) ? 0.f : fast_exp2(sv[2 * i + 1] - m_run);
-        zs += p0 + p1;
-        pk[i] = pack_half2(p0, p1);
+        for (int i = 0; i < 8; ++i) {
+          const float p0 = (16 * cc + 2 * i > lim) ? 0.f : fast_exp2(__uint_as_float(v[2 * i]) - mu);
+          const float p1 = (16 * cc + 2 * i + 1 > lim) ? 0.f : fast_exp2(__uint_as_float(v[2 * i + 1]) - mu);
+          zs += p0 + p1;
+          pk[i] = pack_half2(p0, p1);
+        }
+        *reinterpret_cast<uint4*>(prow + (2 * cc) * 128) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+        *reinterpret_cast<uint4*>(prow + (2 * cc + 1) * 128) = make_uint4(pk[4], pk[5], pk[6], pk[7]);
       }
       z += zs;
-      tmem_st32(tbase + lane_off + kTmP, pk);
-      tmem_wait_st();
       tc_fence_before();
-      mbar_arrive(&sm.p_full);
+      warp_arrive(&sm.s_free[b], lane);  // S[b] read
+      fence_proxy_async();
+      warp_arrive(&sm.p_full, lane);
     }
     // ---------------- epilogue: O / z, rotate back, store
-    if (ok) ok = __all_sync(0xffffffffu, pf_wait(sm, &sm.pv_done, (ntiles - 1) & 1, a.status));
+    if (ok) ok = pf_wait_warp(sm, &sm.pv_done, (ntiles - 1) & 1, a.status);
     if (ok) {
       tc_fence_after();
       const bool bad = sm.poison != 0 || sm.abort != 0;
@@ -337,103 +458,102 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_tc_kernel(const __grid_
         }
       }
     }
+  } else if (warp >= 8 && (warp & 2) == 0) {
+    // ---------------- K decoder (warps 8, 9, 12, 13): key blocks 2kw, 2kw+1 of every tile, by halves
+    const int kw = (warp & 1) + 2 * ((warp - 8) >> 2);
+    const int krow = lane >> 2;        // key within the 8-key block
+    const int xb = lane & 1;           // byte of the half-word
+    const int hsel = (lane & 3) >> 1;  // h = 2m + hsel
+    const uint32_t sel_e = spread_sel(xb), sel_o = spread_sel(2 + xb);
+    const uint32_t ka = smem_u32(sm.ka), kbuf = smem_u32(sm.kb);
+    // stmatrix row address: matrix lane / 8 of the four (group 4 half + lane / 8), its row lane % 8
+    const uint32_t st_off = (uint32_t)(lane >> 3) * 4 * 128 + (uint32_t)(lane & 7) * 16;
+    bool ok = true;
+    for (int j = 0; j < ntiles && ok; ++j) {
+      const int s = j % kPfStages;
+      if (!pf_wait_warp(sm, &sm.rawk_full[s], (j / kPfStages) & 1, a.status)) break;
+      const uint32_t st_codes = smem_u32(sm.rawk[s].codes), st_scales = smem_u32(sm.rawk[s].scales);
+      const int jk0 = j * kPfKeys;
+      for (int half = 0; half < 2; ++half) {
+        // QK(j-1) has read this half of K_a, K_b
+        if (j > 0 && !pf_wait_warp(sm, &sm.k_free[half], (j - 1) & 1, a.status)) {
+          ok = false;
+          break;
+        }
+#pragma unroll 1
+        for (int kbl = 0; kbl < 2; ++kbl) {
+          const int kbk = 2 * kw + kbl;
+          const int key = 8 * kbk + krow;
+          // scales of groups 4 half .. 4 half + 3 (zero past kmax: stale codes give zero)
+          uint2 sc = pf_lds64(st_scales + key * 16 + 8 * half);
+          if (jk0 + key >= kmax) sc = make_uint2(0, 0);
+          const __half2 s2[4] = {scale_pair(sc.x, 0), scale_pair(sc.x, 1), scale_pair(sc.y, 0), scale_pair(sc.y, 1)};
+#pragma unroll 1
+          for (int m = 0; m < 4; ++m) {
+            const int h = 2 * m + hsel;
+            // half-words (G = 4 half .. +3, h): bytes 8 half .. +7 of chunk h
+            const uint2 w = pf_lds64(st_codes + key * 128 + ((h ^ (key & 7)) << 4) + 8 * half);
+            uint32_t va[4], vb[4];
+#pragma unroll
+            for (int gl = 0; gl < 4; ++gl) {
+              const __half2 cv = code_pair(gl < 2 ? w.x : w.y, (gl & 1) ? sel_o : sel_e);
+              const __half2 xa = __hmul2(cv, s2[gl]);
+              va[gl] = h2_as_u32(xa);
+              vb[gl] = h2_as_u32(__hfma2(cv, s2[gl], __hneg2(xa)));  // exact remainder
+            }
+            // matrix (G = 4 half + gl, m): key block kbk, d-block 4G + m
+            const uint32_t off = (uint32_t)kbk * 4096 + (uint32_t)(16 * half + m) * 128 + st_off;
+            stmatrix_x4(ka + off, va[0], va[1], va[2], va[3]);
+            stmatrix_x4(kbuf + off, vb[0], vb[1], vb[2], vb[3]);
+          }
+        }
+        fence_proxy_async();
+        warp_arrive(&sm.k_ready[half], lane);
+      }
+      if (ok) warp_arrive(&sm.rawk_empty[s], lane);
+    }
   } else if (warp >= 8) {
-    // ---------------- decode K and V tiles
-    const int t = threadIdx.x - 256;
+    // ---------------- V decoder (warps 10, 11, 14, 15): key blocks 2vw, 2vw+1 of every tile
+    const int vw = (warp & 1) + 2 * ((warp - 10) >> 2);
+    const int krow = lane >> 2;
+    const int xb = lane & 1;
+    const int hsel = (lane & 3) >> 1;
+    const uint32_t sel_e = spread_sel(xb), sel_o = spread_sel(2 + xb);
+    const uint32_t vt = smem_u32(sm.vt);
+    // stmatrix row address: matrix lane / 8 of the four (group G), its row lane % 8
+    const uint32_t st_off = (uint32_t)(lane >> 3) * 4 * 1024 + (uint32_t)(lane & 7) * 16;
     for (int j = 0; j < ntiles; ++j) {
       const int s = j % kPfStages;
-      if (!pf_wait(sm, &sm.raw_full[s], (j / kPfStages) & 1, a.status)) break;
-      const PfRaw& st = sm.raw[s];
-      // K: thread -> key kk = t/2, groups 4*(t%2) .. +3; K_a, K_b rows
-      if (j > 0 && !pf_wait(sm, &sm.s_full, (j - 1) & 1, a.status)) break;  // QK(j-1) done with ka/kb
-      {
-        const int kk = t >> 1, gh = t & 1;
-        const bool kv = j * kPfKeys + kk < kmax;
-        // chunk h of the row holds half-words (h, G = 0..7); this thread needs G = 4gh .. 4gh+3
-        uint2 w[8];
+      if (!pf_wait_warp(sm, &sm.rawv_full[s], (j / kPfStages) & 1, a.status)) break;
+      if (j > 0 && !pf_wait_warp(sm, &sm.pv_done, (j - 1) & 1, a.status)) break;  // PV(j-1) is done with vt
+      const uint32_t st_codes = smem_u32(sm.rawv[s].codes), st_scales = smem_u32(sm.rawv[s].scales);
+      const int jk0 = j * kPfKeys;
+#pragma unroll 1
+      for (int kbl = 0; kbl < 2; ++kbl) {
+        const int kbk = 2 * vw + kbl;
+        const int key = 8 * kbk + krow;
+        uint4 sc = pf_lds128(st_scales + key * 16);
+        if (jk0 + key >= kmax) sc = make_uint4(0, 0, 0, 0);  // zero scale past kmax: stale codes give zero
+        __half2 s2[8];
 #pragma unroll
-        for (int h = 0; h < 8; ++h)
-          w[h] = *reinterpret_cast<const uint2*>(st.kc + kk * 128 + ((h ^ (kk & 7)) << 4) + 8 * gh);
-        const uint2 sc = *reinterpret_cast<const uint2*>(st.ks + kk * 8 + 4 * gh);
-        uint8_t* arow = sm.ka + (kk >> 3) * 4096 + (kk & 7) * 16;
-        uint8_t* brow = sm.kb + (kk >> 3) * 4096 + (kk & 7) * 16;
+        for (int G = 0; G < 8; ++G) s2[G] = scale_pair(word_at(sc, G >> 1), G & 1);
+#pragma unroll 1
+        for (int m = 0; m < 4; ++m) {
+          const int h = 2 * m + hsel;
+          const uint4 w = pf_lds128(st_codes + key * 128 + ((h ^ (key & 7)) << 4));
+          uint32_t v[8];
 #pragma unroll
-        for (int gl = 0; gl < 4; ++gl) {
-          const int G = 4 * gh + gl;
-          const uint32_t sw = (gl >> 1) ? sc.y : sc.x;
-          const uint32_t s16 = (gl & 1) ? (sw >> 16) : (sw & 0xFFFFu);
-          const __half2 s2 = u32_as_h2(s16 | (s16 << 16));
-#pragma unroll
-          for (int hp = 0; hp < 4; ++hp) {  // half-words h = 2hp, 2hp+1 fill one 16-byte chunk
-            uint32_t av[4], bv[4];
-#pragma unroll
-            for (int e = 0; e < 2; ++e) {
-              const int h = 2 * hp + e;
-              const uint32_t wd = (gl >> 1) ? w[h].y : w[h].x;  // half-words (h, G & ~1), (h, G | 1)
-              const uint32_t hw = (wd >> (16 * (gl & 1))) & 0xFFFFu;
-              const uint32_t x = hw | (hw << 12);
-              const __half2 c01 = u32_as_h2(bias_pair(and_or(x, 0x000F000Fu, 0x64006400u)));
-              const __half2 c23 = u32_as_h2(bias_pair(and_or(x >> 8, 0x000F000Fu, 0x64006400u)));
-              const __half2 a01 = __hmul2(c01, s2), a23 = __hmul2(c23, s2);
-              const __half2 b01 = __hfma2(c01, s2, __hneg2(a01)), b23 = __hfma2(c23, s2, __hneg2(a23));
-              av[2 * e] = h2_as_u32(a01);
-              av[2 * e + 1] = h2_as_u32(a23);
-              bv[2 * e] = h2_as_u32(b01);
-              bv[2 * e + 1] = h2_as_u32(b23);
-            }
-            const int chunk = 4 * G + hp;  // d = 32G + 8hp .. +8
-            const uint4 A = kv ? make_uint4(av[0], av[1], av[2], av[3]) : make_uint4(0, 0, 0, 0);
-            const uint4 B = kv ? make_uint4(bv[0], bv[1], bv[2], bv[3]) : make_uint4(0, 0, 0, 0);
-            *reinterpret_cast<uint4*>(arow + chunk * 128) = A;
-            *reinterpret_cast<uint4*>(brow + chunk * 128) = B;
-          }
+          for (int G = 0; G < 8; ++G)
+            v[G] = h2_as_u32(__hmul2(code_pair(word_at(w, G >> 1), (G & 1) ? sel_o : sel_e), s2[G]));
+          // matrix (G, m): d-block 4G + m, key block kbk -> vt + (4G + m) * 1024 + kbk * 128
+          const uint32_t base = vt + (uint32_t)m * 1024 + (uint32_t)kbk * 128 + st_off;
+          stmatrix_x4_trans(base, v[0], v[1], v[2], v[3]);
+          stmatrix_x4_trans(base + 16 * 1024, v[4], v[5], v[6], v[7]);
         }
       }
       fence_proxy_async();
-      mbar_arrive(&sm.k_ready);
-      // V: thread -> keys 8*kb8 .. +7, stored words wi and wi+16; writes V^T chunks
-      if (j > 0 && !pf_wait(sm, &sm.pv_done, (j - 1) & 1, a.status)) break;  // PV(j-1) done with vt
-      {
-        const int kb8 = t >> 4, wi = t & 15;
-        uint32_t vsw[8];  // V scale word (groups G, G+1) of each of the 8 keys, per stored word
-#pragma unroll
-        for (int ww = 0; ww < 2; ++ww) {
-          const int wd = wi + 16 * ww;     // stored word: half-words 2wd, 2wd+1
-          const int h = (2 * wd) >> 3, G = (2 * wd) & 7;  // G even
-          uint32_t vw[8];
-#pragma unroll
-          for (int k = 0; k < 8; ++k) {
-            const int key = 8 * kb8 + k;
-            const bool kv = j * kPfKeys + key < kmax;
-            vw[k] = *reinterpret_cast<const uint32_t*>(st.vc + key * 128 + (((wd >> 2) ^ (key & 7)) << 4) +
-                                                        4 * (wd & 3));
-            vsw[k] = kv ? *reinterpret_cast<const uint32_t*>(st.vs + key * 8 + G) : 0u;  // zero scale past kmax
-          }
-          // word bytes: [hw(G).b0, hw(G).b1, hw(G+1).b0, hw(G+1).b1]; byte X holds elements (lo, hi)
-#pragma unroll
-          for (int X = 0; X < 4; ++X) {
-            const int Gx = G + (X >> 1);
-            const int d_lo = 32 * Gx + 4 * h + 2 * (X & 1);  // element of the low nibble; d_lo+1 the high
-            uint32_t lo4[4], hi4[4];
-#pragma unroll
-            for (int kp = 0; kp < 4; ++kp) {  // key pair (2kp, 2kp+1)
-              const uint32_t x = prmt(vw[2 * kp], vw[2 * kp + 1], (X | (X << 4) | ((X + 4) << 8) | ((X + 4) << 12)));
-              const uint32_t ssel = (X >> 1) ? 0x7632u : 0x5410u;
-              const __half2 s2 = u32_as_h2(prmt(vsw[2 * kp], vsw[2 * kp + 1], ssel));
-              lo4[kp] = h2_as_u32(__hmul2(u32_as_h2(nib_lo_pair(x)), s2));
-              hi4[kp] = h2_as_u32(__hmul2(u32_as_h2(nib_hi_pair(x)), s2));
-            }
-            uint8_t* base = sm.vt + kb8 * 128;
-            *reinterpret_cast<uint4*>(base + (d_lo >> 3) * 1024 + (d_lo & 7) * 16) =
-                make_uint4(lo4[0], lo4[1], lo4[2], lo4[3]);
-            *reinterpret_cast<uint4*>(base + ((d_lo + 1) >> 3) * 1024 + ((d_lo + 1) & 7) * 16) =
-                make_uint4(hi4[0], hi4[1], hi4[2], hi4[3]);
-          }
-        }
-      }
-      fence_proxy_async();
-      mbar_arrive(&sm.v_ready);
-      mbar_arrive(&sm.raw_empty[s]);
+      warp_arrive(&sm.v_ready, lane);
+      warp_arrive(&sm.rawv_empty[s], lane);
     }
   }
 
