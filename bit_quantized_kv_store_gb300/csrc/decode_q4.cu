@@ -8,11 +8,15 @@
 //
 // GB300 design.  One CTA (4 warps) per (partition of 512 keys, KV head,
 // sequence); up to 3 CTAs per SM.  Warp w owns keys [128w, 128w + 128) of the
-// partition: 8 tiles of 16 keys streamed through a private 3-stage shared-memory
+// partition: 8 tiles of 16 keys streamed through a private 2-stage shared-memory
 // ring.  A tile is 2 KB of K codes and 2 KB of V codes, brought by 2-D TMA
 // tensor copies with the hardware 128-byte swizzle (16-byte chunk c of row r
 // lands at chunk c ^ (r & 7), so the fragment loads below are free of bank
 // conflicts), plus 256 B of K scales and 256 B of V scales by 1-D bulk copies.
+// Fragment words are read one group pair at a time, so that few registers stay
+// live besides the 64 output accumulators.  (Measured at 262K keys: the loads
+// alone would run in ~56 us and the arithmetic alone in ~82 us; the kernel is
+// bound by its arithmetic issue, not by the copies.)
 //  * Scores on the tensor cores: mma.m16n8k16, the 16 keys on M, the <= 8 query
 //    heads of the GQA group on N.  The key codes enter as the exact f16 values
 //    1024 + c / 1024 + 16c (one lop3 per pair); the constant part is removed by
@@ -31,8 +35,9 @@
 
 namespace kvq {
 
-constexpr int kQ4Warps = 4;
-constexpr int kQ4Ring = 3;
+constexpr int kQ4Warps = 4;      // warps per CTA; each owns kPart / kQ4Warps keys of the partition
+constexpr int kQ4MinBlocks = 3;  // resident CTAs per SM the register budget is sized for
+constexpr int kQ4Ring = 2;       // tiles in flight per warp
 constexpr int kQ4TilesPerWarp = kPart / 16 / kQ4Warps;  // 8
 constexpr int kQ4D = 256;
 constexpr int kQ4NG = 8;
@@ -128,6 +133,12 @@ __device__ __forceinline__ uint4 lds128a(uint32_t addr) {
   return v;
 }
 
+__device__ __forceinline__ uint32_t lds32a(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr));
+  return v;
+}
+
 __device__ __forceinline__ uint2 lds64a(uint32_t addr) {
   uint2 v;
   asm volatile("ld.shared.v2.u32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr));
@@ -144,7 +155,7 @@ __device__ __forceinline__ float scale_of(const uint4& v, int G) {
 }
 
 template <bool GATHER>
-__global__ void __launch_bounds__(kQ4Warps * 32, 3) decode_q4_kernel(const __grid_constant__ DecodeArgs a) {
+__global__ void __launch_bounds__(kQ4Warps * 32, kQ4MinBlocks) decode_q4_kernel(const __grid_constant__ DecodeArgs a) {
   extern __shared__ uint8_t smem_raw[];
   // 1024-byte alignment for the swizzled tiles (the launch adds 1 KB of slack)
   Q4Smem& sm = *reinterpret_cast<Q4Smem*>(smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u));
@@ -204,9 +215,7 @@ __global__ void __launch_bounds__(kQ4Warps * 32, 3) decode_q4_kernel(const __gri
     const float* qrow = a.q + ((int64_t)b * a.Hq + kvh * a.group + (live ? g : 0)) * kQ4D;
     const float s = live ? a.qscale : 0.f;
     const float s16 = s * 0.0625f;
-#pragma unroll
-    for (int Gi = 0; Gi < kQ4NG / kQ4Warps; ++Gi) {  // warp w prepares groups 2w, 2w+1
-      const int G = warp * (kQ4NG / kQ4Warps) + Gi;
+    for (int G = warp; G < kQ4NG; G += kQ4Warps) {  // warp w prepares groups w, w + kQ4Warps, ...
       const float4 u0 = *reinterpret_cast<const float4*>(qrow + 32 * G + 8 * t);
       const float4 u1 = *reinterpret_cast<const float4*>(qrow + 32 * G + 8 * t + 4);
       uint4 hi, lo;
@@ -279,37 +288,42 @@ __global__ void __launch_bounds__(kQ4Warps * 32, 3) decode_q4_kernel(const __gri
     const int nvalid = min(16, k1 - key0);
 
     // ---------------- scores S[key][head] for keys g, g+8 and heads 2t, 2t+1
-    const uint4 ka0 = lds128a(sbase + off_ka0);  // half-words (2t, G = 0..7) of row g
-    const uint4 ka1 = lds128a(sbase + off_ka1);  // half-words (2t+1, G)
-    const uint4 kb0 = lds128a(sbase + off_kb0);  // row g+8
-    const uint4 kb1 = lds128a(sbase + off_kb1);
-    const uint4 ska = lds128a(sbase + 4096 + g * 16);
-    const uint4 skb = lds128a(sbase + 4096 + (g + 8) * 16);
     float S[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-    for (int G = 0; G < kQ4NG; ++G) {
-      const uint4 qh = lds128a(qf_addr + G * 1024);
-      const uint4 ql = lds128a(qf_addr + G * 1024 + 512);
-      const uint2 nb = lds64a(qb_addr + G * 32);  // -bias of heads 2t, 2t+1
-      const uint32_t sel = (G & 1) ? 0x4342u : 0x4140u;
-      const uint32_t xa1 = prmt(word_of(ka0, G >> 1), 0u, sel);
-      const uint32_t xa2 = prmt(word_of(ka1, G >> 1), 0u, sel);
-      const uint32_t xb1 = prmt(word_of(kb0, G >> 1), 0u, sel);
-      const uint32_t xb2 = prmt(word_of(kb1, G >> 1), 0u, sel);
-      const uint32_t a10 = nib_lo_pair_biased(xa1), a11 = nib_lo_pair_biased(xb1);
-      const uint32_t a12 = nib_hi_pair_biased(xa1), a13 = nib_hi_pair_biased(xb1);
-      const uint32_t a20 = nib_lo_pair_biased(xa2), a21 = nib_lo_pair_biased(xb2);
-      const uint32_t a22 = nib_hi_pair_biased(xa2), a23 = nib_hi_pair_biased(xb2);
-      float part[4] = {__uint_as_float(nb.x), __uint_as_float(nb.y), __uint_as_float(nb.x), __uint_as_float(nb.y)};
-      mma_f16(part, a10, a11, a12, a13, qh.x, qh.y);
-      mma_f16(part, a20, a21, a22, a23, qh.z, qh.w);
-      mma_f16(part, a10, a11, a12, a13, ql.x, ql.y);
-      mma_f16(part, a20, a21, a22, a23, ql.z, ql.w);
-      const float sa = scale_of(ska, G), sb = scale_of(skb, G);
-      S[0] = fmaf(sa, part[0], S[0]);
-      S[1] = fmaf(sa, part[1], S[1]);
-      S[2] = fmaf(sb, part[2], S[2]);
-      S[3] = fmaf(sb, part[3], S[3]);
+    for (int w = 0; w < kQ4NG / 2; ++w) {  // group pair (2w, 2w+1): one word of each fragment row
+      const uint32_t wa0 = lds32a(sbase + off_ka0 + 4 * w);  // half-words (2t, G = 2w, 2w+1) of row g
+      const uint32_t wa1 = lds32a(sbase + off_ka1 + 4 * w);  // half-words (2t+1, G)
+      const uint32_t wb0 = lds32a(sbase + off_kb0 + 4 * w);  // row g+8
+      const uint32_t wb1 = lds32a(sbase + off_kb1 + 4 * w);
+      const __half2 sca = u32_as_h2(lds32a(sbase + 4096 + g * 16 + 4 * w));  // K scales (2w, 2w+1) of row g
+      const __half2 scb = u32_as_h2(lds32a(sbase + 4096 + (g + 8) * 16 + 4 * w));
+      const float2 fsa = __half22float2(sca), fsb = __half22float2(scb);
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const int G = 2 * w + e;
+        const uint4 qh = lds128a(qf_addr + G * 1024);
+        const uint4 ql = lds128a(qf_addr + G * 1024 + 512);
+        const uint2 nb = lds64a(qb_addr + G * 32);  // -bias of heads 2t, 2t+1
+        const uint32_t sel = e ? 0x4342u : 0x4140u;
+        const uint32_t xa1 = prmt(wa0, 0u, sel);
+        const uint32_t xa2 = prmt(wa1, 0u, sel);
+        const uint32_t xb1 = prmt(wb0, 0u, sel);
+        const uint32_t xb2 = prmt(wb1, 0u, sel);
+        const uint32_t a10 = nib_lo_pair_biased(xa1), a11 = nib_lo_pair_biased(xb1);
+        const uint32_t a12 = nib_hi_pair_biased(xa1), a13 = nib_hi_pair_biased(xb1);
+        const uint32_t a20 = nib_lo_pair_biased(xa2), a21 = nib_lo_pair_biased(xb2);
+        const uint32_t a22 = nib_hi_pair_biased(xa2), a23 = nib_hi_pair_biased(xb2);
+        float part[4] = {__uint_as_float(nb.x), __uint_as_float(nb.y), __uint_as_float(nb.x), __uint_as_float(nb.y)};
+        mma_f16(part, a10, a11, a12, a13, qh.x, qh.y);
+        mma_f16(part, a20, a21, a22, a23, qh.z, qh.w);
+        mma_f16(part, a10, a11, a12, a13, ql.x, ql.y);
+        mma_f16(part, a20, a21, a22, a23, ql.z, ql.w);
+        const float sa = e ? fsa.y : fsa.x, sb = e ? fsb.y : fsb.x;
+        S[0] = fmaf(sa, part[0], S[0]);
+        S[1] = fmaf(sa, part[1], S[1]);
+        S[2] = fmaf(sb, part[2], S[2]);
+        S[3] = fmaf(sb, part[3], S[3]);
+      }
     }
     if (!head0_live) S[0] = S[2] = -INFINITY;
     if (!head1_live) S[1] = S[3] = -INFINITY;
@@ -350,40 +364,39 @@ __global__ void __launch_bounds__(kQ4Warps * 32, 3) decode_q4_kernel(const __gri
     const uint32_t pb0 = movmatrix_trans(pack_half2(p0, p1));  // keys 2t, 2t+1 of head g
     const uint32_t pb1 = movmatrix_trans(pack_half2(p2, p3));  // keys 2t+8, 2t+9
 
-    // V scales of keys 2t, 2t+1, 2t+8, 2t+9 (zero past the end)
-    uint4 sva = lds128a(sbase + 4352 + (2 * t) * 16);
-    uint4 svb = lds128a(sbase + 4352 + (2 * t + 1) * 16);
-    uint4 svc = lds128a(sbase + 4352 + (2 * t + 8) * 16);
-    uint4 svd = lds128a(sbase + 4352 + (2 * t + 9) * 16);
-    if (nvalid < 16) {  // tail tile: stale rows past the end must not reach P.V
-      if (2 * t >= nvalid) sva = make_uint4(0, 0, 0, 0);
-      if (2 * t + 1 >= nvalid) svb = make_uint4(0, 0, 0, 0);
-      if (2 * t + 8 >= nvalid) svc = make_uint4(0, 0, 0, 0);
-      if (2 * t + 9 >= nvalid) svd = make_uint4(0, 0, 0, 0);
-    }
-
-    // V codes: rows 2t, 2t+1, 2t+8, 2t+9, half-word h = g of every group
-    const uint4 v0 = lds128a(sbase + off_v0);
-    const uint4 v1 = lds128a(sbase + off_v1);
-    const uint4 v2 = lds128a(sbase + off_v2);
-    const uint4 v3 = lds128a(sbase + off_v3);
+    // V scales of keys 2t, 2t+1, 2t+8, 2t+9 (zero past the end) and V codes of
+    // the same rows (half-word h = g of every group), loaded one group pair at a
+    // time so that few registers stay live.
+    const bool va_ok = 2 * t < nvalid, vb_ok = 2 * t + 1 < nvalid;
+    const bool vc_ok = 2 * t + 8 < nvalid, vd_ok = 2 * t + 9 < nvalid;
 #pragma unroll
-    for (int G = 0; G < kQ4NG; ++G) {
-      const int w = G >> 1;
-      const uint32_t ssel = (G & 1) ? 0x7632u : 0x5410u;
-      const uint32_t slo = prmt(word_of(sva, w), word_of(svb, w), ssel);
-      const uint32_t shi = prmt(word_of(svc, w), word_of(svd, w), ssel);
-      const uint32_t b0 = h2_as_u32(__hmul2(u32_as_h2(pb0), u32_as_h2(slo)));
-      const uint32_t b1 = h2_as_u32(__hmul2(u32_as_h2(pb1), u32_as_h2(shi)));
-      const uint32_t s0 = (G & 1) ? 0x6622u : 0x4400u;  // byte X of rows a, b -> bytes 0, 2
-      const uint32_t s1 = (G & 1) ? 0x7733u : 0x5511u;  // byte X+1
-      const uint32_t x01 = prmt(word_of(v0, w), word_of(v1, w), s0);
-      const uint32_t x01b = prmt(word_of(v0, w), word_of(v1, w), s1);
-      const uint32_t x23 = prmt(word_of(v2, w), word_of(v3, w), s0);
-      const uint32_t x23b = prmt(word_of(v2, w), word_of(v3, w), s1);
-      // d-tile (G,0): rows g <-> d = 32G+4g, g+8 <-> 32G+4g+2 ; (G,1): +1
-      mma_f16(acc[G][0], nib_lo_pair(x01), nib_lo_pair(x01b), nib_lo_pair(x23), nib_lo_pair(x23b), b0, b1);
-      mma_f16(acc[G][1], nib_hi_pair(x01), nib_hi_pair(x01b), nib_hi_pair(x23), nib_hi_pair(x23b), b0, b1);
+    for (int w = 0; w < kQ4NG / 2; ++w) {
+      const uint32_t swa = va_ok ? lds32a(sbase + 4352 + (2 * t) * 16 + 4 * w) : 0u;
+      const uint32_t swb = vb_ok ? lds32a(sbase + 4352 + (2 * t + 1) * 16 + 4 * w) : 0u;
+      const uint32_t swc = vc_ok ? lds32a(sbase + 4352 + (2 * t + 8) * 16 + 4 * w) : 0u;
+      const uint32_t swd = vd_ok ? lds32a(sbase + 4352 + (2 * t + 9) * 16 + 4 * w) : 0u;
+      const uint32_t cw0 = lds32a(sbase + off_v0 + 4 * w);
+      const uint32_t cw1 = lds32a(sbase + off_v1 + 4 * w);
+      const uint32_t cw2 = lds32a(sbase + off_v2 + 4 * w);
+      const uint32_t cw3 = lds32a(sbase + off_v3 + 4 * w);
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const int G = 2 * w + e;
+        const uint32_t ssel = e ? 0x7632u : 0x5410u;
+        const uint32_t slo = prmt(swa, swb, ssel);
+        const uint32_t shi = prmt(swc, swd, ssel);
+        const uint32_t b0 = h2_as_u32(__hmul2(u32_as_h2(pb0), u32_as_h2(slo)));
+        const uint32_t b1 = h2_as_u32(__hmul2(u32_as_h2(pb1), u32_as_h2(shi)));
+        const uint32_t s0 = e ? 0x6622u : 0x4400u;  // byte X of rows a, b -> bytes 0, 2
+        const uint32_t s1 = e ? 0x7733u : 0x5511u;  // byte X+1
+        const uint32_t x01 = prmt(cw0, cw1, s0);
+        const uint32_t x01b = prmt(cw0, cw1, s1);
+        const uint32_t x23 = prmt(cw2, cw3, s0);
+        const uint32_t x23b = prmt(cw2, cw3, s1);
+        // d-tile (G,0): rows g <-> d = 32G+4g, g+8 <-> 32G+4g+2 ; (G,1): +1
+        mma_f16(acc[G][0], nib_lo_pair(x01), nib_lo_pair(x01b), nib_lo_pair(x23), nib_lo_pair(x23b), b0, b1);
+        mma_f16(acc[G][1], nib_hi_pair(x01), nib_hi_pair(x01b), nib_hi_pair(x23), nib_hi_pair(x23b), b0, b1);
+      }
     }
 
     const int32_t next_page = __shfl_sync(0xffffffffu, my_page, min(i + kQ4Ring, 31));
