@@ -469,7 +469,7 @@ def _row_fp8(K, synth, torch, dev, seed):
     out["fp8_latent"] = {"workload": "absorbed decode, 128 heads x (512 latent + 64 rope) e4m3 rows, context 262144, "
                                      "split-T + merge", "us": ms * 1e3, "flop": flops, "TFLOPs": flops / (ms * 1e-3) / 1e12,
                          "GBs": byts / (ms * 1e-3) / 1e9, "gather_2048_us": gms * 1e3,
-                         "kernel": "decode_rows_kernel (CUDA cores)"}
+                         "kernel": "decode_fp8_kernel (mma.sync f16, split query) + merge_kernel"}
     del c, wsf, wsg
     torch.cuda.empty_cache()
     return out

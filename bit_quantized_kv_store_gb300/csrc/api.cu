@@ -63,15 +63,18 @@ static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 
 // A plane of `rows` rows of `row_bytes` bytes, read in boxes of box_rows rows
 // with the 128-byte shared-memory swizzle.
-static bool encode_rows_map(CUtensorMap* m, const void* base, uint64_t rows, uint32_t row_bytes, uint32_t box_rows) {
+// A plane of `rows` rows of `row_bytes` bytes as a 2-D byte tensor; boxes of
+// box_bytes x box_rows with the given swizzle (box_bytes = the swizzle span).
+static bool encode_rows_map(CUtensorMap* m, const void* base, uint64_t rows, uint32_t row_bytes, uint32_t box_rows,
+                            uint32_t box_bytes = 128, CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B) {
   PFN_cuTensorMapEncodeTiled_v12000 fn = tensor_map_encoder();
   if (!fn) return false;
   cuuint64_t dims[2] = {row_bytes, rows > 0 ? rows : 1};
   cuuint64_t strides[1] = {row_bytes};
-  cuuint32_t box[2] = {row_bytes, box_rows};
+  cuuint32_t box[2] = {box_bytes, box_rows};
   cuuint32_t es[2] = {1, 1};
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, es,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -202,7 +205,8 @@ int32_t kvq_decode_attn(const kvq_cache* cache, const float* q, int32_t num_seqs
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const int group = num_q_heads / cache->num_kv_heads;
   cudaError_t e;
-  if (cache->format == KVQ_FMT_Q4_HAD32) {
+  if (cache->format == KVQ_FMT_Q4_HAD32 || cache->format == KVQ_FMT_FP8_ROW) {
+    const bool fp8 = cache->format == KVQ_FMT_FP8_ROW;
     DecodeArgs a{};
     a.c = *cache;
     a.q = q;
@@ -223,10 +227,13 @@ int32_t kvq_decode_attn(const kvq_cache* cache, const float* q, int32_t num_seqs
     if (!d_sel) {
       const uint64_t rows = static_cast<uint64_t>(cache->num_pages) * cache->num_kv_heads * cache->page_size;
       if (rows >= (1ull << 31)) return KVQ_ERR_UNSUPPORTED;
-      if (!encode_rows_map(&a.tm_k, cache->k, rows, 128, 16) || !encode_rows_map(&a.tm_v, cache->v, rows, 128, 16))
-        return cuda_fail(cudaErrorInvalidValue);
+      const bool ok =
+          fp8 ? encode_rows_map(&a.tm_k, cache->k, rows, 512, 16) &&  // latent codes: 4 column boxes of 128 B
+                    encode_rows_map(&a.tm_v, cache->v, rows, 64, 16, 64, CU_TENSOR_MAP_SWIZZLE_64B)  // rope codes
+              : encode_rows_map(&a.tm_k, cache->k, rows, 128, 16) && encode_rows_map(&a.tm_v, cache->v, rows, 128, 16);
+      if (!ok) return cuda_fail(cudaErrorInvalidValue);
     }
-    e = launch_decode_q4(a, num_seqs, s);
+    e = fp8 ? launch_decode_fp8(a, num_seqs, s) : launch_decode_q4(a, num_seqs, s);
   } else {
     RowsArgs a{*cache, q, num_q_heads, group, cache->format == KVQ_FMT_BF16 ? group : 16, d_seq_lens,
                d_block_tables, max_pages_per_seq, max_seq_len, d_sel, d_sel ? n_sel : 0, sm_scale * kLog2e,

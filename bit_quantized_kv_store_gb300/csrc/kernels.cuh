@@ -9,10 +9,11 @@ namespace kvq {
 
 // Split-T decode over the 4-bit rotated cache (decode_q4.cu).
 struct DecodeArgs {
-  CUtensorMap tm_k;  // K codes plane as [rows][128 B], 16-row boxes, 128-byte swizzle
-  CUtensorMap tm_v;  // V codes plane, same shape
+  CUtensorMap tm_k;  // 4-bit: K codes plane as [rows][128 B], 16-row boxes, 128-byte swizzle;
+                     // fp8: latent codes [rows][512 B], 128 x 16 boxes, 128-byte swizzle
+  CUtensorMap tm_v;  // 4-bit: V codes plane, same shape; fp8: rope codes [rows][64 B], 64-byte swizzle
   kvq_cache c;
-  const float* q;  // [B, Hq, D], rotated
+  const float* q;  // [B, Hq, D] (4-bit: rotated; fp8: [B, Hq, 576])
   int Hq;
   int group;  // Hq / Hk
   const int32_t* seq_lens;
@@ -67,8 +68,9 @@ struct MergeArgs {
 
 // Causal prefill over decoded 4-bit slots (prefill_tc.cu).
 struct PrefillArgs {
-  CUtensorMap tm_k;  // K codes plane as [rows][128 B], 16-row boxes, 128-byte swizzle
-  CUtensorMap tm_v;  // V codes plane, same shape
+  CUtensorMap tm_k;  // 4-bit: K codes plane as [rows][128 B], 16-row boxes, 128-byte swizzle;
+                     // fp8: latent codes [rows][512 B], 128 x 16 boxes, 128-byte swizzle
+  CUtensorMap tm_v;  // 4-bit: V codes plane, same shape; fp8: rope codes [rows][64 B], 64-byte swizzle
   kvq_cache c;
   const void* q;
   int dtype;
@@ -91,6 +93,9 @@ cudaError_t launch_store(const kvq_cache& c, const void* k, const void* v, int d
 cudaError_t launch_rotate(const void* x, int dtype, float* y, int64_t rows, int head_dim, cudaStream_t s);
 cudaError_t launch_decode_q4(const DecodeArgs& a, int B, cudaStream_t s);
 cudaError_t launch_decode_rows(const RowsArgs& a, int B, cudaStream_t s);
+// fp8 latent rows on the tensor cores (decode_fp8.cu); tm_k / tm_v map the latent
+// and rope code planes.
+cudaError_t launch_decode_fp8(const DecodeArgs& a, int B, cudaStream_t s);
 cudaError_t launch_merge(const MergeArgs& a, int B, cudaStream_t s);
 cudaError_t launch_prefill_tc(const PrefillArgs& a, cudaStream_t s);
 
