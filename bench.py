@@ -494,7 +494,7 @@ def _row_bf16(K, synth, torch, dev, seed):
     out["bf16_cache_32k"] = {"workload": "bf16 (unrotated) cache, context 32768, 1 layer, same split-T + merge",
                              "decode_kernel_us": dms * 1e3, "cache_bytes": byts, "achieved_GBs": byts / (dms * 1e-3) / 1e9,
                              "bytes_vs_4bit": byts / (Tb * BYTES_PER_POS_LAYER),
-                             "kernel": "decode_rows_kernel (CUDA cores)"}
+                             "kernel": "decode_bf16_kernel (mma.sync bf16, split query and P)"}
     del c, wsb
     torch.cuda.empty_cache()
     return out

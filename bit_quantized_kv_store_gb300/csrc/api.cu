@@ -205,8 +205,8 @@ int32_t kvq_decode_attn(const kvq_cache* cache, const float* q, int32_t num_seqs
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const int group = num_q_heads / cache->num_kv_heads;
   cudaError_t e;
-  if (cache->format == KVQ_FMT_Q4_HAD32 || cache->format == KVQ_FMT_FP8_ROW) {
-    const bool fp8 = cache->format == KVQ_FMT_FP8_ROW;
+  {
+    const bool fp8 = cache->format == KVQ_FMT_FP8_ROW, bf16 = cache->format == KVQ_FMT_BF16;
     DecodeArgs a{};
     a.c = *cache;
     a.q = q;
@@ -227,19 +227,17 @@ int32_t kvq_decode_attn(const kvq_cache* cache, const float* q, int32_t num_seqs
     if (!d_sel) {
       const uint64_t rows = static_cast<uint64_t>(cache->num_pages) * cache->num_kv_heads * cache->page_size;
       if (rows >= (1ull << 31)) return KVQ_ERR_UNSUPPORTED;
-      const bool ok =
-          fp8 ? encode_rows_map(&a.tm_k, cache->k, rows, 512, 16) &&  // latent codes: 4 column boxes of 128 B
-                    encode_rows_map(&a.tm_v, cache->v, rows, 64, 16, 64, CU_TENSOR_MAP_SWIZZLE_64B)  // rope codes
-              : encode_rows_map(&a.tm_k, cache->k, rows, 128, 16) && encode_rows_map(&a.tm_v, cache->v, rows, 128, 16);
+      bool ok;
+      if (fp8)  // latent codes: 4 column boxes of 128 B; rope codes: one 64-byte box
+        ok = encode_rows_map(&a.tm_k, cache->k, rows, 512, 16) &&
+             encode_rows_map(&a.tm_v, cache->v, rows, 64, 16, 64, CU_TENSOR_MAP_SWIZZLE_64B);
+      else if (bf16)  // 512-byte bf16 rows: 4 column boxes of 128 B
+        ok = encode_rows_map(&a.tm_k, cache->k, rows, 512, 16) && encode_rows_map(&a.tm_v, cache->v, rows, 512, 16);
+      else
+        ok = encode_rows_map(&a.tm_k, cache->k, rows, 128, 16) && encode_rows_map(&a.tm_v, cache->v, rows, 128, 16);
       if (!ok) return cuda_fail(cudaErrorInvalidValue);
     }
-    e = fp8 ? launch_decode_fp8(a, num_seqs, s) : launch_decode_q4(a, num_seqs, s);
-  } else {
-    RowsArgs a{*cache, q, num_q_heads, group, cache->format == KVQ_FMT_BF16 ? group : 16, d_seq_lens,
-               d_block_tables, max_pages_per_seq, max_seq_len, d_sel, d_sel ? n_sel : 0, sm_scale * kLog2e,
-               reinterpret_cast<float*>(ws + w.m_off), reinterpret_cast<float*>(ws + w.z_off),
-               reinterpret_cast<float*>(ws + w.acc_off), w.P, reinterpret_cast<int32_t*>(ws)};
-    e = launch_decode_rows(a, num_seqs, s);
+    e = fp8 ? launch_decode_fp8(a, num_seqs, s) : bf16 ? launch_decode_bf16(a, num_seqs, s) : launch_decode_q4(a, num_seqs, s);
   }
   return e == cudaSuccess ? KVQ_OK : cuda_fail(e);
 }

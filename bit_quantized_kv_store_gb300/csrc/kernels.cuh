@@ -30,27 +30,6 @@ struct DecodeArgs {
   int32_t* status;
 };
 
-// Split-T decode over bf16 rows or fp8 latent rows (decode_rows.cu).
-struct RowsArgs {
-  kvq_cache c;
-  const float* q;  // [B, Hq, W]
-  int Hq;
-  int group;
-  int hb;  // query heads per CTA
-  const int32_t* seq_lens;
-  const int32_t* block_tables;
-  int max_pages;
-  int max_seq_len;
-  const int32_t* sel;
-  int n_sel;
-  float qscale;
-  float* ws_m;
-  float* ws_z;
-  float* ws_acc;
-  int P;
-  int32_t* status;
-};
-
 // Log-sum-exp merge of the partials (merge.cu).
 struct MergeArgs {
   const float* ws_m;
@@ -92,10 +71,12 @@ cudaError_t launch_store(const kvq_cache& c, const void* k, const void* v, int d
                          const int32_t* slots, int32_t* status, cudaStream_t s);
 cudaError_t launch_rotate(const void* x, int dtype, float* y, int64_t rows, int head_dim, cudaStream_t s);
 cudaError_t launch_decode_q4(const DecodeArgs& a, int B, cudaStream_t s);
-cudaError_t launch_decode_rows(const RowsArgs& a, int B, cudaStream_t s);
 // fp8 latent rows on the tensor cores (decode_fp8.cu); tm_k / tm_v map the latent
 // and rope code planes.
 cudaError_t launch_decode_fp8(const DecodeArgs& a, int B, cudaStream_t s);
+// bf16 rows on the tensor cores (decode_bf16.cu); tm_k / tm_v map the K and V
+// planes as [rows][512 B] in 128-byte column boxes.
+cudaError_t launch_decode_bf16(const DecodeArgs& a, int B, cudaStream_t s);
 cudaError_t launch_merge(const MergeArgs& a, int B, cudaStream_t s);
 cudaError_t launch_prefill_tc(const PrefillArgs& a, cudaStream_t s);
 

@@ -94,6 +94,27 @@ def test_decode_262k_context(K):
     close(got, ref, "262K decode, KV head 2")
 
 
+def test_decode_bf16_32k_context(K):
+    """The bf16 comparison cache at 32,769 keys: KV head 1 sampled against the oracle."""
+    dev = "cuda"
+    seed = 1240
+    T = 32769
+    n_pages = (T + PS - 1) // PS
+    c = K.Cache(K.FMT_BF16, HK, D, PS, n_pages, device=dev)
+    k = synth.heavy_tailed((T, HK, D), dev, seed, "k", subset=(seed, "k"))
+    v = synth.heavy_tailed((T, HK, D), dev, seed, "v", subset=(seed, "v"))
+    K.store(c, k, v, torch.arange(T, dtype=torch.int32, device=dev))
+    q = synth.heavy_tailed((1, HQ, D), dev, seed, "q")
+    bt = torch.arange(n_pages, dtype=torch.int32, device=dev).reshape(1, -1)
+    seq = torch.tensor([T], dtype=torch.int32, device=dev)
+    ws = K.alloc_workspace(c, 1, HQ, T, device=dev)
+    out = K.decode(c, q, seq, bt, T, 1 / 16, ws).cpu().numpy()
+    oc = O.Cache(O.BF16, 1, D, PS, n_pages)
+    O.store(oc, bits16(k[:, 1])[:, None], bits16(v[:, 1])[:, None], np.arange(T, dtype=np.int32))
+    ref = O.decode(oc, bits16(q)[:, 6:12], [T], np.arange(n_pages, dtype=np.int32).reshape(1, -1), 1 / 16)
+    close(out[0, 6:12], ref[0], "bf16 32K decode, KV head 1")
+
+
 def test_batched_ragged_paged_decode_full_size(K):
     dev = "cuda"
     seed = 1237

@@ -311,6 +311,42 @@ def test_decode_bf16_cache(K):
         assert_close(out[b], ref[b], what=f"bf16 seq {b}")
 
 
+@pytest.mark.parametrize("T", [1, 16, 17, 511, 513, 4097])
+def test_decode_bf16_lengths(K, T):
+    g, o, bt, q, ml = decode_case(K, [T], fmt=K.FMT_BF16, seed=300 + T)
+    out, _ = run_decode(K, g, bt, q, [T], ml, 1 / 16)
+    ref = O.decode(o, to_np_in(q), [T], bt, 1 / 16)
+    assert_close(out[0], ref[0], what=f"bf16 T={T}")
+
+
+@pytest.mark.parametrize("Hk,Hq", [(1, 8), (3, 21), (2, 2)])
+def test_decode_bf16_gqa_groups(K, Hk, Hq):
+    lens = [700, 45]
+    g, o, bt, q, ml = decode_case(K, lens, Hk=Hk, Hq=Hq, fmt=K.FMT_BF16, seed=400 + Hq)
+    out, _ = run_decode(K, g, bt, q, lens, ml, 0.07)
+    ref = O.decode(o, to_np_in(q), lens, bt, 0.07)
+    for b in range(2):
+        assert_close(out[b], ref[b], what=f"bf16 Hk={Hk} Hq={Hq} seq {b}")
+
+
+def test_decode_bf16_gather_and_bad_page(K):
+    lens = [2600, 900]
+    g, o, bt, q, ml = decode_case(K, lens, fmt=K.FMT_BF16, seed=41)
+    for n_sel in (1, 100, 777):
+        sel = np.stack([synth.distinct_sorted(n_sel, L, 41, b).numpy() for b, L in enumerate(lens)]).astype(np.int32)
+        out, _ = run_decode(K, g, bt, q, lens, ml, 1 / 16, sel=sel)
+        ref = O.decode(o, to_np_in(q), lens, bt, 1 / 16, sel=sel)
+        for b in range(2):
+            assert_close(out[b], ref[b], what=f"bf16 gather n_sel={n_sel} seq {b}")
+    bad = bt.copy()
+    bad[0, 5] = 10_000
+    out, ws = run_decode(K, g, bad, q, lens, ml, 1 / 16)
+    assert K.read_status(ws) & K.DEV_BAD_PAGE
+    assert np.isnan(out[0]).all()
+    ref = O.decode(o, to_np_in(q[1:2]), [lens[1]], bt[1:2], 1 / 16)
+    assert_close(out[1], ref[0], what="bf16 healthy sequence next to a bad one")
+
+
 def test_decode_fp8_latent(K):
     D, R, ps, Hq = 512, 64, 16, 32
     lens = [1100, 40]
