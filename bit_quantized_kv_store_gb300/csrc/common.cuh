@@ -9,6 +9,8 @@
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
+#include <utility>
+
 #include "../../include/kvq.h"
 
 namespace kvq {
@@ -19,6 +21,35 @@ constexpr float kLog2e = 1.4426950408889634f;
 // fp32 nearest value of 1/sqrt(32); the store multiplies by it once after the
 // butterfly (0x3E3504F3).
 constexpr float kHadamardScale = 0.17677669529663687f;
+
+// ---------------------------------------------------------------- programmatic dependent launch
+// Every kernel of the library starts with pdl_wait(): it returns once the
+// preceding kernel in the stream has completed and its memory is visible (at
+// once when there is none), so a kernel launched by launch_pdl may be
+// scheduled while its predecessor drains without reading or overwriting
+// anything early.  Because every kernel waits before it can complete, the
+// ordering is transitive along the stream.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+// Let the next kernel in the stream be scheduled now (its pdl_wait still waits
+// for this whole grid to complete).  Small kernels call it at once; the large
+// ones only near their end, so waiting successor CTAs never take their slots.
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                              Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 __device__ __forceinline__ void set_status(int32_t* st, int32_t bit) {
   if (st) atomicOr(st, bit);

@@ -146,6 +146,7 @@ __device__ __forceinline__ bool bf_issue_tile(const DecodeArgs& a, int b, int kv
 
 template <bool GATHER>
 __global__ void __launch_bounds__(kBfWarps * 32, 1) decode_bf16_kernel(const __grid_constant__ DecodeArgs a) {
+  pdl_wait();
   extern __shared__ uint8_t smem_raw[];
   BfSmem& sm = *reinterpret_cast<BfSmem*>(smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u));
   const int p = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
@@ -363,6 +364,7 @@ __global__ void __launch_bounds__(kBfWarps * 32, 1) decode_bf16_kernel(const __g
       a.ws_z[pi] = bad ? NAN : Z;
     }
   }
+  pdl_trigger();  // after this CTA's last write
 }
 
 cudaError_t launch_decode_bf16(const DecodeArgs& a, int B, cudaStream_t s) {
@@ -372,12 +374,14 @@ cudaError_t launch_decode_bf16(const DecodeArgs& a, int B, cudaStream_t s) {
     cudaError_t e =
         cudaFuncSetAttribute(decode_bf16_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    decode_bf16_kernel<true><<<grid, kBfWarps * 32, smem, s>>>(a);
+    e = launch_pdl(decode_bf16_kernel<true>, grid, dim3(kBfWarps * 32), smem, s, a);
+    if (e != cudaSuccess) return e;
   } else {
     cudaError_t e =
         cudaFuncSetAttribute(decode_bf16_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    decode_bf16_kernel<false><<<grid, kBfWarps * 32, smem, s>>>(a);
+    e = launch_pdl(decode_bf16_kernel<false>, grid, dim3(kBfWarps * 32), smem, s, a);
+    if (e != cudaSuccess) return e;
   }
   return cudaGetLastError();
 }

@@ -130,6 +130,7 @@ __device__ __forceinline__ void consumers_sync() {
 
 template <bool GATHER>
 __global__ void __launch_bounds__((kF8Warps + 1) * 32, 1) decode_fp8_kernel(const __grid_constant__ DecodeArgs a) {
+  pdl_wait();
   extern __shared__ uint8_t smem_raw[];
   F8Smem& sm = *reinterpret_cast<F8Smem*>(smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u));
   const int hblk = blockIdx.x, p = blockIdx.y, b = blockIdx.z;
@@ -441,6 +442,7 @@ __global__ void __launch_bounds__((kF8Warps + 1) * 32, 1) decode_fp8_kernel(cons
       if (lane == 0) mbar_arrive(&sm.empty[s]);
     }
 
+    pdl_trigger();
     // ---------------- partials
     z_part[0] += __shfl_xor_sync(0xffffffffu, z_part[0], 1);
     z_part[0] += __shfl_xor_sync(0xffffffffu, z_part[0], 2);
@@ -483,12 +485,14 @@ cudaError_t launch_decode_fp8(const DecodeArgs& a, int B, cudaStream_t s) {
     cudaError_t e =
         cudaFuncSetAttribute(decode_fp8_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    decode_fp8_kernel<true><<<grid, (kF8Warps + 1) * 32, smem, s>>>(a);
+    e = launch_pdl(decode_fp8_kernel<true>, grid, dim3((kF8Warps + 1) * 32), smem, s, a);
+    if (e != cudaSuccess) return e;
   } else {
     cudaError_t e =
         cudaFuncSetAttribute(decode_fp8_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    decode_fp8_kernel<false><<<grid, (kF8Warps + 1) * 32, smem, s>>>(a);
+    e = launch_pdl(decode_fp8_kernel<false>, grid, dim3((kF8Warps + 1) * 32), smem, s, a);
+    if (e != cudaSuccess) return e;
   }
   return cudaGetLastError();
 }

@@ -156,6 +156,7 @@ __device__ __forceinline__ float scale_of(const uint4& v, int G) {
 
 template <bool GATHER>
 __global__ void __launch_bounds__(kQ4Warps * 32, kQ4MinBlocks) decode_q4_kernel(const __grid_constant__ DecodeArgs a) {
+  pdl_wait();
   extern __shared__ uint8_t smem_raw[];
   // 1024-byte alignment for the swizzled tiles (the launch adds 1 KB of slack)
   Q4Smem& sm = *reinterpret_cast<Q4Smem*>(smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u));
@@ -461,6 +462,7 @@ __global__ void __launch_bounds__(kQ4Warps * 32, kQ4MinBlocks) decode_q4_kernel(
       a.ws_z[pi] = bad ? NAN : Z;
     }
   }
+  pdl_trigger();  // after this CTA's last write
 }
 
 cudaError_t launch_decode_q4(const DecodeArgs& a, int B, cudaStream_t s) {
@@ -470,12 +472,14 @@ cudaError_t launch_decode_q4(const DecodeArgs& a, int B, cudaStream_t s) {
     cudaError_t e =
         cudaFuncSetAttribute(decode_q4_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    decode_q4_kernel<true><<<grid, kQ4Warps * 32, smem, s>>>(a);
+    e = launch_pdl(decode_q4_kernel<true>, grid, dim3(kQ4Warps * 32), smem, s, a);
+    if (e != cudaSuccess) return e;
   } else {
     cudaError_t e =
         cudaFuncSetAttribute(decode_q4_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    decode_q4_kernel<false><<<grid, kQ4Warps * 32, smem, s>>>(a);
+    e = launch_pdl(decode_q4_kernel<false>, grid, dim3(kQ4Warps * 32), smem, s, a);
+    if (e != cudaSuccess) return e;
   }
   return cudaGetLastError();
 }

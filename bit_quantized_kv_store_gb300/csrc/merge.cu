@@ -15,6 +15,8 @@
 namespace kvq {
 
 __global__ void __launch_bounds__(256) merge_kernel(const MergeArgs a) {
+  pdl_wait();
+  pdl_trigger();
   const int grp = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   float* outp = a.out + ((int64_t)b * a.Hq + h) * a.Dv + 32 * grp;
@@ -117,7 +119,8 @@ __global__ void __launch_bounds__(256) merge_kernel(const MergeArgs a) {
 cudaError_t launch_merge(const MergeArgs& a, int B, cudaStream_t s) {
   dim3 grid(a.Dv / 32, a.Hq, B);
   if (B == 0 || a.Hq == 0) return cudaSuccess;
-  merge_kernel<<<grid, 256, 0, s>>>(a);
+  cudaError_t e = launch_pdl(merge_kernel, grid, dim3(256), 0, s, a);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

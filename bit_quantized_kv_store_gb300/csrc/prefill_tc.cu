@@ -175,6 +175,7 @@ __device__ __forceinline__ __half2 scale_pair(uint32_t w, int hi) {
 }
 
 __global__ void __launch_bounds__(kPfThreads, 1) prefill_tc_kernel(const __grid_constant__ PrefillArgs a) {
+  pdl_wait();
   extern __shared__ uint8_t smem_raw[];
   PfSmem& sm = *reinterpret_cast<PfSmem*>(smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -557,6 +558,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_tc_kernel(const __grid_
     }
   }
 
+  pdl_trigger();
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -571,7 +573,8 @@ cudaError_t launch_prefill_tc(const PrefillArgs& a, cudaStream_t s) {
   if (e != cudaSuccess) return e;
   const int qpb = 128 / a.group;
   dim3 grid((a.n_q + qpb - 1) / qpb, a.c.num_kv_heads);
-  prefill_tc_kernel<<<grid, kPfThreads, smem, s>>>(a);
+  e = launch_pdl(prefill_tc_kernel, grid, dim3(kPfThreads), smem, s, a);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

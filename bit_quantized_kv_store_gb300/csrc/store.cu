@@ -29,6 +29,8 @@ template <int NG>
 __global__ void __launch_bounds__(256) store_q4_kernel(kvq_cache c, const void* __restrict__ k,
                                                        const void* __restrict__ v, int dtype, int64_t n_tok,
                                                        const int32_t* __restrict__ slots, int32_t* status) {
+  pdl_wait();
+  pdl_trigger();
   constexpr int D = NG * 32;
   const int lane = threadIdx.x & 31;
   const int64_t row = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
@@ -106,9 +108,67 @@ __global__ void __launch_bounds__(256) store_q4_kernel(kvq_cache c, const void* 
   }
 }
 
+// Latency form of the same store for a handful of rows (a decode step stores one
+// token): one warp per (row, group), so the groups of a row are packed in
+// parallel instead of one after another.  Same arithmetic, same bytes.
+template <int NG>
+__global__ void __launch_bounds__(256) store_q4_group_kernel(kvq_cache c, const void* __restrict__ k,
+                                                             const void* __restrict__ v, int dtype, int64_t n_tok,
+                                                             const int32_t* __restrict__ slots, int32_t* status) {
+  pdl_wait();
+  pdl_trigger();
+  constexpr int D = NG * 32;
+  const int lane = threadIdx.x & 31;
+  const int64_t wid = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  const int Hk = c.num_kv_heads;
+  if (wid >= n_tok * Hk * 2 * NG) return;
+  const int G = static_cast<int>(wid % NG);
+  const int64_t row = wid / NG;
+  const int kv = static_cast<int>(row & 1);
+  const int64_t tok = (row >> 1) / Hk;
+  const int head = static_cast<int>((row >> 1) % Hk);
+  const int32_t slot = slots[tok];
+  if (slot < 0) return;
+  if ((int64_t)slot >= (int64_t)c.num_pages * c.page_size) {
+    if (lane == 0 && G == 0) set_status(status, KVQ_DEV_BAD_SLOT);
+    return;
+  }
+  const int64_t page = slot / c.page_size;
+  const int off = slot % c.page_size;
+  const int64_t r = (page * Hk + head) * c.page_size + off;
+  const void* src = kv ? v : k;
+  float x = load_act(src, dtype, (tok * Hk + head) * D + 32 * G + lane);
+  x = warp_fwht32(x, lane);
+  const float y = __fmul_rn(x, kHadamardScale);
+  float amax = fabsf(y);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+  const float s32 = __fdiv_rn(amax, 8.0f);
+  __half s16 = __float2half_rn(s32);
+  if (__hisinf(s16)) s16 = __ushort_as_half(0x7BFFu);  // saturate to 65504
+  const float s = __half2float(s16);
+  int code = 8;
+  if (s != 0.0f) {
+    float q = rintf(__fdiv_rn(y, s));
+    q = fminf(fmaxf(q, -8.0f), 7.0f);
+    code = static_cast<int>(q) + 8;
+  }
+  uint32_t bits = static_cast<uint32_t>(code) << (4 * (lane & 3));
+  bits |= __shfl_xor_sync(0xffffffffu, bits, 1);
+  bits |= __shfl_xor_sync(0xffffffffu, bits, 2);
+  uint8_t* codes = static_cast<uint8_t*>(kv ? c.v : c.k) + r * (D / 2);
+  if ((lane & 3) == 0) {
+    const int h = lane >> 2;  // half-word (G, h) lives at byte 2 * (h * NG + G)
+    reinterpret_cast<uint16_t*>(codes)[h * NG + G] = static_cast<uint16_t>(bits);
+  }
+  if (lane == 0) (static_cast<uint16_t*>(kv ? c.v_scale : c.k_scale) + r * NG)[G] = __half_as_ushort(s16);
+}
+
 // BF16 comparison format: plain copy / RNE conversion of each value.
 __global__ void store_bf16_kernel(kvq_cache c, const void* __restrict__ k, const void* __restrict__ v, int dtype,
                                   int64_t n_tok, const int32_t* __restrict__ slots, int32_t* status) {
+  pdl_wait();
+  pdl_trigger();
   const int D = c.head_dim, Hk = c.num_kv_heads;
   const int64_t total = n_tok * Hk * D;
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
@@ -144,6 +204,8 @@ __device__ __forceinline__ uint8_t e4m3_encode(float x) {
 __global__ void __launch_bounds__(128) store_fp8_kernel(kvq_cache c, const void* __restrict__ rows, int dtype,
                                                          int64_t n_tok, const int32_t* __restrict__ slots,
                                                          int32_t* status) {
+  pdl_wait();
+  pdl_trigger();
   const int64_t tok = blockIdx.x;
   const int D = c.head_dim, R = c.rope_dim, W = D + R;
   const int32_t slot = slots[tok];
@@ -188,6 +250,8 @@ __global__ void __launch_bounds__(128) store_fp8_kernel(kvq_cache c, const void*
 // y = blockdiag(H) x; one warp per 32-group.
 __global__ void __launch_bounds__(256) rotate_kernel(const void* __restrict__ x, int dtype, float* y,
                                                      int64_t n_groups) {
+  pdl_wait();
+  pdl_trigger();
   const int lane = threadIdx.x & 31;
   const int64_t g = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   if (g >= n_groups) return;
@@ -198,34 +262,50 @@ __global__ void __launch_bounds__(256) rotate_kernel(const void* __restrict__ x,
 
 // ---------------------------------------------------------------- launchers
 
+// Up to this many rows the store runs one warp per (row, group).
+constexpr int64_t kStoreGroupRows = 256;
+
 cudaError_t launch_store(const kvq_cache& c, const void* k, const void* v, int dtype, int64_t n_tok,
                          const int32_t* slots, int32_t* status, cudaStream_t s) {
   if (n_tok == 0) return cudaSuccess;
-  if (c.format == KVQ_FMT_Q4_HAD32) {
+  cudaError_t e = cudaSuccess;
+  if (c.format == KVQ_FMT_Q4_HAD32 && n_tok * c.num_kv_heads * 2 <= kStoreGroupRows) {
+    const int64_t warps = n_tok * c.num_kv_heads * 2 * (c.head_dim / 32);
+    const dim3 blocks((warps + 7) / 8);
+    switch (c.head_dim / 32) {
+      case 1: e = launch_pdl(store_q4_group_kernel<1>, blocks, dim3(256), 0, s, c, k, v, dtype, n_tok, slots, status); break;
+      case 2: e = launch_pdl(store_q4_group_kernel<2>, blocks, dim3(256), 0, s, c, k, v, dtype, n_tok, slots, status); break;
+      case 4: e = launch_pdl(store_q4_group_kernel<4>, blocks, dim3(256), 0, s, c, k, v, dtype, n_tok, slots, status); break;
+      case 8: e = launch_pdl(store_q4_group_kernel<8>, blocks, dim3(256), 0, s, c, k, v, dtype, n_tok, slots, status); break;
+      default: return cudaErrorInvalidValue;
+    }
+  } else if (c.format == KVQ_FMT_Q4_HAD32) {
     const int64_t rows = n_tok * c.num_kv_heads * 2;
     const int64_t blocks = (rows + 7) / 8;
     switch (c.head_dim / 32) {
-      case 1: store_q4_kernel<1><<<blocks, 256, 0, s>>>(c, k, v, dtype, n_tok, slots, status); break;
-      case 2: store_q4_kernel<2><<<blocks, 256, 0, s>>>(c, k, v, dtype, n_tok, slots, status); break;
-      case 4: store_q4_kernel<4><<<blocks, 256, 0, s>>>(c, k, v, dtype, n_tok, slots, status); break;
-      case 8: store_q4_kernel<8><<<blocks, 256, 0, s>>>(c, k, v, dtype, n_tok, slots, status); break;
+      case 1: e = launch_pdl(store_q4_kernel<1>, dim3(blocks), dim3(256), 0, s, c, k, v, dtype, n_tok, slots, status); break;
+      case 2: e = launch_pdl(store_q4_kernel<2>, dim3(blocks), dim3(256), 0, s, c, k, v, dtype, n_tok, slots, status); break;
+      case 4: e = launch_pdl(store_q4_kernel<4>, dim3(blocks), dim3(256), 0, s, c, k, v, dtype, n_tok, slots, status); break;
+      case 8: e = launch_pdl(store_q4_kernel<8>, dim3(blocks), dim3(256), 0, s, c, k, v, dtype, n_tok, slots, status); break;
       default: return cudaErrorInvalidValue;
     }
   } else if (c.format == KVQ_FMT_BF16) {
     const int64_t total = n_tok * c.num_kv_heads * c.head_dim;
     int64_t blocks = (total + 255) / 256;
     if (blocks > 152 * 64) blocks = 152 * 64;
-    store_bf16_kernel<<<blocks, 256, 0, s>>>(c, k, v, dtype, n_tok, slots, status);
+    e = launch_pdl(store_bf16_kernel, dim3(blocks), dim3(256), 0, s, c, k, v, dtype, n_tok, slots, status);
   } else {
-    store_fp8_kernel<<<n_tok, 128, 0, s>>>(c, k, dtype, n_tok, slots, status);
+    e = launch_pdl(store_fp8_kernel, dim3(n_tok), dim3(128), 0, s, c, k, dtype, n_tok, slots, status);
   }
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
 cudaError_t launch_rotate(const void* x, int dtype, float* y, int64_t rows, int head_dim, cudaStream_t s) {
   const int64_t groups = rows * (head_dim / 32);
   if (groups == 0) return cudaSuccess;
-  rotate_kernel<<<(groups + 7) / 8, 256, 0, s>>>(x, dtype, y, groups);
+  cudaError_t e = launch_pdl(rotate_kernel, dim3((groups + 7) / 8), dim3(256), 0, s, x, dtype, y, groups);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

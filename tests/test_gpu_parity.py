@@ -84,8 +84,9 @@ def fill_sequence(K, g, o, k, v, bt_row, T, status=None):
 
 @pytest.mark.parametrize("D", [64, 128, 256])
 @pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
-def test_store_q4_bit_exact(K, D, dtype):
-    Hk, ps, n_pages, T = 3, 32, 9, 250
+@pytest.mark.parametrize("T", [250, 20])  # large stores take the row kernel, small ones the (row, group) kernel
+def test_store_q4_bit_exact(K, D, dtype, T):
+    Hk, ps, n_pages = 3, 32, 9
     k = synth.outlier_normal((T, Hk, D), 4, 20.0, "cpu", D, "k").to(dtype)
     v = synth.heavy_tailed((T, Hk, D), "cpu", D, "v").to(dtype)
     g, o = make_cache_pair(K, K.FMT_Q4_HAD32, Hk, D, ps, n_pages)
