@@ -43,6 +43,8 @@ SIGNATURES = {
     "kvq_decode_workspace_size": (_SZ, [ctypes.POINTER(CacheDesc), _I32, _I32, _I32, _I32]),
     "kvq_decode_attn": (_I32, [ctypes.POINTER(CacheDesc), _P, _I32, _I32, _P, _P, _I32, _I32, _P, _I32, _F, _P,
                                _SZ, _P]),
+    "kvq_decode_attn_unrotated": (_I32, [ctypes.POINTER(CacheDesc), _P, _I32, _I32, _I32, _P, _P, _I32, _I32, _P,
+                                         _I32, _F, _P, _SZ, _P]),
     "kvq_merge": (_I32, [ctypes.POINTER(CacheDesc), _P, _SZ, _I32, _I32, _P, _I32, _I32, _I32, _P, _P]),
     "kvq_prefill_attn": (_I32, [ctypes.POINTER(CacheDesc), _P, _I32, _I32, _I32, _I32, _P, _I32, _F, _P, _P, _P]),
     "kvq_read_status": (_I32, [_P, _P, _P]),
@@ -176,6 +178,17 @@ def decode_attn(cache: Cache, q, seq_lens, block_tables, max_seq_len, sm_scale, 
     _check(lib().kvq_decode_attn(cache.ref, _ptr(q), B, Hq, _ptr(seq_lens), _ptr(block_tables),
                                  block_tables.shape[1], max_seq_len, _ptr(sel), n_sel, float(sm_scale),
                                  _ptr(workspace), workspace.numel(), _stream(stream)), "kvq_decode_attn")
+
+
+def decode_attn_unrotated(cache: Cache, q, seq_lens, block_tables, max_seq_len, sm_scale, workspace, sel=None,
+                          stream=None):
+    """Decode partials from an unrotated query (4-bit format): the rotation runs in the decode kernel."""
+    B, Hq = q.shape[0], q.shape[1]
+    n_sel = 0 if sel is None else sel.shape[1]
+    _check(lib().kvq_decode_attn_unrotated(cache.ref, _ptr(q), _dtype_code(q), B, Hq, _ptr(seq_lens), _ptr(block_tables),
+                                           block_tables.shape[1], max_seq_len, _ptr(sel), n_sel, float(sm_scale),
+                                           _ptr(workspace), workspace.numel(), _stream(stream)),
+           "kvq_decode_attn_unrotated")
 
 
 def merge(cache: Cache, workspace, num_seqs, num_q_heads, seq_lens, max_seq_len, out, n_sel=0, rotate_back=None,

@@ -186,16 +186,18 @@ size_t kvq_decode_workspace_size(const kvq_cache* cache, int32_t num_seqs, int32
   return ws_layout(cache, num_seqs, num_q_heads, max_seq_len, n_sel).total;
 }
 
-int32_t kvq_decode_attn(const kvq_cache* cache, const float* q, int32_t num_seqs, int32_t num_q_heads,
-                        const int32_t* d_seq_lens, const int32_t* d_block_tables, int32_t max_pages_per_seq,
-                        int32_t max_seq_len, const int32_t* d_sel, int32_t n_sel, float sm_scale, void* workspace,
-                        size_t ws_bytes, void* stream) {
+static int32_t decode_attn_impl(const kvq_cache* cache, const float* q, const void* q_raw, int32_t q_dtype,
+                                int32_t num_seqs, int32_t num_q_heads, const int32_t* d_seq_lens,
+                                const int32_t* d_block_tables, int32_t max_pages_per_seq, int32_t max_seq_len,
+                                const int32_t* d_sel, int32_t n_sel, float sm_scale, void* workspace, size_t ws_bytes,
+                                void* stream) {
   int32_t st = check_cache(cache);
   if (st != KVQ_OK) return st;
   st = check_decode_shape(cache, num_seqs, num_q_heads, d_seq_lens, max_seq_len, d_sel != nullptr, n_sel);
   if (st != KVQ_OK) return st;
   if (num_seqs == 0) return KVQ_OK;
-  if (!q || !d_block_tables || max_pages_per_seq < 1 || !workspace || !aligned16(q) || !aligned16(workspace))
+  if ((q_raw ? !aligned16(q_raw) : (!q || !aligned16(q))) || !d_block_tables || max_pages_per_seq < 1 || !workspace ||
+      !aligned16(workspace))
     return KVQ_ERR_INVALID_ARG;
   if (!d_sel && static_cast<int64_t>(max_seq_len) > static_cast<int64_t>(max_pages_per_seq) * cache->page_size)
     return KVQ_ERR_INVALID_ARG;
@@ -219,6 +221,8 @@ int32_t kvq_decode_attn(const kvq_cache* cache, const float* q, int32_t num_seqs
     a.sel = d_sel;
     a.n_sel = d_sel ? n_sel : 0;
     a.qscale = sm_scale * kLog2e;
+    a.q_raw = q_raw;
+    a.q_dtype = q_dtype;
     a.ws_m = reinterpret_cast<float*>(ws + w.m_off);
     a.ws_z = reinterpret_cast<float*>(ws + w.z_off);
     a.ws_acc = reinterpret_cast<float*>(ws + w.acc_off);
@@ -240,6 +244,25 @@ int32_t kvq_decode_attn(const kvq_cache* cache, const float* q, int32_t num_seqs
     e = fp8 ? launch_decode_fp8(a, num_seqs, s) : bf16 ? launch_decode_bf16(a, num_seqs, s) : launch_decode_q4(a, num_seqs, s);
   }
   return e == cudaSuccess ? KVQ_OK : cuda_fail(e);
+}
+
+int32_t kvq_decode_attn(const kvq_cache* cache, const float* q, int32_t num_seqs, int32_t num_q_heads,
+                        const int32_t* d_seq_lens, const int32_t* d_block_tables, int32_t max_pages_per_seq,
+                        int32_t max_seq_len, const int32_t* d_sel, int32_t n_sel, float sm_scale, void* workspace,
+                        size_t ws_bytes, void* stream) {
+  return decode_attn_impl(cache, q, nullptr, 0, num_seqs, num_q_heads, d_seq_lens, d_block_tables,
+                          max_pages_per_seq, max_seq_len, d_sel, n_sel, sm_scale, workspace, ws_bytes, stream);
+}
+
+int32_t kvq_decode_attn_unrotated(const kvq_cache* cache, const void* q, int32_t q_dtype, int32_t num_seqs,
+                                  int32_t num_q_heads, const int32_t* d_seq_lens, const int32_t* d_block_tables,
+                                  int32_t max_pages_per_seq, int32_t max_seq_len, const int32_t* d_sel,
+                                  int32_t n_sel, float sm_scale, void* workspace, size_t ws_bytes, void* stream) {
+  if (!cache || cache->format != KVQ_FMT_Q4_HAD32) return cache ? KVQ_ERR_UNSUPPORTED : KVQ_ERR_INVALID_ARG;
+  if (q_dtype != KVQ_DT_F32 && q_dtype != KVQ_DT_BF16) return KVQ_ERR_INVALID_ARG;
+  if (num_seqs > 0 && !q) return KVQ_ERR_INVALID_ARG;
+  return decode_attn_impl(cache, nullptr, q, q_dtype, num_seqs, num_q_heads, d_seq_lens, d_block_tables,
+                          max_pages_per_seq, max_seq_len, d_sel, n_sel, sm_scale, workspace, ws_bytes, stream);
 }
 
 int32_t kvq_merge(const kvq_cache* cache, const void* workspace, size_t ws_bytes, int32_t num_seqs,

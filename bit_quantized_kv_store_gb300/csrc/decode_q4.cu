@@ -56,6 +56,7 @@ struct Q4Smem {
   Q4Stage stage[kQ4Warps][kQ4Ring];
   uint4 qf[kQ4NG][2][32];  // query fragments [group][hi, lo][lane]
   float2 qbias[kQ4NG][4];  // [group][head pair]: the code offset folded into the score MMA
+  float qrot[8][kQ4D];     // the group's queries rotated in the kernel (unrotated-query entry point)
   uint64_t bar[kQ4Warps][kQ4Ring];
   int poison;
 };
@@ -211,9 +212,40 @@ __global__ void __launch_bounds__(kQ4Warps * 32, kQ4MinBlocks) decode_q4_kernel(
   // group G starts at -bias_G, bias_G = 1024 * sum(B) + 8 * sum(q~) over the
   // group (B the f16 values in the fragments, q~ = B or 16 B), so the MMA
   // returns sum_d q_d (c_d - 8) with the keys' codes used exactly.
+  const float* qsrc = a.q + ((int64_t)b * a.Hq + kvh * a.group) * kQ4D;  // rows of the group's heads
+  if (a.q_raw) {
+    // Rotate the group's queries here, with the arithmetic of the rotation entry
+    // point (fp32 butterfly, stages 1..16, one multiply by fp32(1/sqrt(32))):
+    // warp w takes (head, group) pairs w, w + 4, ..., lane = element.
+    // All loads first (at most 8 heads x 8 groups / 4 warps = 16 per lane), so
+    // their latencies overlap; then the butterflies.
+    constexpr int kPairs = 8 * kQ4NG / kQ4Warps;
+    const int npairs = a.group * kQ4NG;
+    const int64_t qbase = ((int64_t)b * a.Hq + kvh * a.group) * kQ4D + lane;
+    float xs[kPairs];
+#pragma unroll
+    for (int k = 0; k < kPairs; ++k) {
+      const int hg = warp + kQ4Warps * k;  // (head, group) = (hg / 8, hg % 8): elements 32 hg .. of the rows
+      xs[k] = 0.f;
+      if (hg < npairs)
+        xs[k] = a.q_dtype == KVQ_DT_F32
+                    ? static_cast<const float*>(a.q_raw)[qbase + 32 * hg]
+                    : __bfloat162float(static_cast<const __nv_bfloat16*>(a.q_raw)[qbase + 32 * hg]);
+    }
+#pragma unroll
+    for (int k = 0; k < kPairs; ++k) {
+      const int hg = warp + kQ4Warps * k;
+      if (hg < npairs) {  // warp-uniform
+        const float x = warp_fwht32(xs[k], lane);
+        (&sm.qrot[0][0])[32 * hg + lane] = __fmul_rn(x, kHadamardScale);
+      }
+    }
+    __syncthreads();
+    qsrc = &sm.qrot[0][0];
+  }
   {
     const bool live = g < a.group;
-    const float* qrow = a.q + ((int64_t)b * a.Hq + kvh * a.group + (live ? g : 0)) * kQ4D;
+    const float* qrow = qsrc + (live ? g : 0) * kQ4D;
     const float s = live ? a.qscale : 0.f;
     const float s16 = s * 0.0625f;
     for (int G = warp; G < kQ4NG; G += kQ4Warps) {  // warp w prepares groups w, w + kQ4Warps, ...

@@ -23,6 +23,9 @@ struct DecodeArgs {
   const int32_t* sel;  // NULL: dense
   int n_sel;
   float qscale;  // sm_scale * log2(e)
+  const void* q_raw;  // 4-bit format only: unrotated query [B, Hq, 256] of q_dtype, rotated in
+                      // the kernel (then q is unused); NULL: q is already rotated
+  int q_dtype;
   float* ws_m;
   float* ws_z;
   float* ws_acc;

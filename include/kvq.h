@@ -160,11 +160,26 @@ size_t kvq_decode_workspace_size(const kvq_cache* cache, int32_t num_seqs, int32
  *   d_sel: NULL for dense attention, else device int32 [num_seqs, n_sel] absolute
  *       positions, each < seq_lens[b] (gather; n_sel <= 4096, [P3] split-T commit).
  *   Q4 / BF16 need num_q_heads / num_kv_heads <= 8 and head_dim == 256.
- *   FP8_ROW needs head_dim == 512, rope_dim == 64 and num_q_heads % 64 == 0. */
+ *   FP8_ROW needs head_dim == 512, rope_dim == 64 and num_q_heads % 16 == 0. */
 int32_t kvq_decode_attn(const kvq_cache* cache, const float* q, int32_t num_seqs, int32_t num_q_heads,
                         const int32_t* d_seq_lens, const int32_t* d_block_tables, int32_t max_pages_per_seq,
                         int32_t max_seq_len, const int32_t* d_sel, int32_t n_sel, float sm_scale,
                         void* workspace, size_t ws_bytes, void* stream);
+
+/* kvq_decode_attn_unrotated -- kvq_decode_attn for the 4-bit format with the
+ * query rotation done inside the decode kernel ([P1] "What it is": the query
+ * is rotated once, then the 4-bit cache is streamed in rotated space), saving the
+ * separate kvq_rotate_query launch of a decode step.
+ *   q: device [num_seqs, num_q_heads, 256] of q_dtype (KVQ_DT_F32 or KVQ_DT_BF16),
+ *      unrotated.  Each CTA rotates the queries of its GQA group with the
+ *      arithmetic of kvq_rotate_query, so the partials equal those of
+ *      kvq_rotate_query + kvq_decode_attn bit for bit.
+ * Other arguments, workspace and errors as for kvq_decode_attn; formats other
+ * than Q4_HAD32 return KVQ_ERR_UNSUPPORTED. */
+int32_t kvq_decode_attn_unrotated(const kvq_cache* cache, const void* q, int32_t q_dtype, int32_t num_seqs,
+                                  int32_t num_q_heads, const int32_t* d_seq_lens, const int32_t* d_block_tables,
+                                  int32_t max_pages_per_seq, int32_t max_seq_len, const int32_t* d_sel,
+                                  int32_t n_sel, float sm_scale, void* workspace, size_t ws_bytes, void* stream);
 
 /* kvq_merge -- log-sum-exp merge of the partials ([P1] "in-order merge ... and
  * rotate the output back once"; [P3] split-T commit: merge kernel):

@@ -275,6 +275,27 @@ def test_decode_concurrent_equals_solo_and_deterministic(K):
         assert np.array_equal(solo[0], out[b])
 
 
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+@pytest.mark.parametrize("Hk,Hq", [(4, 24), (2, 4), (3, 21)])
+def test_decode_unrotated_query_equals_rotate_then_decode(K, dtype, Hk, Hq):
+    """The in-kernel query rotation gives the same partials, bit for bit (dense and gathered)."""
+    lens = [1500, 700]
+    g, o, bt, q, ml = decode_case(K, lens, Hk=Hk, Hq=Hq, seed=500 + Hq, dtype=dtype)
+    qd = q.to(DEV)
+    seq = torch.tensor(lens, dtype=torch.int32, device=DEV)
+    btd = torch.from_numpy(bt).to(DEV)
+    sel = torch.from_numpy(np.stack([synth.distinct_sorted(300, L, 5, b).numpy() for b, L in enumerate(lens)])
+                           .astype(np.int32)).to(DEV)
+    for s_ in (None, sel):
+        n_sel = 0 if s_ is None else s_.shape[1]
+        ws1 = K.alloc_workspace(g, 2, Hq, ml, n_sel, device=DEV)
+        ws2 = K.alloc_workspace(g, 2, Hq, ml, n_sel, device=DEV)
+        K.decode_attn(g, K.rotate_query(qd), seq, btd, ml, 1 / 16, ws1, sel=s_)
+        K.decode_attn_unrotated(g, qd, seq, btd, ml, 1 / 16, ws2, sel=s_)
+        torch.cuda.synchronize()
+        assert torch.equal(ws1.view(torch.int32), ws2.view(torch.int32))
+
+
 def test_decode_gather(K):
     lens = [3000, 1800]
     g, o, bt, q, ml = decode_case(K, lens, seed=21)
