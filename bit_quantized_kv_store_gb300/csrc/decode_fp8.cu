@@ -10,26 +10,25 @@
 // 4096 absolute indices splits into the same partials).
 //
 // GB300 design.  One CTA per (block of 32 query heads, partition of 512 tokens,
-// sequence): 8 MMA warps and one producer warp.  Tokens stream in tiles of 64
-// through a 2-stage shared-memory ring.  Dense tiles arrive by 2-D TMA: the
-// latent codes as four 128-byte column boxes of 16 rows with the 128-byte
-// swizzle, the rope codes as one 64-byte box with the 64-byte swizzle, the
-// scales by 1-D bulk copies.  Gathered tiles arrive row by row (1-D bulk copies
-// into rows padded to 528 / 80 bytes; scales by plain loads).
-//  * Scores: heads on M (two 16-head blocks), tokens on N, the 576 dims on K.
-//    The codes convert exactly to f16 (cvt of two e4m3 at once); the query is
-//    split into f16 high and low parts (~22 bits) and stays in shared memory
-//    in a permuted dim order, so that each lane's four code bytes of a k-step
-//    are one 32-bit load.  Latent and rope dot products accumulate separately
-//    and take their row scales in fp32.
+// sequence): 8 MMA warps and one producer warp.  Tokens arrive in tiles of 64
+// into one raw stage: dense tiles by 2-D TMA (the latent codes as four 128-byte
+// column boxes of 16 rows with the 128-byte swizzle, the rope codes as one
+// 64-byte box with the 64-byte swizzle, the scales by 1-D bulk copies);
+// gathered tiles row by row (1-D bulk copies into rows padded to 528 / 80
+// bytes; scales by plain loads).
+//  * The 8 MMA warps convert the tile once into an f16 tile in shared memory
+//    (cvt of two e4m3 at once, exact; rows past the end become zeros), which
+//    frees the raw stage for the next tile's copy while the MMAs run.
+//  * Scores: heads on M (two 16-head blocks), tokens on N, the 576 dims on K;
+//    A = the query split into f16 high and low parts (~22 bits) by ldmatrix,
+//    B = the f16 tile by ldmatrix.  Latent and rope dot products accumulate
+//    separately and take their row scales in fp32.
 //  * Softmax: a warp holds 16 tokens of 16 heads; row maxima over the tile's 64
 //    tokens meet in shared memory; base-2 online softmax with running m per
 //    head, partial z per warp.
-//  * Context: P' = f16(p * Lsc) (shared memory) times the exact latent codes;
-//    warp w owns output dims 64w .. 64w+63 for all 32 heads (64 f32
-//    accumulators per thread); each lane reads 8 contiguous code bytes of a
-//    token and builds the B fragments of 8 n-blocks from them (dim of n-block
-//    nb, column n = 64w + 8n + nb).
+//  * Context: P' = f16(p * Lsc) (shared memory, A by ldmatrix) times the exact
+//    latent values (B by ldmatrix.trans from the same f16 tile); warp w owns
+//    output dims 64w .. 64w+63 for all 32 heads (64 f32 accumulators per thread).
 #include <cuda_fp8.h>
 
 #include "kernels.cuh"
@@ -46,6 +45,7 @@ constexpr int kF8QStride = kF8W * 2 + 16;     // bytes per head row of q_hi / q_
 constexpr int kF8PStride = kF8Keys * 2 + 16;  // bytes per head row of P'
 constexpr int kF8GatherL = kF8L + 16;         // padded latent row (gather layout)
 constexpr int kF8GatherR = kF8R + 16;         // padded rope row (gather layout)
+constexpr int kF8TStride = kF8W * 2 + 16;     // bytes per token row of the f16 tile (padded)
 
 struct __align__(1024) F8Stage {
   // dense: [4 column boxes][64 rows][128 B], 128-byte swizzled; gather: [64 rows][528 B]
@@ -57,14 +57,15 @@ struct __align__(1024) F8Stage {
 };
 
 struct F8Smem {
-  F8Stage stage[2];
+  F8Stage raw;
+  uint8_t kf[kF8Keys * kF8TStride];  // the tile as f16: [token][576 values], natural order
   uint8_t qhi[kF8Heads * kF8QStride];
   uint8_t qlo[kF8Heads * kF8QStride];
   uint8_t p[kF8Heads * kF8PStride];
   float red[4][kF8Heads];   // per token quarter: tile row maxima
   float corr[kF8Heads];     // per head: rescale factor of this tile
   float zred[4][kF8Heads];  // end: partial z per token quarter
-  uint64_t full[2], empty[2];
+  uint64_t full, empty;
   int poison;
   int abort;
 };
@@ -82,6 +83,18 @@ __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r
   asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
                : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
                : "r"(addr));
+}
+
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+
+__device__ __forceinline__ uint4 f8_lds128(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
+  return v;
 }
 
 __device__ __forceinline__ uint32_t f8_lds32(uint32_t addr) {
@@ -156,32 +169,37 @@ __global__ void __launch_bounds__((kF8Warps + 1) * 32, 1) decode_fp8_kernel(cons
   const int ntiles = (k1 - k0 + kF8Keys - 1) / kF8Keys;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < 2; ++s) {
-      mbar_init(&sm.full[s], 32);
-      mbar_init(&sm.empty[s], kF8Warps);
-    }
+    mbar_init(&sm.full, 32);         // the producer's lanes
+    mbar_init(&sm.empty, kF8Warps);  // the MMA warps, once the raw tile is converted
     sm.poison = 0;
     sm.abort = 0;
     fence_barrier_init();
   }
-  // ---- queries: scaled, split, stored in the permuted dim order.  Within the
-  // 16 dims of k-step s, k = 2t + j holds dim 16s + 4t + j and k = 8 + 2t + j
-  // holds dim 16s + 4t + 2 + j (t = 0..3, j = 0, 1).
-  for (int i = threadIdx.x; i < kF8Heads * (kF8W / 2); i += blockDim.x) {
-    const int h = i / (kF8W / 2), kp = i % (kF8W / 2);  // k pair index
-    const int s = kp >> 3, kk = 2 * (kp & 7);          // k-step, first k of the pair
-    const int tt = (kk & 7) >> 1, hi8 = kk >> 3;
-    const int d = 16 * s + 4 * tt + 2 * hi8;
-    float x0 = 0.f, x1 = 0.f;
-    if (head0 + h < a.Hq) {
-      const float* qrow = a.q + ((int64_t)b * a.Hq + head0 + h) * kF8W;
-      x0 = qrow[d] * a.qscale;
-      x1 = qrow[d + 1] * a.qscale;
+  // ---- queries: scaled by sm_scale * log2(e), split into f16 high and low parts.
+  // 32 heads x 144 float4 = 16 per thread; all loads are issued before any use.
+  {
+    constexpr int kUnits = kF8Heads * (kF8W / 4);
+    constexpr int kPer = (kUnits + (kF8Warps + 1) * 32 - 1) / ((kF8Warps + 1) * 32);
+    float4 v[kPer];
+#pragma unroll
+    for (int k = 0; k < kPer; ++k) {
+      const int i = threadIdx.x + k * (kF8Warps + 1) * 32;
+      const int h = i / (kF8W / 4), u = i % (kF8W / 4);
+      v[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (i < kUnits && head0 + h < a.Hq)
+        v[k] = *reinterpret_cast<const float4*>(a.q + ((int64_t)b * a.Hq + head0 + h) * kF8W + 4 * u);
     }
-    uint32_t hi, lo;
-    split_f16(x0, x1, hi, lo);
-    *reinterpret_cast<uint32_t*>(sm.qhi + h * kF8QStride + 2 * (16 * s + kk)) = hi;
-    *reinterpret_cast<uint32_t*>(sm.qlo + h * kF8QStride + 2 * (16 * s + kk)) = lo;
+#pragma unroll
+    for (int k = 0; k < kPer; ++k) {
+      const int i = threadIdx.x + k * (kF8Warps + 1) * 32;
+      if (i >= kUnits) break;
+      const int h = i / (kF8W / 4), u = i % (kF8W / 4);
+      uint2 hi, lo;
+      split_f16(v[k].x * a.qscale, v[k].y * a.qscale, hi.x, lo.x);
+      split_f16(v[k].z * a.qscale, v[k].w * a.qscale, hi.y, lo.y);
+      *reinterpret_cast<uint2*>(sm.qhi + h * kF8QStride + 8 * u) = hi;
+      *reinterpret_cast<uint2*>(sm.qlo + h * kF8QStride + 8 * u) = lo;
+    }
   }
   __syncthreads();
 
@@ -190,10 +208,9 @@ __global__ void __launch_bounds__((kF8Warps + 1) * 32, 1) decode_fp8_kernel(cons
     const int32_t* bt = a.block_tables + (int64_t)b * a.max_pages;
     const int32_t Tseq = GATHER ? a.seq_lens[b] : T;
     bool bad = false;
+    F8Stage& st = sm.raw;
     for (int j = 0; j < ntiles; ++j) {
-      const int s = j & 1;
-      if (j >= 2 && !f8_wait(sm, &sm.empty[s], ((j >> 1) - 1) & 1)) break;
-      F8Stage& st = sm.stage[s];
+      if (j >= 1 && !f8_wait(sm, &sm.empty, (j - 1) & 1)) break;  // tile j - 1 converted
       const int key0 = k0 + j * kF8Keys;
       const int nvalid = min(kF8Keys, k1 - key0);
       if (!GATHER) {
@@ -211,15 +228,15 @@ __global__ void __launch_bounds__((kF8Warps + 1) * 32, 1) decode_fp8_kernel(cons
             bytes = 4 * 16 * 128 + 16 * 64 + 2 * 16 * 4;
           }
         }
-        mbar_arrive_expect_tx(&sm.full[s], bytes);
+        mbar_arrive_expect_tx(&sm.full, bytes);
         if (row0 >= 0) {
           const int r = 16 * lane;
 #pragma unroll
           for (int x = 0; x < 4; ++x)
-            f8_tma_2d(st.lc + x * (kF8Keys * 128) + r * 128, &a.tm_k, 128 * x, static_cast<int>(row0), &sm.full[s]);
-          f8_tma_2d(st.rc + r * 64, &a.tm_v, 0, static_cast<int>(row0), &sm.full[s]);
-          bulk_g2s(st.lsc + r, static_cast<const float*>(c.k_scale) + row0, 64, &sm.full[s]);
-          bulk_g2s(st.rsc + r, static_cast<const float*>(c.v_scale) + row0, 64, &sm.full[s]);
+            f8_tma_2d(st.lc + x * (kF8Keys * 128) + r * 128, &a.tm_k, 128 * x, static_cast<int>(row0), &sm.full);
+          f8_tma_2d(st.rc + r * 64, &a.tm_v, 0, static_cast<int>(row0), &sm.full);
+          bulk_g2s(st.lsc + r, static_cast<const float*>(c.k_scale) + row0, 64, &sm.full);
+          bulk_g2s(st.rsc + r, static_cast<const float*>(c.v_scale) + row0, 64, &sm.full);
         }
       } else {
         // each lane: tokens lane and lane + 32 of the tile
@@ -230,13 +247,12 @@ __global__ void __launch_bounds__((kF8Warps + 1) * 32, 1) decode_fp8_kernel(cons
           const int r = lane + 32 * u;
           if (r >= nvalid) continue;
           const int32_t pos = a.sel[(int64_t)b * a.n_sel + key0 + r];
-          int32_t page = -1;
           if (pos < 0 || pos >= Tseq) {
             set_status(a.status, KVQ_DEV_BAD_INDEX);
             bad = true;
             continue;
           }
-          page = bt[pos / c.page_size];
+          const int32_t page = bt[pos / c.page_size];
           if (page < 0 || page >= c.num_pages) {
             set_status(a.status, KVQ_DEV_BAD_PAGE);
             bad = true;
@@ -252,13 +268,13 @@ __global__ void __launch_bounds__((kF8Warps + 1) * 32, 1) decode_fp8_kernel(cons
           st.lsc[r] = rows[u] >= 0 ? static_cast<const float*>(c.k_scale)[rows[u]] : 0.f;
           st.rsc[r] = rows[u] >= 0 ? static_cast<const float*>(c.v_scale)[rows[u]] : 0.f;
         }
-        mbar_arrive_expect_tx(&sm.full[s], bytes);  // release orders the scale stores
+        mbar_arrive_expect_tx(&sm.full, bytes);  // release orders the scale stores
 #pragma unroll
         for (int u = 0; u < 2; ++u) {
           if (rows[u] < 0) continue;
           const int r = lane + 32 * u;
-          bulk_g2s(st.lc + r * kF8GatherL, static_cast<const uint8_t*>(c.k) + rows[u] * kF8L, kF8L, &sm.full[s]);
-          bulk_g2s(st.rc + r * kF8GatherR, static_cast<const uint8_t*>(c.v) + rows[u] * kF8R, kF8R, &sm.full[s]);
+          bulk_g2s(st.lc + r * kF8GatherL, static_cast<const uint8_t*>(c.k) + rows[u] * kF8L, kF8L, &sm.full);
+          bulk_g2s(st.rc + r * kF8GatherR, static_cast<const uint8_t*>(c.v) + rows[u] * kF8R, kF8R, &sm.full);
         }
       }
     }
@@ -268,12 +284,19 @@ __global__ void __launch_bounds__((kF8Warps + 1) * 32, 1) decode_fp8_kernel(cons
     const int mb = warp & 1;   // head block of the scores
     const int nq = warp >> 1;  // token quarter of the scores: tokens 16 nq .. 16 nq + 15
     const uint32_t qhi_a = smem_u32(sm.qhi), qlo_a = smem_u32(sm.qlo), p_a = smem_u32(sm.p);
-    // ldmatrix row addresses: matrix lane / 8 (rows 0-7 / 8-15, k-chunk 0 / 1), row lane % 8
+    const uint32_t kf_a = smem_u32(sm.kf);
+    const uint32_t lc_a = smem_u32(sm.raw.lc), rc_a = smem_u32(sm.raw.rc);
+    // ldmatrix row addresses.  A (queries, P'): matrix lane / 8 = (rows 0-7 / 8-15) x
+    // (k-chunk 0 / 1).  B of the scores (tile rows = tokens): (tokens 0-7, chunk 0),
+    // (0-7, chunk 1), (8-15, chunk 0), (8-15, chunk 1).  B of the context (.trans):
+    // (tokens 0-7, dims +0), (8-15, +0), (0-7, +8), (8-15, +8).
     const int lrow = (lane & 7) + 8 * ((lane >> 3) & 1), lchunk = lane >> 4;
     const uint32_t q_lane = (mb * 16 + lrow) * kF8QStride + 16 * lchunk;
+    const uint32_t ks_lane = kf_a + (16 * nq + (lane & 7) + 8 * (lane >> 4)) * kF8TStride + 16 * ((lane >> 3) & 1);
+    const uint32_t kv_lane = kf_a + ((lane & 7) + 8 * ((lane >> 3) & 1)) * kF8TStride + 16 * (8 * warp + (lane >> 4));
     float m_run[2] = {-INFINITY, -INFINITY};  // heads mb*16 + g, + 8
     float z_part[2] = {0.f, 0.f};
-    float acc[2][8][4];  // [head block][n-block][C fragment]: dims 64 warp + 8 n + nb
+    float acc[2][8][4];  // [head block][n-block][C fragment]: dims 64 warp + 8 nb + 2t, + 1
 #pragma unroll
     for (int x = 0; x < 2; ++x)
 #pragma unroll
@@ -282,12 +305,45 @@ __global__ void __launch_bounds__((kF8Warps + 1) * 32, 1) decode_fp8_kernel(cons
         for (int i = 0; i < 4; ++i) acc[x][n][i] = 0.f;
 
     for (int j = 0; j < ntiles; ++j) {
-      const int s = j & 1;
-      f8_wait(sm, &sm.full[s], (j >> 1) & 1);
-      const F8Stage& st = sm.stage[s];
-      const uint32_t lc_a = smem_u32(st.lc), rc_a = smem_u32(st.rc);
+      f8_wait(sm, &sm.full, j & 1);
       const int key0 = k0 + j * kF8Keys;
       const int nvalid = min(kF8Keys, k1 - key0);
+      consumers_sync();  // every warp is done with the previous tile's f16 values
+
+      // ---------------- convert the raw tile to f16 (rows past the end: zeros)
+      static_assert(kF8Keys * (kF8W / 16) % (kF8Warps * 32) == 0, "conversion chunks per thread");
+#pragma unroll
+      for (int k = 0; k < kF8Keys * (kF8W / 16) / (kF8Warps * 32); ++k) {
+        const int idx = threadIdx.x + k * (kF8Warps * 32);
+        const int r = idx / (kF8W / 16), cchunk = idx % (kF8W / 16);  // 16 codes
+        uint4 w = make_uint4(0, 0, 0, 0);
+        if (r < nvalid)
+          w = f8_lds128(cchunk < kF8L / 16 ? lc_a + lc_off<GATHER>(r, 16 * cchunk)
+                                           : rc_a + rc_off<GATHER>(r, 16 * (cchunk - kF8L / 16)));
+        const uint4 h0 = make_uint4(e4m3x2_to_h2(w.x), e4m3x2_to_h2(w.x >> 16), e4m3x2_to_h2(w.y),
+                                    e4m3x2_to_h2(w.y >> 16));
+        const uint4 h1 = make_uint4(e4m3x2_to_h2(w.z), e4m3x2_to_h2(w.z >> 16), e4m3x2_to_h2(w.w),
+                                    e4m3x2_to_h2(w.w >> 16));
+        uint8_t* dst = sm.kf + r * kF8TStride + 32 * cchunk;
+        *reinterpret_cast<uint4*>(dst) = h0;
+        *reinterpret_cast<uint4*>(dst + 16) = h1;
+      }
+      // the scales of this warp's score columns, read before the raw stage is released
+      float ls[2][2], rs[2][2];  // [f][token 2t, 2t + 1]
+#pragma unroll
+      for (int f = 0; f < 2; ++f) {
+        const int kc = 16 * nq + 8 * f + 2 * t;
+        const float2 l2 = *reinterpret_cast<const float2*>(&sm.raw.lsc[kc]);
+        const float2 r2 = *reinterpret_cast<const float2*>(&sm.raw.rsc[kc]);
+        // rows past the end hold stale or unwritten bytes: their P' must be an exact 0
+        ls[f][0] = kc < nvalid ? l2.x : 0.f;
+        ls[f][1] = kc + 1 < nvalid ? l2.y : 0.f;
+        rs[f][0] = kc < nvalid ? r2.x : 0.f;
+        rs[f][1] = kc + 1 < nvalid ? r2.y : 0.f;
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sm.empty);  // the raw stage may be refilled
+      consumers_sync();                       // the f16 tile is complete
 
       // ---------------- scores for tokens 16 nq + 8 f + n, f = 0, 1
       float cl[2][2][4], cr[2][2][4];  // [f][hi/lo][C]
@@ -297,30 +353,23 @@ __global__ void __launch_bounds__((kF8Warps + 1) * 32, 1) decode_fp8_kernel(cons
         for (int u = 0; u < 2; ++u)
 #pragma unroll
           for (int i = 0; i < 4; ++i) cl[f][u][i] = cr[f][u][i] = 0.f;
-      const int kr0 = 16 * nq + g, kr1 = kr0 + 8;  // the B-fragment token rows of this lane
 #pragma unroll 4
       for (int ks = 0; ks < kF8L / 16; ++ks) {
-        uint32_t ah0, ah1, ah2, ah3, al0, al1, al2, al3;
+        uint32_t ah0, ah1, ah2, ah3, al0, al1, al2, al3, b00, b01, b10, b11;
         ldsm_x4(qhi_a + q_lane + 32 * ks, ah0, ah1, ah2, ah3);
         ldsm_x4(qlo_a + q_lane + 32 * ks, al0, al1, al2, al3);
-        const uint32_t w0 = f8_lds32(lc_a + lc_off<GATHER>(kr0, 16 * ks + 4 * t));
-        const uint32_t w1 = f8_lds32(lc_a + lc_off<GATHER>(kr1, 16 * ks + 4 * t));
-        const uint32_t b00 = e4m3x2_to_h2(w0), b01 = e4m3x2_to_h2(w0 >> 16);
-        const uint32_t b10 = e4m3x2_to_h2(w1), b11 = e4m3x2_to_h2(w1 >> 16);
+        ldsm_x4(ks_lane + 32 * ks, b00, b01, b10, b11);
         mma_f16(cl[0][0], ah0, ah1, ah2, ah3, b00, b01);
         mma_f16(cl[0][1], al0, al1, al2, al3, b00, b01);
         mma_f16(cl[1][0], ah0, ah1, ah2, ah3, b10, b11);
         mma_f16(cl[1][1], al0, al1, al2, al3, b10, b11);
       }
 #pragma unroll
-      for (int ks = 0; ks < kF8R / 16; ++ks) {
-        uint32_t ah0, ah1, ah2, ah3, al0, al1, al2, al3;
-        ldsm_x4(qhi_a + q_lane + 32 * (kF8L / 16 + ks), ah0, ah1, ah2, ah3);
-        ldsm_x4(qlo_a + q_lane + 32 * (kF8L / 16 + ks), al0, al1, al2, al3);
-        const uint32_t w0 = f8_lds32(rc_a + rc_off<GATHER>(kr0, 16 * ks + 4 * t));
-        const uint32_t w1 = f8_lds32(rc_a + rc_off<GATHER>(kr1, 16 * ks + 4 * t));
-        const uint32_t b00 = e4m3x2_to_h2(w0), b01 = e4m3x2_to_h2(w0 >> 16);
-        const uint32_t b10 = e4m3x2_to_h2(w1), b11 = e4m3x2_to_h2(w1 >> 16);
+      for (int ks = kF8L / 16; ks < kF8W / 16; ++ks) {
+        uint32_t ah0, ah1, ah2, ah3, al0, al1, al2, al3, b00, b01, b10, b11;
+        ldsm_x4(qhi_a + q_lane + 32 * ks, ah0, ah1, ah2, ah3);
+        ldsm_x4(qlo_a + q_lane + 32 * ks, al0, al1, al2, al3);
+        ldsm_x4(ks_lane + 32 * ks, b00, b01, b10, b11);
         mma_f16(cr[0][0], ah0, ah1, ah2, ah3, b00, b01);
         mma_f16(cr[0][1], al0, al1, al2, al3, b00, b01);
         mma_f16(cr[1][0], ah0, ah1, ah2, ah3, b10, b11);
@@ -328,21 +377,14 @@ __global__ void __launch_bounds__((kF8Warps + 1) * 32, 1) decode_fp8_kernel(cons
       }
       // C fragment of (f): rows (heads) g, g + 8; columns (tokens) 16 nq + 8 f + 2t, + 1
       float sc[2][4];
-      float lsc[2][2];  // [f][token 2t, 2t+1]
 #pragma unroll
       for (int f = 0; f < 2; ++f) {
         const int kc = 16 * nq + 8 * f + 2 * t;
-        const float2 ls = *reinterpret_cast<const float2*>(&st.lsc[kc]);
-        const float2 rs = *reinterpret_cast<const float2*>(&st.rsc[kc]);
-        // rows past the end hold stale or unwritten bytes: their P' must be an exact 0
-        lsc[f][0] = kc < nvalid ? ls.x : 0.f;
-        lsc[f][1] = kc + 1 < nvalid ? ls.y : 0.f;
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           const float l = cl[f][0][i] + cl[f][1][i], r = cr[f][0][i] + cr[f][1][i];
-          const int kcol = kc + (i & 1);
-          float v = fmaf((i & 1) ? ls.y : ls.x, l, ((i & 1) ? rs.y : rs.x) * r);
-          if (kcol >= nvalid) v = -INFINITY;
+          float v = fmaf(ls[f][i & 1], l, rs[f][i & 1] * r);
+          if (kc + (i & 1) >= nvalid) v = -INFINITY;
           sc[f][i] = v;
         }
       }
@@ -378,9 +420,9 @@ __global__ void __launch_bounds__((kF8Warps + 1) * 32, 1) decode_fp8_kernel(cons
         zs1 += p2 + p3;
         const int kc = 16 * nq + 8 * f + 2 * t;
         *reinterpret_cast<uint32_t*>(sm.p + (mb * 16 + g) * kF8PStride + 2 * kc) =
-            pack_half2(p0 * lsc[f][0], p1 * lsc[f][1]);
+            pack_half2(p0 * ls[f][0], p1 * ls[f][1]);
         *reinterpret_cast<uint32_t*>(sm.p + (mb * 16 + g + 8) * kF8PStride + 2 * kc) =
-            pack_half2(p2 * lsc[f][0], p3 * lsc[f][1]);
+            pack_half2(p2 * ls[f][0], p3 * ls[f][1]);
       }
       z_part[0] = fmaf(z_part[0], c0, zs0);
       z_part[1] = fmaf(z_part[1], c1, zs1);
@@ -390,7 +432,7 @@ __global__ void __launch_bounds__((kF8Warps + 1) * 32, 1) decode_fp8_kernel(cons
       }
       consumers_sync();
 
-      // ---------------- context: O[32 heads][dims 64 warp ..] += P' . Lc
+      // ---------------- context: O[32 heads][dims 64 warp ..] += P' . latent
       {
         float cf[2][2];  // [head block][row g / g + 8]
 #pragma unroll
@@ -411,35 +453,21 @@ __global__ void __launch_bounds__((kF8Warps + 1) * 32, 1) decode_fp8_kernel(cons
             }
         }
       }
-      const int dbase = 64 * warp + 8 * g;  // this lane's 8 latent bytes of a token
 #pragma unroll
       for (int ks = 0; ks < kF8Keys / 16; ++ks) {
         uint32_t a0[4], a1[4];
         ldsm_x4(p_a + (0 * 16 + lrow) * kF8PStride + 16 * (2 * ks + lchunk), a0[0], a0[1], a0[2], a0[3]);
         ldsm_x4(p_a + (1 * 16 + lrow) * kF8PStride + 16 * (2 * ks + lchunk), a1[0], a1[1], a1[2], a1[3]);
-        const int r0 = 16 * ks + 2 * t;
-        uint2 v0 = f8_lds64(lc_a + lc_off<GATHER>(r0, dbase));
-        uint2 v1 = f8_lds64(lc_a + lc_off<GATHER>(r0 + 1, dbase));
-        uint2 v2 = f8_lds64(lc_a + lc_off<GATHER>(r0 + 8, dbase));
-        uint2 v3 = f8_lds64(lc_a + lc_off<GATHER>(r0 + 9, dbase));
-        if (nvalid < kF8Keys) {  // tail tile: stale code bytes (possibly NaN codes) must not meet P' = 0
-          if (r0 >= nvalid) v0 = make_uint2(0, 0);
-          if (r0 + 1 >= nvalid) v1 = make_uint2(0, 0);
-          if (r0 + 8 >= nvalid) v2 = make_uint2(0, 0);
-          if (r0 + 9 >= nvalid) v3 = make_uint2(0, 0);
-        }
 #pragma unroll
-        for (int nb = 0; nb < 8; ++nb) {
-          const uint32_t sel = (nb & 3) | ((4 + (nb & 3)) << 4);
-          const uint32_t lo = (nb < 4) ? prmt(v0.x, v1.x, sel) : prmt(v0.y, v1.y, sel);
-          const uint32_t hi = (nb < 4) ? prmt(v2.x, v3.x, sel) : prmt(v2.y, v3.y, sel);
-          const uint32_t b0 = e4m3x2_to_h2(lo), b1 = e4m3x2_to_h2(hi);
+        for (int nb = 0; nb < 8; nb += 2) {
+          uint32_t b0, b1, b2, b3;  // (n-block nb: tokens 0-7, 8-15), (n-block nb + 1: tokens 0-7, 8-15)
+          ldsm_x4_t(kv_lane + 16 * ks * kF8TStride + 16 * nb, b0, b1, b2, b3);
           mma_f16(acc[0][nb], a0[0], a0[1], a0[2], a0[3], b0, b1);
           mma_f16(acc[1][nb], a1[0], a1[1], a1[2], a1[3], b0, b1);
+          mma_f16(acc[0][nb + 1], a0[0], a0[1], a0[2], a0[3], b2, b3);
+          mma_f16(acc[1][nb + 1], a1[0], a1[1], a1[2], a1[3], b2, b3);
         }
       }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&sm.empty[s]);
     }
 
     pdl_trigger();
@@ -462,13 +490,11 @@ __global__ void __launch_bounds__((kF8Warps + 1) * 32, 1) decode_fp8_kernel(cons
         const int hl = x * 16 + g + 8 * hr;
         if (head0 + hl >= a.Hq) continue;
         const int64_t pi = ((int64_t)b * a.Hq + head0 + hl) * a.P + p;
-        float* dst = a.ws_acc + pi * kF8L;
+        float* dst = a.ws_acc + pi * kF8L + 64 * warp + 2 * t;
 #pragma unroll
-        for (int nb = 0; nb < 8; ++nb) {
-          // columns n = 2t, 2t + 1 of n-block nb: dims 64 warp + 8n + nb
-          dst[64 * warp + 8 * (2 * t) + nb] = bad ? NAN : acc[x][nb][2 * hr];
-          dst[64 * warp + 8 * (2 * t + 1) + nb] = bad ? NAN : acc[x][nb][2 * hr + 1];
-        }
+        for (int nb = 0; nb < 8; ++nb)
+          *reinterpret_cast<float2*>(dst + 8 * nb) =
+              bad ? make_float2(NAN, NAN) : make_float2(acc[x][nb][2 * hr], acc[x][nb][2 * hr + 1]);
         if (warp < 2 && t == 0 && x == mb) {
           // the m of a head is the same in the four warps of its block
           a.ws_m[pi] = bad ? NAN : m_run[hr];
