@@ -2,9 +2,8 @@
 
 One step = one new token through 16 attention layers: per layer, store the
 token's K/V rows (4 KV heads, head_dim 256) into the 4-bit cache, rotate the
-24 query heads and split-T decode over T = context + 1 keys (512-key partitions
-plus the tail) in one kernel (kvq_decode_attn_unrotated), then the log-sum-exp
-merge and rotation back: 3 kernels per layer, captured in a CUDA graph.  The main line is the
+24 query heads, split-T decode over T = context + 1 keys (512-key partitions
+plus the tail), log-sum-exp merge and rotate back.  The main line is the
 32,768-token context (16 layers, heavy-tailed bf16 data); the 262,144-token
 context is measured in the same run and reported under "long_context".
 
@@ -162,6 +161,7 @@ class Workload:
         self.slot = torch.tensor([context], dtype=torch.int32, device=dev)
         self.seq = torch.tensor([self.T], dtype=torch.int32, device=dev)
         self.bt = torch.arange(self.n_pages, dtype=torch.int32, device=dev).reshape(1, -1)
+        self.qrot = torch.empty((1, HQ, D), dtype=torch.float32, device=dev)
         self.out = torch.empty((LAYERS, 1, HQ, D), dtype=torch.float32, device=dev)
         self.ws = K.alloc_workspace(self.caches[0], 1, HQ, self.T, device=dev)
         self.sm_scale = 1.0 / math.sqrt(D)
@@ -170,8 +170,7 @@ class Workload:
     def decode_only(self):
         """The 16 layers' decode launches alone (for the per-launch timing)."""
         for layer in range(LAYERS):
-            self.K.decode_attn_unrotated(self.caches[layer], self.q[0][layer], self.seq, self.bt, self.T,
-                                         self.sm_scale, self.ws)
+            self.K.decode_attn(self.caches[layer], self.qrot, self.seq, self.bt, self.T, self.sm_scale, self.ws)
 
     def step(self, i, ev=None, new_k=None, new_v=None, q=None, out=None):
         """One token through the 16 layers; ev = list of (start, end) events per decode."""
@@ -183,14 +182,14 @@ class Workload:
         for layer in range(LAYERS):
             c = self.caches[layer]
             K.store(c, new_k[layer], new_v[layer], self.slot)
+            K.rotate_query(q[layer], out=self.qrot)
             if ev is not None:
                 ev[layer][0].record()
-            # the query rotation runs inside the decode kernel (kvq_decode_attn_unrotated)
-            K.decode_attn_unrotated(c, q[layer], self.seq, self.bt, self.T, self.sm_scale, self.ws)
+            K.decode_attn(c, self.qrot, self.seq, self.bt, self.T, self.sm_scale, self.ws)
             if ev is not None:
                 ev[layer][1].record()
             K.merge(c, self.ws, 1, HQ, self.seq, self.T, out[layer])
-        return 3 * LAYERS   # kernels launched: store, decode (with the query rotation), merge
+        return 4 * LAYERS   # kernels launched
 
 
 def capture(torch, fn):
@@ -234,7 +233,7 @@ def time_device(W, steps, warmup, torch):
     d1.record()
     torch.cuda.synchronize()
     dec_avg_ms = d0.elapsed_time(d1) / (steps * LAYERS)
-    return total_ms, dec_avg_ms, 3 * LAYERS * steps, graphs
+    return total_ms, dec_avg_ms, 4 * LAYERS * steps, graphs
 
 
 def time_e2e(W, steps, warmup, torch, graphs):
@@ -376,16 +375,18 @@ def _row_batched(K, synth, torch, dev, peak, seed):
     new_slots = torch.tensor([int(bt[i][lens[i] // PS]) * PS + lens[i] % PS for i in range(32)], dtype=torch.int32,
                              device=dev)
     seq = torch.tensor(T, dtype=torch.int32, device=dev)
+    qrot = torch.empty((32, HQ, D), dtype=torch.float32, device=dev)
     o = torch.empty((32, HQ, D), dtype=torch.float32, device=dev)
     ws = K.alloc_workspace(c, 32, HQ, max(T), device=dev)
 
     def batched_step():
         K.store(c, new_k, new_v, new_slots)
-        K.decode_attn_unrotated(c, q, seq, bt, max(T), 1 / 16, ws)
+        K.rotate_query(q, out=qrot)
+        K.decode_attn(c, qrot, seq, bt, max(T), 1 / 16, ws)
         K.merge(c, ws, 32, HQ, seq, max(T), o)
 
     ms = _events_time(torch, batched_step, 10)
-    dec_ms = _events_time(torch, lambda: K.decode_attn_unrotated(c, q, seq, bt, max(T), 1 / 16, ws), 10)
+    dec_ms = _events_time(torch, lambda: K.decode_attn(c, qrot, seq, bt, max(T), 1 / 16, ws), 10)
     byts = sum(T) * BYTES_PER_POS_LAYER
     out["batched_paged_decode"] = {
         "workload": "32 sequences, lengths U{1024..65536} (+1 new token each), 16-token pages, shuffled block "

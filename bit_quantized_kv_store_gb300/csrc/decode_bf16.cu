@@ -197,13 +197,20 @@ __global__ void __launch_bounds__(kBfWarps * 32, 1) decode_bf16_kernel(const __g
     const bool live = g < a.group;
     const float* qrow = a.q + ((int64_t)b * a.Hq + kvh * a.group + (live ? g : 0)) * kBfD;
     const float sc = live ? a.qscale : 0.f;
-    for (int s = warp; s < kBfD / 16; s += kBfWarps) {
-      const float2 u0 = *reinterpret_cast<const float2*>(qrow + 16 * s + 2 * t);
-      const float2 u1 = *reinterpret_cast<const float2*>(qrow + 16 * s + 2 * t + 8);
+    constexpr int kSteps = kBfD / 16 / kBfWarps;  // k-steps per warp; all loads issued first
+    float2 u0[kSteps], u1[kSteps];
+#pragma unroll
+    for (int k = 0; k < kSteps; ++k) {
+      const int s = warp + kBfWarps * k;
+      u0[k] = *reinterpret_cast<const float2*>(qrow + 16 * s + 2 * t);
+      u1[k] = *reinterpret_cast<const float2*>(qrow + 16 * s + 2 * t + 8);
+    }
+#pragma unroll
+    for (int k = 0; k < kSteps; ++k) {
       uint4 f;
-      split_bf16(u0.x * sc, u0.y * sc, f.x, f.z);
-      split_bf16(u1.x * sc, u1.y * sc, f.y, f.w);
-      sm.qf[s][lane] = f;
+      split_bf16(u0[k].x * sc, u0[k].y * sc, f.x, f.z);
+      split_bf16(u1[k].x * sc, u1[k].y * sc, f.y, f.w);
+      sm.qf[warp + kBfWarps * k][lane] = f;
     }
   }
   __syncthreads();

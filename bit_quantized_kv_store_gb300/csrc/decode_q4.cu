@@ -248,9 +248,18 @@ __global__ void __launch_bounds__(kQ4Warps * 32, kQ4MinBlocks) decode_q4_kernel(
     const float* qrow = qsrc + (live ? g : 0) * kQ4D;
     const float s = live ? a.qscale : 0.f;
     const float s16 = s * 0.0625f;
-    for (int G = warp; G < kQ4NG; G += kQ4Warps) {  // warp w prepares groups w, w + kQ4Warps, ...
-      const float4 u0 = *reinterpret_cast<const float4*>(qrow + 32 * G + 8 * t);
-      const float4 u1 = *reinterpret_cast<const float4*>(qrow + 32 * G + 8 * t + 4);
+    constexpr int kGroupsPerWarp = kQ4NG / kQ4Warps;
+    float4 ql0[kGroupsPerWarp], ql1[kGroupsPerWarp];  // all loads issued first
+#pragma unroll
+    for (int k = 0; k < kGroupsPerWarp; ++k) {
+      ql0[k] = *reinterpret_cast<const float4*>(qrow + 32 * (warp + kQ4Warps * k) + 8 * t);
+      ql1[k] = *reinterpret_cast<const float4*>(qrow + 32 * (warp + kQ4Warps * k) + 8 * t + 4);
+    }
+#pragma unroll
+    for (int k = 0; k < kGroupsPerWarp; ++k) {  // warp w prepares groups w, w + kQ4Warps, ...
+      const int G = warp + kQ4Warps * k;
+      const float4 u0 = ql0[k];
+      const float4 u1 = ql1[k];
       uint4 hi, lo;
       // tile (G,0): slots (2t,2t+1) <- d (8t, 8t+2); slots (2t+8, 2t+9) <- d (8t+1, 8t+3); tile (G,1): d + 4
       split_f16(u0.x * s, u0.z * s, hi.x, lo.x);

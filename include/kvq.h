@@ -169,7 +169,10 @@ int32_t kvq_decode_attn(const kvq_cache* cache, const float* q, int32_t num_seqs
 /* kvq_decode_attn_unrotated -- kvq_decode_attn for the 4-bit format with the
  * query rotation done inside the decode kernel ([P1] "What it is": the query
  * is rotated once, then the 4-bit cache is streamed in rotated space), saving the
- * separate kvq_rotate_query launch of a decode step.
+ * separate kvq_rotate_query launch of a decode step.  Every CTA (one per 512-key
+ * partition and KV head) repeats the rotation of its group's queries, so this
+ * pays off for short contexts (few partitions) and costs time at long ones
+ * (measured: -0.15 us per layer at 32K keys, +6 us at 262K keys).
  *   q: device [num_seqs, num_q_heads, 256] of q_dtype (KVQ_DT_F32 or KVQ_DT_BF16),
  *      unrotated.  Each CTA rotates the queries of its GQA group with the
  *      arithmetic of kvq_rotate_query, so the partials equal those of
