@@ -8,25 +8,25 @@
 // rotation.
 //
 // GB300 design: the structure of the 4-bit kernel with bf16 operands fed to
-// mma.m16n8k16 directly.  One CTA (4 warps) per (partition, KV head, sequence);
-// warp w owns keys [128w, 128w + 128) in tiles of 16, streamed through a private
-// 2-stage shared-memory ring: K and V rows (512 B) arrive as four 128-byte
-// column boxes of 16 rows each by 2-D TMA with the 128-byte swizzle (dense), or
-// row by row into 528-byte padded rows (gather).
+// mma.m16n8k16 directly.  One CTA (2 warps, 2 resident per SM) per (partition,
+// KV head, sequence); warp w owns keys [256w, 256w + 256) in tiles of 16,
+// streamed through a private 2-stage shared-memory ring: K and V rows (512 B)
+// arrive as four 128-byte column boxes of 16 rows each by 2-D TMA with the
+// 128-byte swizzle (dense), or row by row into 528-byte padded rows (gather).
 //  * Scores: keys on M (A = K rows by ldmatrix), the <= 8 heads of the GQA group
 //    on N (B = query fragments in shared memory, split into bf16 high and low
 //    parts, ~16 bits); keys enter exactly.
 //  * Context: value dims on M (A = V^T by ldmatrix.trans), heads on N (B = P^T,
 //    transposed in registers by movmatrix, split into bf16 high and low parts).
-//  * Base-2 online softmax per head; the 4 warps' partials are combined in
+//  * Base-2 online softmax per head; the 2 warps' partials are combined in
 //    shared memory.
 #include "kernels.cuh"
 
 namespace kvq {
 
-constexpr int kBfWarps = 4;
+constexpr int kBfWarps = 2;
 constexpr int kBfRing = 2;
-constexpr int kBfTilesPerWarp = kPart / 16 / kBfWarps;  // 8
+constexpr int kBfTilesPerWarp = kPart / 16 / kBfWarps;  // 16
 constexpr int kBfD = 256;
 constexpr int kBfRowG = kBfD * 2 + 16;  // padded row bytes of the gather layout
 
@@ -145,7 +145,7 @@ __device__ __forceinline__ bool bf_issue_tile(const DecodeArgs& a, int b, int kv
 }
 
 template <bool GATHER>
-__global__ void __launch_bounds__(kBfWarps * 32, 1) decode_bf16_kernel(const __grid_constant__ DecodeArgs a) {
+__global__ void __launch_bounds__(kBfWarps * 32, 2) decode_bf16_kernel(const __grid_constant__ DecodeArgs a) {
   pdl_wait();
   extern __shared__ uint8_t smem_raw[];
   BfSmem& sm = *reinterpret_cast<BfSmem*>(smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u));
