@@ -330,6 +330,14 @@ def _events_time(torch, fn, iters, warmup=3):
     return a.elapsed_time(b) / iters
 
 
+def q4_kernel_name(torch, T, n_seqs=1):
+    """The 4-bit decode kernel the library picks for this grid (kvq_set_decode_q4_kernel(0)):
+    the per-warp kernel when partitions x KV heads x sequences fit in one wave of 3 CTAs per SM."""
+    ctas = -(-T // 512) * HK * n_seqs
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    return "decode_q4_warp_kernel" if ctas <= 3 * sms else "decode_q4_round_kernel"
+
+
 def measure_rows(K, synth, torch, dev, peak, tflops_peak, only=None):
     """Batched ragged paged decode, prefill chunk, fp8 latent decode (dense and
     gathered), the bf16-cache comparison and the store, each timed with CUDA
@@ -391,7 +399,8 @@ def _row_batched(K, synth, torch, dev, peak, seed):
     out["batched_paged_decode"] = {
         "workload": "32 sequences, lengths U{1024..65536} (+1 new token each), 16-token pages, shuffled block "
                     "tables, 1 layer, 4 KV / 24 q heads", "us_per_step": ms * 1e3, "decode_kernel_us": dec_ms * 1e3,
-        "cache_bytes": byts, "achieved_GBs": byts / (dec_ms * 1e-3) / 1e9, "frac_of_hbm_peak": byts / (dec_ms * 1e-3) / 1e9 / peak}
+        "cache_bytes": byts, "achieved_GBs": byts / (dec_ms * 1e-3) / 1e9, "frac_of_hbm_peak": byts / (dec_ms * 1e-3) / 1e9 / peak,
+        "kernel": q4_kernel_name(torch, max(T), 32)}
     del c, ws
     torch.cuda.empty_cache()
     return out
@@ -575,7 +584,8 @@ def main():
         long = {"context": args.long_context, "value": ltot * 1e3 / (LAYERS * lsteps * world),
                 "unit": "us/layer-token", "decode_kernel_us": lavg * 1e3,
                 "roofline": {"bound": "hbm", "achieved": lach, "peak": peak, "unit": "GB/s", "frac": lach / peak,
-                             "traffic": None, "bytes_per_launch": lbytes},
+                             "traffic": None, "bytes_per_launch": lbytes,
+                             "kernel": q4_kernel_name(torch, WL.T)},
                 "clocks": clk2.summary()}
         del WL
 
@@ -606,7 +616,8 @@ def main():
                                    f"channels", "l2": "16 layer caches exceed L2 (no flush needed)",
                        "parallelism": f"replicas x{world}"},
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                         "traffic": None, "bytes_per_launch": bytes_per_launch, "kernel": "decode_q4_kernel",
+                         "traffic": None, "bytes_per_launch": bytes_per_launch,
+                         "kernel": q4_kernel_name(torch, args.context + 1),
                          "decode_kernel_us": dec_avg_ms * 1e3, "peak_kind": peak_kind},
             "e2e": {"value": e2e_us, "unit": "us/layer-token", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
             "gpu_launches": launches,
