@@ -562,30 +562,29 @@ __global__ void __launch_bounds__(kQ4Warps * 32, kQ4MinBlocks) decode_q4_warp_ke
 // ---------------------------------------------------------------- round kernel
 namespace q4r {
 
-constexpr int kQ4Warps = 4;      // warps per CTA = tiles per round
-constexpr int kQ4MinBlocks = 4;  // resident CTAs per SM the register budget is sized for
-constexpr int kQ4KStages = 2;    // per-warp K ring (rounds)
-constexpr int kQ4VSlots = 2;     // shared V ring (rounds)
-constexpr int kQ4GPW = kQ4NG / kQ4Warps;  // value groups per warp in P.V (2: a group pair; 1: half of one)
-static_assert(kQ4GPW == 1 || kQ4GPW == 2, "4 or 8 warps");
+constexpr int kQ4Warps = 4;                       // warps per CTA = value group pairs in P.V
+constexpr int kQ4MinBlocks = 4;                   // resident CTAs per SM the register budget is sized for
+constexpr int kQ4TPW = 2;                         // 16-key tiles each warp scores per round
+constexpr int kQ4RoundTiles = kQ4Warps * kQ4TPW;  // 8 tiles = 128 keys per round
 
 struct __align__(1024) Q4Smem {
-  uint8_t kc[kQ4Warps][kQ4KStages][kQ4TileBytes];  // K codes (each tile 1024-byte aligned)
-  uint8_t vc[kQ4VSlots][kQ4Warps][kQ4TileBytes];   // V codes of a round's tiles
-  uint16_t ks[kQ4Warps][kQ4KStages][16 * 8];       // K scales
-  uint16_t vs[kQ4VSlots][kQ4Warps][16 * 8];        // V scales
-  uint4 qf[kQ4NG][2][32];     // query fragments [group][hi, lo][lane]
+  uint8_t kc[kQ4Warps][kQ4TPW][kQ4TileBytes];  // K codes of each warp's tiles of the round (1024-aligned)
+  uint8_t vc[kQ4RoundTiles][kQ4TileBytes];     // V codes of the round's tiles
+  uint16_t ks[kQ4Warps][kQ4TPW][16 * 8];       // K scales
+  uint16_t vs[kQ4RoundTiles][16 * 8];          // V scales
+  uint4 qf[kQ4NG][2][32];                      // query fragments [group][hi, lo][lane]
   float4 qb[kQ4NG][4];        // [group][t]: minus the code-offset bias of heads (2t, 2t+1, 2t, 2t+1)
-  uint2 pb[2][kQ4Warps][32];  // [round parity][tile][lane]: P as B fragments (keys 2t.., 2t+8..)
-  float red[2][kQ4Warps][8];  // [round parity][tile][head]: tile maxima
-  float zs[kQ4Warps][8];      // per-warp sums of the probabilities
-  uint64_t kbar[kQ4Warps][kQ4KStages];
-  uint64_t vbar[kQ4VSlots];
+  uint2 pb[kQ4RoundTiles][32];  // [tile][lane]: P of the round as B fragments (keys 2t.., 2t+8..)
+  float red[kQ4Warps][8];       // [warp][head]: maxima of each warp's tiles of the round
+  float zs[kQ4Warps][8];        // per-warp sums of the probabilities
+  uint64_t kbar[kQ4Warps];      // a warp's K tiles landed (kQ4TPW arrivals)
+  uint64_t vfull;               // the round's V tiles landed (kQ4RoundTiles arrivals)
+  uint64_t vempty;              // every warp is done with the round's V (kQ4Warps arrivals)
   int poison;
 };
-// The unrotated-query entry point rotates the group's queries into V slot 1
-// (8 heads x 256 fp32), which is first filled after the prologue.
-static_assert(sizeof(float) * 8 * kQ4D <= kQ4Warps * kQ4TileBytes, "rotated queries fit V slot 1");
+// The unrotated-query entry point rotates the group's queries (8 heads x 256
+// fp32) into V tiles 0..3, which are first filled after the prologue.
+static_assert(sizeof(float) * 8 * kQ4D <= kQ4RoundTiles / 2 * kQ4TileBytes, "rotated queries fit vc[0..3]");
 
 __device__ __forceinline__ void bar_sync_cta() { asm volatile("bar.sync 1, %0;" ::"n"(kQ4Warps * 32) : "memory"); }
 
@@ -635,6 +634,35 @@ __device__ __forceinline__ bool q4_issue_plane(const DecodeArgs& a, int b, int k
   }
 }
 
+// The calling warp's kQ4TPW tiles of round `rd` of one plane into dc[u], ds[u]
+// (lane 0 issues; every lane takes part in the row shuffles).  A tile past the
+// partition still arrives on `bar`.  Returns true (lane 0) for a bad page/index.
+template <bool GATHER>
+__device__ __forceinline__ bool q4_issue_own(const DecodeArgs& a, int b, int kvh, int k0, int k1, int rd, int warp,
+                                             int lane, int32_t tile_row, const CUtensorMap* map, const void* codes,
+                                             const void* scales, uint8_t (*dc)[kQ4TileBytes], uint16_t (*ds)[16 * 8],
+                                             uint64_t* bar) {
+  const int tile0 = kQ4RoundTiles * rd + kQ4TPW * warp;
+  int32_t rows[kQ4TPW];
+#pragma unroll
+  for (int u = 0; u < kQ4TPW; ++u) rows[u] = __shfl_sync(0xffffffffu, tile_row, (tile0 + u) & 31);
+  bool bad = false;
+  if (lane == 0) {
+    fence_proxy_async();  // the buffers were last read through the generic proxy
+#pragma unroll
+    for (int u = 0; u < kQ4TPW; ++u) {
+      const int key0 = k0 + 16 * (tile0 + u);
+      if (key0 >= k1) {
+        mbar_arrive(bar);
+      } else if (!q4_issue_plane<GATHER>(a, b, kvh, key0, min(16, k1 - key0), rows[u], map, codes, scales, dc[u],
+                                         ds[u], bar)) {
+        bad = true;
+      }
+    }
+  }
+  return bad;
+}
+
 template <bool GATHER>
 __global__ void __launch_bounds__(kQ4Warps * 32, kQ4MinBlocks) decode_q4_round_kernel(const __grid_constant__ DecodeArgs a) {
   pdl_wait();
@@ -660,64 +688,47 @@ __global__ void __launch_bounds__(kQ4Warps * 32, kQ4MinBlocks) decode_q4_round_k
   const int k0 = p * kPart;
   const int k1 = min(k0 + kPart, T);
   const int ntiles = (k1 - k0 + 15) / 16;
-  const int nrounds = (ntiles + kQ4Warps - 1) / kQ4Warps;  // <= 8; warp w's tile of round r: kQ4Warps * r + w
+  const int nrounds = (ntiles + kQ4RoundTiles - 1) / kQ4RoundTiles;  // <= 4
+  // tile u of warp w in round r: kQ4RoundTiles * r + kQ4TPW * w + u
 
-  // Cache row of this warp's tile of round `lane` (its first key), computed once
-  // (the issuing lane then neither waits on a global load nor divides inside
-  // the loop); -1 for a bad page.
-  int32_t my_row = -1;
-  if (!GATHER && lane < nrounds && kQ4Warps * lane + warp < ntiles) {
-    const int key0 = k0 + 16 * (kQ4Warps * lane + warp);
+  // Lane i: the cache row of tile i (its first key), computed once so that the
+  // copies need neither a global load nor a division inside the loop; -1 for a
+  // bad page.
+  int32_t tile_row = -1;
+  if (!GATHER && lane < ntiles) {
+    const int key0 = k0 + 16 * lane;
     const int32_t page = a.block_tables[(int64_t)b * a.max_pages + key0 / a.c.page_size];
-    if (page < 0 || page >= a.c.num_pages)
-      set_status(a.status, KVQ_DEV_BAD_PAGE);
-    else
-      my_row = static_cast<int32_t>(((int64_t)page * a.c.num_kv_heads + kvh) * a.c.page_size + key0 % a.c.page_size);
+    if (page < 0 || page >= a.c.num_pages) {
+      if (warp == 0) set_status(a.status, KVQ_DEV_BAD_PAGE);
+    } else {
+      tile_row = static_cast<int32_t>(((int64_t)page * a.c.num_kv_heads + kvh) * a.c.page_size + key0 % a.c.page_size);
+    }
   }
 
   if (threadIdx.x == 0) {
-    for (int w = 0; w < kQ4Warps; ++w)
-      for (int s = 0; s < kQ4KStages; ++s) mbar_init(&sm.kbar[w][s], 1);
-    for (int s = 0; s < kQ4VSlots; ++s) mbar_init(&sm.vbar[s], kQ4Warps);
+    for (int w = 0; w < kQ4Warps; ++w) mbar_init(&sm.kbar[w], kQ4TPW);
+    mbar_init(&sm.vfull, kQ4RoundTiles);
+    mbar_init(&sm.vempty, kQ4Warps);
     sm.poison = 0;
     fence_barrier_init();
   }
   __syncthreads();
 
   const kvq_cache& c = a.c;
-  bool poisoned = false;
-  {  // first copies: K of rounds 0 .. kQ4KStages-1, V of round 0
-    int32_t pg[kQ4KStages];
-#pragma unroll
-    for (int r = 0; r < kQ4KStages; ++r) pg[r] = __shfl_sync(0xffffffffu, my_row, r);
-    if (lane == 0) {
-      for (int r = 0; r < kQ4KStages; ++r) {
-        const int tile = kQ4Warps * r + warp;
-        if (tile >= ntiles) break;
-        const int key0 = k0 + 16 * tile;
-        if (!q4_issue_plane<GATHER>(a, b, kvh, key0, min(16, k1 - key0), pg[r], &a.tm_k, c.k, c.k_scale,
-                                    sm.kc[warp][r], sm.ks[warp][r], &sm.kbar[warp][r]))
-          poisoned = true;
-      }
-      if (warp < ntiles) {
-        const int key0 = k0 + 16 * warp;
-        if (!q4_issue_plane<GATHER>(a, b, kvh, key0, min(16, k1 - key0), pg[0], &a.tm_v, c.v, c.v_scale,
-                                    sm.vc[0][warp], sm.vs[0][warp], &sm.vbar[0]))
-          poisoned = true;
-      } else {
-        mbar_arrive(&sm.vbar[0]);
-      }
-    }
-  }
+  bool poisoned = q4_issue_own<GATHER>(a, b, kvh, k0, k1, 0, warp, lane, tile_row, &a.tm_k, c.k, c.k_scale,
+                                       sm.kc[warp], sm.ks[warp], &sm.kbar[warp]);
 
-  q4_query_prep<kQ4Warps>(a, b, kvh, warp, lane, reinterpret_cast<float*>(&sm.vc[1][0][0]), sm.qf, sm.qb);
+  q4_query_prep<kQ4Warps>(a, b, kvh, warp, lane, reinterpret_cast<float*>(&sm.vc[0][0]), sm.qf, sm.qb);
+  // V of round 0: vc[0..3] held the rotated queries until the prologue's last barrier
+  poisoned |= q4_issue_own<GATHER>(a, b, kvh, k0, k1, 0, warp, lane, tile_row, &a.tm_v, c.v, c.v_scale,
+                                   &sm.vc[kQ4TPW * warp], &sm.vs[kQ4TPW * warp], &sm.vfull);
   const uint32_t qf_addr = smem_u32(&sm.qf[0][0][lane]);
   const uint32_t qb_addr = smem_u32(&sm.qb[0][t]);
 
-  // P.V accumulators of groups kQ4GPW * w + e, d-tiles (G, 0) and (G, 1)
-  float acc[kQ4GPW][2][4];
+  // P.V accumulators of groups 2w + e, d-tiles (G, 0) and (G, 1)
+  float acc[2][2][4];
 #pragma unroll
-  for (int e = 0; e < kQ4GPW; ++e)
+  for (int e = 0; e < 2; ++e)
 #pragma unroll
     for (int j = 0; j < 2; ++j)
 #pragma unroll
@@ -734,39 +745,43 @@ __global__ void __launch_bounds__(kQ4Warps * 32, kQ4MinBlocks) decode_q4_round_k
   const uint32_t off_ka1 = g * 128 + (((2 * t + 1) ^ sw) << 4);
   const uint32_t off_kb0 = off_ka0 + 8 * 128;
   const uint32_t off_kb1 = off_ka1 + 8 * 128;
-  const int vword = 4 * ((kQ4GPW * warp) >> 1);  // byte of the half-word pair holding this warp's groups
-  const uint32_t off_v0 = (2 * t) * 128 + ((g ^ swv) << 4) + vword;
-  const uint32_t off_v1 = (2 * t + 1) * 128 + ((g ^ (GATHER ? 0 : swv + 1)) << 4) + vword;
+  const uint32_t off_v0 = (2 * t) * 128 + ((g ^ swv) << 4) + 4 * warp;
+  const uint32_t off_v1 = (2 * t + 1) * 128 + ((g ^ (GATHER ? 0 : swv + 1)) << 4) + 4 * warp;
   const uint32_t off_v2 = off_v0 + 8 * 128;
   const uint32_t off_v3 = off_v1 + 8 * 128;
-  const uint32_t vc_base = smem_u32(&sm.vc[0][0][0]);
-  const uint32_t vs_base = smem_u32(&sm.vs[0][0][0]) + vword;
+  const uint32_t kc_base = smem_u32(&sm.kc[warp][0][0]);
+  const uint32_t ks_base = smem_u32(&sm.ks[warp][0][0]);
+  const uint32_t vc_base = smem_u32(&sm.vc[0][0]);
+  const uint32_t vs_base = smem_u32(&sm.vs[0][0]) + 4 * warp;
+  const uint32_t pb_addr = smem_u32(&sm.pb[0][lane]);
 
   for (int r = 0; r < nrounds; ++r) {
-    const int tiles_r = min(kQ4Warps, ntiles - kQ4Warps * r);
-    const int ks_ = r % kQ4KStages;
-    float S[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-    if (warp < tiles_r) {  // warp-uniform
-      const int tile = kQ4Warps * r + warp;
-      const int key0 = k0 + 16 * tile;
-      const int nvalid = min(16, k1 - key0);
+    const uint32_t par = r & 1;
+    const int tile0 = kQ4RoundTiles * r + kQ4TPW * warp;
+    float S[kQ4TPW][4];
+#pragma unroll
+    for (int u = 0; u < kQ4TPW; ++u) S[u][0] = S[u][1] = S[u][2] = S[u][3] = -INFINITY;
+    if (k0 + 16 * tile0 < k1) {  // warp-uniform: this warp has at least one tile in the round
       // mma.sync below is warp-collective: the wait's outcome is made warp-uniform
-      if (!timed_out && !__all_sync(0xffffffffu, mbar_wait_bounded(&sm.kbar[warp][ks_], (r / kQ4KStages) & 1)))
-        timed_out = true;
-      const uint32_t kbase = smem_u32(&sm.kc[warp][ks_][0]);
-      const uint32_t ksb = smem_u32(&sm.ks[warp][ks_][0]);
+      if (!timed_out && !__all_sync(0xffffffffu, mbar_wait_bounded(&sm.kbar[warp], par))) timed_out = true;
 
-      // ---------------- scores S[key][head] for keys g, g+8 and heads 2t, 2t+1
-      S[0] = S[1] = S[2] = S[3] = 0.f;
+      // ---------------- scores S[u][key][head] for keys g, g+8 of tile u and heads 2t, 2t+1
+#pragma unroll
+      for (int u = 0; u < kQ4TPW; ++u) S[u][0] = S[u][1] = S[u][2] = S[u][3] = 0.f;
 #pragma unroll
       for (int w = 0; w < kQ4NG / 2; ++w) {  // group pair (2w, 2w+1): one word of each fragment row
-        const uint32_t wa0 = lds32a(kbase + off_ka0 + 4 * w);  // half-words (2t, G = 2w, 2w+1) of row g
-        const uint32_t wa1 = lds32a(kbase + off_ka1 + 4 * w);  // half-words (2t+1, G)
-        const uint32_t wb0 = lds32a(kbase + off_kb0 + 4 * w);  // row g+8
-        const uint32_t wb1 = lds32a(kbase + off_kb1 + 4 * w);
-        const __half2 sca = u32_as_h2(lds32a(ksb + g * 16 + 4 * w));  // K scales (2w, 2w+1) of row g
-        const __half2 scb = u32_as_h2(lds32a(ksb + (g + 8) * 16 + 4 * w));
-        const float2 fsa = __half22float2(sca), fsb = __half22float2(scb);
+        uint32_t wa0[kQ4TPW], wa1[kQ4TPW], wb0[kQ4TPW], wb1[kQ4TPW];
+        float2 fsa[kQ4TPW], fsb[kQ4TPW];
+#pragma unroll
+        for (int u = 0; u < kQ4TPW; ++u) {
+          const uint32_t kb = kc_base + u * kQ4TileBytes, sb = ks_base + u * kQ4ScaleBytes;
+          wa0[u] = lds32a(kb + off_ka0 + 4 * w);  // half-words (2t, G = 2w, 2w+1) of row g
+          wa1[u] = lds32a(kb + off_ka1 + 4 * w);  // half-words (2t+1, G)
+          wb0[u] = lds32a(kb + off_kb0 + 4 * w);  // row g+8
+          wb1[u] = lds32a(kb + off_kb1 + 4 * w);
+          fsa[u] = __half22float2(u32_as_h2(lds32a(sb + g * 16 + 4 * w)));  // K scales (2w, 2w+1) of row g
+          fsb[u] = __half22float2(u32_as_h2(lds32a(sb + (g + 8) * 16 + 4 * w)));
+        }
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
           const int G = 2 * w + e;
@@ -774,75 +789,63 @@ __global__ void __launch_bounds__(kQ4Warps * 32, kQ4MinBlocks) decode_q4_round_k
           const uint4 ql = lds128a(qf_addr + G * 1024 + 512);
           const float4 nb = lds128f(qb_addr + G * 64);  // -bias of heads (2t, 2t+1, 2t, 2t+1)
           const uint32_t sel = e ? 0x4342u : 0x4140u;
-          const uint32_t xa1 = prmt(wa0, 0u, sel);
-          const uint32_t xa2 = prmt(wa1, 0u, sel);
-          const uint32_t xb1 = prmt(wb0, 0u, sel);
-          const uint32_t xb2 = prmt(wb1, 0u, sel);
-          const uint32_t a10 = nib_lo_pair_biased(xa1), a11 = nib_lo_pair_biased(xb1);
-          const uint32_t a12 = nib_hi_pair_biased(xa1), a13 = nib_hi_pair_biased(xb1);
-          const uint32_t a20 = nib_lo_pair_biased(xa2), a21 = nib_lo_pair_biased(xb2);
-          const uint32_t a22 = nib_hi_pair_biased(xa2), a23 = nib_hi_pair_biased(xb2);
-          float part[4] = {nb.x, nb.y, nb.z, nb.w};
-          mma_f16(part, a10, a11, a12, a13, qh.x, qh.y);
-          mma_f16(part, a20, a21, a22, a23, qh.z, qh.w);
-          mma_f16(part, a10, a11, a12, a13, ql.x, ql.y);
-          mma_f16(part, a20, a21, a22, a23, ql.z, ql.w);
-          const float sa = e ? fsa.y : fsa.x, sb = e ? fsb.y : fsb.x;
-          S[0] = fmaf(sa, part[0], S[0]);
-          S[1] = fmaf(sa, part[1], S[1]);
-          S[2] = fmaf(sb, part[2], S[2]);
-          S[3] = fmaf(sb, part[3], S[3]);
+#pragma unroll
+          for (int u = 0; u < kQ4TPW; ++u) {
+            const uint32_t xa1 = prmt(wa0[u], 0u, sel);
+            const uint32_t xa2 = prmt(wa1[u], 0u, sel);
+            const uint32_t xb1 = prmt(wb0[u], 0u, sel);
+            const uint32_t xb2 = prmt(wb1[u], 0u, sel);
+            const uint32_t a10 = nib_lo_pair_biased(xa1), a11 = nib_lo_pair_biased(xb1);
+            const uint32_t a12 = nib_hi_pair_biased(xa1), a13 = nib_hi_pair_biased(xb1);
+            const uint32_t a20 = nib_lo_pair_biased(xa2), a21 = nib_lo_pair_biased(xb2);
+            const uint32_t a22 = nib_hi_pair_biased(xa2), a23 = nib_hi_pair_biased(xb2);
+            float part[4] = {nb.x, nb.y, nb.z, nb.w};
+            mma_f16(part, a10, a11, a12, a13, qh.x, qh.y);
+            mma_f16(part, a20, a21, a22, a23, qh.z, qh.w);
+            mma_f16(part, a10, a11, a12, a13, ql.x, ql.y);
+            mma_f16(part, a20, a21, a22, a23, ql.z, ql.w);
+            const float sa = e ? fsa[u].y : fsa[u].x, sb = e ? fsb[u].y : fsb[u].x;
+            S[u][0] = fmaf(sa, part[0], S[u][0]);
+            S[u][1] = fmaf(sa, part[1], S[u][1]);
+            S[u][2] = fmaf(sb, part[2], S[u][2]);
+            S[u][3] = fmaf(sb, part[3], S[u][3]);
+          }
         }
       }
       // (The heads past the group have a zero query: their scores are 0, finite,
       // and never leave the kernel, so they need no mask.)
-      if (nvalid < 16) {  // tail tile: mask keys past the end
-        if (g >= nvalid) S[0] = S[1] = -INFINITY;
-        if (g + 8 >= nvalid) S[2] = S[3] = -INFINITY;
+#pragma unroll
+      for (int u = 0; u < kQ4TPW; ++u) {
+        const int nvalid = k1 - (k0 + 16 * (tile0 + u));
+        if (nvalid < 16) {  // warp-uniform: keys past the end (or a tile past the partition)
+          if (g >= nvalid) S[u][0] = S[u][1] = -INFINITY;
+          if (g + 8 >= nvalid) S[u][2] = S[u][3] = -INFINITY;
+        }
       }
 
-      // The K stage is free again: refill it with this warp's tile kQ4KStages rounds ahead.
-      const int32_t next_row = __shfl_sync(0xffffffffu, my_row, min(r + kQ4KStages, 31));
+      // The K tiles are consumed: refill them with round r + 1.
       __syncwarp();
-      const int ntile = tile + kQ4Warps * kQ4KStages;
-      if (lane == 0 && ntile < ntiles) {
-        fence_proxy_async();
-        const int nk0 = k0 + 16 * ntile;
-        if (!q4_issue_plane<GATHER>(a, b, kvh, nk0, min(16, k1 - nk0), next_row, &a.tm_k, c.k, c.k_scale,
-                                    sm.kc[warp][ks_], sm.ks[warp][ks_], &sm.kbar[warp][ks_]))
-          poisoned = true;
-      }
+      if (r + 1 < nrounds)
+        poisoned |= q4_issue_own<GATHER>(a, b, kvh, k0, k1, r + 1, warp, lane, tile_row, &a.tm_k, c.k, c.k_scale,
+                                         sm.kc[warp], sm.ks[warp], &sm.kbar[warp]);
     }
 
     // ---------------- round maximum, shared through shared memory
-    float t0 = fmaxf(S[0], S[2]), t1 = fmaxf(S[1], S[3]);
+    float t0 = fmaxf(S[0][0], S[0][2]), t1 = fmaxf(S[0][1], S[0][3]);
+#pragma unroll
+    for (int u = 1; u < kQ4TPW; ++u) {
+      t0 = fmaxf(t0, fmaxf(S[u][0], S[u][2]));
+      t1 = fmaxf(t1, fmaxf(S[u][1], S[u][3]));
+    }
 #pragma unroll
     for (int o = 4; o < 32; o <<= 1) {
       t0 = fmaxf(t0, __shfl_xor_sync(0xffffffffu, t0, o));
       t1 = fmaxf(t1, __shfl_xor_sync(0xffffffffu, t1, o));
     }
-    if (g == 0) *reinterpret_cast<float2*>(&sm.red[r & 1][warp][2 * t]) = make_float2(t0, t1);
-    const int32_t v_row = __shfl_sync(0xffffffffu, my_row, min(r + 1, 31));
+    if (g == 0) *reinterpret_cast<float2*>(&sm.red[warp][2 * t]) = make_float2(t0, t1);
     bar_sync_cta();  // (1) maxima published; every warp is past the P.V of round r - 1
-
-    // V slot (r + 1) % 2 held round r - 1, which every warp has finished: refill it.
-    if (lane == 0 && r + 1 < nrounds) {
-      const int vslot = (r + 1) % kQ4VSlots;
-      const int vtile = kQ4Warps * (r + 1) + warp;
-      if (vtile < ntiles) {
-        fence_proxy_async();
-        const int vk0 = k0 + 16 * vtile;
-        if (!q4_issue_plane<GATHER>(a, b, kvh, vk0, min(16, k1 - vk0), v_row, &a.tm_v, c.v, c.v_scale,
-                                    sm.vc[vslot][warp], sm.vs[vslot][warp], &sm.vbar[vslot]))
-          poisoned = true;
-      } else {
-        mbar_arrive(&sm.vbar[vslot]);
-      }
-    }
-
-    // ---------------- online softmax (base 2), identical in every warp
     {
-      const uint32_t ra = smem_u32(&sm.red[r & 1][0][2 * t]);
+      const uint32_t ra = smem_u32(&sm.red[0][2 * t]);
 #pragma unroll
       for (int w = 0; w < kQ4Warps; ++w) {
         const float2 mx = lds64f(ra + w * 32);
@@ -850,18 +853,18 @@ __global__ void __launch_bounds__(kQ4Warps * 32, kQ4MinBlocks) decode_q4_round_k
         t1 = fmaxf(t1, mx.y);
       }
     }
+
+    // ---------------- online softmax (base 2), identical in every warp
     // n is finite (m starts at kQ4NoMax); c is exactly 1 while a head's maximum stands
     const float n0 = fmaxf(m0, t0), n1 = fmaxf(m1, t1);
     const float c0 = fast_exp2(m0 - n0), c1 = fast_exp2(m1 - n1);
-    const float p0 = fast_exp2(S[0] - n0), p1 = fast_exp2(S[1] - n1);
-    const float p2 = fast_exp2(S[2] - n0), p3 = fast_exp2(S[3] - n1);
-    z0 = fmaf(z0, c0, p0 + p2);
-    z1 = fmaf(z1, c1, p1 + p3);
     m0 = n0;
     m1 = n1;
+    z0 *= c0;
+    z1 *= c1;
     if (r > 0 && __any_sync(0xffffffffu, c0 != 1.f || c1 != 1.f)) {  // acc is still zero in round 0
 #pragma unroll
-      for (int e = 0; e < kQ4GPW; ++e)
+      for (int e = 0; e < 2; ++e)
 #pragma unroll
         for (int j = 0; j < 2; ++j) {
           acc[e][j][0] *= c0;
@@ -870,65 +873,75 @@ __global__ void __launch_bounds__(kQ4Warps * 32, kQ4MinBlocks) decode_q4_round_k
           acc[e][j][3] *= c1;
         }
     }
-
-    // ---------------- P (keys x heads) -> B fragments (keys on K, heads on N), published
-    const uint32_t pb0 = movmatrix_trans(pack_half2(p0, p1));  // keys 2t, 2t+1 of head g
-    const uint32_t pb1 = movmatrix_trans(pack_half2(p2, p3));  // keys 2t+8, 2t+9
-    sm.pb[r & 1][warp][lane] = make_uint2(pb0, pb1);
+    // P (keys x heads) -> B fragments (keys on K, heads on N), published
+#pragma unroll
+    for (int u = 0; u < kQ4TPW; ++u) {
+      const float p0 = fast_exp2(S[u][0] - n0), p1 = fast_exp2(S[u][1] - n1);
+      const float p2 = fast_exp2(S[u][2] - n0), p3 = fast_exp2(S[u][3] - n1);
+      z0 += p0 + p2;
+      z1 += p1 + p3;
+      const uint32_t pb0 = movmatrix_trans(pack_half2(p0, p1));  // keys 2t, 2t+1 of head g
+      const uint32_t pb1 = movmatrix_trans(pack_half2(p2, p3));  // keys 2t+8, 2t+9
+      sm.pb[kQ4TPW * warp + u][lane] = make_uint2(pb0, pb1);
+    }
     bar_sync_cta();  // (2) every tile's P is published
 
     // ---------------- P.V over the round's tiles for groups 2w, 2w+1
-    const int vs_ = r % kQ4VSlots;
-    if (!timed_out && !__all_sync(0xffffffffu, mbar_wait_bounded(&sm.vbar[vs_], (r / kQ4VSlots) & 1)))
-      timed_out = true;
-    const bool tail_round = k0 + kQ4Warps * 16 * (r + 1) > k1;  // CTA-uniform
-    // Every tile slot of the round is visited.  Keys past the end (the tail of the
-    // last tile, and the slots of tiles the last round does not have) get zero
-    // V scales: their P is zero too, and their codes, stale or not, are finite
-    // once converted, so they add exactly nothing.
-    const uint32_t pb_addr = smem_u32(&sm.pb[r & 1][0][lane]);
+    if (!timed_out && !__all_sync(0xffffffffu, mbar_wait_bounded(&sm.vfull, par))) timed_out = true;
+    const bool tail_round = k0 + kQ4RoundTiles * 16 * (r + 1) > k1;  // CTA-uniform
+    // Every tile of the round is visited.  Keys past the end (the tail of the
+    // last tile, and the tiles the last round does not have) get zero V scales:
+    // their P is zero too, and their codes, stale or not, are finite once
+    // converted, so they add exactly nothing.
 #pragma unroll
-    for (int j = 0; j < kQ4Warps; ++j) {
-      {
-        const uint2 pp = lds64a(pb_addr + j * 256);
-        const uint32_t cb = vc_base + (vs_ * kQ4Warps + j) * kQ4TileBytes;
-        const uint32_t sb = vs_base + (vs_ * kQ4Warps + j) * kQ4ScaleBytes;
-        // V scales of keys 2t, 2t+1, 2t+8, 2t+9 and V codes of the same rows
-        // (half-word h = g of groups 2w, 2w+1).
-        uint32_t swa = lds32a(sb + (2 * t) * 16);
-        uint32_t swb = lds32a(sb + (2 * t + 1) * 16);
-        uint32_t swc = lds32a(sb + (2 * t + 8) * 16);
-        uint32_t swd = lds32a(sb + (2 * t + 9) * 16);
-        const int nvalid = k1 - (k0 + 16 * (kQ4Warps * r + j));
-        if (tail_round && nvalid < 16) {  // CTA-uniform
-          if (2 * t >= nvalid) swa = 0u;
-          if (2 * t + 1 >= nvalid) swb = 0u;
-          if (2 * t + 8 >= nvalid) swc = 0u;
-          if (2 * t + 9 >= nvalid) swd = 0u;
-        }
-        const uint32_t cw0 = lds32a(cb + off_v0);
-        const uint32_t cw1 = lds32a(cb + off_v1);
-        const uint32_t cw2 = lds32a(cb + off_v2);
-        const uint32_t cw3 = lds32a(cb + off_v3);
-#pragma unroll
-        for (int e = 0; e < kQ4GPW; ++e) {
-          const int eh = kQ4GPW == 2 ? e : (warp & 1);  // half-word of the pair: the group's parity
-          const uint32_t ssel = eh ? 0x7632u : 0x5410u;
-          const uint32_t slo = prmt(swa, swb, ssel);
-          const uint32_t shi = prmt(swc, swd, ssel);
-          const uint32_t b0 = h2_as_u32(__hmul2(u32_as_h2(pp.x), u32_as_h2(slo)));
-          const uint32_t b1 = h2_as_u32(__hmul2(u32_as_h2(pp.y), u32_as_h2(shi)));
-          const uint32_t s0 = eh ? 0x6622u : 0x4400u;  // byte X of rows a, b -> bytes 0, 2
-          const uint32_t s1 = eh ? 0x7733u : 0x5511u;  // byte X+1
-          const uint32_t x01 = prmt(cw0, cw1, s0);
-          const uint32_t x01b = prmt(cw0, cw1, s1);
-          const uint32_t x23 = prmt(cw2, cw3, s0);
-          const uint32_t x23b = prmt(cw2, cw3, s1);
-          // d-tile (G,0): rows g <-> d = 32G+4g, g+8 <-> 32G+4g+2 ; (G,1): +1
-          mma_f16(acc[e][0], nib_lo_pair(x01), nib_lo_pair(x01b), nib_lo_pair(x23), nib_lo_pair(x23b), b0, b1);
-          mma_f16(acc[e][1], nib_hi_pair(x01), nib_hi_pair(x01b), nib_hi_pair(x23), nib_hi_pair(x23b), b0, b1);
-        }
+    for (int j = 0; j < kQ4RoundTiles; ++j) {
+      const uint2 pp = lds64a(pb_addr + j * 256);
+      const uint32_t cb = vc_base + j * kQ4TileBytes;
+      const uint32_t sb = vs_base + j * kQ4ScaleBytes;
+      // V scales of keys 2t, 2t+1, 2t+8, 2t+9 and V codes of the same rows
+      // (half-word h = g of groups 2w, 2w+1).
+      uint32_t swa = lds32a(sb + (2 * t) * 16);
+      uint32_t swb = lds32a(sb + (2 * t + 1) * 16);
+      uint32_t swc = lds32a(sb + (2 * t + 8) * 16);
+      uint32_t swd = lds32a(sb + (2 * t + 9) * 16);
+      const int nvalid = k1 - (k0 + 16 * (kQ4RoundTiles * r + j));
+      if (tail_round && nvalid < 16) {  // CTA-uniform
+        if (2 * t >= nvalid) swa = 0u;
+        if (2 * t + 1 >= nvalid) swb = 0u;
+        if (2 * t + 8 >= nvalid) swc = 0u;
+        if (2 * t + 9 >= nvalid) swd = 0u;
       }
+      const uint32_t cw0 = lds32a(cb + off_v0);
+      const uint32_t cw1 = lds32a(cb + off_v1);
+      const uint32_t cw2 = lds32a(cb + off_v2);
+      const uint32_t cw3 = lds32a(cb + off_v3);
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const uint32_t ssel = e ? 0x7632u : 0x5410u;
+        const uint32_t slo = prmt(swa, swb, ssel);
+        const uint32_t shi = prmt(swc, swd, ssel);
+        const uint32_t b0 = h2_as_u32(__hmul2(u32_as_h2(pp.x), u32_as_h2(slo)));
+        const uint32_t b1 = h2_as_u32(__hmul2(u32_as_h2(pp.y), u32_as_h2(shi)));
+        const uint32_t s0 = e ? 0x6622u : 0x4400u;  // byte X of rows a, b -> bytes 0, 2
+        const uint32_t s1 = e ? 0x7733u : 0x5511u;  // byte X+1
+        const uint32_t x01 = prmt(cw0, cw1, s0);
+        const uint32_t x01b = prmt(cw0, cw1, s1);
+        const uint32_t x23 = prmt(cw2, cw3, s0);
+        const uint32_t x23b = prmt(cw2, cw3, s1);
+        // d-tile (G,0): rows g <-> d = 32G+4g, g+8 <-> 32G+4g+2 ; (G,1): +1
+        mma_f16(acc[e][0], nib_lo_pair(x01), nib_lo_pair(x01b), nib_lo_pair(x23), nib_lo_pair(x23b), b0, b1);
+        mma_f16(acc[e][1], nib_hi_pair(x01), nib_hi_pair(x01b), nib_hi_pair(x23), nib_hi_pair(x23b), b0, b1);
+      }
+    }
+
+    // The round's V is consumed once every warp gets here: then each warp
+    // refills its own V tiles with round r + 1.
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&sm.vempty);
+    if (r + 1 < nrounds) {
+      if (!timed_out && !__all_sync(0xffffffffu, mbar_wait_bounded(&sm.vempty, par))) timed_out = true;
+      poisoned |= q4_issue_own<GATHER>(a, b, kvh, k0, k1, r + 1, warp, lane, tile_row, &a.tm_v, c.v, c.v_scale,
+                                       &sm.vc[kQ4TPW * warp], &sm.vs[kQ4TPW * warp], &sm.vfull);
     }
   }
   if (timed_out && lane == 0) set_status(a.status, KVQ_DEV_TIMEOUT);
@@ -953,8 +966,8 @@ __global__ void __launch_bounds__(kQ4Warps * 32, kQ4MinBlocks) decode_q4_round_k
   const int64_t pi0 = ((int64_t)b * a.Hq + kvh * a.group + 2 * t) * a.P + p;  // head 2t
   const int64_t pi1 = pi0 + a.P;                                             // head 2t + 1
 #pragma unroll
-  for (int e = 0; e < kQ4GPW; ++e) {
-    const int d = 32 * (kQ4GPW * warp + e) + 4 * g;
+  for (int e = 0; e < 2; ++e) {
+    const int d = 32 * (2 * warp + e) + 4 * g;
     float4 o0 = make_float4(acc[e][0][0], acc[e][1][0], acc[e][0][2], acc[e][1][2]);
     float4 o1 = make_float4(acc[e][0][1], acc[e][1][1], acc[e][0][3], acc[e][1][3]);
     if (bad) o0 = o1 = make_float4(NAN, NAN, NAN, NAN);
