@@ -330,14 +330,6 @@ def _events_time(torch, fn, iters, warmup=3):
     return a.elapsed_time(b) / iters
 
 
-def q4_kernel_name(torch, T, n_seqs=1):
-    """The 4-bit decode kernel the library picks for this grid (kvq_set_decode_q4_kernel(0)):
-    the per-warp kernel when partitions x KV heads x sequences fit in one wave of 3 CTAs per SM."""
-    ctas = -(-T // 512) * HK * n_seqs
-    sms = torch.cuda.get_device_properties(0).multi_processor_count
-    return "decode_q4_warp_kernel" if ctas <= 3 * sms else "decode_q4_round_kernel"
-
-
 def measure_rows(K, synth, torch, dev, peak, tflops_peak, only=None):
     """Batched ragged paged decode, prefill chunk, fp8 latent decode (dense and
     gathered), the bf16-cache comparison and the store, each timed with CUDA
@@ -400,7 +392,7 @@ def _row_batched(K, synth, torch, dev, peak, seed):
         "workload": "32 sequences, lengths U{1024..65536} (+1 new token each), 16-token pages, shuffled block "
                     "tables, 1 layer, 4 KV / 24 q heads", "us_per_step": ms * 1e3, "decode_kernel_us": dec_ms * 1e3,
         "cache_bytes": byts, "achieved_GBs": byts / (dec_ms * 1e-3) / 1e9, "frac_of_hbm_peak": byts / (dec_ms * 1e-3) / 1e9 / peak,
-        "kernel": q4_kernel_name(torch, max(T), 32)}
+        "kernel": "decode_q4_round_kernel"}
     del c, ws
     torch.cuda.empty_cache()
     return out
@@ -584,8 +576,7 @@ def main():
         long = {"context": args.long_context, "value": ltot * 1e3 / (LAYERS * lsteps * world),
                 "unit": "us/layer-token", "decode_kernel_us": lavg * 1e3,
                 "roofline": {"bound": "hbm", "achieved": lach, "peak": peak, "unit": "GB/s", "frac": lach / peak,
-                             "traffic": None, "bytes_per_launch": lbytes,
-                             "kernel": q4_kernel_name(torch, WL.T)},
+                             "traffic": None, "bytes_per_launch": lbytes, "kernel": "decode_q4_round_kernel"},
                 "clocks": clk2.summary()}
         del WL
 
@@ -617,7 +608,7 @@ def main():
                        "parallelism": f"replicas x{world}"},
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                          "traffic": None, "bytes_per_launch": bytes_per_launch,
-                         "kernel": q4_kernel_name(torch, args.context + 1),
+                         "kernel": "decode_q4_round_kernel",
                          "decode_kernel_us": dec_avg_ms * 1e3, "peak_kind": peak_kind},
             "e2e": {"value": e2e_us, "unit": "us/layer-token", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
             "gpu_launches": launches,

@@ -37,7 +37,6 @@ SIGNATURES = {
     "kvq_version": (_I32, []),
     "kvq_status_string": (ctypes.c_char_p, [_I32]),
     "kvq_last_cuda_error": (_I32, []),
-    "kvq_set_decode_q4_kernel": (_I32, [_I32]),
     "kvq_plane_bytes": (_SZ, [ctypes.POINTER(CacheDesc), _I32]),
     "kvq_store": (_I32, [ctypes.POINTER(CacheDesc), _P, _P, _I32, _I64, _P, _P, _P]),
     "kvq_rotate_query": (_I32, [_P, _I32, _P, _I64, _I32, _P]),
@@ -147,14 +146,6 @@ class Cache:
 
     def nbytes(self):
         return sum(t.numel() * t.element_size() for t in (self.k, self.v, self.k_scale, self.v_scale) if t is not None)
-
-
-DECODE_Q4_KERNELS = {"auto": 0, "warp": 1, "round": 2}
-
-
-def set_decode_q4_kernel(which="auto"):
-    """Select the 4-bit decode kernel: "auto" (by grid size), "warp" or "round"."""
-    _check(lib().kvq_set_decode_q4_kernel(DECODE_Q4_KERNELS[which]), "kvq_set_decode_q4_kernel")
 
 
 def store(cache: Cache, k, v, slot_mapping, status=None, stream=None):

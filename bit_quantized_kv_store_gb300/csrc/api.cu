@@ -134,12 +134,6 @@ const char* kvq_status_string(int32_t s) {
 
 int32_t kvq_last_cuda_error(void) { return g_last_cuda_error; }
 
-int32_t kvq_set_decode_q4_kernel(int32_t which) {
-  if (which < 0 || which > 2) return KVQ_ERR_INVALID_ARG;
-  kvq::set_q4_decode_kernel(which);
-  return KVQ_OK;
-}
-
 size_t kvq_plane_bytes(const kvq_cache* c, int32_t plane) {
   if (!c || c->head_dim <= 0 || c->head_dim % 32 || c->num_kv_heads < 1 || c->page_size <= 0 || c->num_pages < 0)
     return 0;

@@ -74,8 +74,6 @@ cudaError_t launch_store(const kvq_cache& c, const void* k, const void* v, int d
                          const int32_t* slots, int32_t* status, cudaStream_t s);
 cudaError_t launch_rotate(const void* x, int dtype, float* y, int64_t rows, int head_dim, cudaStream_t s);
 cudaError_t launch_decode_q4(const DecodeArgs& a, int B, cudaStream_t s);
-// Which 4-bit decode kernel launch_decode_q4 takes: 0 by grid size, 1 per-warp, 2 round.
-void set_q4_decode_kernel(int which);
 // fp8 latent rows on the tensor cores (decode_fp8.cu); tm_k / tm_v map the latent
 // and rope code planes.
 cudaError_t launch_decode_fp8(const DecodeArgs& a, int B, cudaStream_t s);

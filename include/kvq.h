@@ -110,17 +110,6 @@ const char* kvq_status_string(int32_t status);
 /* The cudaError_t of the last KVQ_ERR_CUDA returned on this thread (0 if none). */
 int32_t kvq_last_cuda_error(void);
 
-/* kvq_set_decode_q4_kernel -- which of the two 4-bit decode kernels
- * kvq_decode_attn (and its variants) launches; both produce the same partials
- * with the same arithmetic, up to the order of fp32 additions:
- *   0 (default): by grid size -- the per-warp kernel when the grid fits in one
- *     wave of it (partitions x KV heads x sequences <= 3 x SM count: short
- *     contexts, latency-bound), else the round kernel (long or many contexts);
- *   1: always the per-warp kernel; 2: always the round kernel.
- * Process-wide (not per thread); meant for tuning and for testing both kernels.
- * Returns KVQ_ERR_INVALID_ARG for another value. */
-int32_t kvq_set_decode_q4_kernel(int32_t which);
-
 /* Bytes of each plane for a cache description (0 for unused planes). */
 size_t kvq_plane_bytes(const kvq_cache* cache, int32_t plane /* 0 k, 1 k_scale, 2 v, 3 v_scale */);
 

@@ -31,15 +31,6 @@ def K():
     return _lib
 
 
-@pytest.fixture(params=["warp", "round"])
-def q4k(request, K):
-    """Runs a 4-bit decode test under each of the two decode kernels (per-warp and
-    round); both must match the oracle."""
-    K.set_decode_q4_kernel(request.param)
-    yield request.param
-    K.set_decode_q4_kernel("auto")
-
-
 DEV = "cuda"
 
 
@@ -232,7 +223,7 @@ def run_decode(K, g, bt, q, lens, max_len, sm_scale, sel=None):
     return out.cpu().numpy(), ws
 
 
-def test_decode_tiny_config(K, q4k):
+def test_decode_tiny_config(K):
     """1 sequence, 1024 keys, 4 KV / 24 query heads, head_dim 256, fp32 inputs with x20 outliers."""
     lens = [1024]
     g, o, bt, q, ml = decode_case(K, lens, dtype=torch.float32, gen="outlier", shuffle=False)
@@ -244,14 +235,14 @@ def test_decode_tiny_config(K, q4k):
 
 
 @pytest.mark.parametrize("T", [1, 2, 15, 16, 17, 127, 128, 129, 511, 512, 513, 1025, 4097])
-def test_decode_lengths(K, q4k, T):
+def test_decode_lengths(K, T):
     g, o, bt, q, ml = decode_case(K, [T], seed=T)
     out, _ = run_decode(K, g, bt, q, [T], ml, 1 / 16)
     ref = O.decode(o, to_np_in(q), [T], bt, 1 / 16)
     assert_close(out[0], ref[0], what=f"T={T}")
 
 
-def test_decode_ragged_paged_batch(K, q4k):
+def test_decode_ragged_paged_batch(K):
     lens = [1, 700, 33, 2048, 1500, 0, 513, 3000]
     g, o, bt, q, ml = decode_case(K, lens, seed=11)
     out, _ = run_decode(K, g, bt, q, lens, ml, 1 / 16)
@@ -264,7 +255,7 @@ def test_decode_ragged_paged_batch(K, q4k):
 
 
 @pytest.mark.parametrize("Hk,Hq", [(1, 1), (2, 4), (1, 8), (8, 8), (3, 21)])
-def test_decode_gqa_groups(K, q4k, Hk, Hq):
+def test_decode_gqa_groups(K, Hk, Hq):
     lens = [900, 77]
     g, o, bt, q, ml = decode_case(K, lens, Hk=Hk, Hq=Hq, seed=Hk * 100 + Hq)
     out, _ = run_decode(K, g, bt, q, lens, ml, 0.07)
@@ -273,7 +264,7 @@ def test_decode_gqa_groups(K, q4k, Hk, Hq):
         assert_close(out[b], ref[b], what=f"Hk={Hk} Hq={Hq} seq {b}")
 
 
-def test_decode_concurrent_equals_solo_and_deterministic(K, q4k):
+def test_decode_concurrent_equals_solo_and_deterministic(K):
     lens = [1200, 530, 4100]
     g, o, bt, q, ml = decode_case(K, lens, seed=3)
     out, _ = run_decode(K, g, bt, q, lens, ml, 1 / 16)
@@ -286,7 +277,7 @@ def test_decode_concurrent_equals_solo_and_deterministic(K, q4k):
 
 @pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
 @pytest.mark.parametrize("Hk,Hq", [(4, 24), (2, 4), (3, 21)])
-def test_decode_unrotated_query_equals_rotate_then_decode(K, q4k, dtype, Hk, Hq):
+def test_decode_unrotated_query_equals_rotate_then_decode(K, dtype, Hk, Hq):
     """The in-kernel query rotation gives the same partials, bit for bit (dense and gathered)."""
     lens = [1500, 700]
     g, o, bt, q, ml = decode_case(K, lens, Hk=Hk, Hq=Hq, seed=500 + Hq, dtype=dtype)
@@ -305,7 +296,7 @@ def test_decode_unrotated_query_equals_rotate_then_decode(K, q4k, dtype, Hk, Hq)
         assert torch.equal(ws1.view(torch.int32), ws2.view(torch.int32))
 
 
-def test_decode_gather(K, q4k):
+def test_decode_gather(K):
     lens = [3000, 1800]
     g, o, bt, q, ml = decode_case(K, lens, seed=21)
     for n_sel in (1, 100, 512, 1300):
@@ -316,7 +307,7 @@ def test_decode_gather(K, q4k):
             assert_close(out[b], ref[b], what=f"gather n_sel={n_sel} seq {b}")
 
 
-def test_decode_bad_page_and_length_are_flagged(K, q4k):
+def test_decode_bad_page_and_length_are_flagged(K):
     lens = [600, 300]
     g, o, bt, q, ml = decode_case(K, lens, seed=4)
     bad = bt.copy()
