@@ -35,6 +35,8 @@
 // a warp refills its own K tiles right after its scores, and its share of the
 // V tiles once an mbarrier shows every warp done with the round's P.V (a round
 // takes microseconds, so the copies have ample lead).
+#include <type_traits>
+
 #include "kernels.cuh"
 
 namespace kvq {
@@ -512,47 +514,56 @@ __global__ void __launch_bounds__(kQ4Warps * 32, kQ4MinBlocks) decode_q4_round_k
     // Every tile of the round is visited.  Keys past the end (the tail of the
     // last tile, and the tiles the last round does not have) get zero V scales:
     // their P is zero too, and their codes, stale or not, are finite once
-    // converted, so they add exactly nothing.
+    // converted, so they add exactly nothing.  Only a tail round checks.
+    auto pv_round = [&](auto tail_tag) {
+      constexpr bool kTail = decltype(tail_tag)::value;
 #pragma unroll
-    for (int j = 0; j < kQ4RoundTiles; ++j) {
-      const uint2 pp = lds64a(pb_addr + j * 256);
-      const uint32_t cb = vc_base + j * kQ4TileBytes;
-      const uint32_t sb = vs_base + j * kQ4ScaleBytes;
-      // V scales of keys 2t, 2t+1, 2t+8, 2t+9 and V codes of the same rows
-      // (half-word h = g of groups 2w, 2w+1).
-      uint32_t swa = lds32a(sb + (2 * t) * 16);
-      uint32_t swb = lds32a(sb + (2 * t + 1) * 16);
-      uint32_t swc = lds32a(sb + (2 * t + 8) * 16);
-      uint32_t swd = lds32a(sb + (2 * t + 9) * 16);
-      const int nvalid = k1 - (k0 + 16 * (kQ4RoundTiles * r + j));
-      if (tail_round && nvalid < 16) {  // CTA-uniform
-        if (2 * t >= nvalid) swa = 0u;
-        if (2 * t + 1 >= nvalid) swb = 0u;
-        if (2 * t + 8 >= nvalid) swc = 0u;
-        if (2 * t + 9 >= nvalid) swd = 0u;
-      }
-      const uint32_t cw0 = lds32a(cb + off_v0);
-      const uint32_t cw1 = lds32a(cb + off_v1);
-      const uint32_t cw2 = lds32a(cb + off_v2);
-      const uint32_t cw3 = lds32a(cb + off_v3);
+      for (int j = 0; j < kQ4RoundTiles; ++j) {
+        const uint2 pp = lds64a(pb_addr + j * 256);
+        const uint32_t cb = vc_base + j * kQ4TileBytes;
+        const uint32_t sb = vs_base + j * kQ4ScaleBytes;
+        // V scales of keys 2t, 2t+1, 2t+8, 2t+9 and V codes of the same rows
+        // (half-word h = g of groups 2w, 2w+1).
+        uint32_t swa = lds32a(sb + (2 * t) * 16);
+        uint32_t swb = lds32a(sb + (2 * t + 1) * 16);
+        uint32_t swc = lds32a(sb + (2 * t + 8) * 16);
+        uint32_t swd = lds32a(sb + (2 * t + 9) * 16);
+        if constexpr (kTail) {
+          const int nvalid = k1 - (k0 + 16 * (kQ4RoundTiles * r + j));
+          if (nvalid < 16) {  // CTA-uniform
+            if (2 * t >= nvalid) swa = 0u;
+            if (2 * t + 1 >= nvalid) swb = 0u;
+            if (2 * t + 8 >= nvalid) swc = 0u;
+            if (2 * t + 9 >= nvalid) swd = 0u;
+          }
+        }
+        const uint32_t cw0 = lds32a(cb + off_v0);
+        const uint32_t cw1 = lds32a(cb + off_v1);
+        const uint32_t cw2 = lds32a(cb + off_v2);
+        const uint32_t cw3 = lds32a(cb + off_v3);
 #pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        const uint32_t ssel = e ? 0x7632u : 0x5410u;
-        const uint32_t slo = prmt(swa, swb, ssel);
-        const uint32_t shi = prmt(swc, swd, ssel);
-        const uint32_t b0 = h2_as_u32(__hmul2(u32_as_h2(pp.x), u32_as_h2(slo)));
-        const uint32_t b1 = h2_as_u32(__hmul2(u32_as_h2(pp.y), u32_as_h2(shi)));
-        const uint32_t s0 = e ? 0x6622u : 0x4400u;  // byte X of rows a, b -> bytes 0, 2
-        const uint32_t s1 = e ? 0x7733u : 0x5511u;  // byte X+1
-        const uint32_t x01 = prmt(cw0, cw1, s0);
-        const uint32_t x01b = prmt(cw0, cw1, s1);
-        const uint32_t x23 = prmt(cw2, cw3, s0);
-        const uint32_t x23b = prmt(cw2, cw3, s1);
-        // d-tile (G,0): rows g <-> d = 32G+4g, g+8 <-> 32G+4g+2 ; (G,1): +1
-        mma_f16(acc[e][0], nib_lo_pair(x01), nib_lo_pair(x01b), nib_lo_pair(x23), nib_lo_pair(x23b), b0, b1);
-        mma_f16(acc[e][1], nib_hi_pair(x01), nib_hi_pair(x01b), nib_hi_pair(x23), nib_hi_pair(x23b), b0, b1);
+        for (int e = 0; e < 2; ++e) {
+          const uint32_t ssel = e ? 0x7632u : 0x5410u;
+          const uint32_t slo = prmt(swa, swb, ssel);
+          const uint32_t shi = prmt(swc, swd, ssel);
+          const uint32_t b0 = h2_as_u32(__hmul2(u32_as_h2(pp.x), u32_as_h2(slo)));
+          const uint32_t b1 = h2_as_u32(__hmul2(u32_as_h2(pp.y), u32_as_h2(shi)));
+          const uint32_t s0 = e ? 0x6622u : 0x4400u;  // byte X of rows a, b -> bytes 0, 2
+          const uint32_t s1 = e ? 0x7733u : 0x5511u;  // byte X+1
+          const uint32_t x01 = prmt(cw0, cw1, s0);
+          const uint32_t x01b = prmt(cw0, cw1, s1);
+          const uint32_t x23 = prmt(cw2, cw3, s0);
+          const uint32_t x23b = prmt(cw2, cw3, s1);
+          // d-tile (G,0): rows g <-> d = 32G+4g, g+8 <-> 32G+4g+2 ; (G,1): +1
+          mma_f16(acc[e][0], nib_lo_pair(x01), nib_lo_pair(x01b), nib_lo_pair(x23), nib_lo_pair(x23b), b0, b1);
+          mma_f16(acc[e][1], nib_hi_pair(x01), nib_hi_pair(x01b), nib_hi_pair(x23), nib_hi_pair(x23b), b0, b1);
+        }
       }
-    }
+    };
+    if (tail_round)
+      pv_round(std::true_type{});
+    else
+      pv_round(std::false_type{});
 
     // The round's V is consumed once every warp gets here: then each warp
     // refills its own V tiles with round r + 1.
