@@ -5,11 +5,15 @@
 // "KV cache quantization: fp8 (KV8) + 4-bit TurboQuant", split-T commit (a
 // log-sum-exp merge kernel over the (m, z, cl) partials).
 //
-// One CTA of 256 threads per (32 output values, query head, sequence).  The
-// partitions are read as float4 rows; thread i takes partitions i/8, i/8 + 32,
-// ... in ascending order, and the 32 per-thread sums are then added in a fixed
-// tree, so the result does not depend on scheduling (bit-reproducible).  The
-// 32 values of a CTA are exactly one Hadamard group, rotated back in one warp.
+// One CTA of 256 threads per (32 output values, query head, sequence), one
+// pass over the partials.  Thread (row r = tid / 8, chunk c = tid % 8) takes
+// partitions r, r + 32, r + 64, ... in ascending order: it loads their m (and,
+// for c == 0, z) and the float4 chunk c of their acc, four partitions per
+// batch with every load of a batch issued before any use, and keeps a running
+// (M_t, Z_t, acc_t) rescaled to its own maximum.  The 32 row-threads' partials
+// are then combined in a fixed tree, so the result does not depend on
+// scheduling (bit-reproducible), and the 32 values of the CTA -- exactly one
+// Hadamard group -- are rotated back in one warp.
 #include "kernels.cuh"
 
 namespace kvq {
@@ -18,7 +22,7 @@ __global__ void __launch_bounds__(256) merge_kernel(const MergeArgs a) {
   pdl_wait();
   pdl_trigger();
   const int grp = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int tid = threadIdx.x, lane = tid & 31;
   float* outp = a.out + ((int64_t)b * a.Hq + h) * a.Dv + 32 * grp;
   int32_t T;
   bool bad = false;
@@ -40,75 +44,75 @@ __global__ void __launch_bounds__(256) merge_kernel(const MergeArgs a) {
   const int64_t base = ((int64_t)b * a.Hq + h) * a.P;
   const float* m = a.ws_m + base;
   const float* z = a.ws_z + base;
+  const int chunk = tid & 7, row = tid >> 3;
+  const float* accp = a.ws_acc + base * a.Dv + 32 * grp + 4 * chunk;
 
-  __shared__ float red[8];
+  __shared__ float s_m[32], s_z[32];  // per row: its maximum, then its z rescaled to the CTA's
   __shared__ float red_acc[32][33];
-  __shared__ float s_M, s_Z;
   __shared__ int s_nan;
-
-  // M = max_p m_p (NaN anywhere poisons the result)
-  float mx = -INFINITY;
-  int nan_seen = 0;
-  for (int i = tid; i < np; i += 256) {
-    const float v = m[i];
-    nan_seen |= isnan(v);
-    mx = fmaxf(mx, v);
-  }
-  for (int o = 16; o > 0; o >>= 1) {
-    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-    nan_seen |= __shfl_xor_sync(0xffffffffu, nan_seen, o);
-  }
   if (tid == 0) s_nan = 0;
-  __syncthreads();
-  if (lane == 0) {
-    red[warp] = mx;
-    if (nan_seen) s_nan = 1;
-  }
-  __syncthreads();
-  if (tid == 0) {
-    float M = red[0];
-    for (int w = 1; w < 8; ++w) M = fmaxf(M, red[w]);
-    s_M = M;
-  }
-  __syncthreads();
-  const float M = s_M;
-  const bool empty = (M == -INFINITY);
 
-  // Z = sum_p z_p 2^(m_p - M), per-thread ascending, then a fixed tree
-  float zs = 0.f;
-  for (int i = tid; i < np; i += 256) zs += empty ? 0.f : z[i] * exp2f(m[i] - M);
-  for (int o = 16; o > 0; o >>= 1) zs += __shfl_xor_sync(0xffffffffu, zs, o);
-  __syncthreads();
-  if (lane == 0) red[warp] = zs;
-  __syncthreads();
-  if (tid == 0) {
-    float Z = 0.f;
-    for (int w = 0; w < 8; ++w) Z += red[w];
-    s_Z = Z;
-  }
-
-  // acc: thread covers float4 chunk (tid % 8) of the group, partitions tid/8 + 32k
-  const int chunk = tid & 7, prow = tid >> 3;
-  float4 s4 = make_float4(0.f, 0.f, 0.f, 0.f);
-  if (!empty) {
-    for (int i = prow; i < np; i += 32) {
-      const float w = exp2f(m[i] - M);
-      const float4 v = *reinterpret_cast<const float4*>(a.ws_acc + (base + i) * a.Dv + 32 * grp + 4 * chunk);
-      s4.x = fmaf(v.x, w, s4.x);
-      s4.y = fmaf(v.y, w, s4.y);
-      s4.z = fmaf(v.z, w, s4.z);
-      s4.w = fmaf(v.w, w, s4.w);
+  // per-thread running partial over partitions row, row + 32, ...
+  float Mt = -INFINITY, Zt = 0.f;
+  float4 At = make_float4(0.f, 0.f, 0.f, 0.f);
+  int nan_seen = 0;
+  for (int i0 = row; i0 < np; i0 += 4 * 32) {
+    float mv[4], zv[4];
+    float4 av[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {  // all loads of the batch first
+      const int i = i0 + 32 * k;
+      mv[k] = -INFINITY;
+      zv[k] = 0.f;
+      av[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (i < np) {
+        mv[k] = m[i];
+        if (chunk == 0) zv[k] = z[i];
+        av[k] = *reinterpret_cast<const float4*>(accp + (int64_t)i * a.Dv);
+      }
+    }
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      if (i0 + 32 * k >= np) break;
+      nan_seen |= isnan(mv[k]);
+      const float Mn = fmaxf(Mt, mv[k]);
+      if (Mn == -INFINITY) continue;  // nothing attended so far
+      const float wo = exp2f(Mt - Mn), wn = exp2f(mv[k] - Mn);
+      Zt = fmaf(Zt, wo, zv[k] * wn);
+      At.x = fmaf(At.x, wo, av[k].x * wn);
+      At.y = fmaf(At.y, wo, av[k].y * wn);
+      At.z = fmaf(At.z, wo, av[k].z * wn);
+      At.w = fmaf(At.w, wo, av[k].w * wn);
+      Mt = Mn;
     }
   }
-  red_acc[prow][4 * chunk + 0] = s4.x;
-  red_acc[prow][4 * chunk + 1] = s4.y;
-  red_acc[prow][4 * chunk + 2] = s4.z;
-  red_acc[prow][4 * chunk + 3] = s4.w;
+  nan_seen = __any_sync(0xffffffffu, nan_seen);
+  __syncthreads();  // s_nan initialised
+  if (nan_seen && lane == 0) s_nan = 1;
+  if (chunk == 0) {
+    s_m[row] = Mt;
+    s_z[row] = Zt;
+  }
   __syncthreads();
-  if (warp == 0) {
-    float o = 0.f;
-    for (int r = 0; r < 32; ++r) o += red_acc[r][lane];  // ascending partition rows
-    const float Z = s_Z;
+  // M = max over the 32 rows; each row's partial rescaled to M
+  float M = s_m[0];
+#pragma unroll 8
+  for (int r = 1; r < 32; ++r) M = fmaxf(M, s_m[r]);
+  const bool empty = (M == -INFINITY);
+  const float wr = (empty || Mt == -INFINITY) ? 0.f : exp2f(Mt - M);
+  red_acc[row][4 * chunk + 0] = At.x * wr;
+  red_acc[row][4 * chunk + 1] = At.y * wr;
+  red_acc[row][4 * chunk + 2] = At.z * wr;
+  red_acc[row][4 * chunk + 3] = At.w * wr;
+  __syncthreads();  // every thread has read s_m
+  if (chunk == 0) s_z[row] = Zt * wr;
+  __syncthreads();
+  if (tid < 32) {
+    float o = 0.f, Z = 0.f;
+    for (int r = 0; r < 32; ++r) {  // ascending rows, a fixed order
+      o += red_acc[r][lane];
+      Z += s_z[r];
+    }
     o = (empty || Z == 0.f) ? 0.f : o / Z;
     if (s_nan) o = NAN;
     if (a.rotate_back) o = __fmul_rn(warp_fwht32(o, lane), kHadamardScale);
