@@ -34,6 +34,7 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 LAYERS, HK, HQ, D, PS = 16, 4, 24, 256, 16
+KERNELS_PER_LAYER = 3  # store + query rotation (one launch), split-T decode, merge
 BYTES_PER_POS_LAYER = HK * 2 * (D // 2 + 2 * (D // 32))   # 1152
 
 
@@ -181,15 +182,15 @@ class Workload:
         out = self.out if out is None else out
         for layer in range(LAYERS):
             c = self.caches[layer]
-            K.store(c, new_k[layer], new_v[layer], self.slot)
-            K.rotate_query(q[layer], out=self.qrot)
+            # store the new token + rotate the query (one launch), decode, merge
+            K.store_rotate(c, new_k[layer], new_v[layer], self.slot, q[layer], out=self.qrot)
             if ev is not None:
                 ev[layer][0].record()
             K.decode_attn(c, self.qrot, self.seq, self.bt, self.T, self.sm_scale, self.ws)
             if ev is not None:
                 ev[layer][1].record()
             K.merge(c, self.ws, 1, HQ, self.seq, self.T, out[layer])
-        return 4 * LAYERS   # kernels launched
+        return KERNELS_PER_LAYER * LAYERS   # kernels launched
 
 
 def capture(torch, fn):
@@ -233,7 +234,7 @@ def time_device(W, steps, warmup, torch):
     d1.record()
     torch.cuda.synchronize()
     dec_avg_ms = d0.elapsed_time(d1) / (steps * LAYERS)
-    return total_ms, dec_avg_ms, 4 * LAYERS * steps, graphs
+    return total_ms, dec_avg_ms, KERNELS_PER_LAYER * LAYERS * steps, graphs
 
 
 def time_e2e(W, steps, warmup, torch, graphs):
@@ -380,8 +381,7 @@ def _row_batched(K, synth, torch, dev, peak, seed):
     ws = K.alloc_workspace(c, 32, HQ, max(T), device=dev)
 
     def batched_step():
-        K.store(c, new_k, new_v, new_slots)
-        K.rotate_query(q, out=qrot)
+        K.store_rotate(c, new_k, new_v, new_slots, q, out=qrot)  # 32 x 4 x (K, V) = 256 rows: the fused form
         K.decode_attn(c, qrot, seq, bt, max(T), 1 / 16, ws)
         K.merge(c, ws, 32, HQ, seq, max(T), o)
 

@@ -40,6 +40,7 @@ SIGNATURES = {
     "kvq_plane_bytes": (_SZ, [ctypes.POINTER(CacheDesc), _I32]),
     "kvq_store": (_I32, [ctypes.POINTER(CacheDesc), _P, _P, _I32, _I64, _P, _P, _P]),
     "kvq_rotate_query": (_I32, [_P, _I32, _P, _I64, _I32, _P]),
+    "kvq_store_rotate": (_I32, [ctypes.POINTER(CacheDesc), _P, _P, _I32, _I64, _P, _P, _P, _I32, _P, _I64, _P]),
     "kvq_decode_workspace_size": (_SZ, [ctypes.POINTER(CacheDesc), _I32, _I32, _I32, _I32]),
     "kvq_decode_attn": (_I32, [ctypes.POINTER(CacheDesc), _P, _I32, _I32, _P, _P, _I32, _I32, _P, _I32, _F, _P,
                                _SZ, _P]),
@@ -160,6 +161,18 @@ def rotate_query(x, out=None, stream=None):
     if out is None:
         out = torch.empty(x.shape, dtype=torch.float32, device=x.device)
     _check(lib().kvq_rotate_query(_ptr(x), _dtype_code(x), _ptr(out), rows, D, _stream(stream)), "kvq_rotate_query")
+    return out
+
+
+def store_rotate(cache: Cache, k, v, slot_mapping, q, out=None, status=None, stream=None):
+    """store(cache, k, v, slot_mapping) and rotate_query(q, out) in one launch
+    (4-bit format, a few tokens); returns the rotated queries."""
+    if out is None:
+        out = torch.empty(q.shape, dtype=torch.float32, device=q.device)
+    rows = q.numel() // q.shape[-1]
+    _check(lib().kvq_store_rotate(cache.ref, _ptr(k), _ptr(v), _dtype_code(k), k.shape[0], _ptr(slot_mapping),
+                                  _ptr(status), _ptr(q), _dtype_code(q), _ptr(out), rows, _stream(stream)),
+           "kvq_store_rotate")
     return out
 
 

@@ -180,6 +180,23 @@ int32_t kvq_rotate_query(const void* x, int32_t dtype, float* y, int64_t rows, i
   return e == cudaSuccess ? KVQ_OK : cuda_fail(e);
 }
 
+int32_t kvq_store_rotate(const kvq_cache* cache, const void* k, const void* v, int32_t dtype, int64_t n_tok,
+                         const int32_t* d_slot_mapping, int32_t* d_status, const void* q, int32_t q_dtype,
+                         float* q_out, int64_t q_rows, void* stream) {
+  int32_t st = check_cache(cache);
+  if (st != KVQ_OK) return st;
+  if (n_tok < 0 || q_rows < 0 || (dtype != KVQ_DT_F32 && dtype != KVQ_DT_BF16) ||
+      (q_dtype != KVQ_DT_F32 && q_dtype != KVQ_DT_BF16))
+    return KVQ_ERR_INVALID_ARG;
+  if (!store_rotate_fits(*cache, n_tok)) return KVQ_ERR_UNSUPPORTED;
+  if (n_tok > 0 && (!k || !v || !d_slot_mapping)) return KVQ_ERR_INVALID_ARG;
+  if (q_rows > 0 && (!q || !q_out)) return KVQ_ERR_INVALID_ARG;
+  if (q_rows > 0 && q == static_cast<const void*>(q_out) && q_dtype != KVQ_DT_F32) return KVQ_ERR_INVALID_ARG;
+  cudaError_t e = launch_store_rotate(*cache, k, v, dtype, n_tok, d_slot_mapping, d_status, q, q_dtype, q_out, q_rows,
+                                      cache->head_dim, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? KVQ_OK : cuda_fail(e);
+}
+
 size_t kvq_decode_workspace_size(const kvq_cache* cache, int32_t num_seqs, int32_t num_q_heads,
                                  int32_t max_seq_len, int32_t n_sel) {
   if (!cache || num_seqs < 0 || num_q_heads < 0 || max_seq_len < 0 || n_sel < 0 || cache->head_dim <= 0) return 0;

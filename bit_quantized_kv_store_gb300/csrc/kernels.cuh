@@ -73,6 +73,11 @@ int32_t record_cuda_failure(cudaError_t e);
 cudaError_t launch_store(const kvq_cache& c, const void* k, const void* v, int dtype, int64_t n_tok,
                          const int32_t* slots, int32_t* status, cudaStream_t s);
 cudaError_t launch_rotate(const void* x, int dtype, float* y, int64_t rows, int head_dim, cudaStream_t s);
+// kvq_store (the few-row 4-bit form) and kvq_rotate_query in one launch.
+bool store_rotate_fits(const kvq_cache& c, int64_t n_tok);
+cudaError_t launch_store_rotate(const kvq_cache& c, const void* k, const void* v, int dtype, int64_t n_tok,
+                                const int32_t* slots, int32_t* status, const void* q, int q_dtype, float* q_out,
+                                int64_t q_rows, int q_head_dim, cudaStream_t s);
 cudaError_t launch_decode_q4(const DecodeArgs& a, int B, cudaStream_t s);
 // fp8 latent rows on the tensor cores (decode_fp8.cu); tm_k / tm_v map the latent
 // and rope code planes.

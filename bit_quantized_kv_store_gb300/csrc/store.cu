@@ -111,15 +111,13 @@ __global__ void __launch_bounds__(256) store_q4_kernel(kvq_cache c, const void* 
 // Latency form of the same store for a handful of rows (a decode step stores one
 // token): one warp per (row, group), so the groups of a row are packed in
 // parallel instead of one after another.  Same arithmetic, same bytes.
+// Warp `wid` of the store: (row, group) = (wid / NG, wid % NG).
 template <int NG>
-__global__ void __launch_bounds__(256) store_q4_group_kernel(kvq_cache c, const void* __restrict__ k,
-                                                             const void* __restrict__ v, int dtype, int64_t n_tok,
-                                                             const int32_t* __restrict__ slots, int32_t* status) {
-  pdl_wait();
-  pdl_trigger();
+__device__ __forceinline__ void store_q4_group_warp(const kvq_cache& c, const void* __restrict__ k,
+                                                    const void* __restrict__ v, int dtype, int64_t n_tok,
+                                                    const int32_t* __restrict__ slots, int32_t* status, int64_t wid) {
   constexpr int D = NG * 32;
   const int lane = threadIdx.x & 31;
-  const int64_t wid = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   const int Hk = c.num_kv_heads;
   if (wid >= n_tok * Hk * 2 * NG) return;
   const int G = static_cast<int>(wid % NG);
@@ -162,6 +160,16 @@ __global__ void __launch_bounds__(256) store_q4_group_kernel(kvq_cache c, const 
     reinterpret_cast<uint16_t*>(codes)[h * NG + G] = static_cast<uint16_t>(bits);
   }
   if (lane == 0) (static_cast<uint16_t*>(kv ? c.v_scale : c.k_scale) + r * NG)[G] = __half_as_ushort(s16);
+}
+
+template <int NG>
+__global__ void __launch_bounds__(256) store_q4_group_kernel(kvq_cache c, const void* __restrict__ k,
+                                                             const void* __restrict__ v, int dtype, int64_t n_tok,
+                                                             const int32_t* __restrict__ slots, int32_t* status) {
+  pdl_wait();
+  pdl_trigger();
+  store_q4_group_warp<NG>(c, k, v, dtype, n_tok, slots, status,
+                          (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5));
 }
 
 // BF16 comparison format: plain copy / RNE conversion of each value.
@@ -247,17 +255,40 @@ __global__ void __launch_bounds__(128) store_fp8_kernel(kvq_cache c, const void*
   }
 }
 
-// y = blockdiag(H) x; one warp per 32-group.
-__global__ void __launch_bounds__(256) rotate_kernel(const void* __restrict__ x, int dtype, float* y,
-                                                     int64_t n_groups) {
-  pdl_wait();
-  pdl_trigger();
+// y = blockdiag(H) x; one warp per 32-group (group g of the rows).
+__device__ __forceinline__ void rotate_warp(const void* __restrict__ x, int dtype, float* y, int64_t n_groups,
+                                            int64_t g) {
   const int lane = threadIdx.x & 31;
-  const int64_t g = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   if (g >= n_groups) return;
   float v = load_act(x, dtype, g * 32 + lane);
   v = warp_fwht32(v, lane);
   y[g * 32 + lane] = __fmul_rn(v, kHadamardScale);
+}
+
+__global__ void __launch_bounds__(256) rotate_kernel(const void* __restrict__ x, int dtype, float* y,
+                                                     int64_t n_groups) {
+  pdl_wait();
+  pdl_trigger();
+  rotate_warp(x, dtype, y, n_groups, (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5));
+}
+
+// The decode step's two independent preparations in one launch: blocks
+// [0, store_blocks) run the store of the new tokens (one warp per (row,
+// group)), the others rotate the queries.  Same arithmetic, same bytes as
+// store_q4_group_kernel + rotate_kernel.
+template <int NG>
+__global__ void __launch_bounds__(256) store_rotate_kernel(kvq_cache c, const void* __restrict__ k,
+                                                           const void* __restrict__ v, int dtype, int64_t n_tok,
+                                                           const int32_t* __restrict__ slots, int32_t* status,
+                                                           int store_blocks, const void* __restrict__ q,
+                                                           int q_dtype, float* q_out, int64_t q_groups) {
+  pdl_wait();
+  pdl_trigger();
+  const int warps = blockDim.x >> 5, w = threadIdx.x >> 5;
+  if ((int)blockIdx.x < store_blocks)
+    store_q4_group_warp<NG>(c, k, v, dtype, n_tok, slots, status, (int64_t)blockIdx.x * warps + w);
+  else
+    rotate_warp(q, q_dtype, q_out, q_groups, (int64_t)(blockIdx.x - store_blocks) * warps + w);
 }
 
 // ---------------------------------------------------------------- launchers
@@ -296,6 +327,32 @@ cudaError_t launch_store(const kvq_cache& c, const void* k, const void* v, int d
     e = launch_pdl(store_bf16_kernel, dim3(blocks), dim3(256), 0, s, c, k, v, dtype, n_tok, slots, status);
   } else {
     e = launch_pdl(store_fp8_kernel, dim3(n_tok), dim3(128), 0, s, c, k, dtype, n_tok, slots, status);
+  }
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
+bool store_rotate_fits(const kvq_cache& c, int64_t n_tok) {
+  const int ng = c.head_dim / 32;
+  return c.format == KVQ_FMT_Q4_HAD32 && c.head_dim % 32 == 0 && n_tok * c.num_kv_heads * 2 <= kStoreGroupRows &&
+         (ng == 1 || ng == 2 || ng == 4 || ng == 8);
+}
+
+cudaError_t launch_store_rotate(const kvq_cache& c, const void* k, const void* v, int dtype, int64_t n_tok,
+                                const int32_t* slots, int32_t* status, const void* q, int q_dtype, float* q_out,
+                                int64_t q_rows, int q_head_dim, cudaStream_t s) {
+  const int64_t store_warps = n_tok * c.num_kv_heads * 2 * (c.head_dim / 32);
+  const int store_blocks = static_cast<int>((store_warps + 7) / 8);
+  const int64_t q_groups = q_rows * (q_head_dim / 32);
+  const dim3 blocks(store_blocks + static_cast<unsigned>((q_groups + 7) / 8));
+  if (blocks.x == 0) return cudaSuccess;
+  cudaError_t e;
+  switch (c.head_dim / 32) {
+    case 1: e = launch_pdl(store_rotate_kernel<1>, blocks, dim3(256), 0, s, c, k, v, dtype, n_tok, slots, status, store_blocks, q, q_dtype, q_out, q_groups); break;
+    case 2: e = launch_pdl(store_rotate_kernel<2>, blocks, dim3(256), 0, s, c, k, v, dtype, n_tok, slots, status, store_blocks, q, q_dtype, q_out, q_groups); break;
+    case 4: e = launch_pdl(store_rotate_kernel<4>, blocks, dim3(256), 0, s, c, k, v, dtype, n_tok, slots, status, store_blocks, q, q_dtype, q_out, q_groups); break;
+    case 8: e = launch_pdl(store_rotate_kernel<8>, blocks, dim3(256), 0, s, c, k, v, dtype, n_tok, slots, status, store_blocks, q, q_dtype, q_out, q_groups); break;
+    default: return cudaErrorInvalidValue;
   }
   if (e != cudaSuccess) return e;
   return cudaGetLastError();

@@ -136,6 +136,20 @@ int32_t kvq_store(const kvq_cache* cache, const void* k, const void* v, int32_t 
 int32_t kvq_rotate_query(const void* x, int32_t dtype, float* y, int64_t rows, int32_t head_dim,
                          void* stream);
 
+/* kvq_store_rotate -- kvq_store of n_tok new tokens and kvq_rotate_query of
+ * q_rows query rows (of the cache's head_dim) in one launch.  A decode step's
+ * two preparations are independent of each other ([P1] "What it is": pack the
+ * new keys and values; rotate the queries once), so one kernel does both and
+ * the step pays one launch latency instead of two.  Same bytes and the same
+ * rotated values as the two calls.  Arguments as for kvq_store (4-bit format
+ * only) and kvq_rotate_query (q: [q_rows, head_dim] of q_dtype; q_out: fp32;
+ * q_out may equal q when q_dtype is F32).  Only for the few-row form of the
+ * store (n_tok * num_kv_heads * 2 <= 256, head_dim in {32, 64, 128, 256});
+ * otherwise KVQ_ERR_UNSUPPORTED (make the two calls). */
+int32_t kvq_store_rotate(const kvq_cache* cache, const void* k, const void* v, int32_t dtype, int64_t n_tok,
+                         const int32_t* d_slot_mapping, int32_t* d_status, const void* q, int32_t q_dtype,
+                         float* q_out, int64_t q_rows, void* stream);
+
 /* Size in bytes of the workspace kvq_decode_attn needs for this problem:
  * a 256-byte header (status word at offset 0), then partial maxima m and sums z
  * [num_seqs][num_q_heads][P] f32 and partial contexts acc [num_seqs][num_q_heads]

@@ -180,6 +180,28 @@ def test_rotate_query(K):
         np.float64).reshape(-1)).reshape(3, 64), atol=1e-5)
 
 
+def test_store_rotate_equals_store_then_rotate(K):
+    """The fused launch writes the same cache bytes as the oracle's store and the
+    same rotated queries as kvq_rotate_query, bit for bit; skipped slots and a
+    bad slot behave as in kvq_store."""
+    Hk, D, ps, n_pages = 4, 256, 16, 6
+    for n_tok, qdt in ((1, torch.bfloat16), (32, torch.float32)):
+        g, o = make_cache_pair(K, K.FMT_Q4_HAD32, Hk, D, ps, n_pages)
+        k = synth.heavy_tailed((n_tok, Hk, D), "cpu", "sr", n_tok, "k").to(torch.bfloat16)
+        v = synth.heavy_tailed((n_tok, Hk, D), "cpu", "sr", n_tok, "v").to(torch.bfloat16)
+        slots = np.arange(n_tok, dtype=np.int32) * 3 % (n_pages * ps)
+        if n_tok > 1:
+            slots[1] = -1                  # skipped
+            slots[2] = n_pages * ps + 5    # out of range: skipped, flagged
+        q = synth.heavy_tailed((5, 24, D), "cpu", "srq", n_tok).to(qdt)
+        status = torch.zeros(1, dtype=torch.int32, device=DEV)
+        qr = K.store_rotate(g, k.to(DEV), v.to(DEV), torch.from_numpy(slots).to(DEV), q.to(DEV), status=status)
+        O.store(o, to_np_in(k), to_np_in(v), slots)
+        check_planes_equal(g, o)
+        assert torch.equal(qr, K.rotate_query(q.to(DEV)))
+        assert (int(status.item()) != 0) == (n_tok > 1)
+
+
 # --------------------------------------------------------------------------- decode
 
 def decode_case(K, lens, Hk=4, Hq=24, D=256, ps=16, fmt=None, seed=0, dtype=torch.bfloat16, shuffle=True, gen="heavy"):
