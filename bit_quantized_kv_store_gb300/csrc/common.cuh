@@ -23,12 +23,15 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kHadamardScale = 0.17677669529663687f;
 
 // ---------------------------------------------------------------- programmatic dependent launch
-// Every kernel of the library starts with pdl_wait(): it returns once the
+// Every kernel of the library calls pdl_wait() before it reads anything a
+// kernel could have written and before any write: it returns once the
 // preceding kernel in the stream has completed and its memory is visible (at
 // once when there is none), so a kernel launched by launch_pdl may be
 // scheduled while its predecessor drains without reading or overwriting
-// anything early.  Because every kernel waits before it can complete, the
-// ordering is transitive along the stream.
+// anything early.  Only caller metadata that no kernel of the library writes
+// (sequence lengths, block tables) may be read before it (the 4-bit decode
+// does, to overlap those loads with the predecessor).  Every CTA calls it
+// before it can exit, so the ordering is transitive along the stream.
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 // Let the next kernel in the stream be scheduled now (its pdl_wait still waits
 // for this whole grid to complete).  Small kernels call it at once; the large

@@ -287,7 +287,6 @@ __device__ __forceinline__ bool q4_issue_own(const DecodeArgs& a, int b, int kvh
 
 template <bool GATHER>
 __global__ void __launch_bounds__(kQ4Warps * 32, kQ4MinBlocks) decode_q4_round_kernel(const __grid_constant__ DecodeArgs a) {
-  pdl_wait();
   extern __shared__ uint8_t smem_raw[];
   // 1024-byte alignment for the swizzled tiles (the launch adds 1 KB of slack)
   Q4Smem& sm = *reinterpret_cast<Q4Smem*>(smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u));
@@ -295,21 +294,23 @@ __global__ void __launch_bounds__(kQ4Warps * 32, kQ4MinBlocks) decode_q4_round_k
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, t = lane & 3;
 
+  // Metadata first: the lengths and block tables are caller inputs that no
+  // kernel of this library writes, so they are read before the wait on the
+  // previous kernel of the stream (programmatic dependent launch) and their
+  // latency overlaps it.  The cache, the queries and every write come after.
   int32_t T;
+  bool bad_len = false;
   if (GATHER) {
     T = a.n_sel;
   } else {
     T = a.seq_lens[b];
-    if (T < 0 || T > a.max_seq_len || (int64_t)T > (int64_t)a.max_pages * a.c.page_size) {
-      if (threadIdx.x == 0 && p == 0 && kvh == 0) set_status(a.status, KVQ_DEV_BAD_LENGTH);
-      return;  // the merge writes NaN for this sequence
-    }
+    bad_len = T < 0 || T > a.max_seq_len || (int64_t)T > (int64_t)a.max_pages * a.c.page_size;
   }
-  const int nparts = (T + kPart - 1) / kPart;
-  if (p >= nparts) return;
+  const int nparts = bad_len ? 0 : (T + kPart - 1) / kPart;
+  const bool active = p < nparts;  // CTA-uniform
   const int k0 = p * kPart;
   const int k1 = min(k0 + kPart, T);
-  const int ntiles = (k1 - k0 + 15) / 16;
+  const int ntiles = active ? (k1 - k0 + 15) / 16 : 0;
   const int nrounds = (ntiles + kQ4RoundTiles - 1) / kQ4RoundTiles;  // <= 4
   // tile u of warp w in round r: kQ4RoundTiles * r + kQ4TPW * w + u
 
@@ -317,24 +318,31 @@ __global__ void __launch_bounds__(kQ4Warps * 32, kQ4MinBlocks) decode_q4_round_k
   // copies need neither a global load nor a division inside the loop; -1 for a
   // bad page.
   int32_t tile_row = -1;
+  bool bad_page = false;
   if (!GATHER && lane < ntiles) {
     const int key0 = k0 + 16 * lane;
     const int32_t page = a.block_tables[(int64_t)b * a.max_pages + key0 / a.c.page_size];
-    if (page < 0 || page >= a.c.num_pages) {
-      if (warp == 0) set_status(a.status, KVQ_DEV_BAD_PAGE);
-    } else {
+    if (page < 0 || page >= a.c.num_pages)
+      bad_page = true;
+    else
       tile_row = static_cast<int32_t>(((int64_t)page * a.c.num_kv_heads + kvh) * a.c.page_size + key0 % a.c.page_size);
-    }
   }
-
-  if (threadIdx.x == 0) {
+  if (active && threadIdx.x == 0) {
     for (int w = 0; w < kQ4Warps; ++w) mbar_init(&sm.kbar[w], kQ4TPW);
     mbar_init(&sm.vfull, kQ4RoundTiles);
     mbar_init(&sm.vempty, kQ4Warps);
     sm.poison = 0;
     fence_barrier_init();
   }
-  __syncthreads();
+
+  pdl_wait();
+  if (bad_len) {
+    if (threadIdx.x == 0 && p == 0 && kvh == 0) set_status(a.status, KVQ_DEV_BAD_LENGTH);
+    return;  // the merge writes NaN for this sequence
+  }
+  if (!active) return;
+  if (bad_page && warp == 0) set_status(a.status, KVQ_DEV_BAD_PAGE);
+  __syncthreads();  // the mbarriers are initialised
 
   const kvq_cache& c = a.c;
   bool poisoned = q4_issue_own<GATHER>(a, b, kvh, k0, k1, 0, warp, lane, tile_row, &a.tm_k, c.k, c.k_scale,
