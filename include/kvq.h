@@ -185,8 +185,9 @@ int32_t kvq_decode_attn(const kvq_cache* cache, const float* q, int32_t num_seqs
  * is rotated once, then the 4-bit cache is streamed in rotated space), saving the
  * separate kvq_rotate_query launch of a decode step.  Every CTA (one per 512-key
  * partition and KV head) repeats the rotation of its group's queries, so this
- * pays off for short contexts (few partitions) and costs time at long ones
- * (measured: -0.15 us per layer at 32K keys, +6 us at 262K keys).
+ * can pay off only for short contexts (few partitions); with the current
+ * decode kernel it measured slower at both 32K keys (+0.6 us per layer) and
+ * 262K keys (+6 us), so the benchmark step rotates with kvq_store_rotate.
  *   q: device [num_seqs, num_q_heads, 256] of q_dtype (KVQ_DT_F32 or KVQ_DT_BF16),
  *      unrotated.  Each CTA rotates the queries of its GQA group with the
  *      arithmetic of kvq_rotate_query, so the partials equal those of
