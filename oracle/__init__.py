@@ -25,8 +25,9 @@ _LIB_PATH = os.path.join(_HERE, "_build", "libkvq_oracle.so")
 _lock = threading.Lock()
 _lib = None
 
-# Formats and input dtypes, mirrored from the C enums of the oracle.
-Q4, BF16, FP8 = 0, 1, 2
+# Formats and input dtypes, mirrored from the C enums of the oracle.  Q4_0: the
+# 4-bit rows without the rotation.
+Q4, BF16, FP8, Q4_0 = 0, 1, 2, 3
 IN_F32, IN_BF16 = 0, 1
 
 
@@ -74,6 +75,7 @@ def _declare(lib):
         "kvo_rotation_constant": (ctypes.c_float, []),
         "kvo_q4_stored_offset": (_I32, [_I32, _I32, _I32]),
         "kvo_q4_quantize_row": (None, [_P, _I32, _P, _P]),
+        "kvo_q4_0_quantize_row": (None, [_P, _I32, _P, _P]),
         "kvo_q4_canon_to_stored": (None, [_P, _I32, _P]),
         "kvo_q4_dequant_row": (None, [_P, _P, _I32, _P]),
         "kvo_fp8_encode_row": (ctypes.c_float, [_P, _I32, _P]),
@@ -158,13 +160,14 @@ def q4_stored_offset(D, G, h):
     return _L().kvo_q4_stored_offset(D, G, h)
 
 
-def q4_quantize_row(x):
-    """One row of D fp32 values -> (canonical codes [D/2] u8, scales [D/32] fp16 bits)."""
+def q4_quantize_row(x, rotate=True):
+    """One row of D fp32 values -> (canonical codes [D/2] u8, scales [D/32] fp16 bits);
+    rotate=False: the unrotated Q4_0 form."""
     x = _c(x, np.float32)
     D = x.size
     canon = np.empty(D // 2, np.uint8)
     sc = np.empty(D // 32, np.uint16)
-    _L().kvo_q4_quantize_row(_ptr(x), D, _ptr(canon), _ptr(sc))
+    (_L().kvo_q4_quantize_row if rotate else _L().kvo_q4_0_quantize_row)(_ptr(x), D, _ptr(canon), _ptr(sc))
     return canon, sc
 
 
@@ -196,7 +199,7 @@ def fp8_encode_row(x):
 class Cache:
     """A paged KV cache held in numpy arrays, laid out as the library's planes.
 
-    Q4:   k/v codes [num_pages, Hk, page_size, D/2] u8, scales [.., D/32] fp16 bits
+    Q4, Q4_0: k/v codes [num_pages, Hk, page_size, D/2] u8, scales [.., D/32] fp16 bits
     BF16: k/v [num_pages, Hk, page_size, D] bf16 bits, no scales
     FP8:  latent codes [num_pages, page_size, D] u8, rope codes [.., rope] u8,
           latent / rope scales [num_pages, page_size] f32
@@ -206,7 +209,7 @@ class Cache:
         self.fmt, self.Hk, self.D, self.page_size, self.num_pages = fmt, num_kv_heads, head_dim, page_size, num_pages
         self.rope = rope_dim
         rows = (num_pages, num_kv_heads, page_size)
-        if fmt == Q4:
+        if fmt in (Q4, Q4_0):
             self.k = np.zeros(rows + (head_dim // 2,), np.uint8)
             self.v = np.zeros_like(self.k)
             self.k_scale = np.zeros(rows + (head_dim // 32,), np.uint16)

@@ -215,13 +215,15 @@ int kvo_q4_stored_offset(int D, int G, int h) {
 }
 
 /* Quantise one row of D fp32 values (D a multiple of 32) into canonical codes
- * (D/2 bytes) and NG fp16 scales, following R2 and R3. */
-void kvo_q4_quantize_row(const float* x, int D, uint8_t* canon, uint16_t* scales) {
+ * (D/2 bytes) and NG fp16 scales, following R2 and R3; `rotate` = 0 skips the
+ * rotation (the unrotated Q4_0 form of "feat(kvcache): add reliable quantized
+ * KV cache", PR body: 32 values -> 16 bytes + one fp16 scale, symmetric). */
+static void q4_quantize_row(const float* x, int D, uint8_t* canon, uint16_t* scales, int rotate) {
   int NG = D / 32;
   for (int G = 0; G < NG; G++) {
     float y[32];
     for (int i = 0; i < 32; i++) y[i] = x[32 * G + i];
-    kvo_fwht32_f32(y);
+    if (rotate) kvo_fwht32_f32(y);
     float amax = 0.0f;
     for (int i = 0; i < 32; i++) {
       float a = fabsf(y[i]);
@@ -248,6 +250,14 @@ void kvo_q4_quantize_row(const float* x, int D, uint8_t* canon, uint16_t* scales
     for (int b = 0; b < 16; b++)
       canon[16 * G + b] = (uint8_t)(codes[2 * b] | (codes[2 * b + 1] << 4));
   }
+}
+
+void kvo_q4_quantize_row(const float* x, int D, uint8_t* canon, uint16_t* scales) {
+  q4_quantize_row(x, D, canon, scales, 1);
+}
+
+void kvo_q4_0_quantize_row(const float* x, int D, uint8_t* canon, uint16_t* scales) {
+  q4_quantize_row(x, D, canon, scales, 0);
 }
 
 /* Canonical bytes -> stored row bytes (R4 layout). */
@@ -291,11 +301,12 @@ void kvo_q4_dequant_row(const uint8_t* stored, const uint16_t* scales, int D, do
 /* Cache description used by the oracle (its own struct, not the library's).  */
 /* ------------------------------------------------------------------------- */
 
-enum { KVO_Q4 = 0, KVO_BF16 = 1, KVO_FP8 = 2 };
+/* KVO_Q4_0: the 4-bit rows without the rotation (same codes, scales and layout). */
+enum { KVO_Q4 = 0, KVO_BF16 = 1, KVO_FP8 = 2, KVO_Q4_0 = 3 };
 enum { KVO_IN_F32 = 0, KVO_IN_BF16 = 1 };
 
 typedef struct {
-  int format;       /* KVO_Q4, KVO_BF16, KVO_FP8 */
+  int format;       /* KVO_Q4, KVO_BF16, KVO_FP8, KVO_Q4_0 */
   int num_kv_heads; /* FP8: 1 */
   int head_dim;     /* Q4/BF16: D; FP8: latent width */
   int rope_dim;     /* FP8 only */
@@ -371,7 +382,7 @@ int kvo_store(const kvo_cache* c, const void* k, const void* v, int dtype, int64
           uint8_t* canon = (uint8_t*)malloc(D / 2);
           uint8_t* dst = (uint8_t*)(kv ? c->v : c->k) + r * (D / 2);
           uint16_t* sc = (uint16_t*)(kv ? c->v_scale : c->k_scale) + r * (D / 32);
-          kvo_q4_quantize_row(row, D, canon, sc);
+          q4_quantize_row(row, D, canon, sc, c->format == KVO_Q4);
           kvo_q4_canon_to_stored(canon, D, dst);
           free(canon);
         }
@@ -397,7 +408,7 @@ static int load_kv(const kvo_cache* c, const int32_t* bt, int64_t pos, int hd, d
   int D = c->head_dim;
   int64_t r = row_index(c, page, hd, off);
   ensure_tables();
-  if (c->format == KVO_Q4) {
+  if (c->format == KVO_Q4 || c->format == KVO_Q4_0) {
     kvo_q4_dequant_row((const uint8_t*)c->k + r * (D / 2), (const uint16_t*)c->k_scale + r * (D / 32),
                        D, kvec);
     kvo_q4_dequant_row((const uint8_t*)c->v + r * (D / 2), (const uint16_t*)c->v_scale + r * (D / 32),

@@ -186,6 +186,45 @@ def test_exact_scale_block_codes_equal_inputs():
         assert np.array_equal(_canon_codes(canon), c + 8)
 
 
+def test_q4_0_exact_scale_block_codes_equal_inputs():
+    """Unrotated Q4_0 ("feat(kvcache): add reliable quantized KV cache", test fixes:
+    an exact-scale block, amax 8.0 so that the scale is 1.0, has codes equal to
+    the inputs): no rotation, so x itself is the code minus 8."""
+    fig = golden("page_figures.txt")
+    for trial in range(50):
+        c = RNG.integers(-8, 8, 256)
+        c.reshape(8, 32)[:, RNG.integers(0, 32)] = -8        # every group reaches |c| = 8 -> amax 8
+        canon, sc = O.q4_quantize_row(c.astype(np.float32), rotate=False)
+        assert np.all(O.f16_bits_to_f64(sc) == fig["exact_scale_scale"])
+        assert np.array_equal(_canon_codes(canon), c + 8)
+    # and the rotated form of the same input differs (the rotation is really skipped)
+    canon_r, _ = O.q4_quantize_row(c.astype(np.float32), rotate=True)
+    assert not np.array_equal(canon_r, canon)
+
+
+def test_q4_0_attention_is_plain_attention_over_dequantized_rows():
+    """Q4_0: out = softmax(sm q . K) V with K, V the dequantized unrotated rows, and
+    those rows within one scale step of the inputs (half a step, except a
+    positive maximum, whose code 8 is clamped to 7; the fp16 scale may round
+    below amax / 8 by up to 2^-11 relative, hence the (1 + 2^-8) margin)."""
+    Hk, Hq, D, ps, T = 1, 3, 64, 16, 40
+    bt = np.array([2, 0, 3], np.int32)
+    k = RNG.standard_normal((T, Hk, D)).astype(np.float32)
+    v = RNG.standard_normal((T, Hk, D)).astype(np.float32)
+    q = RNG.standard_normal((1, Hq, D)).astype(np.float32)
+    c = O.Cache(O.Q4_0, Hk, D, ps, 4)
+    _fill(c, k, v, bt, T)
+    out = O.decode(c, q, [T], bt[None], 1 / 8)
+    Kd = np.stack([O.q4_dequant_row(c.k[bt[j // ps], 0, j % ps], c.k_scale[bt[j // ps], 0, j % ps]) for j in range(T)])
+    Vd = np.stack([O.q4_dequant_row(c.v[bt[j // ps], 0, j % ps], c.v_scale[bt[j // ps], 0, j % ps]) for j in range(T)])
+    for h in range(Hq):
+        assert np.allclose(out[0, h], _np_attention(q[0, h].astype(np.float64), Kd, Vd, 1 / 8), rtol=1e-12, atol=1e-12)
+    step = np.repeat(np.stack([O.f16_bits_to_f64(c.k_scale[bt[j // ps], 0, j % ps]) for j in range(T)]), 32, 1)
+    err = np.abs(Kd - k[:, 0].astype(np.float64))
+    assert np.all(err <= step * (1 + 2.0**-8))              # fp16 scale may round below amax / 8
+    assert np.mean(err <= 0.5 * step * 1.0001) > 0.95
+
+
 def test_row_bytes_match_page_figures():
     fig = golden("page_figures.txt")
     canon, sc = O.q4_quantize_row(np.ones(256, np.float32))
