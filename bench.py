@@ -50,7 +50,7 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-rows", action="store_true", help="skip the other hot-path rows (batched decode, prefill, "
                     "fp8, bf16 cache, store)")
-    ap.add_argument("--only", choices=["batched", "prefill", "fp8", "bf16"], default=None,
+    ap.add_argument("--only", choices=["batched", "prefill", "fp8", "bf16", "q4_0"], default=None,
                     help="run only one of the other hot-path rows and print its measurement (for profiling)")
     ap.add_argument("--layers", type=int, default=16, help="layers per step (16 for the benchmark; fewer "
                     "only to profile a small case)")
@@ -347,6 +347,8 @@ def measure_rows(K, synth, torch, dev, peak, tflops_peak, only=None):
         out.update(_row_fp8(K, synth, torch, dev, seed))
     if want("bf16"):
         out.update(_row_bf16(K, synth, torch, dev, seed))
+    if want("q4_0"):
+        out.update(_row_q4_0(K, synth, torch, dev, peak, seed))
     return out
 
 
@@ -497,6 +499,34 @@ def _row_bf16(K, synth, torch, dev, seed):
                              "bytes_vs_4bit": byts / (Tb * BYTES_PER_POS_LAYER),
                              "kernel": "decode_bf16_kernel (mma.sync bf16, split query and P)"}
     del c, wsb
+    torch.cuda.empty_cache()
+    return out
+
+
+def _row_q4_0(K, synth, torch, dev, peak, seed):
+    """The unrotated 4-bit format at 32K: the store of 4096 tokens (no rotation) and
+    the decode kernel (the same kernel as the rotated format)."""
+    out = {}
+    Tq = 32769
+    npg = (Tq + PS - 1) // PS
+    c = K.Cache(K.FMT_Q4_0, HK, D, PS, npg, device=dev)
+    k = synth.heavy_tailed((Tq, HK, D), dev, seed, "q0k", subset=(seed, "k"))
+    v = synth.heavy_tailed((Tq, HK, D), dev, seed, "q0v", subset=(seed, "v"))
+    K.store(c, k, v, torch.arange(Tq, dtype=torch.int32, device=dev))
+    sk, sv = k[:4096].contiguous(), v[:4096].contiguous()
+    slots = torch.arange(4096, dtype=torch.int32, device=dev)
+    st_ms = _events_time(torch, lambda: K.store(c, sk, sv, slots), 10)
+    q = synth.heavy_tailed((1, HQ, D), dev, seed, "q0q").float()
+    bt = torch.arange(npg, dtype=torch.int32, device=dev).reshape(1, -1)
+    seq = torch.tensor([Tq], dtype=torch.int32, device=dev)
+    ws = K.alloc_workspace(c, 1, HQ, Tq, device=dev)
+    dms = _events_time(torch, lambda: K.decode_attn(c, q, seq, bt, Tq, 1 / 16, ws), 10)
+    byts = Tq * BYTES_PER_POS_LAYER
+    out["q4_0_cache_32k"] = {"workload": "unrotated 4-bit cache (Q4_0), context 32768, 1 layer, same split-T + merge",
+                             "decode_kernel_us": dms * 1e3, "cache_bytes": byts,
+                             "achieved_GBs": byts / (dms * 1e-3) / 1e9, "frac_of_hbm_peak": byts / (dms * 1e-3) / 1e9 / peak,
+                             "store_4096_tokens_us": st_ms * 1e3, "kernel": "decode_q4_round_kernel"}
+    del c, ws
     torch.cuda.empty_cache()
     return out
 

@@ -18,7 +18,7 @@ LIB_PATH = os.path.join(_PKG, "_build", "libkvq.so")
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_WORKSPACE_TOO_SMALL = 0, -1, -2, -3, -4
 DEV_BAD_SLOT, DEV_BAD_PAGE, DEV_BAD_LENGTH, DEV_BAD_INDEX, DEV_TIMEOUT = 1, 2, 4, 8, 16
 DT_F32, DT_BF16 = 0, 1
-FMT_Q4_HAD32, FMT_BF16, FMT_FP8_ROW = 0, 1, 2
+FMT_Q4_HAD32, FMT_BF16, FMT_FP8_ROW, FMT_Q4_0 = 0, 1, 2, 3  # Q4_0: the 4-bit rows without the rotation
 
 _P = ctypes.c_void_p
 _I32 = ctypes.c_int32
@@ -117,7 +117,7 @@ class Cache:
         self.fmt, self.Hk, self.D, self.page_size, self.num_pages = fmt, num_kv_heads, head_dim, page_size, num_pages
         self.rope = rope_dim
         rows = (num_pages, num_kv_heads, page_size)
-        if fmt == FMT_Q4_HAD32:
+        if fmt in (FMT_Q4_HAD32, FMT_Q4_0):
             self.k = torch.zeros(rows + (head_dim // 2,), dtype=torch.uint8, device=device)
             self.v = torch.zeros_like(self.k)
             self.k_scale = torch.zeros(rows + (head_dim // 32,), dtype=torch.float16, device=device)

@@ -19,18 +19,21 @@ int32_t record_cuda_failure(cudaError_t e) { return cuda_fail(e); }
 
 static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// The two 4-bit formats share planes, layout and kernels (Q4_0 without the rotation).
+static bool is_q4(int32_t f) { return f == KVQ_FMT_Q4_HAD32 || f == KVQ_FMT_Q4_0; }
+
 static size_t round256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
 // Validate a cache description; returns KVQ_OK or a negative status.
 static int32_t check_cache(const kvq_cache* c) {
   if (!c) return KVQ_ERR_INVALID_ARG;
-  if (c->format < KVQ_FMT_Q4_HAD32 || c->format > KVQ_FMT_FP8_ROW) return KVQ_ERR_INVALID_ARG;
+  if (c->format < KVQ_FMT_Q4_HAD32 || c->format > KVQ_FMT_Q4_0) return KVQ_ERR_INVALID_ARG;
   if (c->num_kv_heads < 1 || c->head_dim <= 0 || c->page_size <= 0 || c->num_pages < 0)
     return KVQ_ERR_INVALID_ARG;
   if (c->head_dim % 32 != 0) return KVQ_ERR_UNSUPPORTED;  // rows are built from 32-value groups
   if (c->page_size % 16 != 0) return KVQ_ERR_UNSUPPORTED;
   if (!c->k || !c->v || !aligned16(c->k) || !aligned16(c->v)) return KVQ_ERR_INVALID_ARG;
-  if (c->format == KVQ_FMT_Q4_HAD32) {
+  if (is_q4(c->format)) {
     if (!c->k_scale || !c->v_scale || !aligned16(c->k_scale) || !aligned16(c->v_scale)) return KVQ_ERR_INVALID_ARG;
     const int ng = c->head_dim / 32;
     if (ng != 1 && ng != 2 && ng != 4 && ng != 8) return KVQ_ERR_UNSUPPORTED;
@@ -105,7 +108,7 @@ static int32_t check_decode_shape(const kvq_cache* c, int B, int Hq, const int32
   if (gather && (n_sel < 1 || n_sel > 4096)) return KVQ_ERR_INVALID_ARG;
   if (!gather && n_sel != 0) return KVQ_ERR_INVALID_ARG;
   const int group = Hq / c->num_kv_heads;
-  if (c->format == KVQ_FMT_Q4_HAD32 || c->format == KVQ_FMT_BF16) {
+  if (is_q4(c->format) || c->format == KVQ_FMT_BF16) {
     if (c->head_dim != 256 || group > 8) return KVQ_ERR_UNSUPPORTED;
   } else {
     if (c->head_dim != 512 || c->rope_dim != 64 || Hq % 16 != 0) return KVQ_ERR_UNSUPPORTED;
@@ -140,6 +143,7 @@ size_t kvq_plane_bytes(const kvq_cache* c, int32_t plane) {
   const size_t rows = static_cast<size_t>(c->num_pages) * c->num_kv_heads * c->page_size;
   switch (c->format) {
     case KVQ_FMT_Q4_HAD32:
+    case KVQ_FMT_Q4_0:
       return (plane == 0 || plane == 2) ? rows * (c->head_dim / 2) : rows * (c->head_dim / 32) * 2;
     case KVQ_FMT_BF16:
       return (plane == 0 || plane == 2) ? rows * c->head_dim * 2 : 0;
@@ -240,6 +244,7 @@ static int32_t decode_attn_impl(const kvq_cache* cache, const float* q, const vo
     a.qscale = sm_scale * kLog2e;
     a.q_raw = q_raw;
     a.q_dtype = q_dtype;
+    a.q_rotate = cache->format == KVQ_FMT_Q4_HAD32 ? 1 : 0;
     a.ws_m = reinterpret_cast<float*>(ws + w.m_off);
     a.ws_z = reinterpret_cast<float*>(ws + w.z_off);
     a.ws_acc = reinterpret_cast<float*>(ws + w.acc_off);
@@ -275,7 +280,7 @@ int32_t kvq_decode_attn_unrotated(const kvq_cache* cache, const void* q, int32_t
                                   int32_t num_q_heads, const int32_t* d_seq_lens, const int32_t* d_block_tables,
                                   int32_t max_pages_per_seq, int32_t max_seq_len, const int32_t* d_sel,
                                   int32_t n_sel, float sm_scale, void* workspace, size_t ws_bytes, void* stream) {
-  if (!cache || cache->format != KVQ_FMT_Q4_HAD32) return cache ? KVQ_ERR_UNSUPPORTED : KVQ_ERR_INVALID_ARG;
+  if (!cache || !is_q4(cache->format)) return cache ? KVQ_ERR_UNSUPPORTED : KVQ_ERR_INVALID_ARG;
   if (q_dtype != KVQ_DT_F32 && q_dtype != KVQ_DT_BF16) return KVQ_ERR_INVALID_ARG;
   if (num_seqs > 0 && !q) return KVQ_ERR_INVALID_ARG;
   return decode_attn_impl(cache, nullptr, q, q_dtype, num_seqs, num_q_heads, d_seq_lens, d_block_tables,
@@ -308,7 +313,7 @@ int32_t kvq_prefill_attn(const kvq_cache* cache, const void* q, int32_t dtype, i
                          int32_t* d_status, void* stream) {
   int32_t st = check_cache(cache);
   if (st != KVQ_OK) return st;
-  if (cache->format != KVQ_FMT_Q4_HAD32 || cache->head_dim != 256) return KVQ_ERR_UNSUPPORTED;
+  if (!is_q4(cache->format) || cache->head_dim != 256) return KVQ_ERR_UNSUPPORTED;
   if (n_q < 0 || q_start < 0 || num_q_heads < 1 || num_q_heads % cache->num_kv_heads != 0) return KVQ_ERR_INVALID_ARG;
   if (dtype != KVQ_DT_F32 && dtype != KVQ_DT_BF16) return KVQ_ERR_INVALID_ARG;
   if (num_q_heads / cache->num_kv_heads > 8) return KVQ_ERR_UNSUPPORTED;
@@ -329,6 +334,7 @@ int32_t kvq_prefill_attn(const kvq_cache* cache, const void* q, int32_t dtype, i
   a.qscale = sm_scale * kLog2e;
   a.out = out;
   a.status = d_status;
+  a.rotate = cache->format == KVQ_FMT_Q4_HAD32 ? 1 : 0;
   {
     const uint64_t rows = static_cast<uint64_t>(cache->num_pages) * cache->num_kv_heads * cache->page_size;
     if (rows >= (1ull << 31)) return KVQ_ERR_UNSUPPORTED;

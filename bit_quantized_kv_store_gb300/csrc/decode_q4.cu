@@ -122,10 +122,8 @@ __device__ __forceinline__ void q4_query_prep(const DecodeArgs& a, int b, int kv
 #pragma unroll
     for (int k = 0; k < kPairs; ++k) {
       const int hg = warp + kWarps * k;
-      if (hg < npairs) {  // warp-uniform
-        const float x = warp_fwht32(xs[k], lane);
-        qrot[32 * hg + lane] = __fmul_rn(x, kHadamardScale);
-      }
+      if (hg < npairs)  // warp-uniform
+        qrot[32 * hg + lane] = a.q_rotate ? __fmul_rn(warp_fwht32(xs[k], lane), kHadamardScale) : xs[k];
     }
     __syncthreads();
     qsrc = qrot;

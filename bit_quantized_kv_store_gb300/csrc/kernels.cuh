@@ -26,6 +26,7 @@ struct DecodeArgs {
   const void* q_raw;  // 4-bit format only: unrotated query [B, Hq, 256] of q_dtype, rotated in
                       // the kernel (then q is unused); NULL: q is already rotated
   int q_dtype;
+  int q_rotate;       // q_raw only: 1 rotate it (Hadamard format), 0 use it as given (Q4_0)
   float* ws_m;
   float* ws_z;
   float* ws_acc;
@@ -65,6 +66,7 @@ struct PrefillArgs {
   float qscale;
   float* out;
   int32_t* status;
+  int rotate;  // 1: Hadamard format (rotate q, rotate the output back); 0: Q4_0
 };
 
 // Remember a failed CUDA call for kvq_last_cuda_error(); returns KVQ_ERR_CUDA.

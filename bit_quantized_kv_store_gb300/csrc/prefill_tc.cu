@@ -231,12 +231,13 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_tc_kernel(const __grid_
                                     : __bfloat162float(static_cast<const __nv_bfloat16*>(a.q)[qrow + 32 * G + i]);
         x[i] = v;
       }
-      fwht32_regs(x);
+      const bool rot = a.rotate != 0;  // Q4_0: the query as given
+      if (rot) fwht32_regs(x);
       uint32_t hi[16], lo[16];
 #pragma unroll
       for (int i = 0; i < 16; ++i) {
-        const float x0 = __fmul_rn(x[2 * i], kHadamardScale) * a.qscale;
-        const float x1 = __fmul_rn(x[2 * i + 1], kHadamardScale) * a.qscale;
+        const float x0 = (rot ? __fmul_rn(x[2 * i], kHadamardScale) : x[2 * i]) * a.qscale;
+        const float x1 = (rot ? __fmul_rn(x[2 * i + 1], kHadamardScale) : x[2 * i + 1]) * a.qscale;
         split_f16(x0, x1, hi[i], lo[i]);
       }
       __syncwarp();  // the tensor-memory store is warp-collective
@@ -447,15 +448,18 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_tc_kernel(const __grid_
         float x[32];
 #pragma unroll
         for (int i = 0; i < 32; ++i) x[i] = __uint_as_float(o[i]) * inv;
-        fwht32_regs(x);
+        const bool rot = a.rotate != 0;  // Q4_0: nothing to rotate back
+        if (rot) {
+          fwht32_regs(x);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) x[i] = __fmul_rn(x[i], kHadamardScale);
+        }
         if (valid) {
           float* dst = a.out + ((int64_t)(q0 + iq) * a.Hq + kvh * grp + h) * kPfDim + 32 * G;
 #pragma unroll
           for (int i = 0; i < 32; i += 4)
             *reinterpret_cast<float4*>(dst + i) =
-                bad ? make_float4(NAN, NAN, NAN, NAN)
-                    : make_float4(__fmul_rn(x[i], kHadamardScale), __fmul_rn(x[i + 1], kHadamardScale),
-                                  __fmul_rn(x[i + 2], kHadamardScale), __fmul_rn(x[i + 3], kHadamardScale));
+                bad ? make_float4(NAN, NAN, NAN, NAN) : make_float4(x[i], x[i + 1], x[i + 2], x[i + 3]);
         }
       }
     }

@@ -24,8 +24,9 @@ __device__ __forceinline__ float load_act(const void* p, int dtype, int64_t i) {
 }
 
 // One warp per (token, KV head, K|V) row of D = 32*NG values.
-// Lane i handles element 32G + i of every group G.
-template <int NG>
+// Lane i handles element 32G + i of every group G.  ROT = false: the unrotated
+// Q4_0 format (the values as given).
+template <int NG, bool ROT>
 __global__ void __launch_bounds__(256) store_q4_kernel(kvq_cache c, const void* __restrict__ k,
                                                        const void* __restrict__ v, int dtype, int64_t n_tok,
                                                        const int32_t* __restrict__ slots, int32_t* status) {
@@ -56,8 +57,7 @@ __global__ void __launch_bounds__(256) store_q4_kernel(kvq_cache c, const void* 
 #pragma unroll
   for (int G = 0; G < NG; ++G) {
     float x = load_act(src, dtype, base + 32 * G + lane);
-    x = warp_fwht32(x, lane);
-    const float y = __fmul_rn(x, kHadamardScale);
+    const float y = ROT ? __fmul_rn(warp_fwht32(x, lane), kHadamardScale) : x;
     float amax = fabsf(y);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
@@ -112,7 +112,7 @@ __global__ void __launch_bounds__(256) store_q4_kernel(kvq_cache c, const void* 
 // token): one warp per (row, group), so the groups of a row are packed in
 // parallel instead of one after another.  Same arithmetic, same bytes.
 // Warp `wid` of the store: (row, group) = (wid / NG, wid % NG).
-template <int NG>
+template <int NG, bool ROT>
 __device__ __forceinline__ void store_q4_group_warp(const kvq_cache& c, const void* __restrict__ k,
                                                     const void* __restrict__ v, int dtype, int64_t n_tok,
                                                     const int32_t* __restrict__ slots, int32_t* status, int64_t wid) {
@@ -136,8 +136,7 @@ __device__ __forceinline__ void store_q4_group_warp(const kvq_cache& c, const vo
   const int64_t r = (page * Hk + head) * c.page_size + off;
   const void* src = kv ? v : k;
   float x = load_act(src, dtype, (tok * Hk + head) * D + 32 * G + lane);
-  x = warp_fwht32(x, lane);
-  const float y = __fmul_rn(x, kHadamardScale);
+  const float y = ROT ? __fmul_rn(warp_fwht32(x, lane), kHadamardScale) : x;
   float amax = fabsf(y);
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
@@ -162,14 +161,14 @@ __device__ __forceinline__ void store_q4_group_warp(const kvq_cache& c, const vo
   if (lane == 0) (static_cast<uint16_t*>(kv ? c.v_scale : c.k_scale) + r * NG)[G] = __half_as_ushort(s16);
 }
 
-template <int NG>
+template <int NG, bool ROT>
 __global__ void __launch_bounds__(256) store_q4_group_kernel(kvq_cache c, const void* __restrict__ k,
                                                              const void* __restrict__ v, int dtype, int64_t n_tok,
                                                              const int32_t* __restrict__ slots, int32_t* status) {
   pdl_wait();
   pdl_trigger();
-  store_q4_group_warp<NG>(c, k, v, dtype, n_tok, slots, status,
-                          (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5));
+  store_q4_group_warp<NG, ROT>(c, k, v, dtype, n_tok, slots, status,
+                               (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5));
 }
 
 // BF16 comparison format: plain copy / RNE conversion of each value.
@@ -286,7 +285,7 @@ __global__ void __launch_bounds__(256) store_rotate_kernel(kvq_cache c, const vo
   pdl_trigger();
   const int warps = blockDim.x >> 5, w = threadIdx.x >> 5;
   if ((int)blockIdx.x < store_blocks)
-    store_q4_group_warp<NG>(c, k, v, dtype, n_tok, slots, status, (int64_t)blockIdx.x * warps + w);
+    store_q4_group_warp<NG, true>(c, k, v, dtype, n_tok, slots, status, (int64_t)blockIdx.x * warps + w);
   else
     rotate_warp(q, q_dtype, q_out, q_groups, (int64_t)(blockIdx.x - store_blocks) * warps + w);
 }
@@ -300,26 +299,36 @@ cudaError_t launch_store(const kvq_cache& c, const void* k, const void* v, int d
                          const int32_t* slots, int32_t* status, cudaStream_t s) {
   if (n_tok == 0) return cudaSuccess;
   cudaError_t e = cudaSuccess;
-  if (c.format == KVQ_FMT_Q4_HAD32 && n_tok * c.num_kv_heads * 2 <= kStoreGroupRows) {
+  const bool q4 = c.format == KVQ_FMT_Q4_HAD32 || c.format == KVQ_FMT_Q4_0;
+  const bool rot = c.format == KVQ_FMT_Q4_HAD32;
+  if (q4 && n_tok * c.num_kv_heads * 2 <= kStoreGroupRows) {
     const int64_t warps = n_tok * c.num_kv_heads * 2 * (c.head_dim / 32);
     const dim3 blocks((warps + 7) / 8);
+#define KVQ_STORE_GROUP(NG)                                                                                      \
+  e = rot ? launch_pdl(store_q4_group_kernel<NG, true>, blocks, dim3(256), 0, s, c, k, v, dtype, n_tok, slots, status) \
+          : launch_pdl(store_q4_group_kernel<NG, false>, blocks, dim3(256), 0, s, c, k, v, dtype, n_tok, slots, status)
     switch (c.head_dim / 32) {
-      case 1: e = launch_pdl(store_q4_group_kernel<1>, blocks, dim3(256), 0, s, c, k, v, dtype, n_tok, slots, status); break;
-      case 2: e = launch_pdl(store_q4_group_kernel<2>, blocks, dim3(256), 0, s, c, k, v, dtype, n_tok, slots, status); break;
-      case 4: e = launch_pdl(store_q4_group_kernel<4>, blocks, dim3(256), 0, s, c, k, v, dtype, n_tok, slots, status); break;
-      case 8: e = launch_pdl(store_q4_group_kernel<8>, blocks, dim3(256), 0, s, c, k, v, dtype, n_tok, slots, status); break;
+      case 1: KVQ_STORE_GROUP(1); break;
+      case 2: KVQ_STORE_GROUP(2); break;
+      case 4: KVQ_STORE_GROUP(4); break;
+      case 8: KVQ_STORE_GROUP(8); break;
       default: return cudaErrorInvalidValue;
     }
-  } else if (c.format == KVQ_FMT_Q4_HAD32) {
+#undef KVQ_STORE_GROUP
+  } else if (q4) {
     const int64_t rows = n_tok * c.num_kv_heads * 2;
-    const int64_t blocks = (rows + 7) / 8;
+    const dim3 blocks((rows + 7) / 8);
+#define KVQ_STORE_ROW(NG)                                                                                   \
+  e = rot ? launch_pdl(store_q4_kernel<NG, true>, blocks, dim3(256), 0, s, c, k, v, dtype, n_tok, slots, status) \
+          : launch_pdl(store_q4_kernel<NG, false>, blocks, dim3(256), 0, s, c, k, v, dtype, n_tok, slots, status)
     switch (c.head_dim / 32) {
-      case 1: e = launch_pdl(store_q4_kernel<1>, dim3(blocks), dim3(256), 0, s, c, k, v, dtype, n_tok, slots, status); break;
-      case 2: e = launch_pdl(store_q4_kernel<2>, dim3(blocks), dim3(256), 0, s, c, k, v, dtype, n_tok, slots, status); break;
-      case 4: e = launch_pdl(store_q4_kernel<4>, dim3(blocks), dim3(256), 0, s, c, k, v, dtype, n_tok, slots, status); break;
-      case 8: e = launch_pdl(store_q4_kernel<8>, dim3(blocks), dim3(256), 0, s, c, k, v, dtype, n_tok, slots, status); break;
+      case 1: KVQ_STORE_ROW(1); break;
+      case 2: KVQ_STORE_ROW(2); break;
+      case 4: KVQ_STORE_ROW(4); break;
+      case 8: KVQ_STORE_ROW(8); break;
       default: return cudaErrorInvalidValue;
     }
+#undef KVQ_STORE_ROW
   } else if (c.format == KVQ_FMT_BF16) {
     const int64_t total = n_tok * c.num_kv_heads * c.head_dim;
     int64_t blocks = (total + 255) / 256;

@@ -77,6 +77,12 @@ typedef enum { KVQ_DT_F32 = 0, KVQ_DT_BF16 = 1 } kvq_dtype;
  *   32G+4h .. 32G+4h+3) is stored at byte offset 2 * (h * D/32 + G).
  *   Scale plane: row r occupies D/32 fp16 values at r * D/32, in group order.
  *   For D = 256 a row is 128 + 16 = 144 bytes.
+ * KVQ_FMT_Q4_0 ([P2] PR body: 32 values -> 16 bytes + one fp16 scale, symmetric;
+ *   the same shape as GGUF's Q4_0): KVQ_FMT_Q4_HAD32 without the rotation -- the
+ *   same codes, scales and planes computed on the values as given.  Queries are
+ *   used as given (kvq_rotate_query is not needed; kvq_decode_attn_unrotated and
+ *   kvq_prefill_attn skip their rotations) and nothing is rotated back
+ *   (kvq_merge with rotate_back = 0).
  * KVQ_FMT_BF16: unrotated bf16 rows of D values (the uncompressed comparison).
  * KVQ_FMT_FP8_ROW ([P3] KV8 base commit): one latent row per position (num_kv_heads
  *   must be 1): head_dim latent values ("Lc") and rope_dim rope values ("Rc"), each
@@ -88,7 +94,7 @@ typedef enum { KVQ_DT_F32 = 0, KVQ_DT_BF16 = 1 } kvq_dtype;
  * Row index of (page, kv_head, slot) in every plane:
  *   r = (page * num_kv_heads + kv_head) * page_size + slot.
  * A token's slot number is page * page_size + slot; block tables list page ids. */
-typedef enum { KVQ_FMT_Q4_HAD32 = 0, KVQ_FMT_BF16 = 1, KVQ_FMT_FP8_ROW = 2 } kvq_format;
+typedef enum { KVQ_FMT_Q4_HAD32 = 0, KVQ_FMT_BF16 = 1, KVQ_FMT_FP8_ROW = 2, KVQ_FMT_Q4_0 = 3 } kvq_format;
 
 typedef struct kvq_cache {
   int32_t format;       /* kvq_format */

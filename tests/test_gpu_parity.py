@@ -49,7 +49,7 @@ def assert_close(got, ref, tol=TOL, what=""):
 
 def make_cache_pair(K, fmt, Hk, D, ps, n_pages, rope=0):
     g = K.Cache(fmt, Hk, D, ps, n_pages, device=DEV, rope_dim=rope)
-    ofmt = {K.FMT_Q4_HAD32: O.Q4, K.FMT_BF16: O.BF16, K.FMT_FP8_ROW: O.FP8}[fmt]
+    ofmt = {K.FMT_Q4_HAD32: O.Q4, K.FMT_BF16: O.BF16, K.FMT_FP8_ROW: O.FP8, K.FMT_Q4_0: O.Q4_0}[fmt]
     o = O.Cache(ofmt, Hk, D, ps, n_pages, rope_dim=rope)
     return g, o
 
@@ -94,6 +94,42 @@ def test_store_q4_bit_exact(K, D, dtype, T):
     fill_sequence(K, g, o, k, v, bt, T)
     torch.cuda.synchronize()
     check_planes_equal(g, o)
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+@pytest.mark.parametrize("T", [250, 20])
+def test_store_q4_0_bit_exact(K, dtype, T):
+    """The unrotated 4-bit format: codes and scales bit-exact with the oracle,
+    through the row kernel (250 tokens) and the (row, group) kernel (20)."""
+    Hk, D, ps, n_pages = 3, 256, 32, 9
+    k = synth.outlier_normal((T, Hk, D), 4, 20.0, "cpu", D, "k0").to(dtype)
+    v = synth.heavy_tailed((T, Hk, D), "cpu", D, "v0").to(dtype)
+    g, o = make_cache_pair(K, K.FMT_Q4_0, Hk, D, ps, n_pages)
+    bt = synth.page_permutation(n_pages, D, "pages0").numpy().astype(np.int32)
+    fill_sequence(K, g, o, k, v, bt, T)
+    torch.cuda.synchronize()
+    check_planes_equal(g, o)
+
+
+def test_store_q4_0_exact_scale_block(K):
+    """Q4_0 exact-scale rows (amax 8 -> scale 1.0): the stored codes are the inputs
+    plus 8, with no rotation in between."""
+    Hk, D, ps = 1, 256, 16
+    c = np.random.default_rng(5).integers(-8, 8, (3, Hk, D))
+    c.reshape(3, 8, 32)[:, :, 0] = -8
+    g = K.Cache(K.FMT_Q4_0, Hk, D, ps, 1, device=DEV)
+    K.store(g, torch.from_numpy(c.astype(np.float32)).to(DEV), torch.from_numpy(c.astype(np.float32)).to(DEV),
+            torch.arange(3, dtype=torch.int32, device=DEV))
+    torch.cuda.synchronize()
+    assert torch.all(g.k_scale[0, 0, :3] == 1.0)
+    # stored half-word (G, h) holds elements 32G + 4h .. + 3 (low nibble first)
+    st = g.k[0, 0, :3].cpu().numpy()
+    for G in range(8):
+        for h in range(8):
+            o_ = 2 * (h * 8 + G)
+            got = [st[:, o_] & 15, st[:, o_] >> 4, st[:, o_ + 1] & 15, st[:, o_ + 1] >> 4]
+            for j in range(4):
+                assert np.array_equal(got[j], c[:, 0, 32 * G + 4 * h + j] + 8)
 
 
 def test_store_q4_exact_scale_and_edge_rows(K):
@@ -329,6 +365,33 @@ def test_decode_gather(K):
             assert_close(out[b], ref[b], what=f"gather n_sel={n_sel} seq {b}")
 
 
+@pytest.mark.parametrize("lens", [[1], [17, 513], [1025, 3000]])
+def test_decode_q4_0(K, lens):
+    """The unrotated 4-bit format through the same decode kernel and merge (no
+    rotation anywhere), against the oracle; also the unrotated-query entry point,
+    which must leave the query as given."""
+    g, o, bt, q, ml = decode_case(K, lens, fmt=K.FMT_Q4_0, seed=31)
+    out, ws = run_decode(K, g, bt, q, lens, ml, 1 / 16)
+    ref = O.decode(o, to_np_in(q), lens, bt, 1 / 16)
+    for b in range(len(lens)):
+        assert_close(out[b], ref[b], what=f"Q4_0 seq {b}")
+    seq = torch.tensor(lens, dtype=torch.int32, device=DEV)
+    ws2 = K.alloc_workspace(g, len(lens), q.shape[1], ml, device=DEV)
+    K.decode_attn_unrotated(g, q.to(DEV), seq, torch.from_numpy(bt).to(DEV), ml, 1 / 16, ws2)
+    torch.cuda.synchronize()
+    assert torch.equal(ws, ws2)
+
+
+def test_decode_q4_0_gather(K):
+    lens = [2000, 700]
+    g, o, bt, q, ml = decode_case(K, lens, fmt=K.FMT_Q4_0, seed=33)
+    sel = np.stack([synth.distinct_sorted(300, L, 33, b).numpy() for b, L in enumerate(lens)]).astype(np.int32)
+    out, _ = run_decode(K, g, bt, q, lens, ml, 1 / 16, sel=sel)
+    ref = O.decode(o, to_np_in(q), lens, bt, 1 / 16, sel=sel)
+    for b in range(2):
+        assert_close(out[b], ref[b], what=f"Q4_0 gather seq {b}")
+
+
 def test_decode_bad_page_and_length_are_flagged(K):
     lens = [600, 300]
     g, o, bt, q, ml = decode_case(K, lens, seed=4)
@@ -439,6 +502,26 @@ def test_prefill(K, depth, n_q):
     got = out.cpu().numpy()
     for i in range(n_q):
         assert_close(got[i], ref[i], what=f"prefill row {i}")
+
+
+def test_prefill_q4_0(K):
+    """Prefill over the unrotated 4-bit format: the query and the output are used
+    as given (no rotations), against the oracle."""
+    Hk, Hq, D, ps, depth, n_q = 4, 24, 256, 16, 300, 70
+    T = depth + n_q
+    n_pages = (T + ps - 1) // ps + 1
+    g, o = make_cache_pair(K, K.FMT_Q4_0, Hk, D, ps, n_pages)
+    bt = synth.page_permutation(n_pages, "pf0", depth).numpy().astype(np.int32)
+    k = synth.heavy_tailed((T, Hk, D), "cpu", "pfk0", depth)
+    v = synth.heavy_tailed((T, Hk, D), "cpu", "pfv0", depth)
+    fill_sequence(K, g, o, k, v, bt, T)
+    q = synth.heavy_tailed((n_q, Hq, D), "cpu", "pfq0", depth)
+    out = K.prefill_attn(g, q.to(DEV), depth, torch.from_numpy(bt).to(DEV), 1 / 16)
+    torch.cuda.synchronize()
+    ref = O.prefill(o, to_np_in(q), depth, bt, 1 / 16)
+    got = out.cpu().numpy()
+    for i in range(n_q):
+        assert_close(got[i], ref[i], what=f"Q4_0 prefill row {i}")
 
 
 @pytest.mark.parametrize("Hk,Hq,depth,n_q", [(2, 16, 70, 33), (3, 3, 200, 129), (1, 5, 0, 64)])
