@@ -50,7 +50,7 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-rows", action="store_true", help="skip the other hot-path rows (batched decode, prefill, "
                     "fp8, bf16 cache, store)")
-    ap.add_argument("--only", choices=["batched", "prefill", "fp8", "bf16", "q4_0"], default=None,
+    ap.add_argument("--only", choices=["batched", "prefill", "fp8", "bf16", "q4_0", "window"], default=None,
                     help="run only one of the other hot-path rows and print its measurement (for profiling)")
     ap.add_argument("--layers", type=int, default=16, help="layers per step (16 for the benchmark; fewer "
                     "only to profile a small case)")
@@ -349,6 +349,8 @@ def measure_rows(K, synth, torch, dev, peak, tflops_peak, only=None):
         out.update(_row_bf16(K, synth, torch, dev, seed))
     if want("q4_0"):
         out.update(_row_q4_0(K, synth, torch, dev, peak, seed))
+    if want("window"):
+        out.update(_row_window(K, synth, torch, dev, peak, seed))
     return out
 
 
@@ -526,6 +528,40 @@ def _row_q4_0(K, synth, torch, dev, peak, seed):
                              "decode_kernel_us": dms * 1e3, "cache_bytes": byts,
                              "achieved_GBs": byts / (dms * 1e-3) / 1e9, "frac_of_hbm_peak": byts / (dms * 1e-3) / 1e9 / peak,
                              "store_4096_tokens_us": st_ms * 1e3, "kernel": "decode_q4_round_kernel"}
+    del c, ws
+    torch.cuda.empty_cache()
+    return out
+
+
+def _row_window(K, synth, torch, dev, peak, seed):
+    """Decode window (speculative verify): 4 draft rows of one sequence at context
+    262144 sharing its block table; the window call against the same rows decoded
+    as 4 independent sequences (block table repeated, sequence-major order) and
+    against one row."""
+    out = {}
+    R, T0 = 4, 262144
+    T = T0 + R
+    npg = (T + PS - 1) // PS
+    c = K.Cache(K.FMT_Q4_HAD32, HK, D, PS, npg, device=dev)
+    for s0 in range(0, T, 65536):
+        n = min(65536, T - s0)
+        k = synth.heavy_tailed((n, HK, D), dev, seed, "wk", s0, subset=(seed, "k"))
+        v = synth.heavy_tailed((n, HK, D), dev, seed, "wv", s0, subset=(seed, "v"))
+        K.store(c, k, v, torch.arange(s0, s0 + n, dtype=torch.int32, device=dev))
+    q = K.rotate_query(synth.heavy_tailed((R, HQ, D), dev, seed, "wq"))
+    bt = torch.arange(npg, dtype=torch.int32, device=dev)
+    lens = torch.arange(T0 + 1, T + 1, dtype=torch.int32, device=dev)
+    ws = K.alloc_workspace(c, R, HQ, T, device=dev)
+    win_ms = _events_time(torch, lambda: K.decode_window(c, q, lens, bt, T, 1 / 16, ws), 10)
+    bt_rep = bt.reshape(1, -1).repeat(R, 1).contiguous()
+    rows_ms = _events_time(torch, lambda: K.decode_attn(c, q, lens, bt_rep, T, 1 / 16, ws), 10)
+    one_ms = _events_time(torch, lambda: K.decode_attn(c, q[:1], lens[:1], bt_rep[:1], T, 1 / 16, ws), 10)
+    byts = T0 * BYTES_PER_POS_LAYER
+    out["decode_window_262k"] = {
+        "workload": "4 draft rows at positions 262144..262147 of one sequence, shared block table, 1 layer",
+        "window_us": win_ms * 1e3, "as_4_sequences_us": rows_ms * 1e3, "one_row_us": one_ms * 1e3,
+        "window_us_per_row": win_ms * 1e3 / R, "cache_GBs_once": byts / (win_ms * 1e-3) / 1e9,
+        "kernel": "decode_q4_round_kernel (rows of a partition adjacent in the grid)"}
     del c, ws
     torch.cuda.empty_cache()
     return out

@@ -44,6 +44,7 @@ SIGNATURES = {
     "kvq_decode_workspace_size": (_SZ, [ctypes.POINTER(CacheDesc), _I32, _I32, _I32, _I32]),
     "kvq_decode_attn": (_I32, [ctypes.POINTER(CacheDesc), _P, _I32, _I32, _P, _P, _I32, _I32, _P, _I32, _F, _P,
                                _SZ, _P]),
+    "kvq_decode_window": (_I32, [ctypes.POINTER(CacheDesc), _P, _I32, _I32, _P, _P, _I32, _I32, _F, _P, _SZ, _P]),
     "kvq_decode_attn_unrotated": (_I32, [ctypes.POINTER(CacheDesc), _P, _I32, _I32, _I32, _P, _P, _I32, _I32, _P,
                                          _I32, _F, _P, _SZ, _P]),
     "kvq_merge": (_I32, [ctypes.POINTER(CacheDesc), _P, _SZ, _I32, _I32, _P, _I32, _I32, _I32, _P, _P]),
@@ -191,6 +192,30 @@ def decode_attn(cache: Cache, q, seq_lens, block_tables, max_seq_len, sm_scale, 
     _check(lib().kvq_decode_attn(cache.ref, _ptr(q), B, Hq, _ptr(seq_lens), _ptr(block_tables),
                                  block_tables.shape[1], max_seq_len, _ptr(sel), n_sel, float(sm_scale),
                                  _ptr(workspace), workspace.numel(), _stream(stream)), "kvq_decode_attn")
+
+
+def decode_window(cache: Cache, q_rot, row_lens, block_table, max_seq_len, sm_scale, workspace, stream=None):
+    """Partials for a window of rows of one sequence sharing its block table
+    (row i attends keys 0 .. row_lens[i] - 1); merge with merge(num_seqs=rows)."""
+    R, Hq = q_rot.shape[0], q_rot.shape[1]
+    bt = block_table.reshape(-1)
+    _check(lib().kvq_decode_window(cache.ref, _ptr(q_rot), R, Hq, _ptr(row_lens), _ptr(bt), bt.numel(), max_seq_len,
+                                   float(sm_scale), _ptr(workspace), workspace.numel(), _stream(stream)),
+           "kvq_decode_window")
+
+
+def decode_window_causal(cache: Cache, q, prefix_len, block_table, sm_scale, workspace, out=None, stream=None):
+    """One speculative-decoding verify step: the R rows of q sit at positions
+    prefix_len .. prefix_len + R - 1 (their keys already stored) and row i attends
+    keys 0 .. prefix_len + i.  Rotates the queries (Hadamard format), decodes the
+    window, merges; returns the outputs [R, Hq, D]."""
+    R, Hq = q.shape[0], q.shape[1]
+    row_lens = torch.arange(prefix_len + 1, prefix_len + R + 1, dtype=torch.int32, device=q.device)
+    qq = rotate_query(q, stream=stream) if cache.fmt == FMT_Q4_HAD32 else q.float()
+    decode_window(cache, qq, row_lens, block_table, prefix_len + R, sm_scale, workspace, stream=stream)
+    if out is None:
+        out = torch.empty((R, Hq, cache.D), dtype=torch.float32, device=q.device)
+    return merge(cache, workspace, R, Hq, row_lens, prefix_len + R, out, stream=stream)
 
 
 def decode_attn_unrotated(cache: Cache, q, seq_lens, block_tables, max_seq_len, sm_scale, workspace, sel=None,

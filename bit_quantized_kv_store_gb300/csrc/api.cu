@@ -211,7 +211,7 @@ static int32_t decode_attn_impl(const kvq_cache* cache, const float* q, const vo
                                 int32_t num_seqs, int32_t num_q_heads, const int32_t* d_seq_lens,
                                 const int32_t* d_block_tables, int32_t max_pages_per_seq, int32_t max_seq_len,
                                 const int32_t* d_sel, int32_t n_sel, float sm_scale, void* workspace, size_t ws_bytes,
-                                void* stream) {
+                                void* stream, bool window = false) {
   int32_t st = check_cache(cache);
   if (st != KVQ_OK) return st;
   st = check_decode_shape(cache, num_seqs, num_q_heads, d_seq_lens, max_seq_len, d_sel != nullptr, n_sel);
@@ -238,6 +238,8 @@ static int32_t decode_attn_impl(const kvq_cache* cache, const float* q, const vo
     a.seq_lens = d_seq_lens;
     a.block_tables = d_block_tables;
     a.max_pages = max_pages_per_seq;
+    a.bt_stride = window ? 0 : max_pages_per_seq;
+    a.nrows = window ? num_seqs : 0;
     a.max_seq_len = max_seq_len;
     a.sel = d_sel;
     a.n_sel = d_sel ? n_sel : 0;
@@ -274,6 +276,16 @@ int32_t kvq_decode_attn(const kvq_cache* cache, const float* q, int32_t num_seqs
                         size_t ws_bytes, void* stream) {
   return decode_attn_impl(cache, q, nullptr, 0, num_seqs, num_q_heads, d_seq_lens, d_block_tables,
                           max_pages_per_seq, max_seq_len, d_sel, n_sel, sm_scale, workspace, ws_bytes, stream);
+}
+
+int32_t kvq_decode_window(const kvq_cache* cache, const float* q, int32_t num_rows, int32_t num_q_heads,
+                          const int32_t* d_row_lens, const int32_t* d_block_table, int32_t max_pages,
+                          int32_t max_seq_len, float sm_scale, void* workspace, size_t ws_bytes, void* stream) {
+  if (!cache) return KVQ_ERR_INVALID_ARG;
+  if (!is_q4(cache->format)) return KVQ_ERR_UNSUPPORTED;
+  if (num_rows > 64) return KVQ_ERR_INVALID_ARG;
+  return decode_attn_impl(cache, q, nullptr, 0, num_rows, num_q_heads, d_row_lens, d_block_table, max_pages,
+                          max_seq_len, nullptr, 0, sm_scale, workspace, ws_bytes, stream, true);
 }
 
 int32_t kvq_decode_attn_unrotated(const kvq_cache* cache, const void* q, int32_t q_dtype, int32_t num_seqs,

@@ -228,7 +228,7 @@ __device__ __forceinline__ bool q4_issue_plane(const DecodeArgs& a, int b, int k
     return true;
   } else {
     const int32_t T = a.seq_lens[b];
-    const int32_t* bt = a.block_tables + (int64_t)b * a.max_pages;
+    const int32_t* bt = a.block_tables + (int64_t)b * a.bt_stride;
     int64_t rows[16];
     for (int j = 0; j < nvalid; ++j) {
       const int32_t pos = a.sel[(int64_t)b * a.n_sel + key0 + j];
@@ -288,7 +288,8 @@ __global__ void __launch_bounds__(kQ4Warps * 32, kQ4MinBlocks) decode_q4_round_k
   extern __shared__ uint8_t smem_raw[];
   // 1024-byte alignment for the swizzled tiles (the launch adds 1 KB of slack)
   Q4Smem& sm = *reinterpret_cast<Q4Smem*>(smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u));
-  const int p = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
+  const int p = a.nrows > 0 ? blockIdx.x / a.nrows : blockIdx.x, kvh = blockIdx.y;
+  const int b = a.nrows > 0 ? blockIdx.x % a.nrows : blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, t = lane & 3;
 
@@ -319,7 +320,7 @@ __global__ void __launch_bounds__(kQ4Warps * 32, kQ4MinBlocks) decode_q4_round_k
   bool bad_page = false;
   if (!GATHER && lane < ntiles) {
     const int key0 = k0 + 16 * lane;
-    const int32_t page = a.block_tables[(int64_t)b * a.max_pages + key0 / a.c.page_size];
+    const int32_t page = a.block_tables[(int64_t)b * a.bt_stride + key0 / a.c.page_size];
     if (page < 0 || page >= a.c.num_pages)
       bad_page = true;
     else
@@ -632,7 +633,8 @@ cudaError_t launch_decode_q4(const DecodeArgs& a, int B, cudaStream_t s) {
   auto kern = a.sel ? decode_q4_round_kernel<true> : decode_q4_round_kernel<false>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  e = launch_pdl(kern, dim3(a.P, a.c.num_kv_heads, B), dim3(kQ4Warps * 32), smem, s, a);
+  const dim3 grid = a.nrows > 0 ? dim3(a.P * a.nrows, a.c.num_kv_heads, 1) : dim3(a.P, a.c.num_kv_heads, B);
+  e = launch_pdl(kern, grid, dim3(kQ4Warps * 32), smem, s, a);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }

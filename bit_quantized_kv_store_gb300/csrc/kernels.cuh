@@ -32,6 +32,13 @@ struct DecodeArgs {
   float* ws_acc;
   int P;  // partitions per (seq, head) in the workspace
   int32_t* status;
+  // 4-bit decode only.  Block-table row of sequence b: block_tables + b * bt_stride
+  // (bt_stride 0: one table shared by every row of a decode window).  nrows > 0:
+  // the grid enumerates (partition, row) with the row fastest along x (z = 1),
+  // so that the rows of a window read each partition at about the same time
+  // (from L2 after the first); nrows = 0: partitions along x, sequences along z.
+  int bt_stride;
+  int nrows;
 };
 
 // Log-sum-exp merge of the partials (merge.cu).

@@ -186,6 +186,25 @@ int32_t kvq_decode_attn(const kvq_cache* cache, const float* q, int32_t num_seqs
                         int32_t max_seq_len, const int32_t* d_sel, int32_t n_sel, float sm_scale,
                         void* workspace, size_t ws_bytes, void* stream);
 
+/* kvq_decode_window -- kvq_decode_attn for a window of num_rows query rows of ONE
+ * sequence that share its block table: the draft rows of a speculative-decoding
+ * step ([P1] "What it is": shared 512-key chunks plus each row's causal tail).
+ * Row i attends keys 0 .. d_row_lens[i] - 1 of the sequence (a causal window:
+ * prefix_len + i + 1).  The partials are bit-identical to kvq_decode_attn with
+ * num_seqs = num_rows, seq_lens = d_row_lens and the block table repeated for
+ * every row; the rows of a partition are scheduled next to each other, so that
+ * the cache is read from HBM about once for the window (the others hit L2).
+ * Merge with kvq_merge(num_seqs = num_rows, d_seq_lens = d_row_lens).
+ *   q: device fp32 [num_rows, num_q_heads, head_dim] (rotated, as for
+ *      kvq_decode_attn); d_row_lens: device int32 [num_rows];
+ *   d_block_table: device int32 [max_pages], shared by every row.
+ *   4-bit formats only (else KVQ_ERR_UNSUPPORTED); 1 <= num_rows <= 64.
+ * Workspace (kvq_decode_workspace_size with num_seqs = num_rows) and errors as
+ * for kvq_decode_attn. */
+int32_t kvq_decode_window(const kvq_cache* cache, const float* q, int32_t num_rows, int32_t num_q_heads,
+                          const int32_t* d_row_lens, const int32_t* d_block_table, int32_t max_pages,
+                          int32_t max_seq_len, float sm_scale, void* workspace, size_t ws_bytes, void* stream);
+
 /* kvq_decode_attn_unrotated -- kvq_decode_attn for the 4-bit format with the
  * query rotation done inside the decode kernel ([P1] "What it is": the query
  * is rotated once, then the 4-bit cache is streamed in rotated space), saving the

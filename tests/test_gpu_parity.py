@@ -392,6 +392,29 @@ def test_decode_q4_0_gather(K):
         assert_close(out[b], ref[b], what=f"Q4_0 gather seq {b}")
 
 
+@pytest.mark.parametrize("T0,R", [(1000, 4), (513, 3), (40, 8), (0, 2)])
+def test_decode_window_equals_plain_rows(K, T0, R):
+    """A decode window (R draft rows of one sequence sharing its block table, row i
+    attending keys 0 .. T0 + i) gives bit-identical partials and outputs to the
+    plain batched decode of R sequences with those lengths and the block table
+    repeated, and matches the oracle."""
+    g, o, bt, _, _ = decode_case(K, [T0 + R], seed=40 + R)
+    q = synth.heavy_tailed((R, 24, 256), "cpu", "win", T0, R)
+    lens = [T0 + i + 1 for i in range(R)]
+    ml = T0 + R
+    dev_bt = torch.from_numpy(bt).to(DEV)
+    ws_w = K.alloc_workspace(g, R, 24, ml, device=DEV)
+    out_w = K.decode_window_causal(g, q.to(DEV), T0, dev_bt[0], 1 / 16, ws_w)
+    bt_rep = np.repeat(bt, R, axis=0)
+    out_p, ws_p = run_decode(K, g, bt_rep, q, lens, ml, 1 / 16)
+    torch.cuda.synchronize()
+    assert torch.equal(ws_w, ws_p)
+    assert np.array_equal(out_w.cpu().numpy(), out_p)
+    ref = O.decode(o, to_np_in(q), lens, bt_rep, 1 / 16)
+    for i in range(R):
+        assert_close(out_p[i], ref[i], what=f"window row {i}")
+
+
 def test_decode_bad_page_and_length_are_flagged(K):
     lens = [600, 300]
     g, o, bt, q, ml = decode_case(K, lens, seed=4)
