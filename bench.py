@@ -561,7 +561,7 @@ def _row_window(K, synth, torch, dev, peak, seed):
         "workload": "4 draft rows at positions 262144..262147 of one sequence, shared block table, 1 layer",
         "window_us": win_ms * 1e3, "as_4_sequences_us": rows_ms * 1e3, "one_row_us": one_ms * 1e3,
         "window_us_per_row": win_ms * 1e3 / R, "cache_GBs_once": byts / (win_ms * 1e-3) / 1e9,
-        "kernel": "decode_q4_round_kernel (rows of a partition adjacent in the grid)"}
+        "kernel": "decode_q4_round_kernel, window mode: the 4 rows' 24 (row, head) columns in one CTA"}
     del c, ws
     torch.cuda.empty_cache()
     return out

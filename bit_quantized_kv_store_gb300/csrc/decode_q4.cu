@@ -87,11 +87,13 @@ __device__ __forceinline__ float2 lds64f(uint32_t addr) {
   return v;
 }
 
-// Query fragments (B operand of the score MMA) and biases of the CTA's GQA group,
-// written once per CTA by its kWarps warps into qf / qb; ends with __syncthreads.
+// Query fragments (B operand of the score MMA) and biases of one column tile:
+// column g of the tile faces the query row `qrow` (all 256 dims; a dead column
+// passes live = false and gets a zero query).  Warp w prepares groups w,
+// w + kWarps, ...; the caller synchronises before the fragments are read.
 template <int kWarps>
-__device__ __forceinline__ void q4_query_prep(const DecodeArgs& a, int b, int kvh, int warp, int lane, float* qrot,
-                                              uint4 (*qf)[2][32], float4 (*qb)[4]) {
+__device__ __forceinline__ void q4_frag_prep(const float* qrow, bool live, float qscale, int warp, int lane,
+                                             uint4 (*qf)[2][32], float4 (*qb)[4]) {
   const int g = lane >> 2, t = lane & 3;
   // The K codes enter the MMA as 1024 + c (even elements, low nibbles) and
   // 1024 + 16c (odd elements, high nibbles), one lop3 each; the query values
@@ -99,6 +101,59 @@ __device__ __forceinline__ void q4_query_prep(const DecodeArgs& a, int b, int kv
   // group G starts at -bias_G, bias_G = 1024 * sum(B) + 8 * sum(q~) over the
   // group (B the f16 values in the fragments, q~ = B or 16 B), so the MMA
   // returns sum_d q_d (c_d - 8) with the keys' codes used exactly.
+  const float s = live ? qscale : 0.f;
+  const float s16 = s * 0.0625f;
+  constexpr int kGroupsPerWarp = kQ4NG / kWarps;
+  float4 ql0[kGroupsPerWarp], ql1[kGroupsPerWarp];  // all loads issued first
+#pragma unroll
+  for (int k = 0; k < kGroupsPerWarp; ++k) {
+    ql0[k] = *reinterpret_cast<const float4*>(qrow + 32 * (warp + kWarps * k) + 8 * t);
+    ql1[k] = *reinterpret_cast<const float4*>(qrow + 32 * (warp + kWarps * k) + 8 * t + 4);
+  }
+#pragma unroll
+  for (int k = 0; k < kGroupsPerWarp; ++k) {
+    const int G = warp + kWarps * k;
+    const float4 u0 = ql0[k];
+    const float4 u1 = ql1[k];
+    uint4 hi, lo;
+    // tile (G,0): slots (2t,2t+1) <- d (8t, 8t+2); slots (2t+8, 2t+9) <- d (8t+1, 8t+3); tile (G,1): d + 4
+    split_f16(u0.x * s, u0.z * s, hi.x, lo.x);
+    split_f16(u0.y * s16, u0.w * s16, hi.y, lo.y);
+    split_f16(u1.x * s, u1.z * s, hi.z, lo.z);
+    split_f16(u1.y * s16, u1.w * s16, hi.w, lo.w);
+    qf[G][0][lane] = hi;
+    qf[G][1][lane] = lo;
+    float ev = 0.f, od = 0.f;  // sums of the even-slot and odd-slot B values (hi parts, then lo parts)
+    const uint32_t hv[4] = {hi.x, hi.y, hi.z, hi.w}, lv[4] = {lo.x, lo.y, lo.z, lo.w};
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+      const float2 h2 = __half22float2(u32_as_h2(hv[r]));
+      if (r & 1) od += h2.x + h2.y; else ev += h2.x + h2.y;
+    }
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+      const float2 l2 = __half22float2(u32_as_h2(lv[r]));
+      if (r & 1) od += l2.x + l2.y; else ev += l2.x + l2.y;
+    }
+    // bias = 1024 (ev + od) + 8 (ev + 16 od), summed over the 4 lanes of the column
+    float bias = 1032.f * ev + 1152.f * od;
+    bias += __shfl_xor_sync(0xffffffffu, bias, 1);
+    bias += __shfl_xor_sync(0xffffffffu, bias, 2);
+    // column g's bias -> components (g & 1) and 2 + (g & 1) of qb[G][g / 2]
+    if (t == 0) {
+      float* q4 = reinterpret_cast<float*>(&qb[G][g >> 1]);
+      q4[g & 1] = -bias;
+      q4[2 + (g & 1)] = -bias;
+    }
+  }
+}
+
+// Query fragments of one sequence's GQA group (columns = its heads), written
+// once per CTA by its kWarps warps into qf / qb; ends with __syncthreads.
+template <int kWarps>
+__device__ __forceinline__ void q4_query_prep(const DecodeArgs& a, int b, int kvh, int warp, int lane, float* qrot,
+                                              uint4 (*qf)[2][32], float4 (*qb)[4]) {
+  const int g = lane >> 2;
   const float* qsrc = a.q + ((int64_t)b * a.Hq + kvh * a.group) * kQ4D;  // rows of the group's heads
   if (a.q_raw) {
     // Rotate the group's queries here, with the arithmetic of the rotation entry
@@ -128,78 +183,37 @@ __device__ __forceinline__ void q4_query_prep(const DecodeArgs& a, int b, int kv
     __syncthreads();
     qsrc = qrot;
   }
-  {
-    const bool live = g < a.group;
-    const float* qrow = qsrc + (live ? g : 0) * kQ4D;
-    const float s = live ? a.qscale : 0.f;
-    const float s16 = s * 0.0625f;
-    constexpr int kGroupsPerWarp = kQ4NG / kWarps;
-    float4 ql0[kGroupsPerWarp], ql1[kGroupsPerWarp];  // all loads issued first
-#pragma unroll
-    for (int k = 0; k < kGroupsPerWarp; ++k) {
-      ql0[k] = *reinterpret_cast<const float4*>(qrow + 32 * (warp + kWarps * k) + 8 * t);
-      ql1[k] = *reinterpret_cast<const float4*>(qrow + 32 * (warp + kWarps * k) + 8 * t + 4);
-    }
-#pragma unroll
-    for (int k = 0; k < kGroupsPerWarp; ++k) {  // warp w prepares groups w, w + kWarps, ...
-      const int G = warp + kWarps * k;
-      const float4 u0 = ql0[k];
-      const float4 u1 = ql1[k];
-      uint4 hi, lo;
-      // tile (G,0): slots (2t,2t+1) <- d (8t, 8t+2); slots (2t+8, 2t+9) <- d (8t+1, 8t+3); tile (G,1): d + 4
-      split_f16(u0.x * s, u0.z * s, hi.x, lo.x);
-      split_f16(u0.y * s16, u0.w * s16, hi.y, lo.y);
-      split_f16(u1.x * s, u1.z * s, hi.z, lo.z);
-      split_f16(u1.y * s16, u1.w * s16, hi.w, lo.w);
-      qf[G][0][lane] = hi;
-      qf[G][1][lane] = lo;
-      float ev = 0.f, od = 0.f;  // sums of the even-slot and odd-slot B values (hi parts, then lo parts)
-      const uint32_t hv[4] = {hi.x, hi.y, hi.z, hi.w}, lv[4] = {lo.x, lo.y, lo.z, lo.w};
-#pragma unroll
-      for (int r = 0; r < 4; ++r) {
-        const float2 h2 = __half22float2(u32_as_h2(hv[r]));
-        if (r & 1) od += h2.x + h2.y; else ev += h2.x + h2.y;
-      }
-#pragma unroll
-      for (int r = 0; r < 4; ++r) {
-        const float2 l2 = __half22float2(u32_as_h2(lv[r]));
-        if (r & 1) od += l2.x + l2.y; else ev += l2.x + l2.y;
-      }
-      // bias = 1024 (ev + od) + 8 (ev + 16 od), summed over the 4 lanes of the head
-      float bias = 1032.f * ev + 1152.f * od;
-      bias += __shfl_xor_sync(0xffffffffu, bias, 1);
-      bias += __shfl_xor_sync(0xffffffffu, bias, 2);
-      // head g's bias -> components (g & 1) and 2 + (g & 1) of qb[G][g / 2]
-      if (t == 0) {
-        float* q4 = reinterpret_cast<float*>(&qb[G][g >> 1]);
-        q4[g & 1] = -bias;
-        q4[2 + (g & 1)] = -bias;
-      }
-    }
-  }
+  const bool live = g < a.group;
+  q4_frag_prep<kWarps>(qsrc + (live ? g : 0) * kQ4D, live, a.qscale, warp, lane, qf, qb);
   __syncthreads();
 }
 
 namespace q4r {
 
 constexpr int kQ4Warps = 4;                       // warps per CTA = value group pairs in P.V
-constexpr int kQ4MinBlocks = 4;                   // resident CTAs per SM the register budget is sized for
 constexpr int kQ4TPW = 2;                         // 16-key tiles each warp scores per round
 constexpr int kQ4RoundTiles = kQ4Warps * kQ4TPW;  // 8 tiles = 128 keys per round
+constexpr int kQ4MaxColTiles = 4;                 // a decode window stacks up to 32 (row, head) columns
 
+// Resident CTAs per SM the register budget is sized for: one column tile (one
+// sequence's GQA group) fits 128 registers; each further tile adds 16 P.V
+// accumulators per thread.
+constexpr int q4_min_blocks(int nt) { return nt == 1 ? 4 : nt == 2 ? 3 : 2; }
+
+template <int NT>
 struct __align__(1024) Q4Smem {
   uint8_t kc[kQ4Warps][kQ4TPW][kQ4TileBytes];  // K codes of each warp's tiles of the round (1024-aligned)
   uint8_t vc[kQ4RoundTiles][kQ4TileBytes];     // V codes of the round's tiles
   uint16_t ks[kQ4Warps][kQ4TPW][16 * 8];       // K scales
   uint16_t vs[kQ4RoundTiles][16 * 8];          // V scales
-  uint4 qf[kQ4NG][2][32];                      // query fragments [group][hi, lo][lane]
-  float4 qb[kQ4NG][4];        // [group][t]: minus the code-offset bias of heads (2t, 2t+1, 2t, 2t+1)
-  uint2 pb[kQ4RoundTiles][32];  // [tile][lane]: P of the round as B fragments (keys 2t.., 2t+8..)
-  float red[kQ4Warps][8];       // [warp][head]: maxima of each warp's tiles of the round
-  float zs[kQ4Warps][8];        // per-warp sums of the probabilities
-  uint64_t kbar[kQ4Warps];      // a warp's K tiles landed (kQ4TPW arrivals)
-  uint64_t vfull;               // the round's V tiles landed (kQ4RoundTiles arrivals)
-  uint64_t vempty;              // every warp is done with the round's V (kQ4Warps arrivals)
+  uint4 qf[NT][kQ4NG][2][32];                  // query fragments [column tile][group][hi, lo][lane]
+  float4 qb[NT][kQ4NG][4];  // [column tile][group][t]: minus the code-offset bias of columns (2t, 2t+1, 2t, 2t+1)
+  uint2 pb[kQ4RoundTiles][NT][32];  // [tile][column tile][lane]: P of the round as B fragments (keys 2t.., 2t+8..)
+  float red[kQ4Warps][8 * NT];      // [warp][column]: maxima of each warp's tiles of the round
+  float zs[kQ4Warps][8 * NT];       // per-warp sums of the probabilities
+  uint64_t kbar[kQ4Warps];          // a warp's K tiles landed (kQ4TPW arrivals)
+  uint64_t vfull;                   // the round's V tiles landed (kQ4RoundTiles arrivals)
+  uint64_t vempty;                  // every warp is done with the round's V (kQ4Warps arrivals)
   int poison;
 };
 // The unrotated-query entry point rotates the group's queries (8 heads x 256
@@ -283,27 +297,57 @@ __device__ __forceinline__ bool q4_issue_own(const DecodeArgs& a, int b, int kvh
   return bad;
 }
 
-template <bool GATHER>
-__global__ void __launch_bounds__(kQ4Warps * 32, kQ4MinBlocks) decode_q4_round_kernel(const __grid_constant__ DecodeArgs a) {
+// One CTA per (partition, KV head, column set).  NT column tiles of 8 columns
+// face the keys on the MMA's N side.  A plain decode (WIN = false, NT = 1) gives
+// the columns to the heads of one sequence's GQA group.  A decode window
+// (WIN = true) gives them to (row, head) pairs of `rows_per_cta` rows of one
+// sequence, row-major: the rows share the block table and so every key, whose
+// codes are then converted once for all of them; each row keeps its own causal
+// end (its length), its own softmax state and its own partials.
+template <bool GATHER, int NT, bool WIN>
+__global__ void __launch_bounds__(kQ4Warps * 32, q4_min_blocks(NT))
+    decode_q4_round_kernel(const __grid_constant__ DecodeArgs a) {
+  static_assert(!(WIN && GATHER), "decode windows read dense prefixes");
+  static_assert(WIN || NT == 1, "one sequence's group fills one column tile");
   extern __shared__ uint8_t smem_raw[];
   // 1024-byte alignment for the swizzled tiles (the launch adds 1 KB of slack)
-  Q4Smem& sm = *reinterpret_cast<Q4Smem*>(smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u));
-  const int p = a.nrows > 0 ? blockIdx.x / a.nrows : blockIdx.x, kvh = blockIdx.y;
-  const int b = a.nrows > 0 ? blockIdx.x % a.nrows : blockIdx.z;
+  Q4Smem<NT>& sm = *reinterpret_cast<Q4Smem<NT>*>(smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u));
+  const int p = blockIdx.x, kvh = blockIdx.y;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, t = lane & 3;
+  // rows [b, b + nr): one sequence, or a slice of a window's rows
+  const int b = WIN ? blockIdx.z * a.rows_per_cta : blockIdx.z;
+  const int nr = WIN ? min(a.rows_per_cta, a.nrows - b) : 1;
 
   // Metadata first: the lengths and block tables are caller inputs that no
   // kernel of this library writes, so they are read before the wait on the
   // previous kernel of the stream (programmatic dependent launch) and their
   // latency overlaps it.  The cache, the queries and every write come after.
-  int32_t T;
-  bool bad_len = false;
+  int32_t T;                // keys of the CTA's longest row
+  int32_t Tmin = 0;         // window: keys of its shortest row (a bad row counts 0)
+  int32_t row_len = 0;      // window: lane i < nr holds the length of row b + i
+  bool bad_len = false;     // plain: the sequence's length is invalid
+  bool bad_row = false;     // window: some row's length is invalid (that row is skipped)
   if (GATHER) {
     T = a.n_sel;
-  } else {
+  } else if (!WIN) {
     T = a.seq_lens[b];
     bad_len = T < 0 || T > a.max_seq_len || (int64_t)T > (int64_t)a.max_pages * a.c.page_size;
+  } else {
+    bool bad = false;
+    if (lane < nr) {
+      row_len = a.seq_lens[b + lane];
+      bad = row_len < 0 || row_len > a.max_seq_len || (int64_t)row_len > (int64_t)a.max_pages * a.c.page_size;
+      if (bad) row_len = 0;
+    }
+    bad_row = __any_sync(0xffffffffu, bad);
+    T = row_len;
+    Tmin = lane < nr ? row_len : INT32_MAX;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      T = max(T, __shfl_xor_sync(0xffffffffu, T, o));
+      Tmin = min(Tmin, __shfl_xor_sync(0xffffffffu, Tmin, o));
+    }
   }
   const int nparts = bad_len ? 0 : (T + kPart - 1) / kPart;
   const bool active = p < nparts;  // CTA-uniform
@@ -312,6 +356,18 @@ __global__ void __launch_bounds__(kQ4Warps * 32, kQ4MinBlocks) decode_q4_round_k
   const int ntiles = active ? (k1 - k0 + 15) / 16 : 0;
   const int nrounds = (ntiles + kQ4RoundTiles - 1) / kQ4RoundTiles;  // <= 4
   // tile u of warp w in round r: kQ4RoundTiles * r + kQ4TPW * w + u
+
+  // Window: the length of the row of each of this thread's score columns
+  // (columns 8 nt + 2t + c); a column past the CTA's rows takes T.
+  int32_t colen[NT][2];
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+    for (int c = 0; c < 2; ++c) {
+      const int row = (8 * nt + 2 * t + c) / a.group;
+      const int32_t len = __shfl_sync(0xffffffffu, row_len, row & 31);
+      colen[nt][c] = row < nr ? len : T;
+    }
 
   // Lane i: the cache row of tile i (its first key), computed once so that the
   // copies need neither a global load nor a division inside the loop; -1 for a
@@ -339,6 +395,7 @@ __global__ void __launch_bounds__(kQ4Warps * 32, kQ4MinBlocks) decode_q4_round_k
     if (threadIdx.x == 0 && p == 0 && kvh == 0) set_status(a.status, KVQ_DEV_BAD_LENGTH);
     return;  // the merge writes NaN for this sequence
   }
+  if (bad_row && threadIdx.x == 0 && p == 0 && kvh == 0) set_status(a.status, KVQ_DEV_BAD_LENGTH);
   if (!active) return;
   if (bad_page && warp == 0) set_status(a.status, KVQ_DEV_BAD_PAGE);
   __syncthreads();  // the mbarriers are initialised
@@ -347,24 +404,43 @@ __global__ void __launch_bounds__(kQ4Warps * 32, kQ4MinBlocks) decode_q4_round_k
   bool poisoned = q4_issue_own<GATHER>(a, b, kvh, k0, k1, 0, warp, lane, tile_row, &a.tm_k, c.k, c.k_scale,
                                        sm.kc[warp], sm.ks[warp], &sm.kbar[warp]);
 
-  q4_query_prep<kQ4Warps>(a, b, kvh, warp, lane, reinterpret_cast<float*>(&sm.vc[0][0]), sm.qf, sm.qb);
+  if constexpr (WIN) {
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      const int col = 8 * nt + g, row = col / a.group;
+      const bool live = row < nr;
+      const float* qrow = a.q + ((int64_t)(b + (live ? row : 0)) * a.Hq + kvh * a.group + (live ? col - row * a.group : 0)) * kQ4D;
+      q4_frag_prep<kQ4Warps>(qrow, live, a.qscale, warp, lane, sm.qf[nt], sm.qb[nt]);
+    }
+    __syncthreads();
+  } else {
+    q4_query_prep<kQ4Warps>(a, b, kvh, warp, lane, reinterpret_cast<float*>(&sm.vc[0][0]), sm.qf[0], sm.qb[0]);
+  }
   // V of round 0: vc[0..3] held the rotated queries until the prologue's last barrier
   poisoned |= q4_issue_own<GATHER>(a, b, kvh, k0, k1, 0, warp, lane, tile_row, &a.tm_v, c.v, c.v_scale,
                                    &sm.vc[kQ4TPW * warp], &sm.vs[kQ4TPW * warp], &sm.vfull);
-  const uint32_t qf_addr = smem_u32(&sm.qf[0][0][lane]);
-  const uint32_t qb_addr = smem_u32(&sm.qb[0][t]);
+  const uint32_t qf_addr = smem_u32(&sm.qf[0][0][0][lane]);
+  const uint32_t qb_addr = smem_u32(&sm.qb[0][0][t]);
+  constexpr uint32_t kQfTile = sizeof(sm.qf[0]), kQbTile = sizeof(sm.qb[0]);
 
-  // P.V accumulators of groups 2w + e, d-tiles (G, 0) and (G, 1)
-  float acc[2][2][4];
+  // P.V accumulators of groups 2w + e, d-tiles (G, 0) and (G, 1), column tile nt
+  float acc[2][2][NT][4];
 #pragma unroll
   for (int e = 0; e < 2; ++e)
 #pragma unroll
     for (int j = 0; j < 2; ++j)
 #pragma unroll
-      for (int i = 0; i < 4; ++i) acc[e][j][i] = 0.f;
-  float m0 = kQ4NoMax, m1 = kQ4NoMax;  // running max of heads 2t, 2t+1 (base 2), equal in every warp
-  float z0 = 0.f, z1 = 0.f;              // this thread's partial sums over its own tiles' keys
-  const bool head0_live = 2 * t < a.group, head1_live = 2 * t + 1 < a.group;
+      for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) acc[e][j][nt][i] = 0.f;
+  // running max of columns 2t, 2t+1 of each column tile (base 2), equal in every
+  // warp, and this thread's partial sums over its own tiles' keys
+  float m0[NT], m1[NT], z0[NT], z1[NT];
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+    m0[nt] = m1[nt] = kQ4NoMax;
+    z0[nt] = z1[nt] = 0.f;
+  }
   bool timed_out = false;
 
   // Byte offsets of this thread's fragments inside a code tile (swizzle: chunk ^ (row & 7)).
@@ -382,21 +458,25 @@ __global__ void __launch_bounds__(kQ4Warps * 32, kQ4MinBlocks) decode_q4_round_k
   const uint32_t ks_base = smem_u32(&sm.ks[warp][0][0]);
   const uint32_t vc_base = smem_u32(&sm.vc[0][0]);
   const uint32_t vs_base = smem_u32(&sm.vs[0][0]) + 4 * warp;
-  const uint32_t pb_addr = smem_u32(&sm.pb[0][lane]);
+  const uint32_t pb_addr = smem_u32(&sm.pb[0][0][lane]);
 
   for (int r = 0; r < nrounds; ++r) {
     const uint32_t par = r & 1;
     const int tile0 = kQ4RoundTiles * r + kQ4TPW * warp;
-    float S[kQ4TPW][4];
+    float S[kQ4TPW][NT][4];
 #pragma unroll
-    for (int u = 0; u < kQ4TPW; ++u) S[u][0] = S[u][1] = S[u][2] = S[u][3] = -INFINITY;
+    for (int u = 0; u < kQ4TPW; ++u)
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) S[u][nt][0] = S[u][nt][1] = S[u][nt][2] = S[u][nt][3] = -INFINITY;
     if (k0 + 16 * tile0 < k1) {  // warp-uniform: this warp has at least one tile in the round
       // mma.sync below is warp-collective: the wait's outcome is made warp-uniform
       if (!timed_out && !__all_sync(0xffffffffu, mbar_wait_bounded(&sm.kbar[warp], par))) timed_out = true;
 
-      // ---------------- scores S[u][key][head] for keys g, g+8 of tile u and heads 2t, 2t+1
+      // ---------------- scores S[u][nt][key][column] for keys g, g+8 of tile u and columns 2t, 2t+1
 #pragma unroll
-      for (int u = 0; u < kQ4TPW; ++u) S[u][0] = S[u][1] = S[u][2] = S[u][3] = 0.f;
+      for (int u = 0; u < kQ4TPW; ++u)
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) S[u][nt][0] = S[u][nt][1] = S[u][nt][2] = S[u][nt][3] = 0.f;
 #pragma unroll
       for (int w = 0; w < kQ4NG / 2; ++w) {  // group pair (2w, 2w+1): one word of each fragment row
         uint32_t wa0[kQ4TPW], wa1[kQ4TPW], wb0[kQ4TPW], wb1[kQ4TPW];
@@ -414,9 +494,14 @@ __global__ void __launch_bounds__(kQ4Warps * 32, kQ4MinBlocks) decode_q4_round_k
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
           const int G = 2 * w + e;
-          const uint4 qh = lds128a(qf_addr + G * 1024);
-          const uint4 ql = lds128a(qf_addr + G * 1024 + 512);
-          const float4 nb = lds128f(qb_addr + G * 64);  // -bias of heads (2t, 2t+1, 2t, 2t+1)
+          uint4 qh[NT], ql[NT];
+          float4 nb[NT];  // -bias of columns (2t, 2t+1, 2t, 2t+1)
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt) {
+            qh[nt] = lds128a(qf_addr + nt * kQfTile + G * 1024);
+            ql[nt] = lds128a(qf_addr + nt * kQfTile + G * 1024 + 512);
+            nb[nt] = lds128f(qb_addr + nt * kQbTile + G * 64);
+          }
           const uint32_t sel = e ? 0x4342u : 0x4140u;
 #pragma unroll
           for (int u = 0; u < kQ4TPW; ++u) {
@@ -428,27 +513,43 @@ __global__ void __launch_bounds__(kQ4Warps * 32, kQ4MinBlocks) decode_q4_round_k
             const uint32_t a12 = nib_hi_pair_biased(xa1), a13 = nib_hi_pair_biased(xb1);
             const uint32_t a20 = nib_lo_pair_biased(xa2), a21 = nib_lo_pair_biased(xb2);
             const uint32_t a22 = nib_hi_pair_biased(xa2), a23 = nib_hi_pair_biased(xb2);
-            float part[4] = {nb.x, nb.y, nb.z, nb.w};
-            mma_f16(part, a10, a11, a12, a13, qh.x, qh.y);
-            mma_f16(part, a20, a21, a22, a23, qh.z, qh.w);
-            mma_f16(part, a10, a11, a12, a13, ql.x, ql.y);
-            mma_f16(part, a20, a21, a22, a23, ql.z, ql.w);
             const float sa = e ? fsa[u].y : fsa[u].x, sb = e ? fsb[u].y : fsb[u].x;
-            S[u][0] = fmaf(sa, part[0], S[u][0]);
-            S[u][1] = fmaf(sa, part[1], S[u][1]);
-            S[u][2] = fmaf(sb, part[2], S[u][2]);
-            S[u][3] = fmaf(sb, part[3], S[u][3]);
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+              float part[4] = {nb[nt].x, nb[nt].y, nb[nt].z, nb[nt].w};
+              mma_f16(part, a10, a11, a12, a13, qh[nt].x, qh[nt].y);
+              mma_f16(part, a20, a21, a22, a23, qh[nt].z, qh[nt].w);
+              mma_f16(part, a10, a11, a12, a13, ql[nt].x, ql[nt].y);
+              mma_f16(part, a20, a21, a22, a23, ql[nt].z, ql[nt].w);
+              S[u][nt][0] = fmaf(sa, part[0], S[u][nt][0]);
+              S[u][nt][1] = fmaf(sa, part[1], S[u][nt][1]);
+              S[u][nt][2] = fmaf(sb, part[2], S[u][nt][2]);
+              S[u][nt][3] = fmaf(sb, part[3], S[u][nt][3]);
+            }
           }
         }
       }
-      // (The heads past the group have a zero query: their scores are 0, finite,
-      // and never leave the kernel, so they need no mask.)
+      // (Dead columns have a zero query: their scores are 0, finite, and never
+      // leave the kernel, so they need no mask.)
 #pragma unroll
       for (int u = 0; u < kQ4TPW; ++u) {
-        const int nvalid = k1 - (k0 + 16 * (tile0 + u));
-        if (nvalid < 16) {  // warp-uniform: keys past the end (or a tile past the partition)
-          if (g >= nvalid) S[u][0] = S[u][1] = -INFINITY;
-          if (g + 8 >= nvalid) S[u][2] = S[u][3] = -INFINITY;
+        const int kt = k0 + 16 * (tile0 + u);  // the tile's first key
+        if constexpr (WIN) {
+          if (kt + 16 > Tmin) {  // warp-uniform: some row ends before the tile does
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+              for (int cc = 0; cc < 2; ++cc) {
+                if (kt + g >= colen[nt][cc]) S[u][nt][cc] = -INFINITY;
+                if (kt + g + 8 >= colen[nt][cc]) S[u][nt][2 + cc] = -INFINITY;
+              }
+          }
+        } else {
+          const int nvalid = k1 - kt;
+          if (nvalid < 16) {  // warp-uniform: keys past the end (or a tile past the partition)
+            if (g >= nvalid) S[u][0][0] = S[u][0][1] = -INFINITY;
+            if (g + 8 >= nvalid) S[u][0][2] = S[u][0][3] = -INFINITY;
+          }
         }
       }
 
@@ -460,59 +561,77 @@ __global__ void __launch_bounds__(kQ4Warps * 32, kQ4MinBlocks) decode_q4_round_k
     }
 
     // ---------------- round maximum, shared through shared memory
-    float t0 = fmaxf(S[0][0], S[0][2]), t1 = fmaxf(S[0][1], S[0][3]);
+    float t0[NT], t1[NT];
 #pragma unroll
-    for (int u = 1; u < kQ4TPW; ++u) {
-      t0 = fmaxf(t0, fmaxf(S[u][0], S[u][2]));
-      t1 = fmaxf(t1, fmaxf(S[u][1], S[u][3]));
-    }
+    for (int nt = 0; nt < NT; ++nt) {
+      t0[nt] = fmaxf(S[0][nt][0], S[0][nt][2]);
+      t1[nt] = fmaxf(S[0][nt][1], S[0][nt][3]);
 #pragma unroll
-    for (int o = 4; o < 32; o <<= 1) {
-      t0 = fmaxf(t0, __shfl_xor_sync(0xffffffffu, t0, o));
-      t1 = fmaxf(t1, __shfl_xor_sync(0xffffffffu, t1, o));
+      for (int u = 1; u < kQ4TPW; ++u) {
+        t0[nt] = fmaxf(t0[nt], fmaxf(S[u][nt][0], S[u][nt][2]));
+        t1[nt] = fmaxf(t1[nt], fmaxf(S[u][nt][1], S[u][nt][3]));
+      }
+#pragma unroll
+      for (int o = 4; o < 32; o <<= 1) {
+        t0[nt] = fmaxf(t0[nt], __shfl_xor_sync(0xffffffffu, t0[nt], o));
+        t1[nt] = fmaxf(t1[nt], __shfl_xor_sync(0xffffffffu, t1[nt], o));
+      }
+      if (g == 0) *reinterpret_cast<float2*>(&sm.red[warp][8 * nt + 2 * t]) = make_float2(t0[nt], t1[nt]);
     }
-    if (g == 0) *reinterpret_cast<float2*>(&sm.red[warp][2 * t]) = make_float2(t0, t1);
     bar_sync_cta();  // (1) maxima published; every warp is past the P.V of round r - 1
     {
       const uint32_t ra = smem_u32(&sm.red[0][2 * t]);
 #pragma unroll
-      for (int w = 0; w < kQ4Warps; ++w) {
-        const float2 mx = lds64f(ra + w * 32);
-        t0 = fmaxf(t0, mx.x);
-        t1 = fmaxf(t1, mx.y);
-      }
+      for (int w = 0; w < kQ4Warps; ++w)
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+          const float2 mx = lds64f(ra + w * (32 * NT) + 32 * nt);
+          t0[nt] = fmaxf(t0[nt], mx.x);
+          t1[nt] = fmaxf(t1[nt], mx.y);
+        }
     }
 
     // ---------------- online softmax (base 2), identical in every warp
-    // n is finite (m starts at kQ4NoMax); c is exactly 1 while a head's maximum stands
-    const float n0 = fmaxf(m0, t0), n1 = fmaxf(m1, t1);
-    const float c0 = fast_exp2(m0 - n0), c1 = fast_exp2(m1 - n1);
-    m0 = n0;
-    m1 = n1;
-    z0 *= c0;
-    z1 *= c1;
-    if (r > 0 && __any_sync(0xffffffffu, c0 != 1.f || c1 != 1.f)) {  // acc is still zero in round 0
+    // n is finite (m starts at kQ4NoMax); c is exactly 1 while a column's maximum stands
+    float c0[NT], c1[NT];
+    bool moved = false;
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      const float n0 = fmaxf(m0[nt], t0[nt]), n1 = fmaxf(m1[nt], t1[nt]);
+      c0[nt] = fast_exp2(m0[nt] - n0);
+      c1[nt] = fast_exp2(m1[nt] - n1);
+      m0[nt] = n0;
+      m1[nt] = n1;
+      z0[nt] *= c0[nt];
+      z1[nt] *= c1[nt];
+      moved |= c0[nt] != 1.f || c1[nt] != 1.f;
+    }
+    if (r > 0 && __any_sync(0xffffffffu, moved)) {  // acc is still zero in round 0
 #pragma unroll
       for (int e = 0; e < 2; ++e)
 #pragma unroll
-        for (int j = 0; j < 2; ++j) {
-          acc[e][j][0] *= c0;
-          acc[e][j][1] *= c1;
-          acc[e][j][2] *= c0;
-          acc[e][j][3] *= c1;
-        }
-    }
-    // P (keys x heads) -> B fragments (keys on K, heads on N), published
+        for (int j = 0; j < 2; ++j)
 #pragma unroll
-    for (int u = 0; u < kQ4TPW; ++u) {
-      const float p0 = fast_exp2(S[u][0] - n0), p1 = fast_exp2(S[u][1] - n1);
-      const float p2 = fast_exp2(S[u][2] - n0), p3 = fast_exp2(S[u][3] - n1);
-      z0 += p0 + p2;
-      z1 += p1 + p3;
-      const uint32_t pb0 = movmatrix_trans(pack_half2(p0, p1));  // keys 2t, 2t+1 of head g
-      const uint32_t pb1 = movmatrix_trans(pack_half2(p2, p3));  // keys 2t+8, 2t+9
-      sm.pb[kQ4TPW * warp + u][lane] = make_uint2(pb0, pb1);
+          for (int nt = 0; nt < NT; ++nt) {
+            acc[e][j][nt][0] *= c0[nt];
+            acc[e][j][nt][1] *= c1[nt];
+            acc[e][j][nt][2] *= c0[nt];
+            acc[e][j][nt][3] *= c1[nt];
+          }
     }
+    // P (keys x columns) -> B fragments (keys on K, columns on N), published
+#pragma unroll
+    for (int u = 0; u < kQ4TPW; ++u)
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        const float p0 = fast_exp2(S[u][nt][0] - m0[nt]), p1 = fast_exp2(S[u][nt][1] - m1[nt]);
+        const float p2 = fast_exp2(S[u][nt][2] - m0[nt]), p3 = fast_exp2(S[u][nt][3] - m1[nt]);
+        z0[nt] += p0 + p2;
+        z1[nt] += p1 + p3;
+        const uint32_t pb0 = movmatrix_trans(pack_half2(p0, p1));  // keys 2t, 2t+1 of column g
+        const uint32_t pb1 = movmatrix_trans(pack_half2(p2, p3));  // keys 2t+8, 2t+9
+        sm.pb[kQ4TPW * warp + u][nt][lane] = make_uint2(pb0, pb1);
+      }
     bar_sync_cta();  // (2) every tile's P is published
 
     // ---------------- P.V over the round's tiles for groups 2w, 2w+1
@@ -526,7 +645,9 @@ __global__ void __launch_bounds__(kQ4Warps * 32, kQ4MinBlocks) decode_q4_round_k
       constexpr bool kTail = decltype(tail_tag)::value;
 #pragma unroll
       for (int j = 0; j < kQ4RoundTiles; ++j) {
-        const uint2 pp = lds64a(pb_addr + j * 256);
+        uint2 pp[NT];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) pp[nt] = lds64a(pb_addr + (j * NT + nt) * 256);
         const uint32_t cb = vc_base + j * kQ4TileBytes;
         const uint32_t sb = vs_base + j * kQ4ScaleBytes;
         // V scales of keys 2t, 2t+1, 2t+8, 2t+9 and V codes of the same rows
@@ -553,8 +674,6 @@ __global__ void __launch_bounds__(kQ4Warps * 32, kQ4MinBlocks) decode_q4_round_k
           const uint32_t ssel = e ? 0x7632u : 0x5410u;
           const uint32_t slo = prmt(swa, swb, ssel);
           const uint32_t shi = prmt(swc, swd, ssel);
-          const uint32_t b0 = h2_as_u32(__hmul2(u32_as_h2(pp.x), u32_as_h2(slo)));
-          const uint32_t b1 = h2_as_u32(__hmul2(u32_as_h2(pp.y), u32_as_h2(shi)));
           const uint32_t s0 = e ? 0x6622u : 0x4400u;  // byte X of rows a, b -> bytes 0, 2
           const uint32_t s1 = e ? 0x7733u : 0x5511u;  // byte X+1
           const uint32_t x01 = prmt(cw0, cw1, s0);
@@ -562,8 +681,15 @@ __global__ void __launch_bounds__(kQ4Warps * 32, kQ4MinBlocks) decode_q4_round_k
           const uint32_t x23 = prmt(cw2, cw3, s0);
           const uint32_t x23b = prmt(cw2, cw3, s1);
           // d-tile (G,0): rows g <-> d = 32G+4g, g+8 <-> 32G+4g+2 ; (G,1): +1
-          mma_f16(acc[e][0], nib_lo_pair(x01), nib_lo_pair(x01b), nib_lo_pair(x23), nib_lo_pair(x23b), b0, b1);
-          mma_f16(acc[e][1], nib_hi_pair(x01), nib_hi_pair(x01b), nib_hi_pair(x23), nib_hi_pair(x23b), b0, b1);
+          const uint32_t l0 = nib_lo_pair(x01), l1 = nib_lo_pair(x01b), l2 = nib_lo_pair(x23), l3 = nib_lo_pair(x23b);
+          const uint32_t h0 = nib_hi_pair(x01), h1 = nib_hi_pair(x01b), h2 = nib_hi_pair(x23), h3 = nib_hi_pair(x23b);
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt) {
+            const uint32_t b0 = h2_as_u32(__hmul2(u32_as_h2(pp[nt].x), u32_as_h2(slo)));
+            const uint32_t b1 = h2_as_u32(__hmul2(u32_as_h2(pp[nt].y), u32_as_h2(shi)));
+            mma_f16(acc[e][0][nt], l0, l1, l2, l3, b0, b1);
+            mma_f16(acc[e][1][nt], h0, h1, h2, h3, b0, b1);
+          }
         }
       }
     };
@@ -587,56 +713,90 @@ __global__ void __launch_bounds__(kQ4Warps * 32, kQ4MinBlocks) decode_q4_round_k
 
   // ---------------- reduce z across the 8 key-row lanes; sum over warps
 #pragma unroll
-  for (int o = 4; o < 32; o <<= 1) {
-    z0 += __shfl_xor_sync(0xffffffffu, z0, o);
-    z1 += __shfl_xor_sync(0xffffffffu, z1, o);
+  for (int nt = 0; nt < NT; ++nt) {
+#pragma unroll
+    for (int o = 4; o < 32; o <<= 1) {
+      z0[nt] += __shfl_xor_sync(0xffffffffu, z0[nt], o);
+      z1[nt] += __shfl_xor_sync(0xffffffffu, z1[nt], o);
+    }
+    if (g == 0) *reinterpret_cast<float2*>(&sm.zs[warp][8 * nt + 2 * t]) = make_float2(z0[nt], z1[nt]);
   }
-  if (g == 0) *reinterpret_cast<float2*>(&sm.zs[warp][2 * t]) = make_float2(z0, z1);
   if (poisoned && lane == 0) atomicOr(&sm.poison, 1);
   __syncthreads();
   const bool bad = sm.poison != 0;
-  float Z0 = 0.f, Z1 = 0.f;
 #pragma unroll
-  for (int w = 0; w < kQ4Warps; ++w) {
-    Z0 += sm.zs[w][2 * t];
-    Z1 += sm.zs[w][2 * t + 1];
-  }
-  const int64_t pi0 = ((int64_t)b * a.Hq + kvh * a.group + 2 * t) * a.P + p;  // head 2t
-  const int64_t pi1 = pi0 + a.P;                                             // head 2t + 1
+  for (int nt = 0; nt < NT; ++nt) {
+    // columns 8 nt + 2t + cc: row b + row, head kvh * group + col - row * group;
+    // a window row past its own end has no partial in this partition
+    int64_t pi[2];
+    bool live[2];
 #pragma unroll
-  for (int e = 0; e < 2; ++e) {
-    const int d = 32 * (2 * warp + e) + 4 * g;
-    float4 o0 = make_float4(acc[e][0][0], acc[e][1][0], acc[e][0][2], acc[e][1][2]);
-    float4 o1 = make_float4(acc[e][0][1], acc[e][1][1], acc[e][0][3], acc[e][1][3]);
-    if (bad) o0 = o1 = make_float4(NAN, NAN, NAN, NAN);
-    if (head0_live) *reinterpret_cast<float4*>(a.ws_acc + pi0 * kQ4D + d) = o0;
-    if (head1_live) *reinterpret_cast<float4*>(a.ws_acc + pi1 * kQ4D + d) = o1;
-  }
-  if (warp == 0 && g == 0) {
-    if (head0_live) {
-      a.ws_m[pi0] = bad ? NAN : m0;
-      a.ws_z[pi0] = bad ? NAN : Z0;
+    for (int cc = 0; cc < 2; ++cc) {
+      const int col = 8 * nt + 2 * t + cc, row = col / a.group;
+      live[cc] = row < nr && (!WIN || k0 < colen[nt][cc]);
+      pi[cc] = ((int64_t)(b + row) * a.Hq + kvh * a.group + col - row * a.group) * a.P + p;
     }
-    if (head1_live) {
-      a.ws_m[pi1] = bad ? NAN : m1;
-      a.ws_z[pi1] = bad ? NAN : Z1;
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const int d = 32 * (2 * warp + e) + 4 * g;
+      float4 o0 = make_float4(acc[e][0][nt][0], acc[e][1][nt][0], acc[e][0][nt][2], acc[e][1][nt][2]);
+      float4 o1 = make_float4(acc[e][0][nt][1], acc[e][1][nt][1], acc[e][0][nt][3], acc[e][1][nt][3]);
+      if (bad) o0 = o1 = make_float4(NAN, NAN, NAN, NAN);
+      if (live[0]) *reinterpret_cast<float4*>(a.ws_acc + pi[0] * kQ4D + d) = o0;
+      if (live[1]) *reinterpret_cast<float4*>(a.ws_acc + pi[1] * kQ4D + d) = o1;
+    }
+    if (warp == 0 && g == 0) {
+      float Z[2] = {0.f, 0.f};
+#pragma unroll
+      for (int w = 0; w < kQ4Warps; ++w) {
+        Z[0] += sm.zs[w][8 * nt + 2 * t];
+        Z[1] += sm.zs[w][8 * nt + 2 * t + 1];
+      }
+      const float M[2] = {m0[nt], m1[nt]};
+#pragma unroll
+      for (int cc = 0; cc < 2; ++cc)
+        if (live[cc]) {
+          a.ws_m[pi[cc]] = bad ? NAN : M[cc];
+          a.ws_z[pi[cc]] = bad ? NAN : Z[cc];
+        }
     }
   }
   pdl_trigger();  // after this CTA's last write
+}
+
+template <bool GATHER, int NT, bool WIN>
+cudaError_t launch_round(const DecodeArgs& a, dim3 grid, cudaStream_t s) {
+  const size_t smem = sizeof(Q4Smem<NT>) + 1024;  // + slack for the 1024-byte alignment
+  auto kern = decode_q4_round_kernel<GATHER, NT, WIN>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  e = launch_pdl(kern, grid, dim3(kQ4Warps * 32), smem, s, a);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
 }
 
 }  // namespace q4r
 
 cudaError_t launch_decode_q4(const DecodeArgs& a, int B, cudaStream_t s) {
   using namespace q4r;
-  const size_t smem = sizeof(Q4Smem) + 1024;  // + slack for the 1024-byte alignment
-  auto kern = a.sel ? decode_q4_round_kernel<true> : decode_q4_round_kernel<false>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  if (e != cudaSuccess) return e;
-  const dim3 grid = a.nrows > 0 ? dim3(a.P * a.nrows, a.c.num_kv_heads, 1) : dim3(a.P, a.c.num_kv_heads, B);
-  e = launch_pdl(kern, grid, dim3(kQ4Warps * 32), smem, s, a);
-  if (e != cudaSuccess) return e;
-  return cudaGetLastError();
+  if (a.nrows <= 0) {
+    const dim3 grid(a.P, a.c.num_kv_heads, B);
+    return a.sel ? launch_round<true, 1, false>(a, grid, s) : launch_round<false, 1, false>(a, grid, s);
+  }
+  // Decode window: the rows are cut into the fewest even slices whose
+  // (row, head) columns fit kQ4MaxColTiles tiles of 8.
+  const int rmax = 8 * kQ4MaxColTiles / a.group;  // >= 4 (group <= 8)
+  const int nslices = (a.nrows + rmax - 1) / rmax;
+  DecodeArgs w = a;
+  w.rows_per_cta = (a.nrows + nslices - 1) / nslices;
+  const int nt = (w.rows_per_cta * a.group + 7) / 8;
+  const dim3 grid(a.P, a.c.num_kv_heads, (a.nrows + w.rows_per_cta - 1) / w.rows_per_cta);
+  switch (nt) {
+    case 1: return launch_round<false, 1, true>(w, grid, s);
+    case 2: return launch_round<false, 2, true>(w, grid, s);
+    case 3: return launch_round<false, 3, true>(w, grid, s);
+    default: return launch_round<false, 4, true>(w, grid, s);
+  }
 }
 
 }  // namespace kvq

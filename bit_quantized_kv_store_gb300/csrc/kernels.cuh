@@ -34,11 +34,12 @@ struct DecodeArgs {
   int32_t* status;
   // 4-bit decode only.  Block-table row of sequence b: block_tables + b * bt_stride
   // (bt_stride 0: one table shared by every row of a decode window).  nrows > 0:
-  // the grid enumerates (partition, row) with the row fastest along x (z = 1),
-  // so that the rows of a window read each partition at about the same time
-  // (from L2 after the first); nrows = 0: partitions along x, sequences along z.
+  // a decode window of nrows rows (seq_lens holds each row's length), cut into
+  // slices of rows_per_cta rows (set by the launch) whose (row, head) pairs one
+  // CTA scores together; nrows = 0: one sequence per CTA.
   int bt_stride;
   int nrows;
+  int rows_per_cta;
 };
 
 // Log-sum-exp merge of the partials (merge.cu).

@@ -190,10 +190,15 @@ int32_t kvq_decode_attn(const kvq_cache* cache, const float* q, int32_t num_seqs
  * sequence that share its block table: the draft rows of a speculative-decoding
  * step ([P1] "What it is": shared 512-key chunks plus each row's causal tail).
  * Row i attends keys 0 .. d_row_lens[i] - 1 of the sequence (a causal window:
- * prefix_len + i + 1).  The partials are bit-identical to kvq_decode_attn with
- * num_seqs = num_rows, seq_lens = d_row_lens and the block table repeated for
- * every row; the rows of a partition are scheduled next to each other, so that
- * the cache is read from HBM about once for the window (the others hit L2).
+ * prefix_len + i + 1; the lengths may come in any order).  One pass over each
+ * 512-key partition serves every row: the (row, head) pairs of up to
+ * floor(32 / group) rows face the keys together (more rows are cut into even
+ * slices), so a key's codes are read once and converted once for all of them,
+ * and each row masks the keys past its own end.  The partials are bit-identical
+ * to kvq_decode_attn with num_seqs = num_rows, seq_lens = d_row_lens and the
+ * block table repeated for every row.  A row whose length is out of range is
+ * skipped and flagged (KVQ_DEV_BAD_LENGTH; the merge writes NaN for it), the
+ * others are unaffected.
  * Merge with kvq_merge(num_seqs = num_rows, d_seq_lens = d_row_lens).
  *   q: device fp32 [num_rows, num_q_heads, head_dim] (rotated, as for
  *      kvq_decode_attn); d_row_lens: device int32 [num_rows];

@@ -392,7 +392,12 @@ def test_decode_q4_0_gather(K):
         assert_close(out[b], ref[b], what=f"Q4_0 gather seq {b}")
 
 
-@pytest.mark.parametrize("T0,R", [(1000, 4), (513, 3), (40, 8), (0, 2)])
+# R rows of a GQA group of 6 fill ceil(6 R / 8) column tiles of one CTA (at most
+# 4, i.e. 5 rows); more rows are cut into even slices: R = 1 .. 5 cover 1 .. 4
+# tiles (R = 3 with dead columns), R = 6 two slices of 3, R = 8 two of 4, R = 20
+# four of 5.  T0 = 510 puts the rows' ends on both sides of a partition edge.
+@pytest.mark.parametrize("T0,R", [(1000, 4), (513, 3), (40, 8), (0, 2), (300, 1), (510, 5), (100, 6),
+                                  (2000, 20), (4095, 2)])
 def test_decode_window_equals_plain_rows(K, T0, R):
     """A decode window (R draft rows of one sequence sharing its block table, row i
     attending keys 0 .. T0 + i) gives bit-identical partials and outputs to the
@@ -413,6 +418,56 @@ def test_decode_window_equals_plain_rows(K, T0, R):
     ref = O.decode(o, to_np_in(q), lens, bt_rep, 1 / 16)
     for i in range(R):
         assert_close(out_p[i], ref[i], what=f"window row {i}")
+
+
+@pytest.mark.parametrize("Hk,Hq,R", [(1, 8, 4), (1, 8, 9), (3, 9, 7), (2, 2, 33)])
+def test_decode_window_gqa_groups(K, Hk, Hq, R):
+    """Windows over other GQA group sizes (8: 4 rows fill the 4 column tiles; 3:
+    7 rows in 3 tiles; 1: 33 rows cut into two slices) equal the plain rows."""
+    T0 = 700
+    g, o, bt, _, _ = decode_case(K, [T0 + R], Hk=Hk, Hq=Hq, seed=70 + R)
+    q = synth.heavy_tailed((R, Hq, 256), "cpu", "wing", Hq, R)
+    lens = [T0 + i + 1 for i in range(R)]
+    ml = T0 + R
+    dev_bt = torch.from_numpy(bt).to(DEV)
+    ws_w = K.alloc_workspace(g, R, Hq, ml, device=DEV)
+    out_w = K.decode_window_causal(g, q.to(DEV), T0, dev_bt[0], 0.07, ws_w)
+    out_p, _ = run_decode(K, g, np.repeat(bt, R, axis=0), q, lens, ml, 0.07)
+    assert np.array_equal(out_w.cpu().numpy(), out_p)
+    ref = O.decode(o, to_np_in(q[:2]), lens[:2], np.repeat(bt, 2, axis=0), 0.07)
+    for i in range(2):
+        assert_close(out_p[i], ref[i], what=f"window row {i}")
+
+
+def test_decode_window_rows_in_any_order_and_bad_row(K):
+    """Row lengths need not rise with the row index; a row whose length is out of
+    range is flagged and comes out NaN while the other rows still equal their
+    plain decodes."""
+    lens = [900, 37, 1500, 512, 513]
+    R = len(lens)
+    g, o, bt, _, _ = decode_case(K, [max(lens)], seed=91)
+    q = synth.heavy_tailed((R, 24, 256), "cpu", "winb")
+    ml = max(lens)
+    dev_bt = torch.from_numpy(bt).to(DEV)
+    qr = K.rotate_query(q.to(DEV))
+    for bad in (None, 3):
+        ll = list(lens)
+        if bad is not None:
+            ll[bad] = ml + 1
+        dl = torch.tensor(ll, dtype=torch.int32, device=DEV)
+        ws = K.alloc_workspace(g, R, 24, ml, device=DEV)
+        K.decode_window(g, qr, dl, dev_bt[0], ml, 1 / 16, ws)
+        out = torch.empty((R, 24, 256), dtype=torch.float32, device=DEV)
+        K.merge(g, ws, R, 24, dl, ml, out)
+        out = out.cpu().numpy()
+        good = [i for i in range(R) if i != bad]
+        out_p, _ = run_decode(K, g, np.repeat(bt, len(good), axis=0), q[good], [lens[i] for i in good], ml, 1 / 16)
+        assert np.array_equal(out[good], out_p)
+        if bad is None:
+            assert K.read_status(ws) == 0
+        else:
+            assert K.read_status(ws) & K.DEV_BAD_LENGTH
+            assert np.isnan(out[bad]).all()
 
 
 def test_decode_bad_page_and_length_are_flagged(K):
