@@ -43,7 +43,12 @@ namespace kvq {
 
 constexpr int kQ4D = 256;
 constexpr int kQ4NG = 8;
-constexpr int kQ4TileBytes = 16 * 128;  // codes of one 16-key tile
+constexpr int kQ4TileBytes = 16 * 128;  // codes of one 16-key tile (dense: TMA, 128-byte swizzle)
+constexpr int kQ4GatherRow = 144;       // gather: rows padded to 144 bytes (no swizzle), so that the
+                                        // 8 rows of an ldmatrix fall in 8 distinct bank quads
+// Bytes of one code tile in shared memory
+template <bool GATHER>
+__host__ __device__ constexpr int q4_tile_bytes() { return GATHER ? 16 * kQ4GatherRow : kQ4TileBytes; }
 constexpr int kQ4ScaleBytes = 16 * 16;  // fp16 scales of one 16-key tile
 constexpr float kQ4NoMax = -1e30f;      // softmax reference before the first key (finite: no -inf - -inf)
 
@@ -84,6 +89,25 @@ __device__ __forceinline__ uint2 lds64a(uint32_t addr) {
 __device__ __forceinline__ float2 lds64f(uint32_t addr) {
   float2 v;
   asm volatile("ld.shared.v2.f32 {%0,%1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(addr));
+  return v;
+}
+
+// Four 8x8 matrices of 16-bit elements; lane l gives the address of row l & 7 of
+// matrix l >> 3 (16 contiguous bytes).  Plain: lane (g, t) receives elements
+// (g, 2t), (g, 2t + 1) of each matrix.  Transposed: elements (2t, g), (2t + 1, g).
+__device__ __forceinline__ uint4 ldsm_x4(uint32_t addr) {
+  uint4 v;
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(addr));
+  return v;
+}
+
+__device__ __forceinline__ uint4 ldsm_x4_trans(uint32_t addr) {
+  uint4 v;
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(addr));
   return v;
 }
 
@@ -198,12 +222,13 @@ constexpr int kQ4MaxColTiles = 4;                 // a decode window stacks up t
 // Resident CTAs per SM the register budget is sized for: one column tile (one
 // sequence's GQA group) fits 128 registers; each further tile adds 16 P.V
 // accumulators per thread.
-constexpr int q4_min_blocks(int nt) { return nt == 1 ? 4 : nt == 2 ? 3 : 2; }
+__host__ __device__ constexpr int q4_min_blocks(int nt) { return nt == 1 ? 4 : nt == 2 ? 3 : 2; }
 
-template <int NT>
+template <int NT, bool GATHER>
 struct __align__(1024) Q4Smem {
-  uint8_t kc[kQ4Warps][kQ4TPW][kQ4TileBytes];  // K codes of each warp's tiles of the round (1024-aligned)
-  uint8_t vc[kQ4RoundTiles][kQ4TileBytes];     // V codes of the round's tiles
+  static constexpr int kTile = q4_tile_bytes<GATHER>();
+  uint8_t kc[kQ4Warps][kQ4TPW][kTile];  // K codes of each warp's tiles of the round (1024-aligned)
+  uint8_t vc[kQ4RoundTiles][kTile];     // V codes of the round's tiles
   uint16_t ks[kQ4Warps][kQ4TPW][16 * 8];       // K scales
   uint16_t vs[kQ4RoundTiles][16 * 8];          // V scales
   uint4 qf[NT][kQ4NG][2][32];                  // query fragments [column tile][group][hi, lo][lane]
@@ -261,7 +286,7 @@ __device__ __forceinline__ bool q4_issue_plane(const DecodeArgs& a, int b, int k
     }
     mbar_arrive_expect_tx(bar, nvalid * (128 + 16));
     for (int j = 0; j < nvalid; ++j) {
-      bulk_g2s(dc + j * 128, static_cast<const uint8_t*>(codes) + rows[j] * 128, 128, bar);
+      bulk_g2s(dc + j * kQ4GatherRow, static_cast<const uint8_t*>(codes) + rows[j] * 128, 128, bar);
       bulk_g2s(ds + j * 8, static_cast<const uint16_t*>(scales) + rows[j] * 8, 16, bar);
     }
     return true;
@@ -274,8 +299,8 @@ __device__ __forceinline__ bool q4_issue_plane(const DecodeArgs& a, int b, int k
 template <bool GATHER>
 __device__ __forceinline__ bool q4_issue_own(const DecodeArgs& a, int b, int kvh, int k0, int k1, int rd, int warp,
                                              int lane, int32_t tile_row, const CUtensorMap* map, const void* codes,
-                                             const void* scales, uint8_t (*dc)[kQ4TileBytes], uint16_t (*ds)[16 * 8],
-                                             uint64_t* bar) {
+                                             const void* scales, uint8_t (*dc)[q4_tile_bytes<GATHER>()],
+                                             uint16_t (*ds)[16 * 8], uint64_t* bar) {
   const int tile0 = kQ4RoundTiles * rd + kQ4TPW * warp;
   int32_t rows[kQ4TPW];
 #pragma unroll
@@ -311,7 +336,9 @@ __global__ void __launch_bounds__(kQ4Warps * 32, q4_min_blocks(NT))
   static_assert(WIN || NT == 1, "one sequence's group fills one column tile");
   extern __shared__ uint8_t smem_raw[];
   // 1024-byte alignment for the swizzled tiles (the launch adds 1 KB of slack)
-  Q4Smem<NT>& sm = *reinterpret_cast<Q4Smem<NT>*>(smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u));
+  Q4Smem<NT, GATHER>& sm =
+      *reinterpret_cast<Q4Smem<NT, GATHER>*>(smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u));
+  constexpr int kTile = q4_tile_bytes<GATHER>();
   const int p = blockIdx.x, kvh = blockIdx.y;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, t = lane & 3;
@@ -443,17 +470,16 @@ __global__ void __launch_bounds__(kQ4Warps * 32, q4_min_blocks(NT))
   }
   bool timed_out = false;
 
-  // Byte offsets of this thread's fragments inside a code tile (swizzle: chunk ^ (row & 7)).
-  const int sw = GATHER ? 0 : g;       // rows g and g+8 share (row & 7) = g
-  const int swv = GATHER ? 0 : 2 * t;  // rows 2t, 2t+8 -> 2t ; rows 2t+1, 2t+9 -> 2t+1
-  const uint32_t off_ka0 = g * 128 + (((2 * t) ^ sw) << 4);
-  const uint32_t off_ka1 = g * 128 + (((2 * t + 1) ^ sw) << 4);
-  const uint32_t off_kb0 = off_ka0 + 8 * 128;
-  const uint32_t off_kb1 = off_ka1 + 8 * 128;
-  const uint32_t off_v0 = (2 * t) * 128 + ((g ^ swv) << 4) + 4 * warp;
-  const uint32_t off_v1 = (2 * t + 1) * 128 + ((g ^ (GATHER ? 0 : swv + 1)) << 4) + 4 * warp;
-  const uint32_t off_v2 = off_v0 + 8 * 128;
-  const uint32_t off_v3 = off_v1 + 8 * 128;
+  // ldmatrix addresses inside a code tile.  A row is 8 groups of 16 bytes (32
+  // codes each); lane l addresses row (l & 7) + 8 ((l >> 3) & 1), group-chunk
+  // G + (l >> 4), so the four matrices are (keys 0-7, G), (keys 8-15, G),
+  // (keys 0-7, G + 1), (keys 8-15, G + 1).  Dense tiles carry the 128-byte
+  // swizzle (chunk c of row r at c ^ (r & 7)); gather tiles are padded rows.
+  const int lrow = (lane & 7) + 8 * ((lane >> 3) & 1), lhi = lane >> 4;
+  auto chunk_off = [&](int G) -> uint32_t {  // G even
+    return GATHER ? lrow * kQ4GatherRow + ((G + lhi) << 4) : lrow * 128 + (((G + lhi) ^ (lane & 7)) << 4);
+  };
+  const uint32_t off_vl = chunk_off(2 * warp);  // V: groups 2w, 2w + 1 of this warp
   const uint32_t kc_base = smem_u32(&sm.kc[warp][0][0]);
   const uint32_t ks_base = smem_u32(&sm.ks[warp][0][0]);
   const uint32_t vc_base = smem_u32(&sm.vc[0][0]);
@@ -479,15 +505,14 @@ __global__ void __launch_bounds__(kQ4Warps * 32, q4_min_blocks(NT))
         for (int nt = 0; nt < NT; ++nt) S[u][nt][0] = S[u][nt][1] = S[u][nt][2] = S[u][nt][3] = 0.f;
 #pragma unroll
       for (int w = 0; w < kQ4NG / 2; ++w) {  // group pair (2w, 2w+1): one word of each fragment row
-        uint32_t wa0[kQ4TPW], wa1[kQ4TPW], wb0[kQ4TPW], wb1[kQ4TPW];
+        // kw[u]: codes 8t .. 8t+7 of group 2w (.x key g, .y key g+8) and of group 2w+1 (.z, .w)
+        uint4 kw[kQ4TPW];
         float2 fsa[kQ4TPW], fsb[kQ4TPW];
+        const uint32_t okl = chunk_off(2 * w);
 #pragma unroll
         for (int u = 0; u < kQ4TPW; ++u) {
-          const uint32_t kb = kc_base + u * kQ4TileBytes, sb = ks_base + u * kQ4ScaleBytes;
-          wa0[u] = lds32a(kb + off_ka0 + 4 * w);  // half-words (2t, G = 2w, 2w+1) of row g
-          wa1[u] = lds32a(kb + off_ka1 + 4 * w);  // half-words (2t+1, G)
-          wb0[u] = lds32a(kb + off_kb0 + 4 * w);  // row g+8
-          wb1[u] = lds32a(kb + off_kb1 + 4 * w);
+          const uint32_t kb = kc_base + u * kTile, sb = ks_base + u * kQ4ScaleBytes;
+          kw[u] = ldsm_x4(kb + okl);
           fsa[u] = __half22float2(u32_as_h2(lds32a(sb + g * 16 + 4 * w)));  // K scales (2w, 2w+1) of row g
           fsb[u] = __half22float2(u32_as_h2(lds32a(sb + (g + 8) * 16 + 4 * w)));
         }
@@ -502,13 +527,13 @@ __global__ void __launch_bounds__(kQ4Warps * 32, q4_min_blocks(NT))
             ql[nt] = lds128a(qf_addr + nt * kQfTile + G * 1024 + 512);
             nb[nt] = lds128f(qb_addr + nt * kQbTile + G * 64);
           }
-          const uint32_t sel = e ? 0x4342u : 0x4140u;
 #pragma unroll
           for (int u = 0; u < kQ4TPW; ++u) {
-            const uint32_t xa1 = prmt(wa0[u], 0u, sel);
-            const uint32_t xa2 = prmt(wa1[u], 0u, sel);
-            const uint32_t xb1 = prmt(wb0[u], 0u, sel);
-            const uint32_t xb2 = prmt(wb1[u], 0u, sel);
+            const uint32_t wa = e ? kw[u].z : kw[u].x, wb = e ? kw[u].w : kw[u].y;
+            const uint32_t xa1 = prmt(wa, 0u, 0x4140u);  // codes 8t .. 8t+3 of key g: bytes 0, 1 -> halves
+            const uint32_t xa2 = prmt(wa, 0u, 0x4342u);  // codes 8t+4 .. 8t+7
+            const uint32_t xb1 = prmt(wb, 0u, 0x4140u);  // key g+8
+            const uint32_t xb2 = prmt(wb, 0u, 0x4342u);
             const uint32_t a10 = nib_lo_pair_biased(xa1), a11 = nib_lo_pair_biased(xb1);
             const uint32_t a12 = nib_hi_pair_biased(xa1), a13 = nib_hi_pair_biased(xb1);
             const uint32_t a20 = nib_lo_pair_biased(xa2), a21 = nib_lo_pair_biased(xb2);
@@ -648,10 +673,10 @@ __global__ void __launch_bounds__(kQ4Warps * 32, q4_min_blocks(NT))
         uint2 pp[NT];
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) pp[nt] = lds64a(pb_addr + (j * NT + nt) * 256);
-        const uint32_t cb = vc_base + j * kQ4TileBytes;
+        const uint32_t cb = vc_base + j * kTile;
         const uint32_t sb = vs_base + j * kQ4ScaleBytes;
-        // V scales of keys 2t, 2t+1, 2t+8, 2t+9 and V codes of the same rows
-        // (half-word h = g of groups 2w, 2w+1).
+        // V scales of keys 2t, 2t+1, 2t+8, 2t+9 and V codes of the same rows:
+        // codes 4g .. 4g+3 of groups 2w, 2w+1 (ldmatrix, transposed).
         uint32_t swa = lds32a(sb + (2 * t) * 16);
         uint32_t swb = lds32a(sb + (2 * t + 1) * 16);
         uint32_t swc = lds32a(sb + (2 * t + 8) * 16);
@@ -665,21 +690,17 @@ __global__ void __launch_bounds__(kQ4Warps * 32, q4_min_blocks(NT))
             if (2 * t + 9 >= nvalid) swd = 0u;
           }
         }
-        const uint32_t cw0 = lds32a(cb + off_v0);
-        const uint32_t cw1 = lds32a(cb + off_v1);
-        const uint32_t cw2 = lds32a(cb + off_v2);
-        const uint32_t cw3 = lds32a(cb + off_v3);
+        // .x: keys 2t, 2t+1 of group 2w (bytes 2g, 2g+1 of each key, key 2t in the low
+        // half), .y: keys 2t+8, 2t+9; .z, .w: group 2w+1
+        const uint4 vw = ldsm_x4_trans(cb + off_vl);
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
           const uint32_t ssel = e ? 0x7632u : 0x5410u;
           const uint32_t slo = prmt(swa, swb, ssel);
           const uint32_t shi = prmt(swc, swd, ssel);
-          const uint32_t s0 = e ? 0x6622u : 0x4400u;  // byte X of rows a, b -> bytes 0, 2
-          const uint32_t s1 = e ? 0x7733u : 0x5511u;  // byte X+1
-          const uint32_t x01 = prmt(cw0, cw1, s0);
-          const uint32_t x01b = prmt(cw0, cw1, s1);
-          const uint32_t x23 = prmt(cw2, cw3, s0);
-          const uint32_t x23b = prmt(cw2, cw3, s1);
+          const uint32_t x01 = e ? vw.z : vw.x;  // codes 4g, 4g+1 in the low byte of each half
+          const uint32_t x23 = e ? vw.w : vw.y;
+          const uint32_t x01b = x01 >> 8, x23b = x23 >> 8;  // codes 4g+2, 4g+3
           // d-tile (G,0): rows g <-> d = 32G+4g, g+8 <-> 32G+4g+2 ; (G,1): +1
           const uint32_t l0 = nib_lo_pair(x01), l1 = nib_lo_pair(x01b), l2 = nib_lo_pair(x23), l3 = nib_lo_pair(x23b);
           const uint32_t h0 = nib_hi_pair(x01), h1 = nib_hi_pair(x01b), h2 = nib_hi_pair(x23), h3 = nib_hi_pair(x23b);
@@ -766,7 +787,7 @@ __global__ void __launch_bounds__(kQ4Warps * 32, q4_min_blocks(NT))
 
 template <bool GATHER, int NT, bool WIN>
 cudaError_t launch_round(const DecodeArgs& a, dim3 grid, cudaStream_t s) {
-  const size_t smem = sizeof(Q4Smem<NT>) + 1024;  // + slack for the 1024-byte alignment
+  const size_t smem = sizeof(Q4Smem<NT, GATHER>) + 1024;  // + slack for the 1024-byte alignment
   auto kern = decode_q4_round_kernel<GATHER, NT, WIN>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;

@@ -466,10 +466,9 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_tc_kernel(const __grid_
   } else if (warp >= 8 && (warp & 2) == 0) {
     // ---------------- K decoder (warps 8, 9, 12, 13): key blocks 2kw, 2kw+1 of every tile, by halves
     const int kw = (warp & 1) + 2 * ((warp - 8) >> 2);
-    const int krow = lane >> 2;        // key within the 8-key block
-    const int xb = lane & 1;           // byte of the half-word
-    const int hsel = (lane & 3) >> 1;  // h = 2m + hsel
-    const uint32_t sel_e = spread_sel(xb), sel_o = spread_sel(2 + xb);
+    const int krow = lane >> 2;  // key within the 8-key block
+    // byte lane & 3 of word m of a group's 16 bytes: elements 8m + 2 (lane & 3), + 1
+    const uint32_t sel_b = spread_sel(lane & 3);
     const uint32_t ka = smem_u32(sm.ka), kbuf = smem_u32(sm.kb);
     // stmatrix row address: matrix lane / 8 of the four (group 4 half + lane / 8), its row lane % 8
     const uint32_t st_off = (uint32_t)(lane >> 3) * 4 * 128 + (uint32_t)(lane & 7) * 16;
@@ -493,15 +492,16 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_tc_kernel(const __grid_
           uint2 sc = pf_lds64(st_scales + key * 16 + 8 * half);
           if (jk0 + key >= kmax) sc = make_uint2(0, 0);
           const __half2 s2[4] = {scale_pair(sc.x, 0), scale_pair(sc.x, 1), scale_pair(sc.y, 0), scale_pair(sc.y, 1)};
-#pragma unroll 1
+          // the key's code blocks of groups 4 half .. 4 half + 3 (16-byte chunk G of the row)
+          uint4 wg[4];
+#pragma unroll
+          for (int gl = 0; gl < 4; ++gl) wg[gl] = pf_lds128(st_codes + key * 128 + (((4 * half + gl) ^ (key & 7)) << 4));
+#pragma unroll
           for (int m = 0; m < 4; ++m) {
-            const int h = 2 * m + hsel;
-            // half-words (G = 4 half .. +3, h): bytes 8 half .. +7 of chunk h
-            const uint2 w = pf_lds64(st_codes + key * 128 + ((h ^ (key & 7)) << 4) + 8 * half);
             uint32_t va[4], vb[4];
 #pragma unroll
             for (int gl = 0; gl < 4; ++gl) {
-              const __half2 cv = code_pair(gl < 2 ? w.x : w.y, (gl & 1) ? sel_o : sel_e);
+              const __half2 cv = code_pair(word_at(wg[gl], m), sel_b);
               const __half2 xa = __hmul2(cv, s2[gl]);
               va[gl] = h2_as_u32(xa);
               vb[gl] = h2_as_u32(__hfma2(cv, s2[gl], __hneg2(xa)));  // exact remainder
@@ -521,9 +521,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_tc_kernel(const __grid_
     // ---------------- V decoder (warps 10, 11, 14, 15): key blocks 2vw, 2vw+1 of every tile
     const int vw = (warp & 1) + 2 * ((warp - 10) >> 2);
     const int krow = lane >> 2;
-    const int xb = lane & 1;
-    const int hsel = (lane & 3) >> 1;
-    const uint32_t sel_e = spread_sel(xb), sel_o = spread_sel(2 + xb);
+    const uint32_t sel_b = spread_sel(lane & 3);  // as in the K decoder
     const uint32_t vt = smem_u32(sm.vt);
     // stmatrix row address: matrix lane / 8 of the four (group G), its row lane % 8
     const uint32_t st_off = (uint32_t)(lane >> 3) * 4 * 1024 + (uint32_t)(lane & 7) * 16;
@@ -542,14 +540,14 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_tc_kernel(const __grid_
         __half2 s2[8];
 #pragma unroll
         for (int G = 0; G < 8; ++G) s2[G] = scale_pair(word_at(sc, G >> 1), G & 1);
-#pragma unroll 1
+        uint4 wg[8];  // the key's 8 code blocks (16-byte chunk G of the row)
+#pragma unroll
+        for (int G = 0; G < 8; ++G) wg[G] = pf_lds128(st_codes + key * 128 + ((G ^ (key & 7)) << 4));
+#pragma unroll
         for (int m = 0; m < 4; ++m) {
-          const int h = 2 * m + hsel;
-          const uint4 w = pf_lds128(st_codes + key * 128 + ((h ^ (key & 7)) << 4));
           uint32_t v[8];
 #pragma unroll
-          for (int G = 0; G < 8; ++G)
-            v[G] = h2_as_u32(__hmul2(code_pair(word_at(w, G >> 1), (G & 1) ? sel_o : sel_e), s2[G]));
+          for (int G = 0; G < 8; ++G) v[G] = h2_as_u32(__hmul2(code_pair(word_at(wg[G], m), sel_b), s2[G]));
           // matrix (G, m): d-block 4G + m, key block kbk -> vt + (4G + m) * 1024 + kbk * 128
           const uint32_t base = vt + (uint32_t)m * 1024 + (uint32_t)kbk * 128 + st_off;
           stmatrix_x4_trans(base, v[0], v[1], v[2], v[3]);

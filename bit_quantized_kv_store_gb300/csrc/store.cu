@@ -52,7 +52,10 @@ __global__ void __launch_bounds__(256) store_q4_kernel(kvq_cache c, const void* 
   const void* src = kv ? v : k;
   const int64_t base = (tok * Hk + head) * D;
 
-  uint32_t hw[NG];       // lane 4h keeps half-word h of every group
+  // The warp's row is staged in shared memory (group G's 16 bytes at 16G) and
+  // then written with one 16-byte store per group.
+  __shared__ __align__(16) uint8_t stage[8][NG * 16];
+  uint8_t* my_stage = stage[threadIdx.x >> 5];
   uint16_t scale16[NG];  // warp-uniform
 #pragma unroll
   for (int G = 0; G < NG; ++G) {
@@ -71,33 +74,16 @@ __global__ void __launch_bounds__(256) store_q4_kernel(kvq_cache c, const void* 
       q = fminf(fmaxf(q, -8.0f), 7.0f);
       code = static_cast<int>(q) + 8;
     }
-    // gather the four codes of half-word h = lane/4 into lane 4h
+    // gather the four codes of half-word h = lane/4 (elements 4h .. 4h+3) into lane 4h
     uint32_t bits = static_cast<uint32_t>(code) << (4 * (lane & 3));
     bits |= __shfl_xor_sync(0xffffffffu, bits, 1);
     bits |= __shfl_xor_sync(0xffffffffu, bits, 2);
-    hw[G] = bits;
+    if ((lane & 3) == 0) reinterpret_cast<uint16_t*>(my_stage)[8 * G + (lane >> 2)] = static_cast<uint16_t>(bits);
     scale16[G] = __half_as_ushort(s16);
   }
+  __syncwarp();
   uint8_t* codes = static_cast<uint8_t*>(kv ? c.v : c.k) + r * (D / 2);
-  if ((lane & 3) == 0) {
-    const int h = lane >> 2;
-    // half-word (G, h) lives at byte 2 * (h * NG + G): NG consecutive half-words.
-    uint16_t* dst = reinterpret_cast<uint16_t*>(codes + 2 * h * NG);
-    if constexpr (NG % 8 == 0) {
-#pragma unroll
-      for (int G = 0; G < NG; G += 8) {
-        uint4 w;
-        w.x = hw[G] | (hw[G + 1] << 16);
-        w.y = hw[G + 2] | (hw[G + 3] << 16);
-        w.z = hw[G + 4] | (hw[G + 5] << 16);
-        w.w = hw[G + 6] | (hw[G + 7] << 16);
-        reinterpret_cast<uint4*>(dst)[G / 8] = w;
-      }
-    } else {
-#pragma unroll
-      for (int G = 0; G < NG; ++G) dst[G] = static_cast<uint16_t>(hw[G]);
-    }
-  }
+  if (lane < NG) reinterpret_cast<uint4*>(codes)[lane] = reinterpret_cast<const uint4*>(my_stage)[lane];
   uint16_t* sc = static_cast<uint16_t*>(kv ? c.v_scale : c.k_scale) + r * NG;
   if (lane < NG) {
     uint16_t mine = 0;
@@ -155,8 +141,8 @@ __device__ __forceinline__ void store_q4_group_warp(const kvq_cache& c, const vo
   bits |= __shfl_xor_sync(0xffffffffu, bits, 2);
   uint8_t* codes = static_cast<uint8_t*>(kv ? c.v : c.k) + r * (D / 2);
   if ((lane & 3) == 0) {
-    const int h = lane >> 2;  // half-word (G, h) lives at byte 2 * (h * NG + G)
-    reinterpret_cast<uint16_t*>(codes)[h * NG + G] = static_cast<uint16_t>(bits);
+    const int h = lane >> 2;  // half-word h of group G: bytes 16G + 2h, 16G + 2h + 1
+    reinterpret_cast<uint16_t*>(codes)[8 * G + h] = static_cast<uint16_t>(bits);
   }
   if (lane == 0) (static_cast<uint16_t*>(kv ? c.v_scale : c.k_scale) + r * NG)[G] = __half_as_ushort(s16);
 }

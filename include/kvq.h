@@ -71,10 +71,9 @@ typedef enum { KVQ_DT_F32 = 0, KVQ_DT_BF16 = 1 } kvq_dtype;
  *   fp16 scale:  scale = fp16_rne(amax/8) (saturated to 65504),
  *   code = clamp(rint_even(y / scale), -8, 7) + 8  (all codes 8 when scale == 0),
  *   value = (code - 8) * scale, in the rotated space.
- *   Codes plane: row r occupies D/2 bytes at r * D/2.  Inside a row, canonical
- *   group G (16 bytes; byte b = element 2b in the low nibble, 2b+1 in the high
- *   nibble) is cut into 8 half-words; half-word h of group G (elements
- *   32G+4h .. 32G+4h+3) is stored at byte offset 2 * (h * D/32 + G).
+ *   Codes plane: row r occupies D/2 bytes at r * D/2, the groups in order:
+ *   group G at bytes 16G .. 16G + 15, byte b of it holding element 32G + 2b in
+ *   the low nibble and 32G + 2b + 1 in the high nibble.
  *   Scale plane: row r occupies D/32 fp16 values at r * D/32, in group order.
  *   For D = 256 a row is 128 + 16 = 144 bytes.
  * KVQ_FMT_Q4_0 ([P2] PR body: 32 values -> 16 bytes + one fp16 scale, symmetric;

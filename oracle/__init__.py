@@ -73,10 +73,8 @@ def _declare(lib):
         "kvo_fwht32_f32_n": (None, [_P, _I64]),
         "kvo_hadamard32_f64_n": (None, [_P, _P, _I64]),
         "kvo_rotation_constant": (ctypes.c_float, []),
-        "kvo_q4_stored_offset": (_I32, [_I32, _I32, _I32]),
         "kvo_q4_quantize_row": (None, [_P, _I32, _P, _P]),
         "kvo_q4_0_quantize_row": (None, [_P, _I32, _P, _P]),
-        "kvo_q4_canon_to_stored": (None, [_P, _I32, _P]),
         "kvo_q4_dequant_row": (None, [_P, _P, _I32, _P]),
         "kvo_fp8_encode_row": (ctypes.c_float, [_P, _I32, _P]),
         "kvo_store": (_I32, [ctypes.POINTER(_Cache), _P, _P, _I32, _I64, _P]),
@@ -156,26 +154,16 @@ def rotation_constant():
     return _L().kvo_rotation_constant()
 
 
-def q4_stored_offset(D, G, h):
-    return _L().kvo_q4_stored_offset(D, G, h)
-
-
 def q4_quantize_row(x, rotate=True):
-    """One row of D fp32 values -> (canonical codes [D/2] u8, scales [D/32] fp16 bits);
-    rotate=False: the unrotated Q4_0 form."""
+    """One row of D fp32 values -> (stored codes [D/2] u8: group G at bytes 16G ..,
+    element 2b / 2b+1 in the low / high nibble of byte b of its group; scales [D/32]
+    fp16 bits); rotate=False: the unrotated Q4_0 form."""
     x = _c(x, np.float32)
     D = x.size
-    canon = np.empty(D // 2, np.uint8)
+    codes = np.empty(D // 2, np.uint8)
     sc = np.empty(D // 32, np.uint16)
-    (_L().kvo_q4_quantize_row if rotate else _L().kvo_q4_0_quantize_row)(_ptr(x), D, _ptr(canon), _ptr(sc))
-    return canon, sc
-
-
-def q4_canon_to_stored(canon):
-    canon = _c(canon, np.uint8)
-    out = np.empty_like(canon)
-    _L().kvo_q4_canon_to_stored(_ptr(canon), canon.size * 2, _ptr(out))
-    return out
+    (_L().kvo_q4_quantize_row if rotate else _L().kvo_q4_0_quantize_row)(_ptr(x), D, _ptr(codes), _ptr(sc))
+    return codes, sc
 
 
 def q4_dequant_row(stored, scales):

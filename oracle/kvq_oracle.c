@@ -34,10 +34,10 @@
  *  R3  scale = fp16_rne(amax / 8), saturated to 65504; codes are computed with the
  *      stored fp16 scale: code = clamp(rint_even(y / s), -8, 7) + 8; s == 0 gives
  *      code 8 everywhere.
- *  R4  Nibble order inside the 32-value group: byte b holds element 2b in its low
- *      nibble and element 2b + 1 in its high nibble ("canonical" order).  The
- *      stored 4-bit row permutes these canonical bytes by half-words: see
- *      kvo_q4_stored_offset().
+ *  R4  Row layout: the groups' 16-byte code blocks in group order (group G at
+ *      bytes 16G .. 16G + 15, the plainest reading of "32 values -> 16 bytes +
+ *      one fp16 scale"); inside a block, byte b holds element 2b in its low
+ *      nibble and element 2b + 1 in its high nibble.
  *  R5  A decode query at context N attends T keys; the split uses partitions
  *      [512p, 512p + 512) with the last one the tail; the merge takes partitions
  *      in ascending order.
@@ -204,21 +204,11 @@ void kvo_hadamard32_f64(const double* x, double* y) {
 /* 4-bit rotated rows                                                         */
 /* ------------------------------------------------------------------------- */
 
-/* Stored row layout (R4).  A row of D values has NG = D/32 groups; in canonical
- * order group G occupies 16 bytes = 8 half-words, half-word h holding elements
- * 32G + 4h .. 32G + 4h + 3 (byte 0 of the half-word: elements 4h, 4h+1; byte 1:
- * 4h+2, 4h+3; low nibble = even element).  The stored row is the transpose of
- * that NG x 8 half-word matrix: half-word (G, h) sits at byte 2 * (h * NG + G). */
-int kvo_q4_stored_offset(int D, int G, int h) {
-  int NG = D / 32;
-  return 2 * (h * NG + G);
-}
-
-/* Quantise one row of D fp32 values (D a multiple of 32) into canonical codes
- * (D/2 bytes) and NG fp16 scales, following R2 and R3; `rotate` = 0 skips the
+/* Quantise one row of D fp32 values (D a multiple of 32) into its stored code
+ * bytes (D/2, layout R4) and NG fp16 scales, following R2 and R3; `rotate` = 0 skips the
  * rotation (the unrotated Q4_0 form of "feat(kvcache): add reliable quantized
  * KV cache", PR body: 32 values -> 16 bytes + one fp16 scale, symmetric). */
-static void q4_quantize_row(const float* x, int D, uint8_t* canon, uint16_t* scales, int rotate) {
+static void q4_quantize_row(const float* x, int D, uint8_t* codes_out, uint16_t* scales, int rotate) {
   int NG = D / 32;
   for (int G = 0; G < NG; G++) {
     float y[32];
@@ -248,27 +238,16 @@ static void q4_quantize_row(const float* x, int D, uint8_t* canon, uint16_t* sca
       codes[i] = c;
     }
     for (int b = 0; b < 16; b++)
-      canon[16 * G + b] = (uint8_t)(codes[2 * b] | (codes[2 * b + 1] << 4));
+      codes_out[16 * G + b] = (uint8_t)(codes[2 * b] | (codes[2 * b + 1] << 4));
   }
 }
 
-void kvo_q4_quantize_row(const float* x, int D, uint8_t* canon, uint16_t* scales) {
-  q4_quantize_row(x, D, canon, scales, 1);
+void kvo_q4_quantize_row(const float* x, int D, uint8_t* codes, uint16_t* scales) {
+  q4_quantize_row(x, D, codes, scales, 1);
 }
 
-void kvo_q4_0_quantize_row(const float* x, int D, uint8_t* canon, uint16_t* scales) {
-  q4_quantize_row(x, D, canon, scales, 0);
-}
-
-/* Canonical bytes -> stored row bytes (R4 layout). */
-void kvo_q4_canon_to_stored(const uint8_t* canon, int D, uint8_t* stored) {
-  int NG = D / 32;
-  for (int G = 0; G < NG; G++)
-    for (int h = 0; h < 8; h++) {
-      int o = kvo_q4_stored_offset(D, G, h);
-      stored[o] = canon[16 * G + 2 * h];
-      stored[o + 1] = canon[16 * G + 2 * h + 1];
-    }
+void kvo_q4_0_quantize_row(const float* x, int D, uint8_t* codes, uint16_t* scales) {
+  q4_quantize_row(x, D, codes, scales, 0);
 }
 
 /* Tables of every fp16 and e4m3 value, filled once from the definitions above so
@@ -286,9 +265,9 @@ static void ensure_tables(void) {
 /* Value of element e of a stored row: (code - 8) * scale, in fp64. */
 static double q4_element(const uint8_t* stored, const uint16_t* scales, int D, int e) {
   int G = e / 32, i = e % 32;
-  int h = i / 4, j = i % 4; /* j-th element of half-word h */
-  int o = kvo_q4_stored_offset(D, G, h) + j / 2;
-  int code = (j % 2) ? (stored[o] >> 4) : (stored[o] & 0xF);
+  int o = 16 * G + i / 2; /* R4 */
+  int code = (i % 2) ? (stored[o] >> 4) : (stored[o] & 0xF);
+  (void)D;
   return (double)(code - 8) * g_f16_table[scales[G]];
 }
 
@@ -379,12 +358,9 @@ int kvo_store(const kvo_cache* c, const void* k, const void* v, int dtype, int64
           uint16_t* dst = (uint16_t*)(kv ? c->v : c->k) + r * D;
           for (int i = 0; i < D; i++) dst[i] = kvo_f32_to_bf16(row[i]);
         } else {
-          uint8_t* canon = (uint8_t*)malloc(D / 2);
           uint8_t* dst = (uint8_t*)(kv ? c->v : c->k) + r * (D / 2);
           uint16_t* sc = (uint16_t*)(kv ? c->v_scale : c->k_scale) + r * (D / 32);
-          q4_quantize_row(row, D, canon, sc, c->format == KVO_Q4);
-          kvo_q4_canon_to_stored(canon, D, dst);
-          free(canon);
+          q4_quantize_row(row, D, dst, sc, c->format == KVO_Q4);
         }
         free(row);
       }

@@ -122,11 +122,12 @@ def test_store_q4_0_exact_scale_block(K):
             torch.arange(3, dtype=torch.int32, device=DEV))
     torch.cuda.synchronize()
     assert torch.all(g.k_scale[0, 0, :3] == 1.0)
-    # stored half-word (G, h) holds elements 32G + 4h .. + 3 (low nibble first)
+    # group G's codes sit at bytes 16G .. 16G + 15; bytes 2h, 2h + 1 hold elements
+    # 32G + 4h .. + 3 (low nibble first)
     st = g.k[0, 0, :3].cpu().numpy()
     for G in range(8):
         for h in range(8):
-            o_ = 2 * (h * 8 + G)
+            o_ = 16 * G + 2 * h
             got = [st[:, o_] & 15, st[:, o_] >> 4, st[:, o_ + 1] & 15, st[:, o_ + 1] >> 4]
             for j in range(4):
                 assert np.array_equal(got[j], c[:, 0, 32 * G + 4 * h + j] + 8)

@@ -170,7 +170,7 @@ def test_fp32_butterfly_close_to_definition():
 # --------------------------------------------------------------------------- 4-bit rows
 
 def _canon_codes(canon):
-    """Unpack canonical bytes (low nibble = even element) into integer codes."""
+    """Unpack stored code bytes (groups in order, low nibble = even element) into integer codes."""
     return np.stack([canon & 0xF, canon >> 4], -1).reshape(-1).astype(np.int64)
 
 
@@ -259,8 +259,7 @@ def test_quantize_roundtrip_bounds_and_scale():
         inner = ratio <= 7.5
         assert np.all(err[inner] <= 0.5 * np.broadcast_to(s[:, None], err.shape)[inner] * (1 + 1e-5) + 1e-6)
         assert np.all(err <= 1.01 * s[:, None] + 1e-6)
-        stored = O.q4_canon_to_stored(canon)
-        assert np.allclose(O.q4_dequant_row(stored, sc), deq.reshape(-1), rtol=0, atol=0)
+        assert np.allclose(O.q4_dequant_row(canon, sc), deq.reshape(-1), rtol=0, atol=0)
 
 
 def test_zero_row_and_tiny_scale():
@@ -280,14 +279,20 @@ def test_signed_nibble_shift_form():
         assert shifted == c - 8
 
 
-def test_stored_layout_is_a_half_word_permutation():
-    for D in (32, 64, 128, 256):
+def test_stored_layout_is_group_major():
+    """Exact-scale rows whose element i of group G carries code (G + i) % 16: the
+    stored row holds group G in bytes 16G .. 16G + 15, element 2b in the low and
+    2b + 1 in the high nibble of byte b, and dequantising reads the same places."""
+    for D in (32, 64, 256):
         NG = D // 32
-        offs = sorted(O.q4_stored_offset(D, G, h) for G in range(NG) for h in range(8))
-        assert offs == list(range(0, D // 2, 2))
-    canon = RNG.integers(0, 256, 128).astype(np.uint8)
-    stored = O.q4_canon_to_stored(canon)
-    assert sorted(stored.tolist()) == sorted(canon.tolist())
+        c = np.array([[(G + i) % 16 - 8 for i in range(32)] for G in range(NG)], np.int64)
+        c[:, 31] = -8   # amax 8 in every group -> scale 1.0
+        codes, sc = O.q4_quantize_row(c.reshape(-1).astype(np.float32), rotate=False)
+        assert np.all(sc == 0x3C00)
+        for G in range(NG):
+            for b in range(16):
+                assert codes[16 * G + b] == (c[G, 2 * b] + 8) | ((c[G, 2 * b + 1] + 8) << 4)
+        assert np.array_equal(O.q4_dequant_row(codes, sc), c.reshape(-1).astype(np.float64))
 
 
 # --------------------------------------------------------------------------- attention
