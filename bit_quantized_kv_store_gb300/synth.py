@@ -100,3 +100,12 @@ def distinct_sorted(n, upper, *keys):
     """n distinct integers from [0, upper), sorted ascending (host tensor, int64)."""
     g = generator("cpu", "distinct_sorted", *keys)
     return torch.sort(torch.randperm(upper, generator=g)[:n]).values
+
+
+def sign_mask(n, *keys):
+    """n random signs as a bit mask: [n / 32] int32 words, bit i of word i / 32 set
+    with probability 1/2 (host tensor; the bits of each word are uniform)."""
+    g = generator("cpu", "sign_mask", *keys)
+    bits = torch.randint(0, 2, (n // 32, 32), generator=g, dtype=torch.int64)
+    words = (bits << torch.arange(32, dtype=torch.int64)).sum(1)
+    return torch.where(words >= 2**31, words - 2**32, words).to(torch.int32)

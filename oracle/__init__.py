@@ -26,8 +26,9 @@ _lock = threading.Lock()
 _lib = None
 
 # Formats and input dtypes, mirrored from the C enums of the oracle.  Q4_0: the
-# 4-bit rows without the rotation.
-Q4, BF16, FP8, Q4_0 = 0, 1, 2, 3
+# 4-bit rows without the rotation; TQ4: randomized-Hadamard rows with the
+# Lloyd-Max codebook.
+Q4, BF16, FP8, Q4_0, TQ4 = 0, 1, 2, 3, 4
 IN_F32, IN_BF16 = 0, 1
 
 
@@ -59,7 +60,7 @@ _I32 = ctypes.c_int
 class _Cache(ctypes.Structure):
     _fields_ = [("format", ctypes.c_int), ("num_kv_heads", ctypes.c_int), ("head_dim", ctypes.c_int),
                 ("rope_dim", ctypes.c_int), ("page_size", ctypes.c_int), ("num_pages", ctypes.c_int),
-                ("k", _P), ("k_scale", _P), ("v", _P), ("v_scale", _P)]
+                ("k", _P), ("k_scale", _P), ("v", _P), ("v_scale", _P), ("signs", _P)]
 
 
 def _declare(lib):
@@ -77,6 +78,11 @@ def _declare(lib):
         "kvo_q4_0_quantize_row": (None, [_P, _I32, _P, _P]),
         "kvo_q4_dequant_row": (None, [_P, _P, _I32, _P]),
         "kvo_fp8_encode_row": (ctypes.c_float, [_P, _I32, _P]),
+        "kvo_tq4_level": (ctypes.c_double, [_I32]),
+        "kvo_tq4_rotate_f32": (None, [_P, _I32, _P, _P]),
+        "kvo_tq4_rotate_f64": (None, [_P, _I32, _P, _I32, _P]),
+        "kvo_tq4_quantize_row": (ctypes.c_uint16, [_P, _I32, _P, _P]),
+        "kvo_tq4_dequant_row": (None, [_P, ctypes.c_uint16, _I32, _P]),
         "kvo_store": (_I32, [ctypes.POINTER(_Cache), _P, _P, _I32, _I64, _P]),
         "kvo_decode": (_I32, [ctypes.POINTER(_Cache), _P, _I32, _I32, _I32, _P, _P, _I32, _P, _I32,
                               ctypes.c_double, _I32, _P]),
@@ -175,6 +181,43 @@ def q4_dequant_row(stored, scales):
     return out
 
 
+def tq4_levels():
+    """The 16 TQ4 levels, indexed by code (code & 8: negative)."""
+    return np.array([_L().kvo_tq4_level(c) for c in range(16)])
+
+
+def tq4_rotate_f32(x, signs):
+    """The store's fp32 signed butterfly of one row."""
+    x = _c(x, np.float32)
+    y = np.empty_like(x)
+    _L().kvo_tq4_rotate_f32(_ptr(x), x.size, _ptr(_c(signs, np.uint32)), _ptr(y))
+    return y
+
+
+def tq4_rotate_f64(x, signs, inverse=False):
+    """The signed transform by its matrix definition (fp64), forward or inverse."""
+    x = _c(x, np.float64)
+    y = np.empty_like(x)
+    _L().kvo_tq4_rotate_f64(_ptr(x), x.size, _ptr(_c(signs, np.uint32)), int(inverse), _ptr(y))
+    return y
+
+
+def tq4_quantize_row(x, signs):
+    """One row -> (codes [n/2] u8, fp16 scale bits)."""
+    x = _c(x, np.float32)
+    codes = np.empty(x.size // 2, np.uint8)
+    sc = _L().kvo_tq4_quantize_row(_ptr(x), x.size, _ptr(_c(signs, np.uint32)), _ptr(codes))
+    return codes, np.uint16(sc)
+
+
+def tq4_dequant_row(codes, scale):
+    """Rotated-space values of a stored TQ4 row (fp64)."""
+    codes = _c(codes, np.uint8)
+    out = np.empty(codes.size * 2, np.float64)
+    _L().kvo_tq4_dequant_row(_ptr(codes), int(scale), codes.size * 2, _ptr(out))
+    return out
+
+
 def fp8_encode_row(x):
     x = _c(x, np.float32)
     codes = np.empty(x.size, np.uint8)
@@ -191,13 +234,23 @@ class Cache:
     BF16: k/v [num_pages, Hk, page_size, D] bf16 bits, no scales
     FP8:  latent codes [num_pages, page_size, D] u8, rope codes [.., rope] u8,
           latent / rope scales [num_pages, page_size] f32
+    TQ4:  k/v codes [num_pages, Hk, page_size, D/2] u8, one scale per row
+          [num_pages, Hk, page_size] fp16 bits; `signs` the rotation's sign mask
+          [D/32] u32 (bit i set: element i negated)
     """
 
-    def __init__(self, fmt, num_kv_heads, head_dim, page_size, num_pages, rope_dim=0):
+    def __init__(self, fmt, num_kv_heads, head_dim, page_size, num_pages, rope_dim=0, signs=None):
         self.fmt, self.Hk, self.D, self.page_size, self.num_pages = fmt, num_kv_heads, head_dim, page_size, num_pages
         self.rope = rope_dim
+        self.signs = None if signs is None else _c(signs, np.uint32)
         rows = (num_pages, num_kv_heads, page_size)
-        if fmt in (Q4, Q4_0):
+        if fmt == TQ4:
+            assert self.signs is not None and self.signs.size == head_dim // 32
+            self.k = np.zeros(rows + (head_dim // 2,), np.uint8)
+            self.v = np.zeros_like(self.k)
+            self.k_scale = np.zeros(rows, np.uint16)
+            self.v_scale = np.zeros_like(self.k_scale)
+        elif fmt in (Q4, Q4_0):
             self.k = np.zeros(rows + (head_dim // 2,), np.uint8)
             self.v = np.zeros_like(self.k)
             self.k_scale = np.zeros(rows + (head_dim // 32,), np.uint16)
@@ -215,7 +268,7 @@ class Cache:
 
     def _struct(self):
         return _Cache(self.fmt, self.Hk, self.D, self.rope, self.page_size, self.num_pages,
-                      _ptr(self.k), _ptr(self.k_scale), _ptr(self.v), _ptr(self.v_scale))
+                      _ptr(self.k), _ptr(self.k_scale), _ptr(self.v), _ptr(self.v_scale), _ptr(self.signs))
 
 
 def _in(x):

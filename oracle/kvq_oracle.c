@@ -41,6 +41,23 @@
  *  R5  A decode query at context N attends T keys; the split uses partitions
  *      [512p, 512p + 512) with the last one the tail; the merge takes partitions
  *      in ascending order.
+ *  R7  TQ4 rows ([P3] "KV cache quantization: fp8 (KV8) + 4-bit TurboQuant", PR
+ *      body, "Why rotated-int4": a randomized-Hadamard rotation, then a fixed
+ *      16-level Lloyd-Max codebook for N(0,1) scaled by radius/sqrt(n); the
+ *      rotation keeps the radius, so one scale per row).  The pages leave the
+ *      details open; read here as: n = head_dim; the random signs are a
+ *      caller-given bit mask (bit i set: element i negated before the
+ *      transform); y = fp32 butterfly of the signed row (stages h = 1 .. n/2 as
+ *      in R2) times fp32(1/sqrt(n)); ss = fp32 sum of the fp32 squares by the
+ *      pairwise tree (stage h adds element i + h into i for i a multiple of
+ *      2h); scale = fp16_sat(sqrtf(ss * (1/n))), and the codes use the stored
+ *      fp16 scale; the codebook is the Lloyd-Max levels rounded to fp16 (8
+ *      magnitudes M_0 < .. < M_7, the levels being +-M_m); code = 8 * [v < 0] +
+ *      #{k < 7 : |v| > (M_k + M_{k+1}) / 2} for v = y / scale (fp32 division;
+ *      a tie goes to the smaller magnitude); scale 0 gives code 0 everywhere.
+ *      Value = (code & 8 ? -1 : 1) * M_{code & 7} * scale, in the rotated space;
+ *      queries are rotated by the same signed transform, outputs back by its
+ *      inverse (signs after the transform).  Codes are stored as in R4.
  *  R6  fp8 rows: separate scales for the latent part and the rope part, each
  *      amax/448; codes = e4m3(x * (448/amax)) with 448/amax computed once in fp32;
  *      amax == 0 or a non-finite 448/amax stores all-zero codes.
@@ -277,15 +294,99 @@ void kvo_q4_dequant_row(const uint8_t* stored, const uint16_t* scales, int D, do
 }
 
 /* ------------------------------------------------------------------------- */
+/* TQ4 rows (R7)                                                              */
+/* ------------------------------------------------------------------------- */
+
+/* The 16-level Lloyd-Max quantizer of N(0,1) (levels +-M_m), each magnitude
+ * rounded to the nearest fp16 value (written out exactly). */
+static const double kTq4M[8] = {0.12841796875, 0.387939453125, 0.65673828125, 0.9423828125,
+                                1.255859375,   1.6181640625,   2.068359375,   2.732421875};
+
+double kvo_tq4_level(int code) { return (code & 8 ? -1.0 : 1.0) * kTq4M[code & 7]; }
+
+static int tq4_sign(const uint32_t* signs, int i) { return (signs[i / 32] >> (i % 32)) & 1; }
+
+/* The store's rotation: y = fp32 butterfly of the signed row, times fp32(1/sqrt(n)). */
+void kvo_tq4_rotate_f32(const float* x, int n, const uint32_t* signs, float* y) {
+  for (int i = 0; i < n; i++) y[i] = tq4_sign(signs, i) ? -x[i] : x[i];
+  for (int h = 1; h < n; h <<= 1)
+    for (int i = 0; i < n; i++) {
+      if (i & h) continue;
+      float a = y[i], b = y[i + h];
+      y[i] = a + b;
+      y[i + h] = a - b;
+    }
+  const float c = (float)(1.0 / sqrt((double)n));
+  for (int i = 0; i < n; i++) y[i] = y[i] * c;
+}
+
+/* The transform by its matrix definition, fp64: forward y = H (s * x) / sqrt(n),
+ * inverse y = s * (H x) / sqrt(n), H[i][j] = (-1)^popcount(i & j). */
+void kvo_tq4_rotate_f64(const double* x, int n, const uint32_t* signs, int inverse, double* y) {
+  const double c = 1.0 / sqrt((double)n);
+  for (int i = 0; i < n; i++) {
+    double acc = 0.0;
+    for (int j = 0; j < n; j++) {
+      double xj = (!inverse && tq4_sign(signs, j)) ? -x[j] : x[j];
+      acc += (__builtin_popcount((unsigned)(i & j)) & 1) ? -xj : xj;
+    }
+    y[i] = acc * c;
+    if (inverse && tq4_sign(signs, i)) y[i] = -y[i];
+  }
+}
+
+/* Quantise one row of n fp32 values (R7): n/2 code bytes (R4 order) and one fp16
+ * scale (returned). */
+uint16_t kvo_tq4_quantize_row(const float* x, int n, const uint32_t* signs, uint8_t* codes_out) {
+  float* y = (float*)malloc(sizeof(float) * n);
+  float* v = (float*)malloc(sizeof(float) * n);
+  kvo_tq4_rotate_f32(x, n, signs, y);
+  for (int i = 0; i < n; i++) v[i] = y[i] * y[i];
+  for (int h = 1; h < n; h <<= 1)
+    for (int i = 0; i < n; i += 2 * h) v[i] = v[i] + v[i + h];
+  float ss = v[0];
+  uint16_t s16 = kvo_f32_to_f16_sat(sqrtf(ss * (1.0f / (float)n)));
+  float s = (float)kvo_f16_to_f64(s16);
+  float tau[7];
+  for (int k = 0; k < 7; k++) tau[k] = ((float)kTq4M[k] + (float)kTq4M[k + 1]) * 0.5f;
+  for (int i = 0; i < n; i += 2) {
+    int c[2];
+    for (int e = 0; e < 2; e++) {
+      c[e] = 0;
+      if (s > 0.0f) {
+        float r = y[i + e] / s; /* IEEE fp32 division */
+        float a = fabsf(r);
+        int m = 0;
+        for (int k = 0; k < 7; k++) m += a > tau[k];
+        c[e] = (r < 0.0f ? 8 : 0) | m;
+      }
+    }
+    codes_out[i / 2] = (uint8_t)(c[0] | (c[1] << 4));
+  }
+  free(y);
+  free(v);
+  return s16;
+}
+
+/* Rotated-space values of one stored TQ4 row, fp64. */
+void kvo_tq4_dequant_row(const uint8_t* codes, uint16_t scale, int n, double* out) {
+  double s = kvo_f16_to_f64(scale);
+  for (int i = 0; i < n; i++) {
+    int c = (i % 2) ? (codes[i / 2] >> 4) : (codes[i / 2] & 0xF);
+    out[i] = kvo_tq4_level(c) * s;
+  }
+}
+
+/* ------------------------------------------------------------------------- */
 /* Cache description used by the oracle (its own struct, not the library's).  */
 /* ------------------------------------------------------------------------- */
 
 /* KVO_Q4_0: the 4-bit rows without the rotation (same codes, scales and layout). */
-enum { KVO_Q4 = 0, KVO_BF16 = 1, KVO_FP8 = 2, KVO_Q4_0 = 3 };
+enum { KVO_Q4 = 0, KVO_BF16 = 1, KVO_FP8 = 2, KVO_Q4_0 = 3, KVO_TQ4 = 4 };
 enum { KVO_IN_F32 = 0, KVO_IN_BF16 = 1 };
 
 typedef struct {
-  int format;       /* KVO_Q4, KVO_BF16, KVO_FP8, KVO_Q4_0 */
+  int format;       /* KVO_Q4, KVO_BF16, KVO_FP8, KVO_Q4_0, KVO_TQ4 */
   int num_kv_heads; /* FP8: 1 */
   int head_dim;     /* Q4/BF16: D; FP8: latent width */
   int rope_dim;     /* FP8 only */
@@ -294,7 +395,8 @@ typedef struct {
   void* k;          /* Q4: codes; BF16: bf16 rows; FP8: latent e4m3 rows */
   void* k_scale;    /* Q4: fp16 scales; FP8: latent f32 scales */
   void* v;          /* Q4: codes; BF16: bf16 rows; FP8: rope e4m3 rows */
-  void* v_scale;    /* Q4: fp16 scales; FP8: rope f32 scales */
+  void* v_scale;    /* Q4: fp16 scales; FP8: rope f32 scales; TQ4: one fp16 scale per row */
+  const uint32_t* signs; /* TQ4: rotation sign mask [head_dim / 32] */
 } kvo_cache;
 
 /* Row index of (page, head, slot) in every plane. */
@@ -357,6 +459,9 @@ int kvo_store(const kvo_cache* c, const void* k, const void* v, int dtype, int64
         if (c->format == KVO_BF16) {
           uint16_t* dst = (uint16_t*)(kv ? c->v : c->k) + r * D;
           for (int i = 0; i < D; i++) dst[i] = kvo_f32_to_bf16(row[i]);
+        } else if (c->format == KVO_TQ4) {
+          uint8_t* dst = (uint8_t*)(kv ? c->v : c->k) + r * (D / 2);
+          ((uint16_t*)(kv ? c->v_scale : c->k_scale))[r] = kvo_tq4_quantize_row(row, D, c->signs, dst);
         } else {
           uint8_t* dst = (uint8_t*)(kv ? c->v : c->k) + r * (D / 2);
           uint16_t* sc = (uint16_t*)(kv ? c->v_scale : c->k_scale) + r * (D / 32);
@@ -374,7 +479,7 @@ int kvo_store(const kvo_cache* c, const void* k, const void* v, int dtype, int64
 /* ------------------------------------------------------------------------- */
 
 /* Key and value vectors of absolute position pos of a sequence with block table
- * bt, KV head hd, as fp64.  Q4 rows are returned in the rotated space they are
+ * bt, KV head hd, as fp64.  Q4 and TQ4 rows are returned in the rotated space they are
  * stored in.  Returns 0 if the block table points outside the pool. */
 static int load_kv(const kvo_cache* c, const int32_t* bt, int64_t pos, int hd, double* kvec,
                    double* vvec) {
@@ -389,6 +494,9 @@ static int load_kv(const kvo_cache* c, const int32_t* bt, int64_t pos, int hd, d
                        D, kvec);
     kvo_q4_dequant_row((const uint8_t*)c->v + r * (D / 2), (const uint16_t*)c->v_scale + r * (D / 32),
                        D, vvec);
+  } else if (c->format == KVO_TQ4) {
+    kvo_tq4_dequant_row((const uint8_t*)c->k + r * (D / 2), ((const uint16_t*)c->k_scale)[r], D, kvec);
+    kvo_tq4_dequant_row((const uint8_t*)c->v + r * (D / 2), ((const uint16_t*)c->v_scale)[r], D, vvec);
   } else if (c->format == KVO_BF16) {
     for (int i = 0; i < D; i++) {
       kvec[i] = kvo_bf16_to_f32(((const uint16_t*)c->k)[r * D + i]);
@@ -413,13 +521,16 @@ static int key_width(const kvo_cache* c) {
 }
 
 /* Prepare the query of one head in the space the cache is stored in: Q4 rotates
- * each 32-group by H (fp64), the other formats use it as given. */
+ * each 32-group by H (fp64), TQ4 the whole row by its signed transform, the
+ * other formats use it as given. */
 static void prep_query(const kvo_cache* c, const void* q, int dtype, int64_t off, double* out) {
   int W = key_width(c);
   double* tmp = (double*)malloc(sizeof(double) * W);
   for (int i = 0; i < W; i++) tmp[i] = load_in(q, dtype, off + i);
   if (c->format == KVO_Q4) {
     for (int G = 0; G < W / 32; G++) kvo_hadamard32_f64(tmp + 32 * G, out + 32 * G);
+  } else if (c->format == KVO_TQ4) {
+    kvo_tq4_rotate_f64(tmp, W, c->signs, 0, out);
   } else {
     memcpy(out, tmp, sizeof(double) * W);
   }
@@ -430,7 +541,7 @@ static void prep_query(const kvo_cache* c, const void* q, int dtype, int64_t off
  * split == 0: single pass, softmax over all keys at once.
  * split == 1: partitions of 512 listed keys (the last one the tail), each giving
  *             (m_p, z_p, acc_p); merged in ascending p by log-sum-exp.
- * Writes the context (value width) to out, rotated back for Q4.
+ * Writes the context (value width) to out, rotated back for Q4 and TQ4.
  * Returns 0 on a block-table entry outside the pool. */
 static int attend_one(const kvo_cache* c, const int32_t* bt, const double* qv, int hd,
                       const int64_t* pos, int64_t T, double sm_scale, int split, double* out) {
@@ -502,6 +613,8 @@ static int attend_one(const kvo_cache* c, const int32_t* bt, const double* qv, i
   }
   if (c->format == KVO_Q4) {
     for (int G = 0; G < Dv / 32; G++) kvo_hadamard32_f64(o + 32 * G, out + 32 * G);
+  } else if (c->format == KVO_TQ4) {
+    kvo_tq4_rotate_f64(o, Dv, c->signs, 1, out);
   } else {
     memcpy(out, o, sizeof(double) * Dv);
   }
