@@ -50,7 +50,7 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-rows", action="store_true", help="skip the other hot-path rows (batched decode, prefill, "
                     "fp8, bf16 cache, store)")
-    ap.add_argument("--only", choices=["batched", "prefill", "fp8", "bf16", "q4_0", "window"], default=None,
+    ap.add_argument("--only", choices=["batched", "prefill", "fp8", "bf16", "q4_0", "window", "tq4"], default=None,
                     help="run only one of the other hot-path rows and print its measurement (for profiling)")
     ap.add_argument("--layers", type=int, default=16, help="layers per step (16 for the benchmark; fewer "
                     "only to profile a small case)")
@@ -351,6 +351,8 @@ def measure_rows(K, synth, torch, dev, peak, tflops_peak, only=None):
         out.update(_row_q4_0(K, synth, torch, dev, peak, seed))
     if want("window"):
         out.update(_row_window(K, synth, torch, dev, peak, seed))
+    if want("tq4"):
+        out.update(_row_tq4(K, synth, torch, dev, peak, seed))
     return out
 
 
@@ -528,6 +530,44 @@ def _row_q4_0(K, synth, torch, dev, peak, seed):
                              "decode_kernel_us": dms * 1e3, "cache_bytes": byts,
                              "achieved_GBs": byts / (dms * 1e-3) / 1e9, "frac_of_hbm_peak": byts / (dms * 1e-3) / 1e9 / peak,
                              "store_4096_tokens_us": st_ms * 1e3, "kernel": "decode_q4_round_kernel"}
+    del c, ws
+    torch.cuda.empty_cache()
+    return out
+
+
+def _row_tq4(K, synth, torch, dev, peak, seed):
+    """TQ4 rows (randomized Hadamard + 16-level Lloyd-Max codebook, one fp16 scale
+    per row: 130 bytes per row) at 262K: the split-T decode kernel, the full step
+    (query rotation, decode, merge, inverse rotation) and a 4096-token store."""
+    out = {}
+    Tq = 262145
+    npg = (Tq + PS - 1) // PS
+    c = K.Cache(K.FMT_TQ4, HK, D, PS, npg, device=dev, signs=synth.sign_mask(D, seed, "tq4"))
+    for s0 in range(0, Tq, 65536):
+        n = min(65536, Tq - s0)
+        k = synth.heavy_tailed((n, HK, D), dev, seed, "tqk", s0, subset=(seed, "k"))
+        v = synth.heavy_tailed((n, HK, D), dev, seed, "tqv", s0, subset=(seed, "v"))
+        K.store(c, k, v, torch.arange(s0, s0 + n, dtype=torch.int32, device=dev))
+    sk = synth.heavy_tailed((4096, HK, D), dev, seed, "tqsk")
+    sv = synth.heavy_tailed((4096, HK, D), dev, seed, "tqsv")
+    slots = torch.arange(4096, dtype=torch.int32, device=dev)
+    st_ms = _events_time(torch, lambda: K.store(c, sk, sv, slots), 10)
+    q = synth.heavy_tailed((1, HQ, D), dev, seed, "tqq")
+    qr = K.tq4_rotate(c, q)
+    bt = torch.arange(npg, dtype=torch.int32, device=dev).reshape(1, -1)
+    seq = torch.tensor([Tq], dtype=torch.int32, device=dev)
+    ws = K.alloc_workspace(c, 1, HQ, Tq, device=dev)
+    o = torch.empty((1, HQ, D), dtype=torch.float32, device=dev)
+    dms = _events_time(torch, lambda: K.decode_attn(c, qr, seq, bt, Tq, 1 / 16, ws), 10)
+    step_ms = _events_time(torch, lambda: K.decode(c, q, seq, bt, Tq, 1 / 16, ws, out=o), 10)
+    byts = Tq * HK * 2 * (D // 2 + 2)
+    out["tq4_cache_262k"] = {"workload": "TQ4 rows (rotated int4 + Lloyd-Max codebook, 130 B/row), context 262144, "
+                                         "1 layer, 4 KV / 24 q heads",
+                             "decode_kernel_us": dms * 1e3, "cache_bytes": byts,
+                             "achieved_GBs": byts / (dms * 1e-3) / 1e9,
+                             "frac_of_hbm_peak": byts / (dms * 1e-3) / 1e9 / peak,
+                             "step_us": step_ms * 1e3, "store_4096_tokens_us": st_ms * 1e3,
+                             "kernel": "decode_q4_round_kernel<TQ4> (prmt level tables, movmatrix for V)"}
     del c, ws
     torch.cuda.empty_cache()
     return out

@@ -18,7 +18,8 @@ LIB_PATH = os.path.join(_PKG, "_build", "libkvq.so")
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_WORKSPACE_TOO_SMALL = 0, -1, -2, -3, -4
 DEV_BAD_SLOT, DEV_BAD_PAGE, DEV_BAD_LENGTH, DEV_BAD_INDEX, DEV_TIMEOUT = 1, 2, 4, 8, 16
 DT_F32, DT_BF16 = 0, 1
-FMT_Q4_HAD32, FMT_BF16, FMT_FP8_ROW, FMT_Q4_0 = 0, 1, 2, 3  # Q4_0: the 4-bit rows without the rotation
+# Q4_0: the 4-bit rows without the rotation; TQ4: randomized-Hadamard rows with the Lloyd-Max codebook
+FMT_Q4_HAD32, FMT_BF16, FMT_FP8_ROW, FMT_Q4_0, FMT_TQ4 = 0, 1, 2, 3, 4
 
 _P = ctypes.c_void_p
 _I32 = ctypes.c_int32
@@ -29,7 +30,8 @@ _F = ctypes.c_float
 
 class CacheDesc(ctypes.Structure):
     _fields_ = [("format", _I32), ("num_kv_heads", _I32), ("head_dim", _I32), ("rope_dim", _I32),
-                ("page_size", _I32), ("num_pages", _I32), ("k", _P), ("k_scale", _P), ("v", _P), ("v_scale", _P)]
+                ("page_size", _I32), ("num_pages", _I32), ("k", _P), ("k_scale", _P), ("v", _P), ("v_scale", _P),
+                ("signs", _P)]
 
 
 # name -> (restype, argtypes); mirrors include/kvq.h
@@ -40,6 +42,7 @@ SIGNATURES = {
     "kvq_plane_bytes": (_SZ, [ctypes.POINTER(CacheDesc), _I32]),
     "kvq_store": (_I32, [ctypes.POINTER(CacheDesc), _P, _P, _I32, _I64, _P, _P, _P]),
     "kvq_rotate_query": (_I32, [_P, _I32, _P, _I64, _I32, _P]),
+    "kvq_tq4_rotate": (_I32, [ctypes.POINTER(CacheDesc), _P, _I32, _P, _I64, _I32, _P]),
     "kvq_store_rotate": (_I32, [ctypes.POINTER(CacheDesc), _P, _P, _I32, _I64, _P, _P, _P, _I32, _P, _I64, _P]),
     "kvq_decode_workspace_size": (_SZ, [ctypes.POINTER(CacheDesc), _I32, _I32, _I32, _I32]),
     "kvq_decode_attn": (_I32, [ctypes.POINTER(CacheDesc), _P, _I32, _I32, _P, _P, _I32, _I32, _P, _I32, _F, _P,
@@ -112,13 +115,25 @@ class Cache:
     BF16: k, v [num_pages, Hk, page_size, D] bfloat16.
     FP8:  k (latent codes) [num_pages, page_size, D] uint8, v (rope codes)
           [num_pages, page_size, R] uint8, k_scale / v_scale [num_pages, page_size] f32.
+    TQ4:  k, v codes [num_pages, Hk, page_size, D/2] uint8; k_scale, v_scale
+          [num_pages, Hk, page_size] float16; `signs` the rotation's sign mask,
+          int32 [D/32] (bit i set: element i negated), given by the caller.
     """
 
-    def __init__(self, fmt, num_kv_heads, head_dim, page_size, num_pages, device="cuda", rope_dim=0):
+    def __init__(self, fmt, num_kv_heads, head_dim, page_size, num_pages, device="cuda", rope_dim=0, signs=None):
         self.fmt, self.Hk, self.D, self.page_size, self.num_pages = fmt, num_kv_heads, head_dim, page_size, num_pages
         self.rope = rope_dim
+        self.signs = None
         rows = (num_pages, num_kv_heads, page_size)
-        if fmt in (FMT_Q4_HAD32, FMT_Q4_0):
+        if fmt == FMT_TQ4:
+            if signs is None or signs.numel() != head_dim // 32:
+                raise ValueError("TQ4 needs a sign mask of head_dim / 32 words")
+            self.signs = signs.to(device=device, dtype=torch.int32).contiguous()
+            self.k = torch.zeros(rows + (head_dim // 2,), dtype=torch.uint8, device=device)
+            self.v = torch.zeros_like(self.k)
+            self.k_scale = torch.zeros(rows, dtype=torch.float16, device=device)
+            self.v_scale = torch.zeros_like(self.k_scale)
+        elif fmt in (FMT_Q4_HAD32, FMT_Q4_0):
             self.k = torch.zeros(rows + (head_dim // 2,), dtype=torch.uint8, device=device)
             self.v = torch.zeros_like(self.k)
             self.k_scale = torch.zeros(rows + (head_dim // 32,), dtype=torch.float16, device=device)
@@ -140,7 +155,8 @@ class Cache:
     def refresh(self):
         self.desc = CacheDesc(self.fmt, self.Hk, self.D, self.rope, self.page_size, self.num_pages,
                               self.k.data_ptr(), 0 if self.k_scale is None else self.k_scale.data_ptr(),
-                              self.v.data_ptr(), 0 if self.v_scale is None else self.v_scale.data_ptr())
+                              self.v.data_ptr(), 0 if self.v_scale is None else self.v_scale.data_ptr(),
+                              0 if self.signs is None else self.signs.data_ptr())
 
     @property
     def ref(self):
@@ -162,6 +178,16 @@ def rotate_query(x, out=None, stream=None):
     if out is None:
         out = torch.empty(x.shape, dtype=torch.float32, device=x.device)
     _check(lib().kvq_rotate_query(_ptr(x), _dtype_code(x), _ptr(out), rows, D, _stream(stream)), "kvq_rotate_query")
+    return out
+
+
+def tq4_rotate(cache: Cache, x, inverse=False, out=None, stream=None):
+    """The TQ4 cache's signed row transform (queries in; inverse: outputs back)."""
+    rows = x.numel() // cache.D
+    if out is None:
+        out = torch.empty(x.shape, dtype=torch.float32, device=x.device)
+    _check(lib().kvq_tq4_rotate(cache.ref, _ptr(x), _dtype_code(x), _ptr(out), rows, int(inverse), _stream(stream)),
+           "kvq_tq4_rotate")
     return out
 
 
@@ -232,7 +258,7 @@ def decode_attn_unrotated(cache: Cache, q, seq_lens, block_tables, max_seq_len, 
 def merge(cache: Cache, workspace, num_seqs, num_q_heads, seq_lens, max_seq_len, out, n_sel=0, rotate_back=None,
           stream=None):
     if rotate_back is None:
-        rotate_back = cache.fmt == FMT_Q4_HAD32
+        rotate_back = cache.fmt in (FMT_Q4_HAD32, FMT_TQ4)
     _check(lib().kvq_merge(cache.ref, _ptr(workspace), workspace.numel(), num_seqs, num_q_heads, _ptr(seq_lens),
                            max_seq_len, n_sel, int(rotate_back), _ptr(out), _stream(stream)), "kvq_merge")
     return out
@@ -240,11 +266,13 @@ def merge(cache: Cache, workspace, num_seqs, num_q_heads, seq_lens, max_seq_len,
 
 def decode(cache: Cache, q, seq_lens, block_tables, max_seq_len, sm_scale, workspace, out=None, sel=None,
            stream=None):
-    """Rotate the query (4-bit format), decode partials, merge: one decode step."""
+    """Rotate the query (4-bit formats), decode partials, merge: one decode step."""
     B, Hq = q.shape[0], q.shape[1]
     qq = q
     if cache.fmt == FMT_Q4_HAD32:
         qq = rotate_query(q, stream=stream)
+    elif cache.fmt == FMT_TQ4:
+        qq = tq4_rotate(cache, q, stream=stream)
     elif q.dtype != torch.float32:
         qq = q.float()
     decode_attn(cache, qq, seq_lens, block_tables, max_seq_len, sm_scale, workspace, sel=sel, stream=stream)
@@ -271,7 +299,7 @@ def decode_noalloc(cache: Cache, q_rot, seq_lens, block_tables, max_seq_len, sm_
     B, Hq = q_rot.shape[0], q_rot.shape[1]
     n_sel = 0 if sel is None else sel.shape[1]
     if rotate_back is None:
-        rotate_back = cache.fmt == FMT_Q4_HAD32
+        rotate_back = cache.fmt in (FMT_Q4_HAD32, FMT_TQ4)
     _check(lib().kvq_decode_noalloc(cache.ref, _ptr(q_rot), B, Hq, _ptr(seq_lens), _ptr(block_tables),
                                     block_tables.shape[1], max_seq_len, _ptr(sel), n_sel, float(sm_scale),
                                     int(rotate_back), _ptr(out), _ptr(status), _stream(stream)), "kvq_decode_noalloc")

@@ -20,7 +20,7 @@ LIB = os.path.join(BUILD, "libkvq.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", f"-I{os.path.join(ROOT, 'include')}"]
 # The store computes codes that must be bit-exact: no fused multiply-adds there.
-PER_FILE = {"store.cu": ["-fmad=false"]}
+PER_FILE = {"store.cu": ["-fmad=false"], "tq4.cu": ["-fmad=false"]}
 
 
 def _nvcc():

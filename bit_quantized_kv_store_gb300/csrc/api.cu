@@ -27,7 +27,7 @@ static size_t round256(size_t x) { return (x + 255) & ~static_cast<size_t>(255);
 // Validate a cache description; returns KVQ_OK or a negative status.
 static int32_t check_cache(const kvq_cache* c) {
   if (!c) return KVQ_ERR_INVALID_ARG;
-  if (c->format < KVQ_FMT_Q4_HAD32 || c->format > KVQ_FMT_Q4_0) return KVQ_ERR_INVALID_ARG;
+  if (c->format < KVQ_FMT_Q4_HAD32 || c->format > KVQ_FMT_TQ4) return KVQ_ERR_INVALID_ARG;
   if (c->num_kv_heads < 1 || c->head_dim <= 0 || c->page_size <= 0 || c->num_pages < 0)
     return KVQ_ERR_INVALID_ARG;
   if (c->head_dim % 32 != 0) return KVQ_ERR_UNSUPPORTED;  // rows are built from 32-value groups
@@ -37,6 +37,11 @@ static int32_t check_cache(const kvq_cache* c) {
     if (!c->k_scale || !c->v_scale || !aligned16(c->k_scale) || !aligned16(c->v_scale)) return KVQ_ERR_INVALID_ARG;
     const int ng = c->head_dim / 32;
     if (ng != 1 && ng != 2 && ng != 4 && ng != 8) return KVQ_ERR_UNSUPPORTED;
+    if (c->rope_dim != 0) return KVQ_ERR_INVALID_ARG;
+  } else if (c->format == KVQ_FMT_TQ4) {
+    if (!c->k_scale || !c->v_scale || !aligned16(c->k_scale) || !aligned16(c->v_scale)) return KVQ_ERR_INVALID_ARG;
+    if (!c->signs || (reinterpret_cast<uintptr_t>(c->signs) & 3u) != 0) return KVQ_ERR_INVALID_ARG;
+    if (c->head_dim != 64 && c->head_dim != 128 && c->head_dim != 256) return KVQ_ERR_UNSUPPORTED;
     if (c->rope_dim != 0) return KVQ_ERR_INVALID_ARG;
   } else if (c->format == KVQ_FMT_BF16) {
     if (c->rope_dim != 0) return KVQ_ERR_INVALID_ARG;
@@ -108,7 +113,8 @@ static int32_t check_decode_shape(const kvq_cache* c, int B, int Hq, const int32
   if (gather && (n_sel < 1 || n_sel > 4096)) return KVQ_ERR_INVALID_ARG;
   if (!gather && n_sel != 0) return KVQ_ERR_INVALID_ARG;
   const int group = Hq / c->num_kv_heads;
-  if (is_q4(c->format) || c->format == KVQ_FMT_BF16) {
+  if (c->format == KVQ_FMT_TQ4 && gather) return KVQ_ERR_UNSUPPORTED;
+  if (is_q4(c->format) || c->format == KVQ_FMT_BF16 || c->format == KVQ_FMT_TQ4) {
     if (c->head_dim != 256 || group > 8) return KVQ_ERR_UNSUPPORTED;
   } else {
     if (c->head_dim != 512 || c->rope_dim != 64 || Hq % 16 != 0) return KVQ_ERR_UNSUPPORTED;
@@ -147,6 +153,8 @@ size_t kvq_plane_bytes(const kvq_cache* c, int32_t plane) {
       return (plane == 0 || plane == 2) ? rows * (c->head_dim / 2) : rows * (c->head_dim / 32) * 2;
     case KVQ_FMT_BF16:
       return (plane == 0 || plane == 2) ? rows * c->head_dim * 2 : 0;
+    case KVQ_FMT_TQ4:
+      return (plane == 0 || plane == 2) ? rows * (c->head_dim / 2) : rows * 2;
     case KVQ_FMT_FP8_ROW:
       if (plane == 0) return rows * c->head_dim;
       if (plane == 2) return rows * c->rope_dim;
@@ -168,8 +176,24 @@ int32_t kvq_store(const kvq_cache* cache, const void* k, const void* v, int32_t 
   } else if (!v) {
     return KVQ_ERR_INVALID_ARG;
   }
-  cudaError_t e = launch_store(*cache, k, v, dtype, n_tok, d_slot_mapping, d_status,
-                               static_cast<cudaStream_t>(stream));
+  cudaError_t e = cache->format == KVQ_FMT_TQ4
+                      ? launch_store_tq4(*cache, k, v, dtype, n_tok, d_slot_mapping, d_status,
+                                         static_cast<cudaStream_t>(stream))
+                      : launch_store(*cache, k, v, dtype, n_tok, d_slot_mapping, d_status,
+                                     static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? KVQ_OK : cuda_fail(e);
+}
+
+int32_t kvq_tq4_rotate(const kvq_cache* cache, const void* x, int32_t dtype, float* y, int64_t rows,
+                       int32_t inverse, void* stream) {
+  int32_t st = check_cache(cache);
+  if (st != KVQ_OK) return st;
+  if (cache->format != KVQ_FMT_TQ4) return KVQ_ERR_UNSUPPORTED;
+  if (rows < 0 || (dtype != KVQ_DT_F32 && dtype != KVQ_DT_BF16)) return KVQ_ERR_INVALID_ARG;
+  if (rows == 0) return KVQ_OK;
+  if (!x || !y) return KVQ_ERR_INVALID_ARG;
+  if (x == static_cast<const void*>(y) && dtype != KVQ_DT_F32) return KVQ_ERR_INVALID_ARG;
+  cudaError_t e = launch_tq4_rotate(*cache, x, dtype, y, rows, inverse ? 1 : 0, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? KVQ_OK : cuda_fail(e);
 }
 
@@ -247,6 +271,7 @@ static int32_t decode_attn_impl(const kvq_cache* cache, const float* q, const vo
     a.q_raw = q_raw;
     a.q_dtype = q_dtype;
     a.q_rotate = cache->format == KVQ_FMT_Q4_HAD32 ? 1 : 0;
+    a.tq = cache->format == KVQ_FMT_TQ4 ? 1 : 0;
     a.ws_m = reinterpret_cast<float*>(ws + w.m_off);
     a.ws_z = reinterpret_cast<float*>(ws + w.z_off);
     a.ws_acc = reinterpret_cast<float*>(ws + w.acc_off);
@@ -307,7 +332,7 @@ int32_t kvq_merge(const kvq_cache* cache, const void* workspace, size_t ws_bytes
   if (n_sel < 0 || n_sel > 4096) return KVQ_ERR_INVALID_ARG;
   st = check_decode_shape(cache, num_seqs, num_q_heads, d_seq_lens, max_seq_len, n_sel > 0, n_sel);
   if (st != KVQ_OK) return st;
-  if (rotate_back && cache->format != KVQ_FMT_Q4_HAD32) return KVQ_ERR_INVALID_ARG;
+  if (rotate_back && cache->format != KVQ_FMT_Q4_HAD32 && cache->format != KVQ_FMT_TQ4) return KVQ_ERR_INVALID_ARG;
   if (num_seqs == 0) return KVQ_OK;
   if (!workspace || !out || !aligned16(workspace)) return KVQ_ERR_INVALID_ARG;
   const WsLayout w = ws_layout(cache, num_seqs, num_q_heads, max_seq_len, n_sel);
@@ -315,8 +340,11 @@ int32_t kvq_merge(const kvq_cache* cache, const void* workspace, size_t ws_bytes
   const uint8_t* ws = static_cast<const uint8_t*>(workspace);
   MergeArgs a{reinterpret_cast<const float*>(ws + w.m_off), reinterpret_cast<const float*>(ws + w.z_off),
               reinterpret_cast<const float*>(ws + w.acc_off), w.P, num_q_heads, value_width(cache), d_seq_lens,
-              max_seq_len, n_sel, rotate_back ? 1 : 0, out};
+              max_seq_len, n_sel, rotate_back && cache->format == KVQ_FMT_Q4_HAD32 ? 1 : 0, out};
   cudaError_t e = launch_merge(a, num_seqs, static_cast<cudaStream_t>(stream));
+  if (e == cudaSuccess && rotate_back && cache->format == KVQ_FMT_TQ4)  // the row transform needs the whole row
+    e = launch_tq4_rotate(*cache, out, KVQ_DT_F32, out, static_cast<int64_t>(num_seqs) * num_q_heads, 1,
+                          static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? KVQ_OK : cuda_fail(e);
 }
 

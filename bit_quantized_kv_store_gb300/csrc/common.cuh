@@ -140,6 +140,12 @@ __device__ __forceinline__ uint4 lds128(const void* p) {
   return v;
 }
 
+// Element i of an activation tensor of dtype KVQ_DT_F32 or KVQ_DT_BF16, as fp32.
+__device__ __forceinline__ float load_act(const void* p, int dtype, int64_t i) {
+  if (dtype == KVQ_DT_F32) return static_cast<const float*>(p)[i];
+  return __bfloat162float(static_cast<const __nv_bfloat16*>(p)[i]);
+}
+
 // ---------------------------------------------------------------- register ops
 
 __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {

@@ -212,6 +212,63 @@ __device__ __forceinline__ void q4_query_prep(const DecodeArgs& a, int b, int kv
   __syncthreads();
 }
 
+// ---------------------------------------------------------------- TQ4 rows
+// A TQ4 code nibble is sign (bit 3) and magnitude index m (bits 0-2) of the
+// level +-M_m of the 16-level Lloyd-Max codebook; the fp16 bits of M_0..M_7 are
+// 0x301c 0x3635 0x3941 0x3b8a 0x3d06 0x3e79 0x4023 0x4177.  Byte tables of
+// their low and high bytes, for prmt lookups indexed by m.
+constexpr uint32_t kTqLo0 = 0x8a41351cu, kTqLo1 = 0x77237906u;  // low bytes of M_0..M_3, M_4..M_7
+constexpr uint32_t kTqHi0 = 0x3b393630u, kTqHi1 = 0x41403e3du;  // high bytes
+
+// The 8 codes of w (element 2b in the low nibble of byte b) -> 4 f16 pairs
+// (elements 0,1 | 2,3 | 4,5 | 6,7), exactly the codebook levels.
+__device__ __forceinline__ uint4 tq4_levels8(uint32_t w) {
+  const uint32_t m0 = w & 0x7777u, m1 = (w >> 16) & 0x7777u;  // magnitudes of codes 0-3, 4-7 as selectors
+  const uint32_t lo0 = prmt(kTqLo0, kTqLo1, m0), hi0 = prmt(kTqHi0, kTqHi1, m0);
+  const uint32_t lo1 = prmt(kTqLo0, kTqLo1, m1), hi1 = prmt(kTqHi0, kTqHi1, m1);
+  uint4 r;
+  r.x = prmt(lo0, hi0, 0x5140u);  // (low, high) bytes of codes 0, 1
+  r.y = prmt(lo0, hi0, 0x7362u);
+  r.z = prmt(lo1, hi1, 0x5140u);
+  r.w = prmt(lo1, hi1, 0x7362u);
+  // sign bits: code i's bit 3 -> bit 15 (even i) or bit 31 (odd i) of its pair
+  const uint32_t sg = w & 0x88888888u, sg4 = sg << 4;
+  r.x ^= prmt(sg, sg4, 0x0040u) & 0x80008000u;
+  r.y ^= prmt(sg, sg4, 0x1050u) & 0x80008000u;
+  r.z ^= prmt(sg, sg4, 0x2060u) & 0x80008000u;
+  r.w ^= prmt(sg, sg4, 0x3070u) & 0x80008000u;
+  return r;
+}
+
+__device__ __forceinline__ float lds16h(uint32_t addr) {
+  unsigned short v;
+  asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(addr));
+  return __half2float(__ushort_as_half(v));
+}
+
+// TQ4 query fragments of one column tile: column g faces `qrow`; group G's
+// fragment of lane (g, t) holds q[32G + 8t .. 8t + 7] (pairs in order), split
+// into f16 high and low parts.  No bias: the levels enter signed.
+template <int kWarps>
+__device__ __forceinline__ void tq4_frag_prep(const float* qrow, bool live, float qscale, int warp, int lane,
+                                              uint4 (*qf)[2][32]) {
+  const int t = lane & 3;
+  const float s = live ? qscale : 0.f;
+#pragma unroll
+  for (int k = 0; k < kQ4NG / kWarps; ++k) {
+    const int G = warp + kWarps * k;
+    const float4 u0 = *reinterpret_cast<const float4*>(qrow + 32 * G + 8 * t);
+    const float4 u1 = *reinterpret_cast<const float4*>(qrow + 32 * G + 8 * t + 4);
+    uint4 hi, lo;
+    split_f16(u0.x * s, u0.y * s, hi.x, lo.x);
+    split_f16(u0.z * s, u0.w * s, hi.y, lo.y);
+    split_f16(u1.x * s, u1.y * s, hi.z, lo.z);
+    split_f16(u1.z * s, u1.w * s, hi.w, lo.w);
+    qf[G][0][lane] = hi;
+    qf[G][1][lane] = lo;
+  }
+}
+
 namespace q4r {
 
 constexpr int kQ4Warps = 4;                       // warps per CTA = value group pairs in P.V
@@ -250,7 +307,7 @@ __device__ __forceinline__ void bar_sync_cta() { asm volatile("bar.sync 1, %0;" 
 // Issue the copies of one 16-key tile of one plane (codes + scales).  Returns
 // false if a page or a selected index is invalid (the tile then counts as
 // poisoned; the barrier still gets this arrival so that nobody waits on it).
-template <bool GATHER>
+template <bool GATHER, bool TQ = false>
 __device__ __forceinline__ bool q4_issue_plane(const DecodeArgs& a, int b, int kvh, int key0, int nvalid,
                                                int32_t row0, const CUtensorMap* map, const void* codes,
                                                const void* scales, uint8_t* dc, uint16_t* ds, uint64_t* bar) {
@@ -261,9 +318,11 @@ __device__ __forceinline__ bool q4_issue_plane(const DecodeArgs& a, int b, int k
       mbar_arrive(bar);
       return false;
     }
-    mbar_arrive_expect_tx(bar, kQ4TileBytes + kQ4ScaleBytes);
+    // scales: 8 fp16 per row (Q4), or one (TQ4: 16 rows = 32 bytes)
+    constexpr int kScaleBytes = TQ ? 32 : kQ4ScaleBytes;
+    mbar_arrive_expect_tx(bar, kQ4TileBytes + kScaleBytes);
     tma_rows_2d(dc, map, row0, bar);
-    bulk_g2s(ds, static_cast<const uint16_t*>(scales) + (int64_t)row0 * 8, kQ4ScaleBytes, bar);
+    bulk_g2s(ds, static_cast<const uint16_t*>(scales) + (int64_t)row0 * (TQ ? 1 : 8), kScaleBytes, bar);
     return true;
   } else {
     const int32_t T = a.seq_lens[b];
@@ -296,7 +355,7 @@ __device__ __forceinline__ bool q4_issue_plane(const DecodeArgs& a, int b, int k
 // The calling warp's kQ4TPW tiles of round `rd` of one plane into dc[u], ds[u]
 // (lane 0 issues; every lane takes part in the row shuffles).  A tile past the
 // partition still arrives on `bar`.  Returns true (lane 0) for a bad page/index.
-template <bool GATHER>
+template <bool GATHER, bool TQ = false>
 __device__ __forceinline__ bool q4_issue_own(const DecodeArgs& a, int b, int kvh, int k0, int k1, int rd, int warp,
                                              int lane, int32_t tile_row, const CUtensorMap* map, const void* codes,
                                              const void* scales, uint8_t (*dc)[q4_tile_bytes<GATHER>()],
@@ -313,8 +372,8 @@ __device__ __forceinline__ bool q4_issue_own(const DecodeArgs& a, int b, int kvh
       const int key0 = k0 + 16 * (tile0 + u);
       if (key0 >= k1) {
         mbar_arrive(bar);
-      } else if (!q4_issue_plane<GATHER>(a, b, kvh, key0, min(16, k1 - key0), rows[u], map, codes, scales, dc[u],
-                                         ds[u], bar)) {
+      } else if (!q4_issue_plane<GATHER, TQ>(a, b, kvh, key0, min(16, k1 - key0), rows[u], map, codes, scales,
+                                             dc[u], ds[u], bar)) {
         bad = true;
       }
     }
@@ -329,11 +388,12 @@ __device__ __forceinline__ bool q4_issue_own(const DecodeArgs& a, int b, int kvh
 // sequence, row-major: the rows share the block table and so every key, whose
 // codes are then converted once for all of them; each row keeps its own causal
 // end (its length), its own softmax state and its own partials.
-template <bool GATHER, int NT, bool WIN>
+template <bool GATHER, int NT, bool WIN, bool TQ = false>
 __global__ void __launch_bounds__(kQ4Warps * 32, q4_min_blocks(NT))
     decode_q4_round_kernel(const __grid_constant__ DecodeArgs a) {
   static_assert(!(WIN && GATHER), "decode windows read dense prefixes");
   static_assert(WIN || NT == 1, "one sequence's group fills one column tile");
+  static_assert(!TQ || (!GATHER && !WIN), "TQ4 rows: dense single-sequence decode");
   extern __shared__ uint8_t smem_raw[];
   // 1024-byte alignment for the swizzled tiles (the launch adds 1 KB of slack)
   Q4Smem<NT, GATHER>& sm =
@@ -428,7 +488,7 @@ __global__ void __launch_bounds__(kQ4Warps * 32, q4_min_blocks(NT))
   __syncthreads();  // the mbarriers are initialised
 
   const kvq_cache& c = a.c;
-  bool poisoned = q4_issue_own<GATHER>(a, b, kvh, k0, k1, 0, warp, lane, tile_row, &a.tm_k, c.k, c.k_scale,
+  bool poisoned = q4_issue_own<GATHER, TQ>(a, b, kvh, k0, k1, 0, warp, lane, tile_row, &a.tm_k, c.k, c.k_scale,
                                        sm.kc[warp], sm.ks[warp], &sm.kbar[warp]);
 
   if constexpr (WIN) {
@@ -440,11 +500,16 @@ __global__ void __launch_bounds__(kQ4Warps * 32, q4_min_blocks(NT))
       q4_frag_prep<kQ4Warps>(qrow, live, a.qscale, warp, lane, sm.qf[nt], sm.qb[nt]);
     }
     __syncthreads();
+  } else if constexpr (TQ) {
+    const bool live = g < a.group;
+    tq4_frag_prep<kQ4Warps>(a.q + ((int64_t)b * a.Hq + kvh * a.group + (live ? g : 0)) * kQ4D, live, a.qscale, warp,
+                            lane, sm.qf[0]);
+    __syncthreads();
   } else {
     q4_query_prep<kQ4Warps>(a, b, kvh, warp, lane, reinterpret_cast<float*>(&sm.vc[0][0]), sm.qf[0], sm.qb[0]);
   }
   // V of round 0: vc[0..3] held the rotated queries until the prologue's last barrier
-  poisoned |= q4_issue_own<GATHER>(a, b, kvh, k0, k1, 0, warp, lane, tile_row, &a.tm_v, c.v, c.v_scale,
+  poisoned |= q4_issue_own<GATHER, TQ>(a, b, kvh, k0, k1, 0, warp, lane, tile_row, &a.tm_v, c.v, c.v_scale,
                                    &sm.vc[kQ4TPW * warp], &sm.vs[kQ4TPW * warp], &sm.vfull);
   const uint32_t qf_addr = smem_u32(&sm.qf[0][0][0][lane]);
   const uint32_t qb_addr = smem_u32(&sm.qb[0][0][t]);
@@ -485,6 +550,7 @@ __global__ void __launch_bounds__(kQ4Warps * 32, q4_min_blocks(NT))
   const uint32_t vc_base = smem_u32(&sm.vc[0][0]);
   const uint32_t vs_base = smem_u32(&sm.vs[0][0]) + 4 * warp;
   const uint32_t pb_addr = smem_u32(&sm.pb[0][0][lane]);
+  const uint32_t vs_tq = smem_u32(&sm.vs[0][0]);  // TQ4: one fp16 scale per key
 
   for (int r = 0; r < nrounds; ++r) {
     const uint32_t par = r & 1;
@@ -503,6 +569,42 @@ __global__ void __launch_bounds__(kQ4Warps * 32, q4_min_blocks(NT))
       for (int u = 0; u < kQ4TPW; ++u)
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) S[u][nt][0] = S[u][nt][1] = S[u][nt][2] = S[u][nt][3] = 0.f;
+      if constexpr (TQ) {
+        // TQ4: the levels enter signed and exact; one accumulator chain over
+        // all 8 groups, then the row's scale (keys g, g + 8).
+#pragma unroll
+        for (int w = 0; w < kQ4NG / 2; ++w) {
+          uint4 kw[kQ4TPW];
+          const uint32_t okl = chunk_off(2 * w);
+#pragma unroll
+          for (int u = 0; u < kQ4TPW; ++u) kw[u] = ldsm_x4(kc_base + u * kTile + okl);
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const int G = 2 * w + e;
+            const uint4 qh = lds128a(qf_addr + G * 1024);
+            const uint4 ql = lds128a(qf_addr + G * 1024 + 512);
+#pragma unroll
+            for (int u = 0; u < kQ4TPW; ++u) {
+              const uint4 A = tq4_levels8(e ? kw[u].z : kw[u].x);  // key g: elements 8t .. 8t+7
+              const uint4 B = tq4_levels8(e ? kw[u].w : kw[u].y);  // key g + 8
+              float (&part)[4] = S[u][0];
+              mma_f16(part, A.x, B.x, A.y, B.y, qh.x, qh.y);
+              mma_f16(part, A.z, B.z, A.w, B.w, qh.z, qh.w);
+              mma_f16(part, A.x, B.x, A.y, B.y, ql.x, ql.y);
+              mma_f16(part, A.z, B.z, A.w, B.w, ql.z, ql.w);
+            }
+          }
+        }
+#pragma unroll
+        for (int u = 0; u < kQ4TPW; ++u) {
+          const uint32_t sb = ks_base + u * kQ4ScaleBytes;
+          const float sa = lds16h(sb + 2 * g), sc = lds16h(sb + 2 * (g + 8));
+          S[u][0][0] *= sa;
+          S[u][0][1] *= sa;
+          S[u][0][2] *= sc;
+          S[u][0][3] *= sc;
+        }
+      } else {
 #pragma unroll
       for (int w = 0; w < kQ4NG / 2; ++w) {  // group pair (2w, 2w+1): one word of each fragment row
         // kw[u]: codes 8t .. 8t+7 of group 2w (.x key g, .y key g+8) and of group 2w+1 (.z, .w)
@@ -554,6 +656,7 @@ __global__ void __launch_bounds__(kQ4Warps * 32, q4_min_blocks(NT))
           }
         }
       }
+      }
       // (Dead columns have a zero query: their scores are 0, finite, and never
       // leave the kernel, so they need no mask.)
 #pragma unroll
@@ -581,7 +684,7 @@ __global__ void __launch_bounds__(kQ4Warps * 32, q4_min_blocks(NT))
       // The K tiles are consumed: refill them with round r + 1.
       __syncwarp();
       if (r + 1 < nrounds)
-        poisoned |= q4_issue_own<GATHER>(a, b, kvh, k0, k1, r + 1, warp, lane, tile_row, &a.tm_k, c.k, c.k_scale,
+        poisoned |= q4_issue_own<GATHER, TQ>(a, b, kvh, k0, k1, r + 1, warp, lane, tile_row, &a.tm_k, c.k, c.k_scale,
                                          sm.kc[warp], sm.ks[warp], &sm.kbar[warp]);
     }
 
@@ -668,6 +771,39 @@ __global__ void __launch_bounds__(kQ4Warps * 32, q4_min_blocks(NT))
     // converted, so they add exactly nothing.  Only a tail round checks.
     auto pv_round = [&](auto tail_tag) {
       constexpr bool kTail = decltype(tail_tag)::value;
+      if constexpr (TQ) {
+#pragma unroll
+        for (int j = 0; j < kQ4RoundTiles; ++j) {
+          const uint2 pp = lds64a(pb_addr + j * 256);
+          // V scales of keys (2t, 2t+1) and (2t+8, 2t+9), one per row
+          const uint32_t sb = vs_tq + j * kQ4ScaleBytes;
+          uint32_t slo = lds32a(sb + 4 * t), shi = lds32a(sb + 16 + 4 * t);
+          if constexpr (kTail) {
+            const int nvalid = k1 - (k0 + 16 * (kQ4RoundTiles * r + j));
+            if (nvalid < 16) {  // CTA-uniform
+              if (2 * t >= nvalid) slo &= 0xFFFF0000u;
+              if (2 * t + 1 >= nvalid) slo &= 0x0000FFFFu;
+              if (2 * t + 8 >= nvalid) shi &= 0xFFFF0000u;
+              if (2 * t + 9 >= nvalid) shi &= 0x0000FFFFu;
+            }
+          }
+          const uint32_t b0 = h2_as_u32(__hmul2(u32_as_h2(pp.x), u32_as_h2(slo)));
+          const uint32_t b1 = h2_as_u32(__hmul2(u32_as_h2(pp.y), u32_as_h2(shi)));
+          // words of keys g, g + 8 for groups 2w, 2w + 1; levels by key, then
+          // transposed (movmatrix) to pairs of keys per value dim
+          const uint4 vw = ldsm_x4(vc_base + j * kTile + off_vl);
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const uint4 A = tq4_levels8(e ? vw.z : vw.x);  // key g, elements 8t .. 8t+7
+            const uint4 B = tq4_levels8(e ? vw.w : vw.y);  // key g + 8
+            // rows g / g + 8 of the first MMA: dims 8(g/2) + (g&1) + 0 / + 2; second: + 4 / + 6
+            mma_f16(acc[e][0][0], movmatrix_trans(A.x), movmatrix_trans(A.y), movmatrix_trans(B.x),
+                    movmatrix_trans(B.y), b0, b1);
+            mma_f16(acc[e][1][0], movmatrix_trans(A.z), movmatrix_trans(A.w), movmatrix_trans(B.z),
+                    movmatrix_trans(B.w), b0, b1);
+          }
+        }
+      } else {
 #pragma unroll
       for (int j = 0; j < kQ4RoundTiles; ++j) {
         uint2 pp[NT];
@@ -713,6 +849,7 @@ __global__ void __launch_bounds__(kQ4Warps * 32, q4_min_blocks(NT))
           }
         }
       }
+      }
     };
     if (tail_round)
       pv_round(std::true_type{});
@@ -725,7 +862,7 @@ __global__ void __launch_bounds__(kQ4Warps * 32, q4_min_blocks(NT))
     if (lane == 0) mbar_arrive(&sm.vempty);
     if (r + 1 < nrounds) {
       if (!timed_out && !__all_sync(0xffffffffu, mbar_wait_bounded(&sm.vempty, par))) timed_out = true;
-      poisoned |= q4_issue_own<GATHER>(a, b, kvh, k0, k1, r + 1, warp, lane, tile_row, &a.tm_v, c.v, c.v_scale,
+      poisoned |= q4_issue_own<GATHER, TQ>(a, b, kvh, k0, k1, r + 1, warp, lane, tile_row, &a.tm_v, c.v, c.v_scale,
                                        &sm.vc[kQ4TPW * warp], &sm.vs[kQ4TPW * warp], &sm.vfull);
     }
   }
@@ -759,12 +896,26 @@ __global__ void __launch_bounds__(kQ4Warps * 32, q4_min_blocks(NT))
     }
 #pragma unroll
     for (int e = 0; e < 2; ++e) {
-      const int d = 32 * (2 * warp + e) + 4 * g;
-      float4 o0 = make_float4(acc[e][0][nt][0], acc[e][1][nt][0], acc[e][0][nt][2], acc[e][1][nt][2]);
-      float4 o1 = make_float4(acc[e][0][nt][1], acc[e][1][nt][1], acc[e][0][nt][3], acc[e][1][nt][3]);
-      if (bad) o0 = o1 = make_float4(NAN, NAN, NAN, NAN);
-      if (live[0]) *reinterpret_cast<float4*>(a.ws_acc + pi[0] * kQ4D + d) = o0;
-      if (live[1]) *reinterpret_cast<float4*>(a.ws_acc + pi[1] * kQ4D + d) = o1;
+      if constexpr (TQ) {
+        // accumulator rows g, g + 8 of MMA j hold dims d0 + 4j + 0, + 2
+        const int d0 = 32 * (2 * warp + e) + 8 * (g >> 1) + (g & 1);
+#pragma unroll
+        for (int cc = 0; cc < 2; ++cc) {
+          if (!live[cc]) continue;
+          float* o = a.ws_acc + pi[cc] * kQ4D + d0;
+          o[0] = bad ? NAN : acc[e][0][nt][cc];
+          o[2] = bad ? NAN : acc[e][0][nt][2 + cc];
+          o[4] = bad ? NAN : acc[e][1][nt][cc];
+          o[6] = bad ? NAN : acc[e][1][nt][2 + cc];
+        }
+      } else {
+        const int d = 32 * (2 * warp + e) + 4 * g;
+        float4 o0 = make_float4(acc[e][0][nt][0], acc[e][1][nt][0], acc[e][0][nt][2], acc[e][1][nt][2]);
+        float4 o1 = make_float4(acc[e][0][nt][1], acc[e][1][nt][1], acc[e][0][nt][3], acc[e][1][nt][3]);
+        if (bad) o0 = o1 = make_float4(NAN, NAN, NAN, NAN);
+        if (live[0]) *reinterpret_cast<float4*>(a.ws_acc + pi[0] * kQ4D + d) = o0;
+        if (live[1]) *reinterpret_cast<float4*>(a.ws_acc + pi[1] * kQ4D + d) = o1;
+      }
     }
     if (warp == 0 && g == 0) {
       float Z[2] = {0.f, 0.f};
@@ -785,10 +936,10 @@ __global__ void __launch_bounds__(kQ4Warps * 32, q4_min_blocks(NT))
   pdl_trigger();  // after this CTA's last write
 }
 
-template <bool GATHER, int NT, bool WIN>
+template <bool GATHER, int NT, bool WIN, bool TQ = false>
 cudaError_t launch_round(const DecodeArgs& a, dim3 grid, cudaStream_t s) {
   const size_t smem = sizeof(Q4Smem<NT, GATHER>) + 1024;  // + slack for the 1024-byte alignment
-  auto kern = decode_q4_round_kernel<GATHER, NT, WIN>;
+  auto kern = decode_q4_round_kernel<GATHER, NT, WIN, TQ>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   e = launch_pdl(kern, grid, dim3(kQ4Warps * 32), smem, s, a);
@@ -802,8 +953,10 @@ cudaError_t launch_decode_q4(const DecodeArgs& a, int B, cudaStream_t s) {
   using namespace q4r;
   if (a.nrows <= 0) {
     const dim3 grid(a.P, a.c.num_kv_heads, B);
+    if (a.tq) return a.sel ? cudaErrorInvalidValue : launch_round<false, 1, false, true>(a, grid, s);
     return a.sel ? launch_round<true, 1, false>(a, grid, s) : launch_round<false, 1, false>(a, grid, s);
   }
+  if (a.tq) return cudaErrorInvalidValue;
   // Decode window: the rows are cut into the fewest even slices whose
   // (row, head) columns fit kQ4MaxColTiles tiles of 8.
   const int rmax = 8 * kQ4MaxColTiles / a.group;  // >= 4 (group <= 8)

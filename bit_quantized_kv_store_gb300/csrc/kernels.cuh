@@ -40,6 +40,7 @@ struct DecodeArgs {
   int bt_stride;
   int nrows;
   int rows_per_cta;
+  int tq;  // 4-bit decode: 1 for TQ4 rows (codebook levels, one scale per row)
 };
 
 // Log-sum-exp merge of the partials (merge.cu).
@@ -89,6 +90,11 @@ cudaError_t launch_store_rotate(const kvq_cache& c, const void* k, const void* v
                                 const int32_t* slots, int32_t* status, const void* q, int q_dtype, float* q_out,
                                 int64_t q_rows, int q_head_dim, cudaStream_t s);
 cudaError_t launch_decode_q4(const DecodeArgs& a, int B, cudaStream_t s);
+// TQ4 rows (tq4.cu): store, and the signed row rotation (inverse = 1: outputs back).
+cudaError_t launch_store_tq4(const kvq_cache& c, const void* k, const void* v, int dtype, int64_t n_tok,
+                             const int32_t* slots, int32_t* status, cudaStream_t s);
+cudaError_t launch_tq4_rotate(const kvq_cache& c, const void* x, int dtype, float* y, int64_t rows, int inverse,
+                              cudaStream_t s);
 // fp8 latent rows on the tensor cores (decode_fp8.cu); tm_k / tm_v map the latent
 // and rope code planes.
 cudaError_t launch_decode_fp8(const DecodeArgs& a, int B, cudaStream_t s);

@@ -18,11 +18,6 @@
 
 namespace kvq {
 
-__device__ __forceinline__ float load_act(const void* p, int dtype, int64_t i) {
-  if (dtype == KVQ_DT_F32) return static_cast<const float*>(p)[i];
-  return __bfloat162float(static_cast<const __nv_bfloat16*>(p)[i]);
-}
-
 // One warp per (token, KV head, K|V) row of D = 32*NG values.
 // Lane i handles element 32G + i of every group G.  ROT = false: the unrotated
 // Q4_0 format (the values as given).

@@ -82,6 +82,25 @@ typedef enum { KVQ_DT_F32 = 0, KVQ_DT_BF16 = 1 } kvq_dtype;
  *   used as given (kvq_rotate_query is not needed; kvq_decode_attn_unrotated and
  *   kvq_prefill_attn skip their rotations) and nothing is rotated back
  *   (kvq_merge with rotate_back = 0).
+ * KVQ_FMT_TQ4 ([P3] "KV cache quantization: fp8 (KV8) + 4-bit TurboQuant", PR
+ *   body, "Why rotated-int4": a randomized-Hadamard rotation and a fixed 16-level
+ *   Lloyd-Max codebook for N(0,1) scaled by radius / sqrt(n), one scale per row):
+ *   a row of D values (D = 64, 128 or 256) is signed by the cache's sign mask
+ *   (bit i of signs[i / 32] set: element i negated), rotated by the D-point
+ *   Walsh-Hadamard butterfly (stages h = 1 .. D/2, (a, b) -> (a + b, a - b),
+ *   fp32) and multiplied by fp32(1/sqrt(D)); ss = the fp32 sum of the squares by
+ *   the pairwise tree (stage h adds element i + h into i for i a multiple of
+ *   2h); scale = fp16_rne(sqrtf(ss * (1/D))) (saturated to 65504); with
+ *   v = y / scale (fp32 division) the code is 8 * [v < 0] + m, m = the number of
+ *   midpoints (M_k + M_{k+1}) / 2, k < 7, below |v|, where M_0..M_7 =
+ *   0.12841796875, 0.387939453125, 0.65673828125, 0.9423828125, 1.255859375,
+ *   1.6181640625, 2.068359375, 2.732421875 (the Lloyd-Max levels rounded to
+ *   fp16); scale 0 stores code 0.  value = (code & 8 ? -1 : 1) * M_{code & 7} *
+ *   scale, in the rotated space.  Codes plane as for KVQ_FMT_Q4_HAD32 (element
+ *   2b of the row in the low nibble of byte b); scale plane: one fp16 per row.
+ *   For D = 256 a row is 128 + 2 = 130 bytes.  Queries are rotated by the same
+ *   signed transform (kvq_tq4_rotate) and outputs rotated back by its inverse
+ *   (kvq_merge with rotate_back, or kvq_tq4_rotate with inverse = 1).
  * KVQ_FMT_BF16: unrotated bf16 rows of D values (the uncompressed comparison).
  * KVQ_FMT_FP8_ROW ([P3] KV8 base commit): one latent row per position (num_kv_heads
  *   must be 1): head_dim latent values ("Lc") and rope_dim rope values ("Rc"), each
@@ -93,7 +112,13 @@ typedef enum { KVQ_DT_F32 = 0, KVQ_DT_BF16 = 1 } kvq_dtype;
  * Row index of (page, kv_head, slot) in every plane:
  *   r = (page * num_kv_heads + kv_head) * page_size + slot.
  * A token's slot number is page * page_size + slot; block tables list page ids. */
-typedef enum { KVQ_FMT_Q4_HAD32 = 0, KVQ_FMT_BF16 = 1, KVQ_FMT_FP8_ROW = 2, KVQ_FMT_Q4_0 = 3 } kvq_format;
+typedef enum {
+  KVQ_FMT_Q4_HAD32 = 0,
+  KVQ_FMT_BF16 = 1,
+  KVQ_FMT_FP8_ROW = 2,
+  KVQ_FMT_Q4_0 = 3,
+  KVQ_FMT_TQ4 = 4
+} kvq_format;
 
 typedef struct kvq_cache {
   int32_t format;       /* kvq_format */
@@ -106,6 +131,7 @@ typedef struct kvq_cache {
   void* k_scale;        /* Q4: K scale plane (fp16); BF16: unused; FP8_ROW: Lc scales [rows] f32 */
   void* v;              /* Q4: V codes plane; BF16: V plane; FP8_ROW: Rc codes [rows][rope_dim] */
   void* v_scale;        /* Q4: V scale plane; BF16: unused; FP8_ROW: Rc scales [rows] f32 */
+  const void* signs;    /* TQ4: device uint32 [head_dim / 32], the rotation's sign mask; otherwise unused */
 } kvq_cache;
 
 /* Version of the ABI (major * 10000 + minor * 100 + patch). */
@@ -141,6 +167,16 @@ int32_t kvq_store(const kvq_cache* cache, const void* k, const void* v, int32_t 
 int32_t kvq_rotate_query(const void* x, int32_t dtype, float* y, int64_t rows, int32_t head_dim,
                          void* stream);
 
+/* kvq_tq4_rotate -- the TQ4 format's rotation of `rows` rows of head_dim values:
+ * inverse = 0: y = H (s * x) / sqrt(D) (queries into the cache's space);
+ * inverse = 1: y = s * (H x) / sqrt(D) (outputs back), s the cache's signs, H
+ * the D-point Walsh-Hadamard matrix ([P3] "Why rotated-int4": randomized
+ * Hadamard).  fp32 butterfly; x: device [rows, head_dim] of dtype; y: device
+ * fp32 [rows, head_dim], may equal x when dtype is F32.  KVQ_ERR_UNSUPPORTED for
+ * a cache of another format. */
+int32_t kvq_tq4_rotate(const kvq_cache* cache, const void* x, int32_t dtype, float* y, int64_t rows,
+                       int32_t inverse, void* stream);
+
 /* kvq_store_rotate -- kvq_store of n_tok new tokens and kvq_rotate_query of
  * q_rows query rows (of the cache's head_dim) in one launch.  A decode step's
  * two preparations are independent of each other ([P1] "What it is": pack the
@@ -172,13 +208,14 @@ size_t kvq_decode_workspace_size(const kvq_cache* cache, int32_t num_seqs, int32
  *   acc = sum_j 2^(s_j log2(e) - m) * value_j,   s_j = sm_scale * (q . key_j)
  * into the workspace.  Empty partitions get m = -inf, z = 0, acc = 0.
  *   q:  device fp32 [num_seqs, num_q_heads, key width]; Q4: already rotated
- *       (kvq_rotate_query); BF16 / FP8_ROW: as is.  Key width = head_dim
- *       (+ rope_dim for FP8_ROW).
+ *       (kvq_rotate_query); TQ4: already rotated (kvq_tq4_rotate); BF16 /
+ *       FP8_ROW: as is.  Key width = head_dim (+ rope_dim for FP8_ROW).
  *   d_seq_lens: device int32 [num_seqs], each in [0, max_seq_len].
  *   d_block_tables: device int32 [num_seqs, max_pages_per_seq].
  *   d_sel: NULL for dense attention, else device int32 [num_seqs, n_sel] absolute
  *       positions, each < seq_lens[b] (gather; n_sel <= 4096, [P3] split-T commit).
- *   Q4 / BF16 need num_q_heads / num_kv_heads <= 8 and head_dim == 256.
+ *   Q4 / TQ4 / BF16 need num_q_heads / num_kv_heads <= 8 and head_dim == 256
+ *   (TQ4: dense only, d_sel must be NULL).
  *   FP8_ROW needs head_dim == 512, rope_dim == 64 and num_q_heads % 16 == 0. */
 int32_t kvq_decode_attn(const kvq_cache* cache, const float* q, int32_t num_seqs, int32_t num_q_heads,
                         const int32_t* d_seq_lens, const int32_t* d_block_tables, int32_t max_pages_per_seq,
@@ -232,7 +269,9 @@ int32_t kvq_decode_attn_unrotated(const kvq_cache* cache, const void* q, int32_t
  * rotate the output back once"; [P3] split-T commit: merge kernel):
  *   M = max_p m_p,  Z = sum_p z_p 2^(m_p - M),  o = sum_p acc_p 2^(m_p - M) / Z,
  * taking partitions in ascending order in a fixed grouping (runs are
- * bit-reproducible), then out = blockdiag(H) o when rotate_back != 0 (Q4 only).
+ * bit-reproducible), then out = blockdiag(H) o when rotate_back != 0 (Q4_HAD32),
+ * or out = s * (H o) / sqrt(D) (TQ4: a second launch on out; the other formats
+ * take rotate_back = 0).
  * A sequence with no keys gives zeros.  Arguments as for kvq_decode_attn.
  * out: device fp32 [num_seqs, num_q_heads, value width]. */
 int32_t kvq_merge(const kvq_cache* cache, const void* workspace, size_t ws_bytes, int32_t num_seqs,

@@ -47,10 +47,13 @@ def assert_close(got, ref, tol=TOL, what=""):
     return err / scale
 
 
-def make_cache_pair(K, fmt, Hk, D, ps, n_pages, rope=0):
-    g = K.Cache(fmt, Hk, D, ps, n_pages, device=DEV, rope_dim=rope)
-    ofmt = {K.FMT_Q4_HAD32: O.Q4, K.FMT_BF16: O.BF16, K.FMT_FP8_ROW: O.FP8, K.FMT_Q4_0: O.Q4_0}[fmt]
-    o = O.Cache(ofmt, Hk, D, ps, n_pages, rope_dim=rope)
+def make_cache_pair(K, fmt, Hk, D, ps, n_pages, rope=0, sign_seed=0):
+    signs = synth.sign_mask(D, "tq4", sign_seed) if fmt == K.FMT_TQ4 else None
+    g = K.Cache(fmt, Hk, D, ps, n_pages, device=DEV, rope_dim=rope, signs=signs)
+    ofmt = {K.FMT_Q4_HAD32: O.Q4, K.FMT_BF16: O.BF16, K.FMT_FP8_ROW: O.FP8, K.FMT_Q4_0: O.Q4_0,
+            K.FMT_TQ4: O.TQ4}[fmt]
+    o = O.Cache(ofmt, Hk, D, ps, n_pages, rope_dim=rope,
+                signs=None if signs is None else signs.numpy().view(np.uint32))
     return g, o
 
 
@@ -131,6 +134,52 @@ def test_store_q4_0_exact_scale_block(K):
             got = [st[:, o_] & 15, st[:, o_] >> 4, st[:, o_ + 1] & 15, st[:, o_ + 1] >> 4]
             for j in range(4):
                 assert np.array_equal(got[j], c[:, 0, 32 * G + 4 * h + j] + 8)
+
+
+@pytest.mark.parametrize("D", [64, 128, 256])
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+def test_store_tq4_bit_exact(K, D, dtype):
+    """TQ4 rows: codes and the per-row fp16 scale bit-exact with the oracle
+    (rotation, sum of squares, codebook decisions in the same fp32 order)."""
+    Hk, ps, n_pages, T = 3, 32, 9, 250
+    k = synth.outlier_normal((T, Hk, D), 4, 20.0, "cpu", D, "tk").to(dtype)
+    v = synth.heavy_tailed((T, Hk, D), "cpu", D, "tv").to(dtype)
+    g, o = make_cache_pair(K, K.FMT_TQ4, Hk, D, ps, n_pages, sign_seed=D)
+    bt = synth.page_permutation(n_pages, D, "tpages").numpy().astype(np.int32)
+    fill_sequence(K, g, o, k, v, bt, T)
+    torch.cuda.synchronize()
+    check_planes_equal(g, o)
+
+
+def test_store_tq4_edge_rows(K):
+    """Zero rows (scale 0, code 0), tiny rows (scale underflows), huge rows (scale
+    saturates at 65504) and rows built on exact levels."""
+    D, Hk = 256, 1
+    rng = np.random.default_rng(9)
+    rows = [np.zeros(D, np.float32), np.full(D, 1e-9, np.float32),
+            (rng.standard_normal(D) * 1e7).astype(np.float32), (rng.standard_normal(D) * 1e-4).astype(np.float32)]
+    for _ in range(6):
+        rows.append(rng.standard_normal(D).astype(np.float32))
+    x = torch.from_numpy(np.stack(rows)[:, None, :])
+    g, o = make_cache_pair(K, K.FMT_TQ4, Hk, D, 16, 1, sign_seed=5)
+    fill_sequence(K, g, o, x, x, np.array([0], np.int32), x.shape[0])
+    torch.cuda.synchronize()
+    check_planes_equal(g, o)
+    assert bits_u16(g.k_scale)[0, 0, 0] == 0 and np.all(g.k[0, 0, 0].cpu().numpy() == 0)
+    assert bits_u16(g.k_scale)[0, 0, 2] == 0x7BFF
+
+
+@pytest.mark.parametrize("inverse", [False, True])
+def test_tq4_rotate_matches_the_definition(K, inverse):
+    D = 256
+    signs = synth.sign_mask(D, "rot")
+    c = K.Cache(K.FMT_TQ4, 1, D, 16, 1, device=DEV, signs=signs)
+    x = synth.heavy_tailed((37, D), "cpu", "rotx", dtype=torch.float32)
+    y = K.tq4_rotate(c, x.to(DEV), inverse=inverse).cpu().numpy()
+    s = signs.numpy().view(np.uint32)
+    for r in range(x.shape[0]):
+        ref = O.tq4_rotate_f64(x[r].numpy(), s, inverse=inverse)
+        assert np.abs(y[r] - ref).max() <= 1e-6 * np.abs(ref).max()
 
 
 def test_store_q4_exact_scale_and_edge_rows(K):
@@ -254,7 +303,7 @@ def decode_case(K, lens, Hk=4, Hq=24, D=256, ps=16, fmt=None, seed=0, dtype=torc
     for b, npg in enumerate(pages_per):
         bt[b, :npg] = perm[off:off + npg]
         off += npg
-    g, o = make_cache_pair(K, fmt, Hk, D, ps, n_pages)
+    g, o = make_cache_pair(K, fmt, Hk, D, ps, n_pages, sign_seed=seed)
     for b, L in enumerate(lens):
         if L == 0:
             continue
@@ -469,6 +518,41 @@ def test_decode_window_rows_in_any_order_and_bad_row(K):
         else:
             assert K.read_status(ws) & K.DEV_BAD_LENGTH
             assert np.isnan(out[bad]).all()
+
+
+@pytest.mark.parametrize("T", [1, 15, 17, 129, 511, 513, 4097])
+def test_decode_tq4_lengths(K, T):
+    """TQ4 decode (query rotation, split-T partials with the codebook levels,
+    merge and the inverse rotation) against the oracle."""
+    g, o, bt, q, ml = decode_case(K, [T], fmt=K.FMT_TQ4, seed=500 + T)
+    out, _ = run_decode(K, g, bt, q, [T], ml, 1 / 16)
+    ref = O.decode(o, to_np_in(q), [T], bt, 1 / 16)
+    assert_close(out[0], ref[0], what=f"TQ4 T={T}")
+
+
+@pytest.mark.parametrize("Hk,Hq", [(1, 8), (3, 21), (2, 2)])
+def test_decode_tq4_gqa_batch(K, Hk, Hq):
+    lens = [700, 45, 1100]
+    g, o, bt, q, ml = decode_case(K, lens, Hk=Hk, Hq=Hq, fmt=K.FMT_TQ4, seed=600 + Hq)
+    out, _ = run_decode(K, g, bt, q, lens, ml, 0.07)
+    ref = O.decode(o, to_np_in(q), lens, bt, 0.07)
+    for b in range(len(lens)):
+        assert_close(out[b], ref[b], what=f"TQ4 seq {b}")
+
+
+def test_tq4_unsupported_paths_are_refused(K):
+    g, o, bt, q, ml = decode_case(K, [100], fmt=K.FMT_TQ4, seed=3)
+    ws = K.alloc_workspace(g, 1, 24, ml, 4, device=DEV)
+    sel = torch.arange(4, dtype=torch.int32, device=DEV).reshape(1, 4)
+    with pytest.raises(K.KvqError) as e:
+        K.decode_attn(g, K.tq4_rotate(g, q.to(DEV)), torch.tensor([100], dtype=torch.int32, device=DEV),
+                      torch.from_numpy(bt).to(DEV), ml, 1 / 16, ws, sel=sel)
+    assert e.value.status == K.ERR_UNSUPPORTED
+    with pytest.raises(K.KvqError):
+        K.prefill_attn(g, q.to(DEV), 0, torch.from_numpy(bt[0]).to(DEV), 1 / 16)
+    with pytest.raises(K.KvqError):
+        K.decode_window(g, q.to(DEV).float(), torch.tensor([100], dtype=torch.int32, device=DEV),
+                        torch.from_numpy(bt[0]).to(DEV), ml, 1 / 16, ws)
 
 
 def test_decode_bad_page_and_length_are_flagged(K):
