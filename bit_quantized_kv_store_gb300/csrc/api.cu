@@ -89,12 +89,39 @@ static bool encode_rows_map(CUtensorMap* m, const void* base, uint64_t rows, uin
 struct WsLayout {
   size_t m_off, z_off, acc_off, total;
   int P;
+  int part;  // keys per partition
 };
+
+// Resident 4-bit decode CTAs of the GPU: 4 per SM.  0 if the device cannot be
+// queried (then every grid counts as large).
+static int64_t decode_slots() {
+  static const int64_t slots = [] {
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) !=
+                                                   cudaSuccess) {
+      cudaGetLastError();
+      return int64_t{0};
+    }
+    return int64_t{4} * sms;
+  }();
+  return slots;
+}
+
+// Keys per split-T partition: 512 ("shared 512-key chunks"); the 4-bit formats
+// take 256 when the 512-key grid (partitions x KV heads x sequences) would not
+// fill one wave of resident CTAs, so that the CTAs are twice as many and each
+// walks half as far (a few CTAs per SM are latency-bound, not bandwidth-bound).
+static int partition_keys(const kvq_cache* c, int B, int64_t T) {
+  if (!is_q4(c->format) && c->format != KVQ_FMT_TQ4) return kPart;
+  const int64_t ctas = (T + kPart - 1) / kPart * c->num_kv_heads * B;
+  return ctas < decode_slots() ? kPart / 2 : kPart;
+}
 
 static WsLayout ws_layout(const kvq_cache* c, int B, int Hq, int max_seq_len, int n_sel) {
   WsLayout w;
   const int64_t T = n_sel > 0 ? n_sel : max_seq_len;
-  w.P = static_cast<int>((T + kPart - 1) / kPart);
+  w.part = partition_keys(c, B, T);
+  w.P = static_cast<int>((T + w.part - 1) / w.part);
   if (w.P < 1) w.P = 1;
   const size_t n = static_cast<size_t>(B) * Hq * w.P;
   w.m_off = 256;
@@ -276,6 +303,7 @@ static int32_t decode_attn_impl(const kvq_cache* cache, const float* q, const vo
     a.ws_z = reinterpret_cast<float*>(ws + w.z_off);
     a.ws_acc = reinterpret_cast<float*>(ws + w.acc_off);
     a.P = w.P;
+    a.part = w.part;
     a.status = reinterpret_cast<int32_t*>(ws);
     if (!d_sel) {
       const uint64_t rows = static_cast<uint64_t>(cache->num_pages) * cache->num_kv_heads * cache->page_size;
@@ -340,7 +368,7 @@ int32_t kvq_merge(const kvq_cache* cache, const void* workspace, size_t ws_bytes
   const uint8_t* ws = static_cast<const uint8_t*>(workspace);
   MergeArgs a{reinterpret_cast<const float*>(ws + w.m_off), reinterpret_cast<const float*>(ws + w.z_off),
               reinterpret_cast<const float*>(ws + w.acc_off), w.P, num_q_heads, value_width(cache), d_seq_lens,
-              max_seq_len, n_sel, rotate_back && cache->format == KVQ_FMT_Q4_HAD32 ? 1 : 0, out};
+              max_seq_len, n_sel, rotate_back && cache->format == KVQ_FMT_Q4_HAD32 ? 1 : 0, out, w.part};
   cudaError_t e = launch_merge(a, num_seqs, static_cast<cudaStream_t>(stream));
   if (e == cudaSuccess && rotate_back && cache->format == KVQ_FMT_TQ4)  // the row transform needs the whole row
     e = launch_tq4_rotate(*cache, out, KVQ_DT_F32, out, static_cast<int64_t>(num_seqs) * num_q_heads, 1,

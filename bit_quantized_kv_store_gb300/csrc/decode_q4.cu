@@ -436,10 +436,10 @@ __global__ void __launch_bounds__(kQ4Warps * 32, q4_min_blocks(NT))
       Tmin = min(Tmin, __shfl_xor_sync(0xffffffffu, Tmin, o));
     }
   }
-  const int nparts = bad_len ? 0 : (T + kPart - 1) / kPart;
+  const int nparts = bad_len ? 0 : (T + a.part - 1) / a.part;
   const bool active = p < nparts;  // CTA-uniform
-  const int k0 = p * kPart;
-  const int k1 = min(k0 + kPart, T);
+  const int k0 = p * a.part;
+  const int k1 = min(k0 + a.part, T);
   const int ntiles = active ? (k1 - k0 + 15) / 16 : 0;
   const int nrounds = (ntiles + kQ4RoundTiles - 1) / kQ4RoundTiles;  // <= 4
   // tile u of warp w in round r: kQ4RoundTiles * r + kQ4TPW * w + u

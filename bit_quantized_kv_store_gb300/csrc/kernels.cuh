@@ -41,6 +41,7 @@ struct DecodeArgs {
   int nrows;
   int rows_per_cta;
   int tq;  // 4-bit decode: 1 for TQ4 rows (codebook levels, one scale per row)
+  int part;  // 4-bit decode: keys per partition (512, or 256 for grids under one wave)
 };
 
 // Log-sum-exp merge of the partials (merge.cu).
@@ -56,6 +57,7 @@ struct MergeArgs {
   int n_sel;
   int rotate_back;
   float* out;
+  int part;  // keys per partition (as in the decode that wrote the partials)
 };
 
 // Causal prefill over decoded 4-bit slots (prefill_tc.cu).

@@ -36,7 +36,7 @@ __global__ void __launch_bounds__(256) merge_kernel(const MergeArgs a) {
     if (tid < 32) outp[tid] = NAN;
     return;
   }
-  const int np = (T + kPart - 1) / kPart;
+  const int np = (T + a.part - 1) / a.part;
   if (np == 0) {
     if (tid < 32) outp[tid] = 0.f;
     return;
