@@ -35,6 +35,10 @@ sys.path.insert(0, ROOT)
 
 LAYERS, HK, HQ, D, PS = 16, 4, 24, 256, 16
 KERNELS_PER_LAYER = 3  # store + query rotation (one launch), split-T decode, merge
+# DRAM bytes (read + write) of one decode launch, from ncu captures of the
+# current kernel (profiles/decode_q4_round_kernel_{32k,262k}_context.md);
+# None once the kernel changes.
+TRAFFIC_BYTES = {32768: 37866752 + 1280, 262144: 302271744 + 10774528}
 BYTES_PER_POS_LAYER = HK * 2 * (D // 2 + 2 * (D // 32))   # 1152
 
 
@@ -682,7 +686,8 @@ def main():
         long = {"context": args.long_context, "value": ltot * 1e3 / (LAYERS * lsteps * world),
                 "unit": "us/layer-token", "decode_kernel_us": lavg * 1e3,
                 "roofline": {"bound": "hbm", "achieved": lach, "peak": peak, "unit": "GB/s", "frac": lach / peak,
-                             "traffic": None, "bytes_per_launch": lbytes, "kernel": "decode_q4_round_kernel"},
+                             "traffic": TRAFFIC_BYTES.get(args.long_context), "bytes_per_launch": lbytes,
+                             "kernel": "decode_q4_round_kernel"},
                 "clocks": clk2.summary()}
         del WL
 
@@ -713,7 +718,7 @@ def main():
                                    f"channels", "l2": "16 layer caches exceed L2 (no flush needed)",
                        "parallelism": f"replicas x{world}"},
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                         "traffic": None, "bytes_per_launch": bytes_per_launch,
+                         "traffic": TRAFFIC_BYTES.get(args.context), "bytes_per_launch": bytes_per_launch,
                          "kernel": "decode_q4_round_kernel",
                          "decode_kernel_us": dec_avg_ms * 1e3, "peak_kind": peak_kind},
             "e2e": {"value": e2e_us, "unit": "us/layer-token", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
