@@ -35,9 +35,9 @@ sys.path.insert(0, ROOT)
 
 LAYERS, HK, HQ, D, PS = 16, 4, 24, 256, 16
 KERNELS_PER_LAYER = 3  # store + query rotation (one launch), split-T decode, merge
-# DRAM bytes (read + write) of one decode launch, from ncu captures of the
-# current kernel (profiles/decode_q4_round_kernel_{32k,262k}_context.md);
-# None once the kernel changes.
+# DRAM bytes of one decode launch (dram__bytes_read.sum + dram__bytes_write.sum
+# from an ncu capture of the current kernel at each context); to be dropped
+# whenever the kernel changes.
 TRAFFIC_BYTES = {32768: 37866752 + 1280, 262144: 302271744 + 10774528}
 BYTES_PER_POS_LAYER = HK * 2 * (D // 2 + 2 * (D // 32))   # 1152
 
