@@ -54,7 +54,7 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-rows", action="store_true", help="skip the other hot-path rows (batched decode, prefill, "
                     "fp8, bf16 cache, store)")
-    ap.add_argument("--only", choices=["batched", "prefill", "fp8", "bf16", "q4_0", "window", "tq4"], default=None,
+    ap.add_argument("--only", choices=["batched", "prefill", "fp8", "bf16", "q4_0", "window", "tq4", "fp8_prefill"], default=None,
                     help="run only one of the other hot-path rows and print its measurement (for profiling)")
     ap.add_argument("--layers", type=int, default=16, help="layers per step (16 for the benchmark; fewer "
                     "only to profile a small case)")
@@ -357,6 +357,8 @@ def measure_rows(K, synth, torch, dev, peak, tflops_peak, only=None):
         out.update(_row_window(K, synth, torch, dev, peak, seed))
     if want("tq4"):
         out.update(_row_tq4(K, synth, torch, dev, peak, seed))
+    if want("fp8_prefill"):
+        out.update(_row_fp8_prefill(K, synth, torch, dev, seed))
     return out
 
 
@@ -482,6 +484,36 @@ def _row_fp8(K, synth, torch, dev, seed):
                          "GBs": byts / (ms * 1e-3) / 1e9, "gather_2048_us": gms * 1e3,
                          "kernel": "decode_fp8_kernel (mma.sync f16, split query) + merge_kernel"}
     del c, wsf, wsg
+    torch.cuda.empty_cache()
+    return out
+
+
+def _row_fp8_prefill(K, synth, torch, dev, seed):
+    """fp8 latent prefill past the old caps: a 32-row chunk at positions 1048544 ..
+    1048575 (1M keys), 128 heads, causal; one streaming CTA per (row, 32 heads)."""
+    out = {}
+    n_q, Hf, DL, R = 32, 128, 512, 64
+    T = 1 << 20
+    npg = T // PS
+    c = K.Cache(K.FMT_FP8_ROW, 1, DL, PS, npg, device=dev, rope_dim=R)
+    for s0 in range(0, T, 65536):
+        rows_ = synth.latent_rows(65536, DL + R, dev, seed, "fp8pf", s0)
+        K.store(c, rows_, None, torch.arange(s0, s0 + 65536, dtype=torch.int32, device=dev))
+    q = synth.normal((n_q, Hf, DL + R), dev, seed, "fp8pfq")
+    bt = torch.arange(npg, dtype=torch.int32, device=dev)
+    sm = 1 / math.sqrt(DL + R)
+    ws = torch.zeros(K.lib().kvq_prefill_fp8_workspace_size(c.ref, n_q, Hf), dtype=torch.uint8, device=dev)
+    o = torch.empty((n_q, Hf, DL), dtype=torch.float32, device=dev)
+    depth = T - n_q
+    ms = _events_time(torch, lambda: K.prefill_attn_fp8(c, q, depth, bt, sm, workspace=ws, out=o), 3, warmup=1)
+    keys = sum(depth + i + 1 for i in range(n_q))
+    flops = keys * Hf * 2 * (DL + R + DL)
+    out["fp8_prefill_1m"] = {"workload": "fp8 latent prefill chunk of 32 rows at positions 1048544..1048575, 128 heads, "
+                                         "causal over (512 + 64) e4m3 rows",
+                             "ms": ms, "flop": flops, "TFLOPs": flops / (ms * 1e-3) / 1e12,
+                             "kernel": "decode_fp8_kernel (streaming: one CTA per row x 32 heads, the row one "
+                                       "partition) + merge_kernel"}
+    del c, ws
     torch.cuda.empty_cache()
     return out
 

@@ -53,6 +53,8 @@ SIGNATURES = {
     "kvq_merge": (_I32, [ctypes.POINTER(CacheDesc), _P, _SZ, _I32, _I32, _P, _I32, _I32, _I32, _P, _P]),
     "kvq_prefill_attn": (_I32, [ctypes.POINTER(CacheDesc), _P, _I32, _I32, _I32, _I32, _P, _I32, _F, _P, _P, _P]),
     "kvq_read_status": (_I32, [_P, _P, _P]),
+    "kvq_prefill_fp8_workspace_size": (_SZ, [ctypes.POINTER(CacheDesc), _I32, _I32]),
+    "kvq_prefill_attn_fp8": (_I32, [ctypes.POINTER(CacheDesc), _P, _I32, _I32, _I32, _P, _I32, _F, _P, _SZ, _P, _P]),
     "kvq_noalloc_scratch_bytes": (_SZ, []),
     "kvq_decode_noalloc": (_I32, [ctypes.POINTER(CacheDesc), _P, _I32, _I32, _P, _P, _I32, _I32, _P, _I32, _F, _I32,
                                   _P, _P, _P]),
@@ -303,6 +305,23 @@ def decode_noalloc(cache: Cache, q_rot, seq_lens, block_tables, max_seq_len, sm_
     _check(lib().kvq_decode_noalloc(cache.ref, _ptr(q_rot), B, Hq, _ptr(seq_lens), _ptr(block_tables),
                                     block_tables.shape[1], max_seq_len, _ptr(sel), n_sel, float(sm_scale),
                                     int(rotate_back), _ptr(out), _ptr(status), _stream(stream)), "kvq_decode_noalloc")
+    return out
+
+
+def prefill_attn_fp8(cache: Cache, q, q_start, block_table, sm_scale, workspace=None, out=None, stream=None):
+    """Causal prefill of q [n_q, Hq, 576] (positions q_start ..) over the fp8
+    latent cache; returns out [n_q, Hq, 512] (the workspace's first word is the
+    status)."""
+    n_q, Hq = q.shape[0], q.shape[1]
+    if workspace is None:
+        workspace = torch.zeros(lib().kvq_prefill_fp8_workspace_size(cache.ref, n_q, Hq), dtype=torch.uint8,
+                                device=q.device)
+    if out is None:
+        out = torch.empty((n_q, Hq, cache.D), dtype=torch.float32, device=q.device)
+    bt = block_table.reshape(-1)
+    _check(lib().kvq_prefill_attn_fp8(cache.ref, _ptr(q), n_q, Hq, int(q_start), _ptr(bt), bt.numel(),
+                                      float(sm_scale), _ptr(workspace), workspace.numel(), _ptr(out),
+                                      _stream(stream)), "kvq_prefill_attn_fp8")
     return out
 
 

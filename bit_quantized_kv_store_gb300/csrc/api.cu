@@ -413,6 +413,76 @@ int32_t kvq_prefill_attn(const kvq_cache* cache, const void* q, int32_t dtype, i
   return e == cudaSuccess ? KVQ_OK : cuda_fail(e);
 }
 
+// fp8 streaming prefill: one partial (m, z, acc) per (row, head), the whole row
+// being one partition.
+static constexpr int kWholeRow = 1 << 30;
+
+static WsLayout prefill_fp8_layout(int n_q, int Hq) {
+  WsLayout w;
+  w.P = 1;
+  w.part = kWholeRow;
+  const size_t n = static_cast<size_t>(n_q) * Hq;
+  w.m_off = 256;
+  w.z_off = w.m_off + round256(n * sizeof(float));
+  w.acc_off = w.z_off + round256(n * sizeof(float));
+  w.total = w.acc_off + round256(n * 512 * sizeof(float));
+  return w;
+}
+
+size_t kvq_prefill_fp8_workspace_size(const kvq_cache* cache, int32_t n_q, int32_t num_q_heads) {
+  if (!cache || n_q < 0 || num_q_heads < 0) return 0;
+  return prefill_fp8_layout(n_q, num_q_heads).total;
+}
+
+int32_t kvq_prefill_attn_fp8(const kvq_cache* cache, const float* q, int32_t n_q, int32_t num_q_heads,
+                             int32_t q_start, const int32_t* d_block_table, int32_t max_pages, float sm_scale,
+                             void* workspace, size_t ws_bytes, float* out, void* stream) {
+  int32_t st = check_cache(cache);
+  if (st != KVQ_OK) return st;
+  if (cache->format != KVQ_FMT_FP8_ROW) return KVQ_ERR_UNSUPPORTED;
+  if (cache->head_dim != 512 || cache->rope_dim != 64 || num_q_heads < 16 || num_q_heads % 16 != 0)
+    return KVQ_ERR_UNSUPPORTED;
+  if (n_q < 0 || q_start < 0) return KVQ_ERR_INVALID_ARG;
+  if (n_q == 0) return KVQ_OK;
+  if (!q || !aligned16(q) || !out || !d_block_table || max_pages < 1 || !workspace || !aligned16(workspace))
+    return KVQ_ERR_INVALID_ARG;
+  const int64_t max_len = static_cast<int64_t>(q_start) + n_q;
+  if (max_len > static_cast<int64_t>(max_pages) * cache->page_size || max_len >= kWholeRow) return KVQ_ERR_INVALID_ARG;
+  const WsLayout w = prefill_fp8_layout(n_q, num_q_heads);
+  if (ws_bytes < w.total) return KVQ_ERR_WORKSPACE_TOO_SMALL;
+  const uint64_t rows = static_cast<uint64_t>(cache->num_pages) * cache->page_size;
+  if (rows >= (1ull << 31)) return KVQ_ERR_UNSUPPORTED;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  DecodeArgs a{};
+  a.c = *cache;
+  a.q = q;
+  a.Hq = num_q_heads;
+  a.group = num_q_heads;
+  a.block_tables = d_block_table;
+  a.max_pages = max_pages;
+  a.bt_stride = 0;  // every row reads the one table
+  a.max_seq_len = static_cast<int>(max_len);
+  a.qscale = sm_scale * kLog2e;
+  a.ws_m = reinterpret_cast<float*>(ws + w.m_off);
+  a.ws_z = reinterpret_cast<float*>(ws + w.z_off);
+  a.ws_acc = reinterpret_cast<float*>(ws + w.acc_off);
+  a.P = 1;
+  a.part = w.part;
+  a.status = reinterpret_cast<int32_t*>(ws);
+  a.prefill = 1;
+  a.prefill_q0 = q_start;
+  if (!encode_rows_map(&a.tm_k, cache->k, rows, 512, 16) ||
+      !encode_rows_map(&a.tm_v, cache->v, rows, 64, 16, 64, CU_TENSOR_MAP_SWIZZLE_64B))
+    return cuda_fail(cudaErrorInvalidValue);
+  cudaError_t e = launch_decode_fp8(a, n_q, s);
+  if (e == cudaSuccess) {
+    MergeArgs m{a.ws_m, a.ws_z, a.ws_acc, 1, num_q_heads, 512, nullptr, a.max_seq_len, 0, 0, out, w.part, 1, q_start};
+    e = launch_merge(m, n_q, s);
+  }
+  return e == cudaSuccess ? KVQ_OK : cuda_fail(e);
+}
+
 int32_t kvq_read_status(const void* d_status, int32_t* host_code, void* stream) {
   if (!d_status || !host_code) return KVQ_ERR_INVALID_ARG;
   cudaStream_t s = static_cast<cudaStream_t>(stream);

@@ -156,16 +156,17 @@ __global__ void __launch_bounds__((kF8Warps + 1) * 32, 1) decode_fp8_kernel(cons
   if (GATHER) {
     T = a.n_sel;
   } else {
-    T = a.seq_lens[b];
+    T = a.prefill ? a.prefill_q0 + b + 1 : a.seq_lens[b];
     if (T < 0 || T > a.max_seq_len || (int64_t)T > (int64_t)a.max_pages * c.page_size) {
       if (threadIdx.x == 0 && p == 0 && hblk == 0) set_status(a.status, KVQ_DEV_BAD_LENGTH);
       return;  // the merge writes NaN for this sequence
     }
   }
-  const int nparts = (T + kPart - 1) / kPart;
+  // partitions of a.part keys (512; a whole row for the streaming prefill)
+  const int nparts = static_cast<int>(((int64_t)T + a.part - 1) / a.part);
   if (p >= nparts) return;
-  const int k0 = p * kPart;
-  const int k1 = min(k0 + kPart, T);
+  const int k0 = p * a.part;
+  const int k1 = static_cast<int>(min((int64_t)k0 + a.part, (int64_t)T));
   const int ntiles = (k1 - k0 + kF8Keys - 1) / kF8Keys;
 
   if (threadIdx.x == 0) {
@@ -205,7 +206,7 @@ __global__ void __launch_bounds__((kF8Warps + 1) * 32, 1) decode_fp8_kernel(cons
 
   if (warp == kF8Warps) {
     // ---------------- producer warp
-    const int32_t* bt = a.block_tables + (int64_t)b * a.max_pages;
+    const int32_t* bt = a.block_tables + (int64_t)b * a.bt_stride;  // bt_stride 0: one table for every row
     const int32_t Tseq = GATHER ? a.seq_lens[b] : T;
     bool bad = false;
     F8Stage& st = sm.raw;

@@ -41,7 +41,11 @@ struct DecodeArgs {
   int nrows;
   int rows_per_cta;
   int tq;  // 4-bit decode: 1 for TQ4 rows (codebook levels, one scale per row)
-  int part;  // 4-bit decode: keys per partition (512, or 256 for grids under one wave)
+  int part;  // keys per partition (4-bit: 512, or 256 for grids under one wave; fp8 streaming prefill: a whole row)
+  // fp8 prefill chunk: row b is the query at position prefill_q0 + b and attends
+  // keys 0 .. prefill_q0 + b (seq_lens unused); 0: decode
+  int prefill;
+  int prefill_q0;
 };
 
 // Log-sum-exp merge of the partials (merge.cu).
@@ -58,6 +62,8 @@ struct MergeArgs {
   int rotate_back;
   float* out;
   int part;  // keys per partition (as in the decode that wrote the partials)
+  int prefill;     // 1: row b has prefill_q0 + b + 1 keys (seq_lens unused)
+  int prefill_q0;
 };
 
 // Causal prefill over decoded 4-bit slots (prefill_tc.cu).

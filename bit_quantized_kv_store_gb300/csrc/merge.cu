@@ -29,14 +29,14 @@ __global__ void __launch_bounds__(256) merge_kernel(const MergeArgs a) {
   if (a.n_sel > 0) {
     T = a.n_sel;
   } else {
-    T = a.seq_lens[b];
+    T = a.prefill ? a.prefill_q0 + b + 1 : a.seq_lens[b];
     bad = T < 0 || T > a.max_seq_len;
   }
   if (bad) {
     if (tid < 32) outp[tid] = NAN;
     return;
   }
-  const int np = (T + a.part - 1) / a.part;
+  const int np = static_cast<int>(((int64_t)T + a.part - 1) / a.part);
   if (np == 0) {
     if (tid < 32) outp[tid] = 0.f;
     return;

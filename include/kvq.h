@@ -297,6 +297,29 @@ int32_t kvq_prefill_attn(const kvq_cache* cache, const void* q, int32_t dtype, i
 
 /* Copy the device status word at the start of a decode workspace (or any
  * device int32) to *host_code; synchronises `stream`. */
+/* Size in bytes of the workspace kvq_prefill_attn_fp8 needs: a 256-byte header
+ * (status word at offset 0), then m, z [n_q][num_q_heads] f32 and acc
+ * [n_q][num_q_heads][512] f32 (one partial per row and head). */
+size_t kvq_prefill_fp8_workspace_size(const kvq_cache* cache, int32_t n_q, int32_t num_q_heads);
+
+/* kvq_prefill_attn_fp8 -- causal attention of a prompt chunk over the fp8
+ * latent cache ([P3] "KV cache quantization: fp8 (KV8) + 4-bit TurboQuant",
+ * split-T commit: the batch / prefill path keeps a tiled streaming kernel with
+ * one block per (row, heads), the length cap lifted to 1M): query i (absolute
+ * position q_start + i) attends keys 0 .. q_start + i, absorbed as in
+ * kvq_decode_attn (key = Lc ++ Rc, value = Lc).  One CTA per (block of 32
+ * heads, row) streams all of the row's keys with an online softmax (the row is
+ * one partition), then the merge normalises; no length cap beyond the cache.
+ *   q: device fp32 [n_q, num_q_heads, 576]; out: device fp32 [n_q, num_q_heads, 512].
+ *   d_block_table: device int32 [max_pages], the chunk's sequence;
+ *   q_start + n_q <= max_pages * page_size.
+ *   FP8_ROW only (head_dim 512, rope_dim 64, num_q_heads % 16 == 0), else
+ *   KVQ_ERR_UNSUPPORTED.  Bad pages are flagged in the workspace's status word
+ *   (KVQ_DEV_BAD_PAGE) and the affected rows come out NaN. */
+int32_t kvq_prefill_attn_fp8(const kvq_cache* cache, const float* q, int32_t n_q, int32_t num_q_heads,
+                             int32_t q_start, const int32_t* d_block_table, int32_t max_pages, float sm_scale,
+                             void* workspace, size_t ws_bytes, float* out, void* stream);
+
 int32_t kvq_read_status(const void* d_status, int32_t* host_code, void* stream);
 
 /* kvq_decode_noalloc -- kvq_decode_attn followed by kvq_merge, for callers that

@@ -651,15 +651,16 @@ int kvo_decode(const kvo_cache* c, const void* q, int dtype, int B, int Hq, cons
 
 /* Prefill attention over decoded slots [P1 "What it is", prompt chunks]:
  * query i (absolute position q_start + i) attends keys 0 .. q_start + i.
- * q is [n_q, Hq, D] unrotated; out is [n_q, Hq, D] fp64, rotated back.
+ * q is [n_q, Hq, key width] unrotated; out is [n_q, Hq, D] fp64, rotated back
+ * (key width = D, or D + rope for the fp8 latent rows).
  * Only the listed query rows are computed when rows != NULL (rows[r] indexes
  * 0..n_q-1, out then has n_rows entries).  Returns 0 on a bad block table. */
 int kvo_prefill(const kvo_cache* c, const void* q, int dtype, int n_q, int Hq, int64_t q_start,
                 const int32_t* block_table, const int32_t* rows, int n_rows, double sm_scale,
                 double* out) {
-  int D = c->head_dim;
+  int W = key_width(c), D = c->head_dim; /* fp8 rows: 576-wide queries, 512-wide outputs */
   int group = Hq / c->num_kv_heads;
-  double* qv = (double*)malloc(sizeof(double) * D);
+  double* qv = (double*)malloc(sizeof(double) * W);
   int count = rows ? n_rows : n_q;
   int ok = 1;
   for (int r = 0; r < count && ok; r++) {
@@ -668,7 +669,7 @@ int kvo_prefill(const kvo_cache* c, const void* q, int dtype, int n_q, int Hq, i
     int64_t* pos = (int64_t*)malloc(sizeof(int64_t) * T);
     for (int64_t j = 0; j < T; j++) pos[j] = j;
     for (int h = 0; h < Hq && ok; h++) {
-      prep_query(c, q, dtype, ((int64_t)i * Hq + h) * D, qv);
+      prep_query(c, q, dtype, ((int64_t)i * Hq + h) * W, qv);
       ok = attend_one(c, block_table, qv, h / group, pos, T, sm_scale, 0,
                       out + ((int64_t)r * Hq + h) * D);
     }

@@ -648,6 +648,55 @@ def test_decode_fp8_latent(K):
 
 # --------------------------------------------------------------------------- prefill
 
+def _fp8_prefill_case(K, depth, n_q, Hq=32, seed=0):
+    D, R, ps = 512, 64, 16
+    T = depth + n_q
+    n_pages = (T + ps - 1) // ps + 1
+    g, o = make_cache_pair(K, K.FMT_FP8_ROW, 1, D, ps, n_pages, rope=R)
+    bt = synth.page_permutation(n_pages, "fp8pf", seed).numpy().astype(np.int32)
+    fill_sequence(K, g, o, synth.latent_rows(T, D + R, "cpu", "fp8pf", seed), None, bt, T)
+    q = synth.normal((n_q, Hq, D + R), "cpu", "fp8pfq", seed)
+    return g, o, bt, q
+
+
+@pytest.mark.parametrize("depth,n_q,Hq", [(0, 5, 32), (700, 6, 32), (1500, 3, 48)])
+def test_prefill_fp8_matches_oracle(K, depth, n_q, Hq):
+    """fp8 latent prefill (one streaming CTA per row and 32 heads, the whole row one
+    partition) against the oracle's causal prefill."""
+    g, o, bt, q = _fp8_prefill_case(K, depth, n_q, Hq, seed=depth)
+    sm = 1 / math.sqrt(576)
+    out = K.prefill_attn_fp8(g, q.to(DEV), depth, torch.from_numpy(bt).to(DEV), sm).cpu().numpy()
+    ref = O.prefill(o, q.numpy(), depth, bt, sm)
+    for i in range(n_q):
+        assert_close(out[i], ref[i], what=f"fp8 prefill row {i}")
+
+
+def test_prefill_fp8_long_rows_equal_split_decode(K):
+    """At 1M keys (past the pages' old 4096 / 8192 caps): the streaming prefill of
+    the last rows equals the split-T decode + merge of the same rows."""
+    D, R, ps, Hq = 512, 64, 64, 32
+    n_q = 2
+    T = (1 << 20) + n_q
+    n_pages = (T + ps - 1) // ps
+    g = K.Cache(K.FMT_FP8_ROW, 1, D, ps, n_pages, device=DEV, rope_dim=R)
+    for s0 in range(0, T, 1 << 16):
+        n = min(1 << 16, T - s0)
+        K.store(g, synth.latent_rows(n, D + R, DEV, "fp8big", s0), None,
+                torch.arange(s0, s0 + n, dtype=torch.int32, device=DEV))
+    bt = torch.arange(n_pages, dtype=torch.int32, device=DEV)
+    q = synth.normal((n_q, Hq, D + R), DEV, "fp8bigq")
+    sm = 1 / math.sqrt(576)
+    depth = T - n_q
+    out = K.prefill_attn_fp8(g, q, depth, bt, sm)
+    lens = torch.arange(depth + 1, T + 1, dtype=torch.int32, device=DEV)
+    ws = K.alloc_workspace(g, n_q, Hq, T, device=DEV)
+    ref = K.decode(g, q, lens, bt.reshape(1, -1).repeat(n_q, 1).contiguous(), T, sm, ws)
+    torch.cuda.synchronize()
+    for i in range(n_q):
+        assert_close(out[i].cpu().numpy(), ref[i].cpu().numpy().astype(np.float64), tol=1e-4,
+                     what=f"1M-key row {i}")
+
+
 @pytest.mark.parametrize("depth,n_q", [(0, 20), (100, 37), (600, 150)])
 def test_prefill(K, depth, n_q):
     Hk, Hq, D, ps = 4, 24, 256, 16

@@ -458,6 +458,24 @@ def test_prefill_row_equals_decode_at_its_position():
     assert np.array_equal(sub, out[[0, 8, 3]])
 
 
+def test_prefill_row_equals_decode_at_its_position_fp8():
+    """The same for the fp8 latent rows: 576-wide queries, 512-wide outputs."""
+    D, R, ps, Hq = 512, 64, 16, 2
+    depth, n_q = 30, 5
+    T = depth + n_q
+    c = O.Cache(O.FP8, 1, D, ps, 3, rope_dim=R)
+    bt = np.array([2, 0, 1], np.int32)
+    rows = (RNG.standard_normal((T, D + R)) * np.exp(RNG.standard_normal((T, 1)))).astype(np.float32)
+    slots = np.array([bt[j // ps] * ps + j % ps for j in range(T)], np.int32)
+    assert O.store(c, rows, None, slots) == 0
+    q = RNG.standard_normal((n_q, Hq, D + R)).astype(np.float32)
+    out = O.prefill(c, q, depth, bt, 0.05)
+    assert out.shape == (n_q, Hq, D)
+    for i in range(n_q):
+        d = O.decode(c, q[i:i + 1], [depth + i + 1], bt[None], 0.05)
+        assert np.array_equal(out[i], d[0])
+
+
 def test_empty_sequence_gives_zero():
     c = O.Cache(O.Q4, 1, 32, 16, 1)
     out = O.decode(c, np.ones((1, 1, 32), np.float32), [0], np.zeros((1, 1), np.int32), 1.0)
