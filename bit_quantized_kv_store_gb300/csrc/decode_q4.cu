@@ -140,11 +140,13 @@ __device__ __forceinline__ void q4_frag_prep(const float* qrow, bool live, float
     const float4 u0 = ql0[k];
     const float4 u1 = ql1[k];
     uint4 hi, lo;
-    // tile (G,0): slots (2t,2t+1) <- d (8t, 8t+2); slots (2t+8, 2t+9) <- d (8t+1, 8t+3); tile (G,1): d + 4
-    split_f16(u0.x * s, u0.z * s, hi.x, lo.x);
-    split_f16(u0.y * s16, u0.w * s16, hi.y, lo.y);
-    split_f16(u1.x * s, u1.z * s, hi.z, lo.z);
-    split_f16(u1.y * s16, u1.w * s16, hi.w, lo.w);
+    // first MMA of the group: slots (2t, 2t+1) <- d (8t, 8t+4) (low nibbles of
+    // bytes 0, 2 of the key's word), slots (2t+8, 2t+9) <- d (8t+1, 8t+5) (high
+    // nibbles); second MMA: d + 2 (the word shifted by a byte)
+    split_f16(u0.x * s, u1.x * s, hi.x, lo.x);
+    split_f16(u0.y * s16, u1.y * s16, hi.y, lo.y);
+    split_f16(u0.z * s, u1.z * s, hi.z, lo.z);
+    split_f16(u0.w * s16, u1.w * s16, hi.w, lo.w);
     qf[G][0][lane] = hi;
     qf[G][1][lane] = lo;
     float ev = 0.f, od = 0.f;  // sums of the even-slot and odd-slot B values (hi parts, then lo parts)
@@ -631,11 +633,11 @@ __global__ void __launch_bounds__(kQ4Warps * 32, q4_min_blocks(NT))
           }
 #pragma unroll
           for (int u = 0; u < kQ4TPW; ++u) {
-            const uint32_t wa = e ? kw[u].z : kw[u].x, wb = e ? kw[u].w : kw[u].y;
-            const uint32_t xa1 = prmt(wa, 0u, 0x4140u);  // codes 8t .. 8t+3 of key g: bytes 0, 1 -> halves
-            const uint32_t xa2 = prmt(wa, 0u, 0x4342u);  // codes 8t+4 .. 8t+7
-            const uint32_t xb1 = prmt(wb, 0u, 0x4140u);  // key g+8
-            const uint32_t xb2 = prmt(wb, 0u, 0x4342u);
+            // codes 8t .. 8t+7 of keys g (xa1) and g+8 (xb1); the nibble pairs
+            // (0, 4), (1, 5) sit in bits 0-3 / 16-19 and 4-7 / 20-23; shifted by a
+            // byte (xa2, xb2), the pairs (2, 6), (3, 7)
+            const uint32_t xa1 = e ? kw[u].z : kw[u].x, xb1 = e ? kw[u].w : kw[u].y;
+            const uint32_t xa2 = xa1 >> 8, xb2 = xb1 >> 8;
             const uint32_t a10 = nib_lo_pair_biased(xa1), a11 = nib_lo_pair_biased(xb1);
             const uint32_t a12 = nib_hi_pair_biased(xa1), a13 = nib_hi_pair_biased(xb1);
             const uint32_t a20 = nib_lo_pair_biased(xa2), a21 = nib_lo_pair_biased(xb2);

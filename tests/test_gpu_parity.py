@@ -540,6 +540,19 @@ def test_decode_tq4_gqa_batch(K, Hk, Hq):
         assert_close(out[b], ref[b], what=f"TQ4 seq {b}")
 
 
+def test_store_tq4_flags_bad_slots(K):
+    D, Hk, ps = 64, 2, 16
+    g, o = make_cache_pair(K, K.FMT_TQ4, Hk, D, ps, 2, sign_seed=2)
+    k = synth.normal((4, Hk, D), "cpu", "tqbad")
+    slots = torch.tensor([3, -1, 40, 17], dtype=torch.int32)
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    K.store(g, k.to(DEV), k.to(DEV), slots.to(DEV), status=st)
+    torch.cuda.synchronize()
+    assert K.read_status(st) & K.DEV_BAD_SLOT
+    assert O.store(o, k.numpy(), k.numpy(), slots.numpy()) == 1
+    check_planes_equal(g, o)
+
+
 def test_tq4_unsupported_paths_are_refused(K):
     g, o, bt, q, ml = decode_case(K, [100], fmt=K.FMT_TQ4, seed=3)
     ws = K.alloc_workspace(g, 1, 24, ml, 4, device=DEV)
@@ -669,6 +682,24 @@ def test_prefill_fp8_matches_oracle(K, depth, n_q, Hq):
     ref = O.prefill(o, q.numpy(), depth, bt, sm)
     for i in range(n_q):
         assert_close(out[i], ref[i], what=f"fp8 prefill row {i}")
+
+
+def test_prefill_fp8_bad_page_is_flagged(K):
+    """A block-table entry outside the pool: flagged in the workspace's status
+    word; the rows that reach it come out NaN, the rows before it are intact."""
+    depth, n_q, Hq = 60, 40, 32
+    g, o, bt, q = _fp8_prefill_case(K, depth, n_q, Hq, seed=9)
+    sm = 1 / math.sqrt(576)
+    bad = bt.copy()
+    bad[(depth + 20) // 16] = 10_000          # the page of key depth + 20 (page size 16)
+    ws = torch.zeros(K.lib().kvq_prefill_fp8_workspace_size(g.ref, n_q, Hq), dtype=torch.uint8, device=DEV)
+    out = K.prefill_attn_fp8(g, q.to(DEV), depth, torch.from_numpy(bad).to(DEV), sm, workspace=ws).cpu().numpy()
+    assert K.read_status(ws) & K.DEV_BAD_PAGE
+    first_bad = (depth + 20) // 16 * 16 - depth   # row i reads keys 0 .. depth + i
+    assert np.isnan(out[n_q - 1]).all()
+    ref = O.prefill(o, q.numpy(), depth, bt, sm, rows=list(range(first_bad)))
+    for i in range(first_bad):
+        assert_close(out[i], ref[i], what=f"fp8 prefill row {i} before the bad page")
 
 
 def test_prefill_fp8_long_rows_equal_split_decode(K):
