@@ -54,6 +54,7 @@ SIGNATURES = {
     "kvq_prefill_attn": (_I32, [ctypes.POINTER(CacheDesc), _P, _I32, _I32, _I32, _I32, _P, _I32, _F, _P, _P, _P]),
     "kvq_read_status": (_I32, [_P, _P, _P]),
     "kvq_prefill_fp8_workspace_size": (_SZ, [ctypes.POINTER(CacheDesc), _I32, _I32]),
+    "kvq_selftest_wait_timeout": (_I32, [_P, _P]),
     "kvq_prefill_attn_fp8": (_I32, [ctypes.POINTER(CacheDesc), _P, _I32, _I32, _I32, _P, _I32, _F, _P, _SZ, _P, _P]),
     "kvq_noalloc_scratch_bytes": (_SZ, []),
     "kvq_decode_noalloc": (_I32, [ctypes.POINTER(CacheDesc), _P, _I32, _I32, _P, _P, _I32, _I32, _P, _I32, _F, _I32,
@@ -323,6 +324,11 @@ def prefill_attn_fp8(cache: Cache, q, q_start, block_table, sm_scale, workspace=
                                       float(sm_scale), _ptr(workspace), workspace.numel(), _ptr(out),
                                       _stream(stream)), "kvq_prefill_attn_fp8")
     return out
+
+
+def selftest_wait_timeout(d_status, stream=None):
+    """Run the bounded-wait diagnostic (about 2 s); KVQ_DEV_TIMEOUT lands in d_status."""
+    _check(lib().kvq_selftest_wait_timeout(_ptr(d_status), _stream(stream)), "kvq_selftest_wait_timeout")
 
 
 def read_status(d_status, stream=None):

@@ -483,6 +483,12 @@ int32_t kvq_prefill_attn_fp8(const kvq_cache* cache, const float* q, int32_t n_q
   return e == cudaSuccess ? KVQ_OK : cuda_fail(e);
 }
 
+int32_t kvq_selftest_wait_timeout(int32_t* d_status, void* stream) {
+  if (!d_status) return KVQ_ERR_INVALID_ARG;
+  cudaError_t e = launch_wait_timeout_probe(d_status, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? KVQ_OK : cuda_fail(e);
+}
+
 int32_t kvq_read_status(const void* d_status, int32_t* host_code, void* stream) {
   if (!d_status || !host_code) return KVQ_ERR_INVALID_ARG;
   cudaStream_t s = static_cast<cudaStream_t>(stream);

@@ -110,6 +110,8 @@ cudaError_t launch_decode_fp8(const DecodeArgs& a, int B, cudaStream_t s);
 // planes as [rows][512 B] in 128-byte column boxes.
 cudaError_t launch_decode_bf16(const DecodeArgs& a, int B, cudaStream_t s);
 cudaError_t launch_merge(const MergeArgs& a, int B, cudaStream_t s);
+// A barrier wait that nothing completes, bounded like every copy wait (api.cu).
+cudaError_t launch_wait_timeout_probe(int32_t* status, cudaStream_t s);
 cudaError_t launch_prefill_tc(const PrefillArgs& a, cudaStream_t s);
 
 }  // namespace kvq

@@ -120,6 +120,20 @@ __global__ void __launch_bounds__(256) merge_kernel(const MergeArgs a) {
   }
 }
 
+// One thread waits, with the bounded wait of the copy waits, on a barrier that
+// expects one arrival that never comes; it records the timeout and returns.
+__global__ void wait_timeout_probe_kernel(int32_t* status) {
+  __shared__ uint64_t bar;
+  mbar_init(&bar, 1);
+  fence_barrier_init();
+  if (!mbar_wait_bounded(&bar, 0)) set_status(status, KVQ_DEV_TIMEOUT);
+}
+
+cudaError_t launch_wait_timeout_probe(int32_t* status, cudaStream_t s) {
+  wait_timeout_probe_kernel<<<1, 1, 0, s>>>(status);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_merge(const MergeArgs& a, int B, cudaStream_t s) {
   dim3 grid(a.Dv / 32, a.Hq, B);
   if (B == 0 || a.Hq == 0) return cudaSuccess;

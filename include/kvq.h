@@ -322,6 +322,13 @@ int32_t kvq_prefill_attn_fp8(const kvq_cache* cache, const float* q, int32_t n_q
 
 int32_t kvq_read_status(const void* d_status, int32_t* host_code, void* stream);
 
+/* kvq_selftest_wait_timeout -- diagnostic of the kernels' copy waits: one CTA
+ * waits on a shared-memory barrier that nothing completes, with the same bounded
+ * wait the kernels use (about 2 seconds), and ORs KVQ_DEV_TIMEOUT into
+ * *d_status when it gives up.  The kernel then returns normally, so the CUDA
+ * context stays usable.  d_status: device int32. */
+int32_t kvq_selftest_wait_timeout(int32_t* d_status, void* stream);
+
 /* kvq_decode_noalloc -- kvq_decode_attn followed by kvq_merge, for callers that
  * cannot allocate device memory when they decode (a host that owns every device
  * allocation, a memory pool that forbids new ones, a latency-critical path that

@@ -583,6 +583,24 @@ def test_decode_bad_page_and_length_are_flagged(K):
     assert np.isnan(out[1]).all()
 
 
+def test_bounded_wait_ends_with_timeout_status(K):
+    """A copy wait that nothing completes gives up after its bound (~2 s) and
+    reports KVQ_DEV_TIMEOUT; the context stays usable (a decode right after
+    still matches the oracle)."""
+    import time
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    t0 = time.time()
+    K.selftest_wait_timeout(st)
+    code = K.read_status(st)
+    assert code & K.DEV_TIMEOUT
+    assert time.time() - t0 < 30
+    lens = [300]
+    g, o, bt, q, ml = decode_case(K, lens, seed=13)
+    out, ws = run_decode(K, g, bt, q, lens, ml, 1 / 16)
+    assert K.read_status(ws) == 0
+    assert_close(out[0], O.decode(o, to_np_in(q), lens, bt, 1 / 16)[0], what="decode after the timeout")
+
+
 def test_decode_bf16_cache(K):
     lens = [1500, 513, 20]
     g, o, bt, q, ml = decode_case(K, lens, fmt=K.FMT_BF16, seed=8)
