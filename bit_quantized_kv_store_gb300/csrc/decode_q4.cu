@@ -1,23 +1,30 @@
-// decode_q4.cu -- split-T decode attention over the Hadamard-rotated 4-bit cache.
+// decode_q4.cu -- split-T decode attention over the 4-bit caches.
 //
 // Follows "qwen27 CUDA: an opt-in 4-bit attention cache (262K on a 24 GB card)",
 // section "What it is": attend over the 4-bit cache in rotated space, in shared
 // 512-key chunks plus the tail, producing per-chunk partials that are merged in
 // order; and "KV cache quantization: fp8 (KV8) + 4-bit TurboQuant", split-T
-// commit: (H, P) partial online-softmax blocks (cl, m, z) + a log-sum-exp merge.
+// commit: (H, P) partial online-softmax blocks (cl, m, z) + a log-sum-exp merge
+// (and, for the TQ4 rows, its "Why rotated-int4" codebook).
 //
-// GB300 design.  One CTA of 4 warps per (partition of 512 keys, KV head,
-// sequence), 4 CTAs per SM (128 registers, 47 KB of shared memory).  The
-// partition is walked in rounds of 8 tiles of 16 keys (128 keys):
+// GB300 design.  One CTA of 4 warps per (partition, KV head, sequence), 4 CTAs
+// per SM (128 registers, 48 KB of shared memory).  A partition is 512 keys, or
+// 256 when the 512-key grid would fill less than one wave (the host decides and
+// the merge follows).  It is walked in rounds of 8 tiles of 16 keys (128 keys):
+//  * Fragments: a code row is 8 groups of 16 bytes, so the 8 rows x 16 bytes of
+//    an ldmatrix 8x8 matrix are one group of 8 keys: one ldmatrix.x4 gives a
+//    thread its K words of two groups for keys g and g + 8, one
+//    ldmatrix.x4.trans its V words for keys 2t, 2t+1, 2t+8, 2t+9.
 //  * Scores: warp w takes tiles 2w, 2w + 1 of the round, all 256 dims, on the
 //    tensor cores (mma.m16n8k16, the 16 keys of a tile on M, the <= 8 query
 //    heads of the GQA group on N).  The key codes enter as the exact f16
-//    values 1024 + c / 1024 + 16c (one lop3 per pair); the constant part is
-//    removed by starting each group's accumulator at a per-(head, group) query
-//    bias.  The query is split into f16 high and low parts (~22 bits; its
-//    fragments sit in shared memory and are loaded once for both tiles); each
-//    32-value group gets its own partial product multiplied by the group's fp32
-//    scale, so the dequantised keys enter exactly.
+//    values 1024 + c / 1024 + 16c (one lop3 per pair, the pairs taken from the
+//    word by masks and one byte shift); the constant part is removed by
+//    starting each group's accumulator at a per-(head, group) query bias.  The
+//    query is split into f16 high and low parts (~22 bits; its fragments sit
+//    in shared memory and are loaded once for both tiles); each 32-value
+//    group gets its own partial product multiplied by the group's fp32 scale,
+//    so the dequantised keys enter exactly.
 //  * The warps exchange their maxima through shared memory, so that every warp
 //    holds the same running maximum (base 2; the query carries
 //    sm_scale * log2 e), and publish their probabilities as ready-made B
@@ -27,14 +34,19 @@
 //    probabilities are multiplied by the V group scale in f16; V codes minus 8
 //    are exact in f16.  Each thread keeps 16 accumulators; a rescale costs 18
 //    FMULs.  Two named barriers per round.
+// Modes of the same kernel: the gather of selected rows (GATHER); decode
+// windows (WIN: up to 4 column tiles of (row, head) pairs of several rows of
+// one sequence per CTA, each row masked at its own end); TQ4 rows (TQ: the
+// nibbles become fp16 codebook levels by prmt lookups, one scale per row, V
+// transposed per key pair by movmatrix).
 // Copies: a tile of codes (16 rows x 128 B) arrives by a 2-D TMA tensor copy
 // with the hardware 128-byte swizzle (16-byte chunk c of row r lands at chunk
-// c ^ (r & 7), so the fragment loads are free of bank conflicts), its 16 x 8
-// fp16 scales by a 1-D bulk copy; the gather variant (selected rows) copies row
-// by row with 1-D bulk copies into unswizzled tiles.  The rings hold one round:
-// a warp refills its own K tiles right after its scores, and its share of the
-// V tiles once an mbarrier shows every warp done with the round's P.V (a round
-// takes microseconds, so the copies have ample lead).
+// c ^ (r & 7), so the fragment loads are free of bank conflicts), its scales
+// by a 1-D bulk copy; the gather variant copies row by row with 1-D bulk
+// copies into rows padded to 144 bytes.  The rings hold one round: a warp
+// refills its own K tiles right after its scores, and its share of the V tiles
+// once an mbarrier shows every warp done with the round's P.V (a round takes
+// microseconds, so the copies have ample lead).
 #include <type_traits>
 
 #include "kernels.cuh"
