@@ -29,6 +29,10 @@
 //  * Context: P' = f16(p * Lsc) (shared memory, A by ldmatrix) times the exact
 //    latent values (B by ldmatrix.trans from the same f16 tile); warp w owns
 //    output dims 64w .. 64w+63 for all 32 heads (64 f32 accumulators per thread).
+// The prefill of a prompt chunk (the split-T commit's "tiled streaming kernel
+// ... with the cap lifted to 1M") is this kernel with a whole row as its one
+// partition: one CTA per (32 heads, row) streams every key of the row through
+// the same tile loop, rows sharing one block table with lengths q_start + row + 1.
 #include <cuda_fp8.h>
 
 #include "kernels.cuh"
