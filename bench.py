@@ -38,7 +38,7 @@ KERNELS_PER_LAYER = 3  # store + query rotation (one launch), split-T decode, me
 # DRAM bytes of one decode launch (dram__bytes_read.sum + dram__bytes_write.sum
 # from an ncu capture of the current kernel at each context); to be dropped
 # whenever the kernel changes.
-TRAFFIC_BYTES = {32768: 37865984 + 512, 262144: 302253056 + 10773504}
+TRAFFIC_BYTES = {32768: 37866240 + 256, 262144: 302253056 + 10773504}
 BYTES_PER_POS_LAYER = HK * 2 * (D // 2 + 2 * (D // 32))   # 1152
 
 

@@ -92,35 +92,13 @@ struct WsLayout {
   int part;  // keys per partition
 };
 
-// Resident 4-bit decode CTAs of the GPU: 4 per SM.  0 if the device cannot be
-// queried (then every grid counts as large).
-static int64_t decode_slots() {
-  static const int64_t slots = [] {
-    int dev = 0, sms = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) !=
-                                                   cudaSuccess) {
-      cudaGetLastError();
-      return int64_t{0};
-    }
-    return int64_t{4} * sms;
-  }();
-  return slots;
-}
-
-// Keys per split-T partition: 512 ("shared 512-key chunks"); the 4-bit formats
-// take 256 when the 512-key grid (partitions x KV heads x sequences) would not
-// fill one wave of resident CTAs, so that the CTAs are twice as many and each
-// walks half as far (a few CTAs per SM are latency-bound, not bandwidth-bound).
-static int partition_keys(const kvq_cache* c, int B, int64_t T) {
-  if (!is_q4(c->format) && c->format != KVQ_FMT_TQ4) return kPart;
-  const int64_t ctas = (T + kPart - 1) / kPart * c->num_kv_heads * B;
-  return ctas < decode_slots() ? kPart / 2 : kPart;
-}
-
+// Keys per split-T partition: 512 ("shared 512-key chunks") for every format
+// and problem size, so that a sequence's partials do not depend on what else
+// is in the batch (a batched sequence equals its solo decode bit for bit).
 static WsLayout ws_layout(const kvq_cache* c, int B, int Hq, int max_seq_len, int n_sel) {
   WsLayout w;
   const int64_t T = n_sel > 0 ? n_sel : max_seq_len;
-  w.part = partition_keys(c, B, T);
+  w.part = kPart;
   w.P = static_cast<int>((T + w.part - 1) / w.part);
   if (w.P < 1) w.P = 1;
   const size_t n = static_cast<size_t>(B) * Hq * w.P;

@@ -7,10 +7,9 @@
 // commit: (H, P) partial online-softmax blocks (cl, m, z) + a log-sum-exp merge
 // (and, for the TQ4 rows, its "Why rotated-int4" codebook).
 //
-// GB300 design.  One CTA of 4 warps per (partition, KV head, sequence), 4 CTAs
-// per SM (128 registers, 48 KB of shared memory).  A partition is 512 keys, or
-// 256 when the 512-key grid would fill less than one wave (the host decides and
-// the merge follows).  It is walked in rounds of 8 tiles of 16 keys (128 keys):
+// GB300 design.  One CTA of 4 warps per (partition of 512 keys, KV head,
+// sequence), 4 CTAs per SM (128 registers, 48 KB of shared memory).  The
+// partition is walked in rounds of 8 tiles of 16 keys (128 keys):
 //  * Fragments: a code row is 8 groups of 16 bytes, so the 8 rows x 16 bytes of
 //    an ldmatrix 8x8 matrix are one group of 8 keys: one ldmatrix.x4 gives a
 //    thread its K words of two groups for keys g and g + 8, one

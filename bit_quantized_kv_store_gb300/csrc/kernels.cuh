@@ -41,7 +41,7 @@ struct DecodeArgs {
   int nrows;
   int rows_per_cta;
   int tq;  // 4-bit decode: 1 for TQ4 rows (codebook levels, one scale per row)
-  int part;  // keys per partition (4-bit: 512, or 256 for grids under one wave; fp8 streaming prefill: a whole row)
+  int part;  // keys per partition (512; the fp8 streaming prefill: a whole row)
   // fp8 prefill chunk: row b is the query at position prefill_q0 + b and attends
   // keys 0 .. prefill_q0 + b (seq_lens unused); 0: decode
   int prefill;

@@ -15,9 +15,8 @@
 // scheduling (bit-reproducible), and the 32 values of the CTA -- exactly one
 // Hadamard group -- are rotated back in one warp.  (The TQ4 rows' transform
 // spans the whole row, so their rotation back is a second launch, tq4.cu.)
-// The number of keys per partition comes with the arguments: the merge of a
-// 4-bit decode uses the decode's 512 or 256, the fp8 streaming prefill one
-// partition per row, whose length is q_start + row + 1.
+// The number of keys per partition comes with the arguments: 512, or for the
+// fp8 streaming prefill one partition per row, whose length is q_start + row + 1.
 #include "kernels.cuh"
 
 namespace kvq {

@@ -194,12 +194,7 @@ int32_t kvq_store_rotate(const kvq_cache* cache, const void* k, const void* v, i
 /* Size in bytes of the workspace kvq_decode_attn needs for this problem:
  * a 256-byte header (status word at offset 0), then partial maxima m and sums z
  * [num_seqs][num_q_heads][P] f32 and partial contexts acc [num_seqs][num_q_heads]
- * [P][value width] f32, where P = ceil(max(max_seq_len, n_sel) / Kp).  Kp, the
- * keys per partition, is 512; for the 4-bit formats (Q4_HAD32, Q4_0, TQ4) it is
- * 256 when ceil(max(max_seq_len, n_sel) / 512) * num_kv_heads * num_seqs is
- * below 4 x the GPU's SM count (a grid of less than one wave of decode CTAs, so
- * twice as many CTAs that each walk half as far).  The decode and the merge of
- * the same problem use the same Kp. */
+ * [P][value width] f32, where P = ceil(max(max_seq_len, n_sel) / 512). */
 size_t kvq_decode_workspace_size(const kvq_cache* cache, int32_t num_seqs, int32_t num_q_heads,
                                  int32_t max_seq_len, int32_t n_sel);
 
@@ -207,8 +202,8 @@ size_t kvq_decode_workspace_size(const kvq_cache* cache, int32_t num_seqs, int32
  * over the 4-bit cache in rotated space over shared 512-key chunks plus the tail;
  * [P3] split-T commit: dim3(H,P) partial online-softmax blocks (cl, m, z)).
  * For sequence b, query head h (reading KV head h / (num_q_heads / num_kv_heads))
- * and partition p (keys [Kp p, min(Kp p + Kp, T_b)), T_b = seq_lens[b], or the
- * p-th run of Kp entries of sel[b] when gathering; Kp as for the workspace), writes
+ * and partition p (keys [512p, min(512p + 512, T_b)), T_b = seq_lens[b], or the
+ * p-th run of 512 entries of sel[b] when gathering), writes
  *   m = max_j s_j * log2(e),  z = sum_j 2^(s_j log2(e) - m),
  *   acc = sum_j 2^(s_j log2(e) - m) * value_j,   s_j = sm_scale * (q . key_j)
  * into the workspace.  Empty partitions get m = -inf, z = 0, acc = 0.

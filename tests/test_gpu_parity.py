@@ -372,13 +372,16 @@ def test_decode_gqa_groups(K, Hk, Hq):
         assert_close(out[b], ref[b], what=f"Hk={Hk} Hq={Hq} seq {b}")
 
 
-def test_decode_concurrent_equals_solo_and_deterministic(K):
-    lens = [1200, 530, 4100]
+@pytest.mark.parametrize("lens", [[1200, 530, 4100], [40000, 512, 38001, 39999, 20000]])
+def test_decode_concurrent_equals_solo_and_deterministic(K, lens):
+    """A batched sequence equals its solo decode bit for bit, for a small batch
+    and for one whose grid (over two waves) is far larger than any of its
+    sequences' alone."""
     g, o, bt, q, ml = decode_case(K, lens, seed=3)
     out, _ = run_decode(K, g, bt, q, lens, ml, 1 / 16)
     out2, _ = run_decode(K, g, bt, q, lens, ml, 1 / 16)
     assert np.array_equal(out, out2)
-    for b in range(3):
+    for b in range(len(lens)):
         solo, _ = run_decode(K, g, bt[b:b + 1], q[b:b + 1], [lens[b]], lens[b], 1 / 16)
         assert np.array_equal(solo[0], out[b])
 
