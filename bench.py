@@ -299,21 +299,34 @@ def cpu_baseline_decode(context, n_heads, seed=99):
                f"(KV heads {kv_heads}), scaled to 24 heads; oracle is single-threaded"
 
 
+METRIC = "decode attn us/layer-token and achieved HBM GB/s vs peak (4-bit KV)"
+
+
+def workload_config(context, world):
+    return {"workload": f"single-sequence decode, context {context} (T={context + 1}), 16 layers, 4 KV / 24 q heads, "
+                        f"head_dim 256, bf16 inputs, 5% Student-t(3)x10 channels",
+            "l2": "16 layer caches exceed L2 (no flush needed)", "parallelism": f"replicas x{world}"}
+
+
 def run_reference(args):
-    """--impl reference: the CPU oracle on the host cores, same metric and config."""
+    """--impl reference: the CPU oracle on the host cores, same metric and config;
+    each of the W warm-up and K timed steps is one bounded sample (one layer-token,
+    6 of the 24 query heads, scaled to 24)."""
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return
+    for s in range(args.warmup):
+        cpu_baseline_decode(args.context, 6, seed=900 + s)
     samples = []
-    for s in range(args.warmup + args.steps if args.steps <= 3 else 3):
+    for s in range(args.steps):
         us, desc = cpu_baseline_decode(args.context, 6, seed=1000 + s)
         samples.append(us)
-    us = statistics.median(samples)
-    line = {"impl": "reference", "metric": "decode attn us/layer-token (4-bit KV, 32K context)", "value": us,
-            "unit": "us/layer-token", "n_gpus": args.gpus, "steps": len(samples), "warmup": 0,
+    us = statistics.mean(samples)
+    line = {"impl": "reference", "metric": METRIC, "value": us,
+            "unit": "us/layer-token", "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": us * LAYERS / 1e3, "higher_is_better": False, "scaling": "weak", "vs_baseline": None,
             "dtype": "f64", "data": "synthetic",
-            "config": {"workload": f"decode, context {args.context}, 16 layers, 4 KV / 24 q heads, head_dim 256"},
+            "config": workload_config(args.context, int(os.environ.get("WORLD_SIZE", "1"))),
             "cpu_baseline": {"value": us, "unit": "us/layer-token", "cores": 1, "kind": "oracle", "sample": desc},
             "e2e": {"value": us, "unit": "us/layer-token", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line))
@@ -740,15 +753,12 @@ def main():
 
     if rank == 0:
         line = {
-            "metric": "decode attn us/layer-token and achieved HBM GB/s vs peak (4-bit KV)",
+            "metric": METRIC,
             "value": us_per_lt, "unit": "us/layer-token", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": False,
             "scaling": "weak", "vs_baseline": None, "dtype": "int4 codes + fp16 scales; f16 MMA, fp32 accumulate",
             "data": "synthetic",
-            "config": {"workload": f"single-sequence decode, context {args.context} (T={args.context + 1}), "
-                                   f"16 layers, 4 KV / 24 q heads, head_dim 256, bf16 inputs, 5% Student-t(3)x10 "
-                                   f"channels", "l2": "16 layer caches exceed L2 (no flush needed)",
-                       "parallelism": f"replicas x{world}"},
+            "config": workload_config(args.context, world),
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                          "traffic": TRAFFIC_BYTES.get(args.context), "bytes_per_launch": bytes_per_launch,
                          "kernel": "decode_q4_round_kernel",
