@@ -167,8 +167,9 @@ def test_window_full_size_equals_plain_rows(K):
 
 
 def test_fp8_latent_decode_full_size(K):
-    """The fp8 row: 262144 latent rows (512 + 64), 128 heads, split-T + merge;
-    8 of the 128 heads checked (one KV head: every head reads it)."""
+    """The fp8 rows: 262144 latent rows (512 + 64), 128 heads, split-T + merge,
+    dense and over 2048 selected rows; 8 of the 128 heads checked (one KV head:
+    every head reads it)."""
     Tf, Hf, DL, R = 262144, 128, 512, 64
     npg = Tf // PS
     g = K.Cache(K.FMT_FP8_ROW, 1, DL, PS, npg, device=DEV, rope_dim=R)
@@ -187,3 +188,9 @@ def test_fp8_latent_decode_full_size(K):
     heads = [0, 17, 40, 63, 64, 90, 101, 127]
     ref = O.decode(o, q[:, heads].cpu().numpy(), [Tf], bt.cpu().numpy(), sm)
     assert_close(out[0, heads], ref[0], "fp8 decode at 262144")
+    # the gather row: 2048 selected absolute rows of the 262144 (split-T partials + merge)
+    sel = synth.distinct_sorted(2048, Tf, 21, "sel").to(torch.int32).to(DEV).reshape(1, -1)
+    wsg = K.alloc_workspace(g, 1, Hf, Tf, n_sel=2048, device=DEV)
+    outg = K.decode(g, q, seq, bt, Tf, sm, wsg, sel=sel).cpu().numpy()
+    refg = O.decode(o, q[:, heads].cpu().numpy(), [Tf], bt.cpu().numpy(), sm, sel=sel.cpu().numpy())
+    assert_close(outg[0, heads], refg[0], "fp8 gather of 2048 rows at 262144")
