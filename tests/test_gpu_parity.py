@@ -473,6 +473,24 @@ def test_decode_window_equals_plain_rows(K, T0, R):
         assert_close(out_p[i], ref[i], what=f"window row {i}")
 
 
+def test_decode_window_q4_0(K):
+    """Windows over the unrotated 4-bit rows: the queries used as given, the rows
+    bit-identical to the plain decode and close to the oracle."""
+    T0, R = 900, 5
+    g, o, bt, _, _ = decode_case(K, [T0 + R], fmt=K.FMT_Q4_0, seed=55)
+    q = synth.heavy_tailed((R, 24, 256), "cpu", "win0")
+    lens = [T0 + i + 1 for i in range(R)]
+    ml = T0 + R
+    dev_bt = torch.from_numpy(bt).to(DEV)
+    ws_w = K.alloc_workspace(g, R, 24, ml, device=DEV)
+    out_w = K.decode_window_causal(g, q.to(DEV), T0, dev_bt[0], 1 / 16, ws_w)
+    out_p, _ = run_decode(K, g, np.repeat(bt, R, axis=0), q, lens, ml, 1 / 16)
+    assert np.array_equal(out_w.cpu().numpy(), out_p)
+    ref = O.decode(o, to_np_in(q), lens, np.repeat(bt, R, axis=0), 1 / 16)
+    for i in range(R):
+        assert_close(out_p[i], ref[i], what=f"Q4_0 window row {i}")
+
+
 @pytest.mark.parametrize("Hk,Hq,R", [(1, 8, 4), (1, 8, 9), (3, 9, 7), (2, 2, 33)])
 def test_decode_window_gqa_groups(K, Hk, Hq, R):
     """Windows over other GQA group sizes (8: 4 rows fill the 4 column tiles; 3:
