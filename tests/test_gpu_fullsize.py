@@ -209,3 +209,57 @@ def test_fp8_latent_full_size(K):
     out4 = K.decode(c, q, seq, bt, Tf, sm, ws4, sel=torch.from_numpy(sel4).to(dev)).cpu().numpy()
     ref4 = O.decode(oc, q.cpu().numpy()[:, :8], [Tf], bt.cpu().numpy(), sm, sel=sel4)
     close(out4[0, :8], ref4[0], "fp8 gather of 4096 rows (the maximum)")
+
+
+def test_decode_tq4_262k_context(K):
+    """The TQ4 row at 262,145 keys: KV head 3 (query heads 18..23) against the
+    oracle; the sampled head's codes and scales bit-exact."""
+    dev = "cuda"
+    seed = 1241
+    T = 262145
+    n_pages = (T + PS - 1) // PS
+    signs = synth.sign_mask(D, seed, "tq4")
+    c = K.Cache(K.FMT_TQ4, HK, D, PS, n_pages, device=dev, signs=signs)
+    oc = O.Cache(O.TQ4, 1, D, PS, n_pages, signs=signs.numpy().view(np.uint32))
+    kvh = 3
+    for s0 in range(0, T, 65536):
+        n = min(65536, T - s0)
+        k = synth.heavy_tailed((n, HK, D), dev, seed, "k", s0, subset=(seed, "k"))
+        v = synth.heavy_tailed((n, HK, D), dev, seed, "v", s0, subset=(seed, "v"))
+        sl = np.arange(s0, s0 + n, dtype=np.int32)
+        K.store(c, k, v, torch.from_numpy(sl).to(dev))
+        O.store(oc, bits16(k[:, kvh])[:, None], bits16(v[:, kvh])[:, None], sl)
+    assert np.array_equal(c.k[:, kvh].cpu().numpy(), oc.k[:, 0])
+    assert np.array_equal(bits16(c.v_scale[:, kvh]), oc.v_scale[:, 0])
+    q = synth.heavy_tailed((1, HQ, D), dev, seed, "q")
+    bt = torch.arange(n_pages, dtype=torch.int32, device=dev).reshape(1, -1)
+    seq = torch.tensor([T], dtype=torch.int32, device=dev)
+    ws = K.alloc_workspace(c, 1, HQ, T, device=dev)
+    out = K.decode(c, q, seq, bt, T, 1 / 16, ws).cpu().numpy()
+    ref = O.decode(oc, bits16(q)[:, 18:24], [T], bt.cpu().numpy(), 1 / 16)
+    close(out[0, 18:24], ref[0], "TQ4 262K decode, KV head 3")
+
+
+def test_window_262k_equals_plain_rows(K):
+    """The window row: 4 draft rows at positions 262144 .. 262147 of one sequence
+    equal the same rows decoded as 4 sequences, bit for bit."""
+    dev = "cuda"
+    seed = 1242
+    R, T0 = 4, 262144
+    T = T0 + R
+    n_pages = (T + PS - 1) // PS
+    c = K.Cache(K.FMT_Q4_HAD32, HK, D, PS, n_pages, device=dev)
+    for s0 in range(0, T, 65536):
+        n = min(65536, T - s0)
+        k = synth.heavy_tailed((n, HK, D), dev, seed, "k", s0, subset=(seed, "k"))
+        v = synth.heavy_tailed((n, HK, D), dev, seed, "v", s0, subset=(seed, "v"))
+        K.store(c, k, v, torch.arange(s0, s0 + n, dtype=torch.int32, device=dev))
+    q = synth.heavy_tailed((R, HQ, D), dev, seed, "q")
+    bt = torch.arange(n_pages, dtype=torch.int32, device=dev)
+    ws_w = K.alloc_workspace(c, R, HQ, T, device=dev)
+    out_w = K.decode_window_causal(c, q, T0, bt, 1 / 16, ws_w)
+    lens = torch.arange(T0 + 1, T + 1, dtype=torch.int32, device=dev)
+    ws_p = K.alloc_workspace(c, R, HQ, T, device=dev)
+    out_p = K.decode(c, q, lens, bt.reshape(1, -1).repeat(R, 1).contiguous(), T, 1 / 16, ws_p)
+    torch.cuda.synchronize()
+    assert torch.equal(out_w, out_p)
