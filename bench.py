@@ -54,7 +54,7 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-rows", action="store_true", help="skip the other hot-path rows (batched decode, prefill, "
                     "fp8, bf16 cache, store)")
-    ap.add_argument("--only", choices=["batched", "prefill", "fp8", "bf16", "q4_0", "window", "tq4", "fp8_prefill"], default=None,
+    ap.add_argument("--only", choices=["batched", "prefill", "fp8", "bf16", "q4_0", "window", "tq4", "fp8_prefill", "fused_merge"], default=None,
                     help="run only one of the other hot-path rows and print its measurement (for profiling)")
     ap.add_argument("--layers", type=int, default=16, help="layers per step (16 for the benchmark; fewer "
                     "only to profile a small case)")
@@ -372,6 +372,8 @@ def measure_rows(K, synth, torch, dev, peak, tflops_peak, only=None):
         out.update(_row_tq4(K, synth, torch, dev, peak, seed))
     if want("fp8_prefill"):
         out.update(_row_fp8_prefill(K, synth, torch, dev, seed))
+    if want("fused_merge"):
+        out.update(_row_fused_merge(K, synth, torch, dev, seed))
     return out
 
 
@@ -618,6 +620,40 @@ def _row_tq4(K, synth, torch, dev, peak, seed):
                              "step_us": step_ms * 1e3, "store_4096_tokens_us": st_ms * 1e3,
                              "kernel": "decode_q4_round_kernel<TQ4> (prmt level tables, movmatrix for V)"}
     del c, ws
+    torch.cuda.empty_cache()
+    return out
+
+
+def _row_fused_merge(K, synth, torch, dev, seed):
+    """Decode + merge as two launches against one launch whose last CTA per
+    (sequence, KV head) merges (kvq_decode_merged), at 32769 and 262145 keys of
+    one sequence, one layer."""
+    out = {}
+    T = 262145
+    npg = (T + PS - 1) // PS
+    c = K.Cache(K.FMT_Q4_HAD32, HK, D, PS, npg, device=dev)
+    for s0 in range(0, T, 65536):
+        n = min(65536, T - s0)
+        k = synth.heavy_tailed((n, HK, D), dev, seed, "fmk", s0, subset=(seed, "k"))
+        v = synth.heavy_tailed((n, HK, D), dev, seed, "fmv", s0, subset=(seed, "v"))
+        K.store(c, k, v, torch.arange(s0, s0 + n, dtype=torch.int32, device=dev))
+    q = K.rotate_query(synth.heavy_tailed((1, HQ, D), dev, seed, "fmq"))
+    bt = torch.arange(npg, dtype=torch.int32, device=dev).reshape(1, -1)
+    o = torch.empty((1, HQ, D), dtype=torch.float32, device=dev)
+    for Tq in (32769, 262145):
+        seq = torch.tensor([Tq], dtype=torch.int32, device=dev)
+        ws = K.alloc_workspace(c, 1, HQ, Tq, device=dev)
+
+        def two():
+            K.decode_attn(c, q, seq, bt, Tq, 1 / 16, ws)
+            K.merge(c, ws, 1, HQ, seq, Tq, o)
+
+        two_ms = _events_time(torch, two, 20)
+        one_ms = _events_time(torch, lambda: K.decode_merged(c, q, seq, bt, Tq, 1 / 16, ws, out=o), 20)
+        out[f"fused_merge_{Tq - 1}"] = {"workload": f"one sequence, {Tq} keys, 1 layer",
+                                         "decode_then_merge_us": two_ms * 1e3, "decode_merged_us": one_ms * 1e3,
+                                         "kernel": "decode_q4_round_kernel with the last-CTA merge"}
+    del c
     torch.cuda.empty_cache()
     return out
 

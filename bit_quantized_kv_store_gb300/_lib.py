@@ -48,6 +48,8 @@ SIGNATURES = {
     "kvq_decode_attn": (_I32, [ctypes.POINTER(CacheDesc), _P, _I32, _I32, _P, _P, _I32, _I32, _P, _I32, _F, _P,
                                _SZ, _P]),
     "kvq_decode_window": (_I32, [ctypes.POINTER(CacheDesc), _P, _I32, _I32, _P, _P, _I32, _I32, _F, _P, _SZ, _P]),
+    "kvq_decode_merged": (_I32, [ctypes.POINTER(CacheDesc), _P, _I32, _I32, _P, _P, _I32, _I32, _F, _P, _SZ, _P,
+                                 _P]),
     "kvq_decode_attn_unrotated": (_I32, [ctypes.POINTER(CacheDesc), _P, _I32, _I32, _I32, _P, _P, _I32, _I32, _P,
                                          _I32, _F, _P, _SZ, _P]),
     "kvq_merge": (_I32, [ctypes.POINTER(CacheDesc), _P, _SZ, _I32, _I32, _P, _I32, _I32, _I32, _P, _P]),
@@ -221,6 +223,19 @@ def decode_attn(cache: Cache, q, seq_lens, block_tables, max_seq_len, sm_scale, 
     _check(lib().kvq_decode_attn(cache.ref, _ptr(q), B, Hq, _ptr(seq_lens), _ptr(block_tables),
                                  block_tables.shape[1], max_seq_len, _ptr(sel), n_sel, float(sm_scale),
                                  _ptr(workspace), workspace.numel(), _stream(stream)), "kvq_decode_attn")
+
+
+def decode_merged(cache: Cache, q_rot, seq_lens, block_tables, max_seq_len, sm_scale, workspace, out=None,
+                  stream=None):
+    """Decode partials and their merge in one launch (4-bit formats); q_rot as for
+    decode_attn.  Returns out [B, Hq, 256]."""
+    B, Hq = q_rot.shape[0], q_rot.shape[1]
+    if out is None:
+        out = torch.empty((B, Hq, cache.D), dtype=torch.float32, device=q_rot.device)
+    _check(lib().kvq_decode_merged(cache.ref, _ptr(q_rot), B, Hq, _ptr(seq_lens), _ptr(block_tables),
+                                   block_tables.shape[1], max_seq_len, float(sm_scale), _ptr(workspace),
+                                   workspace.numel(), _ptr(out), _stream(stream)), "kvq_decode_merged")
+    return out
 
 
 def decode_window(cache: Cache, q_rot, row_lens, block_table, max_seq_len, sm_scale, workspace, stream=None):

@@ -87,7 +87,7 @@ static bool encode_rows_map(CUtensorMap* m, const void* base, uint64_t rows, uin
 }
 
 struct WsLayout {
-  size_t m_off, z_off, acc_off, total;
+  size_t m_off, z_off, acc_off, ctr_off, total;
   int P;
   int part;  // keys per partition
 };
@@ -105,7 +105,9 @@ static WsLayout ws_layout(const kvq_cache* c, int B, int Hq, int max_seq_len, in
   w.m_off = 256;
   w.z_off = w.m_off + round256(n * sizeof(float));
   w.acc_off = w.z_off + round256(n * sizeof(float));
-  w.total = w.acc_off + round256(n * value_width(c) * sizeof(float));
+  w.ctr_off = w.acc_off + round256(n * value_width(c) * sizeof(float));
+  // completion counters of the fused merge, one per (sequence, KV head)
+  w.total = w.ctr_off + round256(static_cast<size_t>(B) * c->num_kv_heads * sizeof(int32_t));
   return w;
 }
 
@@ -240,7 +242,7 @@ static int32_t decode_attn_impl(const kvq_cache* cache, const float* q, const vo
                                 int32_t num_seqs, int32_t num_q_heads, const int32_t* d_seq_lens,
                                 const int32_t* d_block_tables, int32_t max_pages_per_seq, int32_t max_seq_len,
                                 const int32_t* d_sel, int32_t n_sel, float sm_scale, void* workspace, size_t ws_bytes,
-                                void* stream, bool window = false) {
+                                void* stream, bool window = false, float* fused_out = nullptr) {
   int32_t st = check_cache(cache);
   if (st != KVQ_OK) return st;
   st = check_decode_shape(cache, num_seqs, num_q_heads, d_seq_lens, max_seq_len, d_sel != nullptr, n_sel);
@@ -282,6 +284,8 @@ static int32_t decode_attn_impl(const kvq_cache* cache, const float* q, const vo
     a.ws_acc = reinterpret_cast<float*>(ws + w.acc_off);
     a.P = w.P;
     a.part = w.part;
+    a.fused_out = fused_out;
+    a.merge_ctr = reinterpret_cast<int32_t*>(ws + w.ctr_off);
     a.status = reinterpret_cast<int32_t*>(ws);
     if (!d_sel) {
       const uint64_t rows = static_cast<uint64_t>(cache->num_pages) * cache->num_kv_heads * cache->page_size;
@@ -307,6 +311,21 @@ int32_t kvq_decode_attn(const kvq_cache* cache, const float* q, int32_t num_seqs
                         size_t ws_bytes, void* stream) {
   return decode_attn_impl(cache, q, nullptr, 0, num_seqs, num_q_heads, d_seq_lens, d_block_tables,
                           max_pages_per_seq, max_seq_len, d_sel, n_sel, sm_scale, workspace, ws_bytes, stream);
+}
+
+int32_t kvq_decode_merged(const kvq_cache* cache, const float* q, int32_t num_seqs, int32_t num_q_heads,
+                          const int32_t* d_seq_lens, const int32_t* d_block_tables, int32_t max_pages_per_seq,
+                          int32_t max_seq_len, float sm_scale, void* workspace, size_t ws_bytes, float* out,
+                          void* stream) {
+  if (!cache) return KVQ_ERR_INVALID_ARG;
+  if (!is_q4(cache->format)) return KVQ_ERR_UNSUPPORTED;
+  if (num_seqs > 0 && !out) return KVQ_ERR_INVALID_ARG;
+  // the last CTA keeps its group's partition weights in its 32 KB of ring buffers
+  const int64_t parts = (static_cast<int64_t>(max_seq_len) + kPart - 1) / kPart;
+  if (cache->num_kv_heads > 0 && num_q_heads > 0 && parts * (num_q_heads / cache->num_kv_heads) > 8192)
+    return KVQ_ERR_UNSUPPORTED;
+  return decode_attn_impl(cache, q, nullptr, 0, num_seqs, num_q_heads, d_seq_lens, d_block_tables, max_pages_per_seq,
+                          max_seq_len, nullptr, 0, sm_scale, workspace, ws_bytes, stream, false, out);
 }
 
 int32_t kvq_decode_window(const kvq_cache* cache, const float* q, int32_t num_rows, int32_t num_q_heads,

@@ -310,6 +310,7 @@ struct __align__(1024) Q4Smem {
   uint64_t vfull;                   // the round's V tiles landed (kQ4RoundTiles arrivals)
   uint64_t vempty;                  // every warp is done with the round's V (kQ4Warps arrivals)
   int poison;
+  int last;  // fused merge: this CTA finished its (sequence, KV head) last
 };
 // The unrotated-query entry point rotates the group's queries (8 heads x 256
 // fp32) into V tiles 0..3, which are first filled after the prologue.
@@ -394,6 +395,84 @@ __device__ __forceinline__ bool q4_issue_own(const DecodeArgs& a, int b, int kvh
   return bad;
 }
 
+// The fused merge (kvq_decode_merged): run by the last CTA of a (sequence b, KV
+// head) to finish, once every partial of the group is in memory.  Warp w
+// reduces heads 2w, 2w + 1: the maximum M over the partitions, the weights
+// 2^(m_p - M) (into `wts`) and Z = sum_p z_p 2^(m_p - M), in a fixed order.
+// Then thread i takes dims 2i, 2i + 1 of every head: o = sum_p acc_p w_p / Z in
+// ascending p, rotated back per 32-group (Q4_HAD32) and stored.
+__device__ __forceinline__ void q4_fused_merge(const DecodeArgs& a, int b, int kvh, int np, float* wts, float* zsum,
+                                               bool rotate_back) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int hh = 0; hh < 2; ++hh) {
+    const int h = 2 * warp + hh;
+    if (h >= a.group) break;
+    const int64_t base = ((int64_t)b * a.Hq + kvh * a.group + h) * a.P;
+    float M = -INFINITY;
+    bool nan_seen = false;
+    for (int p = lane; p < np; p += 32) {
+      const float m = __ldcg(a.ws_m + base + p);
+      nan_seen |= isnan(m);
+      M = fmaxf(M, m);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+    nan_seen = __any_sync(0xffffffffu, nan_seen);
+    float Z = 0.f;
+    for (int p = lane; p < np; p += 32) {
+      const float m = __ldcg(a.ws_m + base + p);
+      const float w = (M == -INFINITY) ? 0.f : exp2f(m - M);
+      wts[h * np + p] = w;
+      Z = fmaf(__ldcg(a.ws_z + base + p), w, Z);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) Z += __shfl_xor_sync(0xffffffffu, Z, o);
+    if (lane == 0) zsum[h] = nan_seen ? NAN : Z;
+  }
+  __syncthreads();
+  const int i = threadIdx.x;  // dims 2i, 2i + 1
+  for (int h = 0; h < a.group; ++h) {
+    const int64_t base = ((int64_t)b * a.Hq + kvh * a.group + h) * a.P;
+    const float* accp = a.ws_acc + base * kQ4D + 2 * i;
+    float2 o = make_float2(0.f, 0.f);
+    int p = 0;
+    for (; p + 8 <= np; p += 8) {  // eight loads in flight
+      float2 v[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) v[k] = __ldcg(reinterpret_cast<const float2*>(accp + (int64_t)(p + k) * kQ4D));
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        o.x = fmaf(v[k].x, wts[h * np + p + k], o.x);
+        o.y = fmaf(v[k].y, wts[h * np + p + k], o.y);
+      }
+    }
+    for (; p < np; ++p) {
+      const float2 v = __ldcg(reinterpret_cast<const float2*>(accp + (int64_t)p * kQ4D));
+      o.x = fmaf(v.x, wts[h * np + p], o.x);
+      o.y = fmaf(v.y, wts[h * np + p], o.y);
+    }
+    const float Z = zsum[h];
+    const bool empty = !(Z > 0.f) && !isnan(Z);
+    float x0 = empty ? 0.f : o.x / Z, x1 = empty ? 0.f : o.y / Z;
+    if (rotate_back) {
+      // 32-point butterfly of the group: dims 2i, 2i + 1 here, the other 30 in
+      // the 15 neighbouring lanes (lane bits 0-3)
+      float a0 = x0 + x1, a1 = x0 - x1;
+#pragma unroll
+      for (int o2 = 1; o2 < 16; o2 <<= 1) {
+        const float p0 = __shfl_xor_sync(0xffffffffu, a0, o2), p1 = __shfl_xor_sync(0xffffffffu, a1, o2);
+        const bool upper = (lane & o2) != 0;
+        a0 = upper ? p0 - a0 : a0 + p0;
+        a1 = upper ? p1 - a1 : a1 + p1;
+      }
+      x0 = __fmul_rn(a0, kHadamardScale);
+      x1 = __fmul_rn(a1, kHadamardScale);
+    }
+    *reinterpret_cast<float2*>(a.fused_out + ((int64_t)b * a.Hq + kvh * a.group + h) * kQ4D + 2 * i) =
+        make_float2(x0, x1);
+  }
+}
+
 // One CTA per (partition, KV head, column set).  NT column tiles of 8 columns
 // face the keys on the MMA's N side.  A plain decode (WIN = false, NT = 1) gives
 // the columns to the heads of one sequence's GQA group.  A decode window
@@ -401,12 +480,13 @@ __device__ __forceinline__ bool q4_issue_own(const DecodeArgs& a, int b, int kvh
 // sequence, row-major: the rows share the block table and so every key, whose
 // codes are then converted once for all of them; each row keeps its own causal
 // end (its length), its own softmax state and its own partials.
-template <bool GATHER, int NT, bool WIN, bool TQ = false>
+template <bool GATHER, int NT, bool WIN, bool TQ = false, bool LM = false>
 __global__ void __launch_bounds__(kQ4Warps * 32, q4_min_blocks(NT))
     decode_q4_round_kernel(const __grid_constant__ DecodeArgs a) {
   static_assert(!(WIN && GATHER), "decode windows read dense prefixes");
   static_assert(WIN || NT == 1, "one sequence's group fills one column tile");
   static_assert(!TQ || (!GATHER && !WIN), "TQ4 rows: dense single-sequence decode");
+  static_assert(!LM || (!GATHER && !WIN && !TQ), "the fused merge: dense 4-bit decode");
   extern __shared__ uint8_t smem_raw[];
   // 1024-byte alignment for the swizzled tiles (the launch adds 1 KB of slack)
   Q4Smem<NT, GATHER>& sm =
@@ -491,6 +571,13 @@ __global__ void __launch_bounds__(kQ4Warps * 32, q4_min_blocks(NT))
   }
 
   pdl_wait();
+  if constexpr (LM) {
+    // no partition will count in: partition 0's CTA writes the outputs itself
+    // (NaN for an invalid length, zeros for an empty sequence)
+    if ((bad_len || nparts == 0) && p == 0)
+      for (int i = threadIdx.x; i < a.group * kQ4D; i += kQ4Warps * 32)
+        a.fused_out[((int64_t)b * a.Hq + kvh * a.group) * kQ4D + i] = bad_len ? NAN : 0.f;
+  }
   if (bad_len) {
     if (threadIdx.x == 0 && p == 0 && kvh == 0) set_status(a.status, KVQ_DEV_BAD_LENGTH);
     return;  // the merge writes NaN for this sequence
@@ -946,13 +1033,30 @@ __global__ void __launch_bounds__(kQ4Warps * 32, q4_min_blocks(NT))
         }
     }
   }
+  if constexpr (LM) {
+    // every thread's partials are visible device-wide before the count
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      const int done = atomicAdd(a.merge_ctr + (int64_t)b * a.c.num_kv_heads + kvh, 1);
+      sm.last = done == nparts - 1;
+    }
+    __syncthreads();
+    if (sm.last) {
+      __threadfence();
+      // the ring buffers are free now: weights [group][nparts], sums [group]
+      q4_fused_merge(a, b, kvh, nparts, reinterpret_cast<float*>(&sm.kc[0][0][0]), &sm.red[0][0],
+                     a.q_rotate != 0);
+      if (threadIdx.x == 0) a.merge_ctr[(int64_t)b * a.c.num_kv_heads + kvh] = 0;  // ready for the next launch
+    }
+  }
   pdl_trigger();  // after this CTA's last write
 }
 
-template <bool GATHER, int NT, bool WIN, bool TQ = false>
+template <bool GATHER, int NT, bool WIN, bool TQ = false, bool LM = false>
 cudaError_t launch_round(const DecodeArgs& a, dim3 grid, cudaStream_t s) {
   const size_t smem = sizeof(Q4Smem<NT, GATHER>) + 1024;  // + slack for the 1024-byte alignment
-  auto kern = decode_q4_round_kernel<GATHER, NT, WIN, TQ>;
+  auto kern = decode_q4_round_kernel<GATHER, NT, WIN, TQ, LM>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   e = launch_pdl(kern, grid, dim3(kQ4Warps * 32), smem, s, a);
@@ -967,6 +1071,7 @@ cudaError_t launch_decode_q4(const DecodeArgs& a, int B, cudaStream_t s) {
   if (a.nrows <= 0) {
     const dim3 grid(a.P, a.c.num_kv_heads, B);
     if (a.tq) return a.sel ? cudaErrorInvalidValue : launch_round<false, 1, false, true>(a, grid, s);
+    if (a.fused_out) return a.sel ? cudaErrorInvalidValue : launch_round<false, 1, false, false, true>(a, grid, s);
     return a.sel ? launch_round<true, 1, false>(a, grid, s) : launch_round<false, 1, false>(a, grid, s);
   }
   if (a.tq) return cudaErrorInvalidValue;

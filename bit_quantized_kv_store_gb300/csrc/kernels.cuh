@@ -46,6 +46,10 @@ struct DecodeArgs {
   // keys 0 .. prefill_q0 + b (seq_lens unused); 0: decode
   int prefill;
   int prefill_q0;
+  // 4-bit decode with the fused merge: the merged outputs [B][Hq][256] and the
+  // per-(sequence, KV head) completion counters (zero between launches)
+  float* fused_out;
+  int32_t* merge_ctr;
 };
 
 // Log-sum-exp merge of the partials (merge.cu).

@@ -194,7 +194,10 @@ int32_t kvq_store_rotate(const kvq_cache* cache, const void* k, const void* v, i
 /* Size in bytes of the workspace kvq_decode_attn needs for this problem:
  * a 256-byte header (status word at offset 0), then partial maxima m and sums z
  * [num_seqs][num_q_heads][P] f32 and partial contexts acc [num_seqs][num_q_heads]
- * [P][value width] f32, where P = ceil(max(max_seq_len, n_sel) / 512). */
+ * [P][value width] f32, where P = ceil(max(max_seq_len, n_sel) / 512), then the
+ * completion counters of kvq_decode_merged [num_seqs][num_kv_heads] int32 (zero
+ * before the first kvq_decode_merged on the workspace; each complete call
+ * leaves them zero). */
 size_t kvq_decode_workspace_size(const kvq_cache* cache, int32_t num_seqs, int32_t num_q_heads,
                                  int32_t max_seq_len, int32_t n_sel);
 
@@ -242,6 +245,23 @@ int32_t kvq_decode_attn(const kvq_cache* cache, const float* q, int32_t num_seqs
  *   4-bit formats only (else KVQ_ERR_UNSUPPORTED); 1 <= num_rows <= 64.
  * Workspace (kvq_decode_workspace_size with num_seqs = num_rows) and errors as
  * for kvq_decode_attn. */
+/* kvq_decode_merged -- kvq_decode_attn and kvq_merge (with the rotation back for
+ * Q4_HAD32) in one launch ([P1] "What it is": the shared 512-key chunks and the
+ * in-order merge of one decode round): the last CTA of each (sequence, KV head)
+ * to finish, counted in the workspace, merges that group's partials in
+ * ascending partition order and writes out [num_seqs, num_q_heads, 256] fp32.
+ * The merged values equal kvq_merge's up to the order of the fp32 sums.  The
+ * merge of a group then runs in one CTA, so this is slower than the two
+ * launches once a group has many partitions.
+ *   Arguments as for kvq_decode_attn (dense; 4-bit formats, else
+ *   KVQ_ERR_UNSUPPORTED); ceil(max_seq_len / 512) * (num_q_heads /
+ *   num_kv_heads) <= 8192.  An invalid length gives NaN rows (and
+ *   KVQ_DEV_BAD_LENGTH), an empty sequence zeros. */
+int32_t kvq_decode_merged(const kvq_cache* cache, const float* q, int32_t num_seqs, int32_t num_q_heads,
+                          const int32_t* d_seq_lens, const int32_t* d_block_tables, int32_t max_pages_per_seq,
+                          int32_t max_seq_len, float sm_scale, void* workspace, size_t ws_bytes, float* out,
+                          void* stream);
+
 int32_t kvq_decode_window(const kvq_cache* cache, const float* q, int32_t num_rows, int32_t num_q_heads,
                           const int32_t* d_row_lens, const int32_t* d_block_table, int32_t max_pages,
                           int32_t max_seq_len, float sm_scale, void* workspace, size_t ws_bytes, void* stream);

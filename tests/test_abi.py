@@ -93,7 +93,9 @@ def test_workspace_geometry(K):
         P = -(-T // 512)
         n = B * Hq * P
         r = lambda x: (x + 255) // 256 * 256
-        assert L.kvq_decode_workspace_size(ctypes.byref(d), B, Hq, T, 0) == 256 + 2 * r(4 * n) + r(4 * n * 256)
+        # header, m and z, acc, then one completion counter per (sequence, KV head)
+        assert L.kvq_decode_workspace_size(ctypes.byref(d), B, Hq, T, 0) == \
+            256 + 2 * r(4 * n) + r(4 * n * 256) + r(4 * B * d.num_kv_heads)
 
 
 def test_plane_bytes_match_page_figures(K):

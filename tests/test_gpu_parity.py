@@ -622,6 +622,37 @@ def test_bounded_wait_ends_with_timeout_status(K):
     assert_close(out[0], O.decode(o, to_np_in(q), lens, bt, 1 / 16)[0], what="decode after the timeout")
 
 
+@pytest.mark.parametrize("fmt", ["Q4", "Q4_0"])
+def test_decode_merged_equals_decode_then_merge(K, fmt):
+    """The fused decode + last-CTA merge: close to the two-launch path and to the
+    oracle, for several sequences (one invalid, one empty), twice on the same
+    workspace (the completion counters return to zero)."""
+    f = K.FMT_Q4_HAD32 if fmt == "Q4" else K.FMT_Q4_0
+    lens = [1500, 513, 40, 0, 2049]
+    g, o, bt, q, ml = decode_case(K, lens, fmt=f, seed=77)
+    qd = q.to(DEV)
+    qr = K.rotate_query(qd) if f == K.FMT_Q4_HAD32 else qd.float()
+    seq = torch.tensor(lens, dtype=torch.int32, device=DEV)
+    dbt = torch.from_numpy(bt).to(DEV)
+    ws = K.alloc_workspace(g, len(lens), 24, ml, device=DEV)
+    ref2, _ = run_decode(K, g, bt, q, lens, ml, 1 / 16)
+    ref = O.decode(o, to_np_in(q), lens, bt, 1 / 16)
+    for _ in range(2):
+        out = K.decode_merged(g, qr, seq, dbt, ml, 1 / 16, ws).cpu().numpy()
+        assert K.read_status(ws) == 0
+        for b, L in enumerate(lens):
+            if L == 0:
+                assert np.all(out[b] == 0)
+                continue
+            assert_close(out[b], ref[b], what=f"merged seq {b}")
+            assert np.abs(out[b] - ref2[b]).max() <= 1e-5 * np.abs(ref2[b]).max()
+    bad = torch.tensor([1500, 5000, 40, 0, 2049], dtype=torch.int32, device=DEV)
+    out = K.decode_merged(g, qr, bad, dbt, ml, 1 / 16, ws).cpu().numpy()
+    assert K.read_status(ws) & K.DEV_BAD_LENGTH
+    assert np.isnan(out[1]).all()
+    assert_close(out[0], ref[0], what="merged seq 0 next to an invalid one")
+
+
 def test_decode_bf16_cache(K):
     lens = [1500, 513, 20]
     g, o, bt, q, ml = decode_case(K, lens, fmt=K.FMT_BF16, seed=8)
