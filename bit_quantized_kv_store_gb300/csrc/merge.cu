@@ -9,8 +9,7 @@
 // pass over the partials.  Thread (row r = tid / 8, chunk c = tid % 8) takes
 // partitions r, r + 32, r + 64, ... in ascending order: it loads their m (and,
 // for c == 0, z) and the float4 chunk c of their acc, four partitions per
-// batch (eight beyond 128 partitions) with every load of a batch issued
-// before any use, and keeps a running
+// batch with every load of a batch issued before any use, and keeps a running
 // (M_t, Z_t, acc_t) rescaled to its own maximum.  The 32 row-threads' partials
 // are then combined in a fixed tree, so the result does not depend on
 // scheduling (bit-reproducible), and the 32 values of the CTA -- exactly one
@@ -18,8 +17,6 @@
 // spans the whole row, so their rotation back is a second launch, tq4.cu.)
 // The number of keys per partition comes with the arguments: 512, or for the
 // fp8 streaming prefill one partition per row, whose length is q_start + row + 1.
-#include <type_traits>
-
 #include "kernels.cuh"
 
 namespace kvq {
@@ -62,16 +59,11 @@ __global__ void __launch_bounds__(256) merge_kernel(const MergeArgs a) {
   float Mt = -INFINITY, Zt = 0.f;
   float4 At = make_float4(0.f, 0.f, 0.f, 0.f);
   int nan_seen = 0;
-  // kBatch partitions per thread have their loads in flight together: 8 for long
-  // sequences (fewer dependent L2 round trips), 4 for short ones (fewer
-  // instructions); the order in which a thread combines them is the same.
-  auto walk = [&](auto batch_tag) {
-  constexpr int kBatch = decltype(batch_tag)::value;
-  for (int i0 = row; i0 < np; i0 += kBatch * 32) {
-    float mv[kBatch], zv[kBatch];
-    float4 av[kBatch];
+  for (int i0 = row; i0 < np; i0 += 4 * 32) {
+    float mv[4], zv[4];
+    float4 av[4];
 #pragma unroll
-    for (int k = 0; k < kBatch; ++k) {  // all loads of the batch first
+    for (int k = 0; k < 4; ++k) {  // all loads of the batch first
       const int i = i0 + 32 * k;
       mv[k] = -INFINITY;
       zv[k] = 0.f;
@@ -83,7 +75,7 @@ __global__ void __launch_bounds__(256) merge_kernel(const MergeArgs a) {
       }
     }
 #pragma unroll
-    for (int k = 0; k < kBatch; ++k) {
+    for (int k = 0; k < 4; ++k) {
       if (i0 + 32 * k >= np) break;
       nan_seen |= isnan(mv[k]);
       const float Mn = fmaxf(Mt, mv[k]);
@@ -97,11 +89,6 @@ __global__ void __launch_bounds__(256) merge_kernel(const MergeArgs a) {
       Mt = Mn;
     }
   }
-  };
-  if (np > 4 * 32)
-    walk(std::integral_constant<int, 8>{});
-  else
-    walk(std::integral_constant<int, 4>{});
   nan_seen = __any_sync(0xffffffffu, nan_seen);
   __syncthreads();  // s_nan initialised
   if (nan_seen && lane == 0) s_nan = 1;
