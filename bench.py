@@ -38,7 +38,7 @@ KERNELS_PER_LAYER = 3  # store + query rotation (one launch), split-T decode, me
 # DRAM bytes of one decode launch (dram__bytes_read.sum + dram__bytes_write.sum
 # from an ncu capture of the current kernel at each context); to be dropped
 # whenever the kernel changes.
-TRAFFIC_BYTES = {32768: 37866240 + 256, 262144: 302253056 + 10773504}
+TRAFFIC_BYTES = {32768: 37867008 + 0, 262144: 302277120 + 10575104}
 BYTES_PER_POS_LAYER = HK * 2 * (D // 2 + 2 * (D // 32))   # 1152
 
 
@@ -73,31 +73,115 @@ def load_peaks():
     return 6800.0, "fallback"
 
 
+# NVML clock-event reason bits (nvml.h, nvmlClocksEventReason*), mapped to the
+# names of nvidia-smi's clocks_event_reasons fields; power-brake slowdown is
+# one of the causes nvidia-smi reports as hw_slowdown.
+NVML_REASONS = ((0x8, "hw_slowdown"), (0x80, "hw_slowdown"), (0x40, "hw_thermal_slowdown"),
+                (0x20, "sw_thermal_slowdown"), (0x4, "sw_power_cap"))
+
+
+def nvml_reason_names(mask):
+    return sorted({name for bit, name in NVML_REASONS if mask & bit})
+
+
+class _Nvml:
+    """SM clock, its maximum and the clock-event reasons, read through the
+    driver's management library; one read takes microseconds."""
+
+    def __init__(self, index):
+        import ctypes
+        lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if lib.nvmlInit_v2() != 0:
+            raise OSError("nvmlInit_v2 failed")
+        self.lib, self.ct = lib, ctypes
+        self.h = ctypes.c_void_p()
+        if lib.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(index), ctypes.byref(self.h)) != 0:
+            lib.nvmlShutdown()
+            raise OSError("no NVML handle for device %d" % index)
+        self.reasons_fn = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            lib.nvmlDeviceGetCurrentClocksThrottleReasons
+        mx = ctypes.c_uint(0)
+        lib.nvmlDeviceGetMaxClockInfo(self.h, ctypes.c_int(1), ctypes.byref(mx))  # NVML_CLOCK_SM
+        self.max_mhz = float(mx.value)
+
+    def read(self):
+        ct = self.ct
+        mhz, mask = ct.c_uint(0), ct.c_ulonglong(0)
+        if self.lib.nvmlDeviceGetClockInfo(self.h, ct.c_int(1), ct.byref(mhz)) != 0:
+            return None
+        if self.reasons_fn(self.h, ct.byref(mask)) != 0:
+            return None
+        return float(mhz.value), int(mask.value)
+
+    def close(self):
+        self.lib.nvmlShutdown()
+
+
 class Clocks:
-    """Samples nvidia-smi clocks and throttle reasons while running."""
+    """Samples the SM clock and the throttle reasons.  Through NVML a thread
+    polls every half millisecond and keeps only the samples taken between
+    begin() and end() (the timed region, which at 32K lasts a few
+    milliseconds); without NVML, nvidia-smi samples every 100 ms for the whole
+    block."""
 
     def __init__(self, index=0):
         self.samples, self.proc, self.index = [], None, index
+        self.nvml, self.active, self.stop = None, False, False
+        self.source = None
 
     def __enter__(self):
+        try:
+            self.nvml = _Nvml(self.index)
+            self.source = "nvml"
+            self.t = threading.Thread(target=self._poll, daemon=True)
+            self.t.start()
+            return self
+        except (OSError, AttributeError):
+            self.nvml = None
         q = ("clocks.sm,clocks.max.sm,clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
         try:
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={q}", "--format=csv,noheader,nounits",
                                           "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.source = "nvidia-smi"
             self.t = threading.Thread(target=self._read, daemon=True)
             self.t.start()
         except OSError:
             self.proc = None
         return self
 
+    def begin(self):
+        self.active = True
+
+    def end(self):
+        self.active = False
+
+    def _poll(self):
+        while not self.stop:
+            if self.active:
+                r = self.nvml.read()
+                if r is not None:
+                    mhz, mask = r
+                    self.samples.append((mhz, self.nvml.max_mhz, nvml_reason_names(mask)))
+            time.sleep(0.0005)
+
     def _read(self):
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for line in self.proc.stdout:
             parts = [p.strip() for p in line.split(",")]
-            if len(parts) >= 6:
-                self.samples.append(parts)
+            if len(parts) < 6:
+                continue
+            try:
+                mhz, mx = float(parts[0]), float(parts[1])
+            except ValueError:
+                continue
+            self.samples.append((mhz, mx, [names[i] for i in range(4) if parts[2 + i].lower() == "active"]))
 
     def __exit__(self, *a):
+        self.stop = True
+        if self.nvml:
+            self.t.join(timeout=5)
+            self.nvml.close()
         if self.proc:
             self.proc.terminate()
             try:
@@ -106,14 +190,15 @@ class Clocks:
                 self.proc.kill()
 
     def summary(self):
-        if not self.samples:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
-        sm = [float(s[0]) for s in self.samples if s[0].replace(".", "").isdigit()]
-        mx = [float(s[1]) for s in self.samples if s[1].replace(".", "").isdigit()]
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = sorted({names[i] for s in self.samples for i in range(4) if s[2 + i].lower() == "active"})
-        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
-                "reasons": reasons, "samples": len(self.samples)}
+        return clock_summary(self.samples, self.source)
+
+
+def clock_summary(samples, source):
+    """samples: (sm MHz, max SM MHz, [active reason names]) per read."""
+    if not samples:
+        return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0, "source": source}
+    return {"sm_mhz": statistics.median(s[0] for s in samples), "sm_max_mhz": max(s[1] for s in samples),
+            "reasons": sorted({r for s in samples for r in s[2]}), "samples": len(samples), "source": source}
 
 
 def reduce_max_over_ranks(x, world, device):
@@ -212,10 +297,11 @@ def capture(torch, fn):
     return g
 
 
-def time_device(W, steps, warmup, torch):
+def time_device(W, steps, warmup, torch, clk=None):
     """Device time of `steps` steps (one graph replay each) and the average
     duration of one decode launch (a graph of the 16 layers' decode launches,
-    timed with CUDA events on the replay stream)."""
+    timed with CUDA events on the replay stream).  `clk` samples the clocks
+    from the first timed replay until the device has finished them."""
     n_in = W.new_k.shape[0]
     graphs = [capture(torch, lambda i=i: W.step(i)) for i in range(n_in)]
     dec_graph = capture(torch, W.decode_only)
@@ -223,11 +309,15 @@ def time_device(W, steps, warmup, torch):
         graphs[i % n_in].replay()
     torch.cuda.synchronize()
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if clk:
+        clk.begin()
     t0.record()
     for s in range(steps):
         graphs[s % n_in].replay()
     t1.record()
     torch.cuda.synchronize()
+    if clk:
+        clk.end()
     total_ms = t0.elapsed_time(t1)
     for _ in range(2):
         dec_graph.replay()
@@ -740,7 +830,7 @@ def main():
     W = Workload(K, synth, torch, args.context, n_inputs, 1234 + 1 + rank, dev)
     barrier()
     with Clocks(local) as clk:
-        total_ms, dec_avg_ms, launches, graphs = time_device(W, args.steps, args.warmup, torch)
+        total_ms, dec_avg_ms, launches, graphs = time_device(W, args.steps, args.warmup, torch, clk)
     barrier()
     total_ms = max_over_ranks(total_ms)
     us_per_lt = aggregate_us_per_unit(total_ms, LAYERS * args.steps, world)
@@ -759,7 +849,7 @@ def main():
         lsteps = max(3, args.steps // 4)
         barrier()
         with Clocks(local) as clk2:
-            ltot, lavg, _, lgraphs = time_device(WL, lsteps, max(3, args.warmup // 2), torch)
+            ltot, lavg, _, lgraphs = time_device(WL, lsteps, max(3, args.warmup // 2), torch, clk2)
         del lgraphs
         ltot = max_over_ranks(ltot)
         lbytes = WL.T * BYTES_PER_POS_LAYER
