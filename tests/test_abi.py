@@ -120,3 +120,80 @@ def test_product_path_has_no_oracle_or_cpu_fallback():
                 text = open(os.path.join(dirpath, f)).read()
                 assert "import oracle" not in text and "from oracle" not in text, f
                 assert "kvq_oracle" not in text, f
+
+
+def _tq4_desc(K, D=256, signs=4096):
+    return K.CacheDesc(4, 4, D, 0, 16, 4, 4096, 4096, 4096, 4096, signs)
+
+
+def test_host_validation_of_the_other_entries(K):
+    """Windows, the fused merge, unrotated queries, TQ4, the fp8 prefill, the
+    fused store + rotation and the no-allocation decode reject bad host
+    arguments with their documented codes, before anything is enqueued."""
+    L = K.lib()
+    d = _desc(K)
+    bf = _desc(K, fmt=1)
+    fp8 = _desc(K, fmt=2, Hk=1, D=512, rope=64)
+    dummy = ctypes.c_void_p(4096)
+    f = ctypes.c_float(0.1)
+    ws = L.kvq_decode_workspace_size(ctypes.byref(d), 4, 24, 1000, 0)
+    # kvq_decode_window: 4-bit formats only, at most 64 rows, workspace size
+    win = lambda c=d, rows=4, wsb=ws: (ctypes.byref(c), dummy, rows, 24, dummy, dummy, 100, 1000, f, dummy, wsb, None)
+    assert L.kvq_decode_window(None, dummy, 4, 24, dummy, dummy, 100, 1000, f, dummy, ws, None) == K.ERR_INVALID_ARG
+    assert L.kvq_decode_window(*win(c=bf)) == K.ERR_UNSUPPORTED
+    assert L.kvq_decode_window(*win(rows=65)) == K.ERR_INVALID_ARG
+    assert L.kvq_decode_window(*win(wsb=ws - 1)) == K.ERR_WORKSPACE_TOO_SMALL
+    # kvq_decode_merged: 4-bit only, an output, at most 8192 partition weights per group
+    mg = lambda c=d, out=dummy, msl=1000: (ctypes.byref(c), dummy, 1, 24, dummy, dummy, 100000, msl, f, dummy,
+                                           1 << 40, out, None)
+    assert L.kvq_decode_merged(*mg(c=fp8)) == K.ERR_UNSUPPORTED
+    assert L.kvq_decode_merged(*mg(out=None)) == K.ERR_INVALID_ARG
+    assert L.kvq_decode_merged(*mg(msl=1366 * 512)) == K.ERR_UNSUPPORTED   # 1366 partitions x group 6 > 8192
+    # kvq_decode_attn_unrotated: rotated 4-bit (or Q4_0) only, f32 / bf16 queries
+    un = lambda c=d, qd=0, q=dummy: (ctypes.byref(c), q, qd, 2, 24, dummy, dummy, 100, 1000, None, 0, f, dummy, ws,
+                                     None)
+    assert L.kvq_decode_attn_unrotated(*un(c=bf)) == K.ERR_UNSUPPORTED
+    assert L.kvq_decode_attn_unrotated(*un(qd=7)) == K.ERR_INVALID_ARG
+    assert L.kvq_decode_attn_unrotated(*un(q=None)) == K.ERR_INVALID_ARG
+    # TQ4 caches: the sign mask is required and 4-byte aligned; head_dim 64 / 128 / 256
+    one = ctypes.c_int32(0)
+    st = lambda c: L.kvq_store(ctypes.byref(c), dummy, dummy, 0, 1, ctypes.byref(one), None, None)
+    assert st(_tq4_desc(K, signs=None)) == K.ERR_INVALID_ARG
+    assert st(_tq4_desc(K, signs=4098)) == K.ERR_INVALID_ARG
+    assert st(_tq4_desc(K, D=96)) == K.ERR_UNSUPPORTED
+    # kvq_tq4_rotate: TQ4 caches only; dtype; in place needs f32
+    t = _tq4_desc(K)
+    assert L.kvq_tq4_rotate(ctypes.byref(d), dummy, 0, dummy, 4, 24, None) == K.ERR_UNSUPPORTED
+    assert L.kvq_tq4_rotate(ctypes.byref(t), dummy, 3, ctypes.c_void_p(8192), 4, 24, None) == K.ERR_INVALID_ARG
+    assert L.kvq_tq4_rotate(ctypes.byref(t), dummy, 1, dummy, 4, 24, None) == K.ERR_INVALID_ARG
+    # kvq_prefill_attn_fp8: fp8 latent rows, 16 | heads, the chunk inside the block table, workspace
+    pw = L.kvq_prefill_fp8_workspace_size(ctypes.byref(fp8), 8, 128)
+    assert pw > 0
+    pf = lambda c=fp8, nq=8, hq=128, q0=0, mp=4, wsb=pw: (ctypes.byref(c), dummy, nq, hq, q0, dummy, mp, f, dummy,
+                                                          wsb, dummy, None)
+    assert L.kvq_prefill_attn_fp8(*pf(c=d)) == K.ERR_UNSUPPORTED
+    assert L.kvq_prefill_attn_fp8(*pf(hq=24)) == K.ERR_UNSUPPORTED
+    assert L.kvq_prefill_attn_fp8(*pf(nq=-1)) == K.ERR_INVALID_ARG
+    assert L.kvq_prefill_attn_fp8(*pf(nq=0)) == K.OK
+    assert L.kvq_prefill_attn_fp8(*pf(q0=60)) == K.ERR_INVALID_ARG    # rows 60..67 beyond 4 pages of 16
+    assert L.kvq_prefill_attn_fp8(*pf(wsb=pw - 1)) == K.ERR_WORKSPACE_TOO_SMALL
+    # kvq_store_rotate: dtypes, counts, pointers
+    sr = lambda dt=0, qdt=0, n=1, qr=24, k=dummy, q=dummy, qo=ctypes.c_void_p(8192): (
+        ctypes.byref(d), k, dummy, dt, n, dummy, None, q, qdt, qo, qr, None)
+    assert L.kvq_store_rotate(*sr(dt=4)) == K.ERR_INVALID_ARG
+    assert L.kvq_store_rotate(*sr(qdt=4)) == K.ERR_INVALID_ARG
+    assert L.kvq_store_rotate(*sr(n=-1)) == K.ERR_INVALID_ARG
+    assert L.kvq_store_rotate(*sr(k=None)) == K.ERR_INVALID_ARG
+    assert L.kvq_store_rotate(*sr(q=None)) == K.ERR_INVALID_ARG
+    assert L.kvq_store_rotate(*sr(qdt=1, qo=dummy)) == K.ERR_INVALID_ARG   # in place needs f32
+    # kvq_decode_noalloc: a cache, a workspace that fits the static array, an output
+    scratch = L.kvq_noalloc_scratch_bytes()
+    assert scratch == 16 << 20
+    na = lambda c=d, B=1, msl=1000, out=dummy: (ctypes.byref(c) if c else None, dummy, B, 24, dummy, dummy, 100000,
+                                                msl, None, 0, f, 1, out, None, None)
+    assert L.kvq_decode_noalloc(*na(c=None)) == K.ERR_INVALID_ARG
+    assert L.kvq_decode_noalloc(*na(B=64, msl=262145)) == K.ERR_WORKSPACE_TOO_SMALL
+    assert L.kvq_decode_noalloc(*na(out=None)) == K.ERR_INVALID_ARG
+    # status helpers
+    assert L.kvq_selftest_wait_timeout(None, None) == K.ERR_INVALID_ARG
+    assert L.kvq_read_status(None, dummy, None) == K.ERR_INVALID_ARG
