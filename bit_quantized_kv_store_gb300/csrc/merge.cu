@@ -99,7 +99,7 @@ __global__ void __launch_bounds__(256) merge_kernel(const MergeArgs a) {
   __syncthreads();
   // M = max over the 32 rows; each row's partial rescaled to M
   float M = s_m[0];
-#pragma unroll 8
+#pragma unroll
   for (int r = 1; r < 32; ++r) M = fmaxf(M, s_m[r]);
   const bool empty = (M == -INFINITY);
   const float wr = (empty || Mt == -INFINITY) ? 0.f : exp2f(Mt - M);
@@ -112,7 +112,8 @@ __global__ void __launch_bounds__(256) merge_kernel(const MergeArgs a) {
   __syncthreads();
   if (tid < 32) {
     float o = 0.f, Z = 0.f;
-    for (int r = 0; r < 32; ++r) {  // ascending rows, a fixed order
+#pragma unroll
+    for (int r = 0; r < 32; ++r) {  // ascending rows, a fixed order (unrolled: the loads go ahead of the adds)
       o += red_acc[r][lane];
       Z += s_z[r];
     }
