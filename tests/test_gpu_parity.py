@@ -418,6 +418,19 @@ def test_decode_gather(K):
             assert_close(out[b], ref[b], what=f"gather n_sel={n_sel} seq {b}")
 
 
+def test_decode_gather_at_the_limit(K):
+    """4096 selected rows, the largest list the ABI accepts: eight full 512-entry
+    partitions; the second sequence selects every one of its 4096 rows."""
+    lens = [9000, 4096]
+    g, o, bt, q, ml = decode_case(K, lens, seed=23)
+    sel = np.stack([synth.distinct_sorted(4096, L, 23, b).numpy() for b, L in enumerate(lens)]).astype(np.int32)
+    assert np.array_equal(sel[1], np.arange(4096))
+    out, _ = run_decode(K, g, bt, q, lens, ml, 1 / 16, sel=sel)
+    ref = O.decode(o, to_np_in(q), lens, bt, 1 / 16, sel=sel)
+    for b in range(2):
+        assert_close(out[b], ref[b], what=f"gather n_sel=4096 seq {b}")
+
+
 @pytest.mark.parametrize("lens", [[1], [17, 513], [1025, 3000]])
 def test_decode_q4_0(K, lens):
     """The unrotated 4-bit format through the same decode kernel and merge (no
@@ -450,7 +463,7 @@ def test_decode_q4_0_gather(K):
 # tiles (R = 3 with dead columns), R = 6 two slices of 3, R = 8 two of 4, R = 20
 # four of 5.  T0 = 510 puts the rows' ends on both sides of a partition edge.
 @pytest.mark.parametrize("T0,R", [(1000, 4), (513, 3), (40, 8), (0, 2), (300, 1), (510, 5), (100, 6),
-                                  (2000, 20), (4095, 2)])
+                                  (2000, 20), (4095, 2), (3000, 64)])   # 64: the maximum window (13 slices of 5 rows)
 def test_decode_window_equals_plain_rows(K, T0, R):
     """A decode window (R draft rows of one sequence sharing its block table, row i
     attending keys 0 .. T0 + i) gives bit-identical partials and outputs to the
