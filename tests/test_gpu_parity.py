@@ -755,7 +755,7 @@ def _fp8_prefill_case(K, depth, n_q, Hq=32, seed=0):
     return g, o, bt, q
 
 
-@pytest.mark.parametrize("depth,n_q,Hq", [(0, 5, 32), (700, 6, 32), (1500, 3, 48)])
+@pytest.mark.parametrize("depth,n_q,Hq", [(0, 5, 32), (700, 6, 32), (1500, 3, 48), (3, 1, 16)])
 def test_prefill_fp8_matches_oracle(K, depth, n_q, Hq):
     """fp8 latent prefill (one streaming CTA per row and 32 heads, the whole row one
     partition) against the oracle's causal prefill."""
@@ -811,7 +811,7 @@ def test_prefill_fp8_long_rows_equal_split_decode(K):
                      what=f"1M-key row {i}")
 
 
-@pytest.mark.parametrize("depth,n_q", [(0, 20), (100, 37), (600, 150)])
+@pytest.mark.parametrize("depth,n_q", [(0, 20), (100, 37), (600, 150), (511, 1), (0, 1)])
 def test_prefill(K, depth, n_q):
     Hk, Hq, D, ps = 4, 24, 256, 16
     T = depth + n_q
