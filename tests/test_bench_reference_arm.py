@@ -1,0 +1,28 @@
+"""The benchmark's reference arm (the CPU oracle on the host cores) prints one
+JSON line with the same metric, unit and workload as the GPU arm, and the keys
+the benchmark's consumers read.  Runs on the CPU: one bounded sample."""
+import json
+import subprocess
+import sys
+
+from tests.conftest import ROOT
+
+sys.path.insert(0, ROOT)
+import bench  # noqa: E402
+
+
+def test_reference_arm_line():
+    r = subprocess.run([sys.executable, "bench.py", "--impl", "reference", "--steps", "1", "--warmup", "1"],
+                       cwd=ROOT, capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0, r.stderr[-2000:]
+    d = json.loads(r.stdout.strip().splitlines()[-1])
+    assert d["impl"] == "reference"
+    assert d["metric"] == bench.METRIC and d["unit"] == "us/layer-token"
+    assert d["higher_is_better"] is False and d["n_gpus"] == 1
+    assert d["steps"] == 1 and d["warmup"] == 1
+    assert d["config"] == bench.workload_config(32768, 1)
+    cb = d["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["sample"]
+    assert cb["value"] == d["value"] > 0
+    assert d["e2e"] == {"value": d["value"], "unit": d["unit"], "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
+    assert abs(d["ms_per_step"] - d["value"] * 16 / 1e3) < 1e-6 * d["ms_per_step"]
