@@ -16,6 +16,8 @@ roofline= the decode kernel: algorithmic bytes (codes + scales of K and V of eve
           attended position, 1152 B per position per layer) / average launch time
           measured with CUDA events on the launching stream; peak = measured HBM
           copy bandwidth.
+clocks  = SM clock and throttle reasons sampled through NVML every 0.5 ms inside
+          the timed region (nvidia-smi every 100 ms where NVML cannot be loaded).
 --impl reference times the CPU oracle on the host cores on a bounded sample.
 """
 from __future__ import annotations
