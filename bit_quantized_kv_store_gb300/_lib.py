@@ -96,7 +96,16 @@ def _check(status, where):
 
 
 def _ptr(t):
-    return None if t is None else ctypes.c_void_p(t.data_ptr())
+    """Device address of a tensor for the C ABI (None -> NULL).  The kernels read
+    plain row-major device memory, so a host tensor (whose address the GPU would
+    fault on) or a strided view (read with the wrong layout) is refused here."""
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError(f"kvq: expected a CUDA tensor, got one on {t.device}")
+    if not t.is_contiguous():
+        raise ValueError("kvq: expected a contiguous tensor (call .contiguous())")
+    return ctypes.c_void_p(t.data_ptr())
 
 
 def _stream(stream=None):
@@ -126,6 +135,8 @@ class Cache:
     """
 
     def __init__(self, fmt, num_kv_heads, head_dim, page_size, num_pages, device="cuda", rope_dim=0, signs=None):
+        if torch.device(device).type != "cuda":
+            raise ValueError(f"kvq: the cache planes live in device memory, not on {device}")
         self.fmt, self.Hk, self.D, self.page_size, self.num_pages = fmt, num_kv_heads, head_dim, page_size, num_pages
         self.rope = rope_dim
         self.signs = None
@@ -158,6 +169,9 @@ class Cache:
         self.refresh()
 
     def refresh(self):
+        for t in (self.k, self.v, self.k_scale, self.v_scale, self.signs):
+            if t is not None and not (t.is_cuda and t.is_contiguous()):
+                raise ValueError("kvq: cache planes must be contiguous CUDA tensors")
         self.desc = CacheDesc(self.fmt, self.Hk, self.D, self.rope, self.page_size, self.num_pages,
                               self.k.data_ptr(), 0 if self.k_scale is None else self.k_scale.data_ptr(),
                               self.v.data_ptr(), 0 if self.v_scale is None else self.v_scale.data_ptr(),

@@ -197,3 +197,14 @@ def test_host_validation_of_the_other_entries(K):
     # status helpers
     assert L.kvq_selftest_wait_timeout(None, None) == K.ERR_INVALID_ARG
     assert L.kvq_read_status(None, dummy, None) == K.ERR_INVALID_ARG
+
+
+def test_binding_refuses_host_memory(K):
+    """The binding hands the kernels device addresses only: a host tensor or a
+    host-resident cache is refused before any call."""
+    import torch
+    assert K._ptr(None) is None
+    with pytest.raises(ValueError):
+        K._ptr(torch.zeros(4))
+    with pytest.raises(ValueError):
+        K.Cache(K.FMT_Q4_HAD32, 4, 256, 16, 2, device="cpu")

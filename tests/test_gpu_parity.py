@@ -884,3 +884,14 @@ def test_prefill_bad_page_is_flagged(K):
     torch.cuda.synchronize()
     assert K.read_status(st) & K.DEV_BAD_PAGE
     assert np.isnan(out.cpu().numpy()).all()
+
+
+def test_binding_refuses_strided_views(K):
+    """A strided view would be read as if row-major: the binding refuses it."""
+    q = torch.zeros((2, 24, 512), dtype=torch.float32, device=DEV)[:, :, ::2]
+    with pytest.raises(ValueError):
+        K.rotate_query(q)
+    g = K.Cache(K.FMT_Q4_HAD32, 4, 256, 16, 2, device=DEV)
+    g.k = g.k.transpose(0, 1)
+    with pytest.raises(ValueError):
+        g.refresh()
