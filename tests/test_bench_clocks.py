@@ -58,3 +58,19 @@ def test_sampler_keeps_only_the_marked_window():
     t.join(timeout=2)
     assert n > 0 and len(c.samples) <= n + 1
     assert all(s[2] == ["sw_power_cap"] and s[1] == 2070.0 for s in c.samples)
+
+
+def test_nvidia_smi_fallback_parses_its_lines():
+    class FakeProc:
+        stdout = iter(["2070, 2070, Not Active, Not Active, Not Active, Not Active\n",
+                       "1965, 2070, Not Active, Not Active, Not Active, Active\n",
+                       "garbage\n",
+                       "[N/A], 2070, Not Active, Not Active, Not Active, Not Active\n",
+                       "2070, 2070, Active, Not Active, Not Active, Not Active\n"])
+
+    c = bench.Clocks(0)
+    c.proc = FakeProc()
+    c._read()
+    s = bench.clock_summary(c.samples, "nvidia-smi")
+    assert s["samples"] == 3 and s["sm_mhz"] == 2070.0 and s["sm_max_mhz"] == 2070.0
+    assert s["reasons"] == ["hw_slowdown", "sw_power_cap"]
