@@ -85,6 +85,37 @@ def fill_sequence(K, g, o, k, v, bt_row, T, status=None):
 
 # --------------------------------------------------------------------------- store
 
+@pytest.mark.parametrize("fmt", ["Q4_HAD32", "Q4_0"])
+@pytest.mark.parametrize("reps", [40, 1])  # 40: > 256 rows, the row kernel; 1: the (row, group) kernel
+def test_store_code_ties_round_half_to_even(K, fmt, reps):
+    """Codes exactly on rounding ties (y / s = k + 1/2 for k = -8 .. 7, exact
+    scales): both store kernels keep the even neighbour and clamp +7.5 to code
+    15, bit-exact with the oracle and with the literal table of the expected
+    codes."""
+    from tests import tie_rows
+    if fmt == "Q4_0":
+        x, exp = tie_rows.unrotated_rows()
+        gfmt = K.FMT_Q4_0
+    else:
+        x, exp, _, _ = tie_rows.rotated_rows()
+        gfmt = K.FMT_Q4_HAD32
+    x = np.tile(x, (reps, 1))
+    exp = np.tile(exp, (reps, 1))
+    n, D = x.shape
+    ps = 16
+    n_pages = (n + ps - 1) // ps
+    g, o = make_cache_pair(K, gfmt, 1, D, ps, n_pages)
+    kt = torch.from_numpy(x.reshape(n, 1, D))
+    vt = torch.from_numpy(-x.reshape(n, 1, D))
+    fill_sequence(K, g, o, kt, vt, np.arange(n_pages, dtype=np.int32), n)
+    torch.cuda.synchronize()
+    check_planes_equal(g, o)
+    kb = g.k.cpu().numpy().reshape(-1, D // 2)[:n]
+    codes = np.stack([kb & 15, kb >> 4], -1).reshape(n, D).astype(np.int64)
+    tie = exp >= 0
+    assert np.array_equal(codes[tie], exp[tie])
+
+
 @pytest.mark.parametrize("D", [64, 128, 256])
 @pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
 @pytest.mark.parametrize("T", [250, 20])  # large stores take the row kernel, small ones the (row, group) kernel

@@ -202,6 +202,47 @@ def test_q4_0_exact_scale_block_codes_equal_inputs():
     assert not np.array_equal(canon_r, canon)
 
 
+def test_code_ties_round_half_to_even_and_clamp_unrotated():
+    """Exact halves in exact-scale blocks ("feat(kvcache): add reliable quantized
+    KV cache", test-fix commit: amax 8 -> scale 1.0; its PyTorch reference
+    rounds with torch.round, half to even): y / s = k + 1/2 must store the even
+    neighbour, and +7.5 (even neighbour 8) must clamp to 7.  The expected codes
+    are a literal table; half-away-from-zero and truncation disagree with it on
+    these inputs, so either mistake in the oracle fails here."""
+    from tests import tie_rows
+    x, exp = tie_rows.unrotated_rows()
+    away, trunc = tie_rows.alternative_codes()
+    assert any(away[h] != tie_rows.TIE_CODE[h] for h in tie_rows.HALVES)
+    assert any(trunc[h] != tie_rows.TIE_CODE[h] for h in tie_rows.HALVES)
+    for r in range(x.shape[0]):
+        canon, sc = O.q4_quantize_row(x[r], rotate=False)
+        assert np.all(O.f16_bits_to_f64(sc) == 1.0)
+        codes = _canon_codes(canon)
+        tie = exp[r] >= 0
+        assert np.array_equal(codes[tie], exp[r][tie])
+        amax = np.abs(x[r]) == 8.0
+        assert np.array_equal(codes[amax], np.where(x[r][amax] > 0, 15, 0))   # +8 clamps to code 15, -8 is 0
+
+
+def test_code_ties_round_half_to_even_through_the_rotation():
+    """The same tie rule on the rotated path: inputs built so that the fp32
+    butterfly is exact and one element per group lands on y / s = k + 1/2
+    exactly (checked with numpy fp32 arithmetic and scipy's Hadamard matrix);
+    the oracle's scale must be the fp16 value of amax / 8 and the tie codes the
+    literal table."""
+    from tests import tie_rows
+    x, exp, y, s = tie_rows.rotated_rows()
+    assert sorted({float(y[r][c] / s[r][c // 32]) for r, c in zip(*np.nonzero(exp >= 0))}) == tie_rows.HALVES
+    for r in range(x.shape[0]):
+        canon, sc = O.q4_quantize_row(x[r], rotate=True)
+        assert np.array_equal(O.f16_bits_to_f64(sc), s[r].astype(np.float64))
+        codes = _canon_codes(canon)
+        tie = exp[r] >= 0
+        assert np.array_equal(codes[tie], exp[r][tie])
+        zero = y[r] == 0
+        assert np.all(codes[zero] == 8)
+
+
 def test_q4_0_attention_is_plain_attention_over_dequantized_rows():
     """Q4_0: out = softmax(sm q . K) V with K, V the dequantized unrotated rows, and
     those rows within one scale step of the inputs (half a step, except a
