@@ -10,15 +10,23 @@ context is measured in the same run and reported under "long_context".
 value   = microseconds per layer-token (lower is better), device time with the
           inputs resident in HBM; the 16 layer caches (604 MB at 32K, 4.8 GB at
           262K) exceed the 129 MB L2, so every step reads the cache from HBM.
-e2e     = the same step through the C ABI with the step's inputs copied from
-          pinned host memory and the outputs copied back inside the timed region.
+e2e     = the same step through the public API, call by call (48 C-ABI calls a
+          step), with the step's inputs copied from pinned host memory and the
+          outputs copied back inside the timed region; graph_replay_value is the
+          same with the step replayed as a captured CUDA graph.
 roofline= the decode kernel: algorithmic bytes (codes + scales of K and V of every
           attended position, 1152 B per position per layer) / average launch time
           measured with CUDA events on the launching stream; peak = measured HBM
           copy bandwidth.
 clocks  = SM clock and throttle reasons sampled through NVML every 0.5 ms inside
           the timed region (nvidia-smi every 100 ms where NVML cannot be loaded).
---impl reference times the CPU oracle on the host cores on a bounded sample.
+cpu_baseline = the CPU oracle (single-threaded) on bounded samples of every
+          workload, in spawned processes side by side on the host cores.
+The other rows (batched decode, prefill, store, fp8, bf16, TQ4, windows, ...)
+are printed in full on a line of their own before the headline line; the
+headline carries their timings and fractions under roofline.other_kernels and
+the 262K figures under roofline.long_context.
+--impl reference times the CPU oracle, one layer-token per step.
 """
 from __future__ import annotations
 
@@ -38,10 +46,38 @@ sys.path.insert(0, ROOT)
 LAYERS, HK, HQ, D, PS = 16, 4, 24, 256, 16
 KERNELS_PER_LAYER = 3  # store + query rotation (one launch), split-T decode, merge
 # DRAM bytes of one decode launch (dram__bytes_read.sum + dram__bytes_write.sum
-# from an ncu capture of the current kernel at each context); to be dropped
-# whenever the kernel changes.
-TRAFFIC_BYTES = {32768: 37867008 + 0, 262144: 302277120 + 10575104}
+# from an ncu capture at each context), valid only for the kernel sources whose
+# SHA-256 (first 16 hex digits, over TRAFFIC_SOURCES in order) is recorded
+# beside them: once those sources change, the bench reports no traffic until
+# the capture is taken again.
+TRAFFIC_SOURCES = ("bit_quantized_kv_store_gb300/csrc/decode_q4.cu", "bit_quantized_kv_store_gb300/csrc/common.cuh")
+TRAFFIC_CAPTURE = {"sources_sha16": "5b56ddfa016d6d15",
+                   "bytes": {32768: 37867008 + 0, 262144: 302277120 + 10575104}}
 BYTES_PER_POS_LAYER = HK * 2 * (D // 2 + 2 * (D // 32))   # 1152
+
+
+def sources_sha16(paths=TRAFFIC_SOURCES):
+    import hashlib
+    h = hashlib.sha256()
+    for rel in paths:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def traffic_bytes(context):
+    """ncu DRAM bytes of one decode launch at `context`, or None when the capture
+    predates the current kernel sources."""
+    if sources_sha16() != TRAFFIC_CAPTURE["sources_sha16"]:
+        return None
+    return TRAFFIC_CAPTURE["bytes"].get(context)
+
+
+def _r(x, digits=4):
+    """Round a float to `digits` significant digits for the compact summaries."""
+    if x is None or not isinstance(x, float) or x == 0 or not math.isfinite(x):
+        return x
+    return round(x, max(0, digits - 1 - int(math.floor(math.log10(abs(x))))))
 
 
 def parse():
@@ -333,11 +369,14 @@ def time_device(W, steps, warmup, torch, clk=None):
     return total_ms, dec_avg_ms, KERNELS_PER_LAYER * LAYERS * steps, graphs
 
 
-def time_e2e(W, steps, warmup, torch, graphs):
-    """Host buffers in, host buffers out, copies inside the timed region: the
-    step's new K/V rows and queries are copied from pinned host memory into the
-    device buffers the captured step reads, the step graph runs, and the 16
-    layers' outputs are copied back."""
+def time_e2e(W, steps, warmup, torch, graphs=None):
+    """Host buffers in, host buffers out, copies inside the timed region: every
+    step copies its new K/V rows and queries from pinned host memory into the
+    device buffers the step reads, runs the 16 layers, and copies the 16 layers'
+    outputs back.  graphs=None: the step is issued call by call through the
+    public API (kvq_store_rotate, kvq_decode_attn, kvq_merge per layer: host-side
+    validation, tensor-map encoding and launch on every call); otherwise the
+    captured step graphs are replayed."""
     n_in = W.new_k.shape[0]
     hk = [W.new_k[i].cpu().pin_memory() for i in range(n_in)]
     hv = [W.new_v[i].cpu().pin_memory() for i in range(n_in)]
@@ -348,7 +387,10 @@ def time_e2e(W, steps, warmup, torch, graphs):
         W.new_k[i].copy_(hk[i], non_blocking=True)
         W.new_v[i].copy_(hv[i], non_blocking=True)
         W.q[i].copy_(hq[i], non_blocking=True)
-        graphs[i].replay()
+        if graphs is None:
+            W.step(i)
+        else:
+            graphs[i].replay()
         hout.copy_(W.out, non_blocking=True)
         torch.cuda.current_stream().synchronize()
 
@@ -364,31 +406,191 @@ def time_e2e(W, steps, warmup, torch, graphs):
     return el * 1e3, h2d, d2h
 
 
-def cpu_baseline_decode(context, n_heads, seed=99):
-    """Time the CPU oracle on one layer-token at `context` (store the new token and
-    attend with n_heads of the 24 query heads); returns (us per layer-token, desc)."""
+# --------------------------------------------------------------------------- the CPU oracle legs
+#
+# The oracle (single-threaded C, fp64 attention) timed on the host cores on
+# bounded samples of each workload.  Every leg runs in a process of its own
+# (started with `spawn`, after the GPU measurements) with one thread; the legs
+# run side by side on separate cores.  Cache fills use the oracle's own store
+# and are not timed; the timed part is what the GPU step does: store the new
+# tokens and attend.
+
+def _oracle_env():
     import numpy as np
     import torch
-
+    torch.set_num_threads(1)
     import oracle as O
     from bit_quantized_kv_store_gb300 import synth
-    T = context + 1
-    n_pages = (T + PS - 1) // PS
-    c = O.Cache(O.Q4, HK, D, PS, n_pages)
-    # fill the cache (not timed): the oracle's own store of the same kind of data
-    kv_heads = sorted({h // (HQ // HK) for h in range(n_heads)})
-    k = synth.heavy_tailed((T, HK, D), "cpu", seed, "k").view(torch.int16).numpy().view(np.uint16)
-    v = synth.heavy_tailed((T, HK, D), "cpu", seed, "v").view(torch.int16).numpy().view(np.uint16)
-    O.store(c, k[:context], v[:context], np.arange(context, dtype=np.int32))
-    q = synth.heavy_tailed((1, HQ, D), "cpu", seed, "q").view(torch.int16).numpy().view(np.uint16)
-    bt = np.arange(n_pages, dtype=np.int32).reshape(1, -1)
+    return np, torch, O, synth
+
+
+def _bits(t):
+    import numpy as np
+    import torch
+    return t.contiguous().view(torch.int16).numpy().view(np.uint16)
+
+
+class OracleLayerToken:
+    """One 4-bit cache of `context` positions filled by the oracle's store; step()
+    stores one new token (4 KV heads, K and V) at position `context` and attends
+    all 24 query heads over T = context + 1 keys: one layer-token of the
+    benchmark's step."""
+
+    def __init__(self, context, seed):
+        np, torch, O, synth = _oracle_env()
+        self.np, self.O = np, O
+        self.T = context + 1
+        n_pages = (self.T + PS - 1) // PS
+        self.c = O.Cache(O.Q4, HK, D, PS, n_pages)
+        chunk = 32768
+        for s0 in range(0, context, chunk):
+            n = min(chunk, context - s0)
+            k = _bits(synth.heavy_tailed((n, HK, D), "cpu", seed, "k", s0, subset=(seed, "k")))
+            v = _bits(synth.heavy_tailed((n, HK, D), "cpu", seed, "v", s0, subset=(seed, "v")))
+            O.store(self.c, k, v, np.arange(s0, s0 + n, dtype=np.int32))
+        self.new_k = _bits(synth.heavy_tailed((1, HK, D), "cpu", seed, "newk", subset=(seed, "k")))
+        self.new_v = _bits(synth.heavy_tailed((1, HK, D), "cpu", seed, "newv", subset=(seed, "v")))
+        self.q = _bits(synth.heavy_tailed((1, HQ, D), "cpu", seed, "q"))
+        self.slot = np.array([context], np.int32)
+        self.bt = np.arange(n_pages, dtype=np.int32).reshape(1, -1)
+
+    def step(self):
+        t = time.perf_counter()
+        self.O.store(self.c, self.new_k, self.new_v, self.slot)
+        self.O.decode(self.c, self.q, [self.T], self.bt, 1 / math.sqrt(D))
+        return time.perf_counter() - t
+
+
+def cpu_leg_c1(context=32768, seed=1234 + 1):
+    """32K context: all 16 layers of one step (16 layer-tokens on one filled cache)."""
+    w = OracleLayerToken(context, seed)
+    el = sum(w.step() for _ in range(LAYERS))
+    return {"value": el * 1e6 / LAYERS, "unit": "us/layer-token", "seconds": el,
+            "sample": f"all {LAYERS} layers of one step at context {context}, 24 heads (one oracle-filled cache "
+                      f"reused per layer)"}
+
+
+def cpu_leg_c2(context=262144, seed=1234 + 2):
+    """262K context: one full layer-token; the 16-layer step is extrapolated."""
+    w = OracleLayerToken(context, seed)
+    el = w.step()
+    return {"value": el * 1e6, "unit": "us/layer-token", "seconds": el,
+            "extrapolated_step_s": el * LAYERS,
+            "sample": f"one layer-token at context {context} (store + 24 heads); the {LAYERS}-layer step "
+                      f"extrapolated x{LAYERS}"}
+
+
+def cpu_leg_c3_decode(seed=1234 + 3):
+    """The ragged paged batch: 32 sequences, one layer, the whole batch."""
+    np, torch, O, synth = _oracle_env()
+    lens = synth.ragged_lengths(32, 1024, 65536, seed, "lens").tolist()
+    T = [L + 1 for L in lens]
+    pages = [(t + PS - 1) // PS for t in T]
+    perm = synth.page_permutation(sum(pages), seed, "perm").numpy().astype(np.int32)
+    bt = np.zeros((32, max(pages)), np.int32)
+    off = 0
+    for i, npg in enumerate(pages):
+        bt[i, :npg] = perm[off:off + npg]
+        off += npg
+    c = O.Cache(O.Q4, HK, D, PS, sum(pages))
+    for i, L in enumerate(lens):
+        pos = np.arange(L)
+        k = _bits(synth.heavy_tailed((L, HK, D), "cpu", seed, i, "k", subset=(seed, "k")))
+        v = _bits(synth.heavy_tailed((L, HK, D), "cpu", seed, i, "v", subset=(seed, "v")))
+        O.store(c, k, v, (bt[i][pos // PS] * PS + pos % PS).astype(np.int32))
+    nk = _bits(synth.heavy_tailed((32, HK, D), "cpu", seed, "nk", subset=(seed, "k")))
+    nv = _bits(synth.heavy_tailed((32, HK, D), "cpu", seed, "nv", subset=(seed, "v")))
+    q = _bits(synth.heavy_tailed((32, HQ, D), "cpu", seed, "q"))
+    slots = np.array([bt[i][lens[i] // PS] * PS + lens[i] % PS for i in range(32)], np.int32)
     t = time.perf_counter()
-    O.store(c, k[context:], v[context:], np.array([context], np.int32))
-    O.decode(c, q[:, :n_heads], [T], bt, 1 / 16)
+    O.store(c, nk, nv, slots)
+    O.decode(c, q, T, bt, 1 / math.sqrt(D))
     el = time.perf_counter() - t
-    us = el * 1e6 * (HQ / n_heads)
-    return us, f"one layer-token at context {context}: store of the new token + {n_heads} of {HQ} query heads " \
-               f"(KV heads {kv_heads}), scaled to 24 heads; oracle is single-threaded"
+    return {"value": el * 1e6, "unit": "us/step", "seconds": el, "keys": sum(T),
+            "sample": "the whole batch: 32 sequences (lengths U{1024..65536}), store of the 32 new tokens + "
+                      "24 heads each, 1 layer"}
+
+
+def cpu_leg_c3_prefill(seed=1234 + 3, n_rows=64):
+    """The 4096-token chunk at depth 16384: the chunk's store and 64 seeded query
+    rows (the first, the last and 62 drawn at random); rows/s and the chunk's
+    time extrapolated from them."""
+    np, torch, O, synth = _oracle_env()
+    depth, nq = 16384, 4096
+    Tp = depth + nq
+    npg = (Tp + PS - 1) // PS
+    bt = synth.page_permutation(npg, seed, "pf").numpy().astype(np.int32)
+    c = O.Cache(O.Q4, HK, D, PS, npg)
+    pos = np.arange(Tp)
+    slots = (bt[pos // PS] * PS + pos % PS).astype(np.int32)
+    k = _bits(synth.heavy_tailed((Tp, HK, D), "cpu", seed, "pfk", subset=(seed, "k")))
+    v = _bits(synth.heavy_tailed((Tp, HK, D), "cpu", seed, "pfv", subset=(seed, "v")))
+    O.store(c, k[:depth], v[:depth], slots[:depth])
+    q = _bits(synth.heavy_tailed((nq, HQ, D), "cpu", seed, "pfq"))
+    rows = np.unique(np.concatenate([[0, nq - 1], synth.distinct_sorted(n_rows - 2, nq, seed, "pfrows").numpy()]))
+    t = time.perf_counter()
+    O.store(c, k[depth:], v[depth:], slots[depth:])
+    t_store = time.perf_counter() - t
+    O.prefill(c, q, depth, bt, 1 / math.sqrt(D), rows=rows.astype(np.int32))
+    t_rows = time.perf_counter() - t - t_store
+    per_row = t_rows / rows.size
+    # rows attend 16385 .. 20480 keys; the sampled rows' mean key count scales the chunk
+    keys_sampled = float(np.mean(depth + rows + 1))
+    keys_chunk = depth + (nq + 1) / 2
+    return {"value": rows.size / t_rows, "unit": "query rows/s", "seconds": t_store + t_rows,
+            "rows": int(rows.size), "store_s": t_store,
+            "extrapolated_chunk_s": t_store + per_row * nq * keys_chunk / keys_sampled,
+            "sample": f"{rows.size} seeded rows of the 4096-token chunk at depth 16384 (first, last, random), "
+                      f"24 heads, after the chunk's store; the chunk's time extrapolated by keys"}
+
+
+def cpu_leg_c4(seed=1234 + 4):
+    """fp8 latent rows at 262,144 tokens: the dense absorbed decode (128 heads,
+    one full run) and the 2048-row gather."""
+    np, torch, O, synth = _oracle_env()
+    Tf, Hf, DL, R = 262144, 128, 512, 64
+    npg = Tf // PS
+    c = O.Cache(O.FP8, 1, DL, PS, npg, rope_dim=R)
+    for s0 in range(0, Tf, 65536):
+        rows = synth.latent_rows(65536, DL + R, "cpu", seed, "fp8", s0).numpy()
+        O.store(c, rows, None, np.arange(s0, s0 + 65536, dtype=np.int32))
+    q = synth.normal((1, Hf, DL + R), "cpu", seed, "fp8q").numpy()
+    bt = np.arange(npg, dtype=np.int32).reshape(1, -1)
+    sel = synth.distinct_sorted(2048, Tf, seed, "sel").numpy().astype(np.int32).reshape(1, -1)
+    sm = 1 / math.sqrt(DL + R)
+    t = time.perf_counter()
+    O.decode(c, q, [Tf], bt, sm)
+    dense = time.perf_counter() - t
+    t = time.perf_counter()
+    O.decode(c, q, [Tf], bt, sm, sel=sel)
+    gather = time.perf_counter() - t
+    return {"value": dense * 1e6, "unit": "us/decode", "seconds": dense + gather, "gather_2048_us": gather * 1e6,
+            "sample": "one full dense absorbed decode, 128 heads x 262144 e4m3 rows (512 + 64), and one gather of "
+                      "2048 selected rows"}
+
+
+CPU_LEGS = {"c1_32k_16_layers": cpu_leg_c1, "c2_262k_one_layer": cpu_leg_c2, "c3_batch_decode": cpu_leg_c3_decode,
+            "c3_prefill_64_rows": cpu_leg_c3_prefill, "c4_fp8_dense_and_gather": cpu_leg_c4}
+
+
+def _run_leg(name):
+    os.environ["OMP_NUM_THREADS"] = "1"
+    return name, CPU_LEGS[name]()
+
+
+def cpu_baselines(names=None):
+    """Run the oracle legs side by side in spawned single-threaded processes;
+    returns {name: result}."""
+    import concurrent.futures as cf
+    import multiprocessing as mp
+    names = list(CPU_LEGS) if names is None else names
+    workers = max(1, min(len(names), (os.cpu_count() or 1) - 1))
+    out = {}
+    with cf.ProcessPoolExecutor(max_workers=workers, mp_context=mp.get_context("spawn")) as ex:
+        for name, res in ex.map(_run_leg, names):
+            res["cores"] = 1
+            out[name] = res
+    return out, workers
 
 
 METRIC = "decode attn us/layer-token and achieved HBM GB/s vs peak (4-bit KV)"
@@ -401,43 +603,75 @@ def workload_config(context, world):
 
 
 def run_reference(args):
-    """--impl reference: the CPU oracle on the host cores, same metric and config;
-    each of the W warm-up and K timed steps is one bounded sample (one layer-token,
-    6 of the 24 query heads, scaled to 24)."""
+    """--impl reference: the CPU oracle on one host core, same metric and config.
+    Its step is one layer-token of the 32K workload (store the new token, attend
+    the 24 query heads over 32,769 keys): the metric is per layer-token, so the
+    line reports what was timed, with no extrapolation."""
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return
-    for s in range(args.warmup):
-        cpu_baseline_decode(args.context, 6, seed=900 + s)
-    samples = []
-    for s in range(args.steps):
-        us, desc = cpu_baseline_decode(args.context, 6, seed=1000 + s)
-        samples.append(us)
-    us = statistics.mean(samples)
+    w = OracleLayerToken(args.context, 1234 + 1)
+    for _ in range(args.warmup):
+        w.step()
+    samples = [w.step() for _ in range(args.steps)]
+    us = statistics.mean(samples) * 1e6
+    desc = (f"one layer-token per step (1 of the {LAYERS} layers) at context {args.context}: store of the new token + "
+            f"24 of 24 query heads; single-threaded oracle")
     line = {"impl": "reference", "metric": METRIC, "value": us,
             "unit": "us/layer-token", "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
-            "ms_per_step": us * LAYERS / 1e3, "higher_is_better": False, "scaling": "weak", "vs_baseline": None,
-            "dtype": "f64", "data": "synthetic",
+            "ms_per_step": us / 1e3, "step": "one layer-token", "higher_is_better": False, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": workload_config(args.context, int(os.environ.get("WORLD_SIZE", "1"))),
-            "cpu_baseline": {"value": us, "unit": "us/layer-token", "cores": 1, "kind": "oracle", "sample": desc},
+            "cpu_baseline": {"value": us, "unit": "us/layer-token", "cores": 1, "kind": "oracle", "sample": desc,
+                             "host_cores": os.cpu_count()},
             "e2e": {"value": us, "unit": "us/layer-token", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line))
 
 
 # --------------------------------------------------------------------------- the other hot-path rows
 
-def _events_time(torch, fn, iters, warmup=3):
-    """Average device time (ms) of fn() over iters runs, CUDA events on the current stream."""
+L2_BYTES = 129 * 2 ** 20
+_flush_buf = None
+
+
+def _l2_flush(torch):
+    """Overwrite a buffer of twice the L2 size, so that the next launch finds none
+    of its inputs in L2."""
+    global _flush_buf
+    if _flush_buf is None:
+        _flush_buf = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device="cuda")
+    _flush_buf.zero_()
+
+
+def _events_time(torch, fn, iters, warmup=3, flush=True):
+    """Average device time (ms) of fn() over iters runs, CUDA events on the current
+    stream around each run; with `flush`, L2 is flushed before every run
+    (outside the events), so single-layer rows whose data would fit in L2 read
+    it from HBM."""
     for _ in range(warmup):
         fn()
     torch.cuda.synchronize()
-    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    a.record()
-    for _ in range(iters):
+    if not flush:
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(iters):
+            fn()
+        b.record()
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / iters
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(iters)]
+    for a, b in ev:
+        _l2_flush(torch)
+        a.record()
         fn()
-    b.record()
+        b.record()
     torch.cuda.synchronize()
-    return a.elapsed_time(b) / iters
+    return sum(a.elapsed_time(b) for a, b in ev) / iters
+
+
+def rows_summary(rows):
+    """The rows' timings and roofline fractions only (floats, 4 significant digits)."""
+    return {name: {k: _r(v) for k, v in row.items() if isinstance(v, float)} for name, row in rows.items()}
 
 
 def measure_rows(K, synth, torch, dev, peak, tflops_peak, only=None):
@@ -451,11 +685,11 @@ def measure_rows(K, synth, torch, dev, peak, tflops_peak, only=None):
     if want("batched"):
         out.update(_row_batched(K, synth, torch, dev, peak, seed))
     if want("prefill"):
-        out.update(_row_prefill(K, synth, torch, dev, tflops_peak, seed))
+        out.update(_row_prefill(K, synth, torch, dev, tflops_peak, seed, peak))
     if want("fp8"):
-        out.update(_row_fp8(K, synth, torch, dev, seed))
+        out.update(_row_fp8(K, synth, torch, dev, seed, tflops_peak))
     if want("bf16"):
-        out.update(_row_bf16(K, synth, torch, dev, seed))
+        out.update(_row_bf16(K, synth, torch, dev, seed, peak))
     if want("q4_0"):
         out.update(_row_q4_0(K, synth, torch, dev, peak, seed))
     if want("window"):
@@ -463,7 +697,7 @@ def measure_rows(K, synth, torch, dev, peak, tflops_peak, only=None):
     if want("tq4"):
         out.update(_row_tq4(K, synth, torch, dev, peak, seed))
     if want("fp8_prefill"):
-        out.update(_row_fp8_prefill(K, synth, torch, dev, seed))
+        out.update(_row_fp8_prefill(K, synth, torch, dev, seed, tflops_peak))
     if want("fused_merge"):
         out.update(_row_fused_merge(K, synth, torch, dev, seed))
     return out
@@ -517,7 +751,7 @@ def _row_batched(K, synth, torch, dev, peak, seed):
     return out
 
 
-def _row_prefill(K, synth, torch, dev, tflops_peak, seed):
+def _row_prefill(K, synth, torch, dev, tflops_peak, seed, peak):
     """Prefill chunk: 4096 queries at depth 16384, causal over decoded 4-bit slots;
     also the store of the chunk's rows."""
     out = {}
@@ -549,13 +783,14 @@ def _row_prefill(K, synth, torch, dev, tflops_peak, seed):
     rows = nq * HK * 2
     out["store"] = {"workload": "4096 tokens x 4 KV heads x (K, V) bf16 rows of 256 -> 4-bit rotated rows",
                     "us": st_ms * 1e3, "rows_per_s": rows / (st_ms * 1e-3),
-                    "GBs": rows * (512 + 144) / (st_ms * 1e-3) / 1e9}
+                    "GBs": rows * (512 + 144) / (st_ms * 1e-3) / 1e9,
+                    "frac_of_hbm_peak": rows * (512 + 144) / (st_ms * 1e-3) / 1e9 / peak}
     del c, k, v
     torch.cuda.empty_cache()
     return out
 
 
-def _row_fp8(K, synth, torch, dev, seed):
+def _row_fp8(K, synth, torch, dev, seed, tflops_peak):
     """fp8 latent rows: dense absorbed decode over 262144 rows, 128 heads, and a 2048-row gather."""
     out = {}
     Tf, Hf, DL, R = 262144, 128, 512, 64
@@ -588,6 +823,7 @@ def _row_fp8(K, synth, torch, dev, seed):
     gms = _events_time(torch, fp8_gather, 5)
     out["fp8_latent"] = {"workload": "absorbed decode, 128 heads x (512 latent + 64 rope) e4m3 rows, context 262144, "
                                      "split-T + merge", "us": ms * 1e3, "flop": flops, "TFLOPs": flops / (ms * 1e-3) / 1e12,
+                         "frac_of_bf16_peak": flops / (ms * 1e-3) / 1e12 / tflops_peak,
                          "GBs": byts / (ms * 1e-3) / 1e9, "gather_2048_us": gms * 1e3,
                          "kernel": "decode_fp8_kernel (mma.sync f16, split query) + merge_kernel"}
     del c, wsf, wsg
@@ -595,7 +831,7 @@ def _row_fp8(K, synth, torch, dev, seed):
     return out
 
 
-def _row_fp8_prefill(K, synth, torch, dev, seed):
+def _row_fp8_prefill(K, synth, torch, dev, seed, tflops_peak):
     """fp8 latent prefill past the old caps: a 32-row chunk at positions 1048544 ..
     1048575 (1M keys), 128 heads, causal; one streaming CTA per (row, 32 heads)."""
     out = {}
@@ -618,6 +854,7 @@ def _row_fp8_prefill(K, synth, torch, dev, seed):
     out["fp8_prefill_1m"] = {"workload": "fp8 latent prefill chunk of 32 rows at positions 1048544..1048575, 128 heads, "
                                          "causal over (512 + 64) e4m3 rows",
                              "ms": ms, "flop": flops, "TFLOPs": flops / (ms * 1e-3) / 1e12,
+                             "frac_of_bf16_peak": flops / (ms * 1e-3) / 1e12 / tflops_peak,
                              "kernel": "decode_fp8_kernel (streaming: one CTA per row x 32 heads, the row one "
                                        "partition) + merge_kernel"}
     del c, ws
@@ -625,7 +862,7 @@ def _row_fp8_prefill(K, synth, torch, dev, seed):
     return out
 
 
-def _row_bf16(K, synth, torch, dev, seed):
+def _row_bf16(K, synth, torch, dev, seed, peak):
     """bf16-cache comparison at 32K (same kernel structure, unrotated bf16 rows)."""
     out = {}
     Tb = 32769
@@ -643,6 +880,7 @@ def _row_bf16(K, synth, torch, dev, seed):
     byts = Tb * HK * 2 * D * 2
     out["bf16_cache_32k"] = {"workload": "bf16 (unrotated) cache, context 32768, 1 layer, same split-T + merge",
                              "decode_kernel_us": dms * 1e3, "cache_bytes": byts, "achieved_GBs": byts / (dms * 1e-3) / 1e9,
+                             "frac_of_hbm_peak": byts / (dms * 1e-3) / 1e9 / peak,
                              "bytes_vs_4bit": byts / (Tb * BYTES_PER_POS_LAYER),
                              "kernel": "decode_bf16_kernel (mma.sync bf16, split query and P)"}
     del c, wsb
@@ -838,10 +1076,12 @@ def main():
     us_per_lt = aggregate_us_per_unit(total_ms, LAYERS * args.steps, world)
     bytes_per_launch = W.T * BYTES_PER_POS_LAYER
     achieved = bytes_per_launch / (dec_avg_ms * 1e-3) / 1e9
-    e2e_ms, h2d, d2h = time_e2e(W, max(3, args.steps // 2), 2, torch, graphs)
+    e2e_steps = max(3, args.steps // 2)
+    g_ms, h2d, d2h = time_e2e(W, e2e_steps, 2, torch, graphs)
     del graphs
-    e2e_ms = max_over_ranks(e2e_ms)
-    e2e_us = e2e_ms * 1e3 / (LAYERS * max(3, args.steps // 2) * world)
+    c_ms, _, _ = time_e2e(W, e2e_steps, 2, torch, None)
+    g_us = max_over_ranks(g_ms) * 1e3 / (LAYERS * e2e_steps * world)
+    c_us = max_over_ranks(c_ms) * 1e3 / (LAYERS * e2e_steps * world)
 
     long = None
     if not args.no_long:
@@ -856,12 +1096,13 @@ def main():
         ltot = max_over_ranks(ltot)
         lbytes = WL.T * BYTES_PER_POS_LAYER
         lach = lbytes / (lavg * 1e-3) / 1e9
-        long = {"context": args.long_context, "value": ltot * 1e3 / (LAYERS * lsteps * world),
-                "unit": "us/layer-token", "decode_kernel_us": lavg * 1e3,
-                "roofline": {"bound": "hbm", "achieved": lach, "peak": peak, "unit": "GB/s", "frac": lach / peak,
-                             "traffic": TRAFFIC_BYTES.get(args.long_context), "bytes_per_launch": lbytes,
-                             "kernel": "decode_q4_round_kernel"},
-                "clocks": clk2.summary()}
+        c2 = clk2.summary()
+        long = {"context": args.long_context, "value": _r(ltot * 1e3 / (LAYERS * lsteps * world)),
+                "unit": "us/layer-token", "steps": lsteps, "decode_kernel_us": _r(lavg * 1e3),
+                "achieved": _r(lach), "peak": peak, "frac": _r(lach / peak, 3),
+                "traffic": traffic_bytes(args.long_context), "bytes_per_launch": lbytes,
+                "clocks": {"sm_mhz": c2["sm_mhz"], "sm_max_mhz": c2["sm_max_mhz"], "reasons": c2["reasons"],
+                           "samples": c2["samples"]}}
         del WL
 
     rows = None
@@ -876,10 +1117,18 @@ def main():
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
-        us, desc = cpu_baseline_decode(args.context, HQ)
-        cpu = {"value": us, "unit": "us/layer-token", "cores": 1, "kind": "oracle", "sample": desc}
+        legs, workers = cpu_baselines()
+        c1 = legs["c1_32k_16_layers"]
+        cpu = {"value": c1["value"], "unit": c1["unit"], "cores": 1, "kind": "oracle", "sample": c1["sample"],
+               "host_cores": os.cpu_count(), "legs_side_by_side": workers,
+               "configs": {k: {kk: (_r(vv) if isinstance(vv, float) else vv) for kk, vv in v.items()
+                               if kk != "sample"} for k, v in legs.items()},
+               "samples": {k: v["sample"] for k, v in legs.items()}}
 
     if rank == 0:
+        if rows is not None:
+            # the other rows in full, on a line of their own ahead of the headline
+            print(json.dumps({"rows": rows}))
         line = {
             "metric": METRIC,
             "value": us_per_lt, "unit": "us/layer-token", "n_gpus": world, "steps": args.steps,
@@ -888,14 +1137,17 @@ def main():
             "data": "synthetic",
             "config": workload_config(args.context, world),
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                         "traffic": TRAFFIC_BYTES.get(args.context), "bytes_per_launch": bytes_per_launch,
+                         "traffic": traffic_bytes(args.context), "bytes_per_launch": bytes_per_launch,
                          "kernel": "decode_q4_round_kernel",
-                         "decode_kernel_us": dec_avg_ms * 1e3, "peak_kind": peak_kind},
-            "e2e": {"value": e2e_us, "unit": "us/layer-token", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+                         "decode_kernel_us": dec_avg_ms * 1e3, "peak_kind": peak_kind,
+                         "long_context": None if long is None else
+                         {k: long[k] for k in ("context", "value", "decode_kernel_us", "achieved", "frac", "traffic")},
+                         "other_kernels": None if rows is None else rows_summary(rows)},
+            "e2e": {"value": c_us, "unit": "us/layer-token", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                    "path": "per call through the C ABI (48 calls per step)", "graph_replay_value": g_us},
             "gpu_launches": launches,
             "clocks": clk.summary(),
             "long_context": long,
-            "rows": rows,
             "cpu_baseline": cpu,
         }
         print(json.dumps(line))

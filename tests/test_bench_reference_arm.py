@@ -25,4 +25,21 @@ def test_reference_arm_line():
     assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["sample"]
     assert cb["value"] == d["value"] > 0
     assert d["e2e"] == {"value": d["value"], "unit": d["unit"], "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
-    assert abs(d["ms_per_step"] - d["value"] * 16 / 1e3) < 1e-6 * d["ms_per_step"]
+    # one step is one timed layer-token: no extrapolation between the two
+    assert d["step"] == "one layer-token"
+    assert abs(d["ms_per_step"] - d["value"] / 1e3) < 1e-6 * d["ms_per_step"]
+
+
+def test_traffic_is_reported_only_for_the_captured_sources(monkeypatch):
+    """The ncu traffic figure belongs to the kernel sources it was captured on:
+    once their hash differs, the bench reports none."""
+    cap = dict(bench.TRAFFIC_CAPTURE)
+    monkeypatch.setattr(bench, "TRAFFIC_CAPTURE", dict(cap, sources_sha16=bench.sources_sha16()))
+    assert bench.traffic_bytes(32768) == cap["bytes"][32768]
+    monkeypatch.setattr(bench, "TRAFFIC_CAPTURE", dict(cap, sources_sha16="0" * 16))
+    assert bench.traffic_bytes(32768) is None
+
+
+def test_rows_summary_keeps_the_floats():
+    rows = {"store": {"workload": "text", "us": 12.345678, "rows_per_s": 2.5e9, "cache_bytes": 123}}
+    assert bench.rows_summary(rows) == {"store": {"us": 12.35, "rows_per_s": 2.5e9}}
