@@ -129,6 +129,31 @@ static int32_t check_decode_shape(const kvq_cache* c, int B, int Hq, const int32
   return KVQ_OK;
 }
 
+// The host-side checks of kvq_decode_attn followed by kvq_merge on one
+// workspace of ws_bytes bytes, without enqueuing anything (used by the entry
+// point whose workspace is the library's own scratch array, so that an invalid
+// call leaves no work behind).
+int32_t check_decode_and_merge(const kvq_cache* cache, const float* q, int32_t num_seqs, int32_t num_q_heads,
+                               const int32_t* d_seq_lens, const int32_t* d_block_tables, int32_t max_pages_per_seq,
+                               int32_t max_seq_len, const int32_t* d_sel, int32_t n_sel, int32_t rotate_back,
+                               const float* out, size_t ws_bytes) {
+  int32_t st = check_cache(cache);
+  if (st != KVQ_OK) return st;
+  if (n_sel < 0 || n_sel > 4096) return KVQ_ERR_INVALID_ARG;
+  st = check_decode_shape(cache, num_seqs, num_q_heads, d_seq_lens, max_seq_len, d_sel != nullptr, n_sel);
+  if (st != KVQ_OK) return st;
+  if (rotate_back && cache->format != KVQ_FMT_Q4_HAD32 && cache->format != KVQ_FMT_TQ4) return KVQ_ERR_INVALID_ARG;
+  if (num_seqs == 0) return KVQ_OK;
+  if (!q || !aligned16(q) || !d_block_tables || max_pages_per_seq < 1 || !out) return KVQ_ERR_INVALID_ARG;
+  if (!d_sel && static_cast<int64_t>(max_seq_len) > static_cast<int64_t>(max_pages_per_seq) * cache->page_size)
+    return KVQ_ERR_INVALID_ARG;
+  if (ws_bytes < ws_layout(cache, num_seqs, num_q_heads, max_seq_len, d_sel ? n_sel : 0).total)
+    return KVQ_ERR_WORKSPACE_TOO_SMALL;
+  if (!d_sel && static_cast<uint64_t>(cache->num_pages) * cache->num_kv_heads * cache->page_size >= (1ull << 31))
+    return KVQ_ERR_UNSUPPORTED;
+  return KVQ_OK;
+}
+
 }  // namespace kvq
 
 using namespace kvq;

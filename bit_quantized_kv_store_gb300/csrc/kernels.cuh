@@ -90,6 +90,13 @@ struct PrefillArgs {
   int rotate;  // 1: Hadamard format (rotate q, rotate the output back); 0: Q4_0
 };
 
+// The host-side checks of kvq_decode_attn + kvq_merge on a workspace of ws_bytes
+// bytes (api.cu); enqueues nothing.
+int32_t check_decode_and_merge(const kvq_cache* cache, const float* q, int32_t num_seqs, int32_t num_q_heads,
+                               const int32_t* d_seq_lens, const int32_t* d_block_tables, int32_t max_pages_per_seq,
+                               int32_t max_seq_len, const int32_t* d_sel, int32_t n_sel, int32_t rotate_back,
+                               const float* out, size_t ws_bytes);
+
 // Remember a failed CUDA call for kvq_last_cuda_error(); returns KVQ_ERR_CUDA.
 int32_t record_cuda_failure(cudaError_t e);
 

@@ -9,14 +9,21 @@
 // with the partials in a fixed, file-scope device array instead.
 //
 // The array is kKvqStaticScratchBytes (16 MiB) of device memory that every GPU
-// loading this library holds until the process exits.  Its device address is
-// looked up once per device (cudaGetSymbolAddress with that device current) on
-// the first call made on that device; make that first call before any stream
-// capture begins.  Every call shares the array and the array keeps the last
+// loading this library holds until the process exits.  Host code cannot use the
+// array's name as a device address: its address is looked up with
+// cudaGetSymbolAddress, with the device current, and cached per device together
+// with the unique ID of the CUDA context it was looked up in.  A call made in
+// another context (a non-primary context the caller made current, or the
+// primary context re-created after cudaDeviceReset) looks the address up again.
+// This translation unit is its own module, which CUDA loads lazily: the first
+// lookup in a context loads it and commits the 16 MiB there, so that first call
+// must come outside any region where the caller cannot allocate, and before any
+// stream capture.  Every call shares the array and the array keeps the last
 // call's contents: the status word is cleared on the stream at the start of each
-// call, and calls whose work overlaps on the GPU (different streams or devices
-// sharing a context without ordering) race on it.
-#include <atomic>
+// call, and calls whose work overlaps on the GPU (different streams without
+// ordering) race on it.
+#include <cudaTypedefs.h>
+
 #include <mutex>
 
 #include "kernels.cuh"
@@ -28,25 +35,65 @@ constexpr size_t kKvqStaticScratchBytes = size_t(16) << 20;
 static __device__ __align__(256) uint8_t g_static_scratch[kKvqStaticScratchBytes];
 
 constexpr int kMaxDevices = 64;
-static std::atomic<void*> g_scratch_ptr[kMaxDevices];
+struct ScratchAddr {
+  unsigned long long ctx_id;  // unique ID of the context the address belongs to (0: none yet)
+  void* ptr;
+};
+static ScratchAddr g_scratch[kMaxDevices];
 static std::mutex g_scratch_mu;
 
-// Device address of the scratch array on the current device (looked up once).
+// cuCtxGetCurrent / cuCtxGetId through the runtime's driver entry points (no
+// link-time dependency on libcuda); looked up once.
+struct CtxQueries {
+  PFN_cuCtxGetCurrent_v4000 current = nullptr;
+  PFN_cuCtxGetId_v12000 id = nullptr;
+};
+static const CtxQueries& ctx_queries() {
+  static const CtxQueries q = [] {
+    CtxQueries r;
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult st;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 4000, cudaEnableDefault, &st) == cudaSuccess &&
+        st == cudaDriverEntryPointSuccess)
+      r.current = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(p);
+    p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &st) == cudaSuccess &&
+        st == cudaDriverEntryPointSuccess)
+      r.id = reinterpret_cast<PFN_cuCtxGetId_v12000>(p);
+    return r;
+  }();
+  return q;
+}
+
+// ID of the calling thread's current context, 0 if there is none (or it cannot
+// be read, in which case the address is looked up on every call).
+static unsigned long long current_ctx_id() {
+  const CtxQueries& q = ctx_queries();
+  if (!q.current || !q.id) return 0;
+  CUcontext ctx = nullptr;
+  if (q.current(&ctx) != CUDA_SUCCESS || !ctx) return 0;
+  unsigned long long id = 0;
+  if (q.id(ctx, &id) != CUDA_SUCCESS) return 0;
+  return id;
+}
+
+// Device address of the scratch array in the current device's current context.
 static cudaError_t static_scratch(void** out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-  void* p = g_scratch_ptr[dev].load(std::memory_order_acquire);
-  if (!p) {
-    std::lock_guard<std::mutex> lock(g_scratch_mu);
-    p = g_scratch_ptr[dev].load(std::memory_order_relaxed);
-    if (!p) {
-      e = cudaGetSymbolAddress(&p, g_static_scratch);
-      if (e != cudaSuccess) return e;
-      g_scratch_ptr[dev].store(p, std::memory_order_release);
-    }
+  std::lock_guard<std::mutex> lock(g_scratch_mu);
+  unsigned long long id = current_ctx_id();
+  if (id != 0 && g_scratch[dev].ctx_id == id) {
+    *out = g_scratch[dev].ptr;
+    return cudaSuccess;
   }
+  void* p = nullptr;
+  e = cudaGetSymbolAddress(&p, g_static_scratch);  // binds the primary context if none was current
+  if (e != cudaSuccess) return e;
+  if (id == 0) id = current_ctx_id();
+  g_scratch[dev] = ScratchAddr{id, id != 0 ? p : nullptr};
   *out = p;
   return cudaSuccess;
 }
@@ -63,22 +110,25 @@ int32_t kvq_decode_noalloc(const kvq_cache* cache, const float* q, int32_t num_s
                            const int32_t* d_seq_lens, const int32_t* d_block_tables, int32_t max_pages_per_seq,
                            int32_t max_seq_len, const int32_t* d_sel, int32_t n_sel, float sm_scale,
                            int32_t rotate_back, float* out, int32_t* d_status_out, void* stream) {
-  const size_t need = kvq_decode_workspace_size(cache, num_seqs, num_q_heads, max_seq_len, d_sel ? n_sel : 0);
-  if (cache == nullptr || need == 0) return KVQ_ERR_INVALID_ARG;
-  if (need > kKvqStaticScratchBytes) return KVQ_ERR_WORKSPACE_TOO_SMALL;
+  if (cache == nullptr) return KVQ_ERR_INVALID_ARG;
+  const int32_t ns = d_sel ? n_sel : 0;
+  if (kvq_decode_workspace_size(cache, num_seqs, num_q_heads, max_seq_len, ns) == 0) return KVQ_ERR_INVALID_ARG;
+  // every check of the two calls below, before anything is enqueued
+  int32_t st = check_decode_and_merge(cache, q, num_seqs, num_q_heads, d_seq_lens, d_block_tables, max_pages_per_seq,
+                                      max_seq_len, d_sel, ns, rotate_back, out, kKvqStaticScratchBytes);
+  if (st != KVQ_OK) return st;
   if (num_seqs == 0) return KVQ_OK;
-  if (!out) return KVQ_ERR_INVALID_ARG;
   void* ws = nullptr;
   cudaError_t e = static_scratch(&ws);
   if (e != cudaSuccess) return record_cuda_failure(e);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   e = cudaMemsetAsync(ws, 0, sizeof(int32_t), s);  // the status word must start at zero
   if (e != cudaSuccess) return record_cuda_failure(e);
-  int32_t st = kvq_decode_attn(cache, q, num_seqs, num_q_heads, d_seq_lens, d_block_tables, max_pages_per_seq,
-                               max_seq_len, d_sel, d_sel ? n_sel : 0, sm_scale, ws, kKvqStaticScratchBytes, stream);
+  st = kvq_decode_attn(cache, q, num_seqs, num_q_heads, d_seq_lens, d_block_tables, max_pages_per_seq, max_seq_len,
+                       d_sel, ns, sm_scale, ws, kKvqStaticScratchBytes, stream);
   if (st != KVQ_OK) return st;
-  st = kvq_merge(cache, ws, kKvqStaticScratchBytes, num_seqs, num_q_heads, d_seq_lens, max_seq_len,
-                 d_sel ? n_sel : 0, rotate_back, out, stream);
+  st = kvq_merge(cache, ws, kKvqStaticScratchBytes, num_seqs, num_q_heads, d_seq_lens, max_seq_len, ns, rotate_back,
+                 out, stream);
   if (st != KVQ_OK) return st;
   if (d_status_out) {
     e = cudaMemcpyAsync(d_status_out, ws, sizeof(int32_t), cudaMemcpyDeviceToDevice, s);

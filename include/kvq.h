@@ -19,7 +19,8 @@
  * Conventions for every entry point:
  *  - Pointers named d_* or documented as "device" are device pointers owned by the
  *    caller.  The library never allocates, frees or keeps device memory between
- *    calls and holds no global mutable state; calls are reentrant.
+ *    calls and holds no global mutable state; calls are reentrant.  (The one
+ *    exception is kvq_decode_noalloc's fixed scratch array, described there.)
  *  - `stream` is a cudaStream_t (NULL = the legacy default stream).  All work is
  *    enqueued asynchronously on it.
  *  - Host-side arguments are validated before anything is launched; on failure a
@@ -245,6 +246,10 @@ int32_t kvq_decode_attn(const kvq_cache* cache, const float* q, int32_t num_seqs
  *   4-bit formats only (else KVQ_ERR_UNSUPPORTED); 1 <= num_rows <= 64.
  * Workspace (kvq_decode_workspace_size with num_seqs = num_rows) and errors as
  * for kvq_decode_attn. */
+int32_t kvq_decode_window(const kvq_cache* cache, const float* q, int32_t num_rows, int32_t num_q_heads,
+                          const int32_t* d_row_lens, const int32_t* d_block_table, int32_t max_pages,
+                          int32_t max_seq_len, float sm_scale, void* workspace, size_t ws_bytes, void* stream);
+
 /* kvq_decode_merged -- kvq_decode_attn and kvq_merge (with the rotation back for
  * Q4_HAD32) in one launch ([P1] "What it is": the shared 512-key chunks and the
  * in-order merge of one decode round): the last CTA of each (sequence, KV head)
@@ -261,10 +266,6 @@ int32_t kvq_decode_merged(const kvq_cache* cache, const float* q, int32_t num_se
                           const int32_t* d_seq_lens, const int32_t* d_block_tables, int32_t max_pages_per_seq,
                           int32_t max_seq_len, float sm_scale, void* workspace, size_t ws_bytes, float* out,
                           void* stream);
-
-int32_t kvq_decode_window(const kvq_cache* cache, const float* q, int32_t num_rows, int32_t num_q_heads,
-                          const int32_t* d_row_lens, const int32_t* d_block_table, int32_t max_pages,
-                          int32_t max_seq_len, float sm_scale, void* workspace, size_t ws_bytes, void* stream);
 
 /* kvq_decode_attn_unrotated -- kvq_decode_attn for the 4-bit format with the
  * query rotation done inside the decode kernel ([P1] "What it is": the query
@@ -310,8 +311,6 @@ int32_t kvq_prefill_attn(const kvq_cache* cache, const void* q, int32_t dtype, i
                          int32_t num_q_heads, int32_t q_start, const int32_t* d_block_table,
                          int32_t max_pages, float sm_scale, float* out, int32_t* d_status, void* stream);
 
-/* Copy the device status word at the start of a decode workspace (or any
- * device int32) to *host_code; synchronises `stream`. */
 /* Size in bytes of the workspace kvq_prefill_attn_fp8 needs: a 256-byte header
  * (status word at offset 0), then m, z [n_q][num_q_heads] f32 and acc
  * [n_q][num_q_heads][512] f32 (one partial per row and head). */
@@ -335,6 +334,8 @@ int32_t kvq_prefill_attn_fp8(const kvq_cache* cache, const float* q, int32_t n_q
                              int32_t q_start, const int32_t* d_block_table, int32_t max_pages, float sm_scale,
                              void* workspace, size_t ws_bytes, float* out, void* stream);
 
+/* Copy the device status word at the start of a decode workspace (or any
+ * device int32) to *host_code; synchronises `stream`. */
 int32_t kvq_read_status(const void* d_status, int32_t* host_code, void* stream);
 
 /* kvq_selftest_wait_timeout -- diagnostic of the kernels' copy waits: one CTA
@@ -348,19 +349,25 @@ int32_t kvq_selftest_wait_timeout(int32_t* d_status, void* stream);
  * cannot allocate device memory when they decode (a host that owns every device
  * allocation, a memory pool that forbids new ones, a latency-critical path that
  * cannot afford cudaMalloc).  The pages have no counterpart: this is an
- * interface convenience of this library, with the same arithmetic as the two
- * calls it replaces.
+ * interface convenience of this library, with the same arithmetic (and the same
+ * output bits) as the two calls it replaces.
  * Instead of a caller workspace it uses one file-scope device array of
  * kvq_noalloc_scratch_bytes() bytes (16 MiB), which every GPU that loads the
  * library holds until the process exits.  Problems whose workspace
  * (kvq_decode_workspace_size) exceeds it are rejected with
- * KVQ_ERR_WORKSPACE_TOO_SMALL before anything is enqueued.
- * The first call on a device looks the array's address up
- * (cudaGetSymbolAddress, with that device current): make that first call before
- * any stream capture.  The call allocates and frees nothing.  All calls share the
- * array and it keeps the last call's contents; the status word is cleared on
- * `stream` at the start of every call.  Calls whose GPU work overlaps (on
- * different streams without ordering) race on the array.
+ * KVQ_ERR_WORKSPACE_TOO_SMALL.  Every argument check of the two calls runs
+ * before anything is enqueued; an invalid call enqueues nothing.
+ * Set-up: the array's device address is looked up (cudaGetSymbolAddress, with
+ * the device current) on the first call in each CUDA context and cached with
+ * that context's ID; a call in another context (a non-primary context made
+ * current by the caller, or the primary context re-created after
+ * cudaDeviceReset) looks it up again.  The library loads its modules lazily, so
+ * that first call also loads the array's module and commits its 16 MiB of
+ * device memory: make it outside any region where the caller cannot allocate,
+ * and before any stream capture.  Later calls allocate and free nothing.
+ * All calls share the array and it keeps the last call's contents; the status
+ * word is cleared on `stream` at the start of every call.  Calls whose GPU work
+ * overlaps (on different streams without ordering) race on the array.
  * Arguments as for kvq_decode_attn and kvq_merge; d_status_out (optional device
  * int32) receives a copy of the call's status word. */
 size_t kvq_noalloc_scratch_bytes(void);

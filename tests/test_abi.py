@@ -194,6 +194,20 @@ def test_host_validation_of_the_other_entries(K):
     assert L.kvq_decode_noalloc(*na(c=None)) == K.ERR_INVALID_ARG
     assert L.kvq_decode_noalloc(*na(B=64, msl=262145)) == K.ERR_WORKSPACE_TOO_SMALL
     assert L.kvq_decode_noalloc(*na(out=None)) == K.ERR_INVALID_ARG
+    # every check of the decode and the merge comes before the status word is
+    # cleared: with no GPU here, a call that got past them would fail with
+    # KVQ_ERR_CUDA instead
+    na_rb = lambda c, rb, q=dummy: (ctypes.byref(c), q, 1, 24, dummy, dummy, 100000, 1000, None, 0, f, rb, dummy,
+                                    None, None)
+    assert L.kvq_decode_noalloc(*na_rb(bf, 1)) == K.ERR_INVALID_ARG      # rotate_back on bf16 rows (merge's check)
+    assert L.kvq_decode_noalloc(*na_rb(d, 1, q=None)) == K.ERR_INVALID_ARG
+    assert L.kvq_decode_noalloc(*na_rb(d, 1, q=ctypes.c_void_p(4100))) == K.ERR_INVALID_ARG   # unaligned query
+    assert L.kvq_decode_noalloc(ctypes.byref(d), dummy, 1, 24, dummy, None, 100000, 1000, None, 0, f, 1, dummy,
+                                None, None) == K.ERR_INVALID_ARG   # no block table
+    assert L.kvq_decode_noalloc(ctypes.byref(d), dummy, 1, 24, dummy, dummy, 10, 1000, None, 0, f, 1, dummy,
+                                None, None) == K.ERR_INVALID_ARG   # 10 pages of 16 < 1000 keys
+    assert L.kvq_decode_noalloc(ctypes.byref(d), dummy, 0, 24, None, None, 0, 0, None, 0, f, 1, None,
+                                None, None) == K.OK                # nothing to do, nothing enqueued
     # status helpers
     assert L.kvq_selftest_wait_timeout(None, None) == K.ERR_INVALID_ARG
     assert L.kvq_read_status(None, dummy, None) == K.ERR_INVALID_ARG
