@@ -13,7 +13,8 @@ import os
 import torch
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_PKG, "_build", "libkvq.so")
+# KVQ_SANITIZE=1: the host-sanitizer build (argument validation checked on the CPU)
+LIB_PATH = os.path.join(_PKG, "_build_san" if os.environ.get("KVQ_SANITIZE") == "1" else "_build", "libkvq.so")
 
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_WORKSPACE_TOO_SMALL = 0, -1, -2, -3, -4
 DEV_BAD_SLOT, DEV_BAD_PAGE, DEV_BAD_LENGTH, DEV_BAD_INDEX, DEV_TIMEOUT = 1, 2, 4, 8, 16

@@ -14,11 +14,19 @@ import subprocess
 PKG = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
-BUILD = os.path.join(PKG, "_build")
+# KVQ_SANITIZE=1: a separate build of the host code with AddressSanitizer and
+# UndefinedBehaviorSanitizer, for checking the C ABI's argument validation on
+# the CPU (device code as PTX only: that build never launches a kernel).
+SANITIZE = os.environ.get("KVQ_SANITIZE") == "1"
+BUILD = os.path.join(PKG, "_build_san" if SANITIZE else "_build")
 LIB = os.path.join(BUILD, "libkvq.so")
 
-ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
+ARCH = ["-gencode", "arch=compute_103a,code=compute_103a" if SANITIZE else "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", f"-I{os.path.join(ROOT, 'include')}"]
+SAN_FLAGS = ["-Xcompiler", "-fsanitize=address", "-Xcompiler", "-fsanitize=undefined",  # (-Xcompiler splits at commas)
+             "-Xcompiler", "-fno-sanitize-recover=undefined", "-Xcompiler", "-fno-omit-frame-pointer"]
+if SANITIZE:
+    FLAGS = FLAGS + SAN_FLAGS
 # The store computes codes that must be bit-exact: no fused multiply-adds there.
 PER_FILE = {"store.cu": ["-fmad=false"], "tq4.cu": ["-fmad=false"]}
 
@@ -65,7 +73,7 @@ def build(verbose_ptxas=False) -> str:
                 print(log)
     if not os.path.exists(LIB) or os.path.getmtime(LIB) < max(os.path.getmtime(o) for o in objs):
         tmp = LIB + f".tmp{os.getpid()}"
-        cmd = [_nvcc(), *ARCH, "-shared", "-o", tmp, *objs]
+        cmd = [_nvcc(), *ARCH, "-shared", "-o", tmp, *objs, *(SAN_FLAGS if SANITIZE else [])]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")

@@ -21,7 +21,11 @@ import numpy as np
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "kvq_oracle.c")
-_LIB_PATH = os.path.join(_HERE, "_build", "libkvq_oracle.so")
+# KVQ_SANITIZE=1: a separate build with AddressSanitizer and UndefinedBehaviorSanitizer
+# (run the process with the ASan runtime preloaded; the sanitizer test does).
+_SANITIZE = os.environ.get("KVQ_SANITIZE") == "1"
+_LIB_PATH = os.path.join(_HERE, "_build", "libkvq_oracle_san.so" if _SANITIZE else "libkvq_oracle.so")
+_SAN_FLAGS = ["-O1", "-g", "-fno-omit-frame-pointer", "-fsanitize=address,undefined", "-fno-sanitize-recover=undefined"]
 _lock = threading.Lock()
 _lib = None
 
@@ -37,7 +41,8 @@ def build(force: bool = False) -> str:
     os.makedirs(os.path.dirname(_LIB_PATH), exist_ok=True)
     if force or not os.path.exists(_LIB_PATH) or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC):
         tmp = _LIB_PATH + f".tmp{os.getpid()}"
-        subprocess.check_call(["gcc", "-O2", "-ffp-contract=off", "-fPIC", "-shared", "-std=c11",
+        opt = _SAN_FLAGS if _SANITIZE else ["-O2"]
+        subprocess.check_call(["gcc", *opt, "-ffp-contract=off", "-fPIC", "-shared", "-std=c11",
                                "-o", tmp, _SRC, "-lm"])
         os.replace(tmp, _LIB_PATH)
     return _LIB_PATH
