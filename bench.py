@@ -631,16 +631,19 @@ def run_reference(args):
 # --------------------------------------------------------------------------- the other hot-path rows
 
 L2_BYTES = 129 * 2 ** 20
-_flush_buf = None
+_flush_bufs = None
 
 
 def _l2_flush(torch):
-    """Overwrite a buffer of twice the L2 size, so that the next launch finds none
-    of its inputs in L2."""
-    global _flush_buf
-    if _flush_buf is None:
-        _flush_buf = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device="cuda")
-    _flush_buf.zero_()
+    """Write a buffer of twice the L2 size, then read another one of the same
+    size: the next launch finds none of its inputs in L2, and L2 holds clean
+    lines only (no write-back of the flush's own lines lands in the timed
+    region)."""
+    global _flush_bufs
+    if _flush_bufs is None:
+        _flush_bufs = [torch.zeros(2 * L2_BYTES // 4, dtype=torch.float32, device="cuda") for _ in range(2)]
+    _flush_bufs[0].zero_()
+    _flush_bufs[1].sum()
 
 
 def _events_time(torch, fn, iters, warmup=3, flush=True):

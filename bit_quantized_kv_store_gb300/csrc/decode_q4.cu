@@ -480,8 +480,11 @@ __device__ __forceinline__ void q4_fused_merge(const DecodeArgs& a, int b, int k
 // sequence, row-major: the rows share the block table and so every key, whose
 // codes are then converted once for all of them; each row keeps its own causal
 // end (its length), its own softmax state and its own partials.
-template <bool GATHER, int NT, bool WIN, bool TQ = false, bool LM = false>
-__global__ void __launch_bounds__(kQ4Warps * 32, q4_min_blocks(NT))
+// MINB: resident CTAs per SM the registers are budgeted for (0: q4_min_blocks);
+// a grid that fits in two CTAs per SM takes MINB = 2 (up to 255 registers, more
+// score chains in flight per warp).  The arithmetic is the same PTX either way.
+template <bool GATHER, int NT, bool WIN, bool TQ = false, bool LM = false, int MINB = 0>
+__global__ void __launch_bounds__(kQ4Warps * 32, MINB ? MINB : q4_min_blocks(NT))
     decode_q4_round_kernel(const __grid_constant__ DecodeArgs a) {
   static_assert(!(WIN && GATHER), "decode windows read dense prefixes");
   static_assert(WIN || NT == 1, "one sequence's group fills one column tile");
@@ -743,8 +746,8 @@ __global__ void __launch_bounds__(kQ4Warps * 32, q4_min_blocks(NT))
             const float sa = e ? fsa[u].y : fsa[u].x, sb = e ? fsb[u].y : fsb[u].x;
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt) {
-              float part[4] = {nb[nt].x, nb[nt].y, nb[nt].z, nb[nt].w};
-              mma_f16(part, a10, a11, a12, a13, qh[nt].x, qh[nt].y);
+              float part[4];
+              mma_f16_c(part, a10, a11, a12, a13, qh[nt].x, qh[nt].y, nb[nt].x, nb[nt].y, nb[nt].z, nb[nt].w);
               mma_f16(part, a20, a21, a22, a23, qh[nt].z, qh[nt].w);
               mma_f16(part, a10, a11, a12, a13, ql[nt].x, ql[nt].y);
               mma_f16(part, a20, a21, a22, a23, ql[nt].z, ql[nt].w);
@@ -1053,10 +1056,10 @@ __global__ void __launch_bounds__(kQ4Warps * 32, q4_min_blocks(NT))
   pdl_trigger();  // after this CTA's last write
 }
 
-template <bool GATHER, int NT, bool WIN, bool TQ = false, bool LM = false>
+template <bool GATHER, int NT, bool WIN, bool TQ = false, bool LM = false, int MINB = 0>
 cudaError_t launch_round(const DecodeArgs& a, dim3 grid, cudaStream_t s) {
   const size_t smem = sizeof(Q4Smem<NT, GATHER>) + 1024;  // + slack for the 1024-byte alignment
-  auto kern = decode_q4_round_kernel<GATHER, NT, WIN, TQ, LM>;
+  auto kern = decode_q4_round_kernel<GATHER, NT, WIN, TQ, LM, MINB>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   e = launch_pdl(kern, grid, dim3(kQ4Warps * 32), smem, s, a);
@@ -1066,13 +1069,24 @@ cudaError_t launch_round(const DecodeArgs& a, dim3 grid, cudaStream_t s) {
 
 }  // namespace q4r
 
+// Streaming multiprocessors of the current device.
+static int sm_count() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return 0;
+  return n;
+}
+
 cudaError_t launch_decode_q4(const DecodeArgs& a, int B, cudaStream_t s) {
   using namespace q4r;
   if (a.nrows <= 0) {
     const dim3 grid(a.P, a.c.num_kv_heads, B);
     if (a.tq) return a.sel ? cudaErrorInvalidValue : launch_round<false, 1, false, true>(a, grid, s);
     if (a.fused_out) return a.sel ? cudaErrorInvalidValue : launch_round<false, 1, false, false, true>(a, grid, s);
-    return a.sel ? launch_round<true, 1, false>(a, grid, s) : launch_round<false, 1, false>(a, grid, s);
+    if (a.sel) return launch_round<true, 1, false>(a, grid, s);
+    const int64_t ctas = (int64_t)grid.x * grid.y * grid.z;
+    if (ctas <= 2 * (int64_t)sm_count()) return launch_round<false, 1, false, false, false, 2>(a, grid, s);
+    return launch_round<false, 1, false>(a, grid, s);
   }
   if (a.tq) return cudaErrorInvalidValue;
   // Decode window: the rows are cut into the fewest even slices whose

@@ -18,74 +18,173 @@
 
 namespace kvq {
 
-// One warp per (token, KV head, K|V) row of D = 32*NG values.
-// Lane i handles element 32G + i of every group G.  ROT = false: the unrotated
-// Q4_0 format (the values as given).
-template <int NG, bool ROT>
-__global__ void __launch_bounds__(256) store_q4_kernel(kvq_cache c, const void* __restrict__ k,
-                                                       const void* __restrict__ v, int dtype, int64_t n_tok,
-                                                       const int32_t* __restrict__ slots, int32_t* status) {
+// ---------------------------------------------------------------- the 4-bit code of one value
+// code = clamp(rint_even(fl(y / s)), -8, 7) + 8, with fl(y / s) the IEEE-rounded
+// fp32 quotient and s > 0 (an fp16 value, so a normal fp32 number).
+//
+// Screen: q0 = fl(y * r) with r = rcp.approx(s) (at most 1 ulp off, PTX ISA)
+// is within a relative 2^-22 of the exact quotient Q.  While |Q| < 16 that is
+// an absolute error below 2^-18, and fl(Q) is within 2^-21 of Q; so when q0 is
+// farther than 2^-14 from every half-integer, Q and fl(Q) lie strictly inside
+// the same unit interval (k - 1/2, k + 1/2) around k = rint(q0), and
+// rint_even(fl(Q)) = k without a tie.  (For |Q| >= 16 both k and rint(fl(Q))
+// are beyond the clamp on the same side.)  Anything else -- exact or near ties,
+// NaN, infinities -- takes the IEEE division.
+constexpr float kQ4Screen = 0.5f - 0.00006103515625f;  // 1/2 - 2^-14
+
+__device__ __forceinline__ float rcp_approx(float x) {
+  float r;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+  return r;
+}
+
+// The code from the screened estimate; returns false when the estimate cannot
+// decide it (then call q4_code_exact).
+__device__ __forceinline__ bool q4_code_screened(float y, float r, uint32_t& code) {
+  const float q0 = __fmul_rn(y, r);
+  const float k = rintf(q0);
+  code = static_cast<uint32_t>(static_cast<int>(fminf(fmaxf(k, -8.0f), 7.0f)) + 8);
+  return fabsf(__fsub_rn(q0, k)) < kQ4Screen;
+}
+
+__device__ __forceinline__ uint32_t q4_code_exact(float y, float s) {
+  float q = rintf(__fdiv_rn(y, s));
+  q = fminf(fmaxf(q, -8.0f), 7.0f);
+  return static_cast<uint32_t>(static_cast<int>(q) + 8);
+}
+
+// Bulk form (a prompt chunk): a warp takes kWideSets sets of 8 groups of 32
+// values (a set is one 256-wide row, or 8 / NG narrower rows), lane L holding
+// the 8 consecutive elements 8t .. 8t + 7 (t = L & 3) of group L >> 2 of each
+// set.  The butterfly's stages h = 1, 2, 4 then run inside a lane and h = 8, 16
+// across the group's four lanes: the same additions and subtractions of the
+// same operands as the one-element-per-lane form, with a quarter of the
+// shuffles and selects, and the lane's 8 codes are one 32-bit word of the row
+// (bytes 16G + 4t .. 16G + 4t + 3).  Every load of the warp (its sets' values
+// and slots) is issued before any is used, so the loads of both sets and the
+// slot lookups overlap instead of queueing behind each other.  VEC: the inputs
+// are 16-byte aligned, so a lane loads its 8 values with one (bf16) or two
+// (f32) 16-byte loads.  ROT = false: the unrotated Q4_0 format.
+constexpr int kWideSets = 2;
+
+template <int NG, bool ROT, bool VEC>
+__global__ void __launch_bounds__(256) store_q4_wide_kernel(kvq_cache c, const void* __restrict__ k,
+                                                            const void* __restrict__ v, int dtype, int64_t n_tok,
+                                                            const int32_t* __restrict__ slots, int32_t* status) {
   pdl_wait();
   pdl_trigger();
   constexpr int D = NG * 32;
-  const int lane = threadIdx.x & 31;
-  const int64_t row = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31, t = lane & 3;
   const int Hk = c.num_kv_heads;
-  if (row >= n_tok * Hk * 2) return;
-  const int kv = static_cast<int>(row & 1);
-  const int64_t tok = (row >> 1) / Hk;
-  const int head = static_cast<int>((row >> 1) % Hk);
-  const int32_t slot = slots[tok];
-  if (slot < 0) return;
-  if ((int64_t)slot >= (int64_t)c.num_pages * c.page_size) {
-    if (lane == 0) set_status(status, KVQ_DEV_BAD_SLOT);
-    return;
+  const int64_t total = n_tok * Hk * 2 * NG;
+  const int64_t warp_id = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  // every lane of the warp stays to the end (the shuffles below are warp-wide);
+  // only lanes whose group exists and whose slot is valid store
+  int64_t gg[kWideSets];
+  bool in_range[kWideSets];
+  int32_t slot[kWideSets];
+  float x[kWideSets][8];
+#pragma unroll
+  for (int j = 0; j < kWideSets; ++j) {
+    gg[j] = (warp_id * kWideSets + j) * 8 + (lane >> 2);
+    in_range[j] = gg[j] < total;
+    const int64_t row = gg[j] / NG;
+    const int64_t tok = (row >> 1) / Hk;
+    const int head = static_cast<int>((row >> 1) % Hk);
+    const int G = static_cast<int>(gg[j] % NG);
+    const void* src = (row & 1) ? v : k;
+    const int64_t e0 = (tok * Hk + head) * D + 32 * G + 8 * t;  // first element of the lane
+    slot[j] = in_range[j] ? slots[tok] : -1;
+    if (!in_range[j]) {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) x[j][i] = 0.f;
+    } else if (VEC && dtype == KVQ_DT_BF16) {
+      const uint4 u = *reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(src) + e0);
+      const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        x[j][2 * i] = __uint_as_float(w[i] << 16);
+        x[j][2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+      }
+    } else if (VEC) {
+      const float4 a4 = *reinterpret_cast<const float4*>(static_cast<const float*>(src) + e0);
+      const float4 b4 = *reinterpret_cast<const float4*>(static_cast<const float*>(src) + e0 + 4);
+      x[j][0] = a4.x; x[j][1] = a4.y; x[j][2] = a4.z; x[j][3] = a4.w;
+      x[j][4] = b4.x; x[j][5] = b4.y; x[j][6] = b4.z; x[j][7] = b4.w;
+    } else {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) x[j][i] = load_act(src, dtype, e0 + i);
+    }
   }
-  const int64_t page = slot / c.page_size;
-  const int off = slot % c.page_size;
-  const int64_t r = (page * Hk + head) * c.page_size + off;
-  const void* src = kv ? v : k;
-  const int64_t base = (tok * Hk + head) * D;
-
-  // The warp's row is staged in shared memory (group G's 16 bytes at 16G) and
-  // then written with one 16-byte store per group.
-  __shared__ __align__(16) uint8_t stage[8][NG * 16];
-  uint8_t* my_stage = stage[threadIdx.x >> 5];
-  uint16_t scale16[NG];  // warp-uniform
 #pragma unroll
-  for (int G = 0; G < NG; ++G) {
-    float x = load_act(src, dtype, base + 32 * G + lane);
-    const float y = ROT ? __fmul_rn(warp_fwht32(x, lane), kHadamardScale) : x;
-    float amax = fabsf(y);
+  for (int j = 0; j < kWideSets; ++j) {
+    float* xs = x[j];
+    if (ROT) {
+      // stages h = 1, 2, 4: pairs (i, i + h) inside the lane, (a, b) -> (a + b, a - b)
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-    const float s32 = __fdiv_rn(amax, 8.0f);
+      for (int h = 1; h < 8; h <<= 1)
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+          if ((i & h) == 0) {
+            const float a = xs[i], b = xs[i + h];
+            xs[i] = __fadd_rn(a, b);
+            xs[i + h] = __fsub_rn(a, b);
+          }
+      // stages h = 8, 16: element 8t + i pairs with the same i of lane t ^ 1, t ^ 2;
+      // the lower lane keeps a + b, the upper one a - b (a the lower's value)
+#pragma unroll
+      for (int hl = 1; hl < 4; hl <<= 1) {
+        const bool upper = (t & hl) != 0;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const float o = __shfl_xor_sync(0xffffffffu, xs[i], hl);
+          xs[i] = upper ? __fsub_rn(o, xs[i]) : __fadd_rn(xs[i], o);
+        }
+      }
+#pragma unroll
+      for (int i = 0; i < 8; ++i) xs[i] = __fmul_rn(xs[i], kHadamardScale);
+    }
+    float amax = fabsf(xs[0]);
+#pragma unroll
+    for (int i = 1; i < 8; ++i) amax = fmaxf(amax, fabsf(xs[i]));
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+    const float s32 = __fmul_rn(amax, 0.125f);  // = amax / 8 correctly rounded (a power of two)
     __half s16 = __float2half_rn(s32);
     if (__hisinf(s16)) s16 = __ushort_as_half(0x7BFFu);  // saturate to 65504
     const float s = __half2float(s16);
-    int code = 8;
+    uint32_t word = 0x88888888u;  // scale 0: every code 8
+    bool undecided = false;
     if (s != 0.0f) {
-      float q = rintf(__fdiv_rn(y, s));
-      q = fminf(fmaxf(q, -8.0f), 7.0f);
-      code = static_cast<int>(q) + 8;
-    }
-    // gather the four codes of half-word h = lane/4 (elements 4h .. 4h+3) into lane 4h
-    uint32_t bits = static_cast<uint32_t>(code) << (4 * (lane & 3));
-    bits |= __shfl_xor_sync(0xffffffffu, bits, 1);
-    bits |= __shfl_xor_sync(0xffffffffu, bits, 2);
-    if ((lane & 3) == 0) reinterpret_cast<uint16_t*>(my_stage)[8 * G + (lane >> 2)] = static_cast<uint16_t>(bits);
-    scale16[G] = __half_as_ushort(s16);
-  }
-  __syncwarp();
-  uint8_t* codes = static_cast<uint8_t*>(kv ? c.v : c.k) + r * (D / 2);
-  if (lane < NG) reinterpret_cast<uint4*>(codes)[lane] = reinterpret_cast<const uint4*>(my_stage)[lane];
-  uint16_t* sc = static_cast<uint16_t*>(kv ? c.v_scale : c.k_scale) + r * NG;
-  if (lane < NG) {
-    uint16_t mine = 0;
+      const float r = rcp_approx(s);
+      word = 0;
 #pragma unroll
-    for (int G = 0; G < NG; ++G)
-      if (G == lane) mine = scale16[G];
-    sc[lane] = mine;
+      for (int i = 0; i < 8; ++i) {
+        uint32_t code;
+        undecided |= !q4_code_screened(xs[i], r, code);
+        word |= code << (4 * i);
+      }
+    }
+    if (__any_sync(0xffffffffu, undecided) && undecided) {  // rare: ties and near-ties
+      word = 0;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) word |= q4_code_exact(xs[i], s) << (4 * i);
+    }
+    if (in_range[j]) {
+      const int64_t row = gg[j] / NG;
+      const int G = static_cast<int>(gg[j] % NG);
+      const int sl = slot[j];
+      if (sl >= 0 && (int64_t)sl >= (int64_t)c.num_pages * c.page_size) {
+        if (t == 0 && G == 0) set_status(status, KVQ_DEV_BAD_SLOT);
+      } else if (sl >= 0) {
+        const int64_t r = ((int64_t)(sl / c.page_size) * Hk + static_cast<int>((row >> 1) % Hk)) * c.page_size +
+                          sl % c.page_size;
+        const bool is_v = (row & 1) != 0;
+        uint8_t* codes = static_cast<uint8_t*>(is_v ? c.v : c.k) + r * (D / 2);
+        reinterpret_cast<uint32_t*>(codes)[4 * G + t] = word;
+        if (t == 0) (static_cast<uint16_t*>(is_v ? c.v_scale : c.k_scale) + r * NG)[G] = __half_as_ushort(s16);
+      }
+    }
   }
 }
 
@@ -121,17 +220,13 @@ __device__ __forceinline__ void store_q4_group_warp(const kvq_cache& c, const vo
   float amax = fabsf(y);
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-  const float s32 = __fdiv_rn(amax, 8.0f);
+  const float s32 = __fmul_rn(amax, 0.125f);  // = amax / 8 correctly rounded (a power of two)
   __half s16 = __float2half_rn(s32);
   if (__hisinf(s16)) s16 = __ushort_as_half(0x7BFFu);  // saturate to 65504
   const float s = __half2float(s16);
-  int code = 8;
-  if (s != 0.0f) {
-    float q = rintf(__fdiv_rn(y, s));
-    q = fminf(fmaxf(q, -8.0f), 7.0f);
-    code = static_cast<int>(q) + 8;
-  }
-  uint32_t bits = static_cast<uint32_t>(code) << (4 * (lane & 3));
+  uint32_t code = 8;
+  if (s != 0.0f && !q4_code_screened(y, rcp_approx(s), code)) code = q4_code_exact(y, s);
+  uint32_t bits = code << (4 * (lane & 3));
   bits |= __shfl_xor_sync(0xffffffffu, bits, 1);
   bits |= __shfl_xor_sync(0xffffffffu, bits, 2);
   uint8_t* codes = static_cast<uint8_t*>(kv ? c.v : c.k) + r * (D / 2);
@@ -297,11 +392,22 @@ cudaError_t launch_store(const kvq_cache& c, const void* k, const void* v, int d
     }
 #undef KVQ_STORE_GROUP
   } else if (q4) {
-    const int64_t rows = n_tok * c.num_kv_heads * 2;
-    const dim3 blocks((rows + 7) / 8);
-#define KVQ_STORE_ROW(NG)                                                                                   \
-  e = rot ? launch_pdl(store_q4_kernel<NG, true>, blocks, dim3(256), 0, s, c, k, v, dtype, n_tok, slots, status) \
-          : launch_pdl(store_q4_kernel<NG, false>, blocks, dim3(256), 0, s, c, k, v, dtype, n_tok, slots, status)
+    // kWideSets x 8 groups per warp, 8 warps per block
+    const int64_t groups = n_tok * c.num_kv_heads * 2 * (c.head_dim / 32);
+    const int64_t per_block = 8 * 8 * kWideSets;
+    const dim3 blocks((groups + per_block - 1) / per_block);
+    const bool vec = (reinterpret_cast<uintptr_t>(k) & 15u) == 0 && (reinterpret_cast<uintptr_t>(v) & 15u) == 0;
+#define KVQ_STORE_WIDE(NG, ROT)                                                                                    \
+  e = vec ? launch_pdl(store_q4_wide_kernel<NG, ROT, true>, blocks, dim3(256), 0, s, c, k, v, dtype, n_tok, slots,  \
+                       status)                                                                                     \
+          : launch_pdl(store_q4_wide_kernel<NG, ROT, false>, blocks, dim3(256), 0, s, c, k, v, dtype, n_tok, slots, \
+                       status)
+#define KVQ_STORE_ROW(NG)         \
+  if (rot) {                      \
+    KVQ_STORE_WIDE(NG, true);     \
+  } else {                        \
+    KVQ_STORE_WIDE(NG, false);    \
+  }
     switch (c.head_dim / 32) {
       case 1: KVQ_STORE_ROW(1); break;
       case 2: KVQ_STORE_ROW(2); break;
@@ -310,6 +416,7 @@ cudaError_t launch_store(const kvq_cache& c, const void* k, const void* v, int d
       default: return cudaErrorInvalidValue;
     }
 #undef KVQ_STORE_ROW
+#undef KVQ_STORE_WIDE
   } else if (c.format == KVQ_FMT_BF16) {
     const int64_t total = n_tok * c.num_kv_heads * c.head_dim;
     int64_t blocks = (total + 255) / 256;

@@ -116,6 +116,24 @@ def test_store_code_ties_round_half_to_even(K, fmt, reps):
     assert np.array_equal(codes[tie], exp[tie])
 
 
+@pytest.mark.parametrize("reps", [200, 1])  # 200 rows x (K, V) > 256: the bulk kernel; 1: the (row, group) kernel
+def test_store_codes_near_ties_bit_exact(K, reps):
+    """Quotients y / s within 1 .. 3 ulps of every half-integer, for the scale 1
+    and 0.8125 (unrotated rows, so y is the input): the code depends on the
+    last bit of the IEEE-rounded quotient; both store kernels must match the
+    oracle bit for bit."""
+    from tests import tie_rows
+    x = np.tile(tie_rows.near_tie_rows(), (reps, 1))
+    n, D = x.shape
+    ps = 16
+    n_pages = (n + ps - 1) // ps
+    g, o = make_cache_pair(K, K.FMT_Q4_0, 1, D, ps, n_pages)
+    fill_sequence(K, g, o, torch.from_numpy(x.reshape(n, 1, D)), torch.from_numpy(-x.reshape(n, 1, D)),
+                  np.arange(n_pages, dtype=np.int32), n)
+    torch.cuda.synchronize()
+    check_planes_equal(g, o)
+
+
 @pytest.mark.parametrize("D", [64, 128, 256])
 @pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
 @pytest.mark.parametrize("T", [250, 20])  # large stores take the row kernel, small ones the (row, group) kernel
@@ -128,6 +146,33 @@ def test_store_q4_bit_exact(K, D, dtype, T):
     fill_sequence(K, g, o, k, v, bt, T)
     torch.cuda.synchronize()
     check_planes_equal(g, o)
+
+
+@pytest.mark.parametrize("fmt", ["Q4_HAD32", "Q4_0"])
+@pytest.mark.parametrize("D", [64, 128, 256])
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+def test_store_q4_bulk_ragged_and_unaligned(K, fmt, D, dtype):
+    """The bulk store (8 groups per warp): a row count that leaves the last warp
+    and block part-empty, inputs that start off a 16-byte boundary (element
+    loads instead of vector loads), negative slots (skipped) among valid ones;
+    bit-exact with the oracle."""
+    Hk, ps, T = 3, 16, 173
+    n_pages = (T + ps - 1) // ps + 1
+    gfmt = K.FMT_Q4_HAD32 if fmt == "Q4_HAD32" else K.FMT_Q4_0
+    base_k = synth.outlier_normal((T + 1, Hk, D), 4, 20.0, "cpu", D, "uk").to(dtype).reshape(-1)
+    base_v = synth.heavy_tailed((T + 1, Hk, D), "cpu", D, "uv").to(dtype).reshape(-1)
+    for off in (0, 1):
+        k = base_k[off:off + T * Hk * D].view(T, Hk, D)
+        v = base_v[off:off + T * Hk * D].view(T, Hk, D)
+        g, o = make_cache_pair(K, gfmt, Hk, D, ps, n_pages)
+        slots = np.arange(T, dtype=np.int32)
+        slots[::7] = -1                               # skipped tokens
+        kd, vd = base_k.to(DEV)[off:off + T * Hk * D].view(T, Hk, D), base_v.to(DEV)[off:off + T * Hk * D].view(T, Hk, D)
+        assert (kd.data_ptr() % 16 == 0) == (off == 0)
+        K.store(g, kd, vd, torch.from_numpy(slots).to(DEV))
+        O.store(o, to_np_in(k), to_np_in(v), slots)
+        torch.cuda.synchronize()
+        check_planes_equal(g, o)
 
 
 @pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])

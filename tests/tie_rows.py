@@ -152,3 +152,34 @@ def rotated_rows(D=256, exponents=(-3, 0, 2, 4)):
         ys.append(y)
         ss.append(s)
     return np.stack(xs), np.stack(es), np.stack(ys), np.stack(ss)
+
+
+def near_tie_rows(D=256):
+    """Unrotated rows whose quotients y / s sit within a few ulps of every
+    half-integer k + 1/2 (k = -9 .. 8), for the scale 1 (group maximum 8) and
+    the scale 0.8125 (group maximum 6.5, an exact fp16 value): y = the fp32
+    value nearest (k + 1/2) s, then 1 .. 3 ulps either side.  Their codes
+    depend on the last bit of the rounded quotient.  Returns x [n, D] fp32."""
+    ng = D // 32
+    vals = {1.0: [], 0.8125: []}
+    for s in vals:
+        for k in range(-9, 9):
+            base = np.float32((k + 0.5) * s)
+            up = dn = base
+            cand = [base]
+            for _ in range(3):
+                up = np.nextafter(up, np.float32(np.inf))
+                dn = np.nextafter(dn, np.float32(-np.inf))
+                cand += [up, dn]
+            vals[s] += [c for c in cand if abs(float(c)) <= 8.0 * s]
+    groups = []
+    for s, vs in vals.items():
+        for i in range(0, len(vs), 31):
+            g = np.zeros(32, np.float32)
+            g[0] = np.float32(-8.0 * s)                      # the group maximum: s = fp16(8 s / 8) = s
+            chunk = vs[i:i + 31]
+            g[1:1 + len(chunk)] = chunk
+            groups.append(g)
+    while len(groups) % ng:
+        groups.append(groups[len(groups) % ng])
+    return np.stack(groups).reshape(-1, D)
