@@ -95,10 +95,15 @@ struct WsLayout {
 // Keys per split-T partition: 512 ("shared 512-key chunks") for every format
 // and problem size, so that a sequence's partials do not depend on what else
 // is in the batch (a batched sequence equals its solo decode bit for bit).
+// A gather over selected fp8 latent rows takes runs of kFp8GatherPart entries
+// instead: a selection of a few thousand rows would otherwise give a handful of
+// CTAs per head block.
+constexpr int kFp8GatherPart = 128;
+
 static WsLayout ws_layout(const kvq_cache* c, int B, int Hq, int max_seq_len, int n_sel) {
   WsLayout w;
   const int64_t T = n_sel > 0 ? n_sel : max_seq_len;
-  w.part = kPart;
+  w.part = (n_sel > 0 && c->format == KVQ_FMT_FP8_ROW) ? kFp8GatherPart : kPart;
   w.P = static_cast<int>((T + w.part - 1) / w.part);
   if (w.P < 1) w.P = 1;
   const size_t n = static_cast<size_t>(B) * Hq * w.P;

@@ -146,6 +146,26 @@ __device__ __forceinline__ float load_act(const void* p, int dtype, int64_t i) {
   return __bfloat162float(static_cast<const __nv_bfloat16*>(p)[i]);
 }
 
+// ---------------------------------------------------------------- division by a launch constant
+// n / d for 0 <= n < 2^31 and a divisor d >= 1 known at launch, as one
+// multiply-high, an add and a shift (Granlund and Montgomery, "Division by
+// invariant integers using multiplication", PLDI 1994: with l = ceil(log2 d)
+// and m = floor(2^32 (2^l - d) / d) + 1, n / d = (mulhi(n, m) + n) >> l).
+struct FastDiv {
+  uint32_t d, m, l;
+};
+
+inline FastDiv make_fastdiv(uint32_t d) {
+  uint32_t l = 0;
+  while ((uint64_t(1) << l) < d) ++l;
+  const uint64_t m = ((uint64_t(1) << 32) * ((uint64_t(1) << l) - d)) / d + 1;
+  return FastDiv{d, static_cast<uint32_t>(m), l};
+}
+
+__device__ __forceinline__ uint32_t fast_div(uint32_t n, const FastDiv& f) {
+  return (__umulhi(n, f.m) + n) >> f.l;
+}
+
 // ---------------------------------------------------------------- register ops
 
 __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {

@@ -53,169 +53,144 @@ __device__ __forceinline__ uint32_t q4_code_exact(float y, float s) {
   return static_cast<uint32_t>(static_cast<int>(q) + 8);
 }
 
-// Bulk form (a prompt chunk): a warp takes kWideSets sets of 8 groups of 32
-// values (a set is one 256-wide row, or 8 / NG narrower rows), lane L holding
-// the 8 consecutive elements 8t .. 8t + 7 (t = L & 3) of group L >> 2 of each
-// set.  The butterfly's stages h = 1, 2, 4 then run inside a lane and h = 8, 16
-// across the group's four lanes: the same additions and subtractions of the
-// same operands as the one-element-per-lane form, with a quarter of the
-// shuffles and selects, and the lane's 8 codes are one 32-bit word of the row
-// (bytes 16G + 4t .. 16G + 4t + 3).  Every load of the warp (its sets' values
-// and slots) is issued before any is used, so the loads of both sets and the
-// slot lookups overlap instead of queueing behind each other.  VEC: the inputs
-// are 16-byte aligned, so a lane loads its 8 values with one (bf16) or two
-// (f32) 16-byte loads.  ROT = false: the unrotated Q4_0 format.
-constexpr int kWideSets = 2;
-
+// Bulk form (a prompt chunk): one lane per (row, group of 32 values), so the
+// whole 32-point butterfly (stages h = 1, 2, 4, 8, 16, (a, b) -> (a + b, a - b),
+// the same operations on the same operands as the warp-shuffle form) and the
+// group maximum run in registers, with no shuffles; a warp covers 32
+// consecutive groups (4 rows of 256).  The lane's 16 code bytes and its fp16
+// scale are one 16-byte and one 2-byte store.  VEC: the inputs are 16-byte
+// aligned, so the lane loads its 32 values with 4 (bf16) or 8 (f32) 16-byte
+// loads.  ROT = false: the unrotated Q4_0 format.  The launch keeps
+// n_tok * num_kv_heads * 2 * NG below 2^31 (a larger store is split into
+// several launches), so the group indices are 32-bit; hk and ps divide by
+// num_kv_heads and page_size.
 template <int NG, bool ROT, bool VEC>
-__global__ void __launch_bounds__(256) store_q4_wide_kernel(kvq_cache c, const void* __restrict__ k,
+__global__ void __launch_bounds__(256) store_q4_lane_kernel(kvq_cache c, const void* __restrict__ k,
                                                             const void* __restrict__ v, int dtype, int64_t n_tok,
-                                                            const int32_t* __restrict__ slots, int32_t* status) {
+                                                            const int32_t* __restrict__ slots, int32_t* status,
+                                                            FastDiv hk, FastDiv ps) {
   pdl_wait();
   pdl_trigger();
   constexpr int D = NG * 32;
-  const int lane = threadIdx.x & 31, t = lane & 3;
   const int Hk = c.num_kv_heads;
-  const int64_t total = n_tok * Hk * 2 * NG;
-  const int64_t warp_id = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-  // every lane of the warp stays to the end (the shuffles below are warp-wide);
-  // only lanes whose group exists and whose slot is valid store
-  int64_t gg[kWideSets];
-  bool in_range[kWideSets];
-  int32_t slot[kWideSets];
-  float x[kWideSets][8];
+  const uint32_t gg = blockIdx.x * blockDim.x + threadIdx.x;  // (row, group) of this lane
+  if (gg >= static_cast<uint32_t>(n_tok * Hk * 2 * NG)) return;
+  const uint32_t row = gg / NG, rowh = row >> 1;
+  const int G = static_cast<int>(gg % NG);
+  const uint32_t tok = fast_div(rowh, hk);
+  const uint32_t head = rowh - tok * Hk;
+  const bool is_v = (row & 1) != 0;
+  const int32_t slot = slots[tok];
+  const void* src = is_v ? v : k;
+  const int64_t e0 = ((int64_t)tok * Hk + head) * D + 32 * G;
+  float x[32];
+  if (VEC && dtype == KVQ_DT_BF16) {
 #pragma unroll
-  for (int j = 0; j < kWideSets; ++j) {
-    gg[j] = (warp_id * kWideSets + j) * 8 + (lane >> 2);
-    in_range[j] = gg[j] < total;
-    const int64_t row = gg[j] / NG;
-    const int64_t tok = (row >> 1) / Hk;
-    const int head = static_cast<int>((row >> 1) % Hk);
-    const int G = static_cast<int>(gg[j] % NG);
-    const void* src = (row & 1) ? v : k;
-    const int64_t e0 = (tok * Hk + head) * D + 32 * G + 8 * t;  // first element of the lane
-    slot[j] = in_range[j] ? slots[tok] : -1;
-    if (!in_range[j]) {
-#pragma unroll
-      for (int i = 0; i < 8; ++i) x[j][i] = 0.f;
-    } else if (VEC && dtype == KVQ_DT_BF16) {
-      const uint4 u = *reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(src) + e0);
+    for (int q = 0; q < 4; ++q) {
+      const uint4 u = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(src) + e0)[q];
       const uint32_t w[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
-        x[j][2 * i] = __uint_as_float(w[i] << 16);
-        x[j][2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+        x[8 * q + 2 * i] = __uint_as_float(w[i] << 16);
+        x[8 * q + 2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
       }
-    } else if (VEC) {
-      const float4 a4 = *reinterpret_cast<const float4*>(static_cast<const float*>(src) + e0);
-      const float4 b4 = *reinterpret_cast<const float4*>(static_cast<const float*>(src) + e0 + 4);
-      x[j][0] = a4.x; x[j][1] = a4.y; x[j][2] = a4.z; x[j][3] = a4.w;
-      x[j][4] = b4.x; x[j][5] = b4.y; x[j][6] = b4.z; x[j][7] = b4.w;
-    } else {
-#pragma unroll
-      for (int i = 0; i < 8; ++i) x[j][i] = load_act(src, dtype, e0 + i);
     }
+  } else if (VEC) {
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      const float4 f = reinterpret_cast<const float4*>(static_cast<const float*>(src) + e0)[q];
+      x[4 * q] = f.x; x[4 * q + 1] = f.y; x[4 * q + 2] = f.z; x[4 * q + 3] = f.w;
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < 32; ++i) x[i] = load_act(src, dtype, e0 + i);
   }
+  if (slot < 0) return;
+  if ((int64_t)slot >= (int64_t)c.num_pages * c.page_size) {
+    if (G == 0) set_status(status, KVQ_DEV_BAD_SLOT);
+    return;
+  }
+  if (ROT) {
 #pragma unroll
-  for (int j = 0; j < kWideSets; ++j) {
-    float* xs = x[j];
-    if (ROT) {
-      // stages h = 1, 2, 4: pairs (i, i + h) inside the lane, (a, b) -> (a + b, a - b)
+    for (int h = 1; h < 32; h <<= 1)
 #pragma unroll
-      for (int h = 1; h < 8; h <<= 1)
-#pragma unroll
-        for (int i = 0; i < 8; ++i)
-          if ((i & h) == 0) {
-            const float a = xs[i], b = xs[i + h];
-            xs[i] = __fadd_rn(a, b);
-            xs[i + h] = __fsub_rn(a, b);
-          }
-      // stages h = 8, 16: element 8t + i pairs with the same i of lane t ^ 1, t ^ 2;
-      // the lower lane keeps a + b, the upper one a - b (a the lower's value)
-#pragma unroll
-      for (int hl = 1; hl < 4; hl <<= 1) {
-        const bool upper = (t & hl) != 0;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const float o = __shfl_xor_sync(0xffffffffu, xs[i], hl);
-          xs[i] = upper ? __fsub_rn(o, xs[i]) : __fadd_rn(xs[i], o);
+      for (int i = 0; i < 32; ++i)
+        if ((i & h) == 0) {
+          const float a = x[i], b = x[i + h];
+          x[i] = __fadd_rn(a, b);
+          x[i + h] = __fsub_rn(a, b);
         }
-      }
 #pragma unroll
-      for (int i = 0; i < 8; ++i) xs[i] = __fmul_rn(xs[i], kHadamardScale);
-    }
-    float amax = fabsf(xs[0]);
+    for (int i = 0; i < 32; ++i) x[i] = __fmul_rn(x[i], kHadamardScale);
+  }
+  float amax = fabsf(x[0]);
 #pragma unroll
-    for (int i = 1; i < 8; ++i) amax = fmaxf(amax, fabsf(xs[i]));
-    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
-    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
-    const float s32 = __fmul_rn(amax, 0.125f);  // = amax / 8 correctly rounded (a power of two)
-    __half s16 = __float2half_rn(s32);
-    if (__hisinf(s16)) s16 = __ushort_as_half(0x7BFFu);  // saturate to 65504
-    const float s = __half2float(s16);
-    uint32_t word = 0x88888888u;  // scale 0: every code 8
+  for (int i = 1; i < 32; ++i) amax = fmaxf(amax, fabsf(x[i]));
+  const float s32 = __fmul_rn(amax, 0.125f);  // = amax / 8 correctly rounded (a power of two)
+  __half s16 = __float2half_rn(s32);
+  if (__hisinf(s16)) s16 = __ushort_as_half(0x7BFFu);  // saturate to 65504
+  const float s = __half2float(s16);
+  uint32_t word[4] = {0x88888888u, 0x88888888u, 0x88888888u, 0x88888888u};  // scale 0: every code 8
+  if (s != 0.0f) {
+    const float r = rcp_approx(s);
     bool undecided = false;
-    if (s != 0.0f) {
-      const float r = rcp_approx(s);
-      word = 0;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      word[q] = 0;
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
         uint32_t code;
-        undecided |= !q4_code_screened(xs[i], r, code);
-        word |= code << (4 * i);
+        undecided |= !q4_code_screened(x[8 * q + i], r, code);
+        word[q] |= code << (4 * i);
       }
     }
-    if (__any_sync(0xffffffffu, undecided) && undecided) {  // rare: ties and near-ties
-      word = 0;
+    if (undecided) {  // rare: ties and near-ties
 #pragma unroll
-      for (int i = 0; i < 8; ++i) word |= q4_code_exact(xs[i], s) << (4 * i);
-    }
-    if (in_range[j]) {
-      const int64_t row = gg[j] / NG;
-      const int G = static_cast<int>(gg[j] % NG);
-      const int sl = slot[j];
-      if (sl >= 0 && (int64_t)sl >= (int64_t)c.num_pages * c.page_size) {
-        if (t == 0 && G == 0) set_status(status, KVQ_DEV_BAD_SLOT);
-      } else if (sl >= 0) {
-        const int64_t r = ((int64_t)(sl / c.page_size) * Hk + static_cast<int>((row >> 1) % Hk)) * c.page_size +
-                          sl % c.page_size;
-        const bool is_v = (row & 1) != 0;
-        uint8_t* codes = static_cast<uint8_t*>(is_v ? c.v : c.k) + r * (D / 2);
-        reinterpret_cast<uint32_t*>(codes)[4 * G + t] = word;
-        if (t == 0) (static_cast<uint16_t*>(is_v ? c.v_scale : c.k_scale) + r * NG)[G] = __half_as_ushort(s16);
+      for (int q = 0; q < 4; ++q) {
+        word[q] = 0;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) word[q] |= q4_code_exact(x[8 * q + i], s) << (4 * i);
       }
     }
   }
+  const uint32_t page = fast_div(static_cast<uint32_t>(slot), ps);
+  const int64_t r = ((int64_t)page * Hk + head) * c.page_size + (static_cast<uint32_t>(slot) - page * ps.d);
+  reinterpret_cast<uint4*>(static_cast<uint8_t*>(is_v ? c.v : c.k) + r * (D / 2))[G] =
+      make_uint4(word[0], word[1], word[2], word[3]);
+  (static_cast<uint16_t*>(is_v ? c.v_scale : c.k_scale) + r * NG)[G] = __half_as_ushort(s16);
 }
 
 // Latency form of the same store for a handful of rows (a decode step stores one
 // token): one warp per (row, group), so the groups of a row are packed in
 // parallel instead of one after another.  Same arithmetic, same bytes.
 // Warp `wid` of the store: (row, group) = (wid / NG, wid % NG).
+// (n_tok * num_kv_heads * 2 * NG is at most a few thousand here; hk and ps
+// divide by num_kv_heads and page_size.)
 template <int NG, bool ROT>
 __device__ __forceinline__ void store_q4_group_warp(const kvq_cache& c, const void* __restrict__ k,
                                                     const void* __restrict__ v, int dtype, int64_t n_tok,
-                                                    const int32_t* __restrict__ slots, int32_t* status, int64_t wid) {
+                                                    const int32_t* __restrict__ slots, int32_t* status, int64_t wid,
+                                                    const FastDiv& hk, const FastDiv& ps) {
   constexpr int D = NG * 32;
   const int lane = threadIdx.x & 31;
   const int Hk = c.num_kv_heads;
   if (wid >= n_tok * Hk * 2 * NG) return;
   const int G = static_cast<int>(wid % NG);
-  const int64_t row = wid / NG;
+  const uint32_t row = static_cast<uint32_t>(wid / NG), rowh = row >> 1;
   const int kv = static_cast<int>(row & 1);
-  const int64_t tok = (row >> 1) / Hk;
-  const int head = static_cast<int>((row >> 1) % Hk);
+  const uint32_t tok = fast_div(rowh, hk);
+  const int head = static_cast<int>(rowh - tok * Hk);
   const int32_t slot = slots[tok];
   if (slot < 0) return;
   if ((int64_t)slot >= (int64_t)c.num_pages * c.page_size) {
     if (lane == 0 && G == 0) set_status(status, KVQ_DEV_BAD_SLOT);
     return;
   }
-  const int64_t page = slot / c.page_size;
-  const int off = slot % c.page_size;
-  const int64_t r = (page * Hk + head) * c.page_size + off;
+  const uint32_t page = fast_div(static_cast<uint32_t>(slot), ps);
+  const int off = static_cast<int>(static_cast<uint32_t>(slot) - page * ps.d);
+  const int64_t r = ((int64_t)page * Hk + head) * c.page_size + off;
   const void* src = kv ? v : k;
-  float x = load_act(src, dtype, (tok * Hk + head) * D + 32 * G + lane);
+  float x = load_act(src, dtype, ((int64_t)tok * Hk + head) * D + 32 * G + lane);
   const float y = ROT ? __fmul_rn(warp_fwht32(x, lane), kHadamardScale) : x;
   float amax = fabsf(y);
 #pragma unroll
@@ -240,11 +215,12 @@ __device__ __forceinline__ void store_q4_group_warp(const kvq_cache& c, const vo
 template <int NG, bool ROT>
 __global__ void __launch_bounds__(256) store_q4_group_kernel(kvq_cache c, const void* __restrict__ k,
                                                              const void* __restrict__ v, int dtype, int64_t n_tok,
-                                                             const int32_t* __restrict__ slots, int32_t* status) {
+                                                             const int32_t* __restrict__ slots, int32_t* status,
+                                                             FastDiv hk, FastDiv ps) {
   pdl_wait();
   pdl_trigger();
   store_q4_group_warp<NG, ROT>(c, k, v, dtype, n_tok, slots, status,
-                               (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5));
+                               (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5), hk, ps);
 }
 
 // BF16 comparison format: plain copy / RNE conversion of each value.
@@ -356,12 +332,13 @@ __global__ void __launch_bounds__(256) store_rotate_kernel(kvq_cache c, const vo
                                                            const void* __restrict__ v, int dtype, int64_t n_tok,
                                                            const int32_t* __restrict__ slots, int32_t* status,
                                                            int store_blocks, const void* __restrict__ q,
-                                                           int q_dtype, float* q_out, int64_t q_groups) {
+                                                           int q_dtype, float* q_out, int64_t q_groups, FastDiv hk,
+                                                           FastDiv ps) {
   pdl_wait();
   pdl_trigger();
   const int warps = blockDim.x >> 5, w = threadIdx.x >> 5;
   if ((int)blockIdx.x < store_blocks)
-    store_q4_group_warp<NG, true>(c, k, v, dtype, n_tok, slots, status, (int64_t)blockIdx.x * warps + w);
+    store_q4_group_warp<NG, true>(c, k, v, dtype, n_tok, slots, status, (int64_t)blockIdx.x * warps + w, hk, ps);
   else
     rotate_warp(q, q_dtype, q_out, q_groups, (int64_t)(blockIdx.x - store_blocks) * warps + w);
 }
@@ -377,12 +354,16 @@ cudaError_t launch_store(const kvq_cache& c, const void* k, const void* v, int d
   cudaError_t e = cudaSuccess;
   const bool q4 = c.format == KVQ_FMT_Q4_HAD32 || c.format == KVQ_FMT_Q4_0;
   const bool rot = c.format == KVQ_FMT_Q4_HAD32;
+  const FastDiv hk = make_fastdiv(static_cast<uint32_t>(c.num_kv_heads));
+  const FastDiv ps = make_fastdiv(static_cast<uint32_t>(c.page_size));
   if (q4 && n_tok * c.num_kv_heads * 2 <= kStoreGroupRows) {
     const int64_t warps = n_tok * c.num_kv_heads * 2 * (c.head_dim / 32);
     const dim3 blocks((warps + 7) / 8);
-#define KVQ_STORE_GROUP(NG)                                                                                      \
-  e = rot ? launch_pdl(store_q4_group_kernel<NG, true>, blocks, dim3(256), 0, s, c, k, v, dtype, n_tok, slots, status) \
-          : launch_pdl(store_q4_group_kernel<NG, false>, blocks, dim3(256), 0, s, c, k, v, dtype, n_tok, slots, status)
+#define KVQ_STORE_GROUP(NG)                                                                                        \
+  e = rot ? launch_pdl(store_q4_group_kernel<NG, true>, blocks, dim3(256), 0, s, c, k, v, dtype, n_tok, slots, status, \
+                       hk, ps)                                                                                       \
+          : launch_pdl(store_q4_group_kernel<NG, false>, blocks, dim3(256), 0, s, c, k, v, dtype, n_tok, slots,      \
+                       status, hk, ps)
     switch (c.head_dim / 32) {
       case 1: KVQ_STORE_GROUP(1); break;
       case 2: KVQ_STORE_GROUP(2); break;
@@ -392,31 +373,41 @@ cudaError_t launch_store(const kvq_cache& c, const void* k, const void* v, int d
     }
 #undef KVQ_STORE_GROUP
   } else if (q4) {
-    // kWideSets x 8 groups per warp, 8 warps per block
-    const int64_t groups = n_tok * c.num_kv_heads * 2 * (c.head_dim / 32);
-    const int64_t per_block = 8 * 8 * kWideSets;
-    const dim3 blocks((groups + per_block - 1) / per_block);
-    const bool vec = (reinterpret_cast<uintptr_t>(k) & 15u) == 0 && (reinterpret_cast<uintptr_t>(v) & 15u) == 0;
-#define KVQ_STORE_WIDE(NG, ROT)                                                                                    \
-  e = vec ? launch_pdl(store_q4_wide_kernel<NG, ROT, true>, blocks, dim3(256), 0, s, c, k, v, dtype, n_tok, slots,  \
-                       status)                                                                                     \
-          : launch_pdl(store_q4_wide_kernel<NG, ROT, false>, blocks, dim3(256), 0, s, c, k, v, dtype, n_tok, slots, \
-                       status)
+    // one lane per (row, group); launches of at most 2^30 groups, so that the
+    // kernel's group indices stay 32-bit
+    const int64_t per_tok = static_cast<int64_t>(c.num_kv_heads) * 2 * (c.head_dim / 32);
+    const int64_t max_tok = (int64_t(1) << 30) / per_tok;
+    const size_t esz = dtype == KVQ_DT_F32 ? 4 : 2;
+    const size_t tok_bytes = static_cast<size_t>(c.num_kv_heads) * c.head_dim * esz;
+    const bool vec = (reinterpret_cast<uintptr_t>(k) & 15u) == 0 && (reinterpret_cast<uintptr_t>(v) & 15u) == 0 &&
+                     tok_bytes % 16 == 0;
+    for (int64_t t0 = 0; t0 < n_tok && e == cudaSuccess; t0 += max_tok) {
+      const int64_t nt = n_tok - t0 < max_tok ? n_tok - t0 : max_tok;
+      const void* kc = static_cast<const uint8_t*>(k) + t0 * tok_bytes;
+      const void* vc = static_cast<const uint8_t*>(v) + t0 * tok_bytes;
+      const int32_t* sc = slots + t0;
+      const dim3 blocks(static_cast<unsigned>((nt * per_tok + 255) / 256));  // one lane per (row, group)
+#define KVQ_STORE_WIDE(NG, ROT)                                                                                     \
+  e = vec ? launch_pdl(store_q4_lane_kernel<NG, ROT, true>, blocks, dim3(256), 0, s, c, kc, vc, dtype, nt, sc,      \
+                       status, hk, ps)                                                                              \
+          : launch_pdl(store_q4_lane_kernel<NG, ROT, false>, blocks, dim3(256), 0, s, c, kc, vc, dtype, nt, sc,     \
+                       status, hk, ps)
 #define KVQ_STORE_ROW(NG)         \
   if (rot) {                      \
     KVQ_STORE_WIDE(NG, true);     \
   } else {                        \
     KVQ_STORE_WIDE(NG, false);    \
   }
-    switch (c.head_dim / 32) {
-      case 1: KVQ_STORE_ROW(1); break;
-      case 2: KVQ_STORE_ROW(2); break;
-      case 4: KVQ_STORE_ROW(4); break;
-      case 8: KVQ_STORE_ROW(8); break;
-      default: return cudaErrorInvalidValue;
-    }
+      switch (c.head_dim / 32) {
+        case 1: KVQ_STORE_ROW(1); break;
+        case 2: KVQ_STORE_ROW(2); break;
+        case 4: KVQ_STORE_ROW(4); break;
+        case 8: KVQ_STORE_ROW(8); break;
+        default: return cudaErrorInvalidValue;
+      }
 #undef KVQ_STORE_ROW
 #undef KVQ_STORE_WIDE
+    }
   } else if (c.format == KVQ_FMT_BF16) {
     const int64_t total = n_tok * c.num_kv_heads * c.head_dim;
     int64_t blocks = (total + 255) / 256;
@@ -443,12 +434,14 @@ cudaError_t launch_store_rotate(const kvq_cache& c, const void* k, const void* v
   const int64_t q_groups = q_rows * (q_head_dim / 32);
   const dim3 blocks(store_blocks + static_cast<unsigned>((q_groups + 7) / 8));
   if (blocks.x == 0) return cudaSuccess;
+  const FastDiv hk = make_fastdiv(static_cast<uint32_t>(c.num_kv_heads));
+  const FastDiv ps = make_fastdiv(static_cast<uint32_t>(c.page_size));
   cudaError_t e;
   switch (c.head_dim / 32) {
-    case 1: e = launch_pdl(store_rotate_kernel<1>, blocks, dim3(256), 0, s, c, k, v, dtype, n_tok, slots, status, store_blocks, q, q_dtype, q_out, q_groups); break;
-    case 2: e = launch_pdl(store_rotate_kernel<2>, blocks, dim3(256), 0, s, c, k, v, dtype, n_tok, slots, status, store_blocks, q, q_dtype, q_out, q_groups); break;
-    case 4: e = launch_pdl(store_rotate_kernel<4>, blocks, dim3(256), 0, s, c, k, v, dtype, n_tok, slots, status, store_blocks, q, q_dtype, q_out, q_groups); break;
-    case 8: e = launch_pdl(store_rotate_kernel<8>, blocks, dim3(256), 0, s, c, k, v, dtype, n_tok, slots, status, store_blocks, q, q_dtype, q_out, q_groups); break;
+    case 1: e = launch_pdl(store_rotate_kernel<1>, blocks, dim3(256), 0, s, c, k, v, dtype, n_tok, slots, status, store_blocks, q, q_dtype, q_out, q_groups, hk, ps); break;
+    case 2: e = launch_pdl(store_rotate_kernel<2>, blocks, dim3(256), 0, s, c, k, v, dtype, n_tok, slots, status, store_blocks, q, q_dtype, q_out, q_groups, hk, ps); break;
+    case 4: e = launch_pdl(store_rotate_kernel<4>, blocks, dim3(256), 0, s, c, k, v, dtype, n_tok, slots, status, store_blocks, q, q_dtype, q_out, q_groups, hk, ps); break;
+    case 8: e = launch_pdl(store_rotate_kernel<8>, blocks, dim3(256), 0, s, c, k, v, dtype, n_tok, slots, status, store_blocks, q, q_dtype, q_out, q_groups, hk, ps); break;
     default: return cudaErrorInvalidValue;
   }
   if (e != cudaSuccess) return e;
