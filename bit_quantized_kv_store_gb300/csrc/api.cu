@@ -98,7 +98,7 @@ struct WsLayout {
 // A gather over selected fp8 latent rows takes runs of kFp8GatherPart entries
 // instead: a selection of a few thousand rows would otherwise give a handful of
 // CTAs per head block.
-constexpr int kFp8GatherPart = 128;
+constexpr int kFp8GatherPart = 64;
 
 static WsLayout ws_layout(const kvq_cache* c, int B, int Hq, int max_seq_len, int n_sel) {
   WsLayout w;

@@ -56,15 +56,41 @@ __device__ __forceinline__ uint32_t q4_code_exact(float y, float s) {
 // Bulk form (a prompt chunk): one lane per (row, group of 32 values), so the
 // whole 32-point butterfly (stages h = 1, 2, 4, 8, 16, (a, b) -> (a + b, a - b),
 // the same operations on the same operands as the warp-shuffle form) and the
-// group maximum run in registers, with no shuffles; a warp covers 32
-// consecutive groups (4 rows of 256).  The lane's 16 code bytes and its fp16
-// scale are one 16-byte and one 2-byte store.  VEC: the inputs are 16-byte
-// aligned, so the lane loads its 32 values with 4 (bf16) or 8 (f32) 16-byte
-// loads.  ROT = false: the unrotated Q4_0 format.  The launch keeps
-// n_tok * num_kv_heads * 2 * NG below 2^31 (a larger store is split into
-// several launches), so the group indices are 32-bit; hk and ps divide by
-// num_kv_heads and page_size.
-template <int NG, bool ROT, bool VEC>
+// group maximum run in registers, with no shuffles; consecutive lanes take
+// consecutive groups.  The grid is sized to the GPU and every thread walks the
+// groups with a grid stride, loading the next group's values before it
+// quantises the current one, so the memory latency is paid once per thread and
+// not once per group.  The lane's 16 code bytes and its fp16 scale are one
+// 16-byte and one 2-byte store.  VEC: the inputs are 16-byte aligned (the
+// lane loads its 32 values with 16-byte loads).  ROT = false: the unrotated
+// Q4_0 format.  The launch keeps n_tok * num_kv_heads * 2 * NG below 2^31 (a
+// larger store is split into several launches), so the group indices are
+// 32-bit; hk and ps divide by num_kv_heads and page_size.
+// The raw values of one group into w: 16 words of bf16 pairs (BF) or 32 f32.
+template <bool VEC, bool BF>
+__device__ __forceinline__ void load_group(const void* __restrict__ src, int dtype, int64_t e0,
+                                           uint32_t (&w)[BF ? 16 : 32]) {
+  if constexpr (BF) {
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const uint4 u = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(src) + e0)[q];
+      w[4 * q] = u.x; w[4 * q + 1] = u.y; w[4 * q + 2] = u.z; w[4 * q + 3] = u.w;
+    }
+  } else if constexpr (VEC) {
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      const uint4 u = reinterpret_cast<const uint4*>(static_cast<const float*>(src) + e0)[q];
+      w[4 * q] = u.x; w[4 * q + 1] = u.y; w[4 * q + 2] = u.z; w[4 * q + 3] = u.w;
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < 32; ++i) w[i] = __float_as_uint(load_act(src, dtype, e0 + i));
+  }
+}
+
+// BF: bf16 inputs with VEC (16-byte loads of bf16 pairs); otherwise 32 f32 words
+// (VEC) or element loads of either type.
+template <int NG, bool ROT, bool VEC, bool BF = false>
 __global__ void __launch_bounds__(256) store_q4_lane_kernel(kvq_cache c, const void* __restrict__ k,
                                                             const void* __restrict__ v, int dtype, int64_t n_tok,
                                                             const int32_t* __restrict__ slots, int32_t* status,
@@ -73,91 +99,107 @@ __global__ void __launch_bounds__(256) store_q4_lane_kernel(kvq_cache c, const v
   pdl_trigger();
   constexpr int D = NG * 32;
   const int Hk = c.num_kv_heads;
-  const uint32_t gg = blockIdx.x * blockDim.x + threadIdx.x;  // (row, group) of this lane
-  if (gg >= static_cast<uint32_t>(n_tok * Hk * 2 * NG)) return;
-  const uint32_t row = gg / NG, rowh = row >> 1;
-  const int G = static_cast<int>(gg % NG);
-  const uint32_t tok = fast_div(rowh, hk);
-  const uint32_t head = rowh - tok * Hk;
-  const bool is_v = (row & 1) != 0;
-  const int32_t slot = slots[tok];
-  const void* src = is_v ? v : k;
-  const int64_t e0 = ((int64_t)tok * Hk + head) * D + 32 * G;
-  float x[32];
-  if (VEC && dtype == KVQ_DT_BF16) {
+  const uint32_t total = static_cast<uint32_t>(n_tok * Hk * 2 * NG);
+  const uint32_t stride = gridDim.x * blockDim.x;
+  // where group gg's values start, and which plane it goes to
+  auto locate = [&](uint32_t gg, uint32_t& tok, uint32_t& head, bool& is_v) -> int64_t {
+    const uint32_t row = gg / NG, rowh = row >> 1;
+    tok = fast_div(rowh, hk);
+    head = rowh - tok * Hk;
+    is_v = (row & 1) != 0;
+    return ((int64_t)tok * Hk + head) * D + 32 * static_cast<int>(gg % NG);
+  };
+  uint32_t gg = blockIdx.x * blockDim.x + threadIdx.x;
+  uint32_t nxt[BF ? 16 : 32];
+  if (gg < total) {
+    uint32_t tok, head;
+    bool is_v;
+    const int64_t e0 = locate(gg, tok, head, is_v);
+    load_group<VEC, BF>(is_v ? v : k, dtype, e0, nxt);
+  }
+  for (; gg < total; gg += stride) {
+    uint32_t tok, head;
+    bool is_v;
+    locate(gg, tok, head, is_v);
+    const int G = static_cast<int>(gg % NG);
+    const int32_t slot = slots[tok];
+    float x[32];
+    if constexpr (BF) {
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const uint4 u = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(src) + e0)[q];
-      const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        x[8 * q + 2 * i] = __uint_as_float(w[i] << 16);
-        x[8 * q + 2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+      for (int i = 0; i < 16; ++i) {
+        x[2 * i] = __uint_as_float(nxt[i] << 16);
+        x[2 * i + 1] = __uint_as_float(nxt[i] & 0xFFFF0000u);
       }
+    } else {
+#pragma unroll
+      for (int i = 0; i < 32; ++i) x[i] = __uint_as_float(nxt[i]);
     }
-  } else if (VEC) {
-#pragma unroll
-    for (int q = 0; q < 8; ++q) {
-      const float4 f = reinterpret_cast<const float4*>(static_cast<const float*>(src) + e0)[q];
-      x[4 * q] = f.x; x[4 * q + 1] = f.y; x[4 * q + 2] = f.z; x[4 * q + 3] = f.w;
+    if (gg + stride < total) {  // the next group's loads go ahead of this group's arithmetic
+      uint32_t t2, h2;
+      bool v2;
+      const int64_t e2 = locate(gg + stride, t2, h2, v2);
+      load_group<VEC, BF>(v2 ? v : k, dtype, e2, nxt);
     }
-  } else {
-#pragma unroll
-    for (int i = 0; i < 32; ++i) x[i] = load_act(src, dtype, e0 + i);
-  }
-  if (slot < 0) return;
-  if ((int64_t)slot >= (int64_t)c.num_pages * c.page_size) {
-    if (G == 0) set_status(status, KVQ_DEV_BAD_SLOT);
-    return;
-  }
-  if (ROT) {
-#pragma unroll
-    for (int h = 1; h < 32; h <<= 1)
-#pragma unroll
-      for (int i = 0; i < 32; ++i)
-        if ((i & h) == 0) {
-          const float a = x[i], b = x[i + h];
-          x[i] = __fadd_rn(a, b);
-          x[i + h] = __fsub_rn(a, b);
-        }
-#pragma unroll
-    for (int i = 0; i < 32; ++i) x[i] = __fmul_rn(x[i], kHadamardScale);
-  }
-  float amax = fabsf(x[0]);
-#pragma unroll
-  for (int i = 1; i < 32; ++i) amax = fmaxf(amax, fabsf(x[i]));
-  const float s32 = __fmul_rn(amax, 0.125f);  // = amax / 8 correctly rounded (a power of two)
-  __half s16 = __float2half_rn(s32);
-  if (__hisinf(s16)) s16 = __ushort_as_half(0x7BFFu);  // saturate to 65504
-  const float s = __half2float(s16);
-  uint32_t word[4] = {0x88888888u, 0x88888888u, 0x88888888u, 0x88888888u};  // scale 0: every code 8
-  if (s != 0.0f) {
-    const float r = rcp_approx(s);
-    bool undecided = false;
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      word[q] = 0;
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        uint32_t code;
-        undecided |= !q4_code_screened(x[8 * q + i], r, code);
-        word[q] |= code << (4 * i);
-      }
+    if (slot < 0) continue;
+    if ((int64_t)slot >= (int64_t)c.num_pages * c.page_size) {
+      if (G == 0) set_status(status, KVQ_DEV_BAD_SLOT);
+      continue;
     }
-    if (undecided) {  // rare: ties and near-ties
+    if (ROT) {
+#pragma unroll
+      for (int h = 1; h < 32; h <<= 1)
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+          if ((i & h) == 0) {
+            const float a = x[i], b = x[i + h];
+            x[i] = __fadd_rn(a, b);
+            x[i + h] = __fsub_rn(a, b);
+          }
+#pragma unroll
+      for (int i = 0; i < 32; ++i) x[i] = __fmul_rn(x[i], kHadamardScale);
+    }
+    // the group maximum by a tree (max is exact, so any order gives the same value)
+    float m[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) m[i] = fmaxf(fabsf(x[i]), fabsf(x[i + 16]));
+#pragma unroll
+    for (int w = 8; w > 0; w >>= 1)
+#pragma unroll
+      for (int i = 0; i < w; ++i) m[i] = fmaxf(m[i], m[i + w]);
+    const float amax = m[0];
+    const float s32 = __fmul_rn(amax, 0.125f);  // = amax / 8 correctly rounded (a power of two)
+    __half s16 = __float2half_rn(s32);
+    if (__hisinf(s16)) s16 = __ushort_as_half(0x7BFFu);  // saturate to 65504
+    const float s = __half2float(s16);
+    uint32_t word[4] = {0x88888888u, 0x88888888u, 0x88888888u, 0x88888888u};  // scale 0: every code 8
+    if (s != 0.0f) {
+      const float r = rcp_approx(s);
+      bool undecided = false;
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
         word[q] = 0;
 #pragma unroll
-        for (int i = 0; i < 8; ++i) word[q] |= q4_code_exact(x[8 * q + i], s) << (4 * i);
+        for (int i = 0; i < 8; ++i) {
+          uint32_t code;
+          undecided |= !q4_code_screened(x[8 * q + i], r, code);
+          word[q] |= code << (4 * i);
+        }
+      }
+      if (undecided) {  // rare: ties and near-ties
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          word[q] = 0;
+#pragma unroll
+          for (int i = 0; i < 8; ++i) word[q] |= q4_code_exact(x[8 * q + i], s) << (4 * i);
+        }
       }
     }
+    const uint32_t page = fast_div(static_cast<uint32_t>(slot), ps);
+    const int64_t r = ((int64_t)page * Hk + head) * c.page_size + (static_cast<uint32_t>(slot) - page * ps.d);
+    reinterpret_cast<uint4*>(static_cast<uint8_t*>(is_v ? c.v : c.k) + r * (D / 2))[G] =
+        make_uint4(word[0], word[1], word[2], word[3]);
+    (static_cast<uint16_t*>(is_v ? c.v_scale : c.k_scale) + r * NG)[G] = __half_as_ushort(s16);
   }
-  const uint32_t page = fast_div(static_cast<uint32_t>(slot), ps);
-  const int64_t r = ((int64_t)page * Hk + head) * c.page_size + (static_cast<uint32_t>(slot) - page * ps.d);
-  reinterpret_cast<uint4*>(static_cast<uint8_t*>(is_v ? c.v : c.k) + r * (D / 2))[G] =
-      make_uint4(word[0], word[1], word[2], word[3]);
-  (static_cast<uint16_t*>(is_v ? c.v_scale : c.k_scale) + r * NG)[G] = __half_as_ushort(s16);
 }
 
 // Latency form of the same store for a handful of rows (a decode step stores one
@@ -375,6 +417,14 @@ cudaError_t launch_store(const kvq_cache& c, const void* k, const void* v, int d
   } else if (q4) {
     // one lane per (row, group); launches of at most 2^30 groups, so that the
     // kernel's group indices stay 32-bit
+    int dev = 0, n_sm = 0, per_sm = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      n_sm = 1;
+    {
+      auto kern = rot ? store_q4_lane_kernel<8, true, true, true> : store_q4_lane_kernel<8, false, true, true>;
+      if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, 256, 0) != cudaSuccess || per_sm < 1) per_sm = 1;
+    }
+    const int64_t lane_blocks = static_cast<int64_t>(n_sm) * per_sm;
     const int64_t per_tok = static_cast<int64_t>(c.num_kv_heads) * 2 * (c.head_dim / 32);
     const int64_t max_tok = (int64_t(1) << 30) / per_tok;
     const size_t esz = dtype == KVQ_DT_F32 ? 4 : 2;
@@ -386,12 +436,17 @@ cudaError_t launch_store(const kvq_cache& c, const void* k, const void* v, int d
       const void* kc = static_cast<const uint8_t*>(k) + t0 * tok_bytes;
       const void* vc = static_cast<const uint8_t*>(v) + t0 * tok_bytes;
       const int32_t* sc = slots + t0;
-      const dim3 blocks(static_cast<unsigned>((nt * per_tok + 255) / 256));  // one lane per (row, group)
-#define KVQ_STORE_WIDE(NG, ROT)                                                                                     \
-  e = vec ? launch_pdl(store_q4_lane_kernel<NG, ROT, true>, blocks, dim3(256), 0, s, c, kc, vc, dtype, nt, sc,      \
-                       status, hk, ps)                                                                              \
-          : launch_pdl(store_q4_lane_kernel<NG, ROT, false>, blocks, dim3(256), 0, s, c, kc, vc, dtype, nt, sc,     \
-                       status, hk, ps)
+      // a grid the GPU holds at once (each thread walks several groups)
+      const int64_t need = (nt * per_tok + 255) / 256;
+      const dim3 blocks(static_cast<unsigned>(need < lane_blocks ? need : lane_blocks));
+#define KVQ_STORE_WIDE(NG, ROT)                                                                                      \
+  e = !vec ? launch_pdl(store_q4_lane_kernel<NG, ROT, false>, blocks, dim3(256), 0, s, c, kc, vc, dtype, nt, sc,     \
+                        status, hk, ps)                                                                              \
+    : dtype == KVQ_DT_BF16                                                                                           \
+        ? launch_pdl(store_q4_lane_kernel<NG, ROT, true, true>, blocks, dim3(256), 0, s, c, kc, vc, dtype, nt, sc,   \
+                     status, hk, ps)                                                                                 \
+        : launch_pdl(store_q4_lane_kernel<NG, ROT, true, false>, blocks, dim3(256), 0, s, c, kc, vc, dtype, nt, sc,  \
+                     status, hk, ps)
 #define KVQ_STORE_ROW(NG)         \
   if (rot) {                      \
     KVQ_STORE_WIDE(NG, true);     \

@@ -196,7 +196,7 @@ int32_t kvq_store_rotate(const kvq_cache* cache, const void* k, const void* v, i
  * a 256-byte header (status word at offset 0), then partial maxima m and sums z
  * [num_seqs][num_q_heads][P] f32 and partial contexts acc [num_seqs][num_q_heads]
  * [P][value width] f32, where P = ceil(max_seq_len / 512), or for a gather
- * P = ceil(n_sel / 512) (FP8_ROW: ceil(n_sel / 128)), then the
+ * P = ceil(n_sel / 512) (FP8_ROW: ceil(n_sel / 64)), then the
  * completion counters of kvq_decode_merged [num_seqs][num_kv_heads] int32 (zero
  * before the first kvq_decode_merged on the workspace; each complete call
  * leaves them zero). */
@@ -208,7 +208,7 @@ size_t kvq_decode_workspace_size(const kvq_cache* cache, int32_t num_seqs, int32
  * [P3] split-T commit: dim3(H,P) partial online-softmax blocks (cl, m, z)).
  * For sequence b, query head h (reading KV head h / (num_q_heads / num_kv_heads))
  * and partition p (keys [512p, min(512p + 512, T_b)), T_b = seq_lens[b], or the
- * p-th run of 512 entries of sel[b] when gathering -- 128 entries for FP8_ROW),
+ * p-th run of 512 entries of sel[b] when gathering -- 64 entries for FP8_ROW),
  * writes
  *   m = max_j s_j * log2(e),  z = sum_j 2^(s_j log2(e) - m),
  *   acc = sum_j 2^(s_j log2(e) - m) * value_j,   s_j = sm_scale * (q . key_j)
