@@ -294,21 +294,24 @@ constexpr int kQ4MaxColTiles = 4;                 // a decode window stacks up t
 // accumulators per thread.
 __host__ __device__ constexpr int q4_min_blocks(int nt) { return nt == 1 ? 4 : nt == 2 ? 3 : 2; }
 
-template <int NT, bool GATHER>
+// VR: rounds the V ring holds (1, or 2 where shared memory allows: round r + 1's
+// V is then copied while round r is computed, with no wait for the warps to
+// finish round r's P.V).
+template <int NT, bool GATHER, int VR = 1>
 struct __align__(1024) Q4Smem {
   static constexpr int kTile = q4_tile_bytes<GATHER>();
   uint8_t kc[kQ4Warps][kQ4TPW][kTile];  // K codes of each warp's tiles of the round (1024-aligned)
-  uint8_t vc[kQ4RoundTiles][kTile];     // V codes of the round's tiles
+  uint8_t vc[VR][kQ4RoundTiles][kTile];  // V codes of the round's tiles, by round mod VR
   uint16_t ks[kQ4Warps][kQ4TPW][16 * 8];       // K scales
-  uint16_t vs[kQ4RoundTiles][16 * 8];          // V scales
+  uint16_t vs[VR][kQ4RoundTiles][16 * 8];      // V scales
   uint4 qf[NT][kQ4NG][2][32];                  // query fragments [column tile][group][hi, lo][lane]
   float4 qb[NT][kQ4NG][4];  // [column tile][group][t]: minus the code-offset bias of columns (2t, 2t+1, 2t, 2t+1)
   uint2 pb[kQ4RoundTiles][NT][32];  // [tile][column tile][lane]: P of the round as B fragments (keys 2t.., 2t+8..)
   float red[kQ4Warps][8 * NT];      // [warp][column]: maxima of each warp's tiles of the round
   float zs[kQ4Warps][8 * NT];       // per-warp sums of the probabilities
   uint64_t kbar[kQ4Warps];          // a warp's K tiles landed (kQ4TPW arrivals)
-  uint64_t vfull;                   // the round's V tiles landed (kQ4RoundTiles arrivals)
-  uint64_t vempty;                  // every warp is done with the round's V (kQ4Warps arrivals)
+  uint64_t vfull[VR];               // the round's V tiles landed (kQ4RoundTiles arrivals)
+  uint64_t vempty;                  // VR = 1: every warp is done with the round's V (kQ4Warps arrivals)
   int poison;
   int last;  // fused merge: this CTA finished its (sequence, KV head) last
 };
@@ -482,8 +485,9 @@ __device__ __forceinline__ void q4_fused_merge(const DecodeArgs& a, int b, int k
 // end (its length), its own softmax state and its own partials.
 // MINB: resident CTAs per SM the registers are budgeted for (0: q4_min_blocks);
 // a grid that fits in two CTAs per SM takes MINB = 2 (up to 255 registers, more
-// score chains in flight per warp).  The arithmetic is the same PTX either way.
-template <bool GATHER, int NT, bool WIN, bool TQ = false, bool LM = false, int MINB = 0>
+// score chains in flight per warp) and VR = 2 (a two-round V ring).  The
+// arithmetic is the same either way; only the copy schedule differs.
+template <bool GATHER, int NT, bool WIN, bool TQ = false, bool LM = false, int MINB = 0, int VR = 1>
 __global__ void __launch_bounds__(kQ4Warps * 32, MINB ? MINB : q4_min_blocks(NT))
     decode_q4_round_kernel(const __grid_constant__ DecodeArgs a) {
   static_assert(!(WIN && GATHER), "decode windows read dense prefixes");
@@ -492,8 +496,8 @@ __global__ void __launch_bounds__(kQ4Warps * 32, MINB ? MINB : q4_min_blocks(NT)
   static_assert(!LM || (!GATHER && !WIN && !TQ), "the fused merge: dense 4-bit decode");
   extern __shared__ uint8_t smem_raw[];
   // 1024-byte alignment for the swizzled tiles (the launch adds 1 KB of slack)
-  Q4Smem<NT, GATHER>& sm =
-      *reinterpret_cast<Q4Smem<NT, GATHER>*>(smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u));
+  Q4Smem<NT, GATHER, VR>& sm =
+      *reinterpret_cast<Q4Smem<NT, GATHER, VR>*>(smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u));
   constexpr int kTile = q4_tile_bytes<GATHER>();
   const int p = blockIdx.x, kvh = blockIdx.y;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -567,7 +571,7 @@ __global__ void __launch_bounds__(kQ4Warps * 32, MINB ? MINB : q4_min_blocks(NT)
   }
   if (active && threadIdx.x == 0) {
     for (int w = 0; w < kQ4Warps; ++w) mbar_init(&sm.kbar[w], kQ4TPW);
-    mbar_init(&sm.vfull, kQ4RoundTiles);
+    for (int i = 0; i < VR; ++i) mbar_init(&sm.vfull[i], kQ4RoundTiles);
     mbar_init(&sm.vempty, kQ4Warps);
     sm.poison = 0;
     fence_barrier_init();
@@ -609,11 +613,16 @@ __global__ void __launch_bounds__(kQ4Warps * 32, MINB ? MINB : q4_min_blocks(NT)
                             lane, sm.qf[0]);
     __syncthreads();
   } else {
-    q4_query_prep<kQ4Warps>(a, b, kvh, warp, lane, reinterpret_cast<float*>(&sm.vc[0][0]), sm.qf[0], sm.qb[0]);
+    q4_query_prep<kQ4Warps>(a, b, kvh, warp, lane, reinterpret_cast<float*>(&sm.vc[0][0][0]), sm.qf[0], sm.qb[0]);
   }
-  // V of round 0: vc[0..3] held the rotated queries until the prologue's last barrier
+  // V of round 0: vc[0][0..3] held the rotated queries until the prologue's last barrier
   poisoned |= q4_issue_own<GATHER, TQ>(a, b, kvh, k0, k1, 0, warp, lane, tile_row, &a.tm_v, c.v, c.v_scale,
-                                   &sm.vc[kQ4TPW * warp], &sm.vs[kQ4TPW * warp], &sm.vfull);
+                                   &sm.vc[0][kQ4TPW * warp], &sm.vs[0][kQ4TPW * warp], &sm.vfull[0]);
+  if constexpr (VR == 2) {
+    if (nrounds > 1)
+      poisoned |= q4_issue_own<GATHER, TQ>(a, b, kvh, k0, k1, 1, warp, lane, tile_row, &a.tm_v, c.v, c.v_scale,
+                                       &sm.vc[1][kQ4TPW * warp], &sm.vs[1][kQ4TPW * warp], &sm.vfull[1]);
+  }
   const uint32_t qf_addr = smem_u32(&sm.qf[0][0][0][lane]);
   const uint32_t qb_addr = smem_u32(&sm.qb[0][0][t]);
   constexpr uint32_t kQfTile = sizeof(sm.qf[0]), kQbTile = sizeof(sm.qb[0]);
@@ -650,10 +659,8 @@ __global__ void __launch_bounds__(kQ4Warps * 32, MINB ? MINB : q4_min_blocks(NT)
   const uint32_t off_vl = chunk_off(2 * warp);  // V: groups 2w, 2w + 1 of this warp
   const uint32_t kc_base = smem_u32(&sm.kc[warp][0][0]);
   const uint32_t ks_base = smem_u32(&sm.ks[warp][0][0]);
-  const uint32_t vc_base = smem_u32(&sm.vc[0][0]);
-  const uint32_t vs_base = smem_u32(&sm.vs[0][0]) + 4 * warp;
+  constexpr uint32_t kVcSlot = sizeof(sm.vc[0]), kVsSlot = sizeof(sm.vs[0]);
   const uint32_t pb_addr = smem_u32(&sm.pb[0][0][lane]);
-  const uint32_t vs_tq = smem_u32(&sm.vs[0][0]);  // TQ4: one fp16 scale per key
 
   for (int r = 0; r < nrounds; ++r) {
     const uint32_t par = r & 1;
@@ -810,6 +817,13 @@ __global__ void __launch_bounds__(kQ4Warps * 32, MINB ? MINB : q4_min_blocks(NT)
       if (g == 0) *reinterpret_cast<float2*>(&sm.red[warp][8 * nt + 2 * t]) = make_float2(t0[nt], t1[nt]);
     }
     bar_sync_cta();  // (1) maxima published; every warp is past the P.V of round r - 1
+    if constexpr (VR == 2) {
+      // slot (r + 1) % 2 held round r - 1's V, which every warp is done with: round r + 1's
+      if (r >= 1 && r + 1 < nrounds)
+        poisoned |= q4_issue_own<GATHER, TQ>(a, b, kvh, k0, k1, r + 1, warp, lane, tile_row, &a.tm_v, c.v, c.v_scale,
+                                         &sm.vc[(r + 1) & 1][kQ4TPW * warp], &sm.vs[(r + 1) & 1][kQ4TPW * warp],
+                                         &sm.vfull[(r + 1) & 1]);
+    }
     {
       const uint32_t ra = smem_u32(&sm.red[0][2 * t]);
 #pragma unroll
@@ -866,7 +880,12 @@ __global__ void __launch_bounds__(kQ4Warps * 32, MINB ? MINB : q4_min_blocks(NT)
     bar_sync_cta();  // (2) every tile's P is published
 
     // ---------------- P.V over the round's tiles for groups 2w, 2w+1
-    if (!timed_out && !__all_sync(0xffffffffu, mbar_wait_bounded(&sm.vfull, par))) timed_out = true;
+    const int vslot = VR == 2 ? (r & 1) : 0;
+    const uint32_t vpar = VR == 2 ? ((r >> 1) & 1) : par;
+    if (!timed_out && !__all_sync(0xffffffffu, mbar_wait_bounded(&sm.vfull[vslot], vpar))) timed_out = true;
+    const uint32_t vc_base = smem_u32(&sm.vc[0][0][0]) + vslot * kVcSlot;
+    const uint32_t vs_base = smem_u32(&sm.vs[0][0][0]) + vslot * kVsSlot + 4 * warp;
+    const uint32_t vs_tq = smem_u32(&sm.vs[0][0][0]) + vslot * kVsSlot;  // TQ4: one fp16 scale per key
     const bool tail_round = k0 + kQ4RoundTiles * 16 * (r + 1) > k1;  // CTA-uniform
     // Every tile of the round is visited.  Keys past the end (the tail of the
     // last tile, and the tiles the last round does not have) get zero V scales:
@@ -960,13 +979,15 @@ __global__ void __launch_bounds__(kQ4Warps * 32, MINB ? MINB : q4_min_blocks(NT)
       pv_round(std::false_type{});
 
     // The round's V is consumed once every warp gets here: then each warp
-    // refills its own V tiles with round r + 1.
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&sm.vempty);
-    if (r + 1 < nrounds) {
-      if (!timed_out && !__all_sync(0xffffffffu, mbar_wait_bounded(&sm.vempty, par))) timed_out = true;
-      poisoned |= q4_issue_own<GATHER, TQ>(a, b, kvh, k0, k1, r + 1, warp, lane, tile_row, &a.tm_v, c.v, c.v_scale,
-                                       &sm.vc[kQ4TPW * warp], &sm.vs[kQ4TPW * warp], &sm.vfull);
+    // refills its own V tiles with round r + 1 (a one-round ring).
+    if constexpr (VR == 1) {
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sm.vempty);
+      if (r + 1 < nrounds) {
+        if (!timed_out && !__all_sync(0xffffffffu, mbar_wait_bounded(&sm.vempty, par))) timed_out = true;
+        poisoned |= q4_issue_own<GATHER, TQ>(a, b, kvh, k0, k1, r + 1, warp, lane, tile_row, &a.tm_v, c.v, c.v_scale,
+                                         &sm.vc[0][kQ4TPW * warp], &sm.vs[0][kQ4TPW * warp], &sm.vfull[0]);
+      }
     }
   }
   if (timed_out && lane == 0) set_status(a.status, KVQ_DEV_TIMEOUT);
@@ -1056,10 +1077,10 @@ __global__ void __launch_bounds__(kQ4Warps * 32, MINB ? MINB : q4_min_blocks(NT)
   pdl_trigger();  // after this CTA's last write
 }
 
-template <bool GATHER, int NT, bool WIN, bool TQ = false, bool LM = false, int MINB = 0>
+template <bool GATHER, int NT, bool WIN, bool TQ = false, bool LM = false, int MINB = 0, int VR = 1>
 cudaError_t launch_round(const DecodeArgs& a, dim3 grid, cudaStream_t s) {
-  const size_t smem = sizeof(Q4Smem<NT, GATHER>) + 1024;  // + slack for the 1024-byte alignment
-  auto kern = decode_q4_round_kernel<GATHER, NT, WIN, TQ, LM, MINB>;
+  const size_t smem = sizeof(Q4Smem<NT, GATHER, VR>) + 1024;  // + slack for the 1024-byte alignment
+  auto kern = decode_q4_round_kernel<GATHER, NT, WIN, TQ, LM, MINB, VR>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   e = launch_pdl(kern, grid, dim3(kQ4Warps * 32), smem, s, a);
@@ -1085,7 +1106,7 @@ cudaError_t launch_decode_q4(const DecodeArgs& a, int B, cudaStream_t s) {
     if (a.fused_out) return a.sel ? cudaErrorInvalidValue : launch_round<false, 1, false, false, true>(a, grid, s);
     if (a.sel) return launch_round<true, 1, false>(a, grid, s);
     const int64_t ctas = (int64_t)grid.x * grid.y * grid.z;
-    if (ctas <= 2 * (int64_t)sm_count()) return launch_round<false, 1, false, false, false, 2>(a, grid, s);
+    if (ctas <= 2 * (int64_t)sm_count()) return launch_round<false, 1, false, false, false, 2, 2>(a, grid, s);
     return launch_round<false, 1, false>(a, grid, s);
   }
   if (a.tq) return cudaErrorInvalidValue;
