@@ -51,8 +51,8 @@ KERNELS_PER_LAYER = 3  # store + query rotation (one launch), split-T decode, me
 # beside them: once those sources change, the bench reports no traffic until
 # the capture is taken again.
 TRAFFIC_SOURCES = ("bit_quantized_kv_store_gb300/csrc/decode_q4.cu", "bit_quantized_kv_store_gb300/csrc/common.cuh")
-TRAFFIC_CAPTURE = {"sources_sha16": "5b56ddfa016d6d15",
-                   "bytes": {32768: 37867008 + 0, 262144: 302277120 + 10575104}}
+TRAFFIC_CAPTURE = {"sources_sha16": "69447ea51af25651",
+                   "bytes": {32768: 37867008 + 0, 262144: 302254592 + 10170880}}
 BYTES_PER_POS_LAYER = HK * 2 * (D // 2 + 2 * (D // 32))   # 1152
 
 
