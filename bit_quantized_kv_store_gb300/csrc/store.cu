@@ -22,14 +22,15 @@ namespace kvq {
 // code = clamp(rint_even(fl(y / s)), -8, 7) + 8, with fl(y / s) the IEEE-rounded
 // fp32 quotient and s > 0 (an fp16 value, so a normal fp32 number).
 //
-// Screen: q0 = fl(y * r) with r = rcp.approx(s) (at most 1 ulp off, PTX ISA)
-// is within a relative 2^-22 of the exact quotient Q.  While |Q| < 16 that is
-// an absolute error below 2^-18, and fl(Q) is within 2^-21 of Q; so when q0 is
-// farther than 2^-14 from every half-integer, Q and fl(Q) lie strictly inside
-// the same unit interval (k - 1/2, k + 1/2) around k = rint(q0), and
-// rint_even(fl(Q)) = k without a tie.  (For |Q| >= 16 both k and rint(fl(Q))
-// are beyond the clamp on the same side.)  Anything else -- exact or near ties,
-// NaN, infinities -- takes the IEEE division.
+// Screen: with r = rcp.approx(s) (at most 1 ulp off, PTX ISA), t = fl(y * r + 8)
+// (one fused rounding) is within |Q| 2^-23 + |Q + 8| 2^-24 < 2^-18 of Q + 8
+// while |Q| < 16, Q = y / s exactly, and fl(Q) is within 2^-21 of Q.  So when
+// t is farther than 2^-14 from every half-integer, Q + 8 and fl(Q) + 8 lie
+// strictly inside the same unit interval (k - 1/2, k + 1/2) around k = rint(t),
+// and rint_even(fl(Q)) = k - 8 without a tie (8 is even, so ties keep their
+// side).  For Q >= 16 (Q <= -16) both k and rint(fl(Q)) + 8 are beyond the
+// clamp at 15 (at 0).  Anything else -- exact or near ties, NaN, infinities --
+// takes the IEEE division.
 constexpr float kQ4Screen = 0.5f - 0.00006103515625f;  // 1/2 - 2^-14
 
 __device__ __forceinline__ float rcp_approx(float x) {
@@ -41,10 +42,17 @@ __device__ __forceinline__ float rcp_approx(float x) {
 // The code from the screened estimate; returns false when the estimate cannot
 // decide it (then call q4_code_exact).
 __device__ __forceinline__ bool q4_code_screened(float y, float r, uint32_t& code) {
-  const float q0 = __fmul_rn(y, r);
-  const float k = rintf(q0);
-  code = static_cast<uint32_t>(static_cast<int>(fminf(fmaxf(k, -8.0f), 7.0f)) + 8);
-  return fabsf(__fsub_rn(q0, k)) < kQ4Screen;
+  const float t = __fmaf_rn(y, r, 8.0f);
+  const float k = rintf(t);
+  code = static_cast<uint32_t>(fminf(fmaxf(k, 0.0f), 15.0f));
+  return fabsf(__fsub_rn(t, k)) < kQ4Screen;
+}
+
+// Insert a 4-bit code at bit 4i of w.
+__device__ __forceinline__ uint32_t put_nibble(uint32_t w, uint32_t code, int i) {
+  uint32_t r;
+  asm("bfi.b32 %0, %1, %2, %3, 4;" : "=r"(r) : "r"(code), "r"(w), "r"(4 * i));
+  return r;
 }
 
 __device__ __forceinline__ uint32_t q4_code_exact(float y, float s) {
@@ -90,8 +98,10 @@ __device__ __forceinline__ void load_group(const void* __restrict__ src, int dty
 
 // BF: bf16 inputs with VEC (16-byte loads of bf16 pairs); otherwise 32 f32 words
 // (VEC) or element loads of either type.
+constexpr int kLaneBlock = 128;
+
 template <int NG, bool ROT, bool VEC, bool BF = false>
-__global__ void __launch_bounds__(256) store_q4_lane_kernel(kvq_cache c, const void* __restrict__ k,
+__global__ void __launch_bounds__(kLaneBlock, 5) store_q4_lane_kernel(kvq_cache c, const void* __restrict__ k,
                                                             const void* __restrict__ v, int dtype, int64_t n_tok,
                                                             const int32_t* __restrict__ slots, int32_t* status,
                                                             FastDiv hk, FastDiv ps) {
@@ -174,24 +184,27 @@ __global__ void __launch_bounds__(256) store_q4_lane_kernel(kvq_cache c, const v
     uint32_t word[4] = {0x88888888u, 0x88888888u, 0x88888888u, 0x88888888u};  // scale 0: every code 8
     if (s != 0.0f) {
       const float r = rcp_approx(s);
-      bool undecided = false;
+      uint32_t undecided = 0;  // bit i: value i needs the IEEE division
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
-        word[q] = 0;
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
           uint32_t code;
-          undecided |= !q4_code_screened(x[8 * q + i], r, code);
-          word[q] |= code << (4 * i);
+          if (!q4_code_screened(x[8 * q + i], r, code)) undecided |= 1u << (8 * q + i);
+          word[q] = put_nibble(word[q], code, i);
         }
       }
-      if (undecided) {  // rare: ties and near-ties
+      // ties and near-ties (rare after the rotation; frequent for unrotated
+      // inputs of few mantissa bits, where y / s is often exactly k + 1/2):
+      // only those values take the division
+      while (undecided) {
+        const int i = __ffs(undecided) - 1;
+        undecided &= undecided - 1;
+        float y = x[0];
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          word[q] = 0;
-#pragma unroll
-          for (int i = 0; i < 8; ++i) word[q] |= q4_code_exact(x[8 * q + i], s) << (4 * i);
-        }
+        for (int j = 1; j < 32; ++j)
+          if (j == i) y = x[j];
+        word[i >> 3] = put_nibble(word[i >> 3], q4_code_exact(y, s), i & 7);
       }
     }
     const uint32_t page = fast_div(static_cast<uint32_t>(slot), ps);
@@ -422,9 +435,10 @@ cudaError_t launch_store(const kvq_cache& c, const void* k, const void* v, int d
       n_sm = 1;
     {
       auto kern = rot ? store_q4_lane_kernel<8, true, true, true> : store_q4_lane_kernel<8, false, true, true>;
-      if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, 256, 0) != cudaSuccess || per_sm < 1) per_sm = 1;
+      if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kLaneBlock, 0) != cudaSuccess || per_sm < 1)
+        per_sm = 1;
     }
-    const int64_t lane_blocks = static_cast<int64_t>(n_sm) * per_sm;
+    const int64_t lane_threads = static_cast<int64_t>(n_sm) * per_sm * kLaneBlock;  // resident at once
     const int64_t per_tok = static_cast<int64_t>(c.num_kv_heads) * 2 * (c.head_dim / 32);
     const int64_t max_tok = (int64_t(1) << 30) / per_tok;
     const size_t esz = dtype == KVQ_DT_F32 ? 4 : 2;
@@ -436,16 +450,17 @@ cudaError_t launch_store(const kvq_cache& c, const void* k, const void* v, int d
       const void* kc = static_cast<const uint8_t*>(k) + t0 * tok_bytes;
       const void* vc = static_cast<const uint8_t*>(v) + t0 * tok_bytes;
       const int32_t* sc = slots + t0;
-      // a grid the GPU holds at once (each thread walks several groups)
-      const int64_t need = (nt * per_tok + 255) / 256;
-      const dim3 blocks(static_cast<unsigned>(need < lane_blocks ? need : lane_blocks));
+      // a grid the GPU holds at once, every thread walking the same number of groups
+      const int64_t groups = nt * per_tok;
+      const int64_t per_thread = (groups + lane_threads - 1) / lane_threads;
+      const dim3 blocks(static_cast<unsigned>((groups + per_thread * kLaneBlock - 1) / (per_thread * kLaneBlock)));
 #define KVQ_STORE_WIDE(NG, ROT)                                                                                      \
-  e = !vec ? launch_pdl(store_q4_lane_kernel<NG, ROT, false>, blocks, dim3(256), 0, s, c, kc, vc, dtype, nt, sc,     \
+  e = !vec ? launch_pdl(store_q4_lane_kernel<NG, ROT, false>, blocks, dim3(kLaneBlock), 0, s, c, kc, vc, dtype, nt, sc,     \
                         status, hk, ps)                                                                              \
     : dtype == KVQ_DT_BF16                                                                                           \
-        ? launch_pdl(store_q4_lane_kernel<NG, ROT, true, true>, blocks, dim3(256), 0, s, c, kc, vc, dtype, nt, sc,   \
+        ? launch_pdl(store_q4_lane_kernel<NG, ROT, true, true>, blocks, dim3(kLaneBlock), 0, s, c, kc, vc, dtype, nt, sc,   \
                      status, hk, ps)                                                                                 \
-        : launch_pdl(store_q4_lane_kernel<NG, ROT, true, false>, blocks, dim3(256), 0, s, c, kc, vc, dtype, nt, sc,  \
+        : launch_pdl(store_q4_lane_kernel<NG, ROT, true, false>, blocks, dim3(kLaneBlock), 0, s, c, kc, vc, dtype, nt, sc,  \
                      status, hk, ps)
 #define KVQ_STORE_ROW(NG)         \
   if (rot) {                      \
