@@ -87,9 +87,10 @@ static bool encode_rows_map(CUtensorMap* m, const void* base, uint64_t rows, uin
 }
 
 struct WsLayout {
-  size_t m_off, z_off, acc_off, ctr_off, total;
+  size_t m_off, z_off, acc_off, ctr_off, bm_off, bz_off, bacc_off, total;
   int P;
   int part;  // keys per partition
+  int nblk;  // the fused merge's blocks of kMergeBlock partitions
 };
 
 // Keys per split-T partition: 512 ("shared 512-key chunks") for every format
@@ -111,8 +112,14 @@ static WsLayout ws_layout(const kvq_cache* c, int B, int Hq, int max_seq_len, in
   w.z_off = w.m_off + round256(n * sizeof(float));
   w.acc_off = w.z_off + round256(n * sizeof(float));
   w.ctr_off = w.acc_off + round256(n * value_width(c) * sizeof(float));
-  // completion counters of the fused merge, one per (sequence, KV head)
-  w.total = w.ctr_off + round256(static_cast<size_t>(B) * c->num_kv_heads * sizeof(int32_t));
+  // the fused merge: completion counters per (sequence, KV head) and per block
+  // of kMergeBlock partitions, then the block partials
+  w.nblk = (w.P + kMergeBlock - 1) / kMergeBlock;
+  const size_t nb = static_cast<size_t>(B) * Hq * w.nblk;
+  w.bm_off = w.ctr_off + round256(static_cast<size_t>(B) * c->num_kv_heads * (1 + w.nblk) * sizeof(int32_t));
+  w.bz_off = w.bm_off + round256(nb * sizeof(float));
+  w.bacc_off = w.bz_off + round256(nb * sizeof(float));
+  w.total = w.bacc_off + round256(nb * value_width(c) * sizeof(float));
   return w;
 }
 
@@ -316,6 +323,11 @@ static int32_t decode_attn_impl(const kvq_cache* cache, const float* q, const vo
     a.part = w.part;
     a.fused_out = fused_out;
     a.merge_ctr = reinterpret_cast<int32_t*>(ws + w.ctr_off);
+    a.merge_B = num_seqs;
+    a.merge_nblk = w.nblk;
+    a.merge_m = reinterpret_cast<float*>(ws + w.bm_off);
+    a.merge_z = reinterpret_cast<float*>(ws + w.bz_off);
+    a.merge_acc = reinterpret_cast<float*>(ws + w.bacc_off);
     a.status = reinterpret_cast<int32_t*>(ws);
     if (!d_sel) {
       const uint64_t rows = static_cast<uint64_t>(cache->num_pages) * cache->num_kv_heads * cache->page_size;
@@ -350,9 +362,10 @@ int32_t kvq_decode_merged(const kvq_cache* cache, const float* q, int32_t num_se
   if (!cache) return KVQ_ERR_INVALID_ARG;
   if (!is_q4(cache->format)) return KVQ_ERR_UNSUPPORTED;
   if (num_seqs > 0 && !out) return KVQ_ERR_INVALID_ARG;
-  // the last CTA keeps its group's partition weights in its 32 KB of ring buffers
+  // the last block folder keeps the group's block weights in its 32 KB of ring buffers
   const int64_t parts = (static_cast<int64_t>(max_seq_len) + kPart - 1) / kPart;
-  if (cache->num_kv_heads > 0 && num_q_heads > 0 && parts * (num_q_heads / cache->num_kv_heads) > 8192)
+  const int64_t blocks = (parts + kMergeBlock - 1) / kMergeBlock;
+  if (cache->num_kv_heads > 0 && num_q_heads > 0 && blocks * (num_q_heads / cache->num_kv_heads) > 8192)
     return KVQ_ERR_UNSUPPORTED;
   return decode_attn_impl(cache, q, nullptr, 0, num_seqs, num_q_heads, d_seq_lens, d_block_tables, max_pages_per_seq,
                           max_seq_len, nullptr, 0, sm_scale, workspace, ws_bytes, stream, false, out);

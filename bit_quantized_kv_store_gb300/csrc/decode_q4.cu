@@ -398,67 +398,86 @@ __device__ __forceinline__ bool q4_issue_own(const DecodeArgs& a, int b, int kvh
   return bad;
 }
 
-// The fused merge (kvq_decode_merged): run by the last CTA of a (sequence b, KV
-// head) to finish, once every partial of the group is in memory.  Warp w
-// reduces heads 2w, 2w + 1: the maximum M over the partitions, the weights
-// 2^(m_p - M) (into `wts`) and Z = sum_p z_p 2^(m_p - M), in a fixed order.
-// Then thread i takes dims 2i, 2i + 1 of every head: o = sum_p acc_p w_p / Z in
-// ascending p, rotated back per 32-group (Q4_HAD32) and stored.
-__device__ __forceinline__ void q4_fused_merge(const DecodeArgs& a, int b, int kvh, int np, float* wts, float* zsum,
-                                               bool rotate_back) {
+// The fused merge (kvq_decode_merged) folds partials in two levels: the last
+// CTA of each block of kMergeBlock consecutive partitions of a (sequence b,
+// KV head) folds that block's partials into a block partial, and the last of
+// the group's block folders folds the block partials into the outputs.  The
+// tree depends only on the partition indices, so the outputs do not depend on
+// the batch or on which CTA finishes last.
+// Fold n entries (i ascending) of each of the group's heads: M = max m_i,
+// w_i = 2^(m_i - M), Z = sum z_i w_i, acc = sum acc_i w_i.  Entry i of head h
+// sits at m[h * hs + i], z[h * hs + i], acc[(h * hs + i) * 256 ..].  Warp w
+// computes the weights of heads 2w, 2w + 1 (lanes over i; Z by a fixed xor
+// tree), then thread t takes dims 2t, 2t + 1 of every head.  final = false:
+// (M, Z, acc) go to om, oz, oacc at [h * ohs] (M = NaN if some m_i is NaN);
+// final = true: out = acc / Z (0 for a group without keys, NaN for a NaN),
+// rotated back per 32-group when rotate_back, at out + h * 256.
+__device__ __forceinline__ void q4_fold(const float* m, const float* z, const float* acc, int64_t hs, int n,
+                                        int group, float* wts, float* zsum, bool final, float* om, float* oz,
+                                        float* oacc, int64_t ohs, float* out, bool rotate_back) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  float* mx = zsum + 8;  // [group]: the heads' maxima
   for (int hh = 0; hh < 2; ++hh) {
     const int h = 2 * warp + hh;
-    if (h >= a.group) break;
-    const int64_t base = ((int64_t)b * a.Hq + kvh * a.group + h) * a.P;
+    if (h >= group) break;
     float M = -INFINITY;
     bool nan_seen = false;
-    for (int p = lane; p < np; p += 32) {
-      const float m = __ldcg(a.ws_m + base + p);
-      nan_seen |= isnan(m);
-      M = fmaxf(M, m);
+    for (int i = lane; i < n; i += 32) {
+      const float v = __ldcg(m + h * hs + i);
+      nan_seen |= isnan(v);
+      M = fmaxf(M, v);
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
     nan_seen = __any_sync(0xffffffffu, nan_seen);
     float Z = 0.f;
-    for (int p = lane; p < np; p += 32) {
-      const float m = __ldcg(a.ws_m + base + p);
-      const float w = (M == -INFINITY) ? 0.f : exp2f(m - M);
-      wts[h * np + p] = w;
-      Z = fmaf(__ldcg(a.ws_z + base + p), w, Z);
+    for (int i = lane; i < n; i += 32) {
+      const float v = __ldcg(m + h * hs + i);
+      const float w = (M == -INFINITY) ? 0.f : exp2f(v - M);
+      wts[h * n + i] = w;
+      Z = fmaf(__ldcg(z + h * hs + i), w, Z);
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) Z += __shfl_xor_sync(0xffffffffu, Z, o);
-    if (lane == 0) zsum[h] = nan_seen ? NAN : Z;
+    if (lane == 0) {
+      zsum[h] = nan_seen ? NAN : Z;
+      mx[h] = nan_seen ? NAN : M;
+    }
   }
   __syncthreads();
-  const int i = threadIdx.x;  // dims 2i, 2i + 1
-  for (int h = 0; h < a.group; ++h) {
-    const int64_t base = ((int64_t)b * a.Hq + kvh * a.group + h) * a.P;
-    const float* accp = a.ws_acc + base * kQ4D + 2 * i;
+  const int t = threadIdx.x;  // dims 2t, 2t + 1
+  for (int h = 0; h < group; ++h) {
+    const float* accp = acc + h * hs * kQ4D + 2 * t;
     float2 o = make_float2(0.f, 0.f);
-    int p = 0;
-    for (; p + 8 <= np; p += 8) {  // eight loads in flight
+    int i = 0;
+    for (; i + 8 <= n; i += 8) {  // eight loads in flight
       float2 v[8];
 #pragma unroll
-      for (int k = 0; k < 8; ++k) v[k] = __ldcg(reinterpret_cast<const float2*>(accp + (int64_t)(p + k) * kQ4D));
+      for (int k = 0; k < 8; ++k) v[k] = __ldcg(reinterpret_cast<const float2*>(accp + (int64_t)(i + k) * kQ4D));
 #pragma unroll
       for (int k = 0; k < 8; ++k) {
-        o.x = fmaf(v[k].x, wts[h * np + p + k], o.x);
-        o.y = fmaf(v[k].y, wts[h * np + p + k], o.y);
+        o.x = fmaf(v[k].x, wts[h * n + i + k], o.x);
+        o.y = fmaf(v[k].y, wts[h * n + i + k], o.y);
       }
     }
-    for (; p < np; ++p) {
-      const float2 v = __ldcg(reinterpret_cast<const float2*>(accp + (int64_t)p * kQ4D));
-      o.x = fmaf(v.x, wts[h * np + p], o.x);
-      o.y = fmaf(v.y, wts[h * np + p], o.y);
+    for (; i < n; ++i) {
+      const float2 v = __ldcg(reinterpret_cast<const float2*>(accp + (int64_t)i * kQ4D));
+      o.x = fmaf(v.x, wts[h * n + i], o.x);
+      o.y = fmaf(v.y, wts[h * n + i], o.y);
     }
     const float Z = zsum[h];
+    if (!final) {
+      *reinterpret_cast<float2*>(oacc + h * ohs * kQ4D + 2 * t) = o;
+      if (t == 0) {
+        om[h * ohs] = mx[h];
+        oz[h * ohs] = Z;
+      }
+      continue;
+    }
     const bool empty = !(Z > 0.f) && !isnan(Z);
     float x0 = empty ? 0.f : o.x / Z, x1 = empty ? 0.f : o.y / Z;
     if (rotate_back) {
-      // 32-point butterfly of the group: dims 2i, 2i + 1 here, the other 30 in
+      // 32-point butterfly of the group: dims 2t, 2t + 1 here, the other 30 in
       // the 15 neighbouring lanes (lane bits 0-3)
       float a0 = x0 + x1, a1 = x0 - x1;
 #pragma unroll
@@ -471,8 +490,7 @@ __device__ __forceinline__ void q4_fused_merge(const DecodeArgs& a, int b, int k
       x0 = __fmul_rn(a0, kHadamardScale);
       x1 = __fmul_rn(a1, kHadamardScale);
     }
-    *reinterpret_cast<float2*>(a.fused_out + ((int64_t)b * a.Hq + kvh * a.group + h) * kQ4D + 2 * i) =
-        make_float2(x0, x1);
+    *reinterpret_cast<float2*>(out + h * kQ4D + 2 * t) = make_float2(x0, x1);
   }
 }
 
@@ -1061,17 +1079,33 @@ __global__ void __launch_bounds__(kQ4Warps * 32, MINB ? MINB : q4_min_blocks(NT)
     // every thread's partials are visible device-wide before the count
     __threadfence();
     __syncthreads();
-    if (threadIdx.x == 0) {
-      const int done = atomicAdd(a.merge_ctr + (int64_t)b * a.c.num_kv_heads + kvh, 1);
-      sm.last = done == nparts - 1;
-    }
+    const int64_t grp = (int64_t)b * a.c.num_kv_heads + kvh;   // (sequence, KV head)
+    const int blk = p / kMergeBlock, p0 = blk * kMergeBlock;
+    const int nb = min(kMergeBlock, nparts - p0);             // partitions in this block
+    const int nblk = (nparts + kMergeBlock - 1) / kMergeBlock;
+    int32_t* bctr = a.merge_ctr + a.c.num_kv_heads * (int64_t)a.merge_B + grp * a.merge_nblk + blk;
+    if (threadIdx.x == 0) sm.last = atomicAdd(bctr, 1) == nb - 1;
     __syncthreads();
     if (sm.last) {
       __threadfence();
-      // the ring buffers are free now: weights [group][nparts], sums [group]
-      q4_fused_merge(a, b, kvh, nparts, reinterpret_cast<float*>(&sm.kc[0][0][0]), &sm.red[0][0],
-                     a.q_rotate != 0);
-      if (threadIdx.x == 0) a.merge_ctr[(int64_t)b * a.c.num_kv_heads + kvh] = 0;  // ready for the next launch
+      // the ring buffers are free now: weights [group][n], sums and maxima [group]
+      float* wts = reinterpret_cast<float*>(&sm.kc[0][0][0]);
+      const int64_t h0 = (int64_t)b * a.Hq + kvh * a.group;  // the group's first query head
+      q4_fold(a.ws_m + h0 * a.P + p0, a.ws_z + h0 * a.P + p0, a.ws_acc + (h0 * a.P + p0) * kQ4D, a.P, nb, a.group,
+              wts, &sm.red[0][0], false, a.merge_m + h0 * a.merge_nblk + blk, a.merge_z + h0 * a.merge_nblk + blk,
+              a.merge_acc + (h0 * a.merge_nblk + blk) * kQ4D, a.merge_nblk, nullptr, false);
+      if (threadIdx.x == 0) *bctr = 0;  // ready for the next launch
+      __threadfence();
+      __syncthreads();
+      if (threadIdx.x == 0) sm.last = atomicAdd(a.merge_ctr + grp, 1) == nblk - 1;
+      __syncthreads();
+      if (sm.last) {
+        __threadfence();
+        q4_fold(a.merge_m + h0 * a.merge_nblk, a.merge_z + h0 * a.merge_nblk, a.merge_acc + h0 * a.merge_nblk * kQ4D,
+                a.merge_nblk, nblk, a.group, wts, &sm.red[0][0], true, nullptr, nullptr, nullptr, 0,
+                a.fused_out + h0 * kQ4D, a.q_rotate != 0);
+        if (threadIdx.x == 0) a.merge_ctr[grp] = 0;
+      }
     }
   }
   pdl_trigger();  // after this CTA's last write
@@ -1103,10 +1137,14 @@ cudaError_t launch_decode_q4(const DecodeArgs& a, int B, cudaStream_t s) {
   if (a.nrows <= 0) {
     const dim3 grid(a.P, a.c.num_kv_heads, B);
     if (a.tq) return a.sel ? cudaErrorInvalidValue : launch_round<false, 1, false, true>(a, grid, s);
-    if (a.fused_out) return a.sel ? cudaErrorInvalidValue : launch_round<false, 1, false, false, true>(a, grid, s);
-    if (a.sel) return launch_round<true, 1, false>(a, grid, s);
     const int64_t ctas = (int64_t)grid.x * grid.y * grid.z;
-    if (ctas <= 2 * (int64_t)sm_count()) return launch_round<false, 1, false, false, false, 2, 2>(a, grid, s);
+    const bool small = ctas <= 2 * (int64_t)sm_count();  // one wave at two CTAs per SM
+    if (a.fused_out)
+      return a.sel ? cudaErrorInvalidValue
+                   : small ? launch_round<false, 1, false, false, true, 2, 2>(a, grid, s)
+                           : launch_round<false, 1, false, false, true>(a, grid, s);
+    if (a.sel) return launch_round<true, 1, false>(a, grid, s);
+    if (small) return launch_round<false, 1, false, false, false, 2, 2>(a, grid, s);
     return launch_round<false, 1, false>(a, grid, s);
   }
   if (a.tq) return cudaErrorInvalidValue;

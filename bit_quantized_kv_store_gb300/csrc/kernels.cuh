@@ -7,6 +7,9 @@
 
 namespace kvq {
 
+// Partitions per block of the fused merge's first level (kvq_decode_merged).
+constexpr int kMergeBlock = 8;
+
 // Split-T decode over the 4-bit rotated cache (decode_q4.cu).
 struct DecodeArgs {
   CUtensorMap tm_k;  // 4-bit: K codes plane as [rows][128 B], 16-row boxes, 128-byte swizzle;
@@ -46,10 +49,17 @@ struct DecodeArgs {
   // keys 0 .. prefill_q0 + b (seq_lens unused); 0: decode
   int prefill;
   int prefill_q0;
-  // 4-bit decode with the fused merge: the merged outputs [B][Hq][256] and the
-  // per-(sequence, KV head) completion counters (zero between launches)
+  // 4-bit decode with the fused merge: the merged outputs [B][Hq][256]; the
+  // completion counters (zero between launches): [B][Hk] per (sequence, KV
+  // head), then [B][Hk][merge_nblk] per block of 8 partitions; the block
+  // partials m, z [B][Hq][merge_nblk] and acc [B][Hq][merge_nblk][256]
   float* fused_out;
   int32_t* merge_ctr;
+  int merge_B;
+  int merge_nblk;
+  float* merge_m;
+  float* merge_z;
+  float* merge_acc;
 };
 
 // Log-sum-exp merge of the partials (merge.cu).

@@ -196,10 +196,11 @@ int32_t kvq_store_rotate(const kvq_cache* cache, const void* k, const void* v, i
  * a 256-byte header (status word at offset 0), then partial maxima m and sums z
  * [num_seqs][num_q_heads][P] f32 and partial contexts acc [num_seqs][num_q_heads]
  * [P][value width] f32, where P = ceil(max_seq_len / 512), or for a gather
- * P = ceil(n_sel / 512) (FP8_ROW: ceil(n_sel / 64)), then the
- * completion counters of kvq_decode_merged [num_seqs][num_kv_heads] int32 (zero
- * before the first kvq_decode_merged on the workspace; each complete call
- * leaves them zero). */
+ * P = ceil(n_sel / 512) (FP8_ROW: ceil(n_sel / 64)); then kvq_decode_merged's
+ * completion counters, int32 [num_seqs][num_kv_heads] and [num_seqs]
+ * [num_kv_heads][ceil(P / 8)] (zero before the first kvq_decode_merged on the
+ * workspace; each complete call leaves them zero), and its block partials
+ * (m, z [num_seqs][num_q_heads][ceil(P / 8)] f32, acc [..][value width] f32). */
 size_t kvq_decode_workspace_size(const kvq_cache* cache, int32_t num_seqs, int32_t num_q_heads,
                                  int32_t max_seq_len, int32_t n_sel);
 
@@ -254,14 +255,16 @@ int32_t kvq_decode_window(const kvq_cache* cache, const float* q, int32_t num_ro
 
 /* kvq_decode_merged -- kvq_decode_attn and kvq_merge (with the rotation back for
  * Q4_HAD32) in one launch ([P1] "What it is": the shared 512-key chunks and the
- * in-order merge of one decode round): the last CTA of each (sequence, KV head)
- * to finish, counted in the workspace, merges that group's partials in
- * ascending partition order and writes out [num_seqs, num_q_heads, 256] fp32.
- * The merged values equal kvq_merge's up to the order of the fp32 sums.  The
- * merge of a group then runs in one CTA, so this is slower than the two
- * launches once a group has many partitions.
+ * in-order merge of one decode round).  The merge runs in two levels inside the
+ * decode kernel: the last CTA to finish among each block of 8 consecutive
+ * partitions of a (sequence, KV head) folds that block's partials (ascending
+ * partition order) into a block partial, and the last block folder of the
+ * (sequence, KV head) folds the block partials (ascending) and writes out
+ * [num_seqs, num_q_heads, 256] fp32.  The tree depends only on the partition
+ * indices, so the values do not depend on the batch or on the order in which
+ * CTAs finish; they equal kvq_merge's up to the grouping of the fp32 sums.
  *   Arguments as for kvq_decode_attn (dense; 4-bit formats, else
- *   KVQ_ERR_UNSUPPORTED); ceil(max_seq_len / 512) * (num_q_heads /
+ *   KVQ_ERR_UNSUPPORTED); ceil(ceil(max_seq_len / 512) / 8) * (num_q_heads /
  *   num_kv_heads) <= 8192.  An invalid length gives NaN rows (and
  *   KVQ_DEV_BAD_LENGTH), an empty sequence zeros. */
 int32_t kvq_decode_merged(const kvq_cache* cache, const float* q, int32_t num_seqs, int32_t num_q_heads,

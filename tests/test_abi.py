@@ -93,9 +93,13 @@ def test_workspace_geometry(K):
         P = -(-T // 512)
         n = B * Hq * P
         r = lambda x: (x + 255) // 256 * 256
-        # header, m and z, acc, then one completion counter per (sequence, KV head)
+        nblk = -(-P // 8)
+        nb = B * Hq * nblk
+        # header, m and z, acc; then the fused merge's completion counters (per
+        # (sequence, KV head), and per block of 8 partitions) and block partials
         assert L.kvq_decode_workspace_size(ctypes.byref(d), B, Hq, T, 0) == \
-            256 + 2 * r(4 * n) + r(4 * n * 256) + r(4 * B * d.num_kv_heads)
+            256 + 2 * r(4 * n) + r(4 * n * 256) + r(4 * B * d.num_kv_heads * (1 + nblk)) + 2 * r(4 * nb) + \
+            r(4 * nb * 256)
 
 
 def test_plane_bytes_match_page_figures(K):
@@ -143,12 +147,13 @@ def test_host_validation_of_the_other_entries(K):
     assert L.kvq_decode_window(*win(c=bf)) == K.ERR_UNSUPPORTED
     assert L.kvq_decode_window(*win(rows=65)) == K.ERR_INVALID_ARG
     assert L.kvq_decode_window(*win(wsb=ws - 1)) == K.ERR_WORKSPACE_TOO_SMALL
-    # kvq_decode_merged: 4-bit only, an output, at most 8192 partition weights per group
+    # kvq_decode_merged: 4-bit only, an output, at most 8192 block weights per group
     mg = lambda c=d, out=dummy, msl=1000: (ctypes.byref(c), dummy, 1, 24, dummy, dummy, 100000, msl, f, dummy,
                                            1 << 40, out, None)
     assert L.kvq_decode_merged(*mg(c=fp8)) == K.ERR_UNSUPPORTED
     assert L.kvq_decode_merged(*mg(out=None)) == K.ERR_INVALID_ARG
-    assert L.kvq_decode_merged(*mg(msl=1366 * 512)) == K.ERR_UNSUPPORTED   # 1366 partitions x group 6 > 8192
+    # 1366 blocks of 8 partitions x group 6 > 8192 block weights
+    assert L.kvq_decode_merged(*mg(msl=(1365 * 8 + 1) * 512)) == K.ERR_UNSUPPORTED
     # kvq_decode_attn_unrotated: rotated 4-bit (or Q4_0) only, f32 / bf16 queries
     un = lambda c=d, qd=0, q=dummy: (ctypes.byref(c), q, qd, 2, 24, dummy, dummy, 100, 1000, None, 0, f, dummy, ws,
                                      None)

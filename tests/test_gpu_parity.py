@@ -742,6 +742,29 @@ def test_decode_merged_equals_decode_then_merge(K, fmt):
     assert_close(out[0], ref[0], what="merged seq 0 next to an invalid one")
 
 
+def test_decode_merged_blocks_batch_independent(K):
+    """The fused merge's two levels (blocks of 8 partitions): lengths of 2 and 3
+    blocks and one whose last block holds a single partition; each sequence's
+    outputs against the oracle, equal bit for bit to the same sequence decoded
+    alone (the tree depends only on partition indices), and run to run."""
+    lens = [9000, 4097, 12800, 700]
+    g, o, bt, q, ml = decode_case(K, lens, seed=91)
+    qr = K.rotate_query(q.to(DEV))
+    seq = torch.tensor(lens, dtype=torch.int32, device=DEV)
+    dbt = torch.from_numpy(bt).to(DEV)
+    ws = K.alloc_workspace(g, len(lens), 24, ml, device=DEV)
+    out = K.decode_merged(g, qr, seq, dbt, ml, 1 / 16, ws).clone()
+    again = K.decode_merged(g, qr, seq, dbt, ml, 1 / 16, ws)
+    assert torch.equal(out, again)
+    ref = O.decode(o, to_np_in(q), lens, bt, 1 / 16)
+    for b, L in enumerate(lens):
+        assert_close(out[b].cpu().numpy(), ref[b], what=f"merged blocks seq {b}")
+        ws1 = K.alloc_workspace(g, 1, 24, L, device=DEV)
+        solo = K.decode_merged(g, qr[b:b + 1].contiguous(), seq[b:b + 1].contiguous(),
+                               dbt[b:b + 1].contiguous(), L, 1 / 16, ws1)
+        assert torch.equal(solo[0], out[b]), f"seq {b}: batched != solo"
+
+
 def test_decode_bf16_cache(K):
     lens = [1500, 513, 20]
     g, o, bt, q, ml = decode_case(K, lens, fmt=K.FMT_BF16, seed=8)
