@@ -51,8 +51,8 @@ KERNELS_PER_LAYER = 3  # store + query rotation (one launch), split-T decode, me
 # beside them: once those sources change, the bench reports no traffic until
 # the capture is taken again.
 TRAFFIC_SOURCES = ("bit_quantized_kv_store_gb300/csrc/decode_q4.cu", "bit_quantized_kv_store_gb300/csrc/common.cuh")
-TRAFFIC_CAPTURE = {"sources_sha16": "69447ea51af25651",
-                   "bytes": {32768: 37867008 + 0, 262144: 302254592 + 10170880}}
+TRAFFIC_CAPTURE = {"sources_sha16": "ed752d883fb9de33",
+                   "bytes": {32768: 37863168 + 0, 262144: 302254848 + 10215936}}
 BYTES_PER_POS_LAYER = HK * 2 * (D // 2 + 2 * (D // 32))   # 1152
 
 
@@ -71,6 +71,15 @@ def traffic_bytes(context):
     if sources_sha16() != TRAFFIC_CAPTURE["sources_sha16"]:
         return None
     return TRAFFIC_CAPTURE["bytes"].get(context)
+
+
+def decode_kernel_name(torch, positions, sequences=1):
+    """The decode kernel the library runs for `sequences` sequences of `positions`
+    keys: the warp-specialised form when the grid (512-key partitions x KV heads x
+    sequences) fits one wave of two CTAs per SM, else the round kernel."""
+    ctas = -(-positions // 512) * HK * sequences
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    return "decode_q4_spec_kernel" if ctas <= 2 * sms else "decode_q4_round_kernel"
 
 
 def _r(x, digits=4):
@@ -913,7 +922,7 @@ def _row_q4_0(K, synth, torch, dev, peak, seed):
     out["q4_0_cache_32k"] = {"workload": "unrotated 4-bit cache (Q4_0), context 32768, 1 layer, same split-T + merge",
                              "decode_kernel_us": dms * 1e3, "cache_bytes": byts,
                              "achieved_GBs": byts / (dms * 1e-3) / 1e9, "frac_of_hbm_peak": byts / (dms * 1e-3) / 1e9 / peak,
-                             "store_4096_tokens_us": st_ms * 1e3, "kernel": "decode_q4_round_kernel"}
+                             "store_4096_tokens_us": st_ms * 1e3, "kernel": decode_kernel_name(torch, Tq)}
     del c, ws
     torch.cuda.empty_cache()
     return out
@@ -1104,6 +1113,7 @@ def main():
                 "unit": "us/layer-token", "steps": lsteps, "decode_kernel_us": _r(lavg * 1e3),
                 "achieved": _r(lach), "peak": peak, "frac": _r(lach / peak, 3),
                 "traffic": traffic_bytes(args.long_context), "bytes_per_launch": lbytes,
+                "kernel": decode_kernel_name(torch, WL.T),
                 "clocks": {"sm_mhz": c2["sm_mhz"], "sm_max_mhz": c2["sm_max_mhz"], "reasons": c2["reasons"],
                            "samples": c2["samples"]}}
         del WL
@@ -1141,10 +1151,11 @@ def main():
             "config": workload_config(args.context, world),
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                          "traffic": traffic_bytes(args.context), "bytes_per_launch": bytes_per_launch,
-                         "kernel": "decode_q4_round_kernel",
+                         "kernel": decode_kernel_name(torch, args.context + 1),
                          "decode_kernel_us": dec_avg_ms * 1e3, "peak_kind": peak_kind,
                          "long_context": None if long is None else
-                         {k: long[k] for k in ("context", "value", "decode_kernel_us", "achieved", "frac", "traffic")},
+                         {k: long[k] for k in ("context", "value", "decode_kernel_us", "achieved", "frac", "traffic",
+                                               "kernel")},
                          "other_kernels": None if rows is None else rows_summary(rows)},
             "e2e": {"value": c_us, "unit": "us/layer-token", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                     "path": "per call through the C ABI (48 calls per step)", "graph_replay_value": g_us},

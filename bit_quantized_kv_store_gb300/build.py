@@ -31,6 +31,12 @@ if SANITIZE:
 PER_FILE = {"store.cu": ["-fmad=false"], "tq4.cu": ["-fmad=false"]}
 
 
+def _tool_env():
+    """The environment for the compilers: without a preloaded sanitizer runtime
+    (a sanitized test process preloads one, and nvcc's own tools crash under it)."""
+    return {k: v for k, v in os.environ.items() if k != "LD_PRELOAD"}
+
+
 def _nvcc():
     for cand in (os.environ.get("NVCC"), "/usr/local/cuda/bin/nvcc", "nvcc"):
         if cand and (os.path.isabs(cand) and os.path.exists(cand) or not os.path.isabs(cand)):
@@ -54,7 +60,7 @@ def _compile(src, verbose_ptxas=False):
     cmd = [_nvcc(), *ARCH, *FLAGS, *PER_FILE.get(os.path.basename(src), []), "-c", src, "-o", obj + ".tmp"]
     if verbose_ptxas:
         cmd.insert(1, "-Xptxas=-v")
-    r = subprocess.run(cmd, capture_output=True, text=True)
+    r = subprocess.run(cmd, capture_output=True, text=True, env=_tool_env())
     if r.returncode != 0:
         raise RuntimeError(f"nvcc failed for {src}:\n{r.stdout}\n{r.stderr}")
     os.replace(obj + ".tmp", obj)
@@ -74,7 +80,7 @@ def build(verbose_ptxas=False) -> str:
     if not os.path.exists(LIB) or os.path.getmtime(LIB) < max(os.path.getmtime(o) for o in objs):
         tmp = LIB + f".tmp{os.getpid()}"
         cmd = [_nvcc(), *ARCH, "-shared", "-o", tmp, *objs, *(SAN_FLAGS if SANITIZE else [])]
-        r = subprocess.run(cmd, capture_output=True, text=True)
+        r = subprocess.run(cmd, capture_output=True, text=True, env=_tool_env())
         if r.returncode != 0:
             raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
         os.replace(tmp, LIB)

@@ -8,7 +8,9 @@
 // (and, for the TQ4 rows, its "Why rotated-int4" codebook).
 //
 // GB300 design.  One CTA of 4 warps per (partition of 512 keys, KV head,
-// sequence), 4 CTAs per SM (128 registers, 48 KB of shared memory).  The
+// sequence), 4 CTAs per SM (128 registers, 48 KB of shared memory); a grid that
+// fits in one wave of two CTAs per SM (a short context) runs a warp-specialised
+// form instead (below: 4 scoring and 4 P.V warps per CTA, same arithmetic).  The
 // partition is walked in rounds of 8 tiles of 16 keys (128 keys):
 //  * Fragments: a code row is 8 groups of 16 bytes, so the 8 rows x 16 bytes of
 //    an ldmatrix 8x8 matrix are one group of 8 keys: one ldmatrix.x4 gives a
@@ -33,6 +35,8 @@
 //    probabilities are multiplied by the V group scale in f16; V codes minus 8
 //    are exact in f16.  Each thread keeps 16 accumulators; a rescale costs 18
 //    FMULs.  Two named barriers per round.
+//  * The sums of the probabilities are kept per tile slot (tile u of every
+//    round) and added slot by slot at the end, in the same order in both forms.
 // Modes of the same kernel: the gather of selected rows (GATHER); decode
 // windows (WIN: up to 4 column tiles of (row, head) pairs of several rows of
 // one sequence per CTA, each row masked at its own end); TQ4 rows (TQ: the
@@ -121,6 +125,7 @@ __device__ __forceinline__ uint4 ldsm_x4_trans(uint32_t addr) {
                : "r"(addr));
   return v;
 }
+
 
 // Query fragments (B operand of the score MMA) and biases of one column tile:
 // column g of the tile faces the query row `qrow` (all 256 dims; a dead column
@@ -294,21 +299,22 @@ constexpr int kQ4MaxColTiles = 4;                 // a decode window stacks up t
 // accumulators per thread.
 __host__ __device__ constexpr int q4_min_blocks(int nt) { return nt == 1 ? 4 : nt == 2 ? 3 : 2; }
 
-// VR: rounds the V ring holds (1, or 2 where shared memory allows: round r + 1's
-// V is then copied while round r is computed, with no wait for the warps to
-// finish round r's P.V).
+// Warp w scores the round's tiles 2w, 2w + 1 and runs P.V for the value groups
+// 2w, 2w + 1.  VR: rounds the V ring holds (1, or 2 where shared memory allows:
+// round r + 1's V is then copied while round r is computed, with no wait for
+// the warps to finish round r's P.V).
 template <int NT, bool GATHER, int VR = 1>
 struct __align__(1024) Q4Smem {
   static constexpr int kTile = q4_tile_bytes<GATHER>();
-  uint8_t kc[kQ4Warps][kQ4TPW][kTile];  // K codes of each warp's tiles of the round (1024-aligned)
-  uint8_t vc[VR][kQ4RoundTiles][kTile];  // V codes of the round's tiles, by round mod VR
+  uint8_t kc[kQ4Warps][kQ4TPW][kTile];         // K codes of each warp's tiles of the round (1024-aligned)
+  uint8_t vc[VR][kQ4RoundTiles][kTile];        // V codes of the round's tiles, by round mod VR
   uint16_t ks[kQ4Warps][kQ4TPW][16 * 8];       // K scales
   uint16_t vs[VR][kQ4RoundTiles][16 * 8];      // V scales
   uint4 qf[NT][kQ4NG][2][32];                  // query fragments [column tile][group][hi, lo][lane]
   float4 qb[NT][kQ4NG][4];  // [column tile][group][t]: minus the code-offset bias of columns (2t, 2t+1, 2t, 2t+1)
   uint2 pb[kQ4RoundTiles][NT][32];  // [tile][column tile][lane]: P of the round as B fragments (keys 2t.., 2t+8..)
   float red[kQ4Warps][8 * NT];      // [warp][column]: maxima of each warp's tiles of the round
-  float zs[kQ4Warps][8 * NT];       // per-warp sums of the probabilities
+  float zs[kQ4RoundTiles][8 * NT];  // [tile slot][column]: sums of the probabilities of each slot's tiles
   uint64_t kbar[kQ4Warps];          // a warp's K tiles landed (kQ4TPW arrivals)
   uint64_t vfull[VR];               // the round's V tiles landed (kQ4RoundTiles arrivals)
   uint64_t vempty;                  // VR = 1: every warp is done with the round's V (kQ4Warps arrivals)
@@ -369,23 +375,23 @@ __device__ __forceinline__ bool q4_issue_plane(const DecodeArgs& a, int b, int k
   }
 }
 
-// The calling warp's kQ4TPW tiles of round `rd` of one plane into dc[u], ds[u]
+// The calling warp's TPW tiles of round `rd` of one plane into dc[u], ds[u]
 // (lane 0 issues; every lane takes part in the row shuffles).  A tile past the
 // partition still arrives on `bar`.  Returns true (lane 0) for a bad page/index.
-template <bool GATHER, bool TQ = false>
+template <bool GATHER, bool TQ = false, int TPW = 2>
 __device__ __forceinline__ bool q4_issue_own(const DecodeArgs& a, int b, int kvh, int k0, int k1, int rd, int warp,
                                              int lane, int32_t tile_row, const CUtensorMap* map, const void* codes,
                                              const void* scales, uint8_t (*dc)[q4_tile_bytes<GATHER>()],
                                              uint16_t (*ds)[16 * 8], uint64_t* bar) {
-  const int tile0 = kQ4RoundTiles * rd + kQ4TPW * warp;
-  int32_t rows[kQ4TPW];
+  const int tile0 = kQ4RoundTiles * rd + TPW * warp;
+  int32_t rows[TPW];
 #pragma unroll
-  for (int u = 0; u < kQ4TPW; ++u) rows[u] = __shfl_sync(0xffffffffu, tile_row, (tile0 + u) & 31);
+  for (int u = 0; u < TPW; ++u) rows[u] = __shfl_sync(0xffffffffu, tile_row, (tile0 + u) & 31);
   bool bad = false;
   if (lane == 0) {
     fence_proxy_async();  // the buffers were last read through the generic proxy
 #pragma unroll
-    for (int u = 0; u < kQ4TPW; ++u) {
+    for (int u = 0; u < TPW; ++u) {
       const int key0 = k0 + 16 * (tile0 + u);
       if (key0 >= k1) {
         mbar_arrive(bar);
@@ -494,6 +500,137 @@ __device__ __forceinline__ void q4_fold(const float* m, const float* z, const fl
   }
 }
 
+// Byte offset of this lane's ldmatrix row address for group-chunk G (+ lane >> 4)
+// inside a code tile (see the kernel's fragment layout).  Dense tiles carry the
+// 128-byte swizzle (chunk c of row r at c ^ (r & 7)); gather tiles are padded rows.
+template <bool GATHER>
+__device__ __forceinline__ uint32_t q4_chunk_off(int lrow, int lhi, int lane, int G) {
+  return GATHER ? lrow * kQ4GatherRow + ((G + lhi) << 4) : lrow * 128 + (((G + lhi) ^ (lane & 7)) << 4);
+}
+
+constexpr uint32_t kQfTileBytes = kQ4NG * 2 * 32 * 16;  // query fragments of one column tile
+constexpr uint32_t kQbTileBytes = kQ4NG * 4 * 16;       // query biases of one column tile
+
+// Scores of a warp's TPW tiles of a round (4-bit rows, not TQ4): S[u][nt][.] +=
+// the scaled dot products of keys g, g + 8 of tile u with columns 2t, 2t + 1 of
+// column tile nt (S enters as zeros).  The K codes of tile u sit at kc_base + u *
+// tile bytes, its scales at ks_base + u * 256; the query fragments and biases at
+// qf_addr / qb_addr (this lane's entries of column tile 0).
+template <bool GATHER, int NT, int TPW>
+__device__ __forceinline__ void q4_score_tiles(float (&S)[TPW][NT][4], uint32_t kc_base, uint32_t ks_base,
+                                               uint32_t qf_addr, uint32_t qb_addr, int lrow, int lhi, int lane) {
+  const int g = lane >> 2;
+#pragma unroll
+  for (int w = 0; w < kQ4NG / 2; ++w) {  // group pair (2w, 2w+1): one word of each fragment row
+    // kw[u]: codes 8t .. 8t+7 of group 2w (.x key g, .y key g+8) and of group 2w+1 (.z, .w)
+    uint4 kw[TPW];
+    float2 fsa[TPW], fsb[TPW];
+    const uint32_t okl = q4_chunk_off<GATHER>(lrow, lhi, lane, 2 * w);
+#pragma unroll
+    for (int u = 0; u < TPW; ++u) {
+      const uint32_t kb = kc_base + u * q4_tile_bytes<GATHER>(), sb = ks_base + u * kQ4ScaleBytes;
+      kw[u] = ldsm_x4(kb + okl);
+      fsa[u] = __half22float2(u32_as_h2(lds32a(sb + g * 16 + 4 * w)));  // K scales (2w, 2w+1) of row g
+      fsb[u] = __half22float2(u32_as_h2(lds32a(sb + (g + 8) * 16 + 4 * w)));
+    }
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const int G = 2 * w + e;
+      uint4 qh[NT], ql[NT];
+      float4 nb[NT];  // -bias of columns (2t, 2t+1, 2t, 2t+1)
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        qh[nt] = lds128a(qf_addr + nt * kQfTileBytes + G * 1024);
+        ql[nt] = lds128a(qf_addr + nt * kQfTileBytes + G * 1024 + 512);
+        nb[nt] = lds128f(qb_addr + nt * kQbTileBytes + G * 64);
+      }
+#pragma unroll
+      for (int u = 0; u < TPW; ++u) {
+        // codes 8t .. 8t+7 of keys g (xa1) and g+8 (xb1); the nibble pairs
+        // (0, 4), (1, 5) sit in bits 0-3 / 16-19 and 4-7 / 20-23; shifted by a
+        // byte (xa2, xb2), the pairs (2, 6), (3, 7)
+        const uint32_t xa1 = e ? kw[u].z : kw[u].x, xb1 = e ? kw[u].w : kw[u].y;
+        const uint32_t xa2 = xa1 >> 8, xb2 = xb1 >> 8;
+        const uint32_t a10 = nib_lo_pair_biased(xa1), a11 = nib_lo_pair_biased(xb1);
+        const uint32_t a12 = nib_hi_pair_biased(xa1), a13 = nib_hi_pair_biased(xb1);
+        const uint32_t a20 = nib_lo_pair_biased(xa2), a21 = nib_lo_pair_biased(xb2);
+        const uint32_t a22 = nib_hi_pair_biased(xa2), a23 = nib_hi_pair_biased(xb2);
+        const float sa = e ? fsa[u].y : fsa[u].x, sb = e ? fsb[u].y : fsb[u].x;
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+          float part[4];
+          mma_f16_c(part, a10, a11, a12, a13, qh[nt].x, qh[nt].y, nb[nt].x, nb[nt].y, nb[nt].z, nb[nt].w);
+          mma_f16(part, a20, a21, a22, a23, qh[nt].z, qh[nt].w);
+          mma_f16(part, a10, a11, a12, a13, ql[nt].x, ql[nt].y);
+          mma_f16(part, a20, a21, a22, a23, ql[nt].z, ql[nt].w);
+          S[u][nt][0] = fmaf(sa, part[0], S[u][nt][0]);
+          S[u][nt][1] = fmaf(sa, part[1], S[u][nt][1]);
+          S[u][nt][2] = fmaf(sb, part[2], S[u][nt][2]);
+          S[u][nt][3] = fmaf(sb, part[3], S[u][nt][3]);
+        }
+      }
+    }
+  }
+}
+
+// P.V of one round (4-bit rows, not TQ4): acc[e][.][nt] += the warp's value
+// groups 2w + e of the round's 8 tiles times their probabilities.  pb_addr:
+// this lane's B fragment of tile 0 (tiles 256 * NT bytes apart); vc_base,
+// vs_base: the round's V codes (tile j at + j * tile bytes) and the scale word of
+// the warp's groups; off_vl: the lane's ldmatrix offset of their chunks; kr0:
+// the round's first key, k1: the partition's end (kTail: zero the V scales of
+// keys at or past k1, so their stale codes add nothing).
+template <bool kTail, bool GATHER, int NT>
+__device__ __forceinline__ void q4_pv_tiles(float (&acc)[2][2][NT][4], uint32_t pb_addr, uint32_t vc_base,
+                                            uint32_t vs_base, uint32_t off_vl, int kr0, int k1, int lane) {
+  const int t = lane & 3;
+#pragma unroll
+  for (int j = 0; j < kQ4RoundTiles; ++j) {
+    uint2 pp[NT];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) pp[nt] = lds64a(pb_addr + (j * NT + nt) * 256);
+    const uint32_t cb = vc_base + j * q4_tile_bytes<GATHER>();
+    const uint32_t sb = vs_base + j * kQ4ScaleBytes;
+    // V scales of keys 2t, 2t+1, 2t+8, 2t+9 and V codes of the same rows:
+    // codes 4g .. 4g+3 of groups 2w, 2w+1 (ldmatrix, transposed).
+    uint32_t swa = lds32a(sb + (2 * t) * 16);
+    uint32_t swb = lds32a(sb + (2 * t + 1) * 16);
+    uint32_t swc = lds32a(sb + (2 * t + 8) * 16);
+    uint32_t swd = lds32a(sb + (2 * t + 9) * 16);
+    if constexpr (kTail) {
+      const int nvalid = k1 - (kr0 + 16 * j);
+      if (nvalid < 16) {  // CTA-uniform
+        if (2 * t >= nvalid) swa = 0u;
+        if (2 * t + 1 >= nvalid) swb = 0u;
+        if (2 * t + 8 >= nvalid) swc = 0u;
+        if (2 * t + 9 >= nvalid) swd = 0u;
+      }
+    }
+    // .x: keys 2t, 2t+1 of group 2w (bytes 2g, 2g+1 of each key, key 2t in the low
+    // half), .y: keys 2t+8, 2t+9; .z, .w: group 2w+1
+    const uint4 vw = ldsm_x4_trans(cb + off_vl);
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const uint32_t ssel = e ? 0x7632u : 0x5410u;
+      const uint32_t slo = prmt(swa, swb, ssel);
+      const uint32_t shi = prmt(swc, swd, ssel);
+      const uint32_t x01 = e ? vw.z : vw.x;  // codes 4g, 4g+1 in the low byte of each half
+      const uint32_t x23 = e ? vw.w : vw.y;
+      const uint32_t x01b = x01 >> 8, x23b = x23 >> 8;  // codes 4g+2, 4g+3
+      // d-tile (G,0): rows g <-> d = 32G+4g, g+8 <-> 32G+4g+2 ; (G,1): +1
+      const uint32_t l0 = nib_lo_pair(x01), l1 = nib_lo_pair(x01b), l2 = nib_lo_pair(x23), l3 = nib_lo_pair(x23b);
+      const uint32_t h0 = nib_hi_pair(x01), h1 = nib_hi_pair(x01b), h2 = nib_hi_pair(x23), h3 = nib_hi_pair(x23b);
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        const uint32_t b0 = h2_as_u32(__hmul2(u32_as_h2(pp[nt].x), u32_as_h2(slo)));
+        const uint32_t b1 = h2_as_u32(__hmul2(u32_as_h2(pp[nt].y), u32_as_h2(shi)));
+        mma_f16(acc[e][0][nt], l0, l1, l2, l3, b0, b1);
+        mma_f16(acc[e][1][nt], h0, h1, h2, h3, b0, b1);
+      }
+    }
+  }
+}
+
 // One CTA per (partition, KV head, column set).  NT column tiles of 8 columns
 // face the keys on the MMA's N side.  A plain decode (WIN = false, NT = 1) gives
 // the columns to the heads of one sequence's GQA group.  A decode window
@@ -502,9 +639,9 @@ __device__ __forceinline__ void q4_fold(const float* m, const float* z, const fl
 // codes are then converted once for all of them; each row keeps its own causal
 // end (its length), its own softmax state and its own partials.
 // MINB: resident CTAs per SM the registers are budgeted for (0: q4_min_blocks);
-// a grid that fits in two CTAs per SM takes MINB = 2 (up to 255 registers, more
-// score chains in flight per warp) and VR = 2 (a two-round V ring).  The
-// arithmetic is the same either way; only the copy schedule differs.
+// the fused merge on a grid that fits in two CTAs per SM takes MINB = 2 (up to
+// 255 registers) and VR = 2 (a two-round V ring).  The arithmetic is the same
+// either way; only the copy schedule differs.
 template <bool GATHER, int NT, bool WIN, bool TQ = false, bool LM = false, int MINB = 0, int VR = 1>
 __global__ void __launch_bounds__(kQ4Warps * 32, MINB ? MINB : q4_min_blocks(NT))
     decode_q4_round_kernel(const __grid_constant__ DecodeArgs a) {
@@ -613,8 +750,22 @@ __global__ void __launch_bounds__(kQ4Warps * 32, MINB ? MINB : q4_min_blocks(NT)
   __syncthreads();  // the mbarriers are initialised
 
   const kvq_cache& c = a.c;
-  bool poisoned = q4_issue_own<GATHER, TQ>(a, b, kvh, k0, k1, 0, warp, lane, tile_row, &a.tm_k, c.k, c.k_scale,
+  bool poisoned = q4_issue_own<GATHER, TQ, kQ4TPW>(a, b, kvh, k0, k1, 0, warp, lane, tile_row, &a.tm_k, c.k, c.k_scale,
                                        sm.kc[warp], sm.ks[warp], &sm.kbar[warp]);
+
+  // V of round 0 (and 1), after the query fragments: the in-kernel rotation uses
+  // vc[0][0..3] until the prologue's last barrier, and K(0), which the first
+  // round waits for, goes out alone first
+  auto issue_v01 = [&]() {
+    poisoned |= q4_issue_own<GATHER, TQ, kQ4TPW>(a, b, kvh, k0, k1, 0, warp, lane, tile_row, &a.tm_v, c.v, c.v_scale,
+                                                 &sm.vc[0][kQ4TPW * warp], &sm.vs[0][kQ4TPW * warp], &sm.vfull[0]);
+    if constexpr (VR == 2) {
+      if (nrounds > 1)
+        poisoned |= q4_issue_own<GATHER, TQ, kQ4TPW>(a, b, kvh, k0, k1, 1, warp, lane, tile_row, &a.tm_v, c.v,
+                                                     c.v_scale, &sm.vc[1][kQ4TPW * warp], &sm.vs[1][kQ4TPW * warp],
+                                                     &sm.vfull[1]);
+    }
+  };
 
   if constexpr (WIN) {
 #pragma unroll
@@ -633,17 +784,9 @@ __global__ void __launch_bounds__(kQ4Warps * 32, MINB ? MINB : q4_min_blocks(NT)
   } else {
     q4_query_prep<kQ4Warps>(a, b, kvh, warp, lane, reinterpret_cast<float*>(&sm.vc[0][0][0]), sm.qf[0], sm.qb[0]);
   }
-  // V of round 0: vc[0][0..3] held the rotated queries until the prologue's last barrier
-  poisoned |= q4_issue_own<GATHER, TQ>(a, b, kvh, k0, k1, 0, warp, lane, tile_row, &a.tm_v, c.v, c.v_scale,
-                                   &sm.vc[0][kQ4TPW * warp], &sm.vs[0][kQ4TPW * warp], &sm.vfull[0]);
-  if constexpr (VR == 2) {
-    if (nrounds > 1)
-      poisoned |= q4_issue_own<GATHER, TQ>(a, b, kvh, k0, k1, 1, warp, lane, tile_row, &a.tm_v, c.v, c.v_scale,
-                                       &sm.vc[1][kQ4TPW * warp], &sm.vs[1][kQ4TPW * warp], &sm.vfull[1]);
-  }
+  issue_v01();
   const uint32_t qf_addr = smem_u32(&sm.qf[0][0][0][lane]);
   const uint32_t qb_addr = smem_u32(&sm.qb[0][0][t]);
-  constexpr uint32_t kQfTile = sizeof(sm.qf[0]), kQbTile = sizeof(sm.qb[0]);
 
   // P.V accumulators of groups 2w + e, d-tiles (G, 0) and (G, 1), column tile nt
   float acc[2][2][NT][4];
@@ -656,12 +799,15 @@ __global__ void __launch_bounds__(kQ4Warps * 32, MINB ? MINB : q4_min_blocks(NT)
 #pragma unroll
         for (int i = 0; i < 4; ++i) acc[e][j][nt][i] = 0.f;
   // running max of columns 2t, 2t+1 of each column tile (base 2), equal in every
-  // warp, and this thread's partial sums over its own tiles' keys
-  float m0[NT], m1[NT], z0[NT], z1[NT];
+  // warp, and this thread's partial sums of the probabilities, one per tile slot
+  // u (the warp's tile u of every round), so that the sums are added in the same
+  // order whatever the number of warps
+  float m0[NT], m1[NT], z0[kQ4TPW][NT], z1[kQ4TPW][NT];
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) {
     m0[nt] = m1[nt] = kQ4NoMax;
-    z0[nt] = z1[nt] = 0.f;
+#pragma unroll
+    for (int u = 0; u < kQ4TPW; ++u) z0[u][nt] = z1[u][nt] = 0.f;
   }
   bool timed_out = false;
 
@@ -671,9 +817,7 @@ __global__ void __launch_bounds__(kQ4Warps * 32, MINB ? MINB : q4_min_blocks(NT)
   // (keys 0-7, G + 1), (keys 8-15, G + 1).  Dense tiles carry the 128-byte
   // swizzle (chunk c of row r at c ^ (r & 7)); gather tiles are padded rows.
   const int lrow = (lane & 7) + 8 * ((lane >> 3) & 1), lhi = lane >> 4;
-  auto chunk_off = [&](int G) -> uint32_t {  // G even
-    return GATHER ? lrow * kQ4GatherRow + ((G + lhi) << 4) : lrow * 128 + (((G + lhi) ^ (lane & 7)) << 4);
-  };
+  auto chunk_off = [&](int G) -> uint32_t { return q4_chunk_off<GATHER>(lrow, lhi, lane, G); };  // G even
   const uint32_t off_vl = chunk_off(2 * warp);  // V: groups 2w, 2w + 1 of this warp
   const uint32_t kc_base = smem_u32(&sm.kc[warp][0][0]);
   const uint32_t ks_base = smem_u32(&sm.ks[warp][0][0]);
@@ -733,57 +877,7 @@ __global__ void __launch_bounds__(kQ4Warps * 32, MINB ? MINB : q4_min_blocks(NT)
           S[u][0][3] *= sc;
         }
       } else {
-#pragma unroll
-      for (int w = 0; w < kQ4NG / 2; ++w) {  // group pair (2w, 2w+1): one word of each fragment row
-        // kw[u]: codes 8t .. 8t+7 of group 2w (.x key g, .y key g+8) and of group 2w+1 (.z, .w)
-        uint4 kw[kQ4TPW];
-        float2 fsa[kQ4TPW], fsb[kQ4TPW];
-        const uint32_t okl = chunk_off(2 * w);
-#pragma unroll
-        for (int u = 0; u < kQ4TPW; ++u) {
-          const uint32_t kb = kc_base + u * kTile, sb = ks_base + u * kQ4ScaleBytes;
-          kw[u] = ldsm_x4(kb + okl);
-          fsa[u] = __half22float2(u32_as_h2(lds32a(sb + g * 16 + 4 * w)));  // K scales (2w, 2w+1) of row g
-          fsb[u] = __half22float2(u32_as_h2(lds32a(sb + (g + 8) * 16 + 4 * w)));
-        }
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          const int G = 2 * w + e;
-          uint4 qh[NT], ql[NT];
-          float4 nb[NT];  // -bias of columns (2t, 2t+1, 2t, 2t+1)
-#pragma unroll
-          for (int nt = 0; nt < NT; ++nt) {
-            qh[nt] = lds128a(qf_addr + nt * kQfTile + G * 1024);
-            ql[nt] = lds128a(qf_addr + nt * kQfTile + G * 1024 + 512);
-            nb[nt] = lds128f(qb_addr + nt * kQbTile + G * 64);
-          }
-#pragma unroll
-          for (int u = 0; u < kQ4TPW; ++u) {
-            // codes 8t .. 8t+7 of keys g (xa1) and g+8 (xb1); the nibble pairs
-            // (0, 4), (1, 5) sit in bits 0-3 / 16-19 and 4-7 / 20-23; shifted by a
-            // byte (xa2, xb2), the pairs (2, 6), (3, 7)
-            const uint32_t xa1 = e ? kw[u].z : kw[u].x, xb1 = e ? kw[u].w : kw[u].y;
-            const uint32_t xa2 = xa1 >> 8, xb2 = xb1 >> 8;
-            const uint32_t a10 = nib_lo_pair_biased(xa1), a11 = nib_lo_pair_biased(xb1);
-            const uint32_t a12 = nib_hi_pair_biased(xa1), a13 = nib_hi_pair_biased(xb1);
-            const uint32_t a20 = nib_lo_pair_biased(xa2), a21 = nib_lo_pair_biased(xb2);
-            const uint32_t a22 = nib_hi_pair_biased(xa2), a23 = nib_hi_pair_biased(xb2);
-            const float sa = e ? fsa[u].y : fsa[u].x, sb = e ? fsb[u].y : fsb[u].x;
-#pragma unroll
-            for (int nt = 0; nt < NT; ++nt) {
-              float part[4];
-              mma_f16_c(part, a10, a11, a12, a13, qh[nt].x, qh[nt].y, nb[nt].x, nb[nt].y, nb[nt].z, nb[nt].w);
-              mma_f16(part, a20, a21, a22, a23, qh[nt].z, qh[nt].w);
-              mma_f16(part, a10, a11, a12, a13, ql[nt].x, ql[nt].y);
-              mma_f16(part, a20, a21, a22, a23, ql[nt].z, ql[nt].w);
-              S[u][nt][0] = fmaf(sa, part[0], S[u][nt][0]);
-              S[u][nt][1] = fmaf(sa, part[1], S[u][nt][1]);
-              S[u][nt][2] = fmaf(sb, part[2], S[u][nt][2]);
-              S[u][nt][3] = fmaf(sb, part[3], S[u][nt][3]);
-            }
-          }
-        }
-      }
+        q4_score_tiles<GATHER, NT, kQ4TPW>(S, kc_base, ks_base, qf_addr, qb_addr, lrow, lhi, lane);
       }
       // (Dead columns have a zero query: their scores are 0, finite, and never
       // leave the kernel, so they need no mask.)
@@ -812,8 +906,8 @@ __global__ void __launch_bounds__(kQ4Warps * 32, MINB ? MINB : q4_min_blocks(NT)
       // The K tiles are consumed: refill them with round r + 1.
       __syncwarp();
       if (r + 1 < nrounds)
-        poisoned |= q4_issue_own<GATHER, TQ>(a, b, kvh, k0, k1, r + 1, warp, lane, tile_row, &a.tm_k, c.k, c.k_scale,
-                                         sm.kc[warp], sm.ks[warp], &sm.kbar[warp]);
+        poisoned |= q4_issue_own<GATHER, TQ, kQ4TPW>(a, b, kvh, k0, k1, r + 1, warp, lane, tile_row, &a.tm_k, c.k,
+                                                     c.k_scale, sm.kc[warp], sm.ks[warp], &sm.kbar[warp]);
     }
 
     // ---------------- round maximum, shared through shared memory
@@ -838,7 +932,7 @@ __global__ void __launch_bounds__(kQ4Warps * 32, MINB ? MINB : q4_min_blocks(NT)
     if constexpr (VR == 2) {
       // slot (r + 1) % 2 held round r - 1's V, which every warp is done with: round r + 1's
       if (r >= 1 && r + 1 < nrounds)
-        poisoned |= q4_issue_own<GATHER, TQ>(a, b, kvh, k0, k1, r + 1, warp, lane, tile_row, &a.tm_v, c.v, c.v_scale,
+        poisoned |= q4_issue_own<GATHER, TQ, kQ4TPW>(a, b, kvh, k0, k1, r + 1, warp, lane, tile_row, &a.tm_v, c.v, c.v_scale,
                                          &sm.vc[(r + 1) & 1][kQ4TPW * warp], &sm.vs[(r + 1) & 1][kQ4TPW * warp],
                                          &sm.vfull[(r + 1) & 1]);
     }
@@ -865,8 +959,11 @@ __global__ void __launch_bounds__(kQ4Warps * 32, MINB ? MINB : q4_min_blocks(NT)
       c1[nt] = fast_exp2(m1[nt] - n1);
       m0[nt] = n0;
       m1[nt] = n1;
-      z0[nt] *= c0[nt];
-      z1[nt] *= c1[nt];
+#pragma unroll
+      for (int u = 0; u < kQ4TPW; ++u) {
+        z0[u][nt] *= c0[nt];
+        z1[u][nt] *= c1[nt];
+      }
       moved |= c0[nt] != 1.f || c1[nt] != 1.f;
     }
     if (r > 0 && __any_sync(0xffffffffu, moved)) {  // acc is still zero in round 0
@@ -889,8 +986,8 @@ __global__ void __launch_bounds__(kQ4Warps * 32, MINB ? MINB : q4_min_blocks(NT)
       for (int nt = 0; nt < NT; ++nt) {
         const float p0 = fast_exp2(S[u][nt][0] - m0[nt]), p1 = fast_exp2(S[u][nt][1] - m1[nt]);
         const float p2 = fast_exp2(S[u][nt][2] - m0[nt]), p3 = fast_exp2(S[u][nt][3] - m1[nt]);
-        z0[nt] += p0 + p2;
-        z1[nt] += p1 + p3;
+        z0[u][nt] += p0 + p2;
+        z1[u][nt] += p1 + p3;
         const uint32_t pb0 = movmatrix_trans(pack_half2(p0, p1));  // keys 2t, 2t+1 of column g
         const uint32_t pb1 = movmatrix_trans(pack_half2(p2, p3));  // keys 2t+8, 2t+9
         sm.pb[kQ4TPW * warp + u][nt][lane] = make_uint2(pb0, pb1);
@@ -902,7 +999,7 @@ __global__ void __launch_bounds__(kQ4Warps * 32, MINB ? MINB : q4_min_blocks(NT)
     const uint32_t vpar = VR == 2 ? ((r >> 1) & 1) : par;
     if (!timed_out && !__all_sync(0xffffffffu, mbar_wait_bounded(&sm.vfull[vslot], vpar))) timed_out = true;
     const uint32_t vc_base = smem_u32(&sm.vc[0][0][0]) + vslot * kVcSlot;
-    const uint32_t vs_base = smem_u32(&sm.vs[0][0][0]) + vslot * kVsSlot + 4 * warp;
+    const uint32_t vs_base = smem_u32(&sm.vs[0][0][0]) + vslot * kVsSlot + 4 * warp;  // groups 2w, 2w + 1
     const uint32_t vs_tq = smem_u32(&sm.vs[0][0][0]) + vslot * kVsSlot;  // TQ4: one fp16 scale per key
     const bool tail_round = k0 + kQ4RoundTiles * 16 * (r + 1) > k1;  // CTA-uniform
     // Every tile of the round is visited.  Keys past the end (the tail of the
@@ -944,51 +1041,8 @@ __global__ void __launch_bounds__(kQ4Warps * 32, MINB ? MINB : q4_min_blocks(NT)
           }
         }
       } else {
-#pragma unroll
-      for (int j = 0; j < kQ4RoundTiles; ++j) {
-        uint2 pp[NT];
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt) pp[nt] = lds64a(pb_addr + (j * NT + nt) * 256);
-        const uint32_t cb = vc_base + j * kTile;
-        const uint32_t sb = vs_base + j * kQ4ScaleBytes;
-        // V scales of keys 2t, 2t+1, 2t+8, 2t+9 and V codes of the same rows:
-        // codes 4g .. 4g+3 of groups 2w, 2w+1 (ldmatrix, transposed).
-        uint32_t swa = lds32a(sb + (2 * t) * 16);
-        uint32_t swb = lds32a(sb + (2 * t + 1) * 16);
-        uint32_t swc = lds32a(sb + (2 * t + 8) * 16);
-        uint32_t swd = lds32a(sb + (2 * t + 9) * 16);
-        if constexpr (kTail) {
-          const int nvalid = k1 - (k0 + 16 * (kQ4RoundTiles * r + j));
-          if (nvalid < 16) {  // CTA-uniform
-            if (2 * t >= nvalid) swa = 0u;
-            if (2 * t + 1 >= nvalid) swb = 0u;
-            if (2 * t + 8 >= nvalid) swc = 0u;
-            if (2 * t + 9 >= nvalid) swd = 0u;
-          }
-        }
-        // .x: keys 2t, 2t+1 of group 2w (bytes 2g, 2g+1 of each key, key 2t in the low
-        // half), .y: keys 2t+8, 2t+9; .z, .w: group 2w+1
-        const uint4 vw = ldsm_x4_trans(cb + off_vl);
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          const uint32_t ssel = e ? 0x7632u : 0x5410u;
-          const uint32_t slo = prmt(swa, swb, ssel);
-          const uint32_t shi = prmt(swc, swd, ssel);
-          const uint32_t x01 = e ? vw.z : vw.x;  // codes 4g, 4g+1 in the low byte of each half
-          const uint32_t x23 = e ? vw.w : vw.y;
-          const uint32_t x01b = x01 >> 8, x23b = x23 >> 8;  // codes 4g+2, 4g+3
-          // d-tile (G,0): rows g <-> d = 32G+4g, g+8 <-> 32G+4g+2 ; (G,1): +1
-          const uint32_t l0 = nib_lo_pair(x01), l1 = nib_lo_pair(x01b), l2 = nib_lo_pair(x23), l3 = nib_lo_pair(x23b);
-          const uint32_t h0 = nib_hi_pair(x01), h1 = nib_hi_pair(x01b), h2 = nib_hi_pair(x23), h3 = nib_hi_pair(x23b);
-#pragma unroll
-          for (int nt = 0; nt < NT; ++nt) {
-            const uint32_t b0 = h2_as_u32(__hmul2(u32_as_h2(pp[nt].x), u32_as_h2(slo)));
-            const uint32_t b1 = h2_as_u32(__hmul2(u32_as_h2(pp[nt].y), u32_as_h2(shi)));
-            mma_f16(acc[e][0][nt], l0, l1, l2, l3, b0, b1);
-            mma_f16(acc[e][1][nt], h0, h1, h2, h3, b0, b1);
-          }
-        }
-      }
+        q4_pv_tiles<kTail, GATHER, NT>(acc, pb_addr, vc_base, vs_base, off_vl, k0 + kQ4RoundTiles * 16 * r, k1,
+                                          lane);
       }
     };
     if (tail_round)
@@ -1003,7 +1057,7 @@ __global__ void __launch_bounds__(kQ4Warps * 32, MINB ? MINB : q4_min_blocks(NT)
       if (lane == 0) mbar_arrive(&sm.vempty);
       if (r + 1 < nrounds) {
         if (!timed_out && !__all_sync(0xffffffffu, mbar_wait_bounded(&sm.vempty, par))) timed_out = true;
-        poisoned |= q4_issue_own<GATHER, TQ>(a, b, kvh, k0, k1, r + 1, warp, lane, tile_row, &a.tm_v, c.v, c.v_scale,
+        poisoned |= q4_issue_own<GATHER, TQ, kQ4TPW>(a, b, kvh, k0, k1, r + 1, warp, lane, tile_row, &a.tm_v, c.v, c.v_scale,
                                          &sm.vc[0][kQ4TPW * warp], &sm.vs[0][kQ4TPW * warp], &sm.vfull[0]);
       }
     }
@@ -1011,16 +1065,19 @@ __global__ void __launch_bounds__(kQ4Warps * 32, MINB ? MINB : q4_min_blocks(NT)
   if (timed_out && lane == 0) set_status(a.status, KVQ_DEV_TIMEOUT);
   poisoned = __any_sync(0xffffffffu, poisoned || timed_out);
 
-  // ---------------- reduce z across the 8 key-row lanes; sum over warps
+  // ---------------- reduce z across the 8 key-row lanes; sum over the tile slots
 #pragma unroll
-  for (int nt = 0; nt < NT; ++nt) {
+  for (int u = 0; u < kQ4TPW; ++u)
 #pragma unroll
-    for (int o = 4; o < 32; o <<= 1) {
-      z0[nt] += __shfl_xor_sync(0xffffffffu, z0[nt], o);
-      z1[nt] += __shfl_xor_sync(0xffffffffu, z1[nt], o);
+    for (int nt = 0; nt < NT; ++nt) {
+#pragma unroll
+      for (int o = 4; o < 32; o <<= 1) {
+        z0[u][nt] += __shfl_xor_sync(0xffffffffu, z0[u][nt], o);
+        z1[u][nt] += __shfl_xor_sync(0xffffffffu, z1[u][nt], o);
+      }
+      if (g == 0)
+        *reinterpret_cast<float2*>(&sm.zs[kQ4TPW * warp + u][8 * nt + 2 * t]) = make_float2(z0[u][nt], z1[u][nt]);
     }
-    if (g == 0) *reinterpret_cast<float2*>(&sm.zs[warp][8 * nt + 2 * t]) = make_float2(z0[nt], z1[nt]);
-  }
   if (poisoned && lane == 0) atomicOr(&sm.poison, 1);
   __syncthreads();
   const bool bad = sm.poison != 0;
@@ -1062,9 +1119,9 @@ __global__ void __launch_bounds__(kQ4Warps * 32, MINB ? MINB : q4_min_blocks(NT)
     if (warp == 0 && g == 0) {
       float Z[2] = {0.f, 0.f};
 #pragma unroll
-      for (int w = 0; w < kQ4Warps; ++w) {
-        Z[0] += sm.zs[w][8 * nt + 2 * t];
-        Z[1] += sm.zs[w][8 * nt + 2 * t + 1];
+      for (int u = 0; u < kQ4RoundTiles; ++u) {
+        Z[0] += sm.zs[u][8 * nt + 2 * t];
+        Z[1] += sm.zs[u][8 * nt + 2 * t + 1];
       }
       const float M[2] = {m0[nt], m1[nt]};
 #pragma unroll
@@ -1124,6 +1181,292 @@ cudaError_t launch_round(const DecodeArgs& a, dim3 grid, cudaStream_t s) {
 
 }  // namespace q4r
 
+// ---------------------------------------------------------------- warp-specialised form
+// The same decode for grids that fit in one wave of two CTAs per SM (short
+// contexts, where one CTA per SM sub-partition pair leaves the schedulers idle):
+// 8 warps per CTA.  Warps 0-3 score and run the softmax as the round kernel's
+// warps do (tiles 2w, 2w + 1 of each round); warps 4-7 run P.V as the round
+// kernel's warps do (value groups 2w', 2w' + 1), one round behind.  The
+// probabilities and rescale factors of round r pass through slot r mod 2 of a
+// two-slot buffer, so the scores of round r + 1 overlap the P.V of round r.
+// Every value is computed by the same code as in the round kernel, so the
+// partials are the same bits.  Named barriers: 1 the scoring warps' maxima;
+// 2 + s slot s published (scoring warps arrive, P.V warps wait); 4 + s slot s
+// free again (the other way round); 6 the P.V warps are done with a round's V
+// tiles.  Every warp runs every round, so each barrier is always completed.
+namespace q4s {
+
+using namespace q4r;
+constexpr int kRoles = 4;  // warps per role
+constexpr int kBarMax = 1, kBarFull = 2, kBarEmpty = 4, kBarPv = 6;
+
+struct __align__(1024) SpecSmem {
+  uint8_t kc[2][kRoles][2][kQ4TileBytes];      // K ring: round mod 2, scoring warp, its 2 tiles
+  uint8_t vc[2][kQ4RoundTiles][kQ4TileBytes];  // V ring: round mod 2, tile
+  uint16_t ks[2][kRoles][2][16 * 8];
+  uint16_t vs[2][kQ4RoundTiles][16 * 8];
+  uint4 qf[1][kQ4NG][2][32];
+  float4 qb[1][kQ4NG][4];
+  uint2 pb[2][kQ4RoundTiles][1][32];  // P of round r in slot r mod 2 (B fragments)
+  float cf[2][8];                     // the round's rescale factor per column
+  float red[2][kRoles][8];            // maxima: round mod 2, scoring warp, column
+  float zs[kQ4RoundTiles][8];         // sums of the probabilities per tile slot
+  uint64_t kbar[2][kRoles];
+  uint64_t vfull[2];
+  int poison;
+};
+static_assert(sizeof(float) * 8 * kQ4D <= kQ4RoundTiles / 2 * kQ4TileBytes, "rotated queries fit vc[0][0..3]");
+
+__device__ __forceinline__ void nbar_sync(int id, int n) { asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory"); }
+__device__ __forceinline__ void nbar_arrive(int id, int n) {
+  asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+
+__global__ void __launch_bounds__(2 * kRoles * 32, 2) decode_q4_spec_kernel(const __grid_constant__ DecodeArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  SpecSmem& sm = *reinterpret_cast<SpecSmem*>(smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u));
+  const int p = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int g = lane >> 2, t = lane & 3;
+  const bool scorer = warp < kRoles;
+  const int rw = warp & (kRoles - 1);  // the warp's index within its role
+
+  // metadata before the wait on the previous kernel (as in the round kernel)
+  const int32_t T = a.seq_lens[b];
+  const bool bad_len = T < 0 || T > a.max_seq_len || (int64_t)T > (int64_t)a.max_pages * a.c.page_size;
+  const int nparts = bad_len ? 0 : (T + a.part - 1) / a.part;
+  const bool active = p < nparts;
+  const int k0 = p * a.part;
+  const int k1 = min(k0 + a.part, T);
+  const int ntiles = active ? (k1 - k0 + 15) / 16 : 0;
+  const int nrounds = (ntiles + kQ4RoundTiles - 1) / kQ4RoundTiles;
+  int32_t tile_row = -1;
+  bool bad_page = false;
+  if (lane < ntiles) {
+    const int key0 = k0 + 16 * lane;
+    const int32_t page = a.block_tables[(int64_t)b * a.bt_stride + key0 / a.c.page_size];
+    if (page < 0 || page >= a.c.num_pages)
+      bad_page = true;
+    else
+      tile_row = static_cast<int32_t>(((int64_t)page * a.c.num_kv_heads + kvh) * a.c.page_size + key0 % a.c.page_size);
+  }
+  if (active && threadIdx.x == 0) {
+    for (int k = 0; k < 2; ++k)
+      for (int w = 0; w < kRoles; ++w) mbar_init(&sm.kbar[k][w], 2);
+    for (int i = 0; i < 2; ++i) mbar_init(&sm.vfull[i], kQ4RoundTiles);
+    sm.poison = 0;
+    fence_barrier_init();
+  }
+
+  pdl_wait();
+  if (bad_len) {
+    if (threadIdx.x == 0 && p == 0 && kvh == 0) set_status(a.status, KVQ_DEV_BAD_LENGTH);
+    return;  // the merge writes NaN for this sequence
+  }
+  if (!active) return;
+  if (bad_page && warp == 0) set_status(a.status, KVQ_DEV_BAD_PAGE);
+  __syncthreads();  // the mbarriers are initialised
+
+  const kvq_cache& c = a.c;
+  bool poisoned = false;
+  if (scorer) {
+    poisoned = q4r::q4_issue_own<false, false, 2>(a, b, kvh, k0, k1, 0, rw, lane, tile_row, &a.tm_k, c.k, c.k_scale,
+                                                  sm.kc[0][rw], sm.ks[0][rw], &sm.kbar[0][rw]);
+    if (nrounds > 1)
+      poisoned |= q4r::q4_issue_own<false, false, 2>(a, b, kvh, k0, k1, 1, rw, lane, tile_row, &a.tm_k, c.k,
+                                                     c.k_scale, sm.kc[1][rw], sm.ks[1][rw], &sm.kbar[1][rw]);
+  }
+  // V of rounds 0 and 1, after the query fragments: the in-kernel rotation uses
+  // vc[0][0..3] until its last barrier, and K(0), which the first round waits
+  // for, goes out alone first
+  auto issue_v01 = [&]() {
+    poisoned = q4r::q4_issue_own<false, false, 2>(a, b, kvh, k0, k1, 0, rw, lane, tile_row, &a.tm_v, c.v, c.v_scale,
+                                                  &sm.vc[0][2 * rw], &sm.vs[0][2 * rw], &sm.vfull[0]);
+    if (nrounds > 1)
+      poisoned |= q4r::q4_issue_own<false, false, 2>(a, b, kvh, k0, k1, 1, rw, lane, tile_row, &a.tm_v, c.v,
+                                                     c.v_scale, &sm.vc[1][2 * rw], &sm.vs[1][2 * rw], &sm.vfull[1]);
+  };
+  q4_query_prep<2 * kRoles>(a, b, kvh, warp, lane, reinterpret_cast<float*>(&sm.vc[0][0][0]), sm.qf[0], sm.qb[0]);
+  if (!scorer) issue_v01();
+  const int lrow = (lane & 7) + 8 * ((lane >> 3) & 1), lhi = lane >> 4;
+  bool timed_out = false;
+  float m0 = kQ4NoMax, m1 = kQ4NoMax;
+  float z0[2][1] = {{0.f}, {0.f}}, z1[2][1] = {{0.f}, {0.f}};
+  float acc[2][2][1][4];
+#pragma unroll
+  for (int e = 0; e < 2; ++e)
+#pragma unroll
+    for (int j = 0; j < 2; ++j)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) acc[e][j][0][i] = 0.f;
+
+  if (scorer) {
+    // ---------------- scores and softmax of tiles 2 rw, 2 rw + 1 of every round
+    const uint32_t qf_addr = smem_u32(&sm.qf[0][0][0][lane]);
+    const uint32_t qb_addr = smem_u32(&sm.qb[0][0][t]);
+    for (int r = 0; r < nrounds; ++r) {
+      const int s = r & 1;
+      const uint32_t kc_base = smem_u32(&sm.kc[s][rw][0][0]), ks_base = smem_u32(&sm.ks[s][rw][0][0]);
+      const int tile0 = kQ4RoundTiles * r + 2 * rw;
+      float S[2][1][4];
+#pragma unroll
+      for (int u = 0; u < 2; ++u) S[u][0][0] = S[u][0][1] = S[u][0][2] = S[u][0][3] = -INFINITY;
+      if (k0 + 16 * tile0 < k1) {  // warp-uniform
+        if (!timed_out && !__all_sync(0xffffffffu, mbar_wait_bounded(&sm.kbar[s][rw], (r >> 1) & 1))) timed_out = true;
+#pragma unroll
+        for (int u = 0; u < 2; ++u) S[u][0][0] = S[u][0][1] = S[u][0][2] = S[u][0][3] = 0.f;
+        q4_score_tiles<false, 1, 2>(S, kc_base, ks_base, qf_addr, qb_addr, lrow, lhi, lane);
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          const int nvalid = k1 - (k0 + 16 * (tile0 + u));
+          if (nvalid < 16) {  // warp-uniform
+            if (g >= nvalid) S[u][0][0] = S[u][0][1] = -INFINITY;
+            if (g + 8 >= nvalid) S[u][0][2] = S[u][0][3] = -INFINITY;
+          }
+        }
+        __syncwarp();  // the K tiles are consumed: refill the slot with round r + 2
+        if (r + 2 < nrounds)
+          poisoned |= q4r::q4_issue_own<false, false, 2>(a, b, kvh, k0, k1, r + 2, rw, lane, tile_row, &a.tm_k, c.k,
+                                                         c.k_scale, sm.kc[s][rw], sm.ks[s][rw], &sm.kbar[s][rw]);
+      }
+      // round maximum over the scoring warps
+      float t0 = fmaxf(S[0][0][0], S[0][0][2]), t1 = fmaxf(S[0][0][1], S[0][0][3]);
+      t0 = fmaxf(t0, fmaxf(S[1][0][0], S[1][0][2]));
+      t1 = fmaxf(t1, fmaxf(S[1][0][1], S[1][0][3]));
+#pragma unroll
+      for (int o = 4; o < 32; o <<= 1) {
+        t0 = fmaxf(t0, __shfl_xor_sync(0xffffffffu, t0, o));
+        t1 = fmaxf(t1, __shfl_xor_sync(0xffffffffu, t1, o));
+      }
+      if (g == 0) *reinterpret_cast<float2*>(&sm.red[s][rw][2 * t]) = make_float2(t0, t1);
+      nbar_sync(kBarMax, kRoles * 32);
+#pragma unroll
+      for (int w = 0; w < kRoles; ++w) {
+        const float2 mx = *reinterpret_cast<const float2*>(&sm.red[s][w][2 * t]);
+        t0 = fmaxf(t0, mx.x);
+        t1 = fmaxf(t1, mx.y);
+      }
+      // online softmax (base 2), as in the round kernel
+      const float n0 = fmaxf(m0, t0), n1 = fmaxf(m1, t1);
+      const float c0 = fast_exp2(m0 - n0), c1 = fast_exp2(m1 - n1);
+      m0 = n0;
+      m1 = n1;
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        z0[u][0] *= c0;
+        z1[u][0] *= c1;
+      }
+      if (r >= 2) nbar_sync(kBarEmpty + s, 2 * kRoles * 32);  // the P.V warps are done with slot s
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        const float p0 = fast_exp2(S[u][0][0] - m0), p1 = fast_exp2(S[u][0][1] - m1);
+        const float p2 = fast_exp2(S[u][0][2] - m0), p3 = fast_exp2(S[u][0][3] - m1);
+        z0[u][0] += p0 + p2;
+        z1[u][0] += p1 + p3;
+        const uint32_t pb0 = movmatrix_trans(pack_half2(p0, p1));  // keys 2t, 2t+1 of column g
+        const uint32_t pb1 = movmatrix_trans(pack_half2(p2, p3));  // keys 2t+8, 2t+9
+        sm.pb[s][2 * rw + u][0][lane] = make_uint2(pb0, pb1);
+      }
+      if (rw == 0 && g == 0) *reinterpret_cast<float2*>(&sm.cf[s][2 * t]) = make_float2(c0, c1);
+      nbar_arrive(kBarFull + s, 2 * kRoles * 32);
+    }
+  } else {
+    // ---------------- P.V of value groups 2 rw, 2 rw + 1, one round behind the scores
+    const uint32_t off_vl = q4_chunk_off<false>(lrow, lhi, lane, 2 * rw);
+    for (int r = 0; r < nrounds; ++r) {
+      const int s = r & 1;
+      nbar_sync(kBarFull + s, 2 * kRoles * 32);
+      const float2 cc = *reinterpret_cast<const float2*>(&sm.cf[s][2 * t]);
+      const bool moved = cc.x != 1.f || cc.y != 1.f;
+      if (r > 0 && __any_sync(0xffffffffu, moved)) {  // acc is still zero in round 0
+#pragma unroll
+        for (int e = 0; e < 2; ++e)
+#pragma unroll
+          for (int j = 0; j < 2; ++j) {
+            acc[e][j][0][0] *= cc.x;
+            acc[e][j][0][1] *= cc.y;
+            acc[e][j][0][2] *= cc.x;
+            acc[e][j][0][3] *= cc.y;
+          }
+      }
+      if (!timed_out && !__all_sync(0xffffffffu, mbar_wait_bounded(&sm.vfull[s], (r >> 1) & 1))) timed_out = true;
+      const uint32_t vc_base = smem_u32(&sm.vc[s][0][0]);
+      const uint32_t vs_base = smem_u32(&sm.vs[s][0][0]) + 4 * rw;
+      const uint32_t pb_addr = smem_u32(&sm.pb[s][0][0][lane]);
+      if (k0 + kQ4RoundTiles * 16 * (r + 1) > k1)  // CTA-uniform: the tail round
+        q4_pv_tiles<true, false, 1>(acc, pb_addr, vc_base, vs_base, off_vl, k0 + kQ4RoundTiles * 16 * r, k1, lane);
+      else
+        q4_pv_tiles<false, false, 1>(acc, pb_addr, vc_base, vs_base, off_vl, k0 + kQ4RoundTiles * 16 * r, k1, lane);
+      if (r + 2 < nrounds) nbar_arrive(kBarEmpty + s, 2 * kRoles * 32);  // slot s may take round r + 2
+      nbar_sync(kBarPv, kRoles * 32);  // every P.V warp is done with the round's V tiles
+      if (r + 2 < nrounds)
+        poisoned |= q4r::q4_issue_own<false, false, 2>(a, b, kvh, k0, k1, r + 2, rw, lane, tile_row, &a.tm_v, c.v,
+                                                       c.v_scale, &sm.vc[s][2 * rw], &sm.vs[s][2 * rw], &sm.vfull[s]);
+    }
+  }
+  if (timed_out && lane == 0) set_status(a.status, KVQ_DEV_TIMEOUT);
+  poisoned = __any_sync(0xffffffffu, poisoned || timed_out);
+  if (scorer) {  // z: across the 8 key-row lanes, then per tile slot
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+#pragma unroll
+      for (int o = 4; o < 32; o <<= 1) {
+        z0[u][0] += __shfl_xor_sync(0xffffffffu, z0[u][0], o);
+        z1[u][0] += __shfl_xor_sync(0xffffffffu, z1[u][0], o);
+      }
+      if (g == 0) *reinterpret_cast<float2*>(&sm.zs[2 * rw + u][2 * t]) = make_float2(z0[u][0], z1[u][0]);
+    }
+  }
+  if (poisoned && lane == 0) atomicOr(&sm.poison, 1);
+  __syncthreads();
+  const bool bad = sm.poison != 0;
+  int64_t pi[2];
+  bool live[2];
+#pragma unroll
+  for (int cc = 0; cc < 2; ++cc) {
+    const int col = 2 * t + cc;
+    live[cc] = col < a.group;
+    pi[cc] = ((int64_t)b * a.Hq + kvh * a.group + col) * a.P + p;
+  }
+  if (!scorer) {
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const int d = 32 * (2 * rw + e) + 4 * g;
+      float4 o0 = make_float4(acc[e][0][0][0], acc[e][1][0][0], acc[e][0][0][2], acc[e][1][0][2]);
+      float4 o1 = make_float4(acc[e][0][0][1], acc[e][1][0][1], acc[e][0][0][3], acc[e][1][0][3]);
+      if (bad) o0 = o1 = make_float4(NAN, NAN, NAN, NAN);
+      if (live[0]) *reinterpret_cast<float4*>(a.ws_acc + pi[0] * kQ4D + d) = o0;
+      if (live[1]) *reinterpret_cast<float4*>(a.ws_acc + pi[1] * kQ4D + d) = o1;
+    }
+  } else if (warp == 0 && g == 0) {
+    float Z[2] = {0.f, 0.f};
+#pragma unroll
+    for (int u = 0; u < kQ4RoundTiles; ++u) {
+      Z[0] += sm.zs[u][2 * t];
+      Z[1] += sm.zs[u][2 * t + 1];
+    }
+    const float M[2] = {m0, m1};
+#pragma unroll
+    for (int cc = 0; cc < 2; ++cc)
+      if (live[cc]) {
+        a.ws_m[pi[cc]] = bad ? NAN : M[cc];
+        a.ws_z[pi[cc]] = bad ? NAN : Z[cc];
+      }
+  }
+  pdl_trigger();  // after this CTA's last write
+}
+
+cudaError_t launch_spec(const DecodeArgs& a, dim3 grid, cudaStream_t s) {
+  const size_t smem = sizeof(SpecSmem) + 1024;  // + slack for the 1024-byte alignment
+  cudaError_t e = cudaFuncSetAttribute(decode_q4_spec_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  e = launch_pdl(decode_q4_spec_kernel, grid, dim3(2 * kRoles * 32), smem, s, a);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
+}  // namespace q4s
+
 // Streaming multiprocessors of the current device.
 static int sm_count() {
   int dev = 0, n = 0;
@@ -1144,7 +1487,7 @@ cudaError_t launch_decode_q4(const DecodeArgs& a, int B, cudaStream_t s) {
                    : small ? launch_round<false, 1, false, false, true, 2, 2>(a, grid, s)
                            : launch_round<false, 1, false, false, true>(a, grid, s);
     if (a.sel) return launch_round<true, 1, false>(a, grid, s);
-    if (small) return launch_round<false, 1, false, false, false, 2, 2>(a, grid, s);
+    if (small) return q4s::launch_spec(a, grid, s);
     return launch_round<false, 1, false>(a, grid, s);
   }
   if (a.tq) return cudaErrorInvalidValue;

@@ -61,6 +61,129 @@ __device__ __forceinline__ uint32_t q4_code_exact(float y, float s) {
   return static_cast<uint32_t>(static_cast<int>(q) + 8);
 }
 
+// ---------------------------------------------------------------- packed fp32 pairs
+// f32x2 instructions: two IEEE fp32 operations (round to nearest even), one per
+// half, in one instruction -- the same results as the scalar forms.
+__device__ __forceinline__ uint64_t pk2(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void upk2(uint64_t v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ uint64_t sub2(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ uint64_t mul2(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+  return r;
+}
+
+// One rotated group in registers: x[32] (the raw values) -> the 32 codes in
+// word[0..3] (value 8q + i in nibble i of word q) and the fp16 scale; x ends as
+// the rotated values y.  The butterfly runs on the pairs (x[i], x[i + 16]):
+// stages 1, 2, 4, 8 pair registers i and i + h half by half, stage 16 adds the
+// two halves of a register -- the same operations on the same operands as the
+// scalar butterfly.  Codes: with t = fl(y * rcp(s) + 8) clamped to <= 15 (a t
+// above 15 gives code 15 either way), u = fl(t + 1.5 * 2^23) holds rint_even(t)
+// in its low mantissa bits (|t| < 2^22), and u - 1.5 * 2^23 - t is t's distance
+// to it; the group takes these codes when every distance passes the screen
+// (q4_code_screened's bound).  For an fp16-normal, unsaturated scale, t >= -1/2
+// (|y| <= amax and s >= (amax / 8)(1 - 2^-11)), so no lower clamp is needed.
+// Any other group (a distance near 1/2, a NaN or saturated or subnormal scale)
+// takes the per-value screen and the IEEE division, as the other store forms do.
+__device__ __forceinline__ void q4_group_rotated(float (&x)[32], uint32_t (&word)[4], __half& s16_out) {
+  uint64_t P[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) P[i] = pk2(x[i], x[i + 16]);
+#pragma unroll
+  for (int h = 1; h < 16; h <<= 1)
+#pragma unroll
+    for (int i = 0; i < 16; ++i)
+      if ((i & h) == 0) {
+        const uint64_t a = P[i], b = P[i + h];
+        P[i] = add2(a, b);
+        P[i + h] = sub2(a, b);
+      }
+  const uint64_t C2 = pk2(kHadamardScale, kHadamardScale);
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    float a, b;
+    upk2(P[i], a, b);
+    P[i] = mul2(pk2(__fadd_rn(a, b), __fsub_rn(a, b)), C2);
+    upk2(P[i], x[i], x[i + 16]);
+  }
+  // the group maximum by a tree (max is exact, so any order gives the same value)
+  float m[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) m[i] = fmaxf(fabsf(x[i]), fabsf(x[i + 16]));
+#pragma unroll
+  for (int w = 8; w > 0; w >>= 1)
+#pragma unroll
+    for (int i = 0; i < w; ++i) m[i] = fmaxf(m[i], m[i + w]);
+  const float s32 = __fmul_rn(m[0], 0.125f);  // = amax / 8 correctly rounded (a power of two)
+  __half s16 = __float2half_rn(s32);
+  if (__hisinf(s16)) s16 = __ushort_as_half(0x7BFFu);  // saturate to 65504
+  s16_out = s16;
+  const float s = __half2float(s16);
+  word[0] = word[1] = word[2] = word[3] = 0x88888888u;  // scale 0: every code 8
+  if (s == 0.0f) return;
+  const float r = rcp_approx(s);
+  bool fast = s >= 6.103515625e-05f && s < 65504.0f;  // fp16-normal, unsaturated (false for NaN)
+  if (fast) {
+    const uint64_t R2 = pk2(r, r), E2 = pk2(8.0f, 8.0f), M2 = pk2(12582912.0f, 12582912.0f);
+    float dmax = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      float ta, tb;
+      upk2(fma2(P[i], R2, E2), ta, tb);
+      const uint64_t t2 = pk2(fminf(ta, 15.0f), fminf(tb, 15.0f));
+      const uint64_t u2 = add2(t2, M2);
+      float da, db, ua, ub;
+      upk2(sub2(t2, sub2(u2, M2)), da, db);
+      dmax = fmaxf(dmax, fmaxf(fabsf(da), fabsf(db)));
+      upk2(u2, ua, ub);
+      word[i >> 3] = put_nibble(word[i >> 3], __float_as_uint(ua), i & 7);
+      word[2 + (i >> 3)] = put_nibble(word[2 + (i >> 3)], __float_as_uint(ub), i & 7);
+    }
+    fast = dmax < kQ4Screen;
+  }
+  if (fast) return;
+  word[0] = word[1] = word[2] = word[3] = 0x88888888u;
+  uint32_t undecided = 0;  // bit i: value i needs the IEEE division
+#pragma unroll
+  for (int q = 0; q < 4; ++q)
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      uint32_t code;
+      if (!q4_code_screened(x[8 * q + i], r, code)) undecided |= 1u << (8 * q + i);
+      word[q] = put_nibble(word[q], code, i);
+    }
+  while (undecided) {
+    const int i = __ffs(undecided) - 1;
+    undecided &= undecided - 1;
+    float y = x[0];
+#pragma unroll
+    for (int j = 1; j < 32; ++j)
+      if (j == i) y = x[j];
+    word[i >> 3] = put_nibble(word[i >> 3], q4_code_exact(y, s), i & 7);
+  }
+}
+
 // Bulk form (a prompt chunk): one lane per (row, group of 32 values), so the
 // whole 32-point butterfly (stages h = 1, 2, 4, 8, 16, (a, b) -> (a + b, a - b),
 // the same operations on the same operands as the warp-shuffle form) and the
@@ -120,19 +243,21 @@ __global__ void __launch_bounds__(kLaneBlock, 5) store_q4_lane_kernel(kvq_cache 
     return ((int64_t)tok * Hk + head) * D + 32 * static_cast<int>(gg % NG);
   };
   uint32_t gg = blockIdx.x * blockDim.x + threadIdx.x;
-  uint32_t nxt[BF ? 16 : 32];
+  uint32_t nxt[BF ? 16 : 32];  // the next group's raw values
+  int32_t nslot = -1;          // and its token's slot
   if (gg < total) {
     uint32_t tok, head;
     bool is_v;
     const int64_t e0 = locate(gg, tok, head, is_v);
     load_group<VEC, BF>(is_v ? v : k, dtype, e0, nxt);
+    nslot = slots[tok];
   }
   for (; gg < total; gg += stride) {
     uint32_t tok, head;
     bool is_v;
     locate(gg, tok, head, is_v);
     const int G = static_cast<int>(gg % NG);
-    const int32_t slot = slots[tok];
+    const int32_t slot = nslot;
     float x[32];
     if constexpr (BF) {
 #pragma unroll
@@ -149,25 +274,14 @@ __global__ void __launch_bounds__(kLaneBlock, 5) store_q4_lane_kernel(kvq_cache 
       bool v2;
       const int64_t e2 = locate(gg + stride, t2, h2, v2);
       load_group<VEC, BF>(v2 ? v : k, dtype, e2, nxt);
+      nslot = slots[t2];
     }
-    if (slot < 0) continue;
-    if ((int64_t)slot >= (int64_t)c.num_pages * c.page_size) {
-      if (G == 0) set_status(status, KVQ_DEV_BAD_SLOT);
-      continue;
-    }
-    if (ROT) {
-#pragma unroll
-      for (int h = 1; h < 32; h <<= 1)
-#pragma unroll
-        for (int i = 0; i < 32; ++i)
-          if ((i & h) == 0) {
-            const float a = x[i], b = x[i + h];
-            x[i] = __fadd_rn(a, b);
-            x[i + h] = __fsub_rn(a, b);
-          }
-#pragma unroll
-      for (int i = 0; i < 32; ++i) x[i] = __fmul_rn(x[i], kHadamardScale);
-    }
+    // the codes first: only the stores depend on the slot
+    uint32_t word[4];
+    __half s16;
+    if constexpr (ROT) {
+      q4_group_rotated(x, word, s16);
+    } else {
     // the group maximum by a tree (max is exact, so any order gives the same value)
     float m[16];
 #pragma unroll
@@ -178,10 +292,10 @@ __global__ void __launch_bounds__(kLaneBlock, 5) store_q4_lane_kernel(kvq_cache 
       for (int i = 0; i < w; ++i) m[i] = fmaxf(m[i], m[i + w]);
     const float amax = m[0];
     const float s32 = __fmul_rn(amax, 0.125f);  // = amax / 8 correctly rounded (a power of two)
-    __half s16 = __float2half_rn(s32);
+    s16 = __float2half_rn(s32);
     if (__hisinf(s16)) s16 = __ushort_as_half(0x7BFFu);  // saturate to 65504
     const float s = __half2float(s16);
-    uint32_t word[4] = {0x88888888u, 0x88888888u, 0x88888888u, 0x88888888u};  // scale 0: every code 8
+    word[0] = word[1] = word[2] = word[3] = 0x88888888u;  // scale 0: every code 8
     if (s != 0.0f) {
       const float r = rcp_approx(s);
       uint32_t undecided = 0;  // bit i: value i needs the IEEE division
@@ -206,6 +320,12 @@ __global__ void __launch_bounds__(kLaneBlock, 5) store_q4_lane_kernel(kvq_cache 
           if (j == i) y = x[j];
         word[i >> 3] = put_nibble(word[i >> 3], q4_code_exact(y, s), i & 7);
       }
+    }
+    }
+    if (slot < 0) continue;
+    if ((int64_t)slot >= (int64_t)c.num_pages * c.page_size) {
+      if (G == 0) set_status(status, KVQ_DEV_BAD_SLOT);
+      continue;
     }
     const uint32_t page = fast_div(static_cast<uint32_t>(slot), ps);
     const int64_t r = ((int64_t)page * Hk + head) * c.page_size + (static_cast<uint32_t>(slot) - page * ps.d);

@@ -42,8 +42,10 @@ def build(force: bool = False) -> str:
     if force or not os.path.exists(_LIB_PATH) or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC):
         tmp = _LIB_PATH + f".tmp{os.getpid()}"
         opt = _SAN_FLAGS if _SANITIZE else ["-O2"]
+        # (the compiler runs without a sanitizer runtime a test process may preload)
+        env = {k: v for k, v in os.environ.items() if k != "LD_PRELOAD"}
         subprocess.check_call(["gcc", *opt, "-ffp-contract=off", "-fPIC", "-shared", "-std=c11",
-                               "-o", tmp, _SRC, "-lm"])
+                               "-o", tmp, _SRC, "-lm"], env=env)
         os.replace(tmp, _LIB_PATH)
     return _LIB_PATH
 

@@ -462,6 +462,23 @@ def test_decode_concurrent_equals_solo_and_deterministic(K, lens):
         assert np.array_equal(solo[0], out[b])
 
 
+@pytest.mark.parametrize("L", [32769, 16383 + 200, 1337])
+def test_decode_warp_specialised_equals_round_kernel(K, L):
+    """A grid that fits in one wave of two CTAs per SM (the sequence alone) runs
+    the warp-specialised kernel; next to a 40000-key sequence (79 partitions x 4
+    KV heads x 2 sequences, over two CTAs per SM) it runs the round kernel.  The
+    two give the same bits.  The last partition holds 1, 199 and 313 keys (tail
+    rounds of 1, 5 and 4 tiles)."""
+    lens = [L, 40000]
+    g, o, bt, q, ml = decode_case(K, lens, seed=77)
+    out, _ = run_decode(K, g, bt, q, lens, ml, 1 / 16)
+    solo, _ = run_decode(K, g, bt[:1], q[:1], [L], L, 1 / 16)
+    assert np.array_equal(solo[0], out[0])
+    if L < 2000:
+        ref = O.decode(o, to_np_in(q[:1]), [L], bt[:1], 1 / 16)
+        assert_close(solo[0], ref[0], what=f"warp-specialised L={L}")
+
+
 @pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
 @pytest.mark.parametrize("Hk,Hq", [(4, 24), (2, 4), (3, 21)])
 def test_decode_unrotated_query_equals_rotate_then_decode(K, dtype, Hk, Hq):
