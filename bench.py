@@ -302,6 +302,12 @@ class Workload:
         self.out = torch.empty((LAYERS, 1, HQ, D), dtype=torch.float32, device=dev)
         self.ws = K.alloc_workspace(self.caches[0], 1, HQ, self.T, device=dev)
         self.sm_scale = 1.0 / math.sqrt(D)
+        # per (input set, layer): the views a step hands to the API, made once (a
+        # serving loop keeps its per-layer buffers; slicing them again on every
+        # call would add torch's view overhead to each call)
+        self.views = [[(self.new_k[i][layer], self.new_v[i][layer], self.q[i][layer]) for layer in range(LAYERS)]
+                      for i in range(n_inputs)]
+        self.out_views = [self.out[layer] for layer in range(LAYERS)]
         torch.cuda.synchronize()
 
     def decode_only(self):
@@ -309,23 +315,22 @@ class Workload:
         for layer in range(LAYERS):
             self.K.decode_attn(self.caches[layer], self.qrot, self.seq, self.bt, self.T, self.sm_scale, self.ws)
 
-    def step(self, i, ev=None, new_k=None, new_v=None, q=None, out=None):
-        """One token through the 16 layers; ev = list of (start, end) events per decode."""
+    def step(self, i, ev=None):
+        """One token through the 16 layers (input set i); ev = list of (start, end)
+        events per decode."""
         K = self.K
-        new_k = self.new_k[i] if new_k is None else new_k
-        new_v = self.new_v[i] if new_v is None else new_v
-        q = self.q[i] if q is None else q
-        out = self.out if out is None else out
+        views, outs = self.views[i], self.out_views
         for layer in range(LAYERS):
             c = self.caches[layer]
+            new_k, new_v, q = views[layer]
             # store the new token + rotate the query (one launch), decode, merge
-            K.store_rotate(c, new_k[layer], new_v[layer], self.slot, q[layer], out=self.qrot)
+            K.store_rotate(c, new_k, new_v, self.slot, q, out=self.qrot)
             if ev is not None:
                 ev[layer][0].record()
             K.decode_attn(c, self.qrot, self.seq, self.bt, self.T, self.sm_scale, self.ws)
             if ev is not None:
                 ev[layer][1].record()
-            K.merge(c, self.ws, 1, HQ, self.seq, self.T, out[layer])
+            K.merge(c, self.ws, 1, HQ, self.seq, self.T, outs[layer])
         return KERNELS_PER_LAYER * LAYERS   # kernels launched
 
 

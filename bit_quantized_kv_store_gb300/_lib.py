@@ -106,12 +106,22 @@ def _ptr(t):
         raise ValueError(f"kvq: expected a CUDA tensor, got one on {t.device}")
     if not t.is_contiguous():
         raise ValueError("kvq: expected a contiguous tensor (call .contiguous())")
-    return ctypes.c_void_p(t.data_ptr())
+    return t.data_ptr()
+
+
+# The current stream's handle without building a torch Stream object (the
+# accessor torch's own compiler uses; the public route is the fallback).
+_raw_stream = getattr(torch._C, "_cuda_getCurrentRawStream", None)
 
 
 def _stream(stream=None):
-    s = stream if stream is not None else torch.cuda.current_stream()
-    return ctypes.c_void_p(s.cuda_stream)
+    """The CUDA stream handle to launch on: `stream`'s, else the current
+    device's current torch stream."""
+    if stream is not None:
+        return stream.cuda_stream
+    if _raw_stream is not None:
+        return _raw_stream(torch.cuda.current_device())
+    return torch.cuda.current_stream().cuda_stream
 
 
 def _dtype_code(t):

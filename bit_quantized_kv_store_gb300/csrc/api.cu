@@ -4,6 +4,8 @@
 
 #include <cstdio>
 
+#include <mutex>
+
 #include "kernels.cuh"
 
 namespace kvq {
@@ -69,21 +71,62 @@ static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   return fn;
 }
 
-// A plane of `rows` rows of `row_bytes` bytes, read in boxes of box_rows rows
-// with the 128-byte shared-memory swizzle.
 // A plane of `rows` rows of `row_bytes` bytes as a 2-D byte tensor; boxes of
 // box_bytes x box_rows with the given swizzle (box_bytes = the swizzle span).
+// A tensor map holds nothing but the address and this geometry, so encoded maps
+// are kept (the last kMapCache of them, under a lock) and a call on the same
+// plane reuses one instead of encoding it again.
+namespace {
+struct MapKey {
+  const void* base;
+  uint64_t rows;
+  uint32_t row_bytes, box_rows, box_bytes;
+  int swizzle;
+  bool operator==(const MapKey& o) const {
+    return base == o.base && rows == o.rows && row_bytes == o.row_bytes && box_rows == o.box_rows &&
+           box_bytes == o.box_bytes && swizzle == o.swizzle;
+  }
+};
+constexpr int kMapCache = 64;
+struct MapCache {
+  std::mutex mu;
+  MapKey key[kMapCache] = {};
+  CUtensorMap map[kMapCache];
+  bool used[kMapCache] = {};
+  int next = 0;
+};
+MapCache& map_cache() {
+  static MapCache c;
+  return c;
+}
+}  // namespace
+
 static bool encode_rows_map(CUtensorMap* m, const void* base, uint64_t rows, uint32_t row_bytes, uint32_t box_rows,
                             uint32_t box_bytes = 128, CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B) {
+  const MapKey key{base, rows, row_bytes, box_rows, box_bytes, static_cast<int>(swizzle)};
+  MapCache& mc = map_cache();
+  std::lock_guard<std::mutex> lock(mc.mu);
+  for (int i = 0; i < kMapCache; ++i)
+    if (mc.used[i] && mc.key[i] == key) {
+      *m = mc.map[i];
+      return true;
+    }
   PFN_cuTensorMapEncodeTiled_v12000 fn = tensor_map_encoder();
   if (!fn) return false;
   cuuint64_t dims[2] = {row_bytes, rows > 0 ? rows : 1};
   cuuint64_t strides[1] = {row_bytes};
   cuuint32_t box[2] = {box_bytes, box_rows};
   cuuint32_t es[2] = {1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, es,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  if (fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, es,
+         CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return false;
+  const int slot = mc.next;
+  mc.next = (mc.next + 1) % kMapCache;
+  mc.key[slot] = key;
+  mc.map[slot] = *m;
+  mc.used[slot] = true;
+  return true;
 }
 
 struct WsLayout {

@@ -378,14 +378,12 @@ cudaError_t launch_decode_bf16(const DecodeArgs& a, int B, cudaStream_t s) {
   const size_t smem = sizeof(BfSmem) + 1024;
   dim3 grid(a.P, a.c.num_kv_heads, B);
   if (a.sel) {
-    cudaError_t e =
-        cudaFuncSetAttribute(decode_bf16_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaError_t e = set_max_smem_once<decode_bf16_kernel<true>>((int)smem);
     if (e != cudaSuccess) return e;
     e = launch_pdl(decode_bf16_kernel<true>, grid, dim3(kBfWarps * 32), smem, s, a);
     if (e != cudaSuccess) return e;
   } else {
-    cudaError_t e =
-        cudaFuncSetAttribute(decode_bf16_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaError_t e = set_max_smem_once<decode_bf16_kernel<false>>((int)smem);
     if (e != cudaSuccess) return e;
     e = launch_pdl(decode_bf16_kernel<false>, grid, dim3(kBfWarps * 32), smem, s, a);
     if (e != cudaSuccess) return e;

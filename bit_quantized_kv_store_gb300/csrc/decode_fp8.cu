@@ -513,14 +513,12 @@ cudaError_t launch_decode_fp8(const DecodeArgs& a, int B, cudaStream_t s) {
   const size_t smem = sizeof(F8Smem) + 1024;
   const dim3 grid((a.Hq + kF8Heads - 1) / kF8Heads, a.P, B);
   if (a.sel) {
-    cudaError_t e =
-        cudaFuncSetAttribute(decode_fp8_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaError_t e = set_max_smem_once<decode_fp8_kernel<true>>((int)smem);
     if (e != cudaSuccess) return e;
     e = launch_pdl(decode_fp8_kernel<true>, grid, dim3((kF8Warps + 1) * 32), smem, s, a);
     if (e != cudaSuccess) return e;
   } else {
-    cudaError_t e =
-        cudaFuncSetAttribute(decode_fp8_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaError_t e = set_max_smem_once<decode_fp8_kernel<false>>((int)smem);
     if (e != cudaSuccess) return e;
     e = launch_pdl(decode_fp8_kernel<false>, grid, dim3((kF8Warps + 1) * 32), smem, s, a);
     if (e != cudaSuccess) return e;

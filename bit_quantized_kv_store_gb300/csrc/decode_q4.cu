@@ -1172,7 +1172,7 @@ template <bool GATHER, int NT, bool WIN, bool TQ = false, bool LM = false, int M
 cudaError_t launch_round(const DecodeArgs& a, dim3 grid, cudaStream_t s) {
   const size_t smem = sizeof(Q4Smem<NT, GATHER, VR>) + 1024;  // + slack for the 1024-byte alignment
   auto kern = decode_q4_round_kernel<GATHER, NT, WIN, TQ, LM, MINB, VR>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  cudaError_t e = set_max_smem_once<decode_q4_round_kernel<GATHER, NT, WIN, TQ, LM, MINB, VR>>((int)smem);
   if (e != cudaSuccess) return e;
   e = launch_pdl(kern, grid, dim3(kQ4Warps * 32), smem, s, a);
   if (e != cudaSuccess) return e;
@@ -1458,7 +1458,7 @@ __global__ void __launch_bounds__(2 * kRoles * 32, 2) decode_q4_spec_kernel(cons
 
 cudaError_t launch_spec(const DecodeArgs& a, dim3 grid, cudaStream_t s) {
   const size_t smem = sizeof(SpecSmem) + 1024;  // + slack for the 1024-byte alignment
-  cudaError_t e = cudaFuncSetAttribute(decode_q4_spec_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  cudaError_t e = set_max_smem_once<decode_q4_spec_kernel>((int)smem);
   if (e != cudaSuccess) return e;
   e = launch_pdl(decode_q4_spec_kernel, grid, dim3(2 * kRoles * 32), smem, s, a);
   if (e != cudaSuccess) return e;
@@ -1467,21 +1467,13 @@ cudaError_t launch_spec(const DecodeArgs& a, dim3 grid, cudaStream_t s) {
 
 }  // namespace q4s
 
-// Streaming multiprocessors of the current device.
-static int sm_count() {
-  int dev = 0, n = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-    return 0;
-  return n;
-}
-
 cudaError_t launch_decode_q4(const DecodeArgs& a, int B, cudaStream_t s) {
   using namespace q4r;
   if (a.nrows <= 0) {
     const dim3 grid(a.P, a.c.num_kv_heads, B);
     if (a.tq) return a.sel ? cudaErrorInvalidValue : launch_round<false, 1, false, true>(a, grid, s);
     const int64_t ctas = (int64_t)grid.x * grid.y * grid.z;
-    const bool small = ctas <= 2 * (int64_t)sm_count();  // one wave at two CTAs per SM
+    const bool small = ctas <= 2 * (int64_t)device_sm_count();  // one wave at two CTAs per SM
     if (a.fused_out)
       return a.sel ? cudaErrorInvalidValue
                    : small ? launch_round<false, 1, false, false, true, 2, 2>(a, grid, s)

@@ -3,6 +3,8 @@
 #pragma once
 #include <cuda.h>
 
+#include <atomic>
+
 #include "common.cuh"
 
 namespace kvq {
@@ -109,6 +111,27 @@ int32_t check_decode_and_merge(const kvq_cache* cache, const float* q, int32_t n
 
 // Remember a failed CUDA call for kvq_last_cuda_error(); returns KVQ_ERR_CUDA.
 int32_t record_cuda_failure(cudaError_t e);
+
+// ---------------------------------------------------------------- per-launch invariants (host.cu)
+// Unique ID of the calling thread's current CUDA context (0 if there is none or
+// it cannot be read).  A context re-created by cudaDeviceReset, or another
+// context made current, has another ID.
+unsigned long long current_context_id();
+// Streaming multiprocessors of the current device (queried once per device).
+int device_sm_count();
+
+// Raise Kern's dynamic shared-memory limit to `bytes`, once per CUDA context
+// (the attribute lives as long as the context; a context of another ID, or one
+// whose ID cannot be read, sets it again).
+template <auto Kern>
+cudaError_t set_max_smem_once(int bytes) {
+  static std::atomic<unsigned long long> done_ctx{0};
+  const unsigned long long ctx = current_context_id();
+  if (ctx != 0 && done_ctx.load(std::memory_order_acquire) == ctx) return cudaSuccess;
+  const cudaError_t e = cudaFuncSetAttribute(Kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess && ctx != 0) done_ctx.store(ctx, std::memory_order_release);
+  return e;
+}
 
 cudaError_t launch_store(const kvq_cache& c, const void* k, const void* v, int dtype, int64_t n_tok,
                          const int32_t* slots, int32_t* status, cudaStream_t s);

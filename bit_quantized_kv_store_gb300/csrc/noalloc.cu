@@ -42,41 +42,6 @@ struct ScratchAddr {
 static ScratchAddr g_scratch[kMaxDevices];
 static std::mutex g_scratch_mu;
 
-// cuCtxGetCurrent / cuCtxGetId through the runtime's driver entry points (no
-// link-time dependency on libcuda); looked up once.
-struct CtxQueries {
-  PFN_cuCtxGetCurrent_v4000 current = nullptr;
-  PFN_cuCtxGetId_v12000 id = nullptr;
-};
-static const CtxQueries& ctx_queries() {
-  static const CtxQueries q = [] {
-    CtxQueries r;
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult st;
-    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 4000, cudaEnableDefault, &st) == cudaSuccess &&
-        st == cudaDriverEntryPointSuccess)
-      r.current = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(p);
-    p = nullptr;
-    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &st) == cudaSuccess &&
-        st == cudaDriverEntryPointSuccess)
-      r.id = reinterpret_cast<PFN_cuCtxGetId_v12000>(p);
-    return r;
-  }();
-  return q;
-}
-
-// ID of the calling thread's current context, 0 if there is none (or it cannot
-// be read, in which case the address is looked up on every call).
-static unsigned long long current_ctx_id() {
-  const CtxQueries& q = ctx_queries();
-  if (!q.current || !q.id) return 0;
-  CUcontext ctx = nullptr;
-  if (q.current(&ctx) != CUDA_SUCCESS || !ctx) return 0;
-  unsigned long long id = 0;
-  if (q.id(ctx, &id) != CUDA_SUCCESS) return 0;
-  return id;
-}
-
 // Device address of the scratch array in the current device's current context.
 static cudaError_t static_scratch(void** out) {
   int dev = 0;
@@ -84,7 +49,7 @@ static cudaError_t static_scratch(void** out) {
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
   std::lock_guard<std::mutex> lock(g_scratch_mu);
-  unsigned long long id = current_ctx_id();
+  unsigned long long id = current_context_id();
   if (id != 0 && g_scratch[dev].ctx_id == id) {
     *out = g_scratch[dev].ptr;
     return cudaSuccess;
@@ -92,7 +57,7 @@ static cudaError_t static_scratch(void** out) {
   void* p = nullptr;
   e = cudaGetSymbolAddress(&p, g_static_scratch);  // binds the primary context if none was current
   if (e != cudaSuccess) return e;
-  if (id == 0) id = current_ctx_id();
+  if (id == 0) id = current_context_id();
   g_scratch[dev] = ScratchAddr{id, id != 0 ? p : nullptr};
   *out = p;
   return cudaSuccess;

@@ -570,8 +570,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_tc_kernel(const __grid_
 cudaError_t launch_prefill_tc(const PrefillArgs& a, cudaStream_t s) {
   if (a.n_q == 0) return cudaSuccess;
   const size_t smem = sizeof(PfSmem) + 1024;
-  cudaError_t e =
-      cudaFuncSetAttribute(prefill_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  cudaError_t e = set_max_smem_once<prefill_tc_kernel>(static_cast<int>(smem));
   if (e != cudaSuccess) return e;
   const int qpb = 128 / a.group;
   dim3 grid((a.n_q + qpb - 1) / qpb, a.c.num_kv_heads);

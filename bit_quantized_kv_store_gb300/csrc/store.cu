@@ -550,9 +550,8 @@ cudaError_t launch_store(const kvq_cache& c, const void* k, const void* v, int d
   } else if (q4) {
     // one lane per (row, group); launches of at most 2^30 groups, so that the
     // kernel's group indices stay 32-bit
-    int dev = 0, n_sm = 0, per_sm = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-      n_sm = 1;
+    int n_sm = device_sm_count(), per_sm = 0;
+    if (n_sm < 1) n_sm = 1;
     {
       auto kern = rot ? store_q4_lane_kernel<8, true, true, true> : store_q4_lane_kernel<8, false, true, true>;
       if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kLaneBlock, 0) != cudaSuccess || per_sm < 1)

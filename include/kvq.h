@@ -19,8 +19,13 @@
  * Conventions for every entry point:
  *  - Pointers named d_* or documented as "device" are device pointers owned by the
  *    caller.  The library never allocates, frees or keeps device memory between
- *    calls and holds no global mutable state; calls are reentrant.  (The one
+ *    calls; calls are reentrant and may come from several host threads.  (The one
  *    exception is kvq_decode_noalloc's fixed scratch array, described there.)
+ *    Host-side state is limited to caches of per-call invariants, so that a call
+ *    costs a launch and little more: the last 64 encoded TMA tensor maps (keyed
+ *    by the plane's address and geometry, which is all a map holds; under a
+ *    lock), each kernel's shared-memory attribute (set once per CUDA context)
+ *    and the SM count per device.
  *  - `stream` is a cudaStream_t (NULL = the legacy default stream).  All work is
  *    enqueued asynchronously on it.
  *  - Host-side arguments are validated before anything is launched; on failure a
