@@ -101,7 +101,8 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-rows", action="store_true", help="skip the other hot-path rows (batched decode, prefill, "
                     "fp8, bf16 cache, store)")
-    ap.add_argument("--only", choices=["batched", "prefill", "fp8", "bf16", "q4_0", "window", "tq4", "fp8_prefill", "fused_merge"], default=None,
+    ap.add_argument("--only", choices=["batched", "prefill", "fp8", "bf16", "q4_0", "window", "tq4", "fp8_prefill", "fused_merge",
+                                       "decode_step"], default=None,
                     help="run only one of the other hot-path rows and print its measurement (for profiling)")
     ap.add_argument("--layers", type=int, default=16, help="layers per step (16 for the benchmark; fewer "
                     "only to profile a small case)")
@@ -717,6 +718,8 @@ def measure_rows(K, synth, torch, dev, peak, tflops_peak, only=None):
         out.update(_row_fp8_prefill(K, synth, torch, dev, seed, tflops_peak))
     if want("fused_merge"):
         out.update(_row_fused_merge(K, synth, torch, dev, seed))
+    if want("decode_step"):
+        out.update(_row_decode_step(K, synth, torch, dev, seed, peak))
     return out
 
 
@@ -967,6 +970,50 @@ def _row_tq4(K, synth, torch, dev, peak, seed):
                              "step_us": step_ms * 1e3, "store_4096_tokens_us": st_ms * 1e3,
                              "kernel": "decode_q4_round_kernel<TQ4> (prmt level tables, movmatrix for V)"}
     del c, ws
+    torch.cuda.empty_cache()
+    return out
+
+
+def _row_decode_step(K, synth, torch, dev, seed, peak):
+    """The 32K step with the new token stored and the query rotated inside the
+    decode launch (kvq_decode_step + kvq_merge: two launches per layer) against
+    the three-launch step (kvq_store_rotate + kvq_decode_attn + kvq_merge), both
+    as graphs of 16 layers, plus the fused launch alone."""
+    W = Workload(K, synth, torch, 32768, 1, seed, dev)
+
+    def fused():
+        for layer in range(LAYERS):
+            nk, nv, q = W.views[0][layer]
+            K.decode_step(W.caches[layer], nk, nv, q, W.seq, W.bt, W.T, W.sm_scale, W.ws)
+            K.merge(W.caches[layer], W.ws, 1, HQ, W.seq, W.T, W.out_views[layer])
+
+    def fused_only():
+        for layer in range(LAYERS):
+            nk, nv, q = W.views[0][layer]
+            K.decode_step(W.caches[layer], nk, nv, q, W.seq, W.bt, W.T, W.sm_scale, W.ws)
+
+    res = {}
+    for name, fn in (("fused", fused), ("three", lambda: W.step(0)), ("kernel", fused_only)):
+        g = capture(torch, fn)
+        for _ in range(3):
+            g.replay()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(20):
+            g.replay()
+        b.record()
+        torch.cuda.synchronize()
+        res[name] = a.elapsed_time(b) / (20 * LAYERS) * 1e3
+    byts = W.T * BYTES_PER_POS_LAYER
+    out = {"decode_step_32k": {
+        "workload": "one sequence, 32768 + 1 keys, 16 layers: store + rotation + decode fused in one launch, then the "
+                    "merge", "us_per_layer_token": res["fused"], "three_launch_us_per_layer_token": res["three"],
+        "fused_kernel_us": res["kernel"], "fused_kernel_GBs": byts / (res["kernel"] * 1e-6) / 1e9,
+        "fused_kernel_frac_of_hbm_peak": byts / (res["kernel"] * 1e-6) / 1e9 / peak,
+        "kernel": decode_kernel_name(torch, W.T) + " with the new token stored by its partition's CTA and the query "
+                                                   "rotated in the kernel"}}
+    del W
     torch.cuda.empty_cache()
     return out
 

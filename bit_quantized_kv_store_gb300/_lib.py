@@ -53,6 +53,8 @@ SIGNATURES = {
                                  _P]),
     "kvq_decode_attn_unrotated": (_I32, [ctypes.POINTER(CacheDesc), _P, _I32, _I32, _I32, _P, _P, _I32, _I32, _P,
                                          _I32, _F, _P, _SZ, _P]),
+    "kvq_decode_step": (_I32, [ctypes.POINTER(CacheDesc), _P, _P, _I32, _P, _I32, _I32, _I32, _P, _P, _I32, _I32, _F,
+                               _P, _SZ, _P]),
     "kvq_merge": (_I32, [ctypes.POINTER(CacheDesc), _P, _SZ, _I32, _I32, _P, _I32, _I32, _I32, _P, _P]),
     "kvq_prefill_attn": (_I32, [ctypes.POINTER(CacheDesc), _P, _I32, _I32, _I32, _I32, _P, _I32, _F, _P, _P, _P]),
     "kvq_read_status": (_I32, [_P, _P, _P]),
@@ -248,6 +250,18 @@ def decode_attn(cache: Cache, q, seq_lens, block_tables, max_seq_len, sm_scale, 
     _check(lib().kvq_decode_attn(cache.ref, _ptr(q), B, Hq, _ptr(seq_lens), _ptr(block_tables),
                                  block_tables.shape[1], max_seq_len, _ptr(sel), n_sel, float(sm_scale),
                                  _ptr(workspace), workspace.numel(), _stream(stream)), "kvq_decode_attn")
+
+
+def decode_step(cache: Cache, k_new, v_new, q, seq_lens, block_tables, max_seq_len, sm_scale, workspace,
+                stream=None):
+    """Store each sequence's new K/V rows at position seq_lens[b] - 1, rotate the
+    (unrotated) queries and write the split-T partials, in one launch (4-bit
+    formats); merge with merge()."""
+    B, Hq = q.shape[0], q.shape[1]
+    _check(lib().kvq_decode_step(cache.ref, _ptr(k_new), _ptr(v_new), _dtype_code(k_new), _ptr(q), _dtype_code(q), B,
+                                 Hq, _ptr(seq_lens), _ptr(block_tables), block_tables.shape[1], max_seq_len,
+                                 float(sm_scale), _ptr(workspace), workspace.numel(), _stream(stream)),
+           "kvq_decode_step")
 
 
 def decode_merged(cache: Cache, q_rot, seq_lens, block_tables, max_seq_len, sm_scale, workspace, out=None,

@@ -322,7 +322,8 @@ static int32_t decode_attn_impl(const kvq_cache* cache, const float* q, const vo
                                 int32_t num_seqs, int32_t num_q_heads, const int32_t* d_seq_lens,
                                 const int32_t* d_block_tables, int32_t max_pages_per_seq, int32_t max_seq_len,
                                 const int32_t* d_sel, int32_t n_sel, float sm_scale, void* workspace, size_t ws_bytes,
-                                void* stream, bool window = false, float* fused_out = nullptr) {
+                                void* stream, bool window = false, float* fused_out = nullptr,
+                                const void* new_k = nullptr, const void* new_v = nullptr, int32_t new_dtype = 0) {
   int32_t st = check_cache(cache);
   if (st != KVQ_OK) return st;
   st = check_decode_shape(cache, num_seqs, num_q_heads, d_seq_lens, max_seq_len, d_sel != nullptr, n_sel);
@@ -371,6 +372,9 @@ static int32_t decode_attn_impl(const kvq_cache* cache, const float* q, const vo
     a.merge_m = reinterpret_cast<float*>(ws + w.bm_off);
     a.merge_z = reinterpret_cast<float*>(ws + w.bz_off);
     a.merge_acc = reinterpret_cast<float*>(ws + w.bacc_off);
+    a.new_k = new_k;
+    a.new_v = new_v;
+    a.new_dtype = new_dtype;
     a.status = reinterpret_cast<int32_t*>(ws);
     if (!d_sel) {
       const uint64_t rows = static_cast<uint64_t>(cache->num_pages) * cache->num_kv_heads * cache->page_size;
@@ -433,6 +437,20 @@ int32_t kvq_decode_attn_unrotated(const kvq_cache* cache, const void* q, int32_t
   if (num_seqs > 0 && !q) return KVQ_ERR_INVALID_ARG;
   return decode_attn_impl(cache, nullptr, q, q_dtype, num_seqs, num_q_heads, d_seq_lens, d_block_tables,
                           max_pages_per_seq, max_seq_len, d_sel, n_sel, sm_scale, workspace, ws_bytes, stream);
+}
+
+int32_t kvq_decode_step(const kvq_cache* cache, const void* k_new, const void* v_new, int32_t kv_dtype,
+                        const void* q, int32_t q_dtype, int32_t num_seqs, int32_t num_q_heads,
+                        const int32_t* d_seq_lens, const int32_t* d_block_tables, int32_t max_pages_per_seq,
+                        int32_t max_seq_len, float sm_scale, void* workspace, size_t ws_bytes, void* stream) {
+  if (!cache) return KVQ_ERR_INVALID_ARG;
+  if (cache->format != KVQ_FMT_Q4_HAD32 && cache->format != KVQ_FMT_Q4_0) return KVQ_ERR_UNSUPPORTED;
+  if ((kv_dtype != KVQ_DT_F32 && kv_dtype != KVQ_DT_BF16) || (q_dtype != KVQ_DT_F32 && q_dtype != KVQ_DT_BF16))
+    return KVQ_ERR_INVALID_ARG;
+  if (num_seqs > 0 && (!q || !k_new || !v_new)) return KVQ_ERR_INVALID_ARG;
+  return decode_attn_impl(cache, nullptr, q, q_dtype, num_seqs, num_q_heads, d_seq_lens, d_block_tables,
+                          max_pages_per_seq, max_seq_len, nullptr, 0, sm_scale, workspace, ws_bytes, stream, false,
+                          nullptr, k_new, v_new, kv_dtype);
 }
 
 int32_t kvq_merge(const kvq_cache* cache, const void* workspace, size_t ws_bytes, int32_t num_seqs,

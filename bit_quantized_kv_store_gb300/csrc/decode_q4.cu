@@ -53,6 +53,7 @@
 #include <type_traits>
 
 #include "kernels.cuh"
+#include "q4_code.cuh"
 
 namespace kvq {
 
@@ -631,6 +632,34 @@ __device__ __forceinline__ void q4_pv_tiles(float (&acc)[2][2][NT][4], uint32_t 
   }
 }
 
+// kvq_decode_step: the CTA whose partition holds sequence b's new position pos
+// stores the new K and V rows of KV head kvh there -- the warps take the (plane,
+// group) pairs in turn, each with the warp-level group code of the store kernels
+// (the same bits as kvq_store) -- before it issues any tile copy.  The writes are
+// fenced for the async proxy, and the CTA barrier orders them before the copies
+// that read them back.  A bad page writes nothing (the tile's own check flags
+// and poisons it).
+__device__ __forceinline__ void q4_store_new_token(const DecodeArgs& a, int b, int kvh, int32_t pos, int warp,
+                                                   int lane, int nwarps) {
+  const kvq_cache& c = a.c;
+  const int32_t page = a.block_tables[(int64_t)b * a.bt_stride + pos / c.page_size];
+  if (page >= 0 && page < c.num_pages) {
+    const int64_t row = ((int64_t)page * c.num_kv_heads + kvh) * c.page_size + pos % c.page_size;
+    const int64_t src = ((int64_t)b * c.num_kv_heads + kvh) * kQ4D + lane;
+    const bool rot = c.format == KVQ_FMT_Q4_HAD32;
+    for (int task = warp; task < 2 * kQ4NG; task += nwarps) {  // warp-uniform
+      const int plane = task >= kQ4NG ? 1 : 0, G = task - plane * kQ4NG;
+      const float x = load_act(plane ? a.new_v : a.new_k, a.new_dtype, src + 32 * G);
+      __half s16;
+      const uint32_t code = rot ? q4_group_code_warp<true>(x, lane, s16) : q4_group_code_warp<false>(x, lane, s16);
+      q4_write_group_warp(static_cast<uint8_t*>(plane ? c.v : c.k) + row * (kQ4D / 2),
+                          static_cast<uint16_t*>(plane ? c.v_scale : c.k_scale) + row * kQ4NG, G, code, s16, lane);
+    }
+    fence_proxy_async_global();
+  }
+  __syncthreads();
+}
+
 // One CTA per (partition, KV head, column set).  NT column tiles of 8 columns
 // face the keys on the MMA's N side.  A plain decode (WIN = false, NT = 1) gives
 // the columns to the heads of one sequence's GQA group.  A decode window
@@ -748,6 +777,9 @@ __global__ void __launch_bounds__(kQ4Warps * 32, MINB ? MINB : q4_min_blocks(NT)
   if (!active) return;
   if (bad_page && warp == 0) set_status(a.status, KVQ_DEV_BAD_PAGE);
   __syncthreads();  // the mbarriers are initialised
+  if constexpr (!GATHER && !WIN && !TQ) {
+    if (a.new_k != nullptr && p == (T - 1) / a.part) q4_store_new_token(a, b, kvh, T - 1, warp, lane, kQ4Warps);
+  }
 
   const kvq_cache& c = a.c;
   bool poisoned = q4_issue_own<GATHER, TQ, kQ4TPW>(a, b, kvh, k0, k1, 0, warp, lane, tile_row, &a.tm_k, c.k, c.k_scale,
@@ -1266,6 +1298,7 @@ __global__ void __launch_bounds__(2 * kRoles * 32, 2) decode_q4_spec_kernel(cons
   if (!active) return;
   if (bad_page && warp == 0) set_status(a.status, KVQ_DEV_BAD_PAGE);
   __syncthreads();  // the mbarriers are initialised
+  if (a.new_k != nullptr && p == (T - 1) / a.part) q4_store_new_token(a, b, kvh, T - 1, warp, lane, 2 * kRoles);
 
   const kvq_cache& c = a.c;
   bool poisoned = false;

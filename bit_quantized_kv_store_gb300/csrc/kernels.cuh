@@ -62,6 +62,12 @@ struct DecodeArgs {
   float* merge_m;
   float* merge_z;
   float* merge_acc;
+  // 4-bit dense decode (kvq_decode_step): each sequence's new K and V rows
+  // [B][Hk][256] of new_dtype, stored at position seq_lens[b] - 1 by the CTA whose
+  // partition holds it before that CTA reads its tiles; NULL: nothing to store
+  const void* new_k;
+  const void* new_v;
+  int new_dtype;
 };
 
 // Log-sum-exp merge of the partials (merge.cu).

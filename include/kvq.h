@@ -258,6 +258,31 @@ int32_t kvq_decode_window(const kvq_cache* cache, const float* q, int32_t num_ro
                           const int32_t* d_row_lens, const int32_t* d_block_table, int32_t max_pages,
                           int32_t max_seq_len, float sm_scale, void* workspace, size_t ws_bytes, void* stream);
 
+/* kvq_decode_step -- one decode step of a 4-bit cache in one launch: each
+ * sequence appends its new token and attends with its query ([P1] "What it is":
+ * pack the new keys and values, then attend over the 4-bit cache).  For sequence
+ * b the new rows k_new[b], v_new[b] are stored at logical position
+ * seq_lens[b] - 1 (the cache row d_block_tables maps it to) exactly as kvq_store
+ * stores them, the query q[b] is rotated exactly as kvq_rotate_query rotates it
+ * (KVQ_FMT_Q4_HAD32; KVQ_FMT_Q4_0 uses it as given), and the partials are those
+ * of kvq_decode_attn over positions [0, seq_lens[b]): the same bits as
+ * kvq_store + kvq_rotate_query + kvq_decode_attn.  Inside the launch, the CTA of
+ * each (sequence, KV head) whose 512-key partition holds the new position writes
+ * the token before it reads its tiles; no other CTA reads that row.  Merge with
+ * kvq_merge.
+ *   k_new, v_new: device [num_seqs, num_kv_heads, head_dim] of kv_dtype;
+ *   q: device [num_seqs, num_q_heads, head_dim] of q_dtype, not rotated.
+ *   A sequence of length 0 stores nothing (its outputs are zeros); a new
+ *   position whose block-table entry is outside the pool stores nothing and the
+ *   decode flags KVQ_DEV_BAD_PAGE as kvq_decode_attn does.
+ * KVQ_FMT_Q4_HAD32 and KVQ_FMT_Q4_0 only (else KVQ_ERR_UNSUPPORTED); head_dim
+ * 256.  Workspace (kvq_decode_workspace_size with n_sel = 0) and errors as for
+ * kvq_decode_attn. */
+int32_t kvq_decode_step(const kvq_cache* cache, const void* k_new, const void* v_new, int32_t kv_dtype,
+                        const void* q, int32_t q_dtype, int32_t num_seqs, int32_t num_q_heads,
+                        const int32_t* d_seq_lens, const int32_t* d_block_tables, int32_t max_pages_per_seq,
+                        int32_t max_seq_len, float sm_scale, void* workspace, size_t ws_bytes, void* stream);
+
 /* kvq_decode_merged -- kvq_decode_attn and kvq_merge (with the rotation back for
  * Q4_HAD32) in one launch ([P1] "What it is": the shared 512-key chunks and the
  * in-order merge of one decode round).  The merge runs in two levels inside the

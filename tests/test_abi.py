@@ -131,9 +131,10 @@ def _tq4_desc(K, D=256, signs=4096):
 
 
 def test_host_validation_of_the_other_entries(K):
-    """Windows, the fused merge, unrotated queries, TQ4, the fp8 prefill, the
-    fused store + rotation and the no-allocation decode reject bad host
-    arguments with their documented codes, before anything is enqueued."""
+    """Windows, the fused merge, unrotated queries, the fused decode step, TQ4,
+    the fp8 prefill, the fused store + rotation and the no-allocation decode
+    reject bad host arguments with their documented codes, before anything is
+    enqueued."""
     L = K.lib()
     d = _desc(K)
     bf = _desc(K, fmt=1)
@@ -160,6 +161,19 @@ def test_host_validation_of_the_other_entries(K):
     assert L.kvq_decode_attn_unrotated(*un(c=bf)) == K.ERR_UNSUPPORTED
     assert L.kvq_decode_attn_unrotated(*un(qd=7)) == K.ERR_INVALID_ARG
     assert L.kvq_decode_attn_unrotated(*un(q=None)) == K.ERR_INVALID_ARG
+    # kvq_decode_step: Q4_HAD32 / Q4_0 only, f32 / bf16 rows and queries, all three inputs, workspace size
+    ws2 = L.kvq_decode_workspace_size(ctypes.byref(d), 2, 24, 1000, 0)
+    stp = lambda c=d, kn=dummy, vn=dummy, kd=0, q=dummy, qd=0, wsb=ws2: (
+        ctypes.byref(c), kn, vn, kd, q, qd, 2, 24, dummy, dummy, 100, 1000, f, dummy, wsb, None)
+    assert L.kvq_decode_step(None, *stp()[1:]) == K.ERR_INVALID_ARG
+    assert L.kvq_decode_step(*stp(c=bf)) == K.ERR_UNSUPPORTED
+    assert L.kvq_decode_step(*stp(c=_tq4_desc(K))) == K.ERR_UNSUPPORTED
+    assert L.kvq_decode_step(*stp(kd=5)) == K.ERR_INVALID_ARG
+    assert L.kvq_decode_step(*stp(qd=5)) == K.ERR_INVALID_ARG
+    assert L.kvq_decode_step(*stp(kn=None)) == K.ERR_INVALID_ARG
+    assert L.kvq_decode_step(*stp(vn=None)) == K.ERR_INVALID_ARG
+    assert L.kvq_decode_step(*stp(q=None)) == K.ERR_INVALID_ARG
+    assert L.kvq_decode_step(*stp(wsb=ws2 - 1)) == K.ERR_WORKSPACE_TOO_SMALL
     # TQ4 caches: the sign mask is required and 4-byte aligned; head_dim 64 / 128 / 256
     one = ctypes.c_int32(0)
     st = lambda c: L.kvq_store(ctypes.byref(c), dummy, dummy, 0, 1, ctypes.byref(one), None, None)

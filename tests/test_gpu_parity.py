@@ -479,6 +479,82 @@ def test_decode_warp_specialised_equals_round_kernel(K, L):
         assert_close(solo[0], ref[0], what=f"warp-specialised L={L}")
 
 
+def _clone_q4_cache(K, g):
+    c = K.Cache(g.fmt, g.Hk, g.D, g.page_size, g.num_pages, device=DEV)
+    for name in ("k", "v", "k_scale", "v_scale"):
+        getattr(c, name).copy_(getattr(g, name))
+    return c
+
+
+@pytest.mark.parametrize("fmt", ["Q4_HAD32", "Q4_0"])
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+@pytest.mark.parametrize("lens", [[32769], [1], [512], [513], [1025, 9000, 700, 4097], [40000, 38001, 512, 20000]])
+def test_decode_step_equals_store_rotate_decode(K, fmt, dtype, lens):
+    """kvq_decode_step (store the new token inside the decode, rotate the query in
+    the kernel) gives the same partials and the same cache planes, bit for bit, as
+    kvq_store + kvq_rotate_query + kvq_decode_attn.  The new position falls at a
+    partition's start (1, 513, 1025, 9000 -> 8999 = 17 * 512 + 295: mid), its end
+    (512) and after a full partition (32769: a partition of one key); the first
+    lists run the warp-specialised kernel, the last (a grid over two CTAs per SM)
+    the round kernel."""
+    f = K.FMT_Q4_HAD32 if fmt == "Q4_HAD32" else K.FMT_Q4_0
+    g, o, bt, q, ml = decode_case(K, lens, fmt=f, seed=91, dtype=dtype)
+    g2 = _clone_q4_cache(K, g)
+    B, Hk, D = len(lens), g.Hk, g.D
+    k_new = synth.heavy_tailed((B, Hk, D), "cpu", 91, "knew", dtype=dtype).to(DEV)
+    v_new = synth.heavy_tailed((B, Hk, D), "cpu", 91, "vnew", dtype=dtype).to(DEV)
+    qd = q.to(DEV)
+    seq = torch.tensor(lens, dtype=torch.int32, device=DEV)
+    btd = torch.from_numpy(bt).to(DEV)
+    ps = g.page_size
+    slots = torch.tensor([int(bt[b, (L - 1) // ps]) * ps + (L - 1) % ps for b, L in enumerate(lens)],
+                         dtype=torch.int32, device=DEV)
+    ws1 = K.alloc_workspace(g, B, qd.shape[1], ml, device=DEV)
+    ws2 = K.alloc_workspace(g, B, qd.shape[1], ml, device=DEV)
+    K.decode_step(g, k_new, v_new, qd, seq, btd, ml, 1 / 16, ws1)
+    K.store(g2, k_new, v_new, slots)
+    qr = K.rotate_query(qd) if f == K.FMT_Q4_HAD32 else qd.float()
+    K.decode_attn(g2, qr, seq, btd, ml, 1 / 16, ws2)
+    torch.cuda.synchronize()
+    for name in ("k", "v", "k_scale", "v_scale"):
+        assert torch.equal(getattr(g, name).view(torch.uint8), getattr(g2, name).view(torch.uint8)), name
+    assert torch.equal(ws1.view(torch.int32), ws2.view(torch.int32))
+    if max(lens) < 2000:  # the merged rows against the oracle over the same cache
+        out = torch.empty((B, qd.shape[1], D), dtype=torch.float32, device=DEV)
+        K.merge(g, ws1, B, qd.shape[1], seq, ml, out)
+        O.store(o, to_np_in(k_new.cpu()), to_np_in(v_new.cpu()), slots.cpu().numpy())
+        ref = O.decode(o, to_np_in(q), lens, bt, 1 / 16)
+        for b in range(B):
+            assert_close(out[b].cpu().numpy(), ref[b], what=f"decode_step seq {b}")
+
+
+def test_decode_step_bad_page_flags_and_stores_nothing(K):
+    """A new position mapped to a page outside the pool: nothing is written, the
+    decode flags KVQ_DEV_BAD_PAGE and the sequence's outputs are NaN."""
+    lens = [700, 300]
+    g, o, bt, q, ml = decode_case(K, lens, seed=92)
+    before = [getattr(g, n).clone() for n in ("k", "v", "k_scale", "v_scale")]
+    bt = bt.copy()
+    bt[0, (lens[0] - 1) // g.page_size] = g.num_pages + 5
+    B, Hk, D = 2, g.Hk, g.D
+    k_new = synth.heavy_tailed((B, Hk, D), "cpu", 92, "knew").to(DEV)
+    v_new = synth.heavy_tailed((B, Hk, D), "cpu", 92, "vnew").to(DEV)
+    # the second sequence's new position is written (its page is good); compare the first's pages only
+    seq = torch.tensor(lens, dtype=torch.int32, device=DEV)
+    ws = K.alloc_workspace(g, B, q.shape[1], ml, device=DEV)
+    K.decode_step(g, k_new, v_new, q.to(DEV), seq, torch.from_numpy(bt).to(DEV), ml, 1 / 16, ws)
+    out = torch.empty((B, q.shape[1], D), dtype=torch.float32, device=DEV)
+    K.merge(g, ws, B, q.shape[1], seq, ml, out)
+    torch.cuda.synchronize()
+    assert K.read_status(ws) & K.DEV_BAD_PAGE
+    assert torch.isnan(out[0]).all() and torch.isfinite(out[1]).all()
+    pages0 = set(int(x) for x in bt[0, : (lens[0] + g.page_size - 1) // g.page_size] if 0 <= x < g.num_pages)
+    for t0, name in zip(before, ("k", "v", "k_scale", "v_scale")):
+        t1 = getattr(g, name)
+        for pg in pages0:
+            assert torch.equal(t0[pg], t1[pg]), name
+
+
 @pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
 @pytest.mark.parametrize("Hk,Hq", [(4, 24), (2, 4), (3, 21)])
 def test_decode_unrotated_query_equals_rotate_then_decode(K, dtype, Hk, Hq):
