@@ -10,8 +10,8 @@ context is measured in the same run and reported under "long_context".
 value   = microseconds per layer-token (lower is better), device time with the
           inputs resident in HBM; the 16 layer caches (604 MB at 32K, 4.8 GB at
           262K) exceed the 129 MB L2, so every step reads the cache from HBM.
-e2e     = the same step through the public API, call by call (48 C-ABI calls a
-          step), with the step's inputs copied from pinned host memory and the
+e2e     = the same step through the public API, call by call (32 C-ABI calls a
+          step; 48 with --step separate), with the step's inputs copied from pinned host memory and the
           outputs copied back inside the timed region; graph_replay_value is the
           same with the step replayed as a captured CUDA graph.
 roofline= the decode kernel: algorithmic bytes (codes + scales of K and V of every
@@ -44,15 +44,18 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 LAYERS, HK, HQ, D, PS = 16, 4, 24, 256, 16
-KERNELS_PER_LAYER = 3  # store + query rotation (one launch), split-T decode, merge
+# Launches per layer of a step: the fused form (kvq_decode_step: store, rotation
+# and split-T decode in one launch, then the merge) or the separate one
+# (kvq_store_rotate, kvq_decode_attn, kvq_merge).
+KERNELS_PER_LAYER = {"fused": 2, "separate": 3}
 # DRAM bytes of one decode launch (dram__bytes_read.sum + dram__bytes_write.sum
 # from an ncu capture at each context), valid only for the kernel sources whose
 # SHA-256 (first 16 hex digits, over TRAFFIC_SOURCES in order) is recorded
 # beside them: once those sources change, the bench reports no traffic until
 # the capture is taken again.
 TRAFFIC_SOURCES = ("bit_quantized_kv_store_gb300/csrc/decode_q4.cu", "bit_quantized_kv_store_gb300/csrc/common.cuh")
-TRAFFIC_CAPTURE = {"sources_sha16": "ed752d883fb9de33",
-                   "bytes": {32768: 37863168 + 0, 262144: 302254848 + 10215936}}
+TRAFFIC_CAPTURE = {"sources_sha16": "4898543f3cf84916",
+                   "bytes": {32768: 37862400 + 0, 262144: 302255616 + 10200832}}
 BYTES_PER_POS_LAYER = HK * 2 * (D // 2 + 2 * (D // 32))   # 1152
 
 
@@ -82,6 +85,16 @@ def decode_kernel_name(torch, positions, sequences=1):
     return "decode_q4_spec_kernel" if ctas <= 2 * sms else "decode_q4_round_kernel"
 
 
+def resolve_step(torch, form, positions):
+    """The step form for `positions` keys: auto takes the single launch of
+    kvq_decode_step while the decode grid fits one wave (there the warp-specialised
+    kernel rotates the queries in its prologue at no cost), else the three
+    launches, whose decode kernel runs alone (its events time it alone)."""
+    if form != "auto":
+        return form
+    return "fused" if decode_kernel_name(torch, positions) == "decode_q4_spec_kernel" else "separate"
+
+
 def _r(x, digits=4):
     """Round a float to `digits` significant digits for the compact summaries."""
     if x is None or not isinstance(x, float) or x == 0 or not math.isfinite(x):
@@ -104,6 +117,10 @@ def parse():
     ap.add_argument("--only", choices=["batched", "prefill", "fp8", "bf16", "q4_0", "window", "tq4", "fp8_prefill", "fused_merge",
                                        "decode_step"], default=None,
                     help="run only one of the other hot-path rows and print its measurement (for profiling)")
+    ap.add_argument("--step", choices=["auto", "fused", "separate"], default="auto",
+                    help="the step's launches per layer: fused (kvq_decode_step + kvq_merge), separate "
+                         "(kvq_store_rotate + kvq_decode_attn + kvq_merge), or auto: fused while the decode grid "
+                         "fits one wave of two CTAs per SM, else separate"),
     ap.add_argument("--layers", type=int, default=16, help="layers per step (16 for the benchmark; fewer "
                     "only to profile a small case)")
     args = ap.parse_args()
@@ -273,8 +290,10 @@ class Workload:
     """16 layers of 4-bit caches holding `context` positions, plus the new token's
     K/V rows and queries for each (step, layer)."""
 
-    def __init__(self, K, synth, torch, context, n_inputs, seed, device):
+    def __init__(self, K, synth, torch, context, n_inputs, seed, device, step_form="auto"):
         self.K, self.torch = K, torch
+        self.step_form = resolve_step(torch, step_form, context + 1)
+        self.kernels_per_layer = KERNELS_PER_LAYER[self.step_form]
         self.context = context
         self.T = context + 1
         self.n_pages = (self.T + PS - 1) // PS
@@ -312,9 +331,15 @@ class Workload:
         torch.cuda.synchronize()
 
     def decode_only(self):
-        """The 16 layers' decode launches alone (for the per-launch timing)."""
+        """The 16 layers' decode launches alone (for the per-launch timing): the
+        step's decode kernel (the fused launch, or kvq_decode_attn)."""
         for layer in range(LAYERS):
-            self.K.decode_attn(self.caches[layer], self.qrot, self.seq, self.bt, self.T, self.sm_scale, self.ws)
+            if self.step_form == "fused":
+                new_k, new_v, q = self.views[0][layer]
+                self.K.decode_step(self.caches[layer], new_k, new_v, q, self.seq, self.bt, self.T, self.sm_scale,
+                                   self.ws)
+            else:
+                self.K.decode_attn(self.caches[layer], self.qrot, self.seq, self.bt, self.T, self.sm_scale, self.ws)
 
     def step(self, i, ev=None):
         """One token through the 16 layers (input set i); ev = list of (start, end)
@@ -324,15 +349,21 @@ class Workload:
         for layer in range(LAYERS):
             c = self.caches[layer]
             new_k, new_v, q = views[layer]
-            # store the new token + rotate the query (one launch), decode, merge
-            K.store_rotate(c, new_k, new_v, self.slot, q, out=self.qrot)
-            if ev is not None:
-                ev[layer][0].record()
-            K.decode_attn(c, self.qrot, self.seq, self.bt, self.T, self.sm_scale, self.ws)
+            if self.step_form == "fused":
+                # store the new token, rotate the query and decode (one launch), merge
+                if ev is not None:
+                    ev[layer][0].record()
+                K.decode_step(c, new_k, new_v, q, self.seq, self.bt, self.T, self.sm_scale, self.ws)
+            else:
+                # store the new token + rotate the query (one launch), decode, merge
+                K.store_rotate(c, new_k, new_v, self.slot, q, out=self.qrot)
+                if ev is not None:
+                    ev[layer][0].record()
+                K.decode_attn(c, self.qrot, self.seq, self.bt, self.T, self.sm_scale, self.ws)
             if ev is not None:
                 ev[layer][1].record()
             K.merge(c, self.ws, 1, HQ, self.seq, self.T, outs[layer])
-        return KERNELS_PER_LAYER * LAYERS   # kernels launched
+        return self.kernels_per_layer * LAYERS   # kernels launched
 
 
 def capture(torch, fn):
@@ -381,7 +412,7 @@ def time_device(W, steps, warmup, torch, clk=None):
     d1.record()
     torch.cuda.synchronize()
     dec_avg_ms = d0.elapsed_time(d1) / (steps * LAYERS)
-    return total_ms, dec_avg_ms, KERNELS_PER_LAYER * LAYERS * steps, graphs
+    return total_ms, dec_avg_ms, W.kernels_per_layer * LAYERS * steps, graphs
 
 
 def time_e2e(W, steps, warmup, torch, graphs=None):
@@ -611,9 +642,14 @@ def cpu_baselines(names=None):
 METRIC = "decode attn us/layer-token and achieved HBM GB/s vs peak (4-bit KV)"
 
 
-def workload_config(context, world):
+def workload_config(context, world, step_form="auto"):
+    fused = "store + rotation + decode in one launch (kvq_decode_step), merge"
+    separate = "store + rotation (kvq_store_rotate), decode (kvq_decode_attn), merge"
+    launches = {"fused": fused, "separate": separate,
+                "auto": f"{fused} while the decode grid fits one wave of two CTAs per SM, else {separate}"}[step_form]
     return {"workload": f"single-sequence decode, context {context} (T={context + 1}), 16 layers, 4 KV / 24 q heads, "
                         f"head_dim 256, bf16 inputs, 5% Student-t(3)x10 channels",
+            "step": f"per layer: {launches}",
             "l2": "16 layer caches exceed L2 (no flush needed)", "parallelism": f"replicas x{world}"}
 
 
@@ -636,7 +672,7 @@ def run_reference(args):
             "unit": "us/layer-token", "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": us / 1e3, "step": "one layer-token", "higher_is_better": False, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": workload_config(args.context, int(os.environ.get("WORLD_SIZE", "1"))),
+            "config": workload_config(args.context, int(os.environ.get("WORLD_SIZE", "1")), args.step),
             "cpu_baseline": {"value": us, "unit": "us/layer-token", "cores": 1, "kind": "oracle", "sample": desc,
                              "host_cores": os.cpu_count()},
             "e2e": {"value": us, "unit": "us/layer-token", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -979,7 +1015,7 @@ def _row_decode_step(K, synth, torch, dev, seed, peak):
     decode launch (kvq_decode_step + kvq_merge: two launches per layer) against
     the three-launch step (kvq_store_rotate + kvq_decode_attn + kvq_merge), both
     as graphs of 16 layers, plus the fused launch alone."""
-    W = Workload(K, synth, torch, 32768, 1, seed, dev)
+    W = Workload(K, synth, torch, 32768, 1, seed, dev, "separate")
 
     def fused():
         for layer in range(LAYERS):
@@ -1131,7 +1167,7 @@ def main():
         return
 
     n_inputs = 4
-    W = Workload(K, synth, torch, args.context, n_inputs, 1234 + 1 + rank, dev)
+    W = Workload(K, synth, torch, args.context, n_inputs, 1234 + 1 + rank, dev, args.step)
     barrier()
     with Clocks(local) as clk:
         total_ms, dec_avg_ms, launches, graphs = time_device(W, args.steps, args.warmup, torch, clk)
@@ -1141,6 +1177,8 @@ def main():
     bytes_per_launch = W.T * BYTES_PER_POS_LAYER
     achieved = bytes_per_launch / (dec_avg_ms * 1e-3) / 1e9
     e2e_steps = max(3, args.steps // 2)
+    calls_per_step = W.kernels_per_layer * LAYERS
+    step_form = W.step_form
     g_ms, h2d, d2h = time_e2e(W, e2e_steps, 2, torch, graphs)
     del graphs
     c_ms, _, _ = time_e2e(W, e2e_steps, 2, torch, None)
@@ -1151,7 +1189,7 @@ def main():
     if not args.no_long:
         del W
         torch.cuda.empty_cache()
-        WL = Workload(K, synth, torch, args.long_context, 2, 1234 + 2 + rank, dev)
+        WL = Workload(K, synth, torch, args.long_context, 2, 1234 + 2 + rank, dev, args.step)
         lsteps = max(3, args.steps // 4)
         barrier()
         with Clocks(local) as clk2:
@@ -1165,7 +1203,7 @@ def main():
                 "unit": "us/layer-token", "steps": lsteps, "decode_kernel_us": _r(lavg * 1e3),
                 "achieved": _r(lach), "peak": peak, "frac": _r(lach / peak, 3),
                 "traffic": traffic_bytes(args.long_context), "bytes_per_launch": lbytes,
-                "kernel": decode_kernel_name(torch, WL.T),
+                "kernel": decode_kernel_name(torch, WL.T), "step": WL.step_form,
                 "clocks": {"sm_mhz": c2["sm_mhz"], "sm_max_mhz": c2["sm_max_mhz"], "reasons": c2["reasons"],
                            "samples": c2["samples"]}}
         del WL
@@ -1200,17 +1238,18 @@ def main():
             "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": False,
             "scaling": "weak", "vs_baseline": None, "dtype": "int4 codes + fp16 scales; f16 MMA, fp32 accumulate",
             "data": "synthetic",
-            "config": workload_config(args.context, world),
+            "config": workload_config(args.context, world, args.step),
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                          "traffic": traffic_bytes(args.context), "bytes_per_launch": bytes_per_launch,
-                         "kernel": decode_kernel_name(torch, args.context + 1),
+                         "kernel": decode_kernel_name(torch, args.context + 1), "step": step_form,
                          "decode_kernel_us": dec_avg_ms * 1e3, "peak_kind": peak_kind,
                          "long_context": None if long is None else
                          {k: long[k] for k in ("context", "value", "decode_kernel_us", "achieved", "frac", "traffic",
-                                               "kernel")},
+                                               "kernel", "step")},
                          "other_kernels": None if rows is None else rows_summary(rows)},
             "e2e": {"value": c_us, "unit": "us/layer-token", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                    "path": "per call through the C ABI (48 calls per step)", "graph_replay_value": g_us},
+                    "path": f"per call through the C ABI ({calls_per_step} calls per step)",
+                    "graph_replay_value": g_us},
             "gpu_launches": launches,
             "clocks": clk.summary(),
             "long_context": long,

@@ -389,6 +389,22 @@ static int32_t decode_attn_impl(const kvq_cache* cache, const float* q, const vo
         ok = encode_rows_map(&a.tm_k, cache->k, rows, 128, 16) && encode_rows_map(&a.tm_v, cache->v, rows, 128, 16);
       if (!ok) return cuda_fail(cudaErrorInvalidValue);
     }
+    // An unrotated query on a grid of more than one wave: rotate it once, into
+    // the block-partial area (only the fused merge uses it, and it holds at least
+    // B x Hq x 256 floats), rather than in every CTA of every wave; the same
+    // arithmetic, so the same bits
+    if (q_raw && !fused_out && !decode_q4_one_wave(static_cast<int64_t>(w.P) * cache->num_kv_heads * num_seqs)) {
+      if (a.q_rotate) {
+        float* qr = reinterpret_cast<float*>(ws + w.bacc_off);
+        e = launch_rotate(q_raw, q_dtype, qr, static_cast<int64_t>(num_seqs) * num_q_heads, cache->head_dim, s);
+        if (e != cudaSuccess) return cuda_fail(e);
+        a.q = qr;
+        a.q_raw = nullptr;
+      } else if (q_dtype == KVQ_DT_F32) {  // Q4_0 takes the query as given
+        a.q = static_cast<const float*>(q_raw);
+        a.q_raw = nullptr;
+      }
+    }
     e = fp8 ? launch_decode_fp8(a, num_seqs, s) : bf16 ? launch_decode_bf16(a, num_seqs, s) : launch_decode_q4(a, num_seqs, s);
   }
   return e == cudaSuccess ? KVQ_OK : cuda_fail(e);

@@ -127,14 +127,12 @@ __device__ __forceinline__ uint4 ldsm_x4_trans(uint32_t addr) {
   return v;
 }
 
-
-// Query fragments (B operand of the score MMA) and biases of one column tile:
-// column g of the tile faces the query row `qrow` (all 256 dims; a dead column
-// passes live = false and gets a zero query).  Warp w prepares groups w,
-// w + kWarps, ...; the caller synchronises before the fragments are read.
+// The fragments from this lane's query values u0 = q[8t .. 8t+3], u1 =
+// q[8t+4 .. 8t+7] of each group G = warp + kWarps k (k < 8 / kWarps) of its
+// column's query row (live = false: a dead column, zero query).
 template <int kWarps>
-__device__ __forceinline__ void q4_frag_prep(const float* qrow, bool live, float qscale, int warp, int lane,
-                                             uint4 (*qf)[2][32], float4 (*qb)[4]) {
+__device__ __forceinline__ void q4_frag_build(const float4* ql0, const float4* ql1, bool live, float qscale,
+                                              int warp, int lane, uint4 (*qf)[2][32], float4 (*qb)[4]) {
   const int g = lane >> 2, t = lane & 3;
   // The K codes enter the MMA as 1024 + c (even elements, low nibbles) and
   // 1024 + 16c (odd elements, high nibbles), one lop3 each; the query values
@@ -145,12 +143,6 @@ __device__ __forceinline__ void q4_frag_prep(const float* qrow, bool live, float
   const float s = live ? qscale : 0.f;
   const float s16 = s * 0.0625f;
   constexpr int kGroupsPerWarp = kQ4NG / kWarps;
-  float4 ql0[kGroupsPerWarp], ql1[kGroupsPerWarp];  // all loads issued first
-#pragma unroll
-  for (int k = 0; k < kGroupsPerWarp; ++k) {
-    ql0[k] = *reinterpret_cast<const float4*>(qrow + 32 * (warp + kWarps * k) + 8 * t);
-    ql1[k] = *reinterpret_cast<const float4*>(qrow + 32 * (warp + kWarps * k) + 8 * t + 4);
-  }
 #pragma unroll
   for (int k = 0; k < kGroupsPerWarp; ++k) {
     const int G = warp + kWarps * k;
@@ -191,44 +183,95 @@ __device__ __forceinline__ void q4_frag_prep(const float* qrow, bool live, float
   }
 }
 
-// Query fragments of one sequence's GQA group (columns = its heads), written
-// once per CTA by its kWarps warps into qf / qb; ends with __syncthreads.
+// Query fragments (B operand of the score MMA) and biases of one column tile:
+// column g of the tile faces the query row `qrow` (all 256 dims; a dead column
+// passes live = false and gets a zero query).  Warp w prepares groups w,
+// w + kWarps, ...; the caller synchronises before the fragments are read.
 template <int kWarps>
-__device__ __forceinline__ void q4_query_prep(const DecodeArgs& a, int b, int kvh, int warp, int lane, float* qrot,
-                                              uint4 (*qf)[2][32], float4 (*qb)[4]) {
-  const int g = lane >> 2;
-  const float* qsrc = a.q + ((int64_t)b * a.Hq + kvh * a.group) * kQ4D;  // rows of the group's heads
+__device__ __forceinline__ void q4_frag_prep(const float* qrow, bool live, float qscale, int warp, int lane,
+                                             uint4 (*qf)[2][32], float4 (*qb)[4]) {
+  const int t = lane & 3;
+  constexpr int kGroupsPerWarp = kQ4NG / kWarps;
+  float4 ql0[kGroupsPerWarp], ql1[kGroupsPerWarp];  // all loads issued first
+#pragma unroll
+  for (int k = 0; k < kGroupsPerWarp; ++k) {
+    ql0[k] = *reinterpret_cast<const float4*>(qrow + 32 * (warp + kWarps * k) + 8 * t);
+    ql1[k] = *reinterpret_cast<const float4*>(qrow + 32 * (warp + kWarps * k) + 8 * t + 4);
+  }
+  q4_frag_build<kWarps>(ql0, ql1, live, qscale, warp, lane, qf, qb);
+}
+
+// The query preparation of one sequence's GQA group (columns = its heads) in two
+// halves, so that a kernel can issue the global loads early and build the
+// fragments later: q4_query_load issues them (into registers, not waited for);
+// q4_query_build rotates the group's queries when they come unrotated and writes
+// the fragments into qf / qb, ending with __syncthreads.
+template <int kWarps>
+struct QueryLoads {
+  float xs[8 * kQ4NG / kWarps];     // unrotated queries: the lane's element of each (head, group) pair
+  float4 u0[kQ4NG / kWarps], u1[kQ4NG / kWarps];  // rotated queries: the lane's fragment inputs
+};
+
+template <int kWarps>
+__device__ __forceinline__ void q4_query_load(const DecodeArgs& a, int b, int kvh, int warp, int lane,
+                                              QueryLoads<kWarps>& L) {
   if (a.q_raw) {
-    // Rotate the group's queries here, with the arithmetic of the rotation entry
-    // point (fp32 butterfly, stages 1..16, one multiply by fp32(1/sqrt(32))):
-    // warp w takes (head, group) pairs w, w + 4, ..., lane = element.
-    // All loads first (at most 8 heads x 8 groups / 4 warps = 16 per lane), so
-    // their latencies overlap; then the butterflies.
+    // warp w takes (head, group) pairs w, w + kWarps, ..., lane = element
     constexpr int kPairs = 8 * kQ4NG / kWarps;
     const int npairs = a.group * kQ4NG;
     const int64_t qbase = ((int64_t)b * a.Hq + kvh * a.group) * kQ4D + lane;
-    float xs[kPairs];
 #pragma unroll
     for (int k = 0; k < kPairs; ++k) {
       const int hg = warp + kWarps * k;  // (head, group) = (hg / 8, hg % 8): elements 32 hg .. of the rows
-      xs[k] = 0.f;
+      L.xs[k] = 0.f;
       if (hg < npairs)
-        xs[k] = a.q_dtype == KVQ_DT_F32
-                    ? static_cast<const float*>(a.q_raw)[qbase + 32 * hg]
-                    : __bfloat162float(static_cast<const __nv_bfloat16*>(a.q_raw)[qbase + 32 * hg]);
+        L.xs[k] = a.q_dtype == KVQ_DT_F32
+                      ? static_cast<const float*>(a.q_raw)[qbase + 32 * hg]
+                      : __bfloat162float(static_cast<const __nv_bfloat16*>(a.q_raw)[qbase + 32 * hg]);
     }
+  } else {
+    const int g = lane >> 2, t = lane & 3;
+    const float* qrow = a.q + ((int64_t)b * a.Hq + kvh * a.group + (g < a.group ? g : 0)) * kQ4D;
+#pragma unroll
+    for (int k = 0; k < kQ4NG / kWarps; ++k) {
+      L.u0[k] = *reinterpret_cast<const float4*>(qrow + 32 * (warp + kWarps * k) + 8 * t);
+      L.u1[k] = *reinterpret_cast<const float4*>(qrow + 32 * (warp + kWarps * k) + 8 * t + 4);
+    }
+  }
+}
+
+template <int kWarps>
+__device__ __forceinline__ void q4_query_build(const DecodeArgs& a, int warp, int lane, const QueryLoads<kWarps>& L,
+                                               float* qrot, uint4 (*qf)[2][32], float4 (*qb)[4]) {
+  const int g = lane >> 2;
+  const bool live = g < a.group;
+  if (a.q_raw) {
+    // Rotate with the arithmetic of the rotation entry point (fp32 butterfly,
+    // stages 1..16, one multiply by fp32(1/sqrt(32))), through qrot (8 heads x
+    // 256 fp32 of shared memory), then build the fragments from it.
+    constexpr int kPairs = 8 * kQ4NG / kWarps;
+    const int npairs = a.group * kQ4NG;
 #pragma unroll
     for (int k = 0; k < kPairs; ++k) {
       const int hg = warp + kWarps * k;
       if (hg < npairs)  // warp-uniform
-        qrot[32 * hg + lane] = a.q_rotate ? __fmul_rn(warp_fwht32(xs[k], lane), kHadamardScale) : xs[k];
+        qrot[32 * hg + lane] = a.q_rotate ? __fmul_rn(warp_fwht32(L.xs[k], lane), kHadamardScale) : L.xs[k];
     }
     __syncthreads();
-    qsrc = qrot;
+    q4_frag_prep<kWarps>(qrot + (live ? g : 0) * kQ4D, live, a.qscale, warp, lane, qf, qb);
+  } else {
+    q4_frag_build<kWarps>(L.u0, L.u1, live, a.qscale, warp, lane, qf, qb);
   }
-  const bool live = g < a.group;
-  q4_frag_prep<kWarps>(qsrc + (live ? g : 0) * kQ4D, live, a.qscale, warp, lane, qf, qb);
   __syncthreads();
+}
+
+// Both halves at once (the round kernel).
+template <int kWarps>
+__device__ __forceinline__ void q4_query_prep(const DecodeArgs& a, int b, int kvh, int warp, int lane, float* qrot,
+                                              uint4 (*qf)[2][32], float4 (*qb)[4]) {
+  QueryLoads<kWarps> L;
+  q4_query_load<kWarps>(a, b, kvh, warp, lane, L);
+  q4_query_build<kWarps>(a, warp, lane, L, qrot, qf, qb);
 }
 
 // ---------------------------------------------------------------- TQ4 rows
@@ -1302,6 +1345,10 @@ __global__ void __launch_bounds__(2 * kRoles * 32, 2) decode_q4_spec_kernel(cons
 
   const kvq_cache& c = a.c;
   bool poisoned = false;
+  // the query loads go out ahead of the first rounds' copies (which would
+  // otherwise queue before them); the fragments are built after the copies
+  QueryLoads<2 * kRoles> qload;
+  q4_query_load<2 * kRoles>(a, b, kvh, warp, lane, qload);
   if (scorer) {
     poisoned = q4r::q4_issue_own<false, false, 2>(a, b, kvh, k0, k1, 0, rw, lane, tile_row, &a.tm_k, c.k, c.k_scale,
                                                   sm.kc[0][rw], sm.ks[0][rw], &sm.kbar[0][rw]);
@@ -1319,7 +1366,7 @@ __global__ void __launch_bounds__(2 * kRoles * 32, 2) decode_q4_spec_kernel(cons
       poisoned |= q4r::q4_issue_own<false, false, 2>(a, b, kvh, k0, k1, 1, rw, lane, tile_row, &a.tm_v, c.v,
                                                      c.v_scale, &sm.vc[1][2 * rw], &sm.vs[1][2 * rw], &sm.vfull[1]);
   };
-  q4_query_prep<2 * kRoles>(a, b, kvh, warp, lane, reinterpret_cast<float*>(&sm.vc[0][0][0]), sm.qf[0], sm.qb[0]);
+  q4_query_build<2 * kRoles>(a, warp, lane, qload, reinterpret_cast<float*>(&sm.vc[0][0][0]), sm.qf[0], sm.qb[0]);
   if (!scorer) issue_v01();
   const int lrow = (lane & 7) + 8 * ((lane >> 3) & 1), lhi = lane >> 4;
   bool timed_out = false;
@@ -1500,13 +1547,15 @@ cudaError_t launch_spec(const DecodeArgs& a, dim3 grid, cudaStream_t s) {
 
 }  // namespace q4s
 
+bool decode_q4_one_wave(int64_t ctas) { return ctas <= 2 * static_cast<int64_t>(device_sm_count()); }
+
 cudaError_t launch_decode_q4(const DecodeArgs& a, int B, cudaStream_t s) {
   using namespace q4r;
   if (a.nrows <= 0) {
     const dim3 grid(a.P, a.c.num_kv_heads, B);
     if (a.tq) return a.sel ? cudaErrorInvalidValue : launch_round<false, 1, false, true>(a, grid, s);
     const int64_t ctas = (int64_t)grid.x * grid.y * grid.z;
-    const bool small = ctas <= 2 * (int64_t)device_sm_count();  // one wave at two CTAs per SM
+    const bool small = decode_q4_one_wave(ctas);
     if (a.fused_out)
       return a.sel ? cudaErrorInvalidValue
                    : small ? launch_round<false, 1, false, false, true, 2, 2>(a, grid, s)

@@ -148,6 +148,8 @@ cudaError_t launch_store_rotate(const kvq_cache& c, const void* k, const void* v
                                 const int32_t* slots, int32_t* status, const void* q, int q_dtype, float* q_out,
                                 int64_t q_rows, int q_head_dim, cudaStream_t s);
 cudaError_t launch_decode_q4(const DecodeArgs& a, int B, cudaStream_t s);
+// Whether a dense 4-bit decode grid of `ctas` CTAs runs in one wave (two CTAs per SM).
+bool decode_q4_one_wave(int64_t ctas);
 // TQ4 rows (tq4.cu): store, and the signed row rotation (inverse = 1: outputs back).
 cudaError_t launch_store_tq4(const kvq_cache& c, const void* k, const void* v, int dtype, int64_t n_tok,
                              const int32_t* slots, int32_t* status, cudaStream_t s);

@@ -268,8 +268,11 @@ int32_t kvq_decode_window(const kvq_cache* cache, const float* q, int32_t num_ro
  * of kvq_decode_attn over positions [0, seq_lens[b]): the same bits as
  * kvq_store + kvq_rotate_query + kvq_decode_attn.  Inside the launch, the CTA of
  * each (sequence, KV head) whose 512-key partition holds the new position writes
- * the token before it reads its tiles; no other CTA reads that row.  Merge with
- * kvq_merge.
+ * the token before it reads its tiles; no other CTA reads that row.  A grid of
+ * more than one wave (over two CTAs per SM) of a KVQ_FMT_Q4_HAD32 cache takes a
+ * second launch first that rotates the queries once into the workspace (the
+ * in-kernel rotation would be repeated by every CTA of every wave); a KVQ_FMT_Q4_0
+ * cache with fp32 queries then reads q as given.  Merge with kvq_merge.
  *   k_new, v_new: device [num_seqs, num_kv_heads, head_dim] of kv_dtype;
  *   q: device [num_seqs, num_q_heads, head_dim] of q_dtype, not rotated.
  *   A sequence of length 0 stores nothing (its outputs are zeros); a new
@@ -306,16 +309,16 @@ int32_t kvq_decode_merged(const kvq_cache* cache, const float* q, int32_t num_se
  * query rotation done inside the decode kernel ([P1] "What it is": the query
  * is rotated once, then the 4-bit cache is streamed in rotated space), saving the
  * separate kvq_rotate_query launch of a decode step.  Every CTA (one per 512-key
- * partition and KV head) repeats the rotation of its group's queries, so this
- * can pay off only for short contexts (few partitions); with the current
- * decode kernel it measured slower at both 32K keys (+0.6 us per layer) and
- * 262K keys (+6 us), so the benchmark step rotates with kvq_store_rotate.
+ * partition and KV head) repeats the rotation of its group's queries, which
+ * pays off while the grid runs in one wave (up to two CTAs per SM); a larger
+ * grid (it measured +6 us per layer at 262K keys) takes a rotation launch first
+ * instead, into the workspace, as kvq_decode_step does.
  *   q: device [num_seqs, num_q_heads, 256] of q_dtype (KVQ_DT_F32 or KVQ_DT_BF16),
- *      unrotated.  Each CTA rotates the queries of its GQA group with the
- *      arithmetic of kvq_rotate_query, so the partials equal those of
- *      kvq_rotate_query + kvq_decode_attn bit for bit.
+ *      unrotated (KVQ_FMT_Q4_0: used as given).  The queries of each GQA group
+ *      are rotated with the arithmetic of kvq_rotate_query, so the partials
+ *      equal those of kvq_rotate_query + kvq_decode_attn bit for bit.
  * Other arguments, workspace and errors as for kvq_decode_attn; formats other
- * than Q4_HAD32 return KVQ_ERR_UNSUPPORTED. */
+ * than Q4_HAD32 and Q4_0 return KVQ_ERR_UNSUPPORTED. */
 int32_t kvq_decode_attn_unrotated(const kvq_cache* cache, const void* q, int32_t q_dtype, int32_t num_seqs,
                                   int32_t num_q_heads, const int32_t* d_seq_lens, const int32_t* d_block_tables,
                                   int32_t max_pages_per_seq, int32_t max_seq_len, const int32_t* d_sel,
