@@ -462,6 +462,40 @@ def test_decode_concurrent_equals_solo_and_deterministic(K, lens):
         assert np.array_equal(solo[0], out[b])
 
 
+@pytest.mark.parametrize("Hk,Hq,L", [(4, 24, 100001), (4, 24, 78337), (8, 16, 40000), (2, 12, 160000)])
+def test_decode_split_launch_equals_batched(K, Hk, Hq, L):
+    """One sequence whose grid is over one wave of four CTAs per SM runs in two
+    launches: the round kernel over the whole waves, the warp-specialised kernel
+    over the remaining partitions (started beside the first launch's last wave);
+    next to a short sequence the same partitions run in the round kernel alone.
+    The two give the same bits.  Partitions per KV head: 196 (152 + a tail of 44,
+    the last of 161 keys), 154 (152 + 2, the last of 1 key), 79 (8 KV heads: 76 +
+    3, the last of 64 keys) and 313 (2 KV heads: 304 + 9, the last of 256 keys)."""
+    lens = [L, 600]
+    g, o, bt, q, ml = decode_case(K, lens, Hk=Hk, Hq=Hq, seed=78)
+    out, _ = run_decode(K, g, bt, q, lens, ml, 1 / 16)
+    solo, _ = run_decode(K, g, bt[:1], q[:1], [L], L, 1 / 16)
+    solo2, _ = run_decode(K, g, bt[:1], q[:1], [L], L, 1 / 16)
+    assert np.array_equal(solo, solo2)
+    assert np.array_equal(solo[0], out[0])
+
+
+def test_decode_split_launch_bad_page_in_the_tail(K):
+    """A bad block-table entry in a partition of the tail launch of a split
+    decode: flagged, the sequence's outputs NaN, and the next decode
+    unaffected."""
+    L = 100001
+    g, o, bt, q, ml = decode_case(K, [L], seed=79)
+    good, _ = run_decode(K, g, bt, q, [L], L, 1 / 16)
+    bad_bt = bt.copy()
+    bad_bt[0, (170 * 512 + 40) // g.page_size] = -3  # partition 170: the tail holds 152 .. 195
+    out, ws = run_decode(K, g, bad_bt, q, [L], L, 1 / 16)
+    assert K.read_status(ws) & K.DEV_BAD_PAGE
+    assert np.isnan(out[0]).all()
+    again, _ = run_decode(K, g, bt, q, [L], L, 1 / 16)
+    assert np.array_equal(again, good)
+
+
 @pytest.mark.parametrize("L", [32769, 16383 + 200, 1337])
 def test_decode_warp_specialised_equals_round_kernel(K, L):
     """A grid that fits in one wave of two CTAs per SM (the sequence alone) runs
@@ -499,15 +533,18 @@ def _clone_q4_cache(K, g):
 
 @pytest.mark.parametrize("fmt", ["Q4_HAD32", "Q4_0"])
 @pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
-@pytest.mark.parametrize("lens", [[32769], [1], [512], [513], [1025, 9000, 700, 4097], [40000, 38001, 512, 20000]])
+@pytest.mark.parametrize("lens", [[32769], [1], [512], [513], [1025, 9000, 700, 4097], [40000, 38001, 512, 20000],
+                                  [100001]])
 def test_decode_step_equals_store_rotate_decode(K, fmt, dtype, lens):
     """kvq_decode_step (store the new token inside the decode, rotate the query in
     the kernel) gives the same partials and the same cache planes, bit for bit, as
     kvq_store + kvq_rotate_query + kvq_decode_attn.  The new position falls at a
     partition's start (1, 513, 1025, 9000 -> 8999 = 17 * 512 + 295: mid), its end
     (512) and after a full partition (32769: a partition of one key); the first
-    lists run the warp-specialised kernel on the unrotated query, the last (a grid
-    over two CTAs per SM) one rotation launch and then the round kernel."""
+    lists run the warp-specialised kernel on the unrotated query, the last two (a
+    grid over two CTAs per SM) one rotation launch and then the round kernel (for
+    the single 100001-key sequence in two launches, the new position's
+    partition 195 in the second)."""
     f = K.FMT_Q4_HAD32 if fmt == "Q4_HAD32" else K.FMT_Q4_0
     g, o, bt, q, ml = decode_case(K, lens, fmt=f, seed=91, dtype=dtype)
     g2 = _clone_q4_cache(K, g)
