@@ -463,14 +463,12 @@ def test_decode_concurrent_equals_solo_and_deterministic(K, lens):
 
 
 @pytest.mark.parametrize("Hk,Hq,L", [(4, 24, 100001), (4, 24, 78337), (8, 16, 40000), (2, 12, 160000)])
-def test_decode_split_launch_equals_batched(K, Hk, Hq, L):
-    """One sequence whose grid is over one wave of four CTAs per SM runs in two
-    launches: the round kernel over the whole waves, the warp-specialised kernel
-    over the remaining partitions (started beside the first launch's last wave);
-    next to a short sequence the same partitions run in the round kernel alone.
-    The two give the same bits.  Partitions per KV head: 196 (152 + a tail of 44,
-    the last of 161 keys), 154 (152 + 2, the last of 1 key), 79 (8 KV heads: 76 +
-    3, the last of 64 keys) and 313 (2 KV heads: 304 + 9, the last of 256 keys)."""
+def test_decode_long_sequence_equals_batched(K, Hk, Hq, L):
+    """One sequence whose grid is over one wave of four CTAs per SM (several
+    waves, the last one partial) gives the same bits alone and next to a short
+    sequence, and the same bits twice.  Partitions per KV head: 196 (the last of
+    161 keys), 154 (the last of 1 key), 79 (8 KV heads: the last of 64 keys) and
+    313 (2 KV heads: the last of 256 keys)."""
     lens = [L, 600]
     g, o, bt, q, ml = decode_case(K, lens, Hk=Hk, Hq=Hq, seed=78)
     out, _ = run_decode(K, g, bt, q, lens, ml, 1 / 16)
@@ -480,15 +478,15 @@ def test_decode_split_launch_equals_batched(K, Hk, Hq, L):
     assert np.array_equal(solo[0], out[0])
 
 
-def test_decode_split_launch_bad_page_in_the_tail(K):
-    """A bad block-table entry in a partition of the tail launch of a split
-    decode: flagged, the sequence's outputs NaN, and the next decode
+def test_decode_bad_page_in_a_late_wave(K):
+    """A bad block-table entry in a partition of a later wave of a long
+    sequence's decode: flagged, the sequence's outputs NaN, and the next decode
     unaffected."""
     L = 100001
     g, o, bt, q, ml = decode_case(K, [L], seed=79)
     good, _ = run_decode(K, g, bt, q, [L], L, 1 / 16)
     bad_bt = bt.copy()
-    bad_bt[0, (170 * 512 + 40) // g.page_size] = -3  # partition 170: the tail holds 152 .. 195
+    bad_bt[0, (170 * 512 + 40) // g.page_size] = -3  # partition 170 of 196 (4 KV heads: CTA 680 of 784)
     out, ws = run_decode(K, g, bad_bt, q, [L], L, 1 / 16)
     assert K.read_status(ws) & K.DEV_BAD_PAGE
     assert np.isnan(out[0]).all()
@@ -543,8 +541,8 @@ def test_decode_step_equals_store_rotate_decode(K, fmt, dtype, lens):
     (512) and after a full partition (32769: a partition of one key); the first
     lists run the warp-specialised kernel on the unrotated query, the last two (a
     grid over two CTAs per SM) one rotation launch and then the round kernel (for
-    the single 100001-key sequence in two launches, the new position's
-    partition 195 in the second)."""
+    the single 100001-key sequence, whose new position's partition 195 runs
+    in the grid's second wave)."""
     f = K.FMT_Q4_HAD32 if fmt == "Q4_HAD32" else K.FMT_Q4_0
     g, o, bt, q, ml = decode_case(K, lens, fmt=f, seed=91, dtype=dtype)
     g2 = _clone_q4_cache(K, g)
