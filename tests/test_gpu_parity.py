@@ -486,7 +486,7 @@ def test_decode_bad_page_in_a_late_wave(K):
     g, o, bt, q, ml = decode_case(K, [L], seed=79)
     good, _ = run_decode(K, g, bt, q, [L], L, 1 / 16)
     bad_bt = bt.copy()
-    bad_bt[0, (170 * 512 + 40) // g.page_size] = -3  # partition 170 of 196 (4 KV heads: CTA 680 of 784)
+    bad_bt[0, (170 * 512 + 40) // g.page_size] = -3  # partition 170 of 196 (KV head 3: CTA 758, in the second wave of 608)
     out, ws = run_decode(K, g, bad_bt, q, [L], L, 1 / 16)
     assert K.read_status(ws) & K.DEV_BAD_PAGE
     assert np.isnan(out[0]).all()
