@@ -14,8 +14,9 @@
 // into one raw stage: dense tiles by 2-D TMA (the latent codes as four 128-byte
 // column boxes of 16 rows with the 128-byte swizzle, the rope codes as one
 // 64-byte box with the 64-byte swizzle, the scales by 1-D bulk copies);
-// gathered tiles row by row (1-D bulk copies into rows padded to 528 / 80
-// bytes; scales by plain loads).
+// gathered tiles row by row (the latent rows by 1-D bulk copies, the rope rows
+// and the scales by cp.async through the load path, into rows padded to 528 /
+// 80 bytes), while the MMA warps split the query.
 //  * The 8 MMA warps convert the tile once into an f16 tile in shared memory
 //    (cvt of two e4m3 at once, exact; rows past the end become zeros), which
 //    frees the raw stage for the next tile's copy while the MMAs run.
@@ -180,15 +181,20 @@ __global__ void __launch_bounds__((kF8Warps + 1) * 32, 1) decode_fp8_kernel(cons
     sm.abort = 0;
     fence_barrier_init();
   }
-  // ---- queries: scaled by sm_scale * log2(e), split into f16 high and low parts.
-  // 32 heads x 144 float4 = 16 per thread; all loads are issued before any use.
-  {
+  __syncthreads();  // the barriers are initialised: the producer starts its copies at once
+  // ---- queries: scaled by sm_scale * log2(e), split into f16 high and low parts
+  // by the MMA warps while the producer's first tile is on its way (its row
+  // indices are a chain of dependent loads when gathering).  32 heads x 144
+  // float4 = 18 per thread; all loads are issued before any use.  The barrier
+  // the MMA warps pass after the first tile lands orders these writes before
+  // any score reads them.
+  if (warp < kF8Warps) {
     constexpr int kUnits = kF8Heads * (kF8W / 4);
-    constexpr int kPer = (kUnits + (kF8Warps + 1) * 32 - 1) / ((kF8Warps + 1) * 32);
+    constexpr int kPer = (kUnits + kF8Warps * 32 - 1) / (kF8Warps * 32);
     float4 v[kPer];
 #pragma unroll
     for (int k = 0; k < kPer; ++k) {
-      const int i = threadIdx.x + k * (kF8Warps + 1) * 32;
+      const int i = threadIdx.x + k * kF8Warps * 32;
       const int h = i / (kF8W / 4), u = i % (kF8W / 4);
       v[k] = make_float4(0.f, 0.f, 0.f, 0.f);
       if (i < kUnits && head0 + h < a.Hq)
@@ -196,7 +202,7 @@ __global__ void __launch_bounds__((kF8Warps + 1) * 32, 1) decode_fp8_kernel(cons
     }
 #pragma unroll
     for (int k = 0; k < kPer; ++k) {
-      const int i = threadIdx.x + k * (kF8Warps + 1) * 32;
+      const int i = threadIdx.x + k * kF8Warps * 32;
       if (i >= kUnits) break;
       const int h = i / (kF8W / 4), u = i % (kF8W / 4);
       uint2 hi, lo;
@@ -206,7 +212,6 @@ __global__ void __launch_bounds__((kF8Warps + 1) * 32, 1) decode_fp8_kernel(cons
       *reinterpret_cast<uint2*>(sm.qlo + h * kF8QStride + 8 * u) = lo;
     }
   }
-  __syncthreads();
 
   if (warp == kF8Warps) {
     // ---------------- producer warp
@@ -264,23 +269,37 @@ __global__ void __launch_bounds__((kF8Warps + 1) * 32, 1) decode_fp8_kernel(cons
             continue;
           }
           rows[u] = (int64_t)page * c.page_size + pos % c.page_size;
-          bytes += kF8L + kF8R;
+          bytes += kF8L;
         }
-        // scales by plain loads (4-byte rows are below the bulk-copy granule)
-#pragma unroll
-        for (int u = 0; u < 2; ++u) {
-          const int r = lane + 32 * u;
-          st.lsc[r] = rows[u] >= 0 ? static_cast<const float*>(c.k_scale)[rows[u]] : 0.f;
-          st.rsc[r] = rows[u] >= 0 ? static_cast<const float*>(c.v_scale)[rows[u]] : 0.f;
-        }
-        mbar_arrive_expect_tx(&sm.full, bytes);  // release orders the scale stores
+        // The latent rows by bulk copies (their bytes expected before they are
+        // issued), each lane's own two; the rope rows (4 x 16 bytes) and the
+        // scales (4 bytes, below the bulk-copy granule; zeros for a row without
+        // one) through the load path, so that the copy engine, which takes a
+        // tile's copies one after another, queues only the 64 latent rows.  The
+        // lane's arrival comes once its load-path copies have landed; the phase
+        // also waits for the latent bytes.
+        mbar_expect_tx(&sm.full, bytes);
+        __syncwarp();  // every lane's bytes are expected before any copy can complete
 #pragma unroll
         for (int u = 0; u < 2; ++u) {
           if (rows[u] < 0) continue;
           const int r = lane + 32 * u;
           bulk_g2s(st.lc + r * kF8GatherL, static_cast<const uint8_t*>(c.k) + rows[u] * kF8L, kF8L, &sm.full);
-          bulk_g2s(st.rc + r * kF8GatherR, static_cast<const uint8_t*>(c.v) + rows[u] * kF8R, kF8R, &sm.full);
         }
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          const int r = lane + 32 * u;
+          const int64_t row = rows[u] >= 0 ? rows[u] : 0;
+          if (rows[u] >= 0) {
+#pragma unroll
+            for (int x = 0; x < kF8R / 16; ++x)
+              cp_async_16(st.rc + r * kF8GatherR + 16 * x, static_cast<const uint8_t*>(c.v) + row * kF8R + 16 * x);
+          }
+          const uint32_t n = rows[u] >= 0 ? 4u : 0u;
+          cp_async_4(&st.lsc[r], static_cast<const float*>(c.k_scale) + row, n);
+          cp_async_4(&st.rsc[r], static_cast<const float*>(c.v_scale) + row, n);
+        }
+        cp_async_mbar_arrive(&sm.full);
       }
     }
     if (__any_sync(0xffffffffu, bad) && lane == 0) atomicOr(&sm.poison, 1);
