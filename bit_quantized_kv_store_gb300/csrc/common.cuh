@@ -115,6 +115,12 @@ __device__ __forceinline__ void cp_async_4(void* dst, const void* src, uint32_t 
 __device__ __forceinline__ void cp_async_mbar_arrive(uint64_t* bar) {
   asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
+// The current phase of `bar` also waits for every cp.async this thread issued
+// before (one more pending arrival now, made when they have landed; the phase's
+// expected count is unchanged).  Must come before the phase can complete.
+__device__ __forceinline__ void cp_async_mbar_track(uint64_t* bar) {
+  asm volatile("cp.async.mbarrier.arrive.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
 
 // 1-D bulk copy global -> shared, completing `bytes` transaction bytes on `bar`.
 // Both addresses 16-byte aligned, bytes a multiple of 16.

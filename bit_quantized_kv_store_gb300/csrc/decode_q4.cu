@@ -385,11 +385,9 @@ __device__ __forceinline__ bool q4_issue_plane(const DecodeArgs& a, int b, int k
       mbar_arrive(bar);
       return false;
     }
-    // scales: 8 fp16 per row (Q4), or one (TQ4: 16 rows = 32 bytes)
-    constexpr int kScaleBytes = TQ ? 32 : kQ4ScaleBytes;
-    mbar_arrive_expect_tx(bar, kQ4TileBytes + kScaleBytes);
+    // the codes (the scales came by the caller's lanes through the load path)
+    mbar_arrive_expect_tx(bar, kQ4TileBytes);
     tma_rows_2d(dc, map, row0, bar);
-    bulk_g2s(ds, static_cast<const uint16_t*>(scales) + (int64_t)row0 * (TQ ? 1 : 8), kScaleBytes, bar);
     return true;
   } else {
     const int32_t T = a.seq_lens[b];
@@ -432,6 +430,26 @@ __device__ __forceinline__ bool q4_issue_own(const DecodeArgs& a, int b, int kvh
 #pragma unroll
   for (int u = 0; u < TPW; ++u) rows[u] = __shfl_sync(0xffffffffu, tile_row, (tile0 + u) & 31);
   bool bad = false;
+  if constexpr (!GATHER) {
+    // A dense tile's scales (16 consecutive rows: 256 bytes, TQ4 32) by 16-byte
+    // cp.async through the load path, lanes 16u .. of tile u, so that the copy
+    // engine, which takes its requests one after another, gets one per tile
+    // (the codes); each lane's copy is tracked on the tile's barrier before the
+    // tile's arrival below can complete the phase.
+    static_assert(TPW <= 2, "16 lanes per tile's scales");
+    constexpr int kScaleLanes = (TQ ? 32 : kQ4ScaleBytes) / 16;
+    const int u = lane >> 4, part = lane & 15;
+    int32_t row = rows[0];  // rows[u], without indexing the array by a lane-dependent value
+#pragma unroll
+    for (int v = 1; v < TPW; ++v)
+      if (u == v) row = rows[v];
+    if (u < TPW && part < kScaleLanes && k0 + 16 * (tile0 + u) < k1 && row >= 0) {
+      const uint16_t* src = static_cast<const uint16_t*>(scales) + (int64_t)row * (TQ ? 1 : 8) + 8 * part;
+      cp_async_16(&ds[0][0] + 16 * 8 * u + 8 * part, src);
+      cp_async_mbar_track(bar);
+    }
+    __syncwarp();
+  }
   if (lane == 0) {
     fence_proxy_async();  // the buffers were last read through the generic proxy
 #pragma unroll
