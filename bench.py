@@ -54,8 +54,8 @@ KERNELS_PER_LAYER = {"fused": 2, "separate": 3}
 # beside them: once those sources change, the bench reports no traffic until
 # the capture is taken again.
 TRAFFIC_SOURCES = ("bit_quantized_kv_store_gb300/csrc/decode_q4.cu", "bit_quantized_kv_store_gb300/csrc/common.cuh")
-TRAFFIC_CAPTURE = {"sources_sha16": "4898543f3cf84916",
-                   "bytes": {32768: 37862400 + 0, 262144: 302255616 + 10200832}}
+TRAFFIC_CAPTURE = {"sources_sha16": "3c9c0e5b2a3a4a91",
+                   "bytes": {32768: 37858304 + 0, 262144: 302252032 + 10301696}}
 BYTES_PER_POS_LAYER = HK * 2 * (D // 2 + 2 * (D // 32))   # 1152
 
 
@@ -308,13 +308,19 @@ class Workload:
                 v = synth.heavy_tailed((n, HK, D), dev, seed, layer, "v", s0, subset=(seed, layer, "v"))
                 K.store(c, k, v, torch.arange(s0, s0 + n, dtype=torch.int32, device=dev))
             self.caches.append(c)
-        # per (input set, layer): the new token's K/V rows and the queries
-        self.new_k = torch.stack([synth.heavy_tailed((n_inputs, 1, HK, D), dev, seed, layer, "newk",
-                                                     subset=(seed, layer, "k")) for layer in range(LAYERS)], 1)
-        self.new_v = torch.stack([synth.heavy_tailed((n_inputs, 1, HK, D), dev, seed, layer, "newv",
-                                                     subset=(seed, layer, "v")) for layer in range(LAYERS)], 1)
-        self.q = torch.stack([synth.heavy_tailed((n_inputs, 1, HQ, D), dev, seed, layer, "q")
-                              for layer in range(LAYERS)], 1)
+        # per (input set, layer): the new token's K/V rows and the queries, one
+        # input set in one contiguous buffer (a step's inputs are one copy)
+        nk, nq = LAYERS * HK * D, LAYERS * HQ * D
+        self.inbuf = torch.empty((n_inputs, 2 * nk + nq), dtype=torch.bfloat16, device=dev)
+        self.new_k = self.inbuf[:, :nk].view(n_inputs, LAYERS, 1, HK, D)
+        self.new_v = self.inbuf[:, nk:2 * nk].view(n_inputs, LAYERS, 1, HK, D)
+        self.q = self.inbuf[:, 2 * nk:].view(n_inputs, LAYERS, 1, HQ, D)
+        self.new_k.copy_(torch.stack([synth.heavy_tailed((n_inputs, 1, HK, D), dev, seed, layer, "newk",
+                                                         subset=(seed, layer, "k")) for layer in range(LAYERS)], 1))
+        self.new_v.copy_(torch.stack([synth.heavy_tailed((n_inputs, 1, HK, D), dev, seed, layer, "newv",
+                                                         subset=(seed, layer, "v")) for layer in range(LAYERS)], 1))
+        self.q.copy_(torch.stack([synth.heavy_tailed((n_inputs, 1, HQ, D), dev, seed, layer, "q")
+                                  for layer in range(LAYERS)], 1))
         self.slot = torch.tensor([context], dtype=torch.int32, device=dev)
         self.seq = torch.tensor([self.T], dtype=torch.int32, device=dev)
         self.bt = torch.arange(self.n_pages, dtype=torch.int32, device=dev).reshape(1, -1)
@@ -417,22 +423,18 @@ def time_device(W, steps, warmup, torch, clk=None):
 
 def time_e2e(W, steps, warmup, torch, graphs=None):
     """Host buffers in, host buffers out, copies inside the timed region: every
-    step copies its new K/V rows and queries from pinned host memory into the
-    device buffers the step reads, runs the 16 layers, and copies the 16 layers'
+    step copies its new K/V rows and queries (one pinned host buffer) into the
+    device buffer the step reads, runs the 16 layers, and copies the 16 layers'
     outputs back.  graphs=None: the step is issued call by call through the
     public API (kvq_store_rotate, kvq_decode_attn, kvq_merge per layer: host-side
     validation, tensor-map encoding and launch on every call); otherwise the
     captured step graphs are replayed."""
-    n_in = W.new_k.shape[0]
-    hk = [W.new_k[i].cpu().pin_memory() for i in range(n_in)]
-    hv = [W.new_v[i].cpu().pin_memory() for i in range(n_in)]
-    hq = [W.q[i].cpu().pin_memory() for i in range(n_in)]
+    n_in = W.inbuf.shape[0]
+    hin = [W.inbuf[i].cpu().pin_memory() for i in range(n_in)]  # a step's K/V rows and queries
     hout = torch.empty(W.out.shape, dtype=torch.float32).pin_memory()
 
     def one(i):
-        W.new_k[i].copy_(hk[i], non_blocking=True)
-        W.new_v[i].copy_(hv[i], non_blocking=True)
-        W.q[i].copy_(hq[i], non_blocking=True)
+        W.inbuf[i].copy_(hin[i], non_blocking=True)
         if graphs is None:
             W.step(i)
         else:
@@ -447,7 +449,7 @@ def time_e2e(W, steps, warmup, torch, graphs=None):
     for s in range(steps):
         one(s % n_in)
     el = time.perf_counter() - t
-    h2d = sum(x.numel() * x.element_size() for x in (hk[0], hv[0], hq[0]))
+    h2d = hin[0].numel() * hin[0].element_size()
     d2h = hout.numel() * hout.element_size()
     return el * 1e3, h2d, d2h
 
