@@ -1119,7 +1119,23 @@ def _row_window(K, synth, torch, dev, peak, seed):
         "window_us": win_ms * 1e3, "as_4_sequences_us": rows_ms * 1e3, "one_row_us": one_ms * 1e3,
         "window_us_per_row": win_ms * 1e3 / R, "cache_GBs_once": byts / (win_ms * 1e-3) / 1e9,
         "kernel": "decode_q4_round_kernel, window mode: the 4 rows' 24 (row, head) columns in one CTA"}
-    del c, ws
+    # the same cache, attended at 2048 selected positions of the first row (a
+    # sparse-attention selection; 512-entry partitions, as the dense keys)
+    sel = synth.distinct_sorted(2048, T0 + 1, seed, "q4sel").to(torch.int32).to(dev).reshape(1, -1)
+    wsg = K.alloc_workspace(c, 1, HQ, T0 + 1, n_sel=2048, device=dev)
+    og = torch.empty((1, HQ, D), dtype=torch.float32, device=dev)
+
+    def gather():
+        K.decode_attn(c, q[:1], lens[:1], bt_rep[:1], T0 + 1, 1 / 16, wsg, sel=sel)
+        K.merge(c, wsg, 1, HQ, lens[:1], T0 + 1, og, n_sel=2048)
+
+    g_ms = _events_time(torch, gather, 10)
+    gd_ms = _events_time(torch, lambda: K.decode_attn(c, q[:1], lens[:1], bt_rep[:1], T0 + 1, 1 / 16, wsg, sel=sel), 10)
+    out["q4_gather_262k"] = {
+        "workload": "2048 selected positions of a 262145-key sequence (4-bit rotated cache), 4 KV / 24 q heads, "
+                    "decode + merge", "gather_2048_us": g_ms * 1e3, "decode_us": gd_ms * 1e3,
+        "kernel": "decode_q4_round_kernel, gather mode (rows resolved once per CTA, copied by cp.async)"}
+    del c, ws, wsg
     torch.cuda.empty_cache()
     return out
 

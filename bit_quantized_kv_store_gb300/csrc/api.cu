@@ -376,9 +376,10 @@ static int32_t decode_attn_impl(const kvq_cache* cache, const float* q, const vo
     a.new_v = new_v;
     a.new_dtype = new_dtype;
     a.status = reinterpret_cast<int32_t*>(ws);
+    // cache rows are 32-bit in the kernels (tensor-map coordinates, gathered row lists)
+    const uint64_t rows = static_cast<uint64_t>(cache->num_pages) * cache->num_kv_heads * cache->page_size;
+    if (rows >= (1ull << 31)) return KVQ_ERR_UNSUPPORTED;
     if (!d_sel) {
-      const uint64_t rows = static_cast<uint64_t>(cache->num_pages) * cache->num_kv_heads * cache->page_size;
-      if (rows >= (1ull << 31)) return KVQ_ERR_UNSUPPORTED;
       bool ok;
       if (fp8)  // latent codes: 4 column boxes of 128 B; rope codes: one 64-byte box
         ok = encode_rows_map(&a.tm_k, cache->k, rows, 512, 16) &&

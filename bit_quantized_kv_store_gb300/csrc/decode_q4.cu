@@ -337,6 +337,7 @@ constexpr int kQ4Warps = 4;                       // warps per CTA = value group
 constexpr int kQ4TPW = 2;                         // 16-key tiles each warp scores per round
 constexpr int kQ4RoundTiles = kQ4Warps * kQ4TPW;  // 8 tiles = 128 keys per round
 constexpr int kQ4MaxColTiles = 4;                 // a decode window stacks up to 32 (row, head) columns
+constexpr int kQ4GatherPart = 512;                // entries per partition of a gather (as the dense keys)
 
 // Resident CTAs per SM the register budget is sized for: one column tile (one
 // sequence's GQA group) fits 128 registers; each further tile adds 16 P.V
@@ -362,6 +363,7 @@ struct __align__(1024) Q4Smem {
   uint64_t kbar[kQ4Warps];          // a warp's K tiles landed (kQ4TPW arrivals)
   uint64_t vfull[VR];               // the round's V tiles landed (kQ4RoundTiles arrivals)
   uint64_t vempty;                  // VR = 1: every warp is done with the round's V (kQ4Warps arrivals)
+  int32_t grow[GATHER ? kQ4GatherPart : 1];  // gather: the cache row of each of the partition's entries
   int poison;
   int last;  // fused merge: this CTA finished its (sequence, KV head) last
 };
@@ -371,66 +373,68 @@ static_assert(sizeof(float) * 8 * kQ4D <= kQ4RoundTiles / 2 * kQ4TileBytes, "rot
 
 __device__ __forceinline__ void bar_sync_cta() { asm volatile("bar.sync 1, %0;" ::"n"(kQ4Warps * 32) : "memory"); }
 
-// Issue the copies of one 16-key tile of one plane (codes + scales).  Returns
-// false if a page or a selected index is invalid (the tile then counts as
-// poisoned; the barrier still gets this arrival so that nobody waits on it).
-template <bool GATHER, bool TQ = false>
-__device__ __forceinline__ bool q4_issue_plane(const DecodeArgs& a, int b, int kvh, int key0, int nvalid,
-                                               int32_t row0, const CUtensorMap* map, const void* codes,
-                                               const void* scales, uint8_t* dc, uint16_t* ds, uint64_t* bar) {
-  const kvq_cache& c = a.c;
-  if constexpr (!GATHER) {
-    // `row0` is the cache row of key0, computed ahead by the caller (< 0: bad page)
-    if (row0 < 0) {
-      mbar_arrive(bar);
-      return false;
-    }
-    // the codes (the scales came by the caller's lanes through the load path)
-    mbar_arrive_expect_tx(bar, kQ4TileBytes);
-    tma_rows_2d(dc, map, row0, bar);
-    return true;
-  } else {
-    const int32_t T = a.seq_lens[b];
-    const int32_t* bt = a.block_tables + (int64_t)b * a.bt_stride;
-    int64_t rows[16];
-    for (int j = 0; j < nvalid; ++j) {
-      const int32_t pos = a.sel[(int64_t)b * a.n_sel + key0 + j];
-      int32_t pg = -1;
-      if (pos < 0 || pos >= T) {
-        set_status(a.status, KVQ_DEV_BAD_INDEX);
-      } else {
-        pg = bt[pos / c.page_size];
-        if (pg < 0 || pg >= c.num_pages) set_status(a.status, KVQ_DEV_BAD_PAGE);
-      }
-      if (pg < 0 || pg >= c.num_pages) {
-        mbar_arrive(bar);
-        return false;
-      }
-      rows[j] = ((int64_t)pg * c.num_kv_heads + kvh) * c.page_size + pos % c.page_size;
-    }
-    mbar_arrive_expect_tx(bar, nvalid * (128 + 16));
-    for (int j = 0; j < nvalid; ++j) {
-      bulk_g2s(dc + j * kQ4GatherRow, static_cast<const uint8_t*>(codes) + rows[j] * 128, 128, bar);
-      bulk_g2s(ds + j * 8, static_cast<const uint16_t*>(scales) + rows[j] * 8, 16, bar);
-    }
-    return true;
+// Issue the code copy of one dense 16-key tile of one plane (the scales come by
+// the caller's lanes through the load path).  `row0` is the cache row of the
+// tile's first key, computed ahead by the caller; < 0 (a bad page): no copy,
+// and false (the tile then counts as poisoned; the barrier still gets this
+// arrival so that nobody waits on it).
+__device__ __forceinline__ bool q4_issue_plane(int32_t row0, const CUtensorMap* map, uint8_t* dc, uint64_t* bar) {
+  if (row0 < 0) {
+    mbar_arrive(bar);
+    return false;
   }
+  mbar_arrive_expect_tx(bar, kQ4TileBytes);
+  tma_rows_2d(dc, map, row0, bar);
+  return true;
 }
 
 // The calling warp's TPW tiles of round `rd` of one plane into dc[u], ds[u]
-// (lane 0 issues; every lane takes part in the row shuffles).  A tile past the
-// partition still arrives on `bar`.  Returns true (lane 0) for a bad page/index.
+// (dense: lane 0 issues the code copies, 16 lanes a tile the scales; gather:
+// every lane copies rows).  A tile past the partition still arrives on `bar`.
+// Returns true for a tile with a bad page or index.
 template <bool GATHER, bool TQ = false, int TPW = 2>
 __device__ __forceinline__ bool q4_issue_own(const DecodeArgs& a, int b, int kvh, int k0, int k1, int rd, int warp,
-                                             int lane, int32_t tile_row, const CUtensorMap* map, const void* codes,
-                                             const void* scales, uint8_t (*dc)[q4_tile_bytes<GATHER>()],
-                                             uint16_t (*ds)[16 * 8], uint64_t* bar) {
+                                             int lane, int32_t tile_row, const int32_t* grow, const CUtensorMap* map,
+                                             const void* codes, const void* scales,
+                                             uint8_t (*dc)[q4_tile_bytes<GATHER>()], uint16_t (*ds)[16 * 8],
+                                             uint64_t* bar) {
   const int tile0 = kQ4RoundTiles * rd + TPW * warp;
-  int32_t rows[TPW];
+  if constexpr (GATHER) {
+    // grow[i]: the cache row of the partition's entry i (-1: a bad index or
+    // page, already flagged).  The warp copies its tiles' rows through the load
+    // path, 16 bytes a lane (a row's 128 code bytes by 8 lanes, 4 rows per
+    // instruction; the 16 scale bytes of row l by lane l): one bulk copy per row
+    // would queue 32 requests a tile on the copy engine.  Each lane's copies are
+    // tracked on the barrier before lane 0's arrival for each tile.
+    bool bad = false;
 #pragma unroll
-  for (int u = 0; u < TPW; ++u) rows[u] = __shfl_sync(0xffffffffu, tile_row, (tile0 + u) & 31);
-  bool bad = false;
-  if constexpr (!GATHER) {
+    for (int u = 0; u < TPW; ++u) {
+      const int e0 = 16 * (tile0 + u);  // the tile's first entry in the partition
+      const int nvalid = min(16, k1 - k0 - e0);
+      if (nvalid <= 0) continue;  // warp-uniform
+#pragma unroll
+      for (int x = 0; x < 4; ++x) {
+        const int c = lane + 32 * x, r = c >> 3, part = c & 7;
+        const int32_t row = r < nvalid ? grow[e0 + r] : -1;
+        if (row >= 0)
+          cp_async_16(dc[u] + r * kQ4GatherRow + 16 * part, static_cast<const uint8_t*>(codes) + (int64_t)row * 128 + 16 * part);
+      }
+      const int32_t srow = lane < nvalid ? grow[e0 + lane] : -1;
+      if (lane < 16 && srow >= 0)
+        cp_async_16(ds[u] + 8 * lane, static_cast<const uint16_t*>(scales) + (int64_t)srow * 8);
+      bad |= __any_sync(0xffffffffu, lane < nvalid && srow < 0);
+    }
+    cp_async_mbar_track(bar);
+    __syncwarp();
+    if (lane == 0)
+#pragma unroll
+      for (int u = 0; u < TPW; ++u) mbar_arrive(bar);
+    return bad;
+  } else {
+    int32_t rows[TPW];
+#pragma unroll
+    for (int u = 0; u < TPW; ++u) rows[u] = __shfl_sync(0xffffffffu, tile_row, (tile0 + u) & 31);
+    bool bad = false;
     // A dense tile's scales (16 consecutive rows: 256 bytes, TQ4 32) by 16-byte
     // cp.async through the load path, lanes 16u .. of tile u, so that the copy
     // engine, which takes its requests one after another, gets one per tile
@@ -449,21 +453,19 @@ __device__ __forceinline__ bool q4_issue_own(const DecodeArgs& a, int b, int kvh
       cp_async_mbar_track(bar);
     }
     __syncwarp();
-  }
-  if (lane == 0) {
-    fence_proxy_async();  // the buffers were last read through the generic proxy
+    if (lane == 0) {
+      fence_proxy_async();  // the buffers were last read through the generic proxy
 #pragma unroll
-    for (int u = 0; u < TPW; ++u) {
-      const int key0 = k0 + 16 * (tile0 + u);
-      if (key0 >= k1) {
-        mbar_arrive(bar);
-      } else if (!q4_issue_plane<GATHER, TQ>(a, b, kvh, key0, min(16, k1 - key0), rows[u], map, codes, scales,
-                                             dc[u], ds[u], bar)) {
-        bad = true;
+      for (int u = 0; u < TPW; ++u) {
+        const int key0 = k0 + 16 * (tile0 + u);
+        if (key0 >= k1)
+          mbar_arrive(bar);
+        else if (!q4_issue_plane(rows[u], map, dc[u], bar))
+          bad = true;
       }
     }
+    return bad;
   }
-  return bad;
 }
 
 // The fused merge (kvq_decode_merged) folds partials in two levels: the last
@@ -841,20 +843,46 @@ __global__ void __launch_bounds__(kQ4Warps * 32, MINB ? MINB : q4_min_blocks(NT)
   if constexpr (!GATHER && !WIN && !TQ) {
     if (a.new_k != nullptr && p == (T - 1) / a.part) q4_store_new_token(a, b, kvh, T - 1, warp, lane, kQ4Warps);
   }
+  const int32_t* grow = nullptr;
+  if constexpr (GATHER) {
+    // The partition's selected rows, resolved once and in parallel (each is a
+    // chain of two dependent loads: the selected position, then its page); an
+    // index outside the sequence (or its block table) or a bad page is flagged
+    // and its row poisons the tiles that hold it.
+    const int32_t Tseq = a.seq_lens[b];
+    const int32_t* bt = a.block_tables + (int64_t)b * a.bt_stride;
+    const int64_t tmax = (int64_t)a.max_pages * a.c.page_size;
+    for (int i = threadIdx.x; i < k1 - k0; i += kQ4Warps * 32) {
+      const int32_t pos = a.sel[(int64_t)b * a.n_sel + k0 + i];
+      int32_t row = -1;
+      if (pos < 0 || pos >= Tseq || pos >= tmax) {
+        set_status(a.status, KVQ_DEV_BAD_INDEX);
+      } else {
+        const int32_t pg = bt[pos / a.c.page_size];
+        if (pg < 0 || pg >= a.c.num_pages)
+          set_status(a.status, KVQ_DEV_BAD_PAGE);
+        else
+          row = static_cast<int32_t>(((int64_t)pg * a.c.num_kv_heads + kvh) * a.c.page_size + pos % a.c.page_size);
+      }
+      sm.grow[i] = row;
+    }
+    __syncthreads();
+    grow = sm.grow;
+  }
 
   const kvq_cache& c = a.c;
-  bool poisoned = q4_issue_own<GATHER, TQ, kQ4TPW>(a, b, kvh, k0, k1, 0, warp, lane, tile_row, &a.tm_k, c.k, c.k_scale,
+  bool poisoned = q4_issue_own<GATHER, TQ, kQ4TPW>(a, b, kvh, k0, k1, 0, warp, lane, tile_row, grow, &a.tm_k, c.k, c.k_scale,
                                        sm.kc[warp], sm.ks[warp], &sm.kbar[warp]);
 
   // V of round 0 (and 1), after the query fragments: the in-kernel rotation uses
   // vc[0][0..3] until the prologue's last barrier, and K(0), which the first
   // round waits for, goes out alone first
   auto issue_v01 = [&]() {
-    poisoned |= q4_issue_own<GATHER, TQ, kQ4TPW>(a, b, kvh, k0, k1, 0, warp, lane, tile_row, &a.tm_v, c.v, c.v_scale,
+    poisoned |= q4_issue_own<GATHER, TQ, kQ4TPW>(a, b, kvh, k0, k1, 0, warp, lane, tile_row, grow, &a.tm_v, c.v, c.v_scale,
                                                  &sm.vc[0][kQ4TPW * warp], &sm.vs[0][kQ4TPW * warp], &sm.vfull[0]);
     if constexpr (VR == 2) {
       if (nrounds > 1)
-        poisoned |= q4_issue_own<GATHER, TQ, kQ4TPW>(a, b, kvh, k0, k1, 1, warp, lane, tile_row, &a.tm_v, c.v,
+        poisoned |= q4_issue_own<GATHER, TQ, kQ4TPW>(a, b, kvh, k0, k1, 1, warp, lane, tile_row, grow, &a.tm_v, c.v,
                                                      c.v_scale, &sm.vc[1][kQ4TPW * warp], &sm.vs[1][kQ4TPW * warp],
                                                      &sm.vfull[1]);
     }
@@ -999,7 +1027,7 @@ __global__ void __launch_bounds__(kQ4Warps * 32, MINB ? MINB : q4_min_blocks(NT)
       // The K tiles are consumed: refill them with round r + 1.
       __syncwarp();
       if (r + 1 < nrounds)
-        poisoned |= q4_issue_own<GATHER, TQ, kQ4TPW>(a, b, kvh, k0, k1, r + 1, warp, lane, tile_row, &a.tm_k, c.k,
+        poisoned |= q4_issue_own<GATHER, TQ, kQ4TPW>(a, b, kvh, k0, k1, r + 1, warp, lane, tile_row, grow, &a.tm_k, c.k,
                                                      c.k_scale, sm.kc[warp], sm.ks[warp], &sm.kbar[warp]);
     }
 
@@ -1025,7 +1053,7 @@ __global__ void __launch_bounds__(kQ4Warps * 32, MINB ? MINB : q4_min_blocks(NT)
     if constexpr (VR == 2) {
       // slot (r + 1) % 2 held round r - 1's V, which every warp is done with: round r + 1's
       if (r >= 1 && r + 1 < nrounds)
-        poisoned |= q4_issue_own<GATHER, TQ, kQ4TPW>(a, b, kvh, k0, k1, r + 1, warp, lane, tile_row, &a.tm_v, c.v, c.v_scale,
+        poisoned |= q4_issue_own<GATHER, TQ, kQ4TPW>(a, b, kvh, k0, k1, r + 1, warp, lane, tile_row, grow, &a.tm_v, c.v, c.v_scale,
                                          &sm.vc[(r + 1) & 1][kQ4TPW * warp], &sm.vs[(r + 1) & 1][kQ4TPW * warp],
                                          &sm.vfull[(r + 1) & 1]);
     }
@@ -1150,7 +1178,7 @@ __global__ void __launch_bounds__(kQ4Warps * 32, MINB ? MINB : q4_min_blocks(NT)
       if (lane == 0) mbar_arrive(&sm.vempty);
       if (r + 1 < nrounds) {
         if (!timed_out && !__all_sync(0xffffffffu, mbar_wait_bounded(&sm.vempty, par))) timed_out = true;
-        poisoned |= q4_issue_own<GATHER, TQ, kQ4TPW>(a, b, kvh, k0, k1, r + 1, warp, lane, tile_row, &a.tm_v, c.v, c.v_scale,
+        poisoned |= q4_issue_own<GATHER, TQ, kQ4TPW>(a, b, kvh, k0, k1, r + 1, warp, lane, tile_row, grow, &a.tm_v, c.v, c.v_scale,
                                          &sm.vc[0][kQ4TPW * warp], &sm.vs[0][kQ4TPW * warp], &sm.vfull[0]);
       }
     }
@@ -1368,20 +1396,20 @@ __global__ void __launch_bounds__(2 * kRoles * 32, 2) decode_q4_spec_kernel(cons
   QueryLoads<2 * kRoles> qload;
   q4_query_load<2 * kRoles>(a, b, kvh, warp, lane, qload);
   if (scorer) {
-    poisoned = q4r::q4_issue_own<false, false, 2>(a, b, kvh, k0, k1, 0, rw, lane, tile_row, &a.tm_k, c.k, c.k_scale,
+    poisoned = q4r::q4_issue_own<false, false, 2>(a, b, kvh, k0, k1, 0, rw, lane, tile_row, nullptr, &a.tm_k, c.k, c.k_scale,
                                                   sm.kc[0][rw], sm.ks[0][rw], &sm.kbar[0][rw]);
     if (nrounds > 1)
-      poisoned |= q4r::q4_issue_own<false, false, 2>(a, b, kvh, k0, k1, 1, rw, lane, tile_row, &a.tm_k, c.k,
+      poisoned |= q4r::q4_issue_own<false, false, 2>(a, b, kvh, k0, k1, 1, rw, lane, tile_row, nullptr, &a.tm_k, c.k,
                                                      c.k_scale, sm.kc[1][rw], sm.ks[1][rw], &sm.kbar[1][rw]);
   }
   // V of rounds 0 and 1, after the query fragments: the in-kernel rotation uses
   // vc[0][0..3] until its last barrier, and K(0), which the first round waits
   // for, goes out alone first
   auto issue_v01 = [&]() {
-    poisoned = q4r::q4_issue_own<false, false, 2>(a, b, kvh, k0, k1, 0, rw, lane, tile_row, &a.tm_v, c.v, c.v_scale,
+    poisoned = q4r::q4_issue_own<false, false, 2>(a, b, kvh, k0, k1, 0, rw, lane, tile_row, nullptr, &a.tm_v, c.v, c.v_scale,
                                                   &sm.vc[0][2 * rw], &sm.vs[0][2 * rw], &sm.vfull[0]);
     if (nrounds > 1)
-      poisoned |= q4r::q4_issue_own<false, false, 2>(a, b, kvh, k0, k1, 1, rw, lane, tile_row, &a.tm_v, c.v,
+      poisoned |= q4r::q4_issue_own<false, false, 2>(a, b, kvh, k0, k1, 1, rw, lane, tile_row, nullptr, &a.tm_v, c.v,
                                                      c.v_scale, &sm.vc[1][2 * rw], &sm.vs[1][2 * rw], &sm.vfull[1]);
   };
   q4_query_build<2 * kRoles>(a, warp, lane, qload, reinterpret_cast<float*>(&sm.vc[0][0][0]), sm.qf[0], sm.qb[0]);
@@ -1424,7 +1452,7 @@ __global__ void __launch_bounds__(2 * kRoles * 32, 2) decode_q4_spec_kernel(cons
         }
         __syncwarp();  // the K tiles are consumed: refill the slot with round r + 2
         if (r + 2 < nrounds)
-          poisoned |= q4r::q4_issue_own<false, false, 2>(a, b, kvh, k0, k1, r + 2, rw, lane, tile_row, &a.tm_k, c.k,
+          poisoned |= q4r::q4_issue_own<false, false, 2>(a, b, kvh, k0, k1, r + 2, rw, lane, tile_row, nullptr, &a.tm_k, c.k,
                                                          c.k_scale, sm.kc[s][rw], sm.ks[s][rw], &sm.kbar[s][rw]);
       }
       // round maximum over the scoring warps
@@ -1498,7 +1526,7 @@ __global__ void __launch_bounds__(2 * kRoles * 32, 2) decode_q4_spec_kernel(cons
       if (r + 2 < nrounds) nbar_arrive(kBarEmpty + s, 2 * kRoles * 32);  // slot s may take round r + 2
       nbar_sync(kBarPv, kRoles * 32);  // every P.V warp is done with the round's V tiles
       if (r + 2 < nrounds)
-        poisoned |= q4r::q4_issue_own<false, false, 2>(a, b, kvh, k0, k1, r + 2, rw, lane, tile_row, &a.tm_v, c.v,
+        poisoned |= q4r::q4_issue_own<false, false, 2>(a, b, kvh, k0, k1, r + 2, rw, lane, tile_row, nullptr, &a.tm_v, c.v,
                                                        c.v_scale, &sm.vc[s][2 * rw], &sm.vs[s][2 * rw], &sm.vfull[s]);
     }
   }
@@ -1578,7 +1606,8 @@ cudaError_t launch_decode_q4(const DecodeArgs& a, int B, cudaStream_t s) {
       return a.sel ? cudaErrorInvalidValue
                    : small ? launch_round<false, 1, false, false, true, 2, 2>(a, grid, s)
                            : launch_round<false, 1, false, false, true>(a, grid, s);
-    if (a.sel) return launch_round<true, 1, false>(a, grid, s);
+    if (a.sel)  // the resolved rows of a partition live in shared memory
+      return a.part == kQ4GatherPart ? launch_round<true, 1, false>(a, grid, s) : cudaErrorInvalidValue;
     if (small) return q4s::launch_spec(a, grid, s);
     return launch_round<false, 1, false>(a, grid, s);
   }
