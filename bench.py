@@ -964,12 +964,34 @@ def _row_q4_0(K, synth, torch, dev, peak, seed):
     seq = torch.tensor([Tq], dtype=torch.int32, device=dev)
     ws = K.alloc_workspace(c, 1, HQ, Tq, device=dev)
     dms = _events_time(torch, lambda: K.decode_attn(c, q, seq, bt, Tq, 1 / 16, ws), 10)
+    # timed as the headline times its decode: 16 distinct layer caches (604 MB,
+    # over L2), the 16 launches captured in one graph and replayed, per launch
+    layers = [c]
+    for _ in range(LAYERS - 1):
+        cl = K.Cache(K.FMT_Q4_0, HK, D, PS, npg, device=dev)
+        K.store(cl, k, v, torch.arange(Tq, dtype=torch.int32, device=dev))
+        layers.append(cl)
+    g = capture(torch, lambda: [K.decode_attn(cl, q, seq, bt, Tq, 1 / 16, ws) for cl in layers])
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    reps = 10
+    e0.record()
+    for _ in range(reps):
+        g.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    gms = e0.elapsed_time(e1) / (reps * LAYERS)
     byts = Tq * BYTES_PER_POS_LAYER
-    out["q4_0_cache_32k"] = {"workload": "unrotated 4-bit cache (Q4_0), context 32768, 1 layer, same split-T + merge",
-                             "decode_kernel_us": dms * 1e3, "cache_bytes": byts,
-                             "achieved_GBs": byts / (dms * 1e-3) / 1e9, "frac_of_hbm_peak": byts / (dms * 1e-3) / 1e9 / peak,
+    out["q4_0_cache_32k"] = {"workload": "unrotated 4-bit cache (Q4_0), context 32768, same split-T + merge; the "
+                                         "decode timed over 16 layer caches in one graph (as the headline), and as "
+                                         "one launch with L2 flushed",
+                             "decode_kernel_us": gms * 1e3, "cache_bytes": byts,
+                             "achieved_GBs": byts / (gms * 1e-3) / 1e9, "frac_of_hbm_peak": byts / (gms * 1e-3) / 1e9 / peak,
+                             "single_launch_us": dms * 1e3,
                              "store_4096_tokens_us": st_ms * 1e3, "kernel": decode_kernel_name(torch, Tq)}
-    del c, ws
+    del c, ws, layers, g
     torch.cuda.empty_cache()
     return out
 
