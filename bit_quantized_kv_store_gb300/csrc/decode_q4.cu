@@ -201,20 +201,20 @@ __device__ __forceinline__ void q4_frag_prep(const float* qrow, bool live, float
   q4_frag_build<kWarps>(ql0, ql1, live, qscale, warp, lane, qf, qb);
 }
 
-// The query preparation of one sequence's GQA group (columns = its heads) in two
-// halves, so that a kernel can issue the global loads early and build the
-// fragments later: q4_query_load issues them (into registers, not waited for);
-// q4_query_build rotates the group's queries when they come unrotated and writes
-// the fragments into qf / qb, ending with __syncthreads.
+// The round kernel's query preparation: an unrotated query is rotated one
+// (head, group) pair per warp, lane = element, through a shared-memory scratch
+// (qrot) and then built into fragments.  (The warp-specialised kernel rotates in
+// the fragments' layout instead, below; in the round kernel that form measured
+// 0.7 us slower at 262K keys, though its rotated-query path is the same.)
 template <int kWarps>
-struct QueryLoads {
+struct RoundQueryLoads {
   float xs[8 * kQ4NG / kWarps];     // unrotated queries: the lane's element of each (head, group) pair
   float4 u0[kQ4NG / kWarps], u1[kQ4NG / kWarps];  // rotated queries: the lane's fragment inputs
 };
 
 template <int kWarps>
-__device__ __forceinline__ void q4_query_load(const DecodeArgs& a, int b, int kvh, int warp, int lane,
-                                              QueryLoads<kWarps>& L) {
+__device__ __forceinline__ void q4r_query_load(const DecodeArgs& a, int b, int kvh, int warp, int lane,
+                                              RoundQueryLoads<kWarps>& L) {
   if (a.q_raw) {
     // warp w takes (head, group) pairs w, w + kWarps, ..., lane = element
     constexpr int kPairs = 8 * kQ4NG / kWarps;
@@ -241,7 +241,7 @@ __device__ __forceinline__ void q4_query_load(const DecodeArgs& a, int b, int kv
 }
 
 template <int kWarps>
-__device__ __forceinline__ void q4_query_build(const DecodeArgs& a, int warp, int lane, const QueryLoads<kWarps>& L,
+__device__ __forceinline__ void q4r_query_build(const DecodeArgs& a, int warp, int lane, const RoundQueryLoads<kWarps>& L,
                                                float* qrot, uint4 (*qf)[2][32], float4 (*qb)[4]) {
   const int g = lane >> 2;
   const bool live = g < a.group;
@@ -267,11 +267,89 @@ __device__ __forceinline__ void q4_query_build(const DecodeArgs& a, int warp, in
 
 // Both halves at once (the round kernel).
 template <int kWarps>
-__device__ __forceinline__ void q4_query_prep(const DecodeArgs& a, int b, int kvh, int warp, int lane, float* qrot,
+__device__ __forceinline__ void q4r_query_prep(const DecodeArgs& a, int b, int kvh, int warp, int lane, float* qrot,
                                               uint4 (*qf)[2][32], float4 (*qb)[4]) {
-  QueryLoads<kWarps> L;
-  q4_query_load<kWarps>(a, b, kvh, warp, lane, L);
-  q4_query_build<kWarps>(a, warp, lane, L, qrot, qf, qb);
+  RoundQueryLoads<kWarps> L;
+  q4r_query_load<kWarps>(a, b, kvh, warp, lane, L);
+  q4r_query_build<kWarps>(a, warp, lane, L, qrot, qf, qb);
+}
+
+// The query preparation of one sequence's GQA group (columns = its heads) in two
+// halves, so that a kernel can issue the global loads early and build the
+// fragments later: q4_query_load issues them (into registers, not waited for);
+// q4_query_build rotates the group's queries when they come unrotated and writes
+// the fragments into qf / qb, ending with __syncthreads.  Thread (g, t) of warp
+// w holds, for head g and each of its groups G = w, w + kWarps, ..., the 8
+// values 32 G + 8 t .. + 7: the fragments' own layout.  (The
+// warp-specialised kernel's form; RAW = false compiles the unrotated path out.)
+template <int kWarps>
+struct QueryLoads {
+  float4 u0[kQ4NG / kWarps], u1[kQ4NG / kWarps];  // the thread's 8 values of each of its groups
+};
+
+template <int kWarps, bool RAW = true>
+__device__ __forceinline__ void q4_query_load(const DecodeArgs& a, int b, int kvh, int warp, int lane,
+                                              QueryLoads<kWarps>& L) {
+  const int g = lane >> 2, t = lane & 3;
+  // a column past the group reads head 0 (its fragments are zeroed)
+  const int64_t row = ((int64_t)b * a.Hq + kvh * a.group + (g < a.group ? g : 0)) * kQ4D;
+#pragma unroll
+  for (int k = 0; k < kQ4NG / kWarps; ++k) {
+    const int64_t e0 = row + 32 * (warp + kWarps * k) + 8 * t;
+    if (RAW && a.q_raw != nullptr && a.q_dtype != KVQ_DT_F32) {  // 8 bf16 values: one 16-byte load
+      const uint4 w = *reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(a.q_raw) + e0);
+      L.u0[k] = make_float4(__uint_as_float(w.x << 16), __uint_as_float(w.x & 0xFFFF0000u),
+                            __uint_as_float(w.y << 16), __uint_as_float(w.y & 0xFFFF0000u));
+      L.u1[k] = make_float4(__uint_as_float(w.z << 16), __uint_as_float(w.z & 0xFFFF0000u),
+                            __uint_as_float(w.w << 16), __uint_as_float(w.w & 0xFFFF0000u));
+    } else {
+      const float* src = RAW && a.q_raw != nullptr ? static_cast<const float*>(a.q_raw) : a.q;
+      L.u0[k] = *reinterpret_cast<const float4*>(src + e0);
+      L.u1[k] = *reinterpret_cast<const float4*>(src + e0 + 4);
+    }
+  }
+}
+
+template <int kWarps, bool RAW = true>
+__device__ __forceinline__ void q4_query_build(const DecodeArgs& a, int warp, int lane, QueryLoads<kWarps>& L,
+                                               uint4 (*qf)[2][32], float4 (*qb)[4]) {
+  const int t = lane & 3;
+  const bool live = (lane >> 2) < a.group;
+  if (RAW && a.q_raw != nullptr && a.q_rotate) {
+    // Rotate with the arithmetic of the rotation entry point: the fp32
+    // butterfly, stages 1, 2, 4, 8, 16, (a, b) -> (a + b, a - b) with a the
+    // lower index, then one multiply by fp32(1/sqrt(32)).  Stages 1, 2, 4 pair
+    // the thread's own values; stages 8 and 16 pair threads t ^ 1 and t ^ 2 of
+    // the same head (the same operands, so the same bits).
+#pragma unroll
+    for (int k = 0; k < kQ4NG / kWarps; ++k) {
+      float x[8] = {L.u0[k].x, L.u0[k].y, L.u0[k].z, L.u0[k].w, L.u1[k].x, L.u1[k].y, L.u1[k].z, L.u1[k].w};
+#pragma unroll
+      for (int h = 1; h < 8; h <<= 1)
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+          if ((i & h) == 0) {
+            const float lo = x[i], hi = x[i + h];
+            x[i] = __fadd_rn(lo, hi);
+            x[i + h] = __fsub_rn(lo, hi);
+          }
+#pragma unroll
+      for (int m = 1; m <= 2; m <<= 1) {
+        const bool upper = (t & m) != 0;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const float o = __shfl_xor_sync(0xffffffffu, x[i], m);
+          x[i] = upper ? __fsub_rn(o, x[i]) : __fadd_rn(x[i], o);
+        }
+      }
+#pragma unroll
+      for (int i = 0; i < 8; ++i) x[i] = __fmul_rn(x[i], kHadamardScale);
+      L.u0[k] = make_float4(x[0], x[1], x[2], x[3]);
+      L.u1[k] = make_float4(x[4], x[5], x[6], x[7]);
+    }
+  }
+  q4_frag_build<kWarps>(L.u0, L.u1, live, a.qscale, warp, lane, qf, qb);
+  __syncthreads();
 }
 
 // ---------------------------------------------------------------- TQ4 rows
@@ -367,8 +445,8 @@ struct __align__(1024) Q4Smem {
   int poison;
   int last;  // fused merge: this CTA finished its (sequence, KV head) last
 };
-// The unrotated-query entry point rotates the group's queries (8 heads x 256
-// fp32) into V tiles 0..3, which are first filled after the prologue.
+// The unrotated-query path of the round kernel rotates the group's queries (8
+// heads x 256 fp32) into V tiles 0..3, which are first filled after the prologue.
 static_assert(sizeof(float) * 8 * kQ4D <= kQ4RoundTiles / 2 * kQ4TileBytes, "rotated queries fit vc[0..3]");
 
 __device__ __forceinline__ void bar_sync_cta() { asm volatile("bar.sync 1, %0;" ::"n"(kQ4Warps * 32) : "memory"); }
@@ -903,7 +981,7 @@ __global__ void __launch_bounds__(kQ4Warps * 32, MINB ? MINB : q4_min_blocks(NT)
                             lane, sm.qf[0]);
     __syncthreads();
   } else {
-    q4_query_prep<kQ4Warps>(a, b, kvh, warp, lane, reinterpret_cast<float*>(&sm.vc[0][0][0]), sm.qf[0], sm.qb[0]);
+    q4r_query_prep<kQ4Warps>(a, b, kvh, warp, lane, reinterpret_cast<float*>(&sm.vc[0][0][0]), sm.qf[0], sm.qb[0]);
   }
   issue_v01();
   const uint32_t qf_addr = smem_u32(&sm.qf[0][0][0][lane]);
@@ -1336,7 +1414,6 @@ struct __align__(1024) SpecSmem {
   uint64_t vfull[2];
   int poison;
 };
-static_assert(sizeof(float) * 8 * kQ4D <= kQ4RoundTiles / 2 * kQ4TileBytes, "rotated queries fit vc[0][0..3]");
 
 __device__ __forceinline__ void nbar_sync(int id, int n) { asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory"); }
 __device__ __forceinline__ void nbar_arrive(int id, int n) {
@@ -1402,9 +1479,8 @@ __global__ void __launch_bounds__(2 * kRoles * 32, 2) decode_q4_spec_kernel(cons
       poisoned |= q4r::q4_issue_own<false, false, 2>(a, b, kvh, k0, k1, 1, rw, lane, tile_row, nullptr, &a.tm_k, c.k,
                                                      c.k_scale, sm.kc[1][rw], sm.ks[1][rw], &sm.kbar[1][rw]);
   }
-  // V of rounds 0 and 1, after the query fragments: the in-kernel rotation uses
-  // vc[0][0..3] until its last barrier, and K(0), which the first round waits
-  // for, goes out alone first
+  // V of rounds 0 and 1, after the query fragments: K(0), which the first
+  // round waits for, goes out alone first
   auto issue_v01 = [&]() {
     poisoned = q4r::q4_issue_own<false, false, 2>(a, b, kvh, k0, k1, 0, rw, lane, tile_row, nullptr, &a.tm_v, c.v, c.v_scale,
                                                   &sm.vc[0][2 * rw], &sm.vs[0][2 * rw], &sm.vfull[0]);
@@ -1412,7 +1488,7 @@ __global__ void __launch_bounds__(2 * kRoles * 32, 2) decode_q4_spec_kernel(cons
       poisoned |= q4r::q4_issue_own<false, false, 2>(a, b, kvh, k0, k1, 1, rw, lane, tile_row, nullptr, &a.tm_v, c.v,
                                                      c.v_scale, &sm.vc[1][2 * rw], &sm.vs[1][2 * rw], &sm.vfull[1]);
   };
-  q4_query_build<2 * kRoles>(a, warp, lane, qload, reinterpret_cast<float*>(&sm.vc[0][0][0]), sm.qf[0], sm.qb[0]);
+  q4_query_build<2 * kRoles>(a, warp, lane, qload, sm.qf[0], sm.qb[0]);
   if (!scorer) issue_v01();
   const int lrow = (lane & 7) + 8 * ((lane >> 3) & 1), lhi = lane >> 4;
   bool timed_out = false;
