@@ -1397,6 +1397,37 @@ namespace q4s {
 
 using namespace q4r;
 constexpr int kRoles = 4;  // warps per role
+
+// kvq_decode_step's store of the new token (q4_store_new_token's work) by the 8
+// warps: each warp's two (plane, group) pairs, with both pairs' value loads and
+// the block-table load issued together rather than one after another.
+__device__ __forceinline__ void q4s_store_new_token(const DecodeArgs& a, int b, int kvh, int32_t pos, int warp,
+                                                    int lane) {
+  constexpr int kTasks = 2 * kQ4NG / (2 * kRoles);
+  const kvq_cache& c = a.c;
+  const int64_t src = ((int64_t)b * c.num_kv_heads + kvh) * kQ4D + lane;
+  float x[kTasks];
+#pragma unroll
+  for (int i = 0; i < kTasks; ++i) {
+    const int task = warp + 2 * kRoles * i, plane = task >= kQ4NG ? 1 : 0, G = task - plane * kQ4NG;
+    x[i] = load_act(plane ? a.new_v : a.new_k, a.new_dtype, src + 32 * G);
+  }
+  const int32_t page = a.block_tables[(int64_t)b * a.bt_stride + pos / c.page_size];
+  if (page >= 0 && page < c.num_pages) {
+    const int64_t row = ((int64_t)page * c.num_kv_heads + kvh) * c.page_size + pos % c.page_size;
+    const bool rot = c.format == KVQ_FMT_Q4_HAD32;
+#pragma unroll
+    for (int i = 0; i < kTasks; ++i) {
+      const int task = warp + 2 * kRoles * i, plane = task >= kQ4NG ? 1 : 0, G = task - plane * kQ4NG;
+      __half s16;
+      const uint32_t code = rot ? q4_group_code_warp<true>(x[i], lane, s16) : q4_group_code_warp<false>(x[i], lane, s16);
+      q4_write_group_warp(static_cast<uint8_t*>(plane ? c.v : c.k) + row * (kQ4D / 2),
+                          static_cast<uint16_t*>(plane ? c.v_scale : c.k_scale) + row * kQ4NG, G, code, s16, lane);
+    }
+    fence_proxy_async_global();
+  }
+  __syncthreads();
+}
 constexpr int kBarMax = 1, kBarFull = 2, kBarEmpty = 4, kBarPv = 6;
 
 struct __align__(1024) SpecSmem {
@@ -1464,20 +1495,33 @@ __global__ void __launch_bounds__(2 * kRoles * 32, 2) decode_q4_spec_kernel(cons
   if (!active) return;
   if (bad_page && warp == 0) set_status(a.status, KVQ_DEV_BAD_PAGE);
   __syncthreads();  // the mbarriers are initialised
-  if (a.new_k != nullptr && p == (T - 1) / a.part) q4_store_new_token(a, b, kvh, T - 1, warp, lane, 2 * kRoles);
 
   const kvq_cache& c = a.c;
   bool poisoned = false;
+  auto issue_k01 = [&]() {
+    if (scorer) {
+      poisoned = q4r::q4_issue_own<false, false, 2>(a, b, kvh, k0, k1, 0, rw, lane, tile_row, nullptr, &a.tm_k, c.k,
+                                                    c.k_scale, sm.kc[0][rw], sm.ks[0][rw], &sm.kbar[0][rw]);
+      if (nrounds > 1)
+        poisoned |= q4r::q4_issue_own<false, false, 2>(a, b, kvh, k0, k1, 1, rw, lane, tile_row, nullptr, &a.tm_k, c.k,
+                                                       c.k_scale, sm.kc[1][rw], sm.ks[1][rw], &sm.kbar[1][rw]);
+    }
+  };
   // the query loads go out ahead of the first rounds' copies (which would
   // otherwise queue before them); the fragments are built after the copies
   QueryLoads<2 * kRoles> qload;
-  q4_query_load<2 * kRoles>(a, b, kvh, warp, lane, qload);
-  if (scorer) {
-    poisoned = q4r::q4_issue_own<false, false, 2>(a, b, kvh, k0, k1, 0, rw, lane, tile_row, nullptr, &a.tm_k, c.k, c.k_scale,
-                                                  sm.kc[0][rw], sm.ks[0][rw], &sm.kbar[0][rw]);
-    if (nrounds > 1)
-      poisoned |= q4r::q4_issue_own<false, false, 2>(a, b, kvh, k0, k1, 1, rw, lane, tile_row, nullptr, &a.tm_k, c.k,
-                                                     c.k_scale, sm.kc[1][rw], sm.ks[1][rw], &sm.kbar[1][rw]);
+  if (a.new_k != nullptr && p == (T - 1) / a.part) {
+    // This CTA stores the new token first.  Rounds 0 and 1 do not hold it when
+    // it lies at entry 256 or later of the partition: their K copies then go
+    // out before the store (later rounds' copies are issued after it).
+    const bool k01_first = T - 1 - k0 >= 2 * kQ4RoundTiles * 16;
+    if (k01_first) issue_k01();
+    q4s_store_new_token(a, b, kvh, T - 1, warp, lane);
+    q4_query_load<2 * kRoles>(a, b, kvh, warp, lane, qload);
+    if (!k01_first) issue_k01();
+  } else {
+    q4_query_load<2 * kRoles>(a, b, kvh, warp, lane, qload);
+    issue_k01();
   }
   // V of rounds 0 and 1, after the query fragments: K(0), which the first
   // round waits for, goes out alone first
