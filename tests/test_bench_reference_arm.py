@@ -43,3 +43,34 @@ def test_traffic_is_reported_only_for_the_captured_sources(monkeypatch):
 def test_rows_summary_keeps_the_floats():
     rows = {"store": {"workload": "text", "us": 12.345678, "rows_per_s": 2.5e9, "cache_bytes": 123}}
     assert bench.rows_summary(rows) == {"store": {"us": 12.35, "rows_per_s": 2.5e9}}
+
+
+class _Props:
+    multi_processor_count = 152
+
+
+class _Cuda:
+    @staticmethod
+    def get_device_properties(_):
+        return _Props()
+
+
+class _Torch:
+    cuda = _Cuda()
+
+
+def test_step_form_follows_the_decode_grid():
+    """--step auto takes the single decode-step launch while the decode grid
+    (512-key partitions x 4 KV heads) fits one wave of two CTAs per SM, as the
+    library's choice of the warp-specialised kernel does, and the three
+    launches beyond; the explicit forms are kept as given."""
+    t = _Torch()
+    assert bench.resolve_step(t, "auto", 32769) == "fused"  # 65 x 4 = 260 CTAs <= 304
+    assert bench.resolve_step(t, "auto", 262145) == "separate"  # 513 x 4 = 2052
+    assert bench.resolve_step(t, "auto", 76 * 512) == "fused"  # 304: one wave
+    assert bench.resolve_step(t, "auto", 76 * 512 + 1) == "separate"
+    assert bench.resolve_step(t, "separate", 32769) == "separate"
+    assert bench.resolve_step(t, "fused", 262145) == "fused"
+    assert bench.KERNELS_PER_LAYER == {"fused": 2, "separate": 3}
+    assert "kvq_decode_step" in bench.workload_config(32768, 1, "fused")["step"]
+    assert "kvq_store_rotate" in bench.workload_config(32768, 1, "separate")["step"]
