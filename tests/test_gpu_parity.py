@@ -636,6 +636,32 @@ def test_decode_gather(K):
             assert_close(out[b], ref[b], what=f"gather n_sel={n_sel} seq {b}")
 
 
+def test_decode_gather_bad_index_and_bad_page(K):
+    """A selected position outside its sequence (past its length, or negative)
+    and a selected row on a page outside the pool: each is flagged, the
+    sequence's outputs are NaN, and the other sequence matches the oracle.  The
+    bad entries sit mid-partition (entry 700 of 1300: partition 1, tile 11),
+    so the CTA's other rows are resolved and copied as usual."""
+    lens = [3000, 1800]
+    g, o, bt, q, ml = decode_case(K, lens, seed=22)
+    n_sel = 1300
+    sel = np.stack([synth.distinct_sorted(n_sel, L, 22, b).numpy() for b, L in enumerate(lens)]).astype(np.int32)
+    ref = O.decode(o, to_np_in(q), lens, bt, 1 / 16, sel=sel)
+    for bad_pos, flag in ((lens[0] + 7, K.DEV_BAD_INDEX), (-3, K.DEV_BAD_INDEX)):
+        s1 = sel.copy()
+        s1[0, 700] = bad_pos
+        out, ws = run_decode(K, g, bt, q, lens, ml, 1 / 16, sel=s1)
+        assert K.read_status(ws) & flag
+        assert np.isnan(out[0]).all()
+        assert_close(out[1], ref[1], what=f"healthy sequence next to a bad index {bad_pos}")
+    bt2 = bt.copy()
+    bt2[1, int(sel[1, 700]) // g.page_size] = g.num_pages + 3
+    out, ws = run_decode(K, g, bt2, q, lens, ml, 1 / 16, sel=sel)
+    assert K.read_status(ws) & K.DEV_BAD_PAGE
+    assert np.isnan(out[1]).all()
+    assert_close(out[0], ref[0], what="healthy sequence next to a bad page")
+
+
 def test_decode_gather_at_the_limit(K):
     """4096 selected rows, the largest list the ABI accepts: eight full 512-entry
     partitions; the second sequence selects every one of its 4096 rows."""
