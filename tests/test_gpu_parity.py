@@ -574,6 +574,36 @@ def test_decode_step_equals_store_rotate_decode(K, fmt, dtype, lens):
             assert_close(out[b].cpu().numpy(), ref[b], what=f"decode_step seq {b}")
 
 
+@pytest.mark.parametrize("Hk,Hq", [(2, 4), (3, 21), (8, 8), (1, 8)])
+@pytest.mark.parametrize("lens", [[1025, 9000, 700], [100001]])
+def test_decode_step_gqa_layouts(K, Hk, Hq, lens):
+    """kvq_decode_step for other GQA layouts (groups of 2, 7, 1 and 8 heads):
+    the cache planes and the partials bit-identical to kvq_store +
+    kvq_rotate_query + kvq_decode_attn.  The cases' grids fall on both sides of
+    one wave of two CTAs per SM (the warp-specialised kernel; or a rotation
+    launch, then the round kernel, which stores the new token)."""
+    g, o, bt, q, ml = decode_case(K, lens, Hk=Hk, Hq=Hq, seed=93 + Hq)
+    g2 = _clone_q4_cache(K, g)
+    B, D = len(lens), g.D
+    k_new = synth.heavy_tailed((B, Hk, D), "cpu", 93, "knew").to(DEV)
+    v_new = synth.heavy_tailed((B, Hk, D), "cpu", 93, "vnew").to(DEV)
+    qd = q.to(DEV)
+    seq = torch.tensor(lens, dtype=torch.int32, device=DEV)
+    btd = torch.from_numpy(bt).to(DEV)
+    ps = g.page_size
+    slots = torch.tensor([int(bt[b, (L - 1) // ps]) * ps + (L - 1) % ps for b, L in enumerate(lens)],
+                         dtype=torch.int32, device=DEV)
+    ws1 = K.alloc_workspace(g, B, Hq, ml, device=DEV)
+    ws2 = K.alloc_workspace(g, B, Hq, ml, device=DEV)
+    K.decode_step(g, k_new, v_new, qd, seq, btd, ml, 1 / 16, ws1)
+    K.store(g2, k_new, v_new, slots)
+    K.decode_attn(g2, K.rotate_query(qd), seq, btd, ml, 1 / 16, ws2)
+    torch.cuda.synchronize()
+    for name in ("k", "v", "k_scale", "v_scale"):
+        assert torch.equal(getattr(g, name).view(torch.uint8), getattr(g2, name).view(torch.uint8)), name
+    assert torch.equal(_partials(ws1, B, Hq, ml), _partials(ws2, B, Hq, ml))
+
+
 def test_decode_step_bad_page_flags_and_stores_nothing(K):
     """A new position mapped to a page outside the pool: nothing is written, the
     decode flags KVQ_DEV_BAD_PAGE and the sequence's outputs are NaN."""
