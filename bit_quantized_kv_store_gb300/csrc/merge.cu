@@ -8,8 +8,8 @@
 // One CTA of 256 threads per (32 output values, query head, sequence), one
 // pass over the partials.  Thread (row r = tid / 8, chunk c = tid % 8) takes
 // partitions r, r + 32, r + 64, ... in ascending order: it loads their m (and,
-// for c == 0, z) and the float4 chunk c of their acc, four partitions per
-// batch with every load of a batch issued before any use, and keeps a running
+// for c == 0, z) and the float4 chunk c of their acc, four (or eight)
+// partitions per batch with every load of a batch issued before any use, and keeps a running
 // (M_t, Z_t, acc_t) rescaled to its own maximum.  The 32 row-threads' partials
 // are then combined in a fixed tree, so the result does not depend on
 // scheduling (bit-reproducible), and the 32 values of the CTA -- exactly one
@@ -21,6 +21,10 @@
 
 namespace kvq {
 
+// kBatch: partitions a row-thread loads before using them (4, or 8 for a grid of
+// few CTAs over many partitions: fewer round trips, more registers); the
+// updates run in ascending partition order either way, so the bits are the same.
+template <int kBatch>
 __global__ void __launch_bounds__(256) merge_kernel(const MergeArgs a) {
   pdl_wait();
   pdl_trigger();
@@ -59,11 +63,11 @@ __global__ void __launch_bounds__(256) merge_kernel(const MergeArgs a) {
   float Mt = -INFINITY, Zt = 0.f;
   float4 At = make_float4(0.f, 0.f, 0.f, 0.f);
   int nan_seen = 0;
-  for (int i0 = row; i0 < np; i0 += 4 * 32) {
-    float mv[4], zv[4];
-    float4 av[4];
+  for (int i0 = row; i0 < np; i0 += kBatch * 32) {
+    float mv[kBatch], zv[kBatch];
+    float4 av[kBatch];
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {  // all loads of the batch first
+    for (int k = 0; k < kBatch; ++k) {  // all loads of the batch first
       const int i = i0 + 32 * k;
       mv[k] = -INFINITY;
       zv[k] = 0.f;
@@ -75,7 +79,7 @@ __global__ void __launch_bounds__(256) merge_kernel(const MergeArgs a) {
       }
     }
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
+    for (int k = 0; k < kBatch; ++k) {
       if (i0 + 32 * k >= np) break;
       nan_seen |= isnan(mv[k]);
       const float Mn = fmaxf(Mt, mv[k]);
@@ -141,7 +145,10 @@ cudaError_t launch_wait_timeout_probe(int32_t* status, cudaStream_t s) {
 cudaError_t launch_merge(const MergeArgs& a, int B, cudaStream_t s) {
   dim3 grid(a.Dv / 32, a.Hq, B);
   if (B == 0 || a.Hq == 0) return cudaSuccess;
-  cudaError_t e = launch_pdl(merge_kernel, grid, dim3(256), 0, s, a);
+  const int64_t ctas = (int64_t)grid.x * grid.y * grid.z;
+  const bool deep = a.P > 128 && ctas <= 2 * (int64_t)device_sm_count();
+  cudaError_t e = deep ? launch_pdl(merge_kernel<8>, grid, dim3(256), 0, s, a)
+                       : launch_pdl(merge_kernel<4>, grid, dim3(256), 0, s, a);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
