@@ -54,8 +54,8 @@ KERNELS_PER_LAYER = {"fused": 2, "separate": 3}
 # beside them: once those sources change, the bench reports no traffic until
 # the capture is taken again.
 TRAFFIC_SOURCES = ("bit_quantized_kv_store_gb300/csrc/decode_q4.cu", "bit_quantized_kv_store_gb300/csrc/common.cuh")
-TRAFFIC_CAPTURE = {"sources_sha16": "3e15c583f9e61c95",
-                   "bytes": {32768: 37857280 + 0, 262144: 302277120 + 10203136}}
+TRAFFIC_CAPTURE = {"sources_sha16": "b38fbd4817c6bd5b",
+                   "bytes": {32768: 37858048 + 0, 262144: 302270720 + 10423040}}
 BYTES_PER_POS_LAYER = HK * 2 * (D // 2 + 2 * (D // 32))   # 1152
 
 
@@ -1156,7 +1156,8 @@ def _row_window(K, synth, torch, dev, peak, seed):
     out["q4_gather_262k"] = {
         "workload": "2048 selected positions of a 262145-key sequence (4-bit rotated cache), 4 KV / 24 q heads, "
                     "decode + merge", "gather_2048_us": g_ms * 1e3, "decode_us": gd_ms * 1e3,
-        "kernel": "decode_q4_round_kernel, gather mode (rows resolved once per CTA, copied by cp.async)"}
+        "kernel": "decode_q4_spec_kernel in gather mode (rows resolved once per CTA, copied by cp.async; "
+                  "the round kernel for grids over one wave)"}
     del c, ws, wsg
     torch.cuda.empty_cache()
     return out

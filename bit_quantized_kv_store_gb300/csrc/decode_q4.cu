@@ -1430,9 +1430,11 @@ __device__ __forceinline__ void q4s_store_new_token(const DecodeArgs& a, int b, 
 }
 constexpr int kBarMax = 1, kBarFull = 2, kBarEmpty = 4, kBarPv = 6;
 
+template <bool GATHER>
 struct __align__(1024) SpecSmem {
-  uint8_t kc[2][kRoles][2][kQ4TileBytes];      // K ring: round mod 2, scoring warp, its 2 tiles
-  uint8_t vc[2][kQ4RoundTiles][kQ4TileBytes];  // V ring: round mod 2, tile
+  static constexpr int kTile = q4_tile_bytes<GATHER>();
+  uint8_t kc[2][kRoles][2][kTile];      // K ring: round mod 2, scoring warp, its 2 tiles
+  uint8_t vc[2][kQ4RoundTiles][kTile];  // V ring: round mod 2, tile
   uint16_t ks[2][kRoles][2][16 * 8];
   uint16_t vs[2][kQ4RoundTiles][16 * 8];
   uint4 qf[1][kQ4NG][2][32];
@@ -1444,6 +1446,7 @@ struct __align__(1024) SpecSmem {
   uint64_t kbar[2][kRoles];
   uint64_t vfull[2];
   int poison;
+  int32_t grow[GATHER ? kQ4GatherPart : 1];  // gather: the cache row of each of the partition's entries
 };
 
 __device__ __forceinline__ void nbar_sync(int id, int n) { asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory"); }
@@ -1451,18 +1454,24 @@ __device__ __forceinline__ void nbar_arrive(int id, int n) {
   asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(n) : "memory");
 }
 
+// GATHER: the gather of selected positions (512-entry partitions, the rows
+// resolved once per CTA into shared memory and copied by cp.async), otherwise
+// the dense decode.
+template <bool GATHER>
 __global__ void __launch_bounds__(2 * kRoles * 32, 2) decode_q4_spec_kernel(const __grid_constant__ DecodeArgs a) {
   extern __shared__ uint8_t smem_raw[];
-  SpecSmem& sm = *reinterpret_cast<SpecSmem*>(smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u));
+  SpecSmem<GATHER>& sm =
+      *reinterpret_cast<SpecSmem<GATHER>*>(smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u));
   const int p = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, t = lane & 3;
   const bool scorer = warp < kRoles;
   const int rw = warp & (kRoles - 1);  // the warp's index within its role
 
-  // metadata before the wait on the previous kernel (as in the round kernel)
-  const int32_t T = a.seq_lens[b];
-  const bool bad_len = T < 0 || T > a.max_seq_len || (int64_t)T > (int64_t)a.max_pages * a.c.page_size;
+  // metadata before the wait on the previous kernel (as in the round kernel);
+  // a gather's entries are checked against the sequence one by one instead
+  const int32_t T = GATHER ? a.n_sel : a.seq_lens[b];
+  const bool bad_len = !GATHER && (T < 0 || T > a.max_seq_len || (int64_t)T > (int64_t)a.max_pages * a.c.page_size);
   const int nparts = bad_len ? 0 : (T + a.part - 1) / a.part;
   const bool active = p < nparts;
   const int k0 = p * a.part;
@@ -1471,7 +1480,7 @@ __global__ void __launch_bounds__(2 * kRoles * 32, 2) decode_q4_spec_kernel(cons
   const int nrounds = (ntiles + kQ4RoundTiles - 1) / kQ4RoundTiles;
   int32_t tile_row = -1;
   bool bad_page = false;
-  if (lane < ntiles) {
+  if (!GATHER && lane < ntiles) {
     const int key0 = k0 + 16 * lane;
     const int32_t page = a.block_tables[(int64_t)b * a.bt_stride + key0 / a.c.page_size];
     if (page < 0 || page >= a.c.num_pages)
@@ -1495,22 +1504,46 @@ __global__ void __launch_bounds__(2 * kRoles * 32, 2) decode_q4_spec_kernel(cons
   if (!active) return;
   if (bad_page && warp == 0) set_status(a.status, KVQ_DEV_BAD_PAGE);
   __syncthreads();  // the mbarriers are initialised
+  const int32_t* grow = nullptr;
+  if constexpr (GATHER) {
+    // the partition's selected rows, resolved once and in parallel (as the
+    // round kernel's gather does)
+    const int32_t Tseq = a.seq_lens[b];
+    const int32_t* bt = a.block_tables + (int64_t)b * a.bt_stride;
+    const int64_t tmax = (int64_t)a.max_pages * a.c.page_size;
+    for (int i = threadIdx.x; i < k1 - k0; i += 2 * kRoles * 32) {
+      const int32_t pos = a.sel[(int64_t)b * a.n_sel + k0 + i];
+      int32_t row = -1;
+      if (pos < 0 || pos >= Tseq || pos >= tmax) {
+        set_status(a.status, KVQ_DEV_BAD_INDEX);
+      } else {
+        const int32_t pg = bt[pos / a.c.page_size];
+        if (pg < 0 || pg >= a.c.num_pages)
+          set_status(a.status, KVQ_DEV_BAD_PAGE);
+        else
+          row = static_cast<int32_t>(((int64_t)pg * a.c.num_kv_heads + kvh) * a.c.page_size + pos % a.c.page_size);
+      }
+      sm.grow[i] = row;
+    }
+    __syncthreads();
+    grow = sm.grow;
+  }
 
   const kvq_cache& c = a.c;
   bool poisoned = false;
   auto issue_k01 = [&]() {
     if (scorer) {
-      poisoned = q4r::q4_issue_own<false, false, 2>(a, b, kvh, k0, k1, 0, rw, lane, tile_row, nullptr, &a.tm_k, c.k,
+      poisoned = q4r::q4_issue_own<GATHER, false, 2>(a, b, kvh, k0, k1, 0, rw, lane, tile_row, grow, &a.tm_k, c.k,
                                                     c.k_scale, sm.kc[0][rw], sm.ks[0][rw], &sm.kbar[0][rw]);
       if (nrounds > 1)
-        poisoned |= q4r::q4_issue_own<false, false, 2>(a, b, kvh, k0, k1, 1, rw, lane, tile_row, nullptr, &a.tm_k, c.k,
+        poisoned |= q4r::q4_issue_own<GATHER, false, 2>(a, b, kvh, k0, k1, 1, rw, lane, tile_row, grow, &a.tm_k, c.k,
                                                        c.k_scale, sm.kc[1][rw], sm.ks[1][rw], &sm.kbar[1][rw]);
     }
   };
   // the query loads go out ahead of the first rounds' copies (which would
   // otherwise queue before them); the fragments are built after the copies
   QueryLoads<2 * kRoles> qload;
-  if (a.new_k != nullptr && p == (T - 1) / a.part) {
+  if (!GATHER && a.new_k != nullptr && p == (T - 1) / a.part) {
     // This CTA stores the new token first.  Rounds 0 and 1 do not hold it when
     // it lies at entry 256 or later of the partition: their K copies then go
     // out before the store (later rounds' copies are issued after it).
@@ -1526,10 +1559,10 @@ __global__ void __launch_bounds__(2 * kRoles * 32, 2) decode_q4_spec_kernel(cons
   // V of rounds 0 and 1, after the query fragments: K(0), which the first
   // round waits for, goes out alone first
   auto issue_v01 = [&]() {
-    poisoned = q4r::q4_issue_own<false, false, 2>(a, b, kvh, k0, k1, 0, rw, lane, tile_row, nullptr, &a.tm_v, c.v, c.v_scale,
+    poisoned = q4r::q4_issue_own<GATHER, false, 2>(a, b, kvh, k0, k1, 0, rw, lane, tile_row, grow, &a.tm_v, c.v, c.v_scale,
                                                   &sm.vc[0][2 * rw], &sm.vs[0][2 * rw], &sm.vfull[0]);
     if (nrounds > 1)
-      poisoned |= q4r::q4_issue_own<false, false, 2>(a, b, kvh, k0, k1, 1, rw, lane, tile_row, nullptr, &a.tm_v, c.v,
+      poisoned |= q4r::q4_issue_own<GATHER, false, 2>(a, b, kvh, k0, k1, 1, rw, lane, tile_row, grow, &a.tm_v, c.v,
                                                      c.v_scale, &sm.vc[1][2 * rw], &sm.vs[1][2 * rw], &sm.vfull[1]);
   };
   q4_query_build<2 * kRoles>(a, warp, lane, qload, sm.qf[0], sm.qb[0]);
@@ -1561,7 +1594,7 @@ __global__ void __launch_bounds__(2 * kRoles * 32, 2) decode_q4_spec_kernel(cons
         if (!timed_out && !__all_sync(0xffffffffu, mbar_wait_bounded(&sm.kbar[s][rw], (r >> 1) & 1))) timed_out = true;
 #pragma unroll
         for (int u = 0; u < 2; ++u) S[u][0][0] = S[u][0][1] = S[u][0][2] = S[u][0][3] = 0.f;
-        q4_score_tiles<false, 1, 2>(S, kc_base, ks_base, qf_addr, qb_addr, lrow, lhi, lane);
+        q4_score_tiles<GATHER, 1, 2>(S, kc_base, ks_base, qf_addr, qb_addr, lrow, lhi, lane);
 #pragma unroll
         for (int u = 0; u < 2; ++u) {
           const int nvalid = k1 - (k0 + 16 * (tile0 + u));
@@ -1572,7 +1605,7 @@ __global__ void __launch_bounds__(2 * kRoles * 32, 2) decode_q4_spec_kernel(cons
         }
         __syncwarp();  // the K tiles are consumed: refill the slot with round r + 2
         if (r + 2 < nrounds)
-          poisoned |= q4r::q4_issue_own<false, false, 2>(a, b, kvh, k0, k1, r + 2, rw, lane, tile_row, nullptr, &a.tm_k, c.k,
+          poisoned |= q4r::q4_issue_own<GATHER, false, 2>(a, b, kvh, k0, k1, r + 2, rw, lane, tile_row, grow, &a.tm_k, c.k,
                                                          c.k_scale, sm.kc[s][rw], sm.ks[s][rw], &sm.kbar[s][rw]);
       }
       // round maximum over the scoring warps
@@ -1618,7 +1651,7 @@ __global__ void __launch_bounds__(2 * kRoles * 32, 2) decode_q4_spec_kernel(cons
     }
   } else {
     // ---------------- P.V of value groups 2 rw, 2 rw + 1, one round behind the scores
-    const uint32_t off_vl = q4_chunk_off<false>(lrow, lhi, lane, 2 * rw);
+    const uint32_t off_vl = q4_chunk_off<GATHER>(lrow, lhi, lane, 2 * rw);
     for (int r = 0; r < nrounds; ++r) {
       const int s = r & 1;
       nbar_sync(kBarFull + s, 2 * kRoles * 32);
@@ -1640,13 +1673,13 @@ __global__ void __launch_bounds__(2 * kRoles * 32, 2) decode_q4_spec_kernel(cons
       const uint32_t vs_base = smem_u32(&sm.vs[s][0][0]) + 4 * rw;
       const uint32_t pb_addr = smem_u32(&sm.pb[s][0][0][lane]);
       if (k0 + kQ4RoundTiles * 16 * (r + 1) > k1)  // CTA-uniform: the tail round
-        q4_pv_tiles<true, false, 1>(acc, pb_addr, vc_base, vs_base, off_vl, k0 + kQ4RoundTiles * 16 * r, k1, lane);
+        q4_pv_tiles<true, GATHER, 1>(acc, pb_addr, vc_base, vs_base, off_vl, k0 + kQ4RoundTiles * 16 * r, k1, lane);
       else
-        q4_pv_tiles<false, false, 1>(acc, pb_addr, vc_base, vs_base, off_vl, k0 + kQ4RoundTiles * 16 * r, k1, lane);
+        q4_pv_tiles<false, GATHER, 1>(acc, pb_addr, vc_base, vs_base, off_vl, k0 + kQ4RoundTiles * 16 * r, k1, lane);
       if (r + 2 < nrounds) nbar_arrive(kBarEmpty + s, 2 * kRoles * 32);  // slot s may take round r + 2
       nbar_sync(kBarPv, kRoles * 32);  // every P.V warp is done with the round's V tiles
       if (r + 2 < nrounds)
-        poisoned |= q4r::q4_issue_own<false, false, 2>(a, b, kvh, k0, k1, r + 2, rw, lane, tile_row, nullptr, &a.tm_v, c.v,
+        poisoned |= q4r::q4_issue_own<GATHER, false, 2>(a, b, kvh, k0, k1, r + 2, rw, lane, tile_row, grow, &a.tm_v, c.v,
                                                        c.v_scale, &sm.vc[s][2 * rw], &sm.vs[s][2 * rw], &sm.vfull[s]);
     }
   }
@@ -1702,11 +1735,12 @@ __global__ void __launch_bounds__(2 * kRoles * 32, 2) decode_q4_spec_kernel(cons
   pdl_trigger();  // after this CTA's last write
 }
 
+template <bool GATHER>
 cudaError_t launch_spec(const DecodeArgs& a, dim3 grid, cudaStream_t s) {
-  const size_t smem = sizeof(SpecSmem) + 1024;  // + slack for the 1024-byte alignment
-  cudaError_t e = set_max_smem_once<decode_q4_spec_kernel>((int)smem);
+  const size_t smem = sizeof(SpecSmem<GATHER>) + 1024;  // + slack for the 1024-byte alignment
+  cudaError_t e = set_max_smem_once<decode_q4_spec_kernel<GATHER>>((int)smem);
   if (e != cudaSuccess) return e;
-  e = launch_pdl(decode_q4_spec_kernel, grid, dim3(2 * kRoles * 32), smem, s, a);
+  e = launch_pdl(decode_q4_spec_kernel<GATHER>, grid, dim3(2 * kRoles * 32), smem, s, a);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
@@ -1726,9 +1760,11 @@ cudaError_t launch_decode_q4(const DecodeArgs& a, int B, cudaStream_t s) {
       return a.sel ? cudaErrorInvalidValue
                    : small ? launch_round<false, 1, false, false, true, 2, 2>(a, grid, s)
                            : launch_round<false, 1, false, false, true>(a, grid, s);
-    if (a.sel)  // the resolved rows of a partition live in shared memory
-      return a.part == kQ4GatherPart ? launch_round<true, 1, false>(a, grid, s) : cudaErrorInvalidValue;
-    if (small) return q4s::launch_spec(a, grid, s);
+    if (a.sel) {  // the resolved rows of a partition live in shared memory
+      if (a.part != kQ4GatherPart) return cudaErrorInvalidValue;
+      return small ? q4s::launch_spec<true>(a, grid, s) : launch_round<true, 1, false>(a, grid, s);
+    }
+    if (small) return q4s::launch_spec<false>(a, grid, s);
     return launch_round<false, 1, false>(a, grid, s);
   }
   if (a.tq) return cudaErrorInvalidValue;

@@ -666,6 +666,22 @@ def test_decode_gather(K):
             assert_close(out[b], ref[b], what=f"gather n_sel={n_sel} seq {b}")
 
 
+def test_decode_gather_solo_equals_batched(K):
+    """A gather's partials do not depend on the kernel that runs it: one
+    sequence's selection (8 partitions x 4 KV heads, a grid of one wave: the
+    warp-specialised kernel) equals the same sequence's rows in a batch of ten
+    (320 CTAs: the round kernel), bit for bit, for a full and a ragged
+    selection."""
+    lens = [5000 + 37 * b for b in range(10)]
+    g, o, bt, q, ml = decode_case(K, lens, seed=24)
+    for n_sel in (4096, 1300):
+        sel = np.stack([synth.distinct_sorted(n_sel, L, 24, b).numpy() for b, L in enumerate(lens)]).astype(np.int32)
+        out, _ = run_decode(K, g, bt, q, lens, ml, 1 / 16, sel=sel)
+        for b in (0, 7):
+            solo, _ = run_decode(K, g, bt[b:b + 1], q[b:b + 1], [lens[b]], lens[b], 1 / 16, sel=sel[b:b + 1])
+            assert np.array_equal(solo[0], out[b]), (n_sel, b)
+
+
 def test_decode_gather_bad_index_and_bad_page(K):
     """A selected position outside its sequence (past its length, or negative)
     and a selected row on a page outside the pool: each is flagged, the
