@@ -604,6 +604,37 @@ def test_decode_step_gqa_layouts(K, Hk, Hq, lens):
     assert torch.equal(_partials(ws1, B, Hq, ml), _partials(ws2, B, Hq, ml))
 
 
+def test_decode_step_with_an_empty_sequence(K):
+    """A sequence of length 0 in a decode step stores nothing and its outputs
+    are zeros; the others' planes and partials equal kvq_store (slot -1 for the
+    empty one: skipped) + kvq_rotate_query + kvq_decode_attn."""
+    lens = [0, 700, 513]
+    g, o, bt, q, ml = decode_case(K, lens, seed=95)
+    g2 = _clone_q4_cache(K, g)
+    B, Hk, D, Hq = len(lens), g.Hk, g.D, q.shape[1]
+    k_new = synth.heavy_tailed((B, Hk, D), "cpu", 95, "knew").to(DEV)
+    v_new = synth.heavy_tailed((B, Hk, D), "cpu", 95, "vnew").to(DEV)
+    qd = q.to(DEV)
+    seq = torch.tensor(lens, dtype=torch.int32, device=DEV)
+    btd = torch.from_numpy(bt).to(DEV)
+    ps = g.page_size
+    slots = torch.tensor([int(bt[b, (L - 1) // ps]) * ps + (L - 1) % ps if L > 0 else -1 for b, L in enumerate(lens)],
+                         dtype=torch.int32, device=DEV)
+    ws1 = K.alloc_workspace(g, B, Hq, ml, device=DEV)
+    ws2 = K.alloc_workspace(g, B, Hq, ml, device=DEV)
+    K.decode_step(g, k_new, v_new, qd, seq, btd, ml, 1 / 16, ws1)
+    K.store(g2, k_new, v_new, slots)
+    K.decode_attn(g2, K.rotate_query(qd), seq, btd, ml, 1 / 16, ws2)
+    out = torch.empty((B, Hq, D), dtype=torch.float32, device=DEV)
+    K.merge(g, ws1, B, Hq, seq, ml, out)
+    torch.cuda.synchronize()
+    for name in ("k", "v", "k_scale", "v_scale"):
+        assert torch.equal(getattr(g, name).view(torch.uint8), getattr(g2, name).view(torch.uint8)), name
+    assert torch.equal(_partials(ws1, B, Hq, ml), _partials(ws2, B, Hq, ml))
+    assert K.read_status(ws1) == 0
+    assert torch.count_nonzero(out[0]) == 0 and torch.isfinite(out[1:]).all()
+
+
 def test_decode_step_bad_page_flags_and_stores_nothing(K):
     """A new position mapped to a page outside the pool: nothing is written, the
     decode flags KVQ_DEV_BAD_PAGE and the sequence's outputs are NaN."""
