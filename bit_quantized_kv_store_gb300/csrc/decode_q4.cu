@@ -552,93 +552,170 @@ __device__ __forceinline__ bool q4_issue_own(const DecodeArgs& a, int b, int kvh
 // the group's block folders folds the block partials into the outputs.  The
 // tree depends only on the partition indices, so the outputs do not depend on
 // the batch or on which CTA finishes last.
+constexpr int kQ4FoldCols = 4;  // 4-dim columns per thread in a fold: 8 heads x 64 / 128 threads
+
+// Loads entries i .. i + 3 of a fold thread's columns (column k at ap[k]).
+__device__ __forceinline__ void q4_fold_load(float4 (&v)[kQ4FoldCols][4], const float* const (&ap)[kQ4FoldCols],
+                                             int t, int ncol, int i) {
+#pragma unroll
+  for (int k = 0; k < kQ4FoldCols; ++k)
+    if (t + k * kQ4Warps * 32 < ncol)
+#pragma unroll
+      for (int u = 0; u < 4; ++u) v[k][u] = __ldcg(reinterpret_cast<const float4*>(ap[k] + (int64_t)(i + u) * kQ4D));
+}
+
 // Fold n entries (i ascending) of each of the group's heads: M = max m_i,
 // w_i = 2^(m_i - M), Z = sum z_i w_i, acc = sum acc_i w_i.  Entry i of head h
 // sits at m[h * hs + i], z[h * hs + i], acc[(h * hs + i) * 256 ..].  Warp w
-// computes the weights of heads 2w, 2w + 1 (lanes over i; Z by a fixed xor
-// tree), then thread t takes dims 2t, 2t + 1 of every head.  final = false:
-// (M, Z, acc) go to om, oz, oacc at [h * ohs] (M = NaN if some m_i is NaN);
-// final = true: out = acc / Z (0 for a group without keys, NaN for a NaN),
-// rotated back per 32-group when rotate_back, at out + h * 256.
+// computes the weights of heads 2w and 2w + 1 together (lanes over i; the m_i
+// stashed in wts by the first pass, the z_i read in the second; Z by a fixed
+// xor tree).  Then thread t takes the 4-dim columns t, t + 128, .. of the
+// group (column c: head c / 64, dims 4 (c % 64) ..) and loads four entries of
+// each of its columns at a time; every output is one fused multiply-add chain
+// over i ascending.  final = false: (M, Z, acc) go to om, oz, oacc at
+// [h * ohs] (M = NaN if some m_i is NaN); final = true: out = acc / Z (0 for a
+// group without keys, NaN for a NaN), rotated back per 32-group when
+// rotate_back, at out + h * 256.
 __device__ __forceinline__ void q4_fold(const float* m, const float* z, const float* acc, int64_t hs, int n,
                                         int group, float* wts, float* zsum, bool final, float* om, float* oz,
                                         float* oacc, int64_t ohs, float* out, bool rotate_back) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   float* mx = zsum + 8;  // [group]: the heads' maxima
-  for (int hh = 0; hh < 2; ++hh) {
-    const int h = 2 * warp + hh;
-    if (h >= group) break;
-    float M = -INFINITY;
-    bool nan_seen = false;
+  const int ncol = group * (kQ4D / 4);
+  const int t = threadIdx.x;
+  const float* ap[kQ4FoldCols];
+  int hc[kQ4FoldCols];
+  float4 o[kQ4FoldCols];
+#pragma unroll
+  for (int k = 0; k < kQ4FoldCols; ++k) {
+    const int c = t + k * kQ4Warps * 32;
+    hc[k] = c >> 6;
+    ap[k] = acc + hc[k] * hs * kQ4D + 4 * (c & 63);
+    o[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+  // the first four entries' loads overlap the weights
+  float4 v[kQ4FoldCols][4];
+  if (n >= 4) q4_fold_load(v, ap, t, ncol, 0);
+  const int ha = 2 * warp, hb = 2 * warp + 1;
+  if (ha < group) {
+    const bool two = hb < group;
+    float Ma = -INFINITY, Mb = -INFINITY;
+    bool nan_a = false, nan_b = false;
+#pragma unroll 4
     for (int i = lane; i < n; i += 32) {
-      const float v = __ldcg(m + h * hs + i);
-      nan_seen |= isnan(v);
-      M = fmaxf(M, v);
+      const float va = __ldcg(m + ha * hs + i);
+      const float vb = two ? __ldcg(m + hb * hs + i) : -INFINITY;
+      wts[ha * n + i] = va;
+      if (two) wts[hb * n + i] = vb;
+      nan_a |= isnan(va);
+      nan_b |= isnan(vb);
+      Ma = fmaxf(Ma, va);
+      Mb = fmaxf(Mb, vb);
     }
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-    nan_seen = __any_sync(0xffffffffu, nan_seen);
-    float Z = 0.f;
+    for (int o = 16; o > 0; o >>= 1) {
+      Ma = fmaxf(Ma, __shfl_xor_sync(0xffffffffu, Ma, o));
+      Mb = fmaxf(Mb, __shfl_xor_sync(0xffffffffu, Mb, o));
+    }
+    nan_a = __any_sync(0xffffffffu, nan_a);
+    nan_b = __any_sync(0xffffffffu, nan_b);
+    float Za = 0.f, Zb = 0.f;
+#pragma unroll 4
     for (int i = lane; i < n; i += 32) {
-      const float v = __ldcg(m + h * hs + i);
-      const float w = (M == -INFINITY) ? 0.f : exp2f(v - M);
-      wts[h * n + i] = w;
-      Z = fmaf(__ldcg(z + h * hs + i), w, Z);
+      const float za = __ldcg(z + ha * hs + i);
+      const float zb = two ? __ldcg(z + hb * hs + i) : 0.f;
+      const float wa = (Ma == -INFINITY) ? 0.f : exp2f(wts[ha * n + i] - Ma);
+      wts[ha * n + i] = wa;
+      Za = fmaf(za, wa, Za);
+      if (two) {
+        const float wb = (Mb == -INFINITY) ? 0.f : exp2f(wts[hb * n + i] - Mb);
+        wts[hb * n + i] = wb;
+        Zb = fmaf(zb, wb, Zb);
+      }
     }
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) Z += __shfl_xor_sync(0xffffffffu, Z, o);
+    for (int o = 16; o > 0; o >>= 1) {
+      Za += __shfl_xor_sync(0xffffffffu, Za, o);
+      Zb += __shfl_xor_sync(0xffffffffu, Zb, o);
+    }
     if (lane == 0) {
-      zsum[h] = nan_seen ? NAN : Z;
-      mx[h] = nan_seen ? NAN : M;
+      zsum[ha] = nan_a ? NAN : Za;
+      mx[ha] = nan_a ? NAN : Ma;
+      if (two) {
+        zsum[hb] = nan_b ? NAN : Zb;
+        mx[hb] = nan_b ? NAN : Mb;
+      }
     }
   }
   __syncthreads();
-  const int t = threadIdx.x;  // dims 2t, 2t + 1
-  for (int h = 0; h < group; ++h) {
-    const float* accp = acc + h * hs * kQ4D + 2 * t;
-    float2 o = make_float2(0.f, 0.f);
-    int i = 0;
-    for (; i + 8 <= n; i += 8) {  // eight loads in flight
-      float2 v[8];
+  int i = 0;
+  for (; i + 4 <= n; i += 4) {  // four entries of every column in flight
+    if (i > 0) q4_fold_load(v, ap, t, ncol, i);
 #pragma unroll
-      for (int k = 0; k < 8; ++k) v[k] = __ldcg(reinterpret_cast<const float2*>(accp + (int64_t)(i + k) * kQ4D));
+    for (int k = 0; k < kQ4FoldCols; ++k)
+      if (t + k * kQ4Warps * 32 < ncol)
 #pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        o.x = fmaf(v[k].x, wts[h * n + i + k], o.x);
-        o.y = fmaf(v[k].y, wts[h * n + i + k], o.y);
+        for (int u = 0; u < 4; ++u) {
+          const float w = wts[hc[k] * n + i + u];
+          o[k].x = fmaf(v[k][u].x, w, o[k].x);
+          o[k].y = fmaf(v[k][u].y, w, o[k].y);
+          o[k].z = fmaf(v[k][u].z, w, o[k].z);
+          o[k].w = fmaf(v[k][u].w, w, o[k].w);
+        }
+  }
+  for (; i < n; ++i) {
+#pragma unroll
+    for (int k = 0; k < kQ4FoldCols; ++k)
+      if (t + k * kQ4Warps * 32 < ncol) {
+        const float4 vi = __ldcg(reinterpret_cast<const float4*>(ap[k] + (int64_t)i * kQ4D));
+        const float w = wts[hc[k] * n + i];
+        o[k].x = fmaf(vi.x, w, o[k].x);
+        o[k].y = fmaf(vi.y, w, o[k].y);
+        o[k].z = fmaf(vi.z, w, o[k].z);
+        o[k].w = fmaf(vi.w, w, o[k].w);
       }
+  }
+  if (!final) {
+#pragma unroll
+    for (int k = 0; k < kQ4FoldCols; ++k) {
+      const int c = t + k * kQ4Warps * 32;
+      if (c < ncol) *reinterpret_cast<float4*>(oacc + hc[k] * ohs * kQ4D + 4 * (c & 63)) = o[k];
     }
-    for (; i < n; ++i) {
-      const float2 v = __ldcg(reinterpret_cast<const float2*>(accp + (int64_t)i * kQ4D));
-      o.x = fmaf(v.x, wts[h * n + i], o.x);
-      o.y = fmaf(v.y, wts[h * n + i], o.y);
+    if (t < group) {
+      om[t * ohs] = mx[t];
+      oz[t * ohs] = zsum[t];
     }
-    const float Z = zsum[h];
-    if (!final) {
-      *reinterpret_cast<float2*>(oacc + h * ohs * kQ4D + 2 * t) = o;
-      if (t == 0) {
-        om[h * ohs] = mx[h];
-        oz[h * ohs] = Z;
-      }
-      continue;
-    }
+    return;
+  }
+#pragma unroll
+  for (int k = 0; k < kQ4FoldCols; ++k) {
+    const int c = t + k * kQ4Warps * 32;
+    if (c >= ncol) continue;  // warp-uniform: ncol is a multiple of 64
+    const float Z = zsum[hc[k]];
     const bool empty = !(Z > 0.f) && !isnan(Z);
-    float x0 = empty ? 0.f : o.x / Z, x1 = empty ? 0.f : o.y / Z;
+    float x0 = empty ? 0.f : o[k].x / Z, x1 = empty ? 0.f : o[k].y / Z;
+    float x2 = empty ? 0.f : o[k].z / Z, x3 = empty ? 0.f : o[k].w / Z;
     if (rotate_back) {
-      // 32-point butterfly of the group: dims 2t, 2t + 1 here, the other 30 in
-      // the 15 neighbouring lanes (lane bits 0-3)
-      float a0 = x0 + x1, a1 = x0 - x1;
+      // 32-point butterfly of the group, stages by dim bit 0 .. 4: bits 0, 1
+      // within the thread's 4 dims, bits 2 .. 4 across lanes (lane bits 0 .. 2);
+      // the lower element takes lower + upper, the upper lower - upper
+      const float a0 = x0 + x1, a1 = x0 - x1, a2 = x2 + x3, a3 = x2 - x3;
+      float b[4] = {a0 + a2, a1 + a3, a0 - a2, a1 - a3};
 #pragma unroll
-      for (int o2 = 1; o2 < 16; o2 <<= 1) {
-        const float p0 = __shfl_xor_sync(0xffffffffu, a0, o2), p1 = __shfl_xor_sync(0xffffffffu, a1, o2);
+      for (int o2 = 1; o2 < 8; o2 <<= 1) {
         const bool upper = (lane & o2) != 0;
-        a0 = upper ? p0 - a0 : a0 + p0;
-        a1 = upper ? p1 - a1 : a1 + p1;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const float p = __shfl_xor_sync(0xffffffffu, b[j], o2);
+          b[j] = upper ? p - b[j] : b[j] + p;
+        }
       }
-      x0 = __fmul_rn(a0, kHadamardScale);
-      x1 = __fmul_rn(a1, kHadamardScale);
+      x0 = __fmul_rn(b[0], kHadamardScale);
+      x1 = __fmul_rn(b[1], kHadamardScale);
+      x2 = __fmul_rn(b[2], kHadamardScale);
+      x3 = __fmul_rn(b[3], kHadamardScale);
     }
-    *reinterpret_cast<float2*>(out + h * kQ4D + 2 * t) = make_float2(x0, x1);
+    *reinterpret_cast<float4*>(out + hc[k] * kQ4D + 4 * (c & 63)) = make_float4(x0, x1, x2, x3);
   }
 }
 
