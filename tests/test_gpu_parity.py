@@ -987,6 +987,28 @@ def test_decode_merged_equals_decode_then_merge(K, fmt):
     assert_close(out[0], ref[0], what="merged seq 0 next to an invalid one")
 
 
+@pytest.mark.parametrize("Hk,Hq,lens", [(4, 4, [4500, 700]), (2, 6, [9000, 33]), (1, 8, [8193, 1]),
+                                         (4, 32, [3000, 1200, 4097]), (8, 8, [40000, 2000]),
+                                         (4, 32, [40000, 2000])])
+def test_decode_merged_gqa_groups(K, Hk, Hq, lens):
+    """The fused merge for GQA groups 1, 3, 8 (the fold's columns: 64 per head,
+    up to four per thread) with lengths of one and several blocks of 8
+    partitions; the last two cases' grids are over one wave (the multi-wave
+    launch form).  Against the oracle and the two-launch path (to 1e-5)."""
+    g, o, bt, q, ml = decode_case(K, lens, Hk=Hk, Hq=Hq, seed=Hk * 100 + Hq + 7)
+    qr = K.rotate_query(q.to(DEV))
+    seq = torch.tensor(lens, dtype=torch.int32, device=DEV)
+    dbt = torch.from_numpy(bt).to(DEV)
+    ws = K.alloc_workspace(g, len(lens), Hq, ml, device=DEV)
+    out = K.decode_merged(g, qr, seq, dbt, ml, 0.07, ws).cpu().numpy()
+    assert K.read_status(ws) == 0
+    ref2, _ = run_decode(K, g, bt, q, lens, ml, 0.07)
+    ref = O.decode(o, to_np_in(q), lens, bt, 0.07)
+    for b in range(len(lens)):
+        assert_close(out[b], ref[b], what=f"merged Hk={Hk} Hq={Hq} seq {b}")
+        assert np.abs(out[b] - ref2[b]).max() <= 1e-5 * np.abs(ref2[b]).max()
+
+
 def test_decode_merged_blocks_batch_independent(K):
     """The fused merge's two levels (blocks of 8 partitions): lengths of 2 and 3
     blocks and one whose last block holds a single partition; each sequence's
