@@ -54,8 +54,8 @@ KERNELS_PER_LAYER = {"fused": 2, "separate": 3}
 # beside them: once those sources change, the bench reports no traffic until
 # the capture is taken again.
 TRAFFIC_SOURCES = ("bit_quantized_kv_store_gb300/csrc/decode_q4.cu", "bit_quantized_kv_store_gb300/csrc/common.cuh")
-TRAFFIC_CAPTURE = {"sources_sha16": "c09fb58100c783f3",
-                   "bytes": {32768: 37857280 + 0, 262144: 302260224 + 10204160}}
+TRAFFIC_CAPTURE = {"sources_sha16": "0bbdc4eda11d7094",
+                   "bytes": {32768: 37857024 + 0, 262144: 302254336 + 10246144}}
 BYTES_PER_POS_LAYER = HK * 2 * (D // 2 + 2 * (D // 32))   # 1152
 
 

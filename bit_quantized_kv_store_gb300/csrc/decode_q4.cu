@@ -360,23 +360,26 @@ __device__ __forceinline__ void q4_query_build(const DecodeArgs& a, int warp, in
 constexpr uint32_t kTqLo0 = 0x8a41351cu, kTqLo1 = 0x77237906u;  // low bytes of M_0..M_3, M_4..M_7
 constexpr uint32_t kTqHi0 = 0x3b393630u, kTqHi1 = 0x41403e3du;  // high bytes
 
-// The 8 codes of w (element 2b in the low nibble of byte b) -> 4 f16 pairs
-// (elements 0,1 | 2,3 | 4,5 | 6,7), exactly the codebook levels.
+// The 8 codes of w (element i in nibble i: element 2b in the low nibble of
+// byte b) -> 4 f16 pairs (elements 0,1 | 2,3 | 4,5 | 6,7), exactly the codebook
+// levels.  The magnitudes select the levels' low and high bytes (prmt reads the
+// low 16 bits of its selector: four 3-bit indices once the signs are masked);
+// the signs are spread from bit 3 of each nibble to bit 7 of each high byte
+// before the bytes are interleaved into pairs.
 __device__ __forceinline__ uint4 tq4_levels8(uint32_t w) {
-  const uint32_t m0 = w & 0x7777u, m1 = (w >> 16) & 0x7777u;  // magnitudes of codes 0-3, 4-7 as selectors
-  const uint32_t lo0 = prmt(kTqLo0, kTqLo1, m0), hi0 = prmt(kTqHi0, kTqHi1, m0);
-  const uint32_t lo1 = prmt(kTqLo0, kTqLo1, m1), hi1 = prmt(kTqHi0, kTqHi1, m1);
+  const uint32_t mm = w & 0x77777777u;  // magnitudes of codes 0-3 (low half), 4-7 (high half)
+  const uint32_t lo0 = prmt(kTqLo0, kTqLo1, mm), hi0s = prmt(kTqHi0, kTqHi1, mm);
+  const uint32_t lo1 = prmt(kTqLo0, kTqLo1, mm >> 16), hi1s = prmt(kTqHi0, kTqHi1, mm >> 16);
+  // x = w << 4 holds the signs of codes 0, 2, 4, 6 at bit 7 of its bytes 0-3;
+  // w itself those of codes 1, 3, 5, 7
+  const uint32_t x = w << 4;
+  const uint32_t hi0 = hi0s ^ (prmt(x, w, 0x5140u) & 0x80808080u);  // codes 0, 1, 2, 3
+  const uint32_t hi1 = hi1s ^ (prmt(x, w, 0x7362u) & 0x80808080u);  // codes 4, 5, 6, 7
   uint4 r;
   r.x = prmt(lo0, hi0, 0x5140u);  // (low, high) bytes of codes 0, 1
   r.y = prmt(lo0, hi0, 0x7362u);
   r.z = prmt(lo1, hi1, 0x5140u);
   r.w = prmt(lo1, hi1, 0x7362u);
-  // sign bits: code i's bit 3 -> bit 15 (even i) or bit 31 (odd i) of its pair
-  const uint32_t sg = w & 0x88888888u, sg4 = sg << 4;
-  r.x ^= prmt(sg, sg4, 0x0040u) & 0x80008000u;
-  r.y ^= prmt(sg, sg4, 0x1050u) & 0x80008000u;
-  r.z ^= prmt(sg, sg4, 0x2060u) & 0x80008000u;
-  r.w ^= prmt(sg, sg4, 0x3070u) & 0x80008000u;
   return r;
 }
 
