@@ -249,26 +249,37 @@ __global__ void __launch_bounds__((kF8Warps + 1) * 32, 1) decode_fp8_kernel(cons
           bulk_g2s(st.rsc + r, static_cast<const float*>(c.v_scale) + row0, 64, &sm.full);
         }
       } else {
-        // each lane: tokens lane and lane + 32 of the tile
+        // each lane: tokens lane and lane + 32 of the tile, resolved together
+        // (both selected positions loaded, then both pages: two dependent
+        // loads in all, not two per token)
         uint32_t bytes = 0;
         int64_t rows[2] = {-1, -1};
+        int32_t pos[2], page[2];
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          const int r = lane + 32 * u;
+          pos[u] = r < nvalid ? a.sel[(int64_t)b * a.n_sel + key0 + r] : -1;
+        }
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          const bool in = lane + 32 * u < nvalid && pos[u] >= 0 && pos[u] < Tseq;
+          page[u] = in ? bt[pos[u] / c.page_size] : -1;
+        }
 #pragma unroll
         for (int u = 0; u < 2; ++u) {
           const int r = lane + 32 * u;
           if (r >= nvalid) continue;
-          const int32_t pos = a.sel[(int64_t)b * a.n_sel + key0 + r];
-          if (pos < 0 || pos >= Tseq) {
+          if (pos[u] < 0 || pos[u] >= Tseq) {
             set_status(a.status, KVQ_DEV_BAD_INDEX);
             bad = true;
             continue;
           }
-          const int32_t page = bt[pos / c.page_size];
-          if (page < 0 || page >= c.num_pages) {
+          if (page[u] < 0 || page[u] >= c.num_pages) {
             set_status(a.status, KVQ_DEV_BAD_PAGE);
             bad = true;
             continue;
           }
-          rows[u] = (int64_t)page * c.page_size + pos % c.page_size;
+          rows[u] = (int64_t)page[u] * c.page_size + pos[u] % c.page_size;
           bytes += kF8L;
         }
         // The latent rows by bulk copies (their bytes expected before they are
