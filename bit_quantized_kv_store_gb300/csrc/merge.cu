@@ -24,10 +24,11 @@ namespace kvq {
 // kBatch: partitions a row-thread loads before using them (4; for a grid of few
 // CTAs over many partitions 8, or 17 past 256 partitions, so that a 262K-key
 // sequence's 513 take one round trip, still at two CTAs per SM: fewer round
-// trips, more registers); the updates run in ascending partition order either
-// way, so the bits are the same.
+// trips, more registers; for a grid of many waves 2, at six CTAs per SM: more
+// CTAs resident, more round trips); the updates run in ascending partition
+// order either way, so the bits are the same.
 template <int kBatch>
-__global__ void __launch_bounds__(256, kBatch > 8 ? 2 : 1) merge_kernel(const MergeArgs a) {
+__global__ void __launch_bounds__(256, kBatch > 8 ? 2 : kBatch == 2 ? 6 : 1) merge_kernel(const MergeArgs a) {
   pdl_wait();
   pdl_trigger();
   const int grp = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
@@ -148,10 +149,13 @@ cudaError_t launch_merge(const MergeArgs& a, int B, cudaStream_t s) {
   dim3 grid(a.Dv / 32, a.Hq, B);
   if (B == 0 || a.Hq == 0) return cudaSuccess;
   const int64_t ctas = (int64_t)grid.x * grid.y * grid.z;
-  const bool deep = a.P > 128 && ctas <= 2 * (int64_t)device_sm_count();
-  cudaError_t e = !deep        ? launch_pdl(merge_kernel<4>, grid, dim3(256), 0, s, a)
-                  : a.P > 256 ? launch_pdl(merge_kernel<17>, grid, dim3(256), 0, s, a)
-                              : launch_pdl(merge_kernel<8>, grid, dim3(256), 0, s, a);
+  const int64_t n_sm = device_sm_count();
+  const bool deep = a.P > 128 && ctas <= 2 * n_sm;
+  const bool wide = ctas > 8 * n_sm;  // many waves: more CTAs resident per SM
+  cudaError_t e = deep ? (a.P > 256 ? launch_pdl(merge_kernel<17>, grid, dim3(256), 0, s, a)
+                                    : launch_pdl(merge_kernel<8>, grid, dim3(256), 0, s, a))
+                       : wide ? launch_pdl(merge_kernel<2>, grid, dim3(256), 0, s, a)
+                              : launch_pdl(merge_kernel<4>, grid, dim3(256), 0, s, a);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
